@@ -1,0 +1,279 @@
+/*
+ * dl.h - C ABI of the GB300 decode-step library (libdl_gb300.so).
+ *
+ * The library runs the data-parallel hot path of a one-row / N-row transformer
+ * decode step over a resident f16 KV cache, one hand-written sm_103a CUDA kernel
+ * per call:
+ *
+ *   dl_gemv_q8        block-quantised (Q8_0) projection GEMV over 1..8 rows per
+ *                     command, longer launches tiled by eight rows
+ *   dl_rope_kv_store  fused RoPE of q (in place) and k, with the K/V store into
+ *                     the f16 mirror
+ *   dl_decode_attn    split-KV decode attention with GQA, the split sized by the
+ *                     command's rows
+ *   dl_attn_merge     log-sum-exp merge of the split pieces
+ *
+ * plus host-side helpers (weight packing, RoPE tables, the row-grouping and
+ * split planner, status words).
+ *
+ * Conventions shared by every call:
+ *  - Every pointer argument documented as "device" is caller-owned device
+ *    memory; the library allocates nothing and keeps no global mutable state.
+ *  - Every GPU call is asynchronous on the caller's stream (`stream` is a
+ *    cudaStream_t; NULL means the legacy default stream) and never synchronises.
+ *  - Every call returns an int status: DL_OK or a negative DL_E_* code.  On a
+ *    non-OK return nothing was launched and no memory was touched.  The text of
+ *    the last failure on the calling thread is available from dl_last_error().
+ *  - Conditions only the GPU can see (a position outside the cache, a key
+ *    count past what the plan covers) are never trapped: the kernel skips the
+ *    offending write and ORs a DL_STATUS_* bit into a caller-provided device
+ *    status word, which dl_status_read() (or any device-to-host copy) reports.
+ *  - f16 values travel as uint16_t bit patterns (IEEE 754 binary16).
+ *
+ * Sources (pull-request texts; no formulas are printed there):
+ *  [ENC]  daScript PR #4473 "dasLLAMA: the audio towers on the CUDA home, q8 + f16
+ *         on every GPU home", commit "cud_router_enc_cols tiles every router
+ *         launch": a projection launch holds eight activation columns, longer
+ *         launches are tiled, every row equal to the row stepped alone.
+ *  [ROPE] daScript PR #4293 "dasLLAMA llama leg ...", commit "The decode
+ *         rope-and-store rides one template on both homes" (GkRopeKvStore).
+ *  [GRP]  the same PR, commit "The Vulkan batched step past eight rows runs in
+ *         groups, never a row at a time", and the PR body's twelve-stream line.
+ *  [SPL]  the same PR, commit "The decode attention's split follows the
+ *         command's rows, not the planes' height", and the "Not done" note on
+ *         one-row and N-row commands summing keys alike.
+ *  [Q8]   the same pages' "q8" lane: Q8_0 blocks of 32 int8 values and one f16
+ *         scale.
+ */
+#ifndef DL_GB300_H
+#define DL_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define DL_OK            0
+#define DL_E_ARG        (-1)  /* null pointer, bad stride, bad count */
+#define DL_E_SHAPE      (-2)  /* unsupported head_dim / group / row count / width */
+#define DL_E_ALIGN      (-3)  /* a pointer or stride breaks the 16-byte rule */
+#define DL_E_WORKSPACE  (-4)  /* caller's workspace smaller than required */
+#define DL_E_CUDA       (-5)  /* a CUDA runtime call failed (see dl_last_error) */
+#define DL_E_RANGE      (-6)  /* a device status word reports an out-of-range value */
+
+/* bits a kernel ORs into a device status word */
+#define DL_STATUS_POS_RANGE     0x1  /* rope/store: pos < 0 or pos >= capacity (row skipped) */
+#define DL_STATUS_REGION_RANGE  0x2  /* rope/store: region outside the cache (row skipped) */
+#define DL_STATUS_SEQLEN_RANGE  0x4  /* attention: seqlen < 1 or past the plan (keys clipped) */
+
+#define DL_MAX_ROWS 8          /* rows one command steps at once */
+
+typedef void *dl_stream_t;     /* a cudaStream_t */
+
+/* Text of the calling thread's last failure ("" if none).  Host only. */
+const char *dl_last_error(void);
+
+/* Library version as an integer MMmmpp. */
+int dl_version(void);
+
+/*
+ * Copy a device status word to the host.  Synchronises the device (test and
+ * debug use).  Returns DL_OK and stores the word, or DL_E_CUDA.
+ */
+int dl_status_read(const int32_t *status_dev, int32_t *host_out);
+
+/* ------------------------------------------------------------ Q8_0 weights
+ *
+ * Interchange form [Q8]: a row-major [n_out][n_in/32] array of 34-byte blocks,
+ * each an f16 scale d (little-endian) followed by 32 int8 values q; weight
+ * (o, 32b+i) is d[o][b] * q[o][b][i].
+ *
+ * Device form (written by dl_q8_pack, read by dl_gemv_q8): two planes.
+ *  qs: tiles of 16 output rows x 32 inputs (512 bytes), tile (rt, kt) at byte
+ *      ((rt * KT) + kt) * 512 with KT = 4 * ceil(n_in / 128); inside a tile the
+ *      16 bytes of lane t = 4g + c hold, in order, the values of rows g, g+8 at
+ *      inputs {2c, 2c+1}, then {2c+8, 2c+9}, for the tile's first 16 inputs and
+ *      then its second 16 (the operand order of a 16x8x16 tensor-core product).
+ *  d:  per 16 rows and 4 consecutive tiles, 128 bytes: lane group g's 16 bytes
+ *      hold (d[g], d[g+8]) for those 4 tiles.
+ * Rows past n_out and inputs past n_in are zero-filled.  Both planes must be
+ * 16-byte aligned.
+ */
+typedef struct dl_q8_weight {
+    const void *qs;     /* device, packed int8 tiles */
+    const void *d;      /* device, packed f16 scales */
+    int64_t n_out;      /* output features */
+    int64_t n_in;       /* input features, a multiple of 32 */
+} dl_q8_weight;
+
+/* Sizes in bytes of the two device planes for an [n_out][n_in] weight.  Host only. */
+int dl_q8_packed_size(int64_t n_out, int64_t n_in, size_t *qs_bytes, size_t *d_bytes);
+
+/*
+ * Convert interchange blocks (device, n_out * n_in/32 * 34 bytes, any alignment)
+ * into the device form (qs, d: device, sizes from dl_q8_packed_size, 16-byte
+ * aligned).  One-time preparation, not part of a decode step.
+ */
+int dl_q8_pack(const uint8_t *blocks, int64_t n_out, int64_t n_in,
+               void *qs, void *d, dl_stream_t stream);
+
+/*
+ * Q8_0 GEMV [ENC][Q8]:  y[r][o] = sum_b d[o][b] * sum_{i<32} q[o][b][i] * x[r][32b+i]
+ * for r < rows, o < n_out.
+ *   W        host struct describing the device planes
+ *   x        device f32, row r at x + r*x_stride (x_stride >= n_in, in elements)
+ *   y        device f32, row r at y + r*y_stride (y_stride >= n_out); must not alias x
+ * Rows are stepped eight at a time: the weights are read once per group of up
+ * to eight rows, and a row's result does not depend on the rows stepped with it.
+ * x and the planes must be 16-byte aligned and x_stride a multiple of 4.
+ * Arithmetic: int8 and f16 scales exact; products and sums in f32.
+ */
+int dl_gemv_q8(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
+               float *y, int64_t y_stride, dl_stream_t stream);
+
+/* ---------------------------------------------------------------- KV cache */
+
+/*
+ * The f16 KV mirror: K and V planes laid out [region][kv_head][slot][head_dim];
+ * element (reg, h, slot, d) of a plane P sits at P[reg*region_stride +
+ * (h*capacity + slot)*head_dim + d].  A token at position p lives in slot p.
+ * Each session (stream) owns one region.
+ */
+typedef struct dl_kv_cache {
+    uint16_t *k;              /* device f16 K plane */
+    uint16_t *v;              /* device f16 V plane */
+    int64_t region_stride;    /* elements between regions, >= n_kv*capacity*head_dim */
+    int n_regions;
+    int n_kv;                 /* KV heads */
+    int head_dim;             /* 64 or 128 */
+    int capacity;             /* slots per head and region */
+} dl_kv_cache;
+
+/* ------------------------------------------------------------------- RoPE */
+
+/*
+ * Rotary embedding table: f32 [max_pos][rot_dim/2][2] holding (cos a, sin a),
+ * a = p * theta^(-2j/rot_dim), evaluated in double precision on the host and
+ * rounded to f32.  The caller copies it to the device.
+ */
+typedef struct dl_rope {
+    const float *cos_sin;     /* device table from dl_rope_table_build */
+    int max_pos;              /* table rows */
+    int rot_dim;              /* rotated channels: even, <= head_dim */
+    int neox;                 /* 1: pairs (j, j + rot_dim/2); 0: pairs (2j, 2j+1) */
+} dl_rope;
+
+/* Bytes of a table (host only). */
+int dl_rope_table_bytes(int rot_dim, int max_pos, size_t *bytes);
+/* Fill host_out (rot_dim/2 * 2 * max_pos floats) (host only). */
+int dl_rope_table_build(double theta, int rot_dim, int max_pos, float *host_out);
+
+/*
+ * Fused RoPE and KV store [ROPE], one launch for `rows` token rows:
+ *  - the bias rows (optional) are added first: bias = [q bias (n_q*D) | k bias
+ *    (n_kv*D) | v bias (n_kv*D)];
+ *  - every q head is rotated in place (f32);
+ *  - every k head is rotated, clamped into +-65504 and stored as f16 (round to
+ *    nearest even) in slot pos[r] of its KV head in region row_region[r];
+ *  - every v head is clamped and stored as f16 the same way;
+ *  - channels >= rot_dim pass through unrotated.
+ *   q        device f32, row r at q + r*q_stride, n_q heads of head_dim
+ *   k, v     device f32, rows at k + r*k_stride / v + r*v_stride, n_kv heads
+ *   bias     device f32 or NULL
+ *   pos      device int32 [rows]
+ *   row_region device int32 [rows] or NULL (all rows in region 0)
+ *   status   device int32 status word or NULL; a row whose pos or region is out of
+ *            range is skipped and DL_STATUS_POS_RANGE / _REGION_RANGE is set
+ * pos must be < rope->max_pos.
+ */
+int dl_rope_kv_store(float *q, int64_t q_stride,
+                     const float *k, int64_t k_stride,
+                     const float *v, int64_t v_stride,
+                     const float *bias, const int32_t *pos, const int32_t *row_region,
+                     int rows, int n_q, const dl_rope *rope, const dl_kv_cache *kv,
+                     int32_t *status, dl_stream_t stream);
+
+/* --------------------------------------------------------------- planning */
+
+/*
+ * Row grouping [GRP]: n rows run as the fewest groups of at most `max_rows`
+ * rows whose sizes differ by at most one, larger groups first (12 -> 6+6,
+ * 9 -> 5+4).  Writes the sizes into sizes[] (capacity >= ceil(n/max_rows)) and
+ * returns the group count (>= 0) or DL_E_ARG.  Host only.
+ */
+int dl_plan_groups(int n, int max_rows, int *sizes);
+
+/*
+ * Split plan of one attention command (at most DL_MAX_ROWS rows) [SPL].
+ * Rows in the same region form a session: one work item serves all of a
+ * session's query heads that share a KV head, so each key is read once per
+ * session and step.  The keys are cut into pieces of `chunk` keys; the piece
+ * count is chosen from the command's own rows and the SM count so that the
+ * work items fill the GPU (not from the planes' height).
+ */
+typedef struct dl_attn_plan {
+    int rows;                      /* rows of the command, 1..8 */
+    int n_q, n_kv, head_dim;
+    int chunk;                     /* keys per piece (a multiple of 32) */
+    int max_splits;                /* pieces of the longest row; partial stride */
+    int n_sessions;
+    int n_work;                    /* work items (CTAs) of dl_decode_attn */
+    int sm_count;                  /* SMs the plan was sized for */
+    int row_region[DL_MAX_ROWS];   /* region of each row */
+    int row_keys_max[DL_MAX_ROWS]; /* planned key bound of each row (host seqlen) */
+    int sess_rows[DL_MAX_ROWS];    /* rows sorted by session */
+    int sess_begin[DL_MAX_ROWS + 1];  /* session s owns sess_rows[sess_begin[s] .. sess_begin[s+1]) */
+    int sess_splits[DL_MAX_ROWS];  /* pieces of session s */
+    int sess_item0[DL_MAX_ROWS + 1];  /* first work item of session s (items = n_kv * splits) */
+    size_t workspace_bytes;        /* bytes of the partials workspace */
+} dl_attn_plan;
+
+/*
+ * Build a plan.
+ *   seqlen_host   host int32 [rows]: keys each row attends (>= 1); the device
+ *                 seqlen passed later must not exceed these
+ *   region_host   host int32 [rows] or NULL (all rows region 0)
+ *   sm_count      SMs to fill; 0 = query the current device
+ *   force_chunk   0 = automatic; otherwise the piece length (rounded up to 32)
+ * Host only (plus one device attribute query when sm_count == 0).
+ */
+int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *region_host,
+                       int n_q, int n_kv, int head_dim, int sm_count, int force_chunk,
+                       dl_attn_plan *out);
+
+/*
+ * Split-KV decode attention [SPL].  For row r, query head h (KV head
+ * h / (n_q/n_kv)) and piece p covering keys [p*chunk, (p+1)*chunk) of
+ * [0, seqlen[r]) of region plan->row_region[r]: scores s_j = q.k_j / sqrt(D),
+ * m = max s_j, l = sum exp(s_j - m), o = sum exp(s_j - m) v_j / l, lse = m + ln l.
+ *   q          device f32, row r at q + r*q_stride (n_q heads of head_dim)
+ *   seqlen     device int32 [rows], 1 <= seqlen[r] <= plan->row_keys_max[r] and
+ *              <= kv->capacity; violations clip and set DL_STATUS_SEQLEN_RANGE
+ *   workspace  device, >= plan->workspace_bytes, 16-byte aligned: the pieces'
+ *              (o, lse), read by dl_attn_merge
+ * Pieces past a row's last key are neither computed nor written.
+ */
+int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv,
+                   const int32_t *seqlen, const dl_attn_plan *plan,
+                   void *workspace, size_t workspace_bytes,
+                   int32_t *status, dl_stream_t stream);
+
+/*
+ * Log-sum-exp merge of the pieces of every (row, head):
+ *   M = max_p lse_p, w_p = exp(lse_p - M), out = sum w_p o_p / sum w_p,
+ *   LSE = M + ln sum w_p  (natural log of the scaled scores' exp-sum).
+ * Reads only the pieces dl_decode_attn wrote for the same seqlen.
+ *   out   device f32, row r at out + r*out_stride, n_q*head_dim values
+ *   lse   device f32 [rows][n_q] or NULL
+ */
+int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t *seqlen,
+                  float *out, int64_t out_stride, float *lse, dl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DL_GB300_H */

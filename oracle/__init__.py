@@ -204,3 +204,28 @@ def plan_groups(n: int, max_rows: int = 8):
     if g < 0:
         raise ValueError("plan_groups rejected n=%d" % n)
     return [int(s) for s in sizes[:g]]
+
+
+def layer_step(blocks: dict, x, kcache, vcache, pos, *, n_q, n_kv, head_dim, theta, chunk, n_splits,
+               regions=None, x_ffn=None, h=None):
+    """One decode layer step in the oracle, the same sequence the library runs:
+    QKV GEMV -> rope + KV store -> split attention + merge -> O GEMV, and the
+    gate/up and down GEMVs on their own activation rows.  Caches are updated in
+    place (uint16 f16 planes).  Returns a dict of float64 results."""
+    D = head_dim
+    qkv = gemv_q8(blocks["wqkv"], x)
+    qd, kd = n_q * D, n_kv * D
+    q = qkv[:, :qd].astype(np.float32)
+    k = qkv[:, qd:qd + kd].astype(np.float32)
+    v = qkv[:, qd + kd:].astype(np.float32)
+    pos = np.asarray(pos, np.int32)
+    qr = rope_kv_store(q, k, v, pos, kcache, vcache, n_q=n_q, n_kv=n_kv, head_dim=D, rot_dim=D,
+                       theta=theta, row_region=None if regions is None else np.asarray(regions, np.int32))
+    out, lse = attention(qr, kcache, vcache, pos + 1, n_q=n_q, n_kv=n_kv, head_dim=D, chunk=chunk,
+                         n_splits=n_splits, row_region=None if regions is None else np.asarray(regions, np.int32))
+    res = {"qkv": qkv, "q": qr, "attn": out, "lse": lse,
+           "y_o": gemv_q8(blocks["wo"], out.astype(np.float32))}
+    if "wgu" in blocks and x_ffn is not None:
+        res["gu"] = gemv_q8(blocks["wgu"], x_ffn)
+        res["y_down"] = gemv_q8(blocks["wdown"], h)
+    return res

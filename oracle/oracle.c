@@ -94,6 +94,23 @@ uint16_t orc_double_to_half(double x)
     return (uint16_t)(sign | ((u + 15) << 10) | ((int)r - 1024));
 }
 
+/*
+ * Decoded value of every binary16 pattern, filled on first use from
+ * orc_half_to_double (a speed-up of the attention loops only; same values).
+ */
+static double orc_h2d_table[65536];
+static int orc_h2d_ready = 0;
+
+static double orc_h2d(uint16_t h)
+{
+    if (!orc_h2d_ready) {
+        for (int i = 0; i < 65536; ++i)
+            orc_h2d_table[i] = orc_half_to_double((uint16_t)i);
+        orc_h2d_ready = 1;
+    }
+    return orc_h2d_table[h];
+}
+
 /* ---------------------------------------------------------------- Q8_0 --- */
 
 static int orc_s8(uint8_t b)   /* two's complement byte -> int, without relying on char signedness */
@@ -257,7 +274,7 @@ static double orc_score(const double *q, const uint16_t *kc, int64_t kbase, int 
 {
     double s = 0.0;
     for (int d = 0; d < D; ++d)
-        s += q[d] * orc_half_to_double(kc[kbase + d]);
+        s += q[d] * orc_h2d(kc[kbase + d]);
     return s / sqrt((double)D);
 }
 
@@ -310,7 +327,7 @@ int orc_attn_split(const double *q, int64_t q_stride, int rows, int n_q, int n_k
                     double w = exp(orc_score(qv, kcache, hbase + (int64_t)j * D, D) - m);
                     l += w;
                     for (int d = 0; d < D; ++d)
-                        o[d] += w * orc_half_to_double(vcache[hbase + (int64_t)j * D + d]);
+                        o[d] += w * orc_h2d(vcache[hbase + (int64_t)j * D + d]);
                 }
                 for (int d = 0; d < D; ++d) o[d] /= l;
                 *lse = m + log(l);
@@ -387,13 +404,12 @@ int orc_attn_full(const double *q, int64_t q_stride, int rows, int n_q, int n_kv
             }
             double Z = 0.0;
             for (int j = 0; j < L; ++j) Z += exp(sc[j] - M);
+            for (int j = 0; j < L; ++j) sc[j] = exp(sc[j] - M) / Z;     /* softmax weights */
             double *ov = out + r * out_stride + (int64_t)h * D;
-            for (int d = 0; d < D; ++d) {
-                double acc = 0.0;
-                for (int j = 0; j < L; ++j)
-                    acc += exp(sc[j] - M) / Z * orc_half_to_double(vcache[hbase + (int64_t)j * D + d]);
-                ov[d] = acc;
-            }
+            for (int d = 0; d < D; ++d) ov[d] = 0.0;
+            for (int j = 0; j < L; ++j)
+                for (int d = 0; d < D; ++d)
+                    ov[d] += sc[j] * orc_h2d(vcache[hbase + (int64_t)j * D + d]);
             lse[(int64_t)r * n_q + h] = M + log(Z);
         }
         free(sc);

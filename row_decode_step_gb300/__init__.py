@@ -1,0 +1,292 @@
+"""GB300 decode-step library: Python binding of libdl_gb300.so.
+
+Argument marshalling only.  Every step of the decode path runs in the library's
+CUDA kernels; torch supplies device memory (tensors) and the current stream.
+There is no fallback: if the shared library is missing or a call fails, an
+exception is raised.
+
+The functions carry the C names of include/dl.h (dl_gemv_q8, dl_rope_kv_store,
+dl_decode_attn, dl_attn_merge, ...) and take torch tensors where the C call
+takes device pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdl_gb300.so")
+
+DL_OK = 0
+DL_E_ARG = -1
+DL_E_SHAPE = -2
+DL_E_ALIGN = -3
+DL_E_WORKSPACE = -4
+DL_E_CUDA = -5
+DL_E_RANGE = -6
+DL_STATUS_POS_RANGE = 0x1
+DL_STATUS_REGION_RANGE = 0x2
+DL_STATUS_SEQLEN_RANGE = 0x4
+DL_MAX_ROWS = 8
+
+_ERRNAMES = {DL_E_ARG: "DL_E_ARG", DL_E_SHAPE: "DL_E_SHAPE", DL_E_ALIGN: "DL_E_ALIGN",
+             DL_E_WORKSPACE: "DL_E_WORKSPACE", DL_E_CUDA: "DL_E_CUDA", DL_E_RANGE: "DL_E_RANGE"}
+
+
+class DLError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("%s (%d): %s" % (_ERRNAMES.get(code, "DL_E_?"), code, msg))
+        self.code = code
+
+
+class dl_q8_weight(ctypes.Structure):
+    _fields_ = [("qs", ctypes.c_void_p), ("d", ctypes.c_void_p),
+                ("n_out", ctypes.c_int64), ("n_in", ctypes.c_int64)]
+
+
+class dl_kv_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("region_stride", ctypes.c_int64),
+                ("n_regions", ctypes.c_int), ("n_kv", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("capacity", ctypes.c_int)]
+
+
+class dl_rope(ctypes.Structure):
+    _fields_ = [("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int), ("rot_dim", ctypes.c_int),
+                ("neox", ctypes.c_int)]
+
+
+_R = DL_MAX_ROWS
+
+
+class dl_attn_plan(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int), ("n_q", ctypes.c_int), ("n_kv", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("chunk", ctypes.c_int), ("max_splits", ctypes.c_int),
+                ("n_sessions", ctypes.c_int), ("n_work", ctypes.c_int), ("sm_count", ctypes.c_int),
+                ("row_region", ctypes.c_int * _R), ("row_keys_max", ctypes.c_int * _R),
+                ("sess_rows", ctypes.c_int * _R), ("sess_begin", ctypes.c_int * (_R + 1)),
+                ("sess_splits", ctypes.c_int * _R), ("sess_item0", ctypes.c_int * (_R + 1)),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libdl_gb300.so is not built (run __graft_entry__.build() or "
+                               "python row_decode_step_gb300/_build.py)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        sig = {
+            "dl_last_error": ([], ctypes.c_char_p),
+            "dl_version": ([], I),
+            "dl_status_read": ([P, P], I),
+            "dl_q8_packed_size": ([I64, I64, P, P], I),
+            "dl_q8_pack": ([P, I64, I64, P, P, P], I),
+            "dl_gemv_q8": ([P, P, I, I64, P, I64, P], I),
+            "dl_rope_table_bytes": ([I, I, P], I),
+            "dl_rope_table_build": ([ctypes.c_double, I, I, P], I),
+            "dl_rope_kv_store": ([P, I64, P, I64, P, I64, P, P, P, I, I, P, P, P, P], I),
+            "dl_plan_groups": ([I, I, P], I),
+            "dl_attn_plan_build": ([I, P, P, I, I, I, I, I, P], I),
+            "dl_decode_attn": ([P, I64, P, P, P, P, SZ, P, P], I),
+            "dl_attn_merge": ([P, P, P, P, I64, P, P], I),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != DL_OK:
+        raise DLError(rc, lib().dl_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+# ------------------------------------------------------------------ weights
+
+class PackedQ8:
+    """A Q8_0 weight in the library's device form (two planes kept alive here)."""
+
+    def __init__(self, qs: torch.Tensor, d: torch.Tensor, n_out: int, n_in: int):
+        self.qs, self.d, self.n_out, self.n_in = qs, d, int(n_out), int(n_in)
+        self.c = dl_q8_weight(qs.data_ptr(), d.data_ptr(), self.n_out, self.n_in)
+
+    @property
+    def nbytes_q8_0(self) -> int:
+        """Bytes of the same matrix in the 34-bytes-per-32 interchange form."""
+        return self.n_out * self.n_in // 32 * 34
+
+
+def dl_q8_packed_size(n_out: int, n_in: int):
+    qb, db = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().dl_q8_packed_size(n_out, n_in, ctypes.byref(qb), ctypes.byref(db)))
+    return qb.value, db.value
+
+
+def dl_q8_pack(blocks: torch.Tensor, n_out: int, n_in: int, stream=None) -> PackedQ8:
+    """Pack interchange Q8_0 blocks (uint8 CUDA tensor, n_out*n_in/32*34 bytes)."""
+    _dev(blocks, torch.uint8, "blocks")
+    if not blocks.is_contiguous() or blocks.numel() != n_out * (n_in // 32) * 34:
+        raise ValueError("blocks must be contiguous [n_out][n_in/32][34]")
+    qb, db = dl_q8_packed_size(n_out, n_in)
+    qs = torch.empty(qb, dtype=torch.uint8, device=blocks.device)
+    d = torch.empty(db, dtype=torch.uint8, device=blocks.device)
+    _check(lib().dl_q8_pack(_ptr(blocks), n_out, n_in, _ptr(qs), _ptr(d), _stream(stream)))
+    return PackedQ8(qs, d, n_out, n_in)
+
+
+def dl_gemv_q8(W: PackedQ8, x: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y[r] = W x[r] for every row of x (f32 [rows][>= n_in], rows may exceed eight)."""
+    _dev(x, torch.float32, "x")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit inner stride")
+    rows = x.shape[0]
+    if y is None:
+        y = torch.empty(rows, W.n_out, dtype=torch.float32, device=x.device)
+    _dev(y, torch.float32, "y")
+    _check(lib().dl_gemv_q8(ctypes.byref(W.c), _ptr(x), rows, x.stride(0), _ptr(y), y.stride(0),
+                            _stream(stream)))
+    return y
+
+
+# ------------------------------------------------------------------ KV cache
+
+class KVCache:
+    """An f16 mirror [n_regions][n_kv][capacity][head_dim] for K and V."""
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor):
+        assert k.shape == v.shape and k.dim() == 4
+        _dev(k, torch.float16, "k")
+        _dev(v, torch.float16, "v")
+        self.k, self.v = k, v
+        n_reg, n_kv, cap, D = k.shape
+        self.c = dl_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), n_reg, n_kv, D, cap)
+
+    @classmethod
+    def empty(cls, n_regions, n_kv, capacity, head_dim, device="cuda"):
+        shape = (n_regions, n_kv, capacity, head_dim)
+        return cls(torch.empty(shape, dtype=torch.float16, device=device),
+                   torch.empty(shape, dtype=torch.float16, device=device))
+
+
+class Rope:
+    def __init__(self, table: torch.Tensor, max_pos: int, rot_dim: int, neox: bool = True):
+        self.table = table
+        self.c = dl_rope(table.data_ptr(), max_pos, rot_dim, 1 if neox else 0)
+
+
+def dl_rope_table_build(theta: float, rot_dim: int, max_pos: int) -> torch.Tensor:
+    """Host f32 table [max_pos][rot_dim/2][2] of (cos, sin), built in double precision."""
+    t = torch.empty(max_pos, rot_dim // 2, 2, dtype=torch.float32)
+    _check(lib().dl_rope_table_build(float(theta), rot_dim, max_pos, _ptr(t)))
+    return t
+
+
+def make_rope(theta: float, rot_dim: int, max_pos: int, neox: bool = True, device="cuda") -> Rope:
+    return Rope(dl_rope_table_build(theta, rot_dim, max_pos).to(device), max_pos, rot_dim, neox)
+
+
+def dl_rope_kv_store(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos: torch.Tensor,
+                     rope: Rope, kv: KVCache, n_q: int, bias: Optional[torch.Tensor] = None,
+                     row_region: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev(t, torch.float32, n)
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("%s must be 2-D rows with unit inner stride" % n)
+    _dev(pos, torch.int32, "pos")
+    if bias is not None:
+        _dev(bias, torch.float32, "bias")
+    if row_region is not None:
+        _dev(row_region, torch.int32, "row_region")
+    if status is not None:
+        _dev(status, torch.int32, "status")
+    _check(lib().dl_rope_kv_store(_ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(v), v.stride(0),
+                                  _ptr(bias), _ptr(pos), _ptr(row_region), q.shape[0], n_q,
+                                  ctypes.byref(rope.c), ctypes.byref(kv.c), _ptr(status), _stream(stream)))
+
+
+# ------------------------------------------------------------------ planning and attention
+
+def dl_plan_groups(n: int, max_rows: int = DL_MAX_ROWS):
+    sizes = (ctypes.c_int * max(1, -(-n // max_rows)))()
+    g = lib().dl_plan_groups(n, max_rows, sizes)
+    if g < 0:
+        _check(g)
+    return [sizes[i] for i in range(g)]
+
+
+def dl_attn_plan_build(seqlen: Sequence[int], n_q: int, n_kv: int, head_dim: int,
+                       regions: Optional[Sequence[int]] = None, sm_count: int = 0,
+                       force_chunk: int = 0) -> dl_attn_plan:
+    rows = len(seqlen)
+    sl = (ctypes.c_int32 * rows)(*[int(s) for s in seqlen])
+    rg = None if regions is None else (ctypes.c_int32 * rows)(*[int(r) for r in regions])
+    plan = dl_attn_plan()
+    _check(lib().dl_attn_plan_build(rows, sl, rg, n_q, n_kv, head_dim, sm_count, force_chunk,
+                                    ctypes.byref(plan)))
+    return plan
+
+
+def workspace_for(plan: dl_attn_plan, device="cuda") -> torch.Tensor:
+    return torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=device)
+
+
+def dl_decode_attn(q: torch.Tensor, kv: KVCache, seqlen: torch.Tensor, plan: dl_attn_plan,
+                   workspace: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    _dev(q, torch.float32, "q")
+    _dev(seqlen, torch.int32, "seqlen")
+    _dev(workspace, torch.uint8, "workspace")
+    _check(lib().dl_decode_attn(_ptr(q), q.stride(0), ctypes.byref(kv.c), _ptr(seqlen), ctypes.byref(plan),
+                                _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+
+
+def dl_attn_merge(workspace: torch.Tensor, plan: dl_attn_plan, seqlen: torch.Tensor,
+                  out: torch.Tensor, lse: Optional[torch.Tensor] = None, stream=None) -> None:
+    _dev(out, torch.float32, "out")
+    _check(lib().dl_attn_merge(_ptr(workspace), ctypes.byref(plan), _ptr(seqlen), _ptr(out), out.stride(0),
+                               _ptr(lse), _stream(stream)))
+
+
+def dl_status_read(status: torch.Tensor) -> int:
+    v = ctypes.c_int32()
+    _check(lib().dl_status_read(_ptr(status), ctypes.byref(v)))
+    return v.value
+
+
+def decode_attention(q, kv, seqlen, plan, workspace, out=None, lse=None, status=None, stream=None):
+    """dl_decode_attn followed by dl_attn_merge; returns (out, lse)."""
+    rows = plan.rows
+    if out is None:
+        out = torch.empty(rows, plan.n_q * plan.head_dim, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(rows, plan.n_q, dtype=torch.float32, device=q.device)
+    dl_decode_attn(q, kv, seqlen, plan, workspace, status=status, stream=stream)
+    dl_attn_merge(workspace, plan, seqlen, out, lse, stream=stream)
+    return out, lse

@@ -1,0 +1,539 @@
+// Split-KV decode attention with GQA and its log-sum-exp merge, after daScript
+// PR #4293 ("The decode attention's split follows the command's rows, not the
+// planes' height"): a row's keys are cut into pieces sized so that the work
+// items of the command fill the GPU, each piece yields a softmax partial
+// (o, lse), and the partials are merged.
+//
+// Work item = (session, KV head, piece).  A session's rows share a region, so
+// one CTA scores every query head of every session row that reads the KV head:
+// each key is loaded from HBM once per session and step.  KV tiles of 32 keys
+// are staged in shared memory with cp.async (16-byte copies, double-buffered);
+// scores use one lane per key, the online softmax reduces over the warp with
+// shuffles, and P.V runs with lanes over head dimensions.
+#include <cuda_fp16.h>
+#include <cmath>
+#include <cstring>
+
+#include "dl_common.cuh"
+
+namespace {
+
+constexpr int kAttnThreads = 128;
+constexpr int kTile = 32;          // keys per tile
+constexpr int kMaxQ = 32;          // queries one work item serves (session rows x group)
+
+struct AttnArgs {
+    const float *q;
+    int64_t q_stride;
+    const uint16_t *kc, *vc;
+    int64_t region_stride;
+    int capacity;
+    const int32_t *seqlen;
+    float *part_o;       // [rows][n_q][max_splits][D]
+    float *part_lse;     // [rows][n_q][max_splits]
+    int32_t *status;
+    float qscale;        // log2(e) / sqrt(D)
+    dl_attn_plan plan;
+};
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Clip a row's device key count to what the plan and the cache cover.
+__device__ __forceinline__ int clip_len(int L, int planned, int capacity, int32_t *status, bool report)
+{
+    const int hi = min(planned, capacity);
+    if (L < 1 || L > hi) {
+        if (report) dl_status_or(status, DL_STATUS_SEQLEN_RANGE);
+        L = L < 1 ? 0 : hi;
+    }
+    return L;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads) decode_attn_cc_kernel(AttnArgs a)
+{
+    constexpr int PITCH = D + 8;                 // halves per staged row (16-byte pad: conflict-free)
+    constexpr int NQS = kAttnThreads / (D / 2);  // query slices of the P.V phase
+    constexpr int QPS = kMaxQ / NQS;             // queries per slice (upper bound)
+    const dl_attn_plan &P = a.plan;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint16_t *ks = reinterpret_cast<uint16_t *>(smem);            // [2][kTile][PITCH]
+    uint16_t *vs = ks + 2 * kTile * PITCH;                        // [2][kTile][PITCH]
+    float *qs = reinterpret_cast<float *>(vs + 2 * kTile * PITCH);  // [kMaxQ][D]
+    float *ps = qs + kMaxQ * D;                                   // [kMaxQ][kTile]
+    float *al = ps + kMaxQ * kTile;                               // [kMaxQ]
+    float *sm_m = al + kMaxQ;                                     // [kMaxQ]
+    float *sm_l = sm_m + kMaxQ;                                   // [kMaxQ]
+    __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS];
+
+    // ---- which (session, KV head, piece)
+    const int item = blockIdx.x;
+    int s = 0;
+    while (s + 1 < P.n_sessions && item >= P.sess_item0[s + 1]) ++s;
+    const int local = item - P.sess_item0[s];
+    const int splits = P.sess_splits[s];
+    const int h = local / splits, piece = local - h * splits;
+    const int rb = P.sess_begin[s], nrows = P.sess_begin[s + 1] - rb;
+    const int G = P.n_q / P.n_kv;
+    const int Q = nrows * G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid < nrows) {
+        const int r = P.sess_rows[rb + tid];
+        s_row[tid] = r;
+        s_len[tid] = clip_len(a.seqlen[r], P.row_keys_max[r], a.capacity, a.status, piece == 0 && h == 0);
+    }
+    __syncthreads();
+    int lmax = 0;
+    for (int i = 0; i < nrows; ++i) lmax = max(lmax, s_len[i]);
+    const int k0 = piece * P.chunk;
+    const int k1 = min(k0 + P.chunk, lmax);
+    if (k0 >= k1) return;                      // no row of the session reaches this piece
+
+    const int reg = P.row_region[s_row[0]];
+    const uint16_t *kbase = a.kc + (int64_t)reg * a.region_stride + (int64_t)h * a.capacity * D;
+    const uint16_t *vbase = a.vc + (int64_t)reg * a.region_stride + (int64_t)h * a.capacity * D;
+
+    // ---- stage the queries, pre-scaled into the log2 domain
+    for (int i = tid; i < Q * D; i += kAttnThreads) {
+        const int qi = i / D, d = i - qi * D;
+        const int rq = qi / G, gq = qi - rq * G;
+        qs[i] = a.q[s_row[rq] * a.q_stride + (h * G + gq) * D + d] * a.qscale;
+    }
+
+    auto load_tile = [&](int buf, int t0) {
+        constexpr int CH = D * 2 / 16;         // 16-byte chunks per key row
+        for (int i = tid; i < kTile * CH; i += kAttnThreads) {
+            const int t = i / CH, ch = i - t * CH;
+            uint16_t *dk = ks + (buf * kTile + t) * PITCH + ch * 8;
+            uint16_t *dv = vs + (buf * kTile + t) * PITCH + ch * 8;
+            const int key = t0 + t;
+            if (key < k1) {
+                cp_async16(dk, kbase + (int64_t)key * D + ch * 8);
+                cp_async16(dv, vbase + (int64_t)key * D + ch * 8);
+            } else {
+                *reinterpret_cast<uint4 *>(dk) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(dv) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        cp_async_commit();
+    };
+
+    // softmax state of this warp's queries (q = warp + 4*i), replicated over lanes
+    constexpr int WQ = kMaxQ / 4;
+    float m_run[WQ], l_run[WQ];
+#pragma unroll
+    for (int i = 0; i < WQ; ++i) {
+        m_run[i] = -INFINITY;
+        l_run[i] = 0.f;
+    }
+    // P.V accumulators: dims (2*dp, 2*dp+1) of queries qslice + NQS*i
+    const int dp = tid % (D / 2), qslice = tid / (D / 2);
+    float o0[QPS], o1[QPS];
+#pragma unroll
+    for (int i = 0; i < QPS; ++i) o0[i] = o1[i] = 0.f;
+
+    const int ntiles = (k1 - k0 + kTile - 1) / kTile;
+    load_tile(0, k0);
+    for (int it = 0; it < ntiles; ++it) {
+        const int buf = it & 1;
+        const int t0 = k0 + it * kTile;
+        if (it + 1 < ntiles) {
+            load_tile(buf ^ 1, t0 + kTile);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+
+        // ---- scores: lane = key, warp's queries
+        {
+            const uint16_t *krow = ks + (buf * kTile + lane) * PITCH;
+            float acc[WQ];
+#pragma unroll
+            for (int i = 0; i < WQ; ++i) acc[i] = 0.f;
+#pragma unroll 4
+            for (int c8 = 0; c8 < D; c8 += 8) {
+                const uint4 kw = *reinterpret_cast<const uint4 *>(krow + c8);
+                const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
+                const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
+                const float2 k45 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.z));
+                const float2 k67 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.w));
+#pragma unroll
+                for (int i = 0; i < WQ; ++i) {
+                    const int qi = warp + 4 * i;
+                    if (qi < Q) {
+                        const float4 qa = *reinterpret_cast<const float4 *>(qs + qi * D + c8);
+                        const float4 qb = *reinterpret_cast<const float4 *>(qs + qi * D + c8 + 4);
+                        float v = acc[i];
+                        v = fmaf(qa.x, k01.x, v); v = fmaf(qa.y, k01.y, v);
+                        v = fmaf(qa.z, k23.x, v); v = fmaf(qa.w, k23.y, v);
+                        v = fmaf(qb.x, k45.x, v); v = fmaf(qb.y, k45.y, v);
+                        v = fmaf(qb.z, k67.x, v); v = fmaf(qb.w, k67.y, v);
+                        acc[i] = v;
+                    }
+                }
+            }
+            const int key = t0 + lane;
+#pragma unroll
+            for (int i = 0; i < WQ; ++i) {
+                const int qi = warp + 4 * i;
+                if (qi < Q) {
+                    const bool valid = key < s_len[qi / G];
+                    const float sc = valid ? acc[i] : -INFINITY;
+                    const float mt = warp_max(sc);
+                    const float mn = fmaxf(m_run[i], mt);
+                    const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m_run[i] - mn);
+                    const float p = valid ? exp2f(sc - mn) : 0.f;
+                    l_run[i] = l_run[i] * alpha + warp_sum(p);
+                    m_run[i] = mn;
+                    ps[qi * kTile + lane] = p;
+                    if (lane == 0) al[qi] = alpha;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- P.V: lanes over head-dimension pairs
+        {
+#pragma unroll
+            for (int i = 0; i < QPS; ++i) {
+                const int qi = qslice + NQS * i;
+                if (qi < Q) {
+                    const float alpha = al[qi];
+                    o0[i] *= alpha;
+                    o1[i] *= alpha;
+                }
+            }
+            const uint16_t *vcol = vs + buf * kTile * PITCH + 2 * dp;
+#pragma unroll 4
+            for (int t = 0; t < kTile; t += 4) {
+                float2 vv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    vv[u] = __half22float2(*reinterpret_cast<const __half2 *>(vcol + (t + u) * PITCH));
+#pragma unroll
+                for (int i = 0; i < QPS; ++i) {
+                    const int qi = qslice + NQS * i;
+                    if (qi < Q) {
+                        const float4 p4 = *reinterpret_cast<const float4 *>(ps + qi * kTile + t);
+                        o0[i] = fmaf(p4.x, vv[0].x, o0[i]); o1[i] = fmaf(p4.x, vv[0].y, o1[i]);
+                        o0[i] = fmaf(p4.y, vv[1].x, o0[i]); o1[i] = fmaf(p4.y, vv[1].y, o1[i]);
+                        o0[i] = fmaf(p4.z, vv[2].x, o0[i]); o1[i] = fmaf(p4.z, vv[2].y, o1[i]);
+                        o0[i] = fmaf(p4.w, vv[3].x, o0[i]); o1[i] = fmaf(p4.w, vv[3].y, o1[i]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- publish (m, l) and write this piece's partials for rows that reach it
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < WQ; ++i) {
+            const int qi = warp + 4 * i;
+            if (qi < Q) {
+                sm_m[qi] = m_run[i];
+                sm_l[qi] = l_run[i];
+            }
+        }
+    }
+    __syncthreads();
+    const int ms = P.max_splits;
+#pragma unroll
+    for (int i = 0; i < QPS; ++i) {
+        const int qi = qslice + NQS * i;
+        if (qi < Q) {
+            const int rq = qi / G, gq = qi - rq * G;
+            if (s_len[rq] > k0) {
+                const int r = s_row[rq], head = h * G + gq;
+                const float inv = 1.f / sm_l[qi];
+                float *po = a.part_o + (((int64_t)r * P.n_q + head) * ms + piece) * D;
+                *reinterpret_cast<float2 *>(po + 2 * dp) = make_float2(o0[i] * inv, o1[i] * inv);
+                if (dp == 0)
+                    a.part_lse[((int64_t)r * P.n_q + head) * ms + piece] =
+                        (sm_m[qi] + log2f(sm_l[qi])) * 0.69314718055994530942f;
+            }
+        }
+    }
+}
+
+struct MergeArgs {
+    const float *part_o, *part_lse;
+    const int32_t *seqlen;
+    float *out, *lse;
+    int64_t out_stride;
+    int rows, n_q, chunk, max_splits, capacity;
+    int row_keys_max[DL_MAX_ROWS];
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_merge_kernel(MergeArgs a)
+{
+    constexpr int VPL = D / 32;              // values per lane
+    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= a.rows * a.n_q) return;
+    const int r = gw / a.n_q, h = gw - r * a.n_q;
+    const int L = clip_len(a.seqlen[r], a.row_keys_max[r], a.capacity, nullptr, false);
+    const int np = (L + a.chunk - 1) / a.chunk;
+    const float *pl = a.part_lse + ((int64_t)r * a.n_q + h) * a.max_splits;
+    float M = -INFINITY;
+    for (int p = lane; p < np; p += 32) M = fmaxf(M, pl[p]);
+    M = warp_max(M);
+    float acc[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
+    float W = 0.f;
+    const float *po = a.part_o + ((int64_t)r * a.n_q + h) * a.max_splits * D;
+    for (int p = 0; p < np; ++p) {
+        const float w = __expf(pl[p] - M);
+        W += w;
+        const float *src = po + (int64_t)p * D + lane * VPL;
+        if constexpr (VPL == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src);
+            acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+            acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
+        } else {
+            const float2 v = *reinterpret_cast<const float2 *>(src);
+            acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+        }
+    }
+    float *dst = a.out + r * a.out_stride + h * D + lane * VPL;
+    if (np == 0) {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) dst[i] = 0.f;
+        if (a.lse && lane == 0) a.lse[r * a.n_q + h] = -INFINITY;
+        return;
+    }
+    const float inv = 1.f / W;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) dst[i] = acc[i] * inv;
+    if (a.lse && lane == 0) a.lse[r * a.n_q + h] = M + logf(W);
+}
+
+size_t attn_smem_bytes(int D)
+{
+    const int pitch = D + 8;
+    return (size_t)4 * kTile * pitch * 2 + (size_t)kMaxQ * D * 4 + (size_t)kMaxQ * kTile * 4 + 3 * kMaxQ * 4;
+}
+
+int check_plan(const dl_attn_plan *P)
+{
+    if (!P || P->rows < 1 || P->rows > DL_MAX_ROWS || P->n_sessions < 1 || P->n_sessions > DL_MAX_ROWS ||
+        P->chunk < kTile || P->chunk % kTile != 0 || P->max_splits < 1 || P->n_work < 1 ||
+        P->n_kv < 1 || P->n_q % P->n_kv != 0 || (P->head_dim != 64 && P->head_dim != 128))
+        return dl::fail(DL_E_ARG, "dl attention: invalid plan");
+    return DL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dl_plan_groups(int n, int max_rows, int *sizes)
+{
+    if (n < 0 || max_rows <= 0 || !sizes) return dl::fail(DL_E_ARG, "dl_plan_groups: n=%d max_rows=%d", n, max_rows);
+    if (n == 0) return 0;
+    const int g = (n + max_rows - 1) / max_rows;
+    const int base = n / g, rem = n % g;
+    for (int i = 0; i < g; ++i) sizes[i] = base + (i < rem ? 1 : 0);
+    return g;
+}
+
+int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *region_host,
+                       int n_q, int n_kv, int head_dim, int sm_count, int force_chunk,
+                       dl_attn_plan *out)
+{
+    dl::clear_error();
+    if (!out || !seqlen_host) return dl::fail(DL_E_ARG, "dl_attn_plan_build: null pointer");
+    if (rows < 1 || rows > DL_MAX_ROWS)
+        return dl::fail(DL_E_SHAPE, "dl_attn_plan_build: rows=%d (a command steps 1..%d rows)", rows, DL_MAX_ROWS);
+    if (n_kv < 1 || n_q < n_kv || n_q % n_kv != 0 || n_q / n_kv > kMaxQ)
+        return dl::fail(DL_E_SHAPE, "dl_attn_plan_build: n_q=%d n_kv=%d", n_q, n_kv);
+    if (head_dim != 64 && head_dim != 128)
+        return dl::fail(DL_E_SHAPE, "dl_attn_plan_build: head_dim=%d (64 or 128)", head_dim);
+    if (force_chunk < 0) return dl::fail(DL_E_ARG, "dl_attn_plan_build: force_chunk=%d", force_chunk);
+    for (int r = 0; r < rows; ++r)
+        if (seqlen_host[r] < 1) return dl::fail(DL_E_ARG, "dl_attn_plan_build: seqlen[%d]=%d", r, seqlen_host[r]);
+    if (sm_count <= 0) {
+        int rc = dl::device_sm_count(&sm_count);
+        if (rc != DL_OK) return rc;
+    }
+    dl_attn_plan P;
+    memset(&P, 0, sizeof(P));
+    P.rows = rows;
+    P.n_q = n_q;
+    P.n_kv = n_kv;
+    P.head_dim = head_dim;
+    P.sm_count = sm_count;
+    const int G = n_q / n_kv;
+    const int max_sess_rows = kMaxQ / G;   // rows one work item can serve
+    for (int r = 0; r < rows; ++r) {
+        P.row_region[r] = region_host ? region_host[r] : 0;
+        P.row_keys_max[r] = seqlen_host[r];
+        if (P.row_region[r] < 0) return dl::fail(DL_E_ARG, "dl_attn_plan_build: region[%d]=%d", r, P.row_region[r]);
+    }
+    // sessions: rows sharing a region, in order of first appearance, at most max_sess_rows each
+    bool taken[DL_MAX_ROWS] = {false};
+    int ns = 0, nr = 0;
+    for (int r = 0; r < rows; ++r) {
+        if (taken[r]) continue;
+        P.sess_begin[ns] = nr;
+        int cnt = 0;
+        for (int r2 = r; r2 < rows && cnt < max_sess_rows; ++r2) {
+            if (taken[r2] || P.row_region[r2] != P.row_region[r]) continue;
+            taken[r2] = true;
+            P.sess_rows[nr++] = r2;
+            ++cnt;
+        }
+        ++ns;
+    }
+    P.sess_begin[ns] = nr;
+    P.n_sessions = ns;
+    int lmax[DL_MAX_ROWS];
+    int64_t total = 0;
+    for (int s = 0; s < ns; ++s) {
+        lmax[s] = 0;
+        for (int i = P.sess_begin[s]; i < P.sess_begin[s + 1]; ++i) lmax[s] = std::max(lmax[s], seqlen_host[P.sess_rows[i]]);
+        total += (int64_t)lmax[s] * n_kv;
+    }
+    // pieces sized from this command's own work: about two work items per SM
+    int chunk;
+    if (force_chunk > 0) {
+        chunk = (int)dl::ceil_div(force_chunk, kTile) * kTile;
+    } else {
+        const int64_t target = 2LL * sm_count;
+        chunk = (int)(dl::ceil_div(dl::ceil_div(total, target), kTile) * kTile);
+        if (chunk < kTile) chunk = kTile;
+    }
+    P.chunk = chunk;
+    int items = 0, ms = 0;
+    for (int s = 0; s < ns; ++s) {
+        P.sess_splits[s] = (int)dl::ceil_div(lmax[s], chunk);
+        P.sess_item0[s] = items;
+        items += n_kv * P.sess_splits[s];
+        ms = std::max(ms, P.sess_splits[s]);
+    }
+    P.sess_item0[ns] = items;
+    P.n_work = items;
+    P.max_splits = ms;
+    const size_t po = (size_t)rows * n_q * ms * head_dim * 4;
+    const size_t pl = (size_t)rows * n_q * ms * 4;
+    P.workspace_bytes = ((po + 15) / 16) * 16 + ((pl + 15) / 16) * 16;
+    *out = P;
+    return DL_OK;
+}
+
+int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
+                   const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
+                   int32_t *status, dl_stream_t stream)
+{
+    dl::clear_error();
+    if (!q || !kv || !kv->k || !kv->v || !seqlen || !workspace) return dl::fail(DL_E_ARG, "dl_decode_attn: null pointer");
+    int rc = check_plan(plan);
+    if (rc != DL_OK) return rc;
+    if (kv->head_dim != plan->head_dim || kv->n_kv != plan->n_kv)
+        return dl::fail(DL_E_SHAPE, "dl_decode_attn: cache heads/dim differ from the plan");
+    if (kv->capacity <= 0 || kv->region_stride < (int64_t)kv->n_kv * kv->capacity * kv->head_dim)
+        return dl::fail(DL_E_ARG, "dl_decode_attn: bad cache geometry");
+    for (int r = 0; r < plan->rows; ++r) {
+        if (plan->row_region[r] >= kv->n_regions) return dl::fail(DL_E_ARG, "dl_decode_attn: plan region past the cache");
+        if (plan->row_keys_max[r] > kv->capacity)
+            return dl::fail(DL_E_ARG, "dl_decode_attn: plan covers %d keys of row %d, the cache holds %d",
+                            plan->row_keys_max[r], r, kv->capacity);
+    }
+    if (workspace_bytes < plan->workspace_bytes)
+        return dl::fail(DL_E_WORKSPACE, "dl_decode_attn: workspace %zu < %zu bytes", workspace_bytes, plan->workspace_bytes);
+    if (!dl::aligned16(workspace) || !dl::aligned16(kv->k) || !dl::aligned16(kv->v) || !dl::aligned16(q) ||
+        (q_stride % 4) != 0 || (kv->region_stride % 8) != 0)
+        return dl::fail(DL_E_ALIGN, "dl_decode_attn: q, cache planes and workspace must be 16-byte aligned");
+    if (q_stride < (int64_t)plan->n_q * plan->head_dim) return dl::fail(DL_E_ARG, "dl_decode_attn: q_stride too small");
+
+    AttnArgs a{};
+    a.q = q;
+    a.q_stride = q_stride;
+    a.kc = kv->k;
+    a.vc = kv->v;
+    a.region_stride = kv->region_stride;
+    a.capacity = kv->capacity;
+    a.seqlen = seqlen;
+    const size_t po = (size_t)plan->rows * plan->n_q * plan->max_splits * plan->head_dim * 4;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((po + 15) / 16) * 16);
+    a.status = status;
+    a.qscale = (float)(1.4426950408889634 / std::sqrt((double)plan->head_dim));
+    a.plan = *plan;
+    const size_t smem = attn_smem_bytes(plan->head_dim);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (plan->head_dim == 128) {
+        e = cudaFuncSetAttribute(decode_attn_cc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
+        decode_attn_cc_kernel<128><<<plan->n_work, kAttnThreads, smem, st>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(decode_attn_cc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
+        decode_attn_cc_kernel<64><<<plan->n_work, kAttnThreads, smem, st>>>(a);
+    }
+    return dl::check_launch("dl_decode_attn");
+}
+
+int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t *seqlen,
+                  float *out, int64_t out_stride, float *lse, dl_stream_t stream)
+{
+    dl::clear_error();
+    if (!workspace || !seqlen || !out) return dl::fail(DL_E_ARG, "dl_attn_merge: null pointer");
+    int rc = check_plan(plan);
+    if (rc != DL_OK) return rc;
+    if (out_stride < (int64_t)plan->n_q * plan->head_dim) return dl::fail(DL_E_ARG, "dl_attn_merge: out_stride too small");
+    if (!dl::aligned16(out) || (out_stride % 4) != 0 || !dl::aligned16(workspace))
+        return dl::fail(DL_E_ALIGN, "dl_attn_merge: out and workspace must be 16-byte aligned");
+    MergeArgs m{};
+    const size_t po = (size_t)plan->rows * plan->n_q * plan->max_splits * plan->head_dim * 4;
+    m.part_o = static_cast<const float *>(workspace);
+    m.part_lse = reinterpret_cast<const float *>(static_cast<const char *>(workspace) + ((po + 15) / 16) * 16);
+    m.seqlen = seqlen;
+    m.out = out;
+    m.lse = lse;
+    m.out_stride = out_stride;
+    m.rows = plan->rows;
+    m.n_q = plan->n_q;
+    m.chunk = plan->chunk;
+    m.max_splits = plan->max_splits;
+    m.capacity = 0x7fffffff;   // dl_decode_attn refuses plans that reach past the cache
+    for (int r = 0; r < DL_MAX_ROWS; ++r) m.row_keys_max[r] = plan->row_keys_max[r];
+    const int warps = plan->rows * plan->n_q;
+    const unsigned grid = (unsigned)dl::ceil_div(warps, 4);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (plan->head_dim == 128)
+        attn_merge_kernel<128><<<grid, 128, 0, st>>>(m);
+    else
+        attn_merge_kernel<64><<<grid, 128, 0, st>>>(m);
+    return dl::check_launch("dl_attn_merge");
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+"""A decoder layer's decode step driven through the library's calls.
+
+The step is the path's sequence of launches on one stream, per command of at
+most eight rows:
+
+    dl_gemv_q8(Wqkv)  ->  dl_rope_kv_store  ->  dl_decode_attn  ->  dl_attn_merge
+    ->  dl_gemv_q8(Wo)  ->  dl_gemv_q8(Wgate|up)  ->  dl_gemv_q8(Wdown)
+
+Norms, SwiGLU and residual adds are not part of the path: the gate/up and down
+projections read their own activation buffers (filled by the caller).  More
+than eight rows run as the fewest balanced commands, the weights read once per
+command.  Nothing here computes: it owns buffers and issues the calls.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+from . import (KVCache, PackedQ8, Rope, dl_attn_merge, dl_attn_plan_build, dl_decode_attn, dl_gemv_q8,
+               dl_plan_groups, dl_rope_kv_store, workspace_for)
+
+
+@dataclasses.dataclass
+class LayerWeights:
+    """Packed Q8_0 projections of one layer (gate and up concatenated; FFN optional)."""
+    wqkv: PackedQ8
+    wo: PackedQ8
+    wgu: Optional[PackedQ8] = None
+    wdown: Optional[PackedQ8] = None
+
+    def q8_bytes(self) -> int:
+        return sum(w.nbytes_q8_0 for w in (self.wqkv, self.wo, self.wgu, self.wdown) if w is not None)
+
+
+class Command:
+    """Buffers and plan of one command (1..8 rows) of a layer step."""
+
+    def __init__(self, rows: Sequence[int], positions: Sequence[int], regions: Sequence[int],
+                 n_q: int, n_kv: int, head_dim: int, hidden: int, ffn: int, device, sm_count: int = 0,
+                 force_chunk: int = 0):
+        n = len(rows)
+        assert 1 <= n <= 8
+        self.rows = list(rows)
+        self.n = n
+        D = head_dim
+        self.n_q, self.n_kv, self.D = n_q, n_kv, D
+        self.positions = [int(p) for p in positions]
+        self.regions = [int(r) for r in regions]
+        self.seqlen_host = [p + 1 for p in self.positions]
+        self.plan = dl_attn_plan_build(self.seqlen_host, n_q, n_kv, D, regions=self.regions,
+                                       sm_count=sm_count, force_chunk=force_chunk)
+        dev = device
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.x = torch.zeros(n, hidden, **f32)
+        self.qkv = torch.zeros(n, (n_q + 2 * n_kv) * D, **f32)
+        self.attn = torch.zeros(n, n_q * D, **f32)
+        self.lse = torch.zeros(n, n_q, **f32)
+        self.y_o = torch.zeros(n, hidden, **f32)
+        self.x_ffn = torch.zeros(n, hidden, **f32) if ffn else None
+        self.gu = torch.zeros(n, 2 * ffn, **f32) if ffn else None
+        self.h = torch.zeros(n, ffn, **f32) if ffn else None
+        self.y_down = torch.zeros(n, hidden, **f32) if ffn else None
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.pos = torch.tensor(self.positions, **i32)
+        self.seqlen = torch.tensor(self.seqlen_host, **i32)
+        self.region = torch.tensor(self.regions, **i32)
+        self.status = torch.zeros(1, **i32)
+        self.workspace = workspace_for(self.plan, dev)
+        qd, kd = n_q * D, n_kv * D
+        self.q = self.qkv[:, :qd]
+        self.k = self.qkv[:, qd:qd + kd]
+        self.v = self.qkv[:, qd + kd:]
+
+    def run(self, W: LayerWeights, rope: Rope, kv: KVCache, stream=None):
+        dl_gemv_q8(W.wqkv, self.x, self.qkv, stream=stream)
+        dl_rope_kv_store(self.q, self.k, self.v, self.pos, rope, kv, self.n_q, row_region=self.region,
+                         status=self.status, stream=stream)
+        dl_decode_attn(self.q, kv, self.seqlen, self.plan, self.workspace, status=self.status, stream=stream)
+        dl_attn_merge(self.workspace, self.plan, self.seqlen, self.attn, self.lse, stream=stream)
+        dl_gemv_q8(W.wo, self.attn, self.y_o, stream=stream)
+        if W.wgu is not None:
+            dl_gemv_q8(W.wgu, self.x_ffn, self.gu, stream=stream)
+            dl_gemv_q8(W.wdown, self.h, self.y_down, stream=stream)
+
+    @property
+    def launches(self) -> int:
+        return 7
+
+
+class LayerStep:
+    """All commands of one layer step: rows grouped into commands of at most eight."""
+
+    def __init__(self, positions: Sequence[int], regions: Sequence[int], n_q: int, n_kv: int, head_dim: int,
+                 hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0):
+        n = len(positions)
+        sizes = dl_plan_groups(n)
+        self.commands: List[Command] = []
+        r0 = 0
+        for s in sizes:
+            idx = list(range(r0, r0 + s))
+            self.commands.append(Command(idx, [positions[i] for i in idx], [regions[i] for i in idx],
+                                         n_q, n_kv, head_dim, hidden, ffn, device, sm_count, force_chunk))
+            r0 += s
+        self.group_sizes = sizes
+
+    def run(self, W: LayerWeights, rope: Rope, kv: KVCache, stream=None):
+        for c in self.commands:
+            c.run(W, rope, kv, stream)
+
+    @property
+    def launches(self) -> int:
+        return sum(c.launches for c in self.commands)

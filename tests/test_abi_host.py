@@ -1,0 +1,118 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol include/dl.h
+declares, and its host-only logic (packed sizes, grouping, split plans, RoPE
+tables, argument refusals) behaves as documented."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "dl.h")
+
+
+@pytest.fixture(scope="module")
+def dl():
+    from row_decode_step_gb300 import _build
+    _build.build()
+    import row_decode_step_gb300 as m
+    m.lib()
+    return m
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dl_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(dl):
+    names = _declared_functions()
+    assert len(names) >= 13
+    L = ctypes.CDLL(dl.LIB_PATH)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_version_and_error_text(dl):
+    assert dl.lib().dl_version() == 100
+    with pytest.raises(dl.DLError) as e:
+        dl.dl_q8_packed_size(16, 33)
+    assert e.value.code == dl.DL_E_SHAPE and "n_in" in str(e.value)
+
+
+def test_packed_sizes_match_q8_bytes(dl):
+    for n_out, n_in in ((5120, 3072), (3072, 3072), (16384, 3072), (3072, 8192), (2048, 8192)):
+        qb, db = dl.dl_q8_packed_size(n_out, n_in)
+        assert qb + db == n_out * n_in // 32 * 34
+    # ragged shapes pad to whole tiles
+    qb, db = dl.dl_q8_packed_size(37, 96)
+    assert qb == 3 * 4 * 512 and db == 3 * 4 * 32
+
+
+def test_grouping_matches_oracle_and_golden(dl):
+    for n in range(0, 70):
+        assert dl.dl_plan_groups(n) == (oracle.plan_groups(n) if n else [])
+    assert dl.dl_plan_groups(12) == [6, 6]
+
+
+def test_attn_plan_fills_sms(dl):
+    for rows, sl, regs in ((1, [5121], None), (8, list(range(5121, 5129)), None),
+                           (8, list(range(32761, 32769)), None),
+                           (6, [600, 8000, 513, 4000, 2222, 7777], list(range(6)))):
+        p = dl.dl_attn_plan_build(sl, 24, 8, 128, regions=regs, sm_count=148)
+        assert p.rows == rows and p.chunk % 32 == 0
+        # every key of every row is covered by the pieces of its session
+        for s in range(p.n_sessions):
+            rws = [p.sess_rows[i] for i in range(p.sess_begin[s], p.sess_begin[s + 1])]
+            assert p.sess_splits[s] * p.chunk >= max(sl[r] for r in rws)
+            assert (p.sess_splits[s] - 1) * p.chunk < max(sl[r] for r in rws)
+        assert p.n_work == sum(8 * p.sess_splits[s] for s in range(p.n_sessions))
+        # enough work items to cover the SMs whenever the keys allow it
+        total_tiles = sum(8 * math.ceil(max(sl) / 32) for _ in range(1))
+        assert p.n_work >= min(148, total_tiles)
+        assert p.workspace_bytes >= rows * 24 * p.max_splits * 129 * 4
+
+
+def test_attn_plan_sessions(dl):
+    # rows of one region share work items; different regions do not
+    p = dl.dl_attn_plan_build([100, 101, 50, 102], 24, 8, 128, regions=[3, 3, 1, 3], sm_count=148)
+    assert p.n_sessions == 2
+    assert [p.sess_rows[i] for i in range(4)] == [0, 1, 3, 2]
+    # a session wider than one work item's 32 queries is split
+    p = dl.dl_attn_plan_build([64] * 8, 32, 4, 64, sm_count=148)   # group 8: four rows per item
+    assert p.n_sessions == 2
+
+
+def test_attn_plan_refusals(dl):
+    for args, code in ((([5] * 9, 24, 8, 128), dl.DL_E_SHAPE),
+                       (([0], 24, 8, 128), dl.DL_E_ARG),
+                       (([5], 24, 7, 128), dl.DL_E_SHAPE),
+                       (([5], 24, 8, 96), dl.DL_E_SHAPE)):
+        with pytest.raises(dl.DLError) as e:
+            dl.dl_attn_plan_build(*args, sm_count=148)
+        assert e.value.code == code
+
+
+def test_rope_table_against_double_math(dl):
+    t = dl.dl_rope_table_build(500000.0, 128, 40000).numpy()
+    for p in (0, 1, 127, 5120, 32767, 39999):
+        for j in (0, 1, 31, 63):
+            a = p * 500000.0 ** (-2.0 * j / 128)
+            assert t[p, j, 0] == np.float32(math.cos(a))
+            assert t[p, j, 1] == np.float32(math.sin(a))
+
+
+def test_null_and_shape_refusals_before_any_launch(dl):
+    L = dl.lib()
+    assert L.dl_gemv_q8(None, None, 1, 0, None, 0, None) == dl.DL_E_ARG
+    assert L.dl_rope_kv_store(None, 0, None, 0, None, 0, None, None, None, 1, 8, None, None, None, None) == dl.DL_E_ARG
+    assert L.dl_plan_groups(-1, 8, None) == dl.DL_E_ARG
+    assert L.dl_status_read(None, None) == dl.DL_E_ARG
+    w = dl.dl_q8_weight(16, 16, 64, 100)   # n_in not a multiple of 32
+    x = ctypes.c_float(0)
+    assert L.dl_gemv_q8(ctypes.byref(w), ctypes.byref(x), 1, 128, ctypes.byref(x), 64, None) == dl.DL_E_SHAPE

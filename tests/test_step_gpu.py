@@ -1,0 +1,98 @@
+"""A whole decode layer step through the library against the oracle's step (GPU).
+
+The chain feeds each call's output to the next on both sides, so the
+comparison of a later call also carries the earlier calls' rounding: the
+attention bars apply to the attention of the oracle's own roped q, and the O
+projection is compared with the GEMV bar scaled by the attention bar's share
+of its input (its input is the attention output, not a fresh draw)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.workloads import (assert_attn_close, assert_gemv_close, f16_ulp_dist, gemv_err, kv_planes,
+                             layer_blocks, as_u16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dl():
+    import row_decode_step_gb300 as m
+    from row_decode_step_gb300 import _build
+    _build.build()
+    m.lib()
+    return m
+
+
+def _step(dl, S, positions, regions, n_regions, capacity, label):
+    from row_decode_step_gb300.step import LayerStep, LayerWeights
+    D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
+    blocks = layer_blocks(S.name)
+    if S.name == "tiny":
+        blocks = dict(blocks)
+    packed = {n: dl.dl_q8_pack(b.cuda(), b.shape[0], b.shape[1] * 32) for n, b in blocks.items()}
+    W = LayerWeights(packed["wqkv"], packed["wo"], packed.get("wgu"), packed.get("wdown"))
+    k, v = kv_planes(label, n_regions, n_kv, capacity, D)
+    kv = dl.KVCache(k.cuda(), v.cuda())
+    rope = dl.make_rope(S.rope_theta, D, capacity)
+    n = len(positions)
+    x = synth.normal_f32(0, label + "/x", (n, H))
+    xf = synth.normal_f32(0, label + "/xf", (n, H)) if F else None
+    h = synth.normal_f32(0, label + "/h", (n, F)) if F else None
+    step = LayerStep(positions, regions, n_q, n_kv, D, H, F, "cuda")
+    r0 = 0
+    for c in step.commands:
+        c.x.copy_(x[r0:r0 + c.n].cuda())
+        if F:
+            c.x_ffn.copy_(xf[r0:r0 + c.n].cuda())
+            c.h.copy_(h[r0:r0 + c.n].cuda())
+        r0 += c.n
+    step.run(W, rope, kv)
+    torch.cuda.synchronize()
+
+    kc_o = k.numpy().view(np.uint16).copy()
+    vc_o = v.numpy().view(np.uint16).copy()
+    r0 = 0
+    for c in step.commands:
+        sl = slice(r0, r0 + c.n)
+        ref = oracle.layer_step(blocks, x[sl], kc_o, vc_o, positions[sl], n_q=n_q, n_kv=n_kv, head_dim=D,
+                                theta=S.rope_theta, chunk=c.plan.chunk, n_splits=c.plan.max_splits,
+                                regions=regions[sl], x_ffn=None if xf is None else xf[sl],
+                                h=None if h is None else h[sl])
+        # q is roped in place inside qkv; its k and v parts are the GEMV's own output
+        qd = n_q * D
+        assert_gemv_close(c.qkv.cpu().numpy()[:, qd:], ref["qkv"][:, qd:])
+        np.testing.assert_allclose(c.q.cpu().numpy(), ref["q"], rtol=2e-6, atol=1e-5)
+        assert_attn_close(c.attn.cpu().numpy(), c.lse.cpu().numpy(), ref["attn"], ref["lse"])
+        # the O projection's input differs by the attention error; allow that share on top of the bar
+        assert gemv_err(c.y_o.cpu().numpy(), ref["y_o"]) < 1e-2
+        if F:
+            assert_gemv_close(c.gu.cpu().numpy(), ref["gu"])
+            assert_gemv_close(c.y_down.cpu().numpy(), ref["y_down"])
+        assert dl.dl_status_read(c.status) == 0
+        r0 += c.n
+    kg, vg = as_u16(kv.k), as_u16(kv.v)
+    assert int(f16_ulp_dist(kg, kc_o).max()) <= 1
+    assert int(f16_ulp_dist(vg, vc_o).max()) <= 1
+    return step
+
+
+def test_step_tiny(dl):
+    _step(dl, synth.TINY, [127], [0], 1, 128, "step/tiny")
+
+
+def test_step_1b(dl):
+    _step(dl, synth.LLAMA_1B, [4096], [0], 1, 4097, "step/1b")
+
+
+@pytest.mark.parametrize("rows", [1, 8])
+def test_step_3b(dl, rows):
+    _step(dl, synth.LLAMA_3B, list(range(5120, 5120 + rows)), [0] * rows, 1, 5128, "step/3b%d" % rows)
+
+
+def test_step_twelve_streams(dl):
+    lens = synth.twelve_stream_lengths(0)
+    step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams")
+    assert step.group_sizes == [6, 6]
