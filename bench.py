@@ -1,0 +1,544 @@
+#!/usr/bin/env python
+"""Decode layer-step benchmark of the GB300 decode-step library.
+
+One step = one decode layer step of the Llama-3.2-3B-shaped layer over one
+batch of rows: QKV GEMV, RoPE + KV store, split-KV attention, merge, O GEMV,
+gate/up GEMV, down GEMV (Q8_0 weights, f16 KV mirror, f32 activations).  The
+headline workload is 8 rows of one session at positions 5120..5127 over 5120
+cached keys; 1 row and 12 independent streams (6 + 6 rows) are measured beside
+it.  Eight distinct layers (weights and caches, about 1 GB) are cycled, so the
+inputs of consecutive steps are larger than L2.  Steps are replayed from CUDA
+graphs and timed with CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica (independent sessions, no data
+exchange); the value is all ranks' layer-steps over the slowest rank's time.
+`--impl reference` times the CPU oracle on a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode layer-steps/sec and achieved HBM GB/s (% of GB300 peak) at 1/8/12 rows"
+UNIT = "layer-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--layers", type=int, default=8)
+    p.add_argument("--workload", default="3b-8", choices=["3b-8", "3b-1", "3b-12", "1b-1", "3b-8-32k"])
+    p.add_argument("--no-extras", action="store_true", help="skip the 1-row and 12-stream side measurements")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--gemv-path", type=int, default=0, choices=[0, 1, 2],
+                   help="inner product of the GEMVs: 0 library choice, 1 CUDA cores (<= 2 rows), 2 tensor cores")
+    p.add_argument("--attn-path", type=int, default=0, choices=[0, 1, 2],
+                   help="inner product of the attention: 0 library choice, 1 CUDA cores, 2 tensor cores")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def workload(name):
+    import synth
+    if name == "3b-8":
+        return dict(shape=synth.LLAMA_3B, positions=list(range(5120, 5128)), regions=[0] * 8, n_regions=1,
+                    capacity=5128, desc="Llama-3.2-3B-shaped layer step, 8 rows of one session at "
+                    "positions 5120-5127 over 5120 cached keys")
+    if name == "3b-1":
+        return dict(shape=synth.LLAMA_3B, positions=[5120], regions=[0], n_regions=1, capacity=5128,
+                    desc="Llama-3.2-3B-shaped layer step, 1 row at position 5120 over 5120 cached keys")
+    if name == "3b-12":
+        lens = synth.twelve_stream_lengths(0)
+        return dict(shape=synth.LLAMA_3B, positions=lens, regions=list(range(12)), n_regions=12,
+                    capacity=max(lens) + 1, desc="Llama-3.2-3B-shaped layer step, 12 one-row streams "
+                    "(cache lengths U{512..8192}, seed 0) run as 6+6-row commands")
+    if name == "1b-1":
+        return dict(shape=synth.LLAMA_1B, positions=[4096], regions=[0], n_regions=1, capacity=4097,
+                    desc="Llama-3.2-1B-shaped layer step, 1 row at position 4096 over 4096 cached keys")
+    if name == "3b-8-32k":
+        return dict(shape=synth.LLAMA_3B, positions=list(range(32760, 32768)), regions=[0] * 8, n_regions=1,
+                    capacity=32768, desc="Llama-3.2-3B-shaped layer step, 8 rows at 32760-32767 over "
+                    "32760 cached keys")
+    raise ValueError(name)
+
+
+def step_bytes(wl, step):
+    """Algorithmic HBM bytes of one layer step: weights once per command, each session's keys
+    once, the new K/V rows, and every call's activation rows in and out (f32)."""
+    S = wl["shape"]
+    D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
+    w_bytes = sum(no * ni // 32 * 34 for no, ni in S.projections().values())
+    total = 0
+    for c in step.commands:
+        n = c.n
+        total += w_bytes
+        p = c.plan
+        keys = 0
+        for s in range(p.n_sessions):
+            rows = [p.sess_rows[i] for i in range(p.sess_begin[s], p.sess_begin[s + 1])]
+            keys += max(c.seqlen_host[r] for r in rows)
+        total += keys * n_kv * D * 2 * 2                  # K and V read
+        total += n * n_kv * D * 2 * 2                     # new K and V rows
+        qkv = (n_q + 2 * n_kv) * D
+        act = n * (H + qkv) + n * (qkv + n_q * D)         # QKV GEMV in/out; rope q in/out, k, v in
+        act += n * n_q * D * 2 + n * n_q                  # attention q in, merge out + lse
+        act += n * (n_q * D + H)                          # O GEMV
+        if F:
+            act += n * (H + 2 * F) + n * (F + H)          # gate/up, down
+        total += act * 4
+    return total
+
+
+def gu_bytes(wl, rows):
+    S = wl["shape"]
+    return 2 * S.ffn * S.hidden // 32 * 34 + rows * (S.hidden + 2 * S.ffn) * 4
+
+
+# ----------------------------------------------------------------------------- peaks, clocks, traffic
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs_sustained", "hbm_gbs"):
+            if isinstance(d.get(key), (int, float)) and d[key] > 0:
+                return float(d[key]), "measured (%s)" % key
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.rows = []
+        self.proc = None
+        self.err = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu_index)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError as e:
+            self.err = str(e)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 9:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.err or not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": self.err or "no samples"}
+        sel = [p for (t, p) in self.rows if t0 <= t <= t1] or [p for (_, p) in self.rows]
+        sm = [float(p[1]) for p in sel if p[1].replace(".", "", 1).isdigit()]
+        mx = [float(p[2]) for p in sel if p[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in sel for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sel)}
+
+
+def traffic_for(kernel_tag):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    src = os.path.join(ROOT, "row_decode_step_gb300", "csrc", "gemv_q8.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(path):
+            parts = line.split("#", 1)[0].split()
+            if len(parts) == 3 and parts[0] == kernel_tag and parts[1] == digest:
+                return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def build_layers(wl, L, dev, seed=0):
+    import synth
+    import torch
+    import row_decode_step_gb300 as dl
+    from row_decode_step_gb300.step import LayerWeights
+    S = wl["shape"]
+    layers, caches = [], []
+    for l in range(L):
+        packed = {}
+        for name, (n_out, n_in) in S.projections().items():
+            blocks = synth.q8_0_blocks_from_normal(seed, "%s/L%d/%s" % (S.name, l, name), n_out, n_in, device=dev)
+            packed[name] = dl.dl_q8_pack(blocks, n_out, n_in)
+            del blocks
+        layers.append(LayerWeights(packed["wqkv"], packed["wo"], packed.get("wgu"), packed.get("wdown")))
+        k = synth.kv_cache_normal(seed, "%s/L%d/K" % (S.name, l), wl["n_regions"], S.n_kv, wl["capacity"],
+                                  S.head_dim, device=dev)
+        v = synth.kv_cache_normal(seed, "%s/L%d/V" % (S.name, l), wl["n_regions"], S.n_kv, wl["capacity"],
+                                  S.head_dim, device=dev)
+        caches.append(dl.KVCache(k, v))
+    torch.cuda.synchronize()
+    return layers, caches
+
+
+def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0)):
+    import synth
+    import torch
+    import row_decode_step_gb300 as dl
+    from row_decode_step_gb300.step import LayerStep
+    S = wl["shape"]
+    layers, caches = build_layers(wl, L, dev)
+    rope = dl.make_rope(S.rope_theta, S.head_dim, wl["capacity"], device=dev)
+    step = LayerStep(wl["positions"], wl["regions"], S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, dev,
+                     gemv_path=paths[0], attn_path=paths[1])
+    for i, c in enumerate(step.commands):
+        c.x.copy_(synth.normal_f32(0, "bench/x%d" % i, tuple(c.x.shape), device=dev))
+        if c.x_ffn is not None:
+            c.x_ffn.copy_(synth.normal_f32(0, "bench/xf%d" % i, tuple(c.x_ffn.shape), device=dev))
+            c.h.copy_(synth.normal_f32(0, "bench/h%d" % i, tuple(c.h.shape), device=dev))
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for l in range(L):                      # eager pass: sets kernel attributes, checks the path
+            step.run(layers[l], rope, caches[l])
+    stream.synchronize()
+    # one graph holds the L layer steps back to back (launch gaps overlapped by PDL); K steps
+    # replay it K // L times, then single-layer graphs for the remainder
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for l in range(L):
+            step.run(layers[l], rope, caches[l])
+    g_one = []
+    for l in range(L):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step.run(layers[l], rope, caches[l])
+        g_one.append(g)
+    torch.cuda.synchronize()
+
+    def replay(n):
+        for _ in range(n // L):
+            g_all.replay()
+        for l in range(n % L):
+            g_one[l].replay()
+
+    with torch.cuda.stream(stream):
+        replay(max(3, warmup))
+    stream.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device()).start() if want_clocks else None
+    # soak so that the clock sampler sees the GPU under this load before the timed region
+    t_soak = time.time()
+    with torch.cuda.stream(stream):
+        while time.time() - t_soak < 1.0:
+            replay(4 * L)
+            stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        replay(steps)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1)
+    clocks = None
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+        clocks = sampler.summary(t0 - 0.2, t1 + 0.2)
+    status = sum(int(c.status.item()) for c in step.commands)
+
+    # the dominant kernel on its own: the gate/up GEMV of every layer, back to back, timed on its stream
+    gu_ms = None
+    if S.ffn:
+        c0 = step.commands[0]
+        g_gu = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_gu, stream=stream):
+            for l in range(L):
+                dl.dl_gemv_q8(layers[l].wgu, c0.x_ffn, c0.gu, path=paths[0])
+        reps = max(4, min(200, steps // L))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_gu.replay()
+            k0 = torch.cuda.Event(enable_timing=True)
+            k1 = torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            for _ in range(reps):
+                g_gu.replay()
+            k1.record(stream)
+        torch.cuda.synchronize()
+        gu_ms = k0.elapsed_time(k1) / (reps * L)
+        del g_gu
+    graphs = g_one
+
+    e2e = None
+    if want_e2e:
+        e2e = measure_e2e(step, graphs, L, max(10, min(steps, 500)), stream, dev)
+    return dict(ms_total=ms, ms_per_step=ms / steps, status=status, gu_ms=gu_ms, clocks=clocks, step=step,
+                launches_per_step=step.launches, e2e=e2e)
+
+
+def measure_e2e(step, graphs, L, steps, stream, dev):
+    """Same steps through host buffers: per step, the activation rows and positions are copied
+    from pinned host memory, the graph runs, and the step's outputs are read back."""
+    import torch
+    host_in, host_out = [], []
+    h2d = d2h = 0
+    for c in step.commands:
+        ins = [c.x, c.pos, c.seqlen] + ([c.x_ffn, c.h] if c.x_ffn is not None else [])
+        outs = [c.y_o] + ([c.y_down] if c.y_down is not None else [])
+        hi = [t.detach().cpu().pin_memory() for t in ins]
+        ho = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        host_in.append(list(zip(hi, ins)))
+        host_out.append(list(zip(outs, ho)))
+        h2d += sum(t.numel() * t.element_size() for t in ins)
+        d2h += sum(t.numel() * t.element_size() for t in outs)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            for pairs in host_in:
+                for h, d in pairs:
+                    d.copy_(h, non_blocking=True)
+            graphs[i % L].replay()
+            for pairs in host_out:
+                for d, h in pairs:
+                    h.copy_(d, non_blocking=True)
+            stream.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": steps / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps}
+
+
+def cpu_baseline_sample(wl, budget_s=12.0):
+    """The oracle, as it stands, on one full layer step of the workload (host cores, one thread)."""
+    import numpy as np
+    import oracle
+    import synth
+    S = wl["shape"]
+    D = S.head_dim
+    blocks = {}
+    for name, (n_out, n_in) in S.projections().items():
+        blocks[name] = synth.q8_0_blocks_from_normal(0, "%s/L0/%s" % (S.name, name), n_out, n_in).numpy()
+    k = synth.kv_cache_normal(0, "%s/L0/K" % S.name, wl["n_regions"], S.n_kv, wl["capacity"], D).numpy().view(np.uint16)
+    v = synth.kv_cache_normal(0, "%s/L0/V" % S.name, wl["n_regions"], S.n_kv, wl["capacity"], D).numpy().view(np.uint16)
+    n = len(wl["positions"])
+    x = synth.normal_f32(0, "bench/x0", (n, S.hidden)).numpy()
+    xf = synth.normal_f32(0, "bench/xf0", (n, S.hidden)).numpy()
+    h = synth.normal_f32(0, "bench/h0", (n, S.ffn)).numpy()
+    oracle.lib()
+    reps, t_total = 0, 0.0
+    while reps < 5 and t_total < budget_s:
+        kc, vc = k.copy(), v.copy()
+        t0 = time.perf_counter()
+        for g0 in range(0, n, 8):
+            sl = slice(g0, min(n, g0 + 8))
+            pos = np.array(wl["positions"][sl], np.int32)
+            oracle.layer_step(blocks, x[sl], kc, vc, pos, n_q=S.n_q, n_kv=S.n_kv, head_dim=D,
+                              theta=S.rope_theta, chunk=256, n_splits=-(-int(pos.max() + 1) // 256),
+                              regions=np.array(wl["regions"][sl], np.int32), x_ffn=xf[sl], h=h[sl])
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": reps / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d full layer step(s) of the workload on layer 0, single-threaded C oracle (double)" % reps}
+
+
+def run_ours(args):
+    import torch
+    import row_decode_step_gb300 as dl
+    from row_decode_step_gb300 import _build
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(dl.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    dl.lib()
+
+    wl = workload(args.workload)
+    res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path))
+    ms = res["ms_total"]
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    steps = args.steps
+    value = world * steps / (ms / 1e3)
+    step = res["step"]
+    rows = len(wl["positions"])
+    sb = step_bytes(wl, step)
+    peak, peak_src = hbm_peak()
+    step_gbs = sb / (ms / steps / 1e3) / 1e9
+    gu_avg_ms = res["gu_ms"]
+    gu_gbs = gu_bytes(wl, step.commands[0].n) / (gu_avg_ms / 1e3) / 1e9 if gu_avg_ms else None
+    extras = {}
+    if not args.no_extras and args.workload == "3b-8":
+        for name in ("3b-1", "3b-12"):
+            w2 = workload(name)
+            r2 = measure(w2, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
+                         want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path))
+            sb2 = step_bytes(w2, r2["step"])
+            extras[name] = {"rows": len(w2["positions"]), "layer_steps_per_s": 1e3 / r2["ms_per_step"],
+                            "ms_per_step": r2["ms_per_step"],
+                            "tokens_per_s": len(w2["positions"]) * 1e3 / r2["ms_per_step"],
+                            "algorithmic_gbs": sb2 / (r2["ms_per_step"] / 1e3) / 1e9,
+                            "hbm_frac": sb2 / (r2["ms_per_step"] / 1e3) / 1e9 / peak,
+                            "commands": len(r2["step"].commands), "status": r2["status"]}
+            del r2
+            torch.cuda.empty_cache()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(wl)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "q8_0 weights x f32 activations, f16 KV, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) Q8_0 weights, N(0,1) activations and f16 KV; no trained weights)",
+        "config": {"workload": wl["desc"], "rows": rows, "layers_cycled": args.layers,
+                   "l2": "inputs larger than L2: %d distinct layers cycled (%.2f GB)" % (
+                       args.layers, args.layers * sb / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "commands": [c.n for c in step.commands],
+                   "attn_chunk": [c.plan.chunk for c in step.commands],
+                   "attn_work_items": [c.plan.n_work for c in step.commands],
+                   "gemv_path": args.gemv_path, "attn_path": args.attn_path},
+        "tokens_per_s": rows * value,
+        "step": {"algorithmic_bytes": sb, "algorithmic_gbs": step_gbs, "hbm_frac": step_gbs / peak,
+                 "peak_gbs": peak, "peak_source": peak_src},
+        "roofline": {"kernel": "gemv_q8 gate/up projection (16384 x 3072, %d rows), timed back to back "
+                               "over the %d layers" % (step.commands[0].n, args.layers),
+                     "bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": (gu_gbs / peak) if gu_gbs else None,
+                     "traffic": traffic_for("gemv_gu_%drows" % step.commands[0].n),
+                     "launch_ms": gu_avg_ms, "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": res["e2e"],
+        "gpu_launches": res["launches_per_step"] * steps,
+        "clocks": res["clocks"],
+        "device_status": res["status"],
+        "side_workloads": extras,
+    }
+    print(json.dumps(line))
+
+
+# ----------------------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import synth
+    wl = workload(args.workload)
+    S = wl["shape"]
+    D = S.head_dim
+    n = len(wl["positions"])
+    # a bounded sample of the step: every 32nd output row of each projection and the
+    # attention of one KV head (its query heads) for every row; scaled to a whole step
+    FR = 32
+    blocks = {}
+    for name, (n_out, n_in) in S.projections().items():
+        b = synth.q8_0_blocks_from_normal(0, "%s/L0/%s" % (S.name, name), n_out, n_in).numpy()
+        blocks[name] = np.ascontiguousarray(b[::FR])
+    kc = synth.kv_cache_normal(0, "%s/L0/K" % S.name, wl["n_regions"], S.n_kv, wl["capacity"], D)
+    vc = synth.kv_cache_normal(0, "%s/L0/V" % S.name, wl["n_regions"], S.n_kv, wl["capacity"], D)
+    k1 = np.ascontiguousarray(kc.numpy().view(np.uint16)[:, :1])
+    v1 = np.ascontiguousarray(vc.numpy().view(np.uint16)[:, :1])
+    G = S.n_q // S.n_kv
+    x = synth.normal_f32(0, "bench/x0", (n, S.hidden)).numpy()
+    xf = synth.normal_f32(0, "bench/xf0", (n, S.hidden)).numpy()
+    h = synth.normal_f32(0, "bench/h0", (n, S.ffn)).numpy()
+    q = synth.normal_f32(0, "bench/q0", (n, G * D)).numpy().astype(np.float64)
+    seqlen = np.array([p + 1 for p in wl["positions"]], np.int32)
+    regions = np.array(wl["regions"], np.int32)
+    oracle.lib()
+
+    def one():
+        tg = time.perf_counter()
+        for g0 in range(0, n, 8):
+            sl = slice(g0, min(n, g0 + 8))
+            oracle.gemv_q8(blocks["wqkv"], x[sl])
+            oracle.gemv_q8(blocks["wo"], x[sl])
+            oracle.gemv_q8(blocks["wgu"], xf[sl])
+            oracle.gemv_q8(blocks["wdown"], h[sl])
+        t_gemv = time.perf_counter() - tg
+        ta = time.perf_counter()
+        oracle.attention(q, k1, v1, seqlen, n_q=G, n_kv=1, head_dim=D, chunk=256,
+                         n_splits=-(-int(seqlen.max()) // 256), row_region=regions)
+        t_attn = time.perf_counter() - ta
+        return t_gemv * FR + t_attn * S.n_kv
+
+    for _ in range(args.warmup):
+        one()
+    est = [one() for _ in range(args.steps)]
+    sec_per_step = sum(est) / len(est)
+    value = 1.0 / sec_per_step
+    sample = ("per step: 1/%d of every projection's output rows and 1 of %d KV heads' attention, "
+              "scaled to the whole layer step; single-threaded C oracle (double)" % (FR, S.n_kv))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": wl["desc"], "rows": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    a = parse_args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

@@ -134,6 +134,16 @@ int dl_q8_pack(const uint8_t *blocks, int64_t n_out, int64_t n_in,
 int dl_gemv_q8(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
                float *y, int64_t y_stride, dl_stream_t stream);
 
+/*
+ * dl_gemv_q8 with the inner product chosen by the caller (testing and
+ * measurement): path 0 = automatic (what dl_gemv_q8 does), 1 = f32 CUDA-core
+ * FMAs (commands of 1 or 2 rows only, else DL_E_SHAPE), 2 = f16 tensor-core
+ * products on the exact int8 weights with each activation block split into two
+ * power-of-two-scaled f16 terms and f32 accumulation.  Same result contract.
+ */
+int dl_gemv_q8_ex(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
+                  float *y, int64_t y_stride, int path, dl_stream_t stream);
+
 /* ---------------------------------------------------------------- KV cache */
 
 /*
@@ -260,6 +270,18 @@ int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv,
                    const int32_t *seqlen, const dl_attn_plan *plan,
                    void *workspace, size_t workspace_bytes,
                    int32_t *status, dl_stream_t stream);
+
+/*
+ * dl_decode_attn with the inner product chosen by the caller (testing and
+ * measurement): path 0 = automatic (what dl_decode_attn does: CUDA cores when a
+ * work item serves at most 4 queries, tensor cores above), 1 = f32 CUDA-core
+ * dot products, 2 = 16x8x16 f16 tensor-core products with q split into two f16
+ * terms (hi + lo) and probabilities in f16, f32 accumulation and softmax.
+ */
+int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv,
+                      const int32_t *seqlen, const dl_attn_plan *plan,
+                      void *workspace, size_t workspace_bytes,
+                      int32_t *status, int path, dl_stream_t stream);
 
 /*
  * Log-sum-exp merge of the pieces of every (row, head):

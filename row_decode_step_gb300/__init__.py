@@ -90,12 +90,14 @@ def lib() -> ctypes.CDLL:
             "dl_q8_packed_size": ([I64, I64, P, P], I),
             "dl_q8_pack": ([P, I64, I64, P, P, P], I),
             "dl_gemv_q8": ([P, P, I, I64, P, I64, P], I),
+            "dl_gemv_q8_ex": ([P, P, I, I64, P, I64, I, P], I),
             "dl_rope_table_bytes": ([I, I, P], I),
             "dl_rope_table_build": ([ctypes.c_double, I, I, P], I),
             "dl_rope_kv_store": ([P, I64, P, I64, P, I64, P, P, P, I, I, P, P, P, P], I),
             "dl_plan_groups": ([I, I, P], I),
             "dl_attn_plan_build": ([I, P, P, I, I, I, I, I, P], I),
             "dl_decode_attn": ([P, I64, P, P, P, P, SZ, P, P], I),
+            "dl_decode_attn_ex": ([P, I64, P, P, P, P, SZ, P, I, P], I),
             "dl_attn_merge": ([P, P, P, P, I64, P, P], I),
         }
         for name, (args, res) in sig.items():
@@ -161,8 +163,13 @@ def dl_q8_pack(blocks: torch.Tensor, n_out: int, n_in: int, stream=None) -> Pack
     return PackedQ8(qs, d, n_out, n_in)
 
 
-def dl_gemv_q8(W: PackedQ8, x: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """y[r] = W x[r] for every row of x (f32 [rows][>= n_in], rows may exceed eight)."""
+GEMV_PATH_AUTO, GEMV_PATH_CUDA_CORE, GEMV_PATH_TENSOR = 0, 1, 2
+
+
+def dl_gemv_q8(W: PackedQ8, x: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None,
+               path: int = GEMV_PATH_AUTO) -> torch.Tensor:
+    """y[r] = W x[r] for every row of x (f32 [rows][>= n_in], rows may exceed eight).
+    `path` selects the inner product (dl_gemv_q8_ex); the default is the library's choice."""
     _dev(x, torch.float32, "x")
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit inner stride")
@@ -170,8 +177,12 @@ def dl_gemv_q8(W: PackedQ8, x: torch.Tensor, y: Optional[torch.Tensor] = None, s
     if y is None:
         y = torch.empty(rows, W.n_out, dtype=torch.float32, device=x.device)
     _dev(y, torch.float32, "y")
-    _check(lib().dl_gemv_q8(ctypes.byref(W.c), _ptr(x), rows, x.stride(0), _ptr(y), y.stride(0),
-                            _stream(stream)))
+    if path == GEMV_PATH_AUTO:
+        _check(lib().dl_gemv_q8(ctypes.byref(W.c), _ptr(x), rows, x.stride(0), _ptr(y), y.stride(0),
+                                _stream(stream)))
+    else:
+        _check(lib().dl_gemv_q8_ex(ctypes.byref(W.c), _ptr(x), rows, x.stride(0), _ptr(y), y.stride(0),
+                                   path, _stream(stream)))
     return y
 
 
@@ -258,13 +269,22 @@ def workspace_for(plan: dl_attn_plan, device="cuda") -> torch.Tensor:
     return torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=device)
 
 
+ATTN_PATH_AUTO, ATTN_PATH_CUDA_CORE, ATTN_PATH_TENSOR = 0, 1, 2
+
+
 def dl_decode_attn(q: torch.Tensor, kv: KVCache, seqlen: torch.Tensor, plan: dl_attn_plan,
-                   workspace: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+                   workspace: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None,
+                   path: int = ATTN_PATH_AUTO) -> None:
     _dev(q, torch.float32, "q")
     _dev(seqlen, torch.int32, "seqlen")
     _dev(workspace, torch.uint8, "workspace")
-    _check(lib().dl_decode_attn(_ptr(q), q.stride(0), ctypes.byref(kv.c), _ptr(seqlen), ctypes.byref(plan),
-                                _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+    if path == ATTN_PATH_AUTO:
+        _check(lib().dl_decode_attn(_ptr(q), q.stride(0), ctypes.byref(kv.c), _ptr(seqlen), ctypes.byref(plan),
+                                    _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+    else:
+        _check(lib().dl_decode_attn_ex(_ptr(q), q.stride(0), ctypes.byref(kv.c), _ptr(seqlen),
+                                       ctypes.byref(plan), _ptr(workspace), workspace.numel(), _ptr(status),
+                                       path, _stream(stream)))
 
 
 def dl_attn_merge(workspace: torch.Tensor, plan: dl_attn_plan, seqlen: torch.Tensor,
@@ -280,13 +300,13 @@ def dl_status_read(status: torch.Tensor) -> int:
     return v.value
 
 
-def decode_attention(q, kv, seqlen, plan, workspace, out=None, lse=None, status=None, stream=None):
+def decode_attention(q, kv, seqlen, plan, workspace, out=None, lse=None, status=None, stream=None, path=0):
     """dl_decode_attn followed by dl_attn_merge; returns (out, lse)."""
     rows = plan.rows
     if out is None:
         out = torch.empty(rows, plan.n_q * plan.head_dim, dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty(rows, plan.n_q, dtype=torch.float32, device=q.device)
-    dl_decode_attn(q, kv, seqlen, plan, workspace, status=status, stream=stream)
+    dl_decode_attn(q, kv, seqlen, plan, workspace, status=status, stream=stream, path=path)
     dl_attn_merge(workspace, plan, seqlen, out, lse, stream=stream)
     return out, lse

@@ -13,6 +13,7 @@
 #include <cuda_fp16.h>
 #include <cmath>
 #include <cstring>
+#include <algorithm>
 
 #include "dl_common.cuh"
 
@@ -21,6 +22,7 @@ namespace {
 constexpr int kAttnThreads = 128;
 constexpr int kTile = 32;          // keys per tile
 constexpr int kMaxQ = 32;          // queries one work item serves (session rows x group)
+constexpr int kCudaCoreMaxQ = 4;   // queries per work item up to which the CUDA-core form is used
 
 struct AttnArgs {
     const float *q;
@@ -71,7 +73,7 @@ __device__ __forceinline__ int clip_len(int L, int planned, int capacity, int32_
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads) decode_attn_cc_kernel(AttnArgs a)
+__global__ void __launch_bounds__(kAttnThreads) decode_attn_cc_kernel(const __grid_constant__ AttnArgs a)
 {
     constexpr int PITCH = D + 8;                 // halves per staged row (16-byte pad: conflict-free)
     constexpr int NQS = kAttnThreads / (D / 2);  // query slices of the P.V phase
@@ -99,6 +101,22 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_cc_kernel(AttnArgs a
     const int G = P.n_q / P.n_kv;
     const int Q = nrows * G;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ask L2 for this piece's keys and values (planned bound) before waiting on the previous kernel
+    if (tid == 0) {
+        int lplan = 0;
+        for (int i = 0; i < nrows; ++i) lplan = max(lplan, P.row_keys_max[P.sess_rows[rb + i]]);
+        lplan = min(lplan, a.capacity);
+        const int p0 = piece * P.chunk, p1 = min(p0 + P.chunk, lplan);
+        if (p1 > p0) {
+            const int64_t off = (int64_t)P.row_region[P.sess_rows[rb]] * a.region_stride +
+                                ((int64_t)h * a.capacity + p0) * D;
+            dl_prefetch_l2(a.kc + off, (uint32_t)(p1 - p0) * D * 2u);
+            dl_prefetch_l2(a.vc + off, (uint32_t)(p1 - p0) * D * 2u);
+        }
+    }
+    dl_pdl_launch_dependents();
+    dl_pdl_wait();
 
     if (tid < nrows) {
         const int r = P.sess_rows[rb + tid];
@@ -281,6 +299,319 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_cc_kernel(AttnArgs a
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core form for sessions of several rows (many queries per KV head):
+// queries are the 16-row M side of 16x8x16 f16 products.  Each warp owns one
+// 16-query tile and a contiguous share of the piece's keys, streams 16-key
+// blocks of K and V into its own double-buffered, XOR-swizzled shared-memory
+// ring with cp.async, and keeps (m, l, O) for its queries in registers: scores
+// S = Q K^T with Q split into two f16 terms (hi + lo, near-f32 exact), online
+// softmax in the log2 domain on the accumulator fragments, then O += P V with P
+// in f16 (the running maximum's own entry is exactly 1).  The warps holding the
+// same queries combine their (m, l, O) in shared memory at the end.
+
+__device__ __forceinline__ void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(float lo, float hi)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+constexpr int kMmaKB = 16;      // keys per block of the tensor-core form
+
+size_t attn_mma_smem_bytes(int D)
+{
+    const size_t ring = (size_t)4 * 2 * 2 * kMmaKB * D * 2;             // warps x stages x (K,V) x block
+    const size_t comb = (size_t)4 * 16 * D * 4 + (size_t)4 * 16 * 2 * 4;  // O, m, l of every warp
+    const size_t qf = (size_t)2 * (D / 16) * 32 * 32;                    // query fragments, 2 tiles
+    return (ring > comb ? ring : comb) + qf;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 2) decode_attn_mma_kernel(const __grid_constant__ AttnArgs a)
+{
+    constexpr int KB = kMmaKB;
+    constexpr int CPR = D / 8;      // 16-byte chunks per key row
+    constexpr int NKS = D / 16;     // k-steps of the score product
+    constexpr int NDT = D / 8;      // 8-wide column tiles of the output
+    constexpr int BLK = KB * D;     // halves per K (or V) block
+    const dl_attn_plan &P = a.plan;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS];
+
+    const int item = blockIdx.x;
+    int s = 0;
+    while (s + 1 < P.n_sessions && item >= P.sess_item0[s + 1]) ++s;
+    const int local = item - P.sess_item0[s];
+    const int splits = P.sess_splits[s];
+    const int h = local / splits, piece = local - h * splits;
+    const int rb = P.sess_begin[s], nrows = P.sess_begin[s + 1] - rb;
+    const int G = P.n_q / P.n_kv;
+    const int Q = nrows * G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, c = lane & 3;
+
+    if (tid == 0) {
+        int lplan = 0;
+        for (int i = 0; i < nrows; ++i) lplan = max(lplan, P.row_keys_max[P.sess_rows[rb + i]]);
+        lplan = min(lplan, a.capacity);
+        const int p0 = piece * P.chunk, p1 = min(p0 + P.chunk, lplan);
+        if (p1 > p0) {
+            const int64_t off = (int64_t)P.row_region[P.sess_rows[rb]] * a.region_stride +
+                                ((int64_t)h * a.capacity + p0) * D;
+            dl_prefetch_l2(a.kc + off, (uint32_t)(p1 - p0) * D * 2u);
+            dl_prefetch_l2(a.vc + off, (uint32_t)(p1 - p0) * D * 2u);
+        }
+    }
+    dl_pdl_launch_dependents();
+    dl_pdl_wait();
+
+    if (tid < nrows) {
+        const int r = P.sess_rows[rb + tid];
+        s_row[tid] = r;
+        s_len[tid] = clip_len(a.seqlen[r], P.row_keys_max[r], a.capacity, a.status, piece == 0 && h == 0);
+    }
+    __syncthreads();
+    int lmax = 0;
+    for (int i = 0; i < nrows; ++i) lmax = max(lmax, s_len[i]);
+    const int k0 = piece * P.chunk;
+    const int k1 = min(k0 + P.chunk, lmax);
+    if (k0 >= k1) return;
+
+    const int reg = P.row_region[s_row[0]];
+    const uint16_t *kbase = a.kc + (int64_t)reg * a.region_stride + (int64_t)h * a.capacity * D;
+    const uint16_t *vbase = a.vc + (int64_t)reg * a.region_stride + (int64_t)h * a.capacity * D;
+
+    const int MT = (Q + 15) >> 4;          // 16-query tiles (1 or 2)
+    const int KS = 4 / MT;                 // warps sharing one query tile
+    const int mt = warp % MT, ksp = warp / MT;
+    const int nblk = (k1 - k0 + KB - 1) / KB;
+    const int b_begin = ksp * nblk / KS, b_end = (ksp + 1) * nblk / KS;
+
+    // ---- query operand fragments (log2-domain scaled, hi + lo f16 terms) in shared memory:
+    // [query tile][k-step][lane] 32 bytes = a0..a3 hi then a0..a3 lo
+    const int r0 = mt * 16 + g, r1 = r0 + 8;
+    unsigned char *qfrag = smem + (size_t)4 * 2 * 2 * BLK * 2;
+    for (int fi = tid; fi < MT * NKS * 32; fi += kAttnThreads) {
+        const int t = fi & 31, ks = (fi >> 5) % NKS, qt = (fi >> 5) / NKS;
+        const int gg = t >> 2, cc = t & 3;
+        const int q0i = qt * 16 + gg, q1i = q0i + 8;
+        const float *q0 = q0i < Q ? a.q + (int64_t)s_row[q0i / G] * a.q_stride + (h * G + q0i % G) * D : nullptr;
+        const float *q1 = q1i < Q ? a.q + (int64_t)s_row[q1i / G] * a.q_stride + (h * G + q1i % G) * D : nullptr;
+        uint32_t hv[4], lv[4];
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            const float *src = (part & 1) ? q1 : q0;
+            const int col = ks * 16 + 2 * cc + (part >> 1) * 8;
+            float2 v = make_float2(0.f, 0.f);
+            if (src) v = *reinterpret_cast<const float2 *>(src + col);
+            v.x *= a.qscale;
+            v.y *= a.qscale;
+            const __half2 hq = __floats2half2_rn(v.x, v.y);
+            const float2 hf = __half22float2(hq);
+            hv[part] = *reinterpret_cast<const uint32_t *>(&hq);
+            lv[part] = h2_bits(v.x - hf.x, v.y - hf.y);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(qfrag + (size_t)fi * 32);
+        dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        dst[1] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+    }
+    __syncthreads();
+    const unsigned char *myq = qfrag + (size_t)mt * NKS * 32 * 32 + lane * 32;
+    const int len0 = r0 < Q ? s_len[r0 / G] : 0;
+    const int len1 = r1 < Q ? s_len[r1 / G] : 0;
+
+    float o[NDT][4];
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem) + warp * 2 * 2 * BLK;   // [stage][K, V][KB][D]
+    auto load_block = [&](int stage, int b) {
+        uint16_t *kd = ring + stage * 2 * BLK, *vd = kd + BLK;
+        const int kb0 = k0 + b * KB;
+#pragma unroll
+        for (int i = lane; i < KB * CPR; i += 32) {
+            const int key = i / CPR, ch = i - key * CPR;
+            const int off = key * D + ((ch ^ (key & 7)) << 3);
+            const int kk = kb0 + key;
+            if (kk < k1) {
+                cp_async16(kd + off, kbase + (int64_t)kk * D + ch * 8);
+                cp_async16(vd + off, vbase + (int64_t)kk * D + ch * 8);
+            } else {
+                *reinterpret_cast<uint4 *>(kd + off) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(vd + off) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        cp_async_commit();
+    };
+
+    if (b_begin < b_end) load_block(0, b_begin);
+    for (int b = b_begin; b < b_end; ++b) {
+        const int stage = (b - b_begin) & 1;
+        if (b + 1 < b_end) {
+            load_block(stage ^ 1, b + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncwarp();
+        const uint32_t ksm = static_cast<uint32_t>(__cvta_generic_to_shared(ring + stage * 2 * BLK));
+        const uint32_t vsm = ksm + BLK * 2;
+
+        // scores of 16 keys: two 8-key column tiles, hi and lo terms in independent chains
+        float sc[2][4], sl[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
+        }
+#pragma unroll
+        for (int ks = 0; ks < NKS; ks += 2) {
+            const uint4 qa = *reinterpret_cast<const uint4 *>(myq + (ks * 32) * 32);
+            const uint4 qb = *reinterpret_cast<const uint4 *>(myq + (ks * 32) * 32 + 16);
+            const uint4 qc = *reinterpret_cast<const uint4 *>(myq + ((ks + 1) * 32) * 32);
+            const uint4 qd = *reinterpret_cast<const uint4 *>(myq + ((ks + 1) * 32) * 32 + 16);
+            const uint32_t qh0[4] = {qa.x, qa.y, qa.z, qa.w}, ql0[4] = {qb.x, qb.y, qb.z, qb.w};
+            const uint32_t qh1[4] = {qc.x, qc.y, qc.z, qc.w}, ql1[4] = {qd.x, qd.y, qd.z, qd.w};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int key = nt * 8 + (lane & 7);
+                const int ch = 2 * ks + (lane >> 3);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(b0, b1, b2, b3, ksm + (uint32_t)(key * D + ((ch ^ (key & 7)) << 3)) * 2u);
+                mma_f16(sc[nt], qh0, b0, b1);
+                mma_f16(sl[nt], ql0, b0, b1);
+                mma_f16(sc[nt], qh1, b2, b3);
+                mma_f16(sl[nt], ql1, b2, b3);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[nt][e] += sl[nt][e];
+        // mask keys past each row's count, online softmax per row (quad of lanes = one row)
+        const int kb0 = k0 + b * KB;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int key = kb0 + nt * 8 + 2 * c + e;
+                if (key >= len0) sc[nt][e] = -INFINITY;
+                if (key >= len1) sc[nt][2 + e] = -INFINITY;
+                mx0 = fmaxf(mx0, sc[nt][e]);
+                mx1 = fmaxf(mx1, sc[nt][2 + e]);
+            }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
+        const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+        float ps[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            ps[nt][0] = sc[nt][0] == -INFINITY ? 0.f : exp2f(sc[nt][0] - mn0);
+            ps[nt][1] = sc[nt][1] == -INFINITY ? 0.f : exp2f(sc[nt][1] - mn0);
+            ps[nt][2] = sc[nt][2] == -INFINITY ? 0.f : exp2f(sc[nt][2] - mn1);
+            ps[nt][3] = sc[nt][3] == -INFINITY ? 0.f : exp2f(sc[nt][3] - mn1);
+        }
+        l0 = l0 * al0 + (ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1]);
+        l1 = l1 * al1 + (ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3]);
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < NDT; ++i) {
+                o[i][0] *= al0;
+                o[i][1] *= al0;
+                o[i][2] *= al1;
+                o[i][3] *= al1;
+            }
+        }
+        const uint32_t pa[4] = {h2_bits(ps[0][0], ps[0][1]), h2_bits(ps[0][2], ps[0][3]),
+                                h2_bits(ps[1][0], ps[1][1]), h2_bits(ps[1][2], ps[1][3])};
+        // O += P V: two 8-wide output tiles per transposed 4-matrix load
+        const int vkey = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int j = 0; j < NDT / 2; ++j) {
+            const int ch = 2 * j + (lane >> 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(b0, b1, b2, b3, vsm + (uint32_t)(vkey * D + ((ch ^ (vkey & 7)) << 3)) * 2u);
+            mma_f16(o[2 * j], pa, b0, b1);
+            mma_f16(o[2 * j + 1], pa, b2, b3);
+        }
+        __syncwarp();
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+    // ---- combine the warps that share a query tile, then write this piece's partials
+    __syncthreads();                                   // every warp is done with its ring
+    float *co = reinterpret_cast<float *>(smem);       // [4 warps][16][D]
+    float *cm = co + 4 * 16 * D;                       // [4 warps][16]
+    float *cl = cm + 4 * 16;                           // [4 warps][16]
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) {
+        *reinterpret_cast<float2 *>(co + (warp * 16 + g) * D + i * 8 + 2 * c) = make_float2(o[i][0], o[i][1]);
+        *reinterpret_cast<float2 *>(co + (warp * 16 + g + 8) * D + i * 8 + 2 * c) = make_float2(o[i][2], o[i][3]);
+    }
+    if (c == 0) {
+        cm[warp * 16 + g] = m0;
+        cm[warp * 16 + g + 8] = m1;
+        cl[warp * 16 + g] = l0;
+        cl[warp * 16 + g + 8] = l1;
+    }
+    __syncthreads();
+    const int ms = P.max_splits;
+    for (int e = tid; e < MT * 16 * D; e += kAttnThreads) {
+        const int qt = e / (16 * D), rem = e - qt * 16 * D;
+        const int row = rem / D, d = rem - row * D;
+        const int qi = qt * 16 + row;
+        if (qi >= Q) continue;
+        const int rq = qi / G, gq = qi - rq * G;
+        if (s_len[rq] <= k0) continue;
+        float M = -INFINITY;
+        for (int kq = 0; kq < KS; ++kq) M = fmaxf(M, cm[(kq * MT + qt) * 16 + row]);
+        float wsum = 0.f, acc = 0.f;
+        for (int kq = 0; kq < KS; ++kq) {
+            const int w = kq * MT + qt;
+            const float mw = cm[w * 16 + row];
+            const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            wsum += f * cl[w * 16 + row];
+            acc += f * co[(w * 16 + row) * D + d];
+        }
+        const int r = s_row[rq], head = h * G + gq;
+        const int64_t pidx = ((int64_t)r * P.n_q + head) * ms + piece;
+        a.part_o[pidx * D + d] = acc / wsum;
+        if (d == 0) a.part_lse[pidx] = (M + log2f(wsum)) * 0.69314718055994530942f;
+    }
+}
+
 struct MergeArgs {
     const float *part_o, *part_lse;
     const int32_t *seqlen;
@@ -290,17 +621,27 @@ struct MergeArgs {
     int row_keys_max[DL_MAX_ROWS];
 };
 
+// One CTA per (row, head); its four warps take every fourth piece, so the pieces'
+// loads are in flight together, and combine their sums in shared memory.
 template <int D>
-__global__ void __launch_bounds__(128) attn_merge_kernel(MergeArgs a)
+__global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__ MergeArgs a)
 {
     constexpr int VPL = D / 32;              // values per lane
-    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= a.rows * a.n_q) return;
-    const int r = gw / a.n_q, h = gw - r * a.n_q;
+    __shared__ float s_acc[4][D];
+    __shared__ float s_w[4];
+    dl_pdl_launch_dependents();
+    dl_pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x / a.n_q, h = blockIdx.x - (blockIdx.x / a.n_q) * a.n_q;
     const int L = clip_len(a.seqlen[r], a.row_keys_max[r], a.capacity, nullptr, false);
     const int np = (L + a.chunk - 1) / a.chunk;
     const float *pl = a.part_lse + ((int64_t)r * a.n_q + h) * a.max_splits;
+    float *dst = a.out + r * a.out_stride + h * D;
+    if (np == 0) {
+        for (int d = threadIdx.x; d < D; d += 128) dst[d] = 0.f;
+        if (a.lse && threadIdx.x == 0) a.lse[r * a.n_q + h] = -INFINITY;
+        return;
+    }
     float M = -INFINITY;
     for (int p = lane; p < np; p += 32) M = fmaxf(M, pl[p]);
     M = warp_max(M);
@@ -308,31 +649,42 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(MergeArgs a)
 #pragma unroll
     for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
     float W = 0.f;
-    const float *po = a.part_o + ((int64_t)r * a.n_q + h) * a.max_splits * D;
-    for (int p = 0; p < np; ++p) {
-        const float w = __expf(pl[p] - M);
-        W += w;
-        const float *src = po + (int64_t)p * D + lane * VPL;
-        if constexpr (VPL == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-            acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(src);
-            acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+    const float *po = a.part_o + ((int64_t)r * a.n_q + h) * a.max_splits * D + lane * VPL;
+    for (int p0 = warp; p0 < np; p0 += 16) {
+        float w[4], v[4][VPL];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int p = p0 + 4 * u;
+            w[u] = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
+            if (p < np) {
+                w[u] = __expf(pl[p] - M);
+                if constexpr (VPL == 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(po + (int64_t)p * D);
+                    v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2 *>(po + (int64_t)p * D);
+                    v[u][0] = t.x; v[u][1] = t.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            W += w[u];
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
         }
     }
-    float *dst = a.out + r * a.out_stride + h * D + lane * VPL;
-    if (np == 0) {
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) dst[i] = 0.f;
-        if (a.lse && lane == 0) a.lse[r * a.n_q + h] = -INFINITY;
-        return;
-    }
-    const float inv = 1.f / W;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) dst[i] = acc[i] * inv;
-    if (a.lse && lane == 0) a.lse[r * a.n_q + h] = M + logf(W);
+    for (int i = 0; i < VPL; ++i) s_acc[warp][lane * VPL + i] = acc[i];
+    if (lane == 0) s_w[warp] = W;
+    __syncthreads();
+    const float Wt = s_w[0] + s_w[1] + s_w[2] + s_w[3];
+    const float inv = 1.f / Wt;
+    for (int d = threadIdx.x; d < D; d += 128)
+        dst[d] = (s_acc[0][d] + s_acc[1][d] + s_acc[2][d] + s_acc[3][d]) * inv;
+    if (a.lse && threadIdx.x == 0) a.lse[r * a.n_q + h] = M + logf(Wt);
 }
 
 size_t attn_smem_bytes(int D)
@@ -448,9 +800,9 @@ int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *regi
     return DL_OK;
 }
 
-int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
-                   const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
-                   int32_t *status, dl_stream_t stream)
+static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
+                            const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
+                            int32_t *status, int path, dl_stream_t stream)
 {
     dl::clear_error();
     if (!q || !kv || !kv->k || !kv->v || !seqlen || !workspace) return dl::fail(DL_E_ARG, "dl_decode_attn: null pointer");
@@ -487,19 +839,33 @@ int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv, cons
     a.status = status;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)plan->head_dim));
     a.plan = *plan;
-    const size_t smem = attn_smem_bytes(plan->head_dim);
+    if (path < 0 || path > 2) return dl::fail(DL_E_ARG, "dl_decode_attn: path=%d", path);
+    int qmax = 0;
+    for (int si = 0; si < plan->n_sessions; ++si)
+        qmax = std::max(qmax, (plan->sess_begin[si + 1] - plan->sess_begin[si]) * (plan->n_q / plan->n_kv));
+    const bool mma = path == 2 || (path == 0 && qmax > kCudaCoreMaxQ);
+    const size_t smem = mma ? attn_mma_smem_bytes(plan->head_dim) : attn_smem_bytes(plan->head_dim);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (plan->head_dim == 128) {
-        e = cudaFuncSetAttribute(decode_attn_cc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
-        decode_attn_cc_kernel<128><<<plan->n_work, kAttnThreads, smem, st>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(decode_attn_cc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
-        decode_attn_cc_kernel<64><<<plan->n_work, kAttnThreads, smem, st>>>(a);
-    }
-    return dl::check_launch("dl_decode_attn");
+    auto kern = mma ? (plan->head_dim == 128 ? decode_attn_mma_kernel<128> : decode_attn_mma_kernel<64>)
+                    : (plan->head_dim == 128 ? decode_attn_cc_kernel<128> : decode_attn_cc_kernel<64>);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
+    return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kAttnThreads), smem, st, "dl_decode_attn: launch", a);
+}
+
+int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
+                   const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
+                   int32_t *status, dl_stream_t stream)
+{
+    return decode_attn_impl(q, q_stride, kv, seqlen, plan, workspace, workspace_bytes, status, 0, stream);
+}
+
+int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
+                      const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
+                      int32_t *status, int path, dl_stream_t stream)
+{
+    return decode_attn_impl(q, q_stride, kv, seqlen, plan, workspace, workspace_bytes, status, path, stream);
 }
 
 int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t *seqlen,
@@ -526,14 +892,10 @@ int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t
     m.max_splits = plan->max_splits;
     m.capacity = 0x7fffffff;   // dl_decode_attn refuses plans that reach past the cache
     for (int r = 0; r < DL_MAX_ROWS; ++r) m.row_keys_max[r] = plan->row_keys_max[r];
-    const int warps = plan->rows * plan->n_q;
-    const unsigned grid = (unsigned)dl::ceil_div(warps, 4);
+    const unsigned grid = (unsigned)(plan->rows * plan->n_q);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (plan->head_dim == 128)
-        attn_merge_kernel<128><<<grid, 128, 0, st>>>(m);
-    else
-        attn_merge_kernel<64><<<grid, 128, 0, st>>>(m);
-    return dl::check_launch("dl_attn_merge");
+    auto kern = plan->head_dim == 128 ? attn_merge_kernel<128> : attn_merge_kernel<64>;
+    return dl::launch_pdl(kern, dim3(grid), dim3(128), 0, st, "dl_attn_merge: launch", m);
 }
 
 }  // extern "C"

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <cstddef>
+#include <utility>
 
 #include "dl.h"
 
@@ -26,7 +27,40 @@ int device_sm_count(int *out);
 // Check the launch that was just issued; returns DL_OK or DL_E_CUDA.
 int check_launch(const char *what);
 
+
+// Launch `kern` on `st` as a programmatic dependent of the previous kernel in the
+// stream (it may start before that kernel ends and must call dl_pdl_wait()
+// before touching anything the previous kernel writes or reads).
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      const char *what, Args &&...args)
+{
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&lc, kern, std::forward<Args>(args)...);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return DL_OK;
+}
+
 }  // namespace dl
+
+// Device side: wait for the previous kernel of the stream (no-op without PDL).
+__device__ __forceinline__ void dl_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Device side: let the next kernel of the stream begin launching.
+__device__ __forceinline__ void dl_pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+// Device side: ask L2 to fetch [p, p + bytes) (16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void dl_prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // Device side: OR bits into a status word (no trap, no assert).
 __device__ __forceinline__ void dl_status_or(int32_t *status, int32_t bits)

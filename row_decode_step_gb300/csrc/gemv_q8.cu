@@ -8,22 +8,34 @@
 // same +16, c = t%4 (the A-operand order of a 16x8x16 tensor-core product).
 // Scales: per 16 rows and 4 tiles, 128 bytes; lane group g reads 16 bytes.
 //
-// Kernel shape: a CTA of 8 warps owns RTC row tiles and one K-slice; the
-// slice's activations are staged once in shared memory, the warps split the
-// slice's k-tiles, each streaming 16-byte weight loads (L1 bypass) straight into
-// registers.  Partial sums are reduced across warps in shared memory and, when
-// K is split over several CTAs, across a thread-block cluster through
-// distributed shared memory (fixed order: deterministic).
+// Kernel shape (2-D tiling of the matrix):
+//  * a CTA of 8 warps owns a run of row tiles and one K-slice of 8*KW k-tiles;
+//    warp w owns KW consecutive k-tiles of the slice for every row tile of the
+//    CTA, so its share of the activations is loaded from global memory once and
+//    kept in registers for the whole launch;
+//  * the warps stream their weight tiles with 16-byte L1-bypassing loads, two
+//    groups in flight; partial sums of a group of row tiles are reduced across
+//    the warps in shared memory in a fixed order;
+//  * the K-slices of one run of row tiles form a thread-block cluster whose
+//    partials are summed through distributed shared memory in rank order (no
+//    atomics: results do not depend on timing);
+//  * before waiting on the previous kernel (programmatic dependent launch) each
+//    CTA asks L2 to prefetch all of its weights, so weight streaming overlaps the
+//    previous kernel's tail.
+// Two inner products share this shape: f32 CUDA-core FMAs (few rows) and
+// 16x8x16 f16 tensor-core products on exact int8 weights with the activations
+// split into two f16 terms (hi + lo) per power-of-two-scaled block, f32
+// accumulation (more rows, where FMAs would bound the kernel).
 #include <cuda_fp16.h>
 #include <cstdio>
+#include <type_traits>
 
 #include "dl_common.cuh"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = 8;
-constexpr size_t kXsBudget = 96 * 1024;   // bytes of staged activations per CTA
+
+enum { PATH_AUTO = 0, PATH_CUDA_CORE = 1, PATH_TENSOR = 2 };
 
 struct GemvArgs {
     const uint4 *qs;        // packed weight tiles
@@ -32,28 +44,12 @@ struct GemvArgs {
     float *y;
     int64_t x_stride, y_stride;
     int n_out, n_in;
+    int nr;                 // rows of this command, 1..8
     int KT;                 // k-tiles, padded to a multiple of 4
     int RT;                 // row tiles
     int cs;                 // K-slices (= cluster size)
-    int ksl;                // k-tiles per slice (multiple of 4)
+    int ksl;                // k-tiles per K-slice
 };
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// int8 byte `sel` of w (already XOR-ed with 0x80 so it reads as q + 128) to float q:
-// the byte becomes the low mantissa bits of 2^23, and 2^23 + 128 is subtracted.
-__device__ __forceinline__ float s8_to_f32(uint32_t wx, uint32_t sel)
-{
-    uint32_t bits = __byte_perm(wx, 0x4B000000u, 0x7540u | sel);
-    return __uint_as_float(bits) - 8388736.0f;
-}
 
 __device__ __forceinline__ void cluster_sync_all()
 {
@@ -71,161 +67,363 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
     return v;
 }
 
-template <int NR, int RTC>
-__global__ void __launch_bounds__(kThreads, 2) gemv_q8_cc_kernel(GemvArgs a)
+// byte `sel` of wx (a stored weight byte, q + 128) to float q: the byte becomes the low
+// mantissa bits of 2^23 and 2^23 + 128 is subtracted.
+__device__ __forceinline__ float s8_to_f32(uint32_t wx, uint32_t sel)
 {
-    constexpr int U = (8 / RTC) > 0 ? (8 / RTC) : 1;   // k-tiles in flight per step
-    extern __shared__ __align__(16) unsigned char smem[];
+    return __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | sel)) - 8388736.0f;
+}
+
+// bytes (0,1) or (2,3) of wx (stored weight bytes, q + 128) to an f16x2 pair of exact
+// integers: each byte becomes the low mantissa of 1024 (f16 0x64xx) and 1024 + 128 is
+// subtracted.
+__device__ __forceinline__ uint32_t s8x2_to_h2(uint32_t wx, uint32_t sel)
+{
+    const uint32_t v = __byte_perm(wx, 0x64646464u, sel);
+    __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&v), __halves2half2(__ushort_as_half(0x6480),
+                                                                               __ushort_as_half(0x6480)));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void mma16816(float &c0, float &c1, float &c2, float &c3, uint32_t a0, uint32_t a1,
+                                         uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// power-of-two scale bringing a block maximum m into [2^13, 2^14), and its inverse
+__device__ __forceinline__ void block_scale(float m, float &s, float &sinv)
+{
+    const uint32_t bits = __float_as_uint(m);
+    int e = (int)((bits >> 23) & 0xFF) - 126;          // m = f * 2^e, f in [0.5, 1)
+    if (m == 0.f || !(m < INFINITY)) e = 14;           // zero, inf, nan: no scaling
+    int es = 14 - e, ei = e - 14;
+    es = max(-126, min(127, es));
+    ei = max(-126, min(127, ei));
+    s = __uint_as_float((uint32_t)(es + 127) << 23);
+    sinv = __uint_as_float((uint32_t)(ei + 127) << 23);
+}
+
+// Offsets (in floats) of the 8 inputs a lane of quad position c holds inside a 32-input block.
+__device__ __forceinline__ int lane_k(int c, int j)
+{
+    return 2 * c + (j & 1) + ((j >> 1) & 1) * 8 + (j >> 2) * 16;
+}
+
+// ---- asynchronous bulk copies into shared memory, tracked by mbarriers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait: false if the phase never completed (the caller then stops using the stage).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    for (int spin = 0; spin < (1 << 22); ++spin)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+constexpr int kConsumers = 8;                        // consumer warps, one row tile each
+constexpr int kThreads5 = (kConsumers + 1) * 32;     // and one producer warp
+constexpr int kStages = 3;                           // ring depth, in groups of 4 k-tiles
+constexpr int kStageBytes = kConsumers * 4 * 512;    // one group of the CTA's 8 row tiles
+
+// Shared-memory bytes of a launch: weight ring, activation fragments, cluster partials.
+size_t gemv_smem(bool mma, int nrc, int ksl)
+{
+    const size_t fb = mma ? 32 : (size_t)nrc * 32;
+    return (size_t)kStages * kStageBytes + (size_t)ksl * 32 * fb + (size_t)kConsumers * 128 * 4;
+}
+
+template <bool MMA, int NRC>
+__global__ void __launch_bounds__(kThreads5, 2) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
+{
+    constexpr int FB = MMA ? 32 : NRC * 32;          // fragment bytes per lane and k-tile
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+    __shared__ int s_rowmax[8];
+    __shared__ int s_fail;
+
+    unsigned char *ring = smem;
+    unsigned char *xf = smem + kStages * kStageBytes;
+    float *cpart = reinterpret_cast<float *>(xf + (size_t)a.ksl * 32 * FB);
 
     const int slice = blockIdx.x % a.cs;
-    const int rt0 = (blockIdx.x / a.cs) * RTC;
-    const int kt0 = slice * a.ksl;
-    const int nkt = min(a.KT, kt0 + a.ksl) - kt0;
-
-    float *xs = reinterpret_cast<float *>(smem);           // [ksl][NR][4 quads][8]
-    float *red = xs + (size_t)a.ksl * NR * 32;             // [8 warps][RTC*16*NR]
-    float *cpart = red + kWarps * RTC * 16 * NR;           // [RTC*16*NR]
-
-    // ---- stage this slice's activations in lane order
-    {
-        const int k4n = nkt * 8;                           // float4 per row
-        for (int idx = threadIdx.x; idx < NR * k4n; idx += kThreads) {
-            const int r = idx / k4n;
-            const int k4 = idx - r * k4n;
-            const int k = (kt0 * 32) + k4 * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (k < a.n_in) v = *reinterpret_cast<const float4 *>(a.x + r * a.x_stride + k);
-            const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int kk = k4 * 4 + q;            // slice-local input
-                const int ktl = kk >> 5, m32 = kk & 31;
-                const int h = m32 >> 4, m = m32 & 15;
-                const int c = (m & 7) >> 1;
-                const int j = h * 4 + ((m >> 3) << 1) + (m & 1);
-                xs[((ktl * NR + r) * 4 + c) * 8 + j] = e[q];
-            }
-        }
-    }
-    __syncthreads();
-
+    const int rt0 = (blockIdx.x / a.cs) * kConsumers;
+    const int kt0 = slice * a.ksl, kt1 = min(a.KT, kt0 + a.ksl);
+    const int nkt = kt1 - kt0, ng = nkt >> 2, gb = kt0 >> 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int per = nkt / kWarps, rem = nkt % kWarps;
-    const int wk0 = warp * per + min(warp, rem);
-    const int wk1 = wk0 + per + (warp < rem ? 1 : 0);
-
-    float acc[RTC][2][NR];
-#pragma unroll
-    for (int i = 0; i < RTC; ++i)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) acc[i][h][r] = 0.f;
-
+    const int nrt = min(kConsumers, a.RT - rt0);
     const int KG = a.KT >> 2;
-    for (int kt = wk0; kt < wk1; kt += U) {
-        uint4 wv[U][RTC];
-        uint32_t sp[U][RTC];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int i = 0; i < RTC; ++i) {
-                const int rt = rt0 + i;
-                const int ktg = kt0 + kt + u;
-                if (kt + u < wk1 && rt < a.RT) {
-                    wv[u][i] = ld_stream(a.qs + ((size_t)rt * a.KT + ktg) * 32 + lane);
-                    sp[u][i] = __ldg(a.d + (((size_t)rt * KG + (ktg >> 2)) * 8 + g) * 4 + (ktg & 3));
-                } else {
-                    wv[u][i] = make_uint4(0u, 0u, 0u, 0u);
-                    sp[u][i] = 0u;
-                }
-            }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (kt + u >= wk1) break;
-            const float *xk = xs + ((size_t)(kt + u) * NR * 4 + c) * 8;
-#pragma unroll
-            for (int i = 0; i < RTC; ++i) {
-                const uint32_t w0 = wv[u][i].x ^ 0x80808080u, w1 = wv[u][i].y ^ 0x80808080u;
-                const uint32_t w2 = wv[u][i].z ^ 0x80808080u, w3 = wv[u][i].w ^ 0x80808080u;
-                // row g: bytes 0,1 of each word; row g+8: bytes 2,3
-                float wg[8], wh[8];
-                wg[0] = s8_to_f32(w0, 0); wg[1] = s8_to_f32(w0, 1);
-                wg[2] = s8_to_f32(w1, 0); wg[3] = s8_to_f32(w1, 1);
-                wg[4] = s8_to_f32(w2, 0); wg[5] = s8_to_f32(w2, 1);
-                wg[6] = s8_to_f32(w3, 0); wg[7] = s8_to_f32(w3, 1);
-                wh[0] = s8_to_f32(w0, 2); wh[1] = s8_to_f32(w0, 3);
-                wh[2] = s8_to_f32(w1, 2); wh[3] = s8_to_f32(w1, 3);
-                wh[4] = s8_to_f32(w2, 2); wh[5] = s8_to_f32(w2, 3);
-                wh[6] = s8_to_f32(w3, 2); wh[7] = s8_to_f32(w3, 3);
-                const float dg = __half2float(__ushort_as_half((unsigned short)(sp[u][i] & 0xFFFFu)));
-                const float dh = __half2float(__ushort_as_half((unsigned short)(sp[u][i] >> 16)));
-#pragma unroll
-                for (int r = 0; r < NR; ++r) {
-                    const float4 xa = *reinterpret_cast<const float4 *>(xk + r * 32);
-                    const float4 xb = *reinterpret_cast<const float4 *>(xk + r * 32 + 4);
-                    float sg = wg[0] * xa.x;
-                    sg = fmaf(wg[1], xa.y, sg); sg = fmaf(wg[2], xa.z, sg); sg = fmaf(wg[3], xa.w, sg);
-                    sg = fmaf(wg[4], xb.x, sg); sg = fmaf(wg[5], xb.y, sg);
-                    sg = fmaf(wg[6], xb.z, sg); sg = fmaf(wg[7], xb.w, sg);
-                    float sh = wh[0] * xa.x;
-                    sh = fmaf(wh[1], xa.y, sh); sh = fmaf(wh[2], xa.z, sh); sh = fmaf(wh[3], xa.w, sh);
-                    sh = fmaf(wh[4], xb.x, sh); sh = fmaf(wh[5], xb.y, sh);
-                    sh = fmaf(wh[6], xb.z, sh); sh = fmaf(wh[7], xb.w, sh);
-                    acc[i][0][r] = fmaf(dg, sg, acc[i][0][r]);
-                    acc[i][1][r] = fmaf(dh, sh, acc[i][1][r]);
-                }
-            }
-        }
-    }
+    const bool producer = warp == kConsumers;
+    const unsigned char *qs = reinterpret_cast<const unsigned char *>(a.qs);
 
-    // ---- reduce the quad (the four lanes holding one row's 32 inputs)
-#pragma unroll
-    for (int i = 0; i < RTC; ++i)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                float v = acc[i][h][r];
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                acc[i][h][r] = v;
-            }
-    if (c == 0) {
-#pragma unroll
-        for (int i = 0; i < RTC; ++i)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                red[warp * RTC * 16 * NR + (i * 16 + g) * NR + r] = acc[i][0][r];
-                red[warp * RTC * 16 * NR + (i * 16 + g + 8) * NR + r] = acc[i][1][r];
-            }
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], kConsumers);
+        }
+        for (int r = 0; r < 8; ++r) s_rowmax[r] = 0;
+        s_fail = 0;
+        mbar_init_fence();
     }
     __syncthreads();
 
-    // ---- reduce the warps (fixed order), then the cluster's K-slices
-    constexpr int E = RTC * 16 * NR;
-    for (int e = threadIdx.x; e < E; e += kThreads) {
-        float s = 0.f;
+    // group j of this slice: the CTA's row tiles at k-tiles 4(gb+j) .. 4(gb+j)+3, 2 KB each
+    auto issue = [&](int j) {
+        const int st = j % kStages;
+        mbar_expect_tx(&full[st], (uint32_t)nrt * 2048u);
+        for (int i = 0; i < nrt; ++i)
+            bulk_g2s(ring + st * kStageBytes + i * 2048, qs + ((size_t)(rt0 + i) * a.KT + 4 * (size_t)(gb + j)) * 512,
+                     2048u, &full[st]);
+    };
+    // the weights do not depend on the previous kernel: start the ring before waiting on it
+    if (producer && lane == 0)
+        for (int j = 0; j < kStages && j < ng; ++j) issue(j);
+    dl_pdl_launch_dependents();
+    dl_pdl_wait();
+
+    // ---- the slice's activations, as operand fragments in shared memory (every thread)
+    const int npairs = nkt * 32;                     // (k-tile, lane) pairs
+    if constexpr (MMA) {
+        // one power-of-two scale per activation row over the slice
+        for (int pi = threadIdx.x; pi < npairs; pi += kThreads5) {
+            const int kt = kt0 + (pi >> 5), t = pi & 31, gg = t >> 2, cc = t & 3;
+            if (gg >= a.nr || kt * 32 >= a.n_in) continue;
+            const float *xr = a.x + (int64_t)gg * a.x_stride + kt * 32;
+            float m = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += red[w * E + e];
+            for (int e = 0; e < 8; e += 2) {
+                const float2 v = __ldg(reinterpret_cast<const float2 *>(xr + lane_k(cc, e)));
+                m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
+            }
+            atomicMax(&s_rowmax[gg], __float_as_int(m));
+        }
+        __syncthreads();
+        for (int pi = threadIdx.x; pi < npairs; pi += kThreads5) {
+            const int ktl = pi >> 5, kt = kt0 + ktl, t = pi & 31, gg = t >> 2, cc = t & 3;
+            uint32_t hv[4] = {0u, 0u, 0u, 0u}, lv[4] = {0u, 0u, 0u, 0u};
+            if (gg < a.nr && kt * 32 < a.n_in) {
+                float sc, si;
+                block_scale(__int_as_float(s_rowmax[gg]), sc, si);
+                const float *xr = a.x + (int64_t)gg * a.x_stride + kt * 32;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 v = __ldg(reinterpret_cast<const float2 *>(xr + lane_k(cc, 2 * e)));
+                    const float x0 = v.x * sc, x1 = v.y * sc;
+                    const __half2 h = __floats2half2_rn(x0, x1);
+                    const float2 hf = __half22float2(h);
+                    hv[e] = *reinterpret_cast<const uint32_t *>(&h);
+                    lv[e] = pack_h2(x0 - hf.x, x1 - hf.y);
+                }
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(xf + (size_t)pi * FB);
+            dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            dst[1] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        }
+    } else {
+        for (int pi = threadIdx.x; pi < npairs; pi += kThreads5) {
+            const int kt = kt0 + (pi >> 5), t = pi & 31, cc = t & 3;
+            float4 *dst = reinterpret_cast<float4 *>(xf + (size_t)pi * FB);
+#pragma unroll
+            for (int r = 0; r < NRC; ++r) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                if (r < a.nr && kt * 32 < a.n_in) {
+                    const float *xr = a.x + (int64_t)r * a.x_stride + kt * 32;
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const float2 w = __ldg(reinterpret_cast<const float2 *>(xr + lane_k(cc, e)));
+                        v[e] = w.x;
+                        v[e + 1] = w.y;
+                    }
+                }
+                dst[2 * r] = make_float4(v[0], v[1], v[2], v[3]);
+                dst[2 * r + 1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+        }
+    }
+    __syncthreads();
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};             // tensor path: C fragment
+    float accg[NRC], acch[NRC];                      // CUDA-core path: rows g, g+8
+#pragma unroll
+    for (int r = 0; r < NRC; ++r) accg[r] = acch[r] = 0.f;
+
+    if (producer) {
+        // refill each stage once every consumer warp has released it
+        if (lane == 0) {
+            for (int j = kStages; j < ng; ++j) {
+                const int st = j % kStages;
+                if (!mbar_wait(&empty[st], (uint32_t)(((j / kStages) - 1) & 1))) {
+                    atomicExch(&s_fail, 1);
+                    break;
+                }
+                issue(j);
+            }
+        }
+    } else {
+        const int rt = rt0 + warp;
+        const bool live = warp < nrt;
+        const uint4 *dsc = reinterpret_cast<const uint4 *>(a.d);
+        uint4 scn = make_uint4(0u, 0u, 0u, 0u);
+        if (live && ng > 0) scn = __ldg(dsc + ((size_t)rt * KG + gb) * 8 + g);
+        for (int j = 0; j < ng; ++j) {
+            const int st = j % kStages;
+            const uint4 sc4 = scn;
+            if (live && j + 1 < ng) scn = __ldg(dsc + ((size_t)rt * KG + gb + j + 1) * 8 + g);
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (uint32_t)((j / kStages) & 1)))) {
+                if (lane == 0) atomicExch(&s_fail, 1);
+                break;
+            }
+            if (live) {
+                const unsigned char *sw = ring + st * kStageBytes + warp * 2048;
+                const uint32_t sp[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(sw + q * 512 + lane * 16);
+                    const float dg = __half2float(__ushort_as_half((unsigned short)(sp[q] & 0xFFFFu)));
+                    const float dh = __half2float(__ushort_as_half((unsigned short)(sp[q] >> 16)));
+                    const unsigned char *fr = xf + ((size_t)(4 * j + q) * 32 + lane) * FB;
+                    if constexpr (MMA) {
+                        const uint4 bh = *reinterpret_cast<const uint4 *>(fr);
+                        const uint4 bl = *reinterpret_cast<const uint4 *>(fr + 16);
+                        const uint32_t a0 = s8x2_to_h2(w.x, 0x5150), a1 = s8x2_to_h2(w.x, 0x5352);
+                        const uint32_t a2 = s8x2_to_h2(w.y, 0x5150), a3 = s8x2_to_h2(w.y, 0x5352);
+                        const uint32_t a4 = s8x2_to_h2(w.z, 0x5150), a5 = s8x2_to_h2(w.z, 0x5352);
+                        const uint32_t a6 = s8x2_to_h2(w.w, 0x5150), a7 = s8x2_to_h2(w.w, 0x5352);
+                        float h0 = 0.f, h1 = 0.f, h2 = 0.f, h3 = 0.f;    // hi terms
+                        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;    // lo terms (independent chain)
+                        mma16816(h0, h1, h2, h3, a0, a1, a2, a3, bh.x, bh.y);
+                        mma16816(l0, l1, l2, l3, a0, a1, a2, a3, bl.x, bl.y);
+                        mma16816(h0, h1, h2, h3, a4, a5, a6, a7, bh.z, bh.w);
+                        mma16816(l0, l1, l2, l3, a4, a5, a6, a7, bl.z, bl.w);
+                        acc[0] = fmaf(dg, h0 + l0, acc[0]);
+                        acc[1] = fmaf(dg, h1 + l1, acc[1]);
+                        acc[2] = fmaf(dh, h2 + l2, acc[2]);
+                        acc[3] = fmaf(dh, h3 + l3, acc[3]);
+                    } else {
+                        float wg[8], wh[8];
+                        wg[0] = s8_to_f32(w.x, 0); wg[1] = s8_to_f32(w.x, 1);
+                        wg[2] = s8_to_f32(w.y, 0); wg[3] = s8_to_f32(w.y, 1);
+                        wg[4] = s8_to_f32(w.z, 0); wg[5] = s8_to_f32(w.z, 1);
+                        wg[6] = s8_to_f32(w.w, 0); wg[7] = s8_to_f32(w.w, 1);
+                        wh[0] = s8_to_f32(w.x, 2); wh[1] = s8_to_f32(w.x, 3);
+                        wh[2] = s8_to_f32(w.y, 2); wh[3] = s8_to_f32(w.y, 3);
+                        wh[4] = s8_to_f32(w.z, 2); wh[5] = s8_to_f32(w.z, 3);
+                        wh[6] = s8_to_f32(w.w, 2); wh[7] = s8_to_f32(w.w, 3);
+#pragma unroll
+                        for (int r = 0; r < NRC; ++r) {
+                            const float4 xa = *reinterpret_cast<const float4 *>(fr + r * 32);
+                            const float4 xb = *reinterpret_cast<const float4 *>(fr + r * 32 + 16);
+                            float sg = wg[0] * xa.x, sh = wh[0] * xa.x;
+                            sg = fmaf(wg[1], xa.y, sg); sh = fmaf(wh[1], xa.y, sh);
+                            sg = fmaf(wg[2], xa.z, sg); sh = fmaf(wh[2], xa.z, sh);
+                            sg = fmaf(wg[3], xa.w, sg); sh = fmaf(wh[3], xa.w, sh);
+                            sg = fmaf(wg[4], xb.x, sg); sh = fmaf(wh[4], xb.x, sh);
+                            sg = fmaf(wg[5], xb.y, sg); sh = fmaf(wh[5], xb.y, sh);
+                            sg = fmaf(wg[6], xb.z, sg); sh = fmaf(wh[6], xb.z, sh);
+                            sg = fmaf(wg[7], xb.w, sg); sh = fmaf(wh[7], xb.w, sh);
+                            accg[r] = fmaf(dg, sg, accg[r]);
+                            acch[r] = fmaf(dh, sh, acch[r]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+    }
+    __syncthreads();
+    const bool failed = s_fail != 0;
+
+    // ---- results: each consumer warp holds complete sums of its row tile over the slice
+    const int rt = rt0 + warp;
+    const bool mine = !producer && warp < nrt;
+    auto emit = [&](int o, int col, float v) {         // o: output row, col: activation row
+        if (failed) v = __int_as_float(0x7fc00000);
         if (a.cs == 1) {
-            const int i = e / (16 * NR), row = (e / NR) % 16, r = e % NR;
-            const int o = (rt0 + i) * 16 + row;
-            if (o < a.n_out) a.y[r * a.y_stride + o] = s;
+            if (o < a.n_out) a.y[(int64_t)col * a.y_stride + o] = v;
         } else {
-            cpart[e] = s;
+            cpart[(warp * 16 + (o - rt * 16)) * 8 + col] = v;
+        }
+    };
+    if (mine) {
+        if constexpr (MMA) {
+            float s0, si0, s1, si1;
+            block_scale(__int_as_float(s_rowmax[2 * c]), s0, si0);
+            block_scale(__int_as_float(s_rowmax[2 * c + 1]), s1, si1);
+            if (2 * c < a.nr) {
+                emit(rt * 16 + g, 2 * c, acc[0] * si0);
+                emit(rt * 16 + g + 8, 2 * c, acc[2] * si0);
+            }
+            if (2 * c + 1 < a.nr) {
+                emit(rt * 16 + g, 2 * c + 1, acc[1] * si1);
+                emit(rt * 16 + g + 8, 2 * c + 1, acc[3] * si1);
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < NRC; ++r) {
+                float vg = accg[r], vh = acch[r];
+                vg += __shfl_xor_sync(0xffffffffu, vg, 1);
+                vg += __shfl_xor_sync(0xffffffffu, vg, 2);
+                vh += __shfl_xor_sync(0xffffffffu, vh, 1);
+                vh += __shfl_xor_sync(0xffffffffu, vh, 2);
+                if (c == 0 && r < a.nr) {
+                    emit(rt * 16 + g, r, vg);
+                    emit(rt * 16 + g + 8, r, vh);
+                }
+            }
         }
     }
     if (a.cs > 1) {
+        // every K-slice of this run of row tiles holds its partials in shared memory: sum in rank order
         cluster_sync_all();
-        for (int e = threadIdx.x; e < E; e += kThreads) {
-            if (e % a.cs != slice) continue;
-            float s = 0.f;
-            for (int q = 0; q < a.cs; ++q) s += ld_dsmem_f32(cpart + e, (uint32_t)q);
-            const int i = e / (16 * NR), row = (e / NR) % 16, r = e % NR;
-            const int o = (rt0 + i) * 16 + row;
-            if (o < a.n_out) a.y[r * a.y_stride + o] = s;
+        for (int e = threadIdx.x; e < nrt * 128; e += kThreads5) {
+            if ((e >> 3) % a.cs != slice) continue;      // each rank finishes a share of the rows
+            const int col = e & 7;
+            if (col >= a.nr) continue;
+            float sum = 0.f;
+            for (int q = 0; q < a.cs; ++q) sum += ld_dsmem_f32(cpart + e, (uint32_t)q);
+            const int o = rt0 * 16 + (e >> 3);
+            if (o < a.n_out) a.y[(int64_t)col * a.y_stride + o] = sum;
         }
         cluster_sync_all();   // keep this CTA's shared memory alive until every peer has read it
     }
@@ -236,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_cc_kernel(GemvArgs a)
 __device__ __forceinline__ uint32_t q8_byte(const uint8_t *blocks, int64_t n_out, int64_t n_in,
                                             int64_t o, int64_t k)
 {
-    if (o >= n_out || k >= n_in) return 0u;
-    return blocks[(o * (n_in / 32) + k / 32) * 34 + 2 + (k % 32)];
+    if (o >= n_out || k >= n_in) return 0x80u;       // a zero weight, stored biased
+    return blocks[(o * (n_in / 32) + k / 32) * 34 + 2 + (k % 32)] ^ 0x80u;   // q + 128
 }
 
 __global__ void q8_pack_qs_kernel(const uint8_t *blocks, int64_t n_out, int64_t n_in, int KT,
@@ -290,95 +488,196 @@ __global__ void q8_pack_d_kernel(const uint8_t *blocks, int64_t n_out, int64_t n
     d[u] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+
 // ---------------------------------------------------------------- launch
 
 struct GemvCfg {
-    int rtc, cs, ksl;
+    bool mma;
+    int nrc, cs, ksl, grid;
     size_t smem;
-    int grid;
 };
 
-size_t gemv_smem(int NR, int rtc, int ksl)
+void *pick_kernel(bool mma, int nrc)
 {
-    return (size_t)ksl * NR * 32 * 4 + (size_t)kWarps * rtc * 16 * NR * 4 + (size_t)rtc * 16 * NR * 4;
+    if (mma) return reinterpret_cast<void *>(gemv_q8_kernel<true, 1>);
+    if (nrc == 1) return reinterpret_cast<void *>(gemv_q8_kernel<false, 1>);
+    return reinterpret_cast<void *>(gemv_q8_kernel<false, 2>);
 }
 
-GemvCfg gemv_choose(int NR, int RT, int KT, int sm)
+// The dynamic shared-memory limit is a per-function attribute shared by every launch of the
+// kernel (graph nodes and profilers re-launch against it): set it once to the largest size any
+// launch shape may use, never to one launch's own size.
+constexpr int kSmemLimit = 200 * 1024;
+
+int prepare_kernel(const void *kern, size_t smem, int cs)
 {
-    GemvCfg best{0, 0, 0, 0, 0};
-    const int rtcs[4] = {8, 4, 2, 1};
-    for (int ri = 0; ri < 4; ++ri) {
-        const int rtc = rtcs[ri];
-        if (rtc * NR > 16) continue;
-        for (int cs = 1; cs <= 8; ++cs) {
-            const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
-            if ((int)dl::ceil_div(KT, ksl) != cs) continue;          // every slice holds k-tiles
-            if ((size_t)NR * ksl * 128 > kXsBudget) continue;
-            const int grid = (int)dl::ceil_div(RT, rtc) * cs;
-            GemvCfg cfg{rtc, cs, ksl, gemv_smem(NR, rtc, ksl), grid};
-            if (grid >= 2 * sm) return cfg;                          // enough CTAs: keep reuse
-            if (grid > best.grid) best = cfg;
+    if (smem > (size_t)kSmemLimit) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: %zu bytes of shared memory", smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8: set shared memory");
+    if (cs > 8) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8: allow a large cluster");
+    }
+    return DL_OK;
+}
+
+// CTAs of one launch shape that are resident at once (clusters counted whole).
+int resident_ctas(const void *kern, int cs, size_t smem, int sm)
+{
+    if (cs <= 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads5, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return per_sm * sm;
+    }
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)cs);
+    lc.blockDim = dim3(kThreads5);
+    lc.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters * cs;
+}
+
+// Launch shape: K split into cs slices of whole groups of 4 k-tiles, 8 row tiles per CTA;
+// the smallest slice whose grid is resident in one wave, then the fewest slices.
+int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
+{
+    const bool mma = path == PATH_TENSOR || (path == PATH_AUTO && nr > 2);
+    if (!mma && nr > 2) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: the CUDA-core path serves 1 or 2 rows per command");
+    const int nrc = mma ? 1 : nr;
+    const void *kern = pick_kernel(mma, nrc);
+    const int mgroups = (int)dl::ceil_div(RT, kConsumers);
+    GemvCfg best{};
+    int best_ksl = -1;
+    for (int cs = 1; cs <= 16; ++cs) {
+        const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
+        if ((int)dl::ceil_div(KT, ksl) != cs) continue;
+        const size_t smem = gemv_smem(mma, nrc, ksl);
+        if (smem > (size_t)kSmemLimit) continue;
+        if (prepare_kernel(kern, smem, cs) != DL_OK) return DL_E_CUDA;
+        const int grid = mgroups * cs;
+        if (grid > resident_ctas(kern, cs, smem, sm)) continue;
+        if (best_ksl < 0 || ksl < best_ksl) {
+            best_ksl = ksl;
+            best = GemvCfg{mma, nrc, cs, ksl, grid, smem};
         }
     }
-    return best;
+    if (best_ksl < 0) {
+        // more row tiles than one wave holds: whole-K CTAs in several waves, or the
+        // smallest slices that fit shared memory
+        for (int cs = 1; cs <= 16 && best_ksl < 0; ++cs) {
+            const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
+            if ((int)dl::ceil_div(KT, ksl) != cs) continue;
+            const size_t smem = gemv_smem(mma, nrc, ksl);
+            if (smem > (size_t)kSmemLimit) continue;
+            if (prepare_kernel(kern, smem, cs) != DL_OK) return DL_E_CUDA;
+            best_ksl = ksl;
+            best = GemvCfg{mma, nrc, cs, ksl, mgroups * cs, smem};
+        }
+        if (best_ksl < 0) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no launch shape for %d k-tiles", KT);
+    }
+    *out = best;
+    return DL_OK;
 }
 
-template <int NR, int RTC>
-int launch_cc(const GemvArgs &a, const GemvCfg &cfg, cudaStream_t st)
+int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
 {
-    auto kern = gemv_q8_cc_kernel<NR, RTC>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
-    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8: set shared memory");
+    GemvCfg cfg;
+    int rc = choose_cfg(nr, a.RT, a.KT, sm, path, &cfg);
+    if (rc != DL_OK) return rc;
+    a.nr = nr;
+    a.cs = cfg.cs;
+    a.ksl = cfg.ksl;
+    const void *kern = pick_kernel(cfg.mma, cfg.nrc);
+    rc = prepare_kernel(kern, cfg.smem, cfg.cs);     // the shape search left another candidate's limit
+    if (rc != DL_OK) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid);
-    lc.blockDim = dim3(kThreads);
+    lc.blockDim = dim3(kThreads5);
     lc.dynamicSmemBytes = cfg.smem;
     lc.stream = st;
-    cudaLaunchAttribute attr[1];
-    lc.attrs = attr;
-    lc.numAttrs = 0;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     if (cfg.cs > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)cfg.cs;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        lc.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)cfg.cs;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
-    e = cudaLaunchKernelEx(&lc, kern, a);
+    lc.attrs = attr;
+    lc.numAttrs = na;
+    void *args[1] = {&a};
+    cudaError_t e = cudaLaunchKernelExC(&lc, kern, args);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8: launch");
     return DL_OK;
 }
 
-template <int NR>
-int launch_rows(const GemvArgs &a, const GemvCfg &cfg, cudaStream_t st)
+int gemv_impl(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride, float *y, int64_t y_stride,
+              int path, dl_stream_t stream)
 {
-    switch (cfg.rtc) {
-    case 1: return launch_cc<NR, 1>(a, cfg, st);
-    case 2: return launch_cc<NR, 2>(a, cfg, st);
-    case 4: if constexpr (NR <= 4) return launch_cc<NR, 4>(a, cfg, st); break;
-    case 8: if constexpr (NR <= 2) return launch_cc<NR, 8>(a, cfg, st); break;
-    }
-    return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no kernel for %d rows x %d row tiles", NR, cfg.rtc);
-}
+    dl::clear_error();
+    if (!W || !x || !y || !W->qs || !W->d) return dl::fail(DL_E_ARG, "dl_gemv_q8: null pointer");
+    if (rows < 0) return dl::fail(DL_E_ARG, "dl_gemv_q8: rows=%d", rows);
+    if (path < PATH_AUTO || path > PATH_TENSOR) return dl::fail(DL_E_ARG, "dl_gemv_q8: path=%d", path);
+    int rc = dl_q8_packed_size(W->n_out, W->n_in, nullptr, nullptr);
+    if (rc != DL_OK) return rc;
+    if (rows == 0) return DL_OK;
+    if (x_stride < W->n_in || y_stride < W->n_out)
+        return dl::fail(DL_E_ARG, "dl_gemv_q8: strides %lld/%lld below the row widths",
+                        (long long)x_stride, (long long)y_stride);
+    if (!dl::aligned16(x) || (x_stride % 4) != 0 || !dl::aligned16(W->qs) || !dl::aligned16(W->d))
+        return dl::fail(DL_E_ALIGN, "dl_gemv_q8: x, its stride and the weight planes must be 16-byte aligned");
+    const char *xb = reinterpret_cast<const char *>(x), *yb = reinterpret_cast<const char *>(y);
+    const char *xe = xb + ((size_t)(rows - 1) * x_stride + W->n_in) * 4;
+    const char *ye = yb + ((size_t)(rows - 1) * y_stride + W->n_out) * 4;
+    if (xb < ye && yb < xe) return dl::fail(DL_E_ARG, "dl_gemv_q8: y overlaps x");
+    int sm = 0;
+    rc = dl::device_sm_count(&sm);
+    if (rc != DL_OK) return rc;
 
-int gemv_group(const GemvArgs &a, int nr, int sm, cudaStream_t st)
-{
-    const GemvCfg cfg = gemv_choose(nr, a.RT, a.KT, sm);
-    if (cfg.grid == 0) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no launch shape for n_in=%d", a.n_in);
-    GemvArgs b = a;
-    b.cs = cfg.cs;
-    b.ksl = cfg.ksl;
-    switch (nr) {
-    case 1: return launch_rows<1>(b, cfg, st);
-    case 2: return launch_rows<2>(b, cfg, st);
-    case 3: return launch_rows<3>(b, cfg, st);
-    case 4: return launch_rows<4>(b, cfg, st);
-    case 5: return launch_rows<5>(b, cfg, st);
-    case 6: return launch_rows<6>(b, cfg, st);
-    case 7: return launch_rows<7>(b, cfg, st);
-    case 8: return launch_rows<8>(b, cfg, st);
+    GemvArgs a{};
+    a.qs = static_cast<const uint4 *>(W->qs);
+    a.d = static_cast<const uint32_t *>(W->d);
+    a.x_stride = x_stride;
+    a.y_stride = y_stride;
+    a.n_out = (int)W->n_out;
+    a.n_in = (int)W->n_in;
+    a.KT = (int)(dl::ceil_div(W->n_in, 128) * 4);
+    a.RT = (int)dl::ceil_div(W->n_out, 16);
+
+    int sizes[64];
+    int done = 0;
+    while (done < rows) {
+        // commands of at most eight rows, in the fewest balanced groups
+        const int chunk = rows - done > 8 * 64 ? 8 * 64 : rows - done;
+        const int ng = dl_plan_groups(chunk, DL_MAX_ROWS, sizes);
+        if (ng < 0) return ng;
+        for (int gi = 0; gi < ng; ++gi) {
+            a.x = x + (size_t)done * x_stride;
+            a.y = y + (size_t)done * y_stride;
+            rc = gemv_group(a, sizes[gi], sm, path, static_cast<cudaStream_t>(stream));
+            if (rc != DL_OK) return rc;
+            done += sizes[gi];
+        }
     }
-    return dl::fail(DL_E_SHAPE, "dl_gemv_q8: bad group size %d", nr);
+    return DL_OK;
 }
 
 }  // namespace
@@ -421,51 +720,13 @@ int dl_q8_pack(const uint8_t *blocks, int64_t n_out, int64_t n_in, void *qs, voi
 int dl_gemv_q8(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
                float *y, int64_t y_stride, dl_stream_t stream)
 {
-    dl::clear_error();
-    if (!W || !x || !y || !W->qs || !W->d) return dl::fail(DL_E_ARG, "dl_gemv_q8: null pointer");
-    if (rows < 0) return dl::fail(DL_E_ARG, "dl_gemv_q8: rows=%d", rows);
-    int rc = dl_q8_packed_size(W->n_out, W->n_in, nullptr, nullptr);
-    if (rc != DL_OK) return rc;
-    if (rows == 0) return DL_OK;
-    if (x_stride < W->n_in || y_stride < W->n_out)
-        return dl::fail(DL_E_ARG, "dl_gemv_q8: strides %lld/%lld below the row widths",
-                        (long long)x_stride, (long long)y_stride);
-    if (!dl::aligned16(x) || (x_stride % 4) != 0 || !dl::aligned16(W->qs) || !dl::aligned16(W->d))
-        return dl::fail(DL_E_ALIGN, "dl_gemv_q8: x, its stride and the weight planes must be 16-byte aligned");
-    const char *xb = reinterpret_cast<const char *>(x), *yb = reinterpret_cast<const char *>(y);
-    const char *xe = xb + ((size_t)(rows - 1) * x_stride + W->n_in) * 4;
-    const char *ye = yb + ((size_t)(rows - 1) * y_stride + W->n_out) * 4;
-    if (xb < ye && yb < xe) return dl::fail(DL_E_ARG, "dl_gemv_q8: y overlaps x");
-    int sm = 0;
-    rc = dl::device_sm_count(&sm);
-    if (rc != DL_OK) return rc;
+    return gemv_impl(W, x, rows, x_stride, y, y_stride, PATH_AUTO, stream);
+}
 
-    GemvArgs a{};
-    a.qs = static_cast<const uint4 *>(W->qs);
-    a.d = static_cast<const uint32_t *>(W->d);
-    a.x_stride = x_stride;
-    a.y_stride = y_stride;
-    a.n_out = (int)W->n_out;
-    a.n_in = (int)W->n_in;
-    a.KT = (int)(dl::ceil_div(W->n_in, 128) * 4);
-    a.RT = (int)dl::ceil_div(W->n_out, 16);
-
-    int sizes[64];
-    int done = 0;
-    while (done < rows) {
-        // commands of at most eight rows, in the fewest balanced groups
-        const int chunk = rows - done > 8 * 64 ? 8 * 64 : rows - done;
-        const int ng = dl_plan_groups(chunk, DL_MAX_ROWS, sizes);
-        if (ng < 0) return ng;
-        for (int gi = 0; gi < ng; ++gi) {
-            a.x = x + (size_t)done * x_stride;
-            a.y = y + (size_t)done * y_stride;
-            rc = gemv_group(a, sizes[gi], sm, static_cast<cudaStream_t>(stream));
-            if (rc != DL_OK) return rc;
-            done += sizes[gi];
-        }
-    }
-    return DL_OK;
+int dl_gemv_q8_ex(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
+                  float *y, int64_t y_stride, int path, dl_stream_t stream)
+{
+    return gemv_impl(W, x, rows, x_stride, y, y_stride, path, stream);
 }
 
 }  // extern "C"

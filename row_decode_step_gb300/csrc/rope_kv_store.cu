@@ -34,6 +34,8 @@ __device__ __forceinline__ unsigned short to_half_clamped(float v)
 
 __global__ void __launch_bounds__(256) rope_kv_store_kernel(RopeArgs a)
 {
+    dl_pdl_launch_dependents();
+    dl_pdl_wait();
     const int r = blockIdx.y;
     const int half = a.D >> 1;
     const int pairs_total = (a.n_q + a.n_kv) * half;
@@ -175,8 +177,8 @@ int dl_rope_kv_store(float *q, int64_t q_stride, const float *k, int64_t k_strid
     a.max_pos = rope->max_pos; a.capacity = kv->capacity; a.n_regions = kv->n_regions;
     const int pairs = (n_q + kv->n_kv) * (D / 2);
     dim3 grid((unsigned)dl::ceil_div(pairs, 256), (unsigned)rows);
-    rope_kv_store_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return dl::check_launch("dl_rope_kv_store");
+    return dl::launch_pdl(rope_kv_store_kernel, grid, dim3(256), 0, static_cast<cudaStream_t>(stream),
+                          "dl_rope_kv_store: launch", a);
 }
 
 }  // extern "C"

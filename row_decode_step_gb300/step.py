@@ -39,9 +39,10 @@ class Command:
 
     def __init__(self, rows: Sequence[int], positions: Sequence[int], regions: Sequence[int],
                  n_q: int, n_kv: int, head_dim: int, hidden: int, ffn: int, device, sm_count: int = 0,
-                 force_chunk: int = 0):
+                 force_chunk: int = 0, gemv_path: int = 0, attn_path: int = 0):
         n = len(rows)
         assert 1 <= n <= 8
+        self.gemv_path, self.attn_path = gemv_path, attn_path
         self.rows = list(rows)
         self.n = n
         D = head_dim
@@ -74,15 +75,17 @@ class Command:
         self.v = self.qkv[:, qd + kd:]
 
     def run(self, W: LayerWeights, rope: Rope, kv: KVCache, stream=None):
-        dl_gemv_q8(W.wqkv, self.x, self.qkv, stream=stream)
+        gp = self.gemv_path if (self.gemv_path != 1 or self.n <= 2) else 0
+        dl_gemv_q8(W.wqkv, self.x, self.qkv, stream=stream, path=gp)
         dl_rope_kv_store(self.q, self.k, self.v, self.pos, rope, kv, self.n_q, row_region=self.region,
                          status=self.status, stream=stream)
-        dl_decode_attn(self.q, kv, self.seqlen, self.plan, self.workspace, status=self.status, stream=stream)
+        dl_decode_attn(self.q, kv, self.seqlen, self.plan, self.workspace, status=self.status, stream=stream,
+                       path=self.attn_path)
         dl_attn_merge(self.workspace, self.plan, self.seqlen, self.attn, self.lse, stream=stream)
-        dl_gemv_q8(W.wo, self.attn, self.y_o, stream=stream)
+        dl_gemv_q8(W.wo, self.attn, self.y_o, stream=stream, path=gp)
         if W.wgu is not None:
-            dl_gemv_q8(W.wgu, self.x_ffn, self.gu, stream=stream)
-            dl_gemv_q8(W.wdown, self.h, self.y_down, stream=stream)
+            dl_gemv_q8(W.wgu, self.x_ffn, self.gu, stream=stream, path=gp)
+            dl_gemv_q8(W.wdown, self.h, self.y_down, stream=stream, path=gp)
 
     @property
     def launches(self) -> int:
@@ -93,7 +96,8 @@ class LayerStep:
     """All commands of one layer step: rows grouped into commands of at most eight."""
 
     def __init__(self, positions: Sequence[int], regions: Sequence[int], n_q: int, n_kv: int, head_dim: int,
-                 hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0):
+                 hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0, gemv_path: int = 0,
+                 attn_path: int = 0):
         n = len(positions)
         sizes = dl_plan_groups(n)
         self.commands: List[Command] = []
@@ -101,7 +105,8 @@ class LayerStep:
         for s in sizes:
             idx = list(range(r0, r0 + s))
             self.commands.append(Command(idx, [positions[i] for i in idx], [regions[i] for i in idx],
-                                         n_q, n_kv, head_dim, hidden, ffn, device, sm_count, force_chunk))
+                                         n_q, n_kv, head_dim, hidden, ffn, device, sm_count, force_chunk,
+                                         gemv_path, attn_path))
             r0 += s
         self.group_sizes = sizes
 

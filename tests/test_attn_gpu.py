@@ -19,7 +19,7 @@ def dl():
     return m
 
 
-def _run(dl, q, k, v, seqlen, regions, n_q, n_kv, D, force_chunk=0, poison=True):
+def _run(dl, q, k, v, seqlen, regions, n_q, n_kv, D, force_chunk=0, poison=True, path=0):
     plan = dl.dl_attn_plan_build(seqlen, n_q, n_kv, D, regions=regions, force_chunk=force_chunk)
     kv = dl.KVCache(k.cuda(), v.cuda())
     ws = dl.workspace_for(plan)
@@ -27,7 +27,7 @@ def _run(dl, q, k, v, seqlen, regions, n_q, n_kv, D, force_chunk=0, poison=True)
         ws.view(torch.float32)[:ws.numel() // 4].fill_(float("nan"))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     sl = torch.tensor(seqlen, dtype=torch.int32, device="cuda")
-    out, lse = dl.decode_attention(q.cuda(), kv, sl, plan, ws, status=status)
+    out, lse = dl.decode_attention(q.cuda(), kv, sl, plan, ws, status=status, path=path)
     torch.cuda.synchronize()
     assert dl.dl_status_read(status) == 0
     return out.cpu().numpy(), lse.cpu().numpy(), plan
@@ -53,12 +53,14 @@ CONFIGS = {
 }
 
 
+@pytest.mark.parametrize("path", [0, 1, 2])
 @pytest.mark.parametrize("name", list(CONFIGS))
-def test_attention_configs(dl, name):
+def test_attention_configs(dl, name, path):
+    """Both inner products (CUDA cores, tensor cores) and the automatic choice."""
     n_q, n_kv, D, n_reg, cap, seqlen, regions = CONFIGS[name]
     k, v = kv_planes("attn/" + name, n_reg, n_kv, cap, D)
     q = synth.normal_f32(0, "attn/%s/q" % name, (len(seqlen), n_q * D))
-    out, lse, plan = _run(dl, q, k, v, seqlen, regions, n_q, n_kv, D)
+    out, lse, plan = _run(dl, q, k, v, seqlen, regions, n_q, n_kv, D, path=path)
     ro, rl = _ref(q, k, v, seqlen, regions, n_q, n_kv, D, plan)
     assert_attn_close(out, lse, ro, rl)
 
@@ -90,13 +92,14 @@ def test_attention_long_context_split_invariance(dl):
     ro, rl = oracle.attn_full(q.numpy().astype(np.float64), k.numpy().view(np.uint16), v.numpy().view(np.uint16),
                               np.array(seqlen, np.int32), n_q=n_q, n_kv=n_kv, head_dim=D)
     assert_attn_close(out_auto, lse_auto, ro, rl)
-    for chunk in (32768, 2 * plan.chunk, 4096, 96):
-        out, lse, p2 = _run(dl, q, k, v, seqlen, None, n_q, n_kv, D, force_chunk=chunk)
+    for chunk, path in ((32768, 0), (2 * plan.chunk, 0), (4096, 1), (96, 2), (plan.chunk, 1)):
+        out, lse, p2 = _run(dl, q, k, v, seqlen, None, n_q, n_kv, D, force_chunk=chunk, path=path)
         assert_attn_close(out, lse, ro, rl)
         assert np.max(np.abs(out - out_auto)) <= 2e-3
 
 
-def test_attention_peaked_query_teeth(dl):
+@pytest.mark.parametrize("path", [1, 2])
+def test_attention_peaked_query_teeth(dl, path):
     """A query aimed at one key returns that key's value; the control fails on a wrong value row."""
     n_q, n_kv, D, cap = 2, 1, 128, 700
     k, v = kv_planes("attn/peak", 1, n_kv, cap, D)
@@ -106,7 +109,7 @@ def test_attention_peaked_query_teeth(dl):
     q[0, :D] = 30.0 * K[0, 0, j] / np.linalg.norm(K[0, 0, j]) * np.sqrt(D)
     q[0, D:] = synth.normal_f32(0, "attn/peak/q2", (D,)).numpy()
     q = torch.from_numpy(q)
-    out, lse, plan = _run(dl, q, k, v, [cap], None, n_q, n_kv, D)
+    out, lse, plan = _run(dl, q, k, v, [cap], None, n_q, n_kv, D, path=path)
     ro, rl = _ref(q, k, v, [cap], None, n_q, n_kv, D, plan)
     assert_attn_close(out, lse, ro, rl)
     V = v.numpy().astype(np.float64)

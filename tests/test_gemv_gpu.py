@@ -19,9 +19,9 @@ def dl():
     return m
 
 
-def _run(dl, blocks, n_out, n_in, x):
+def _run(dl, blocks, n_out, n_in, x, path=0):
     W = dl.dl_q8_pack(blocks.cuda(), n_out, n_in)
-    y = dl.dl_gemv_q8(W, x.cuda())
+    y = dl.dl_gemv_q8(W, x.cuda(), path=path)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
@@ -48,6 +48,34 @@ def test_gemv_full_layer(dl, shape, rows):
         y = _run(dl, blocks, n_out, n_in, x)
         ref = oracle.gemv_q8(blocks, x)
         assert_gemv_close(y, ref)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("rows", [1, 2])
+def test_gemv_both_inner_products(dl, path, rows):
+    """The CUDA-core and tensor-core inner products each meet the bar on the 3B QKV shape."""
+    blocks = layer_blocks("llama-3.2-3b")["wqkv"]
+    n_out, n_in = blocks.shape[0], blocks.shape[1] * 32
+    x = synth.normal_f32(0, "paths/x/%d" % rows, (rows, n_in))
+    assert_gemv_close(_run(dl, blocks, n_out, n_in, x, path=path), oracle.gemv_q8(blocks, x))
+
+
+def test_gemv_tensor_path_wide_range(dl):
+    """Activation blocks spanning 1e-6 .. 1e6 (past the f16 range) keep the bar on the tensor path."""
+    n_out, n_in, rows = 64, 512, 3
+    blocks = synth.q8_0_blocks_from_normal(6, "gemv/range", n_out, n_in)
+    x = synth.normal_f32(6, "gemv/range/x", (rows, n_in))
+    scale = torch.logspace(-6, 6, n_in // 32).repeat_interleave(32)
+    x = x * scale
+    assert_gemv_close(_run(dl, blocks, n_out, n_in, x, path=2), oracle.gemv_q8(blocks, x))
+
+
+def test_gemv_cuda_core_path_refuses_wide_commands(dl):
+    blocks = synth.q8_0_blocks_from_normal(7, "gemv/wide", 32, 64)
+    W = dl.dl_q8_pack(blocks.cuda(), 32, 64)
+    with pytest.raises(dl.DLError) as e:
+        dl.dl_gemv_q8(W, torch.zeros(3, 64, device="cuda"), path=1)
+    assert e.value.code == dl.DL_E_SHAPE
 
 
 def test_gemv_rows_match_single_rows(dl):

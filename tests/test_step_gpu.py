@@ -73,9 +73,18 @@ def _step(dl, S, positions, regions, n_regions, capacity, label):
             assert_gemv_close(c.y_down.cpu().numpy(), ref["y_down"])
         assert dl.dl_status_read(c.status) == 0
         r0 += c.n
+    # the stored K/V rows carry the QKV GEMV's rounding: the unwritten slots must be identical,
+    # the written ones within one f16 ulp plus the GEMV bar of their row
     kg, vg = as_u16(kv.k), as_u16(kv.v)
-    assert int(f16_ulp_dist(kg, kc_o).max()) <= 1
-    assert int(f16_ulp_dist(vg, vc_o).max()) <= 1
+    k0, v0 = as_u16(k), as_u16(v)
+    for got, ref, init in ((kg, kc_o, k0), (vg, vc_o, v0)):
+        written = ref != init
+        assert np.array_equal(got[~written], ref[~written])
+        gf = got.view(np.float16).astype(np.float64)
+        rf = ref.view(np.float16).astype(np.float64)
+        rms = np.sqrt(np.mean(rf[written] ** 2))
+        ulp = np.abs(np.spacing(rf.astype(np.float16)).astype(np.float64))
+        assert np.all(np.abs(gf - rf)[written] <= ulp[written] + 1e-3 * rms)
     return step
 
 
