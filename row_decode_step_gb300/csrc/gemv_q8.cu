@@ -216,71 +216,82 @@ __global__ void __launch_bounds__(kThreads5, 2) gemv_q8_kernel(const __grid_cons
     // the weights do not depend on the previous kernel: start the ring before waiting on it
     if (producer && lane == 0)
         for (int j = 0; j < kStages && j < ng; ++j) issue(j);
+    if (producer && lane < nrt && ng > kStages)
+        dl_prefetch_l2(qs + ((size_t)(rt0 + lane) * a.KT + 4 * (size_t)(gb + kStages)) * 512,
+                       (uint32_t)(ng - kStages) * 2048u);
     dl_pdl_launch_dependents();
     dl_pdl_wait();
 
-    // ---- the slice's activations, as operand fragments in shared memory (every thread)
+    // ---- the slice's activations, as operand fragments in shared memory (every thread).
+    // One pass over global memory: each (k-tile, lane) slot first receives the lane's raw f32
+    // inputs (the CUDA-core operand); the tensor path then rewrites it in place as f16 hi/lo
+    // terms scaled by one power of two per activation row.
     const int npairs = nkt * 32;                     // (k-tile, lane) pairs
-    if constexpr (MMA) {
-        // one power-of-two scale per activation row over the slice
-        for (int pi = threadIdx.x; pi < npairs; pi += kThreads5) {
-            const int kt = kt0 + (pi >> 5), t = pi & 31, gg = t >> 2, cc = t & 3;
-            if (gg >= a.nr || kt * 32 >= a.n_in) continue;
-            const float *xr = a.x + (int64_t)gg * a.x_stride + kt * 32;
-            float m = 0.f;
+    {
+        constexpr int PB = 4;                        // slots per thread per batch, loads issued together
+        for (int base = threadIdx.x; base < npairs; base += PB * kThreads5) {
+            float v[PB][NRC][8];
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const float2 v = __ldg(reinterpret_cast<const float2 *>(xr + lane_k(cc, e)));
-                m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
-            }
-            atomicMax(&s_rowmax[gg], __float_as_int(m));
-        }
-        __syncthreads();
-        for (int pi = threadIdx.x; pi < npairs; pi += kThreads5) {
-            const int ktl = pi >> 5, kt = kt0 + ktl, t = pi & 31, gg = t >> 2, cc = t & 3;
-            uint32_t hv[4] = {0u, 0u, 0u, 0u}, lv[4] = {0u, 0u, 0u, 0u};
-            if (gg < a.nr && kt * 32 < a.n_in) {
-                float sc, si;
-                block_scale(__int_as_float(s_rowmax[gg]), sc, si);
-                const float *xr = a.x + (int64_t)gg * a.x_stride + kt * 32;
+            for (int u = 0; u < PB; ++u) {
+                const int pi = base + u * kThreads5;
+                const int kt = kt0 + (pi >> 5), t = pi & 31, cc = t & 3;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 v = __ldg(reinterpret_cast<const float2 *>(xr + lane_k(cc, 2 * e)));
-                    const float x0 = v.x * sc, x1 = v.y * sc;
-                    const __half2 h = __floats2half2_rn(x0, x1);
-                    const float2 hf = __half22float2(h);
-                    hv[e] = *reinterpret_cast<const uint32_t *>(&h);
-                    lv[e] = pack_h2(x0 - hf.x, x1 - hf.y);
-                }
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(xf + (size_t)pi * FB);
-            dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            dst[1] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-        }
-    } else {
-        for (int pi = threadIdx.x; pi < npairs; pi += kThreads5) {
-            const int kt = kt0 + (pi >> 5), t = pi & 31, cc = t & 3;
-            float4 *dst = reinterpret_cast<float4 *>(xf + (size_t)pi * FB);
-#pragma unroll
-            for (int r = 0; r < NRC; ++r) {
-                float v[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = 0.f;
-                if (r < a.nr && kt * 32 < a.n_in) {
-                    const float *xr = a.x + (int64_t)r * a.x_stride + kt * 32;
+                for (int r = 0; r < NRC; ++r) {
+                    const int row = MMA ? (t >> 2) : r;
+                    const bool ok = pi < npairs && row < a.nr && kt * 32 < a.n_in;
 #pragma unroll
                     for (int e = 0; e < 8; e += 2) {
-                        const float2 w = __ldg(reinterpret_cast<const float2 *>(xr + lane_k(cc, e)));
-                        v[e] = w.x;
-                        v[e + 1] = w.y;
+                        float2 w = make_float2(0.f, 0.f);
+                        if (ok) w = __ldg(reinterpret_cast<const float2 *>(a.x + (int64_t)row * a.x_stride + kt * 32 + lane_k(cc, e)));
+                        v[u][r][e] = w.x;
+                        v[u][r][e + 1] = w.y;
                     }
                 }
-                dst[2 * r] = make_float4(v[0], v[1], v[2], v[3]);
-                dst[2 * r + 1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+#pragma unroll
+            for (int u = 0; u < PB; ++u) {
+                const int pi = base + u * kThreads5;
+                if (pi >= npairs) break;
+                float4 *dst = reinterpret_cast<float4 *>(xf + (size_t)pi * FB);
+#pragma unroll
+                for (int r = 0; r < NRC; ++r) {
+                    dst[2 * r] = make_float4(v[u][r][0], v[u][r][1], v[u][r][2], v[u][r][3]);
+                    dst[2 * r + 1] = make_float4(v[u][r][4], v[u][r][5], v[u][r][6], v[u][r][7]);
+                }
+                if constexpr (MMA) {
+                    const int gg = (pi & 31) >> 2;
+                    float m = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][0][e]));
+                    if (gg < a.nr && m > 0.f) atomicMax(&s_rowmax[gg], __float_as_int(m));
+                }
             }
         }
     }
     __syncthreads();
+    if constexpr (MMA) {
+        for (int pi = threadIdx.x; pi < npairs; pi += kThreads5) {
+            const int gg = (pi & 31) >> 2;
+            float sc, si;
+            block_scale(__int_as_float(s_rowmax[gg]), sc, si);
+            uint4 *slot = reinterpret_cast<uint4 *>(xf + (size_t)pi * FB);
+            const uint4 r0 = slot[0], r1 = slot[1];
+            const float x[8] = {__uint_as_float(r0.x), __uint_as_float(r0.y), __uint_as_float(r0.z), __uint_as_float(r0.w),
+                                __uint_as_float(r1.x), __uint_as_float(r1.y), __uint_as_float(r1.z), __uint_as_float(r1.w)};
+            uint32_t hv[4], lv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float x0 = x[2 * e] * sc, x1 = x[2 * e + 1] * sc;
+                const __half2 h = __floats2half2_rn(x0, x1);
+                const float2 hf = __half22float2(h);
+                hv[e] = *reinterpret_cast<const uint32_t *>(&h);
+                lv[e] = pack_h2(x0 - hf.x, x1 - hf.y);
+            }
+            slot[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            slot[1] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        }
+        __syncthreads();
+    }
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};             // tensor path: C fragment
     float accg[NRC], acch[NRC];                      // CUDA-core path: rows g, g+8
