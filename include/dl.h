@@ -294,6 +294,34 @@ int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv,
 int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t *seqlen,
                   float *out, int64_t out_stride, float *lse, dl_stream_t stream);
 
+/* ------------------------------------------------------------- no-allocation form
+ *
+ * (No counterpart on the pages: an addition for callers that cannot allocate
+ * device memory, e.g. a host that passes only one step's tensors and owns all
+ * other device memory through its own pool, or an engine whose device budget is
+ * fixed once serving starts.)
+ *
+ * dl_decode_attn followed by dl_attn_merge, with the pieces' partials kept in a
+ * fixed array inside the library (dl_decode_attention_noalloc_max_bytes() bytes,
+ * 8 MiB, held by every GPU that loads the library until the process exits)
+ * instead of a caller workspace.  Same arguments and results as those two calls;
+ * allocates nothing.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (current device at the call); make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents.
+ *    Nothing in it has to start at zero: a call writes every partial it reads.
+ *    Calls whose kernels overlap on the GPU (other streams, other threads) race
+ *    on the array; serialise them.
+ *  - A plan whose workspace_bytes exceeds the array is refused with
+ *    DL_E_WORKSPACE before anything is launched.
+ */
+size_t dl_decode_attention_noalloc_max_bytes(void);
+int dl_decode_attention_noalloc(const float *q, int64_t q_stride, const dl_kv_cache *kv,
+                                const int32_t *seqlen, const dl_attn_plan *plan,
+                                float *out, int64_t out_stride, float *lse,
+                                int32_t *status, dl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

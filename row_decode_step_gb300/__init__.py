@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
             "dl_decode_attn": ([P, I64, P, P, P, P, SZ, P, P], I),
             "dl_decode_attn_ex": ([P, I64, P, P, P, P, SZ, P, I, P], I),
             "dl_attn_merge": ([P, P, P, P, I64, P, P], I),
+            "dl_decode_attention_noalloc_max_bytes": ([], SZ),
+            "dl_decode_attention_noalloc": ([P, I64, P, P, P, P, I64, P, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
