@@ -384,6 +384,22 @@ def cpu_baseline_sample(wl, budget_s=12.0):
             "sample": "%d full layer step(s) of the workload on layer 0, single-threaded C oracle (double)" % reps}
 
 
+def combine_ranks(ms_local, steps, world, device):
+    """Whole-job time and throughput of `world` replicas that each ran `steps` layer steps.
+
+    The job takes as long as its slowest rank (max over ranks); every rank did the same
+    fixed work, so the job's throughput is world * steps over that time.  Returns
+    (ms, layer_steps_per_s) on every rank.
+    """
+    import torch
+    ms = float(ms_local)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * steps / (ms / 1e3)
+
+
 def run_ours(args):
     import torch
     import row_decode_step_gb300 as dl
@@ -403,13 +419,8 @@ def run_ours(args):
 
     wl = workload(args.workload)
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path))
-    ms = res["ms_total"]
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
     steps = args.steps
-    value = world * steps / (ms / 1e3)
+    ms, value = combine_ranks(res["ms_total"], steps, world, dev)
     step = res["step"]
     rows = len(wl["positions"])
     sb = step_bytes(wl, step)

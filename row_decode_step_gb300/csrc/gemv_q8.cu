@@ -3,29 +3,30 @@
 // router launch": eight activation columns per launch, longer launches tiled).
 //
 // Device weight form: tiles of 16 output rows x 32 inputs (one Q8_0 block per
-// row), 512 bytes each, lane t of a warp owning the 16 bytes at 16*t; a lane
-// holds rows g = t/4 and g+8 at the eight inputs {2c, 2c+1, 2c+8, 2c+9} and the
-// same +16, c = t%4 (the A-operand order of a 16x8x16 tensor-core product).
-// Scales: per 16 rows and 4 tiles, 128 bytes; lane group g reads 16 bytes.
+// row), 512 bytes each, in the A-operand order of the 16x8x32 int8 tensor-core
+// product: lane t = 4g + c owns 16 bytes = row g at inputs 4c..4c+3, row g+8 at
+// the same inputs, row g at 16+4c..16+4c+3, row g+8 at those.  The tiles of one
+// row tile are contiguous along K.  Scales: per 16 rows and 4 tiles, 128 bytes;
+// lane group g reads 16 bytes = (d[g], d[g+8]) for the 4 tiles.
 //
-// Kernel shape (2-D tiling of the matrix):
-//  * a CTA of 8 warps owns a run of row tiles and one K-slice of 8*KW k-tiles;
-//    warp w owns KW consecutive k-tiles of the slice for every row tile of the
-//    CTA, so its share of the activations is loaded from global memory once and
-//    kept in registers for the whole launch;
-//  * the warps stream their weight tiles with 16-byte L1-bypassing loads, two
-//    groups in flight; partial sums of a group of row tiles are reduced across
-//    the warps in shared memory in a fixed order;
-//  * the K-slices of one run of row tiles form a thread-block cluster whose
-//    partials are summed through distributed shared memory in rank order (no
-//    atomics: results do not depend on timing);
-//  * before waiting on the previous kernel (programmatic dependent launch) each
-//    CTA asks L2 to prefetch all of its weights, so weight streaming overlaps the
-//    previous kernel's tail.
-// Two inner products share this shape: f32 CUDA-core FMAs (few rows) and
-// 16x8x16 f16 tensor-core products on exact int8 weights with the activations
-// split into two f16 terms (hi + lo) per power-of-two-scaled block, f32
-// accumulation (more rows, where FMAs would bound the kernel).
+// Kernel shape:
+//  * a CTA = one producer warp + 8 consumer warps owns a run of row tiles and one
+//    K-slice; the producer streams one row tile's slice (weights, then scales: two
+//    contiguous bulk copies) into each stage of a shared-memory ring, tracked by
+//    mbarriers, and issues the first stages before waiting on the previous kernel
+//    (programmatic dependent launch);
+//  * each consumer warp owns an eighth of the slice's k-tiles; its activations are
+//    loaded once and kept in registers as operands for the whole launch;
+//  * per row tile each warp adds its k-tiles into a 16x8 accumulator and parks it
+//    in shared memory; the warps' partials are summed once at the end in a fixed
+//    order, and the K-slices of a thread-block cluster through distributed shared
+//    memory in rank order (no atomics: results do not depend on timing).
+// Two inner products share this shape.  Tensor path: the int8 weights enter
+// 16x8x32 int8 products as they are; each activation row is quantised per warp to
+// two int8 terms, x ~ s (h + l/254) with s = max|x|/127, so that both products are
+// exact in int32 and 254 h-sum + l-sum is formed exactly before one conversion to
+// f32 (activation error <= max|x| / 64516 per element).  CUDA-core path: the
+// weights are widened to f32 and multiplied with the f32 activations by FMAs.
 #include <cuda_fp16.h>
 #include <cstdio>
 #include <type_traits>
@@ -33,7 +34,6 @@
 #include "dl_common.cuh"
 
 namespace {
-
 
 enum { PATH_AUTO = 0, PATH_CUDA_CORE = 1, PATH_TENSOR = 2 };
 
@@ -48,15 +48,21 @@ struct GemvArgs {
     int KT;                 // k-tiles, padded to a multiple of 4
     int RT;                 // row tiles
     int cs;                 // K-slices (= cluster size)
-    int ksl;                // k-tiles per K-slice
+    int ksl;                // k-tiles per K-slice (multiple of 4)
+    int rpr;                // row tiles per CTA
+    int stages;             // ring depth
 };
 
+constexpr int kConsumers = 8;                        // consumer warps, each a share of the K-slice
+constexpr int kThreads = (kConsumers + 1) * 32;      // and one producer warp
+constexpr int kMaxStages = 8;
+
+// ---- cluster and shared-memory helpers
 __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
-
 __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
 {
     uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
@@ -66,64 +72,11 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
     return v;
 }
-
-// byte `sel` of wx (a stored weight byte, q + 128) to float q: the byte becomes the low
-// mantissa bits of 2^23 and 2^23 + 128 is subtracted.
-__device__ __forceinline__ float s8_to_f32(uint32_t wx, uint32_t sel)
-{
-    return __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | sel)) - 8388736.0f;
-}
-
-// bytes (0,1) or (2,3) of wx (stored weight bytes, q + 128) to an f16x2 pair of exact
-// integers: each byte becomes the low mantissa of 1024 (f16 0x64xx) and 1024 + 128 is
-// subtracted.
-__device__ __forceinline__ uint32_t s8x2_to_h2(uint32_t wx, uint32_t sel)
-{
-    const uint32_t v = __byte_perm(wx, 0x64646464u, sel);
-    __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&v), __halves2half2(__ushort_as_half(0x6480),
-                                                                               __ushort_as_half(0x6480)));
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ void mma16816(float &c0, float &c1, float &c2, float &c3, uint32_t a0, uint32_t a1,
-                                         uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                 "{%0,%1,%2,%3};"
-                 : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
-{
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// power-of-two scale bringing a block maximum m into [2^13, 2^14), and its inverse
-__device__ __forceinline__ void block_scale(float m, float &s, float &sinv)
-{
-    const uint32_t bits = __float_as_uint(m);
-    int e = (int)((bits >> 23) & 0xFF) - 126;          // m = f * 2^e, f in [0.5, 1)
-    if (m == 0.f || !(m < INFINITY)) e = 14;           // zero, inf, nan: no scaling
-    int es = 14 - e, ei = e - 14;
-    es = max(-126, min(127, es));
-    ei = max(-126, min(127, ei));
-    s = __uint_as_float((uint32_t)(es + 127) << 23);
-    sinv = __uint_as_float((uint32_t)(ei + 127) << 23);
-}
-
-// Offsets (in floats) of the 8 inputs a lane of quad position c holds inside a 32-input block.
-__device__ __forceinline__ int lane_k(int c, int j)
-{
-    return 2 * c + (j & 1) + ((j >> 1) & 1) * 8 + (j >> 2) * 16;
-}
-
-// ---- asynchronous bulk copies into shared memory, tracked by mbarriers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// ---- asynchronous bulk copies into shared memory, tracked by mbarriers
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -132,6 +85,10 @@ __device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
@@ -153,157 +110,147 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     return false;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+// ---- arithmetic helpers
+// stored weight byte `sel` of w (int8) to float, through the biased byte q + 128 placed in
+// the low mantissa of 2^23 (2^23 + 128 subtracted)
+__device__ __forceinline__ float s8_to_f32(uint32_t w, uint32_t sel)
 {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+    return __uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | sel)) - 8388736.0f;
+}
+__device__ __forceinline__ void imma16832(int &c0, int &c1, int &c2, int &c3, const uint4 &a, uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+r"(c0), "+r"(c1), "+r"(c2), "+r"(c3)
+                 : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d)
+{
+    return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) | ((uint32_t)(d & 0xFF) << 24);
 }
 
-constexpr int kConsumers = 8;                        // consumer warps, one row tile each
-constexpr int kThreads5 = (kConsumers + 1) * 32;     // and one producer warp
-constexpr int kStages = 3;                           // ring depth, in groups of 4 k-tiles
-constexpr int kStageBytes = kConsumers * 4 * 512;    // one group of the CTA's 8 row tiles
-
-// Shared-memory bytes of a launch: weight ring, activation fragments, cluster partials.
-size_t gemv_smem(bool mma, int nrc, int ksl)
+// Shared-memory bytes of a launch: a ring of `stages` row-tile stages of `ksl` k-tiles (weights
+// then scales), per-warp partials of `rpr` row tiles, and the cluster partials.
+size_t gemv_smem(int ksl, int stages, int rpr)
 {
-    const size_t fb = mma ? 32 : (size_t)nrc * 32;
-    return (size_t)kStages * kStageBytes + (size_t)ksl * 32 * fb + (size_t)kConsumers * 128 * 4;
+    const size_t sb = (size_t)ksl * 512 + (size_t)ksl * 32;
+    return (size_t)stages * sb + (size_t)rpr * kConsumers * 128 * 4 + (size_t)rpr * 128 * 4;
 }
 
-template <bool MMA, int NRC>
-__global__ void __launch_bounds__(kThreads5, 2) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
+template <bool MMA, int NRC, int KWM>
+__global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
 {
-    constexpr int FB = MMA ? 32 : NRC * 32;          // fragment bytes per lane and k-tile
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
-    __shared__ int s_rowmax[8];
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
     __shared__ int s_fail;
 
-    unsigned char *ring = smem;
-    unsigned char *xf = smem + kStages * kStageBytes;
-    float *cpart = reinterpret_cast<float *>(xf + (size_t)a.ksl * 32 * FB);
-
+    const int S = a.stages;
     const int slice = blockIdx.x % a.cs;
-    const int rt0 = (blockIdx.x / a.cs) * kConsumers;
+    const int rt0 = (blockIdx.x / a.cs) * a.rpr;
+    const int nrt = max(0, min(a.rpr, a.RT - rt0));      // row tiles of this CTA
     const int kt0 = slice * a.ksl, kt1 = min(a.KT, kt0 + a.ksl);
-    const int nkt = kt1 - kt0, ng = nkt >> 2, gb = kt0 >> 2;
+    const int nkt = kt1 - kt0;
+    const uint32_t wbytes = (uint32_t)nkt * 512u, dbytes = (uint32_t)nkt * 32u;
+    const size_t SB = (size_t)a.ksl * 544;
+    unsigned char *ring = smem;
+    float *red = reinterpret_cast<float *>(smem + S * SB);          // [kConsumers][rpr][128]
+    float *cpart = red + kConsumers * a.rpr * 128;                  // [rpr][128]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int nrt = min(kConsumers, a.RT - rt0);
     const int KG = a.KT >> 2;
     const bool producer = warp == kConsumers;
     const unsigned char *qs = reinterpret_cast<const unsigned char *>(a.qs);
+    const unsigned char *dp = reinterpret_cast<const unsigned char *>(a.d);
 
     if (threadIdx.x == 0) {
-        for (int st = 0; st < kStages; ++st) {
+        for (int st = 0; st < S; ++st) {
             mbar_init(&full[st], 1);
             mbar_init(&empty[st], kConsumers);
         }
-        for (int r = 0; r < 8; ++r) s_rowmax[r] = 0;
         s_fail = 0;
         mbar_init_fence();
     }
     __syncthreads();
 
-    // group j of this slice: the CTA's row tiles at k-tiles 4(gb+j) .. 4(gb+j)+3, 2 KB each
+    // stage j: row tile rt0 + j, this slice's k-tiles (contiguous), then their scales (contiguous)
     auto issue = [&](int j) {
-        const int st = j % kStages;
-        mbar_expect_tx(&full[st], (uint32_t)nrt * 2048u);
-        for (int i = 0; i < nrt; ++i)
-            bulk_g2s(ring + st * kStageBytes + i * 2048, qs + ((size_t)(rt0 + i) * a.KT + 4 * (size_t)(gb + j)) * 512,
-                     2048u, &full[st]);
+        const int st = j % S;
+        const int rt = rt0 + j;
+        unsigned char *dst = ring + st * SB;
+        mbar_expect_tx(&full[st], wbytes + dbytes);
+        bulk_g2s(dst, qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
+        bulk_g2s(dst + (size_t)a.ksl * 512, dp + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
     };
     // the weights do not depend on the previous kernel: start the ring before waiting on it
     if (producer && lane == 0)
-        for (int j = 0; j < kStages && j < ng; ++j) issue(j);
-    if (producer && lane < nrt && ng > kStages)
-        dl_prefetch_l2(qs + ((size_t)(rt0 + lane) * a.KT + 4 * (size_t)(gb + kStages)) * 512,
-                       (uint32_t)(ng - kStages) * 2048u);
+        for (int j = 0; j < S && j < nrt; ++j) issue(j);
     dl_pdl_launch_dependents();
     dl_pdl_wait();
 
-    // ---- the slice's activations, as operand fragments in shared memory (every thread).
-    // One pass over global memory: each (k-tile, lane) slot first receives the lane's raw f32
-    // inputs (the CUDA-core operand); the tensor path then rewrites it in place as f16 hi/lo
-    // terms scaled by one power of two per activation row.
-    const int npairs = nkt * 32;                     // (k-tile, lane) pairs
-    {
-        constexpr int PB = 4;                        // slots per thread per batch, loads issued together
-        for (int base = threadIdx.x; base < npairs; base += PB * kThreads5) {
-            float v[PB][NRC][8];
+    // ---- this warp's share of the slice and its activations, kept in registers
+    const int wk0 = (warp * nkt) / kConsumers, wk1 = ((warp + 1) * nkt) / kConsumers;   // slice-local
+    const int nw = producer ? 0 : min(wk1 - wk0, KWM);
+    if (!producer && lane == 0 && wk1 - wk0 > KWM) atomicExch(&s_fail, 1);   // launch shape broken: poison
+    float xv[KWM][NRC][8];
 #pragma unroll
-            for (int u = 0; u < PB; ++u) {
-                const int pi = base + u * kThreads5;
-                const int kt = kt0 + (pi >> 5), t = pi & 31, cc = t & 3;
+    for (int j = 0; j < KWM; ++j) {
+        const int kt = kt0 + wk0 + j;
+        const bool live = j < nw && kt * 32 < a.n_in;
 #pragma unroll
-                for (int r = 0; r < NRC; ++r) {
-                    const int row = MMA ? (t >> 2) : r;
-                    const bool ok = pi < npairs && row < a.nr && kt * 32 < a.n_in;
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        float2 w = make_float2(0.f, 0.f);
-                        if (ok) w = __ldg(reinterpret_cast<const float2 *>(a.x + (int64_t)row * a.x_stride + kt * 32 + lane_k(cc, e)));
-                        v[u][r][e] = w.x;
-                        v[u][r][e + 1] = w.y;
-                    }
-                }
+        for (int r = 0; r < NRC; ++r) {
+            const int row = MMA ? g : r;
+            const bool ok = live && row < a.nr;
+            float4 lo4 = make_float4(0.f, 0.f, 0.f, 0.f), hi4 = lo4;
+            if (ok) {
+                const float *xr = a.x + (int64_t)row * a.x_stride + kt * 32;
+                lo4 = __ldg(reinterpret_cast<const float4 *>(xr + 4 * c));
+                hi4 = __ldg(reinterpret_cast<const float4 *>(xr + 16 + 4 * c));
             }
-#pragma unroll
-            for (int u = 0; u < PB; ++u) {
-                const int pi = base + u * kThreads5;
-                if (pi >= npairs) break;
-                float4 *dst = reinterpret_cast<float4 *>(xf + (size_t)pi * FB);
-#pragma unroll
-                for (int r = 0; r < NRC; ++r) {
-                    dst[2 * r] = make_float4(v[u][r][0], v[u][r][1], v[u][r][2], v[u][r][3]);
-                    dst[2 * r + 1] = make_float4(v[u][r][4], v[u][r][5], v[u][r][6], v[u][r][7]);
-                }
-                if constexpr (MMA) {
-                    const int gg = (pi & 31) >> 2;
-                    float m = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][0][e]));
-                    if (gg < a.nr && m > 0.f) atomicMax(&s_rowmax[gg], __float_as_int(m));
-                }
-            }
+            xv[j][r][0] = lo4.x; xv[j][r][1] = lo4.y; xv[j][r][2] = lo4.z; xv[j][r][3] = lo4.w;
+            xv[j][r][4] = hi4.x; xv[j][r][5] = hi4.y; xv[j][r][6] = hi4.z; xv[j][r][7] = hi4.w;
         }
     }
-    __syncthreads();
+    // tensor path: activation row g quantised over this warp's inputs to two int8 terms,
+    // x ~ s (h + l/254); the products' scale s/254 is applied per accumulator column at the end
+    uint32_t bh[KWM][2], bl[KWM][2];
+    float cs0 = 0.f, cs1 = 0.f;
     if constexpr (MMA) {
-        for (int pi = threadIdx.x; pi < npairs; pi += kThreads5) {
-            const int gg = (pi & 31) >> 2;
-            float sc, si;
-            block_scale(__int_as_float(s_rowmax[gg]), sc, si);
-            uint4 *slot = reinterpret_cast<uint4 *>(xf + (size_t)pi * FB);
-            const uint4 r0 = slot[0], r1 = slot[1];
-            const float x[8] = {__uint_as_float(r0.x), __uint_as_float(r0.y), __uint_as_float(r0.z), __uint_as_float(r0.w),
-                                __uint_as_float(r1.x), __uint_as_float(r1.y), __uint_as_float(r1.z), __uint_as_float(r1.w)};
-            uint32_t hv[4], lv[4];
+        float m = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float x0 = x[2 * e] * sc, x1 = x[2 * e + 1] * sc;
-                const __half2 h = __floats2half2_rn(x0, x1);
-                const float2 hf = __half22float2(h);
-                hv[e] = *reinterpret_cast<const uint32_t *>(&h);
-                lv[e] = pack_h2(x0 - hf.x, x1 - hf.y);
+        for (int j = 0; j < KWM; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[j][0][e]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const float s = m / 127.f;
+        const float inv = m > 0.f ? 127.f / m : 0.f;
+#pragma unroll
+        for (int j = 0; j < KWM; ++j)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                int hq[4], lq[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float t = fminf(fmaxf(xv[j][0][4 * half + e] * inv, -127.f), 127.f);
+                    const float hr = rintf(t);
+                    hq[e] = (int)hr;
+                    lq[e] = (int)rintf((t - hr) * 254.f);
+                }
+                bh[j][half] = pack_s8x4(hq[0], hq[1], hq[2], hq[3]);
+                bl[j][half] = pack_s8x4(lq[0], lq[1], lq[2], lq[3]);
             }
-            slot[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            slot[1] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-        }
-        __syncthreads();
+        // accumulator columns of this lane are rows 2c and 2c+1 (held by lanes 8c and 8c+4)
+        const float sc = s / 254.f;
+        cs0 = __shfl_sync(0xffffffffu, sc, 8 * c);
+        cs1 = __shfl_sync(0xffffffffu, sc, 8 * c + 4);
     }
-
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};             // tensor path: C fragment
-    float accg[NRC], acch[NRC];                      // CUDA-core path: rows g, g+8
-#pragma unroll
-    for (int r = 0; r < NRC; ++r) accg[r] = acch[r] = 0.f;
 
     if (producer) {
         // refill each stage once every consumer warp has released it
         if (lane == 0) {
-            for (int j = kStages; j < ng; ++j) {
-                const int st = j % kStages;
-                if (!mbar_wait(&empty[st], (uint32_t)(((j / kStages) - 1) & 1))) {
+            for (int j = S; j < nrt; ++j) {
+                const int st = j % S;
+                if (!mbar_wait(&empty[st], (uint32_t)(((j / S) - 1) & 1))) {
                     atomicExch(&s_fail, 1);
                     break;
                 }
@@ -311,123 +258,100 @@ __global__ void __launch_bounds__(kThreads5, 2) gemv_q8_kernel(const __grid_cons
             }
         }
     } else {
-        const int rt = rt0 + warp;
-        const bool live = warp < nrt;
-        const uint4 *dsc = reinterpret_cast<const uint4 *>(a.d);
-        uint4 scn = make_uint4(0u, 0u, 0u, 0u);
-        if (live && ng > 0) scn = __ldg(dsc + ((size_t)rt * KG + gb) * 8 + g);
-        for (int j = 0; j < ng; ++j) {
-            const int st = j % kStages;
-            const uint4 sc4 = scn;
-            if (live && j + 1 < ng) scn = __ldg(dsc + ((size_t)rt * KG + gb + j + 1) * 8 + g);
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (uint32_t)((j / kStages) & 1)))) {
+        for (int i = 0; i < nrt; ++i) {
+            const int st = i % S;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (uint32_t)((i / S) & 1)))) {
                 if (lane == 0) atomicExch(&s_fail, 1);
                 break;
             }
-            if (live) {
-                const unsigned char *sw = ring + st * kStageBytes + warp * 2048;
-                const uint32_t sp[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+            const unsigned char *sw = ring + st * SB;
+            const unsigned char *sd = sw + (size_t)a.ksl * 512;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float accg[NRC], acch[NRC];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(sw + q * 512 + lane * 16);
-                    const float dg = __half2float(__ushort_as_half((unsigned short)(sp[q] & 0xFFFFu)));
-                    const float dh = __half2float(__ushort_as_half((unsigned short)(sp[q] >> 16)));
-                    const unsigned char *fr = xf + ((size_t)(4 * j + q) * 32 + lane) * FB;
-                    if constexpr (MMA) {
-                        const uint4 bh = *reinterpret_cast<const uint4 *>(fr);
-                        const uint4 bl = *reinterpret_cast<const uint4 *>(fr + 16);
-                        const uint32_t a0 = s8x2_to_h2(w.x, 0x5150), a1 = s8x2_to_h2(w.x, 0x5352);
-                        const uint32_t a2 = s8x2_to_h2(w.y, 0x5150), a3 = s8x2_to_h2(w.y, 0x5352);
-                        const uint32_t a4 = s8x2_to_h2(w.z, 0x5150), a5 = s8x2_to_h2(w.z, 0x5352);
-                        const uint32_t a6 = s8x2_to_h2(w.w, 0x5150), a7 = s8x2_to_h2(w.w, 0x5352);
-                        float h0 = 0.f, h1 = 0.f, h2 = 0.f, h3 = 0.f;    // hi terms
-                        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;    // lo terms (independent chain)
-                        mma16816(h0, h1, h2, h3, a0, a1, a2, a3, bh.x, bh.y);
-                        mma16816(l0, l1, l2, l3, a0, a1, a2, a3, bl.x, bl.y);
-                        mma16816(h0, h1, h2, h3, a4, a5, a6, a7, bh.z, bh.w);
-                        mma16816(l0, l1, l2, l3, a4, a5, a6, a7, bl.z, bl.w);
-                        acc[0] = fmaf(dg, h0 + l0, acc[0]);
-                        acc[1] = fmaf(dg, h1 + l1, acc[1]);
-                        acc[2] = fmaf(dh, h2 + l2, acc[2]);
-                        acc[3] = fmaf(dh, h3 + l3, acc[3]);
-                    } else {
-                        float wg[8], wh[8];
-                        wg[0] = s8_to_f32(w.x, 0); wg[1] = s8_to_f32(w.x, 1);
-                        wg[2] = s8_to_f32(w.y, 0); wg[3] = s8_to_f32(w.y, 1);
-                        wg[4] = s8_to_f32(w.z, 0); wg[5] = s8_to_f32(w.z, 1);
-                        wg[6] = s8_to_f32(w.w, 0); wg[7] = s8_to_f32(w.w, 1);
-                        wh[0] = s8_to_f32(w.x, 2); wh[1] = s8_to_f32(w.x, 3);
-                        wh[2] = s8_to_f32(w.y, 2); wh[3] = s8_to_f32(w.y, 3);
-                        wh[4] = s8_to_f32(w.z, 2); wh[5] = s8_to_f32(w.z, 3);
-                        wh[6] = s8_to_f32(w.w, 2); wh[7] = s8_to_f32(w.w, 3);
+            for (int r = 0; r < NRC; ++r) accg[r] = acch[r] = 0.f;
 #pragma unroll
-                        for (int r = 0; r < NRC; ++r) {
-                            const float4 xa = *reinterpret_cast<const float4 *>(fr + r * 32);
-                            const float4 xb = *reinterpret_cast<const float4 *>(fr + r * 32 + 16);
-                            float sg = wg[0] * xa.x, sh = wh[0] * xa.x;
-                            sg = fmaf(wg[1], xa.y, sg); sh = fmaf(wh[1], xa.y, sh);
-                            sg = fmaf(wg[2], xa.z, sg); sh = fmaf(wh[2], xa.z, sh);
-                            sg = fmaf(wg[3], xa.w, sg); sh = fmaf(wh[3], xa.w, sh);
-                            sg = fmaf(wg[4], xb.x, sg); sh = fmaf(wh[4], xb.x, sh);
-                            sg = fmaf(wg[5], xb.y, sg); sh = fmaf(wh[5], xb.y, sh);
-                            sg = fmaf(wg[6], xb.z, sg); sh = fmaf(wh[6], xb.z, sh);
-                            sg = fmaf(wg[7], xb.w, sg); sh = fmaf(wh[7], xb.w, sh);
-                            accg[r] = fmaf(dg, sg, accg[r]);
-                            acch[r] = fmaf(dh, sh, acch[r]);
+            for (int j = 0; j < KWM; ++j) {
+                if (j >= nw) break;
+                const int kl = wk0 + j;                                  // slice-local k-tile
+                const uint4 w = *reinterpret_cast<const uint4 *>(sw + kl * 512 + lane * 16);
+                const uint32_t sp = *reinterpret_cast<const uint32_t *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4);
+                const float dg = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
+                const float dh = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
+                if constexpr (MMA) {
+                    int h0 = 0, h1 = 0, h2 = 0, h3 = 0, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
+                    imma16832(h0, h1, h2, h3, w, bh[j][0], bh[j][1]);
+                    imma16832(l0, l1, l2, l3, w, bl[j][0], bl[j][1]);
+                    // 254 h-sum + l-sum is exact in int32 (|h-sum| <= 32*127*127)
+                    acc[0] = fmaf(dg, (float)(h0 * 254 + l0), acc[0]);
+                    acc[1] = fmaf(dg, (float)(h1 * 254 + l1), acc[1]);
+                    acc[2] = fmaf(dh, (float)(h2 * 254 + l2), acc[2]);
+                    acc[3] = fmaf(dh, (float)(h3 * 254 + l3), acc[3]);
+                } else {
+                    // row g: words 0 and 2; row g+8: words 1 and 3
+                    float wg[8], wh[8];
+                    wg[0] = s8_to_f32(w.x, 0); wg[1] = s8_to_f32(w.x, 1); wg[2] = s8_to_f32(w.x, 2); wg[3] = s8_to_f32(w.x, 3);
+                    wg[4] = s8_to_f32(w.z, 0); wg[5] = s8_to_f32(w.z, 1); wg[6] = s8_to_f32(w.z, 2); wg[7] = s8_to_f32(w.z, 3);
+                    wh[0] = s8_to_f32(w.y, 0); wh[1] = s8_to_f32(w.y, 1); wh[2] = s8_to_f32(w.y, 2); wh[3] = s8_to_f32(w.y, 3);
+                    wh[4] = s8_to_f32(w.w, 0); wh[5] = s8_to_f32(w.w, 1); wh[6] = s8_to_f32(w.w, 2); wh[7] = s8_to_f32(w.w, 3);
+#pragma unroll
+                    for (int r = 0; r < NRC; ++r) {
+                        float sg = wg[0] * xv[j][r][0], sh = wh[0] * xv[j][r][0];
+#pragma unroll
+                        for (int e = 1; e < 8; ++e) {
+                            sg = fmaf(wg[e], xv[j][r][e], sg);
+                            sh = fmaf(wh[e], xv[j][r][e], sh);
                         }
+                        accg[r] = fmaf(dg, sg, accg[r]);
+                        acch[r] = fmaf(dh, sh, acch[r]);
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            if (lane == 0) mbar_arrive(&empty[st]);            // the stage is free for the producer
+            float *rw = red + (warp * a.rpr + i) * 128;
+            if constexpr (MMA) {
+                *reinterpret_cast<float2 *>(rw + g * 8 + 2 * c) = make_float2(acc[0] * cs0, acc[1] * cs1);
+                *reinterpret_cast<float2 *>(rw + (g + 8) * 8 + 2 * c) = make_float2(acc[2] * cs0, acc[3] * cs1);
+            } else {
+#pragma unroll
+                for (int r = 0; r < NRC; ++r) {
+                    float vg = accg[r], vh = acch[r];
+                    vg += __shfl_xor_sync(0xffffffffu, vg, 1);
+                    vg += __shfl_xor_sync(0xffffffffu, vg, 2);
+                    vh += __shfl_xor_sync(0xffffffffu, vh, 1);
+                    vh += __shfl_xor_sync(0xffffffffu, vh, 2);
+                    if (c == 0) {
+                        rw[g * 8 + r] = vg;
+                        rw[(g + 8) * 8 + r] = vh;
+                    }
+                }
+            }
         }
     }
     __syncthreads();
     const bool failed = s_fail != 0;
 
-    // ---- results: each consumer warp holds complete sums of its row tile over the slice
-    const int rt = rt0 + warp;
-    const bool mine = !producer && warp < nrt;
-    auto emit = [&](int o, int col, float v) {         // o: output row, col: activation row
-        if (failed) v = __int_as_float(0x7fc00000);
-        if (a.cs == 1) {
-            if (o < a.n_out) a.y[(int64_t)col * a.y_stride + o] = v;
-        } else {
-            cpart[(warp * 16 + (o - rt * 16)) * 8 + col] = v;
-        }
-    };
-    if (mine) {
-        if constexpr (MMA) {
-            float s0, si0, s1, si1;
-            block_scale(__int_as_float(s_rowmax[2 * c]), s0, si0);
-            block_scale(__int_as_float(s_rowmax[2 * c + 1]), s1, si1);
-            if (2 * c < a.nr) {
-                emit(rt * 16 + g, 2 * c, acc[0] * si0);
-                emit(rt * 16 + g + 8, 2 * c, acc[2] * si0);
-            }
-            if (2 * c + 1 < a.nr) {
-                emit(rt * 16 + g, 2 * c + 1, acc[1] * si1);
-                emit(rt * 16 + g + 8, 2 * c + 1, acc[3] * si1);
-            }
-        } else {
+    // ---- sum the warps' partials in a fixed order; finish here or hand to the cluster
+    for (int e = threadIdx.x; e < nrt * 128; e += kThreads) {
+        const int i = e >> 7, el = e & 127;
+        const int row = el >> 3, col = el & 7;
+        if (col >= a.nr) continue;
+        float sum = 0.f;
 #pragma unroll
-            for (int r = 0; r < NRC; ++r) {
-                float vg = accg[r], vh = acch[r];
-                vg += __shfl_xor_sync(0xffffffffu, vg, 1);
-                vg += __shfl_xor_sync(0xffffffffu, vg, 2);
-                vh += __shfl_xor_sync(0xffffffffu, vh, 1);
-                vh += __shfl_xor_sync(0xffffffffu, vh, 2);
-                if (c == 0 && r < a.nr) {
-                    emit(rt * 16 + g, r, vg);
-                    emit(rt * 16 + g + 8, r, vh);
-                }
-            }
+        for (int w = 0; w < kConsumers; ++w) sum += red[(w * a.rpr + i) * 128 + el];
+        if (failed) sum = __int_as_float(0x7fc00000);
+        if (a.cs == 1) {
+            const int o = (rt0 + i) * 16 + row;
+            if (o < a.n_out) a.y[(int64_t)col * a.y_stride + o] = sum;
+        } else {
+            cpart[e] = sum;
         }
     }
     if (a.cs > 1) {
         // every K-slice of this run of row tiles holds its partials in shared memory: sum in rank order
         cluster_sync_all();
-        for (int e = threadIdx.x; e < nrt * 128; e += kThreads5) {
+        for (int e = threadIdx.x; e < nrt * 128; e += kThreads) {
             if ((e >> 3) % a.cs != slice) continue;      // each rank finishes a share of the rows
             const int col = e & 7;
             if (col >= a.nr) continue;
@@ -445,10 +369,12 @@ __global__ void __launch_bounds__(kThreads5, 2) gemv_q8_kernel(const __grid_cons
 __device__ __forceinline__ uint32_t q8_byte(const uint8_t *blocks, int64_t n_out, int64_t n_in,
                                             int64_t o, int64_t k)
 {
-    if (o >= n_out || k >= n_in) return 0x80u;       // a zero weight, stored biased
-    return blocks[(o * (n_in / 32) + k / 32) * 34 + 2 + (k % 32)] ^ 0x80u;   // q + 128
+    if (o >= n_out || k >= n_in) return 0u;
+    return blocks[(o * (n_in / 32) + k / 32) * 34 + 2 + (k % 32)];
 }
 
+// lane t = 4g + c of tile (rt, kt): word 0 = row g at inputs 4c..4c+3, word 1 = row g+8 there,
+// words 2 and 3 = the same rows at 16+4c..16+4c+3
 __global__ void q8_pack_qs_kernel(const uint8_t *blocks, int64_t n_out, int64_t n_in, int KT,
                                   int64_t units, uint4 *qs)
 {
@@ -458,14 +384,15 @@ __global__ void q8_pack_qs_kernel(const uint8_t *blocks, int64_t n_out, int64_t 
     const int64_t t = u >> 5;
     const int64_t kt = t % KT, rt = t / KT;
     const int g = lane >> 2, c = lane & 3;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    uint32_t w[4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int h = j >> 3, p = (j >> 1) & 3, e = j & 1;
-        const int row = g + (p & 1) * 8;
-        const int kk = 2 * c + (p >> 1) * 8 + h * 16 + e;
-        const uint32_t b = q8_byte(blocks, n_out, n_in, rt * 16 + row, kt * 32 + kk);
-        w[j >> 2] |= b << (8 * (j & 3));
+    for (int q = 0; q < 4; ++q) {
+        const int row = g + (q & 1) * 8;
+        const int k0 = 4 * c + (q >> 1) * 16;
+        uint32_t v = 0u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) v |= q8_byte(blocks, n_out, n_in, rt * 16 + row, kt * 32 + k0 + b) << (8 * b);
+        w[q] = v;
     }
     qs[u] = make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -499,20 +426,27 @@ __global__ void q8_pack_d_kernel(const uint8_t *blocks, int64_t n_out, int64_t n
     d[u] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-
 // ---------------------------------------------------------------- launch
 
 struct GemvCfg {
     bool mma;
-    int nrc, cs, ksl, grid;
+    int nrc, kwm, cs, ksl, rpr, stages, grid;
     size_t smem;
 };
 
-void *pick_kernel(bool mma, int nrc)
+template <bool MMA, int NRC, int KWM>
+void *kptr() { return reinterpret_cast<void *>(gemv_q8_kernel<MMA, NRC, KWM>); }
+
+void *pick_kernel(bool mma, int nrc, int kwm)
 {
-    if (mma) return reinterpret_cast<void *>(gemv_q8_kernel<true, 1>);
-    if (nrc == 1) return reinterpret_cast<void *>(gemv_q8_kernel<false, 1>);
-    return reinterpret_cast<void *>(gemv_q8_kernel<false, 2>);
+    switch (kwm) {
+    case 1: return mma ? kptr<true, 1, 1>() : nrc == 1 ? kptr<false, 1, 1>() : kptr<false, 2, 1>();
+    case 2: return mma ? kptr<true, 1, 2>() : nrc == 1 ? kptr<false, 1, 2>() : kptr<false, 2, 2>();
+    case 4: return mma ? kptr<true, 1, 4>() : nrc == 1 ? kptr<false, 1, 4>() : kptr<false, 2, 4>();
+    case 6: return mma ? kptr<true, 1, 6>() : nullptr;
+    case 8: return mma ? kptr<true, 1, 8>() : nrc == 1 ? kptr<false, 1, 8>() : nullptr;
+    }
+    return nullptr;
 }
 
 // The dynamic shared-memory limit is a per-function attribute shared by every launch of the
@@ -520,9 +454,8 @@ void *pick_kernel(bool mma, int nrc)
 // launch shape may use, never to one launch's own size.
 constexpr int kSmemLimit = 200 * 1024;
 
-int prepare_kernel(const void *kern, size_t smem, int cs)
+int prepare_kernel(const void *kern, int cs)
 {
-    if (smem > (size_t)kSmemLimit) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: %zu bytes of shared memory", smem);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8: set shared memory");
     if (cs > 8) {
@@ -532,20 +465,12 @@ int prepare_kernel(const void *kern, size_t smem, int cs)
     return DL_OK;
 }
 
-// CTAs of one launch shape that are resident at once (clusters counted whole).
-int resident_ctas(const void *kern, int cs, size_t smem, int sm)
+// Clusters of `cs` CTAs of this shape that are resident at once.
+int resident_clusters(const void *kern, int cs, size_t smem)
 {
-    if (cs <= 1) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads5, smem) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
-        return per_sm * sm;
-    }
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cs);
-    lc.blockDim = dim3(kThreads5);
+    lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -559,46 +484,82 @@ int resident_ctas(const void *kern, int cs, size_t smem, int sm)
         cudaGetLastError();
         return 0;
     }
-    return clusters * cs;
+    return clusters;
 }
 
-// Launch shape: K split into cs slices of whole groups of 4 k-tiles, 8 row tiles per CTA;
-// the smallest slice whose grid is resident in one wave, then the fewest slices.
+// Launch shape.  K is cut into cs slices of ksl k-tiles (whole groups of 4); each CTA takes
+// rpr consecutive row tiles of one slice and streams them one row tile per ring stage.  The
+// shape with the least work per CTA whose grid is resident in one wave wins (near-ties go
+// to fewer slices).
 int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
 {
     const bool mma = path == PATH_TENSOR || (path == PATH_AUTO && nr > 2);
     if (!mma && nr > 2) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: the CUDA-core path serves 1 or 2 rows per command");
     const int nrc = mma ? 1 : nr;
-    const void *kern = pick_kernel(mma, nrc);
-    const int mgroups = (int)dl::ceil_div(RT, kConsumers);
+    const int kw_max = (!mma && nrc == 2) ? 4 : 8;
     GemvCfg best{};
-    int best_ksl = -1;
+    long best_cost = -1;
     for (int cs = 1; cs <= 16; ++cs) {
         const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
         if ((int)dl::ceil_div(KT, ksl) != cs) continue;
-        const size_t smem = gemv_smem(mma, nrc, ksl);
-        if (smem > (size_t)kSmemLimit) continue;
-        if (prepare_kernel(kern, smem, cs) != DL_OK) return DL_E_CUDA;
-        const int grid = mgroups * cs;
-        if (grid > resident_ctas(kern, cs, smem, sm)) continue;
-        if (best_ksl < 0 || ksl < best_ksl) {
-            best_ksl = ksl;
-            best = GemvCfg{mma, nrc, cs, ksl, grid, smem};
+        const int kw = (int)dl::ceil_div(ksl, kConsumers);             // k-tiles per consumer warp
+        if (kw > kw_max || (size_t)ksl * 544 > 48 * 1024) continue;
+        const int kwm = kw <= 1 ? 1 : kw <= 2 ? 2 : kw <= 4 ? 4 : (mma && kw <= 6) ? 6 : 8;
+        const size_t sb = (size_t)ksl * 544;
+        // two CTAs per SM when shared memory allows, else one; the ring takes what the
+        // partials leave (2 to 8 stages)
+        for (int per_sm = 2; per_sm >= 1; --per_sm) {
+            const int ranges = (per_sm * sm) / cs;
+            if (ranges < 1) continue;
+            const int rpr = (int)dl::ceil_div(RT, ranges);
+            const size_t limit = per_sm == 2 ? (size_t)112 * 1024 : (size_t)kSmemLimit;
+            const size_t fixed = gemv_smem(ksl, 0, rpr);
+            if (fixed + 2 * sb > limit) continue;
+            int stages = (int)((limit - fixed) / sb);
+            if (stages > kMaxStages) stages = kMaxStages;
+            const size_t smem = gemv_smem(ksl, stages, rpr);
+            const long cost = (long)rpr * ksl * 100 + cs;        // bytes per CTA, then fewer slices
+            if (best_cost < 0 || cost * 100 < best_cost * 95) {
+                best_cost = cost;
+                best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs, smem};
+            }
+            break;
         }
     }
-    if (best_ksl < 0) {
-        // more row tiles than one wave holds: whole-K CTAs in several waves, or the
-        // smallest slices that fit shared memory
-        for (int cs = 1; cs <= 16 && best_ksl < 0; ++cs) {
+    if (best_cost < 0) {
+        // no single-wave shape (very many row tiles): CTAs of as many row tiles as shared memory
+        // holds, in several waves
+        for (int cs = 1; cs <= 16 && best_cost < 0; ++cs) {
             const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
             if ((int)dl::ceil_div(KT, ksl) != cs) continue;
-            const size_t smem = gemv_smem(mma, nrc, ksl);
-            if (smem > (size_t)kSmemLimit) continue;
-            if (prepare_kernel(kern, smem, cs) != DL_OK) return DL_E_CUDA;
-            best_ksl = ksl;
-            best = GemvCfg{mma, nrc, cs, ksl, mgroups * cs, smem};
+            const int kw = (int)dl::ceil_div(ksl, kConsumers);
+            if (kw > kw_max || (size_t)ksl * 544 > 48 * 1024) continue;
+            const int kwm = kw <= 1 ? 1 : kw <= 2 ? 2 : kw <= 4 ? 4 : (mma && kw <= 6) ? 6 : 8;
+            const size_t sb = (size_t)ksl * 544;
+            const int stages = 3;
+            int rpr = (int)(((size_t)112 * 1024 - stages * sb) / ((size_t)kConsumers * 512 + 512));
+            if (rpr < 1) continue;
+            if (rpr > RT) rpr = RT;
+            best_cost = 0;
+            best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
+                           gemv_smem(ksl, stages, rpr)};
         }
-        if (best_ksl < 0) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no launch shape for %d k-tiles", KT);
+        if (best_cost < 0) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no launch shape for %d k-tiles", KT);
+    }
+    const void *kern = pick_kernel(best.mma, best.nrc, best.kwm);
+    if (!kern) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no kernel for this shape");
+    int rc = prepare_kernel(kern, best.cs);
+    if (rc != DL_OK) return rc;
+    if (best.cs > 1 && best_cost > 0) {
+        // a one-wave shape stays one wave with clusters: grow the row tiles per CTA until every
+        // cluster is resident at once, within the shared-memory limit
+        while (resident_clusters(kern, best.cs, best.smem) < best.grid / best.cs && best.rpr < RT) {
+            const size_t smem = gemv_smem(best.ksl, best.stages, best.rpr + 1);
+            if (smem > (size_t)kSmemLimit) break;
+            best.rpr += 1;
+            best.smem = smem;
+            best.grid = (int)dl::ceil_div(RT, best.rpr) * best.cs;
+        }
     }
     *out = best;
     return DL_OK;
@@ -612,12 +573,12 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     a.nr = nr;
     a.cs = cfg.cs;
     a.ksl = cfg.ksl;
-    const void *kern = pick_kernel(cfg.mma, cfg.nrc);
-    rc = prepare_kernel(kern, cfg.smem, cfg.cs);     // the shape search left another candidate's limit
-    if (rc != DL_OK) return rc;
+    a.rpr = cfg.rpr;
+    a.stages = cfg.stages;
+    const void *kern = pick_kernel(cfg.mma, cfg.nrc, cfg.kwm);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid);
-    lc.blockDim = dim3(kThreads5);
+    lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = cfg.smem;
     lc.stream = st;
     cudaLaunchAttribute attr[2];

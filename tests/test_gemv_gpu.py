@@ -79,7 +79,14 @@ def test_gemv_cuda_core_path_refuses_wide_commands(dl):
 
 
 def test_gemv_rows_match_single_rows(dl):
-    """Rows stepped together equal the same rows stepped one at a time (tails of 2, 9, 16)."""
+    """Rows stepped together agree with the same rows stepped one at a time (tails of 2, 9, 16).
+
+    One row takes the CUDA-core inner product (activations in f32); a command of 2 or
+    more rows takes the int8 tensor path, whose two-term activation code x ~ s(h + l/254),
+    s = max|x|/127 over a warp's inputs, is off by at most s/508 per element.  Summed
+    against N(0, 0.02) weights that stays near 1e-4 of the output scale, so the two agree
+    at 3e-4, well inside the 1e-3 bar each of them meets against the oracle.
+    """
     n_out, n_in = 384, 1024
     blocks = synth.q8_0_blocks_from_normal(2, "gemv/tail", n_out, n_in)
     W = dl.dl_q8_pack(blocks.cuda(), n_out, n_in)
@@ -88,7 +95,24 @@ def test_gemv_rows_match_single_rows(dl):
         y = dl.dl_gemv_q8(W, x[:n])
         ys = torch.cat([dl.dl_gemv_q8(W, x[r:r + 1]) for r in range(n)])
         torch.cuda.synchronize()
-        assert gemv_err(y.cpu().numpy(), ys.cpu().numpy().astype(np.float64)) < 1e-5
+        assert gemv_err(y.cpu().numpy(), ys.cpu().numpy().astype(np.float64)) < 3e-4
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_gemv_row_independent_of_other_rows(dl, path):
+    """A row's outputs do not depend on the other rows of its command: bit-identical when they change."""
+    n_out, n_in = 384, 1024
+    rows = 2 if path == 1 else 9
+    blocks = synth.q8_0_blocks_from_normal(2, "gemv/indep", n_out, n_in)
+    W = dl.dl_q8_pack(blocks.cuda(), n_out, n_in)
+    x = synth.normal_f32(2, "gemv/indep/x", (rows, n_in)).cuda()
+    y0 = dl.dl_gemv_q8(W, x, path=path)
+    x2 = x.clone()
+    x2[1:] = 1e3 * synth.normal_f32(3, "gemv/indep/x2", (rows - 1, n_in)).cuda()
+    y1 = dl.dl_gemv_q8(W, x2, path=path)
+    torch.cuda.synchronize()
+    assert torch.equal(y0[0], y1[0])
+    assert not torch.equal(y0[1], y1[1])
 
 
 def test_gemv_strides_and_poisoned_padding(dl):

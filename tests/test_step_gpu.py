@@ -64,7 +64,9 @@ def _step(dl, S, positions, regions, n_regions, capacity, label):
         # q is roped in place inside qkv; its k and v parts are the GEMV's own output
         qd = n_q * D
         assert_gemv_close(c.qkv.cpu().numpy()[:, qd:], ref["qkv"][:, qd:])
-        np.testing.assert_allclose(c.q.cpu().numpy(), ref["q"], rtol=2e-6, atol=1e-5)
+        # roped q carries the GEMV's error through a rotation of channel pairs, which keeps each
+        # pair's error norm: at most sqrt(2) times the GEMV bar per element
+        assert gemv_err(c.q.cpu().numpy(), ref["q"]) < 1e-3 * np.sqrt(2)
         assert_attn_close(c.attn.cpu().numpy(), c.lse.cpu().numpy(), ref["attn"], ref["lse"])
         # the O projection's input differs by the attention error; allow that share on top of the bar
         assert gemv_err(c.y_o.cpu().numpy(), ref["y_o"]) < 1e-2
