@@ -94,12 +94,13 @@ int dl_status_read(const int32_t *status_dev, int32_t *host_out);
  * Device form (written by dl_q8_pack, read by dl_gemv_q8): two planes.
  *  qs: tiles of 16 output rows x 32 inputs (512 bytes), tile (rt, kt) at byte
  *      ((rt * KT) + kt) * 512 with KT = 4 * ceil(n_in / 128); inside a tile the
- *      16 bytes of lane t = 4g + c hold, in order, row g at inputs 4c..4c+3, row
- *      g+8 at the same inputs, row g at 16+4c..16+4c+3 and row g+8 there (the
- *      A-operand order of a 16x8x32 int8 tensor-core product), as signed bytes.
+ *      16 bytes of lane t = 4g + c are four words, word p holding inputs kb and
+ *      kb + 1 (kb = 16*(p/2) + 8*(p%2) + 2c) of row g, then of row g + 8 (the
+ *      A-operand order of two 16x8x16 f16 tensor-core products), each weight as
+ *      the biased byte q + 128.
  *  d:  per 16 rows and 4 consecutive tiles, 128 bytes: lane group g's 16 bytes
  *      hold (d[g], d[g+8]) for those 4 tiles.
- * Rows past n_out and inputs past n_in are zero-filled.  Both planes must be
+ * Rows past n_out and inputs past n_in hold q = 0 and d = 0.  Both planes must be
  * 16-byte aligned.
  */
 typedef struct dl_q8_weight {
@@ -129,19 +130,20 @@ int dl_q8_pack(const uint8_t *blocks, int64_t n_out, int64_t n_in,
  * Rows are stepped eight at a time: the weights are read once per group of up
  * to eight rows, and a row's result does not depend on the rows stepped with it.
  * x and the planes must be 16-byte aligned and x_stride a multiple of 4.
- * Arithmetic: see dl_gemv_q8_ex (the automatic choice is the tensor path).
+ * Arithmetic: see dl_gemv_q8_ex (path 0).
  */
 int dl_gemv_q8(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
                float *y, int64_t y_stride, dl_stream_t stream);
 
 /*
  * dl_gemv_q8 with the inner product chosen by the caller (testing and
- * measurement): path 0 = automatic (what dl_gemv_q8 does: tensor cores),
- * 1 = f32 CUDA-core FMAs on the widened weights (commands of 1 or 2 rows only,
- * else DL_E_SHAPE), 2 = 16x8x32 int8 tensor-core products on the weights as
- * stored, each activation row quantised per block of inputs to two int8 terms
- * x ~ s (h + l/254) with s = max|x|/127 (error <= max|x|/64516 per element), the
- * two products exact in int32, scaled and summed in f32.  Same result contract.
+ * measurement): path 0 = automatic (what dl_gemv_q8 does: CUDA cores for
+ * commands of 1 or 2 rows, tensor cores for 3 to 8), 1 = f32 CUDA-core FMAs on
+ * the widened weights (commands of 1 or 2 rows only, else DL_E_SHAPE), 2 =
+ * 16x8x16 f16 tensor-core products with f32 accumulation on the weights as
+ * 1152 + q (exact in f16), each activation row scaled per block of inputs by a
+ * power of two and split into two f16 terms (about 22 significant bits), the
+ * bias 1152 * sum(x) removed per block.  Same result contract.
  */
 int dl_gemv_q8_ex(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
                   float *y, int64_t y_stride, int path, dl_stream_t stream);

@@ -10,12 +10,16 @@
 // are staged in shared memory with cp.async (16-byte copies, double-buffered);
 // scores use one lane per key, the online softmax reduces over the warp with
 // shuffles, and P.V runs with lanes over head dimensions.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cmath>
 #include <cstring>
 #include <algorithm>
+#include <mutex>
 
 #include "dl_common.cuh"
+#include "dl_async.cuh"
 
 namespace {
 
@@ -115,8 +119,8 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_cc_kernel(const __gr
             dl_prefetch_l2(a.vc + off, (uint32_t)(p1 - p0) * D * 2u);
         }
     }
-    dl_pdl_launch_dependents();
     dl_pdl_wait();
+    dl_pdl_launch_dependents();
 
     if (tid < nrows) {
         const int r = P.sess_rows[rb + tid];
@@ -301,14 +305,18 @@ __global__ void __launch_bounds__(kAttnThreads) decode_attn_cc_kernel(const __gr
 
 // ---------------------------------------------------------------------------
 // Tensor-core form for sessions of several rows (many queries per KV head):
-// queries are the 16-row M side of 16x8x16 f16 products.  Each warp owns one
-// 16-query tile and a contiguous share of the piece's keys, streams 16-key
-// blocks of K and V into its own double-buffered, XOR-swizzled shared-memory
-// ring with cp.async, and keeps (m, l, O) for its queries in registers: scores
-// S = Q K^T with Q split into two f16 terms (hi + lo, near-f32 exact), online
-// softmax in the log2 domain on the accumulator fragments, then O += P V with P
-// in f16 (the running maximum's own entry is exactly 1).  The warps holding the
-// same queries combine their (m, l, O) in shared memory at the end.
+// queries are the 16-row M side of 16x8x16 f16 products.  A producer warp
+// streams 32-key stages of K and V through tensor maps (128-byte swizzle, so
+// that the matrix loads below are conflict-free) into a ring of mbarrier-
+// tracked shared-memory stages.  Stages whose keys all lie below the lowest
+// position this command writes do not depend on the previous kernel and are
+// issued before waiting on it.  Each consumer warp owns one 16-query tile and
+// every KS-th stage (KS = 4 / query tiles), and keeps (m, l, O) for its queries
+// in registers: scores S = Q K^T with Q split into two f16 terms (hi + lo,
+// near-f32 exact), online softmax in the log2 domain on the accumulator
+// fragments, then O += P V with P in f16 (the running maximum's own entry is
+// exactly 1).  The warps holding the same queries combine their (m, l, O) in
+// shared memory at the end.
 
 __device__ __forceinline__ void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, uint32_t addr)
 {
@@ -336,28 +344,51 @@ __device__ __forceinline__ uint32_t h2_bits(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-constexpr int kMmaKB = 16;      // keys per block of the tensor-core form
+constexpr int kStKeys = 32;                  // keys per stage
+constexpr int kMmaConsumers = 4;             // consumer warps
+constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
+constexpr int kMmaMaxStages = 8;
+constexpr int kHalfTile = kStKeys * 128;     // bytes of 32 keys x 64 dims (one swizzled box)
+
+// Ring depth per head dimension: two CTAs fit on an SM.
+__host__ __device__ constexpr int mma_stages(int D) { return D == 128 ? 5 : 8; }
 
 size_t attn_mma_smem_bytes(int D)
 {
-    const size_t ring = (size_t)4 * 2 * 2 * kMmaKB * D * 2;             // warps x stages x (K,V) x block
-    const size_t comb = (size_t)4 * 16 * D * 4 + (size_t)4 * 16 * 2 * 4;  // O, m, l of every warp
+    const size_t stage = (size_t)2 * kStKeys * D * 2;                    // K and V of 32 keys
     const size_t qf = (size_t)2 * (D / 16) * 32 * 32;                    // query fragments, 2 tiles
-    return (ring > comb ? ring : comb) + qf;
+    return 1024 + (size_t)mma_stages(D) * stage + qf;                   // + alignment slack
+}
+
+// OR of `flag` over the consumer warps (uniform result).
+__device__ __forceinline__ bool attn_consumers_any(bool flag)
+{
+    uint32_t r;
+    asm volatile("{\n .reg .pred pin, pout;\n setp.ne.u32 pin, %1, 0;\n"
+                 " bar.red.or.pred pout, 1, %2, pin;\n selp.u32 %0, 1, 0, pout;\n}"
+                 : "=r"(r) : "r"((uint32_t)flag), "r"((uint32_t)(kMmaConsumers * 32)) : "memory");
+    return r != 0;
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 2) decode_attn_mma_kernel(const __grid_constant__ AttnArgs a)
+__global__ void __launch_bounds__(kMmaThreads, 2)
+decode_attn_mma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv)
 {
-    constexpr int KB = kMmaKB;
-    constexpr int CPR = D / 8;      // 16-byte chunks per key row
     constexpr int NKS = D / 16;     // k-steps of the score product
     constexpr int NDT = D / 8;      // 8-wide column tiles of the output
-    constexpr int BLK = KB * D;     // halves per K (or V) block
+    constexpr int NH = D / 64;      // 64-dim boxes per key row
+    constexpr int S = mma_stages(D);
+    constexpr uint32_t kStageBytes = 2u * kStKeys * D * 2u;
     const dl_attn_plan &P = a.plan;
 
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full[kMmaMaxStages], empty[kMmaMaxStages];
     __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS];
+    __shared__ unsigned char s_qrow[kMaxQ], s_qhead[kMaxQ];   // query -> (session row, head in group)
+    // the swizzled boxes want 1024-byte aligned destinations
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                            ~static_cast<uintptr_t>(1023));
 
     const int item = blockIdx.x;
     int s = 0;
@@ -370,61 +401,104 @@ __global__ void __launch_bounds__(kAttnThreads, 2) decode_attn_mma_kernel(const 
     const int Q = nrows * G;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, c = lane & 3;
+    const bool producer = warp == kMmaConsumers;
 
+    const int MT = (Q + 15) >> 4;               // 16-query tiles (1 or 2)
+    const int KS = kMmaConsumers / MT;          // warps sharing one query tile
     if (tid == 0) {
-        int lplan = 0;
-        for (int i = 0; i < nrows; ++i) lplan = max(lplan, P.row_keys_max[P.sess_rows[rb + i]]);
-        lplan = min(lplan, a.capacity);
-        const int p0 = piece * P.chunk, p1 = min(p0 + P.chunk, lplan);
-        if (p1 > p0) {
-            const int64_t off = (int64_t)P.row_region[P.sess_rows[rb]] * a.region_stride +
-                                ((int64_t)h * a.capacity + p0) * D;
-            dl_prefetch_l2(a.kc + off, (uint32_t)(p1 - p0) * D * 2u);
-            dl_prefetch_l2(a.vc + off, (uint32_t)(p1 - p0) * D * 2u);
+        for (int i = 0; i < S; ++i) {
+            dla::mbar_init(&full[i], 1);
+            dla::mbar_init(&empty[i], (uint32_t)MT);   // released by the query tiles' warps
         }
+        dla::mbar_init_fence();
     }
-    dl_pdl_launch_dependents();
-    dl_pdl_wait();
-
+    // the key counts come from the caller, not from the previous kernel: read them now
     if (tid < nrows) {
         const int r = P.sess_rows[rb + tid];
         s_row[tid] = r;
         s_len[tid] = clip_len(a.seqlen[r], P.row_keys_max[r], a.capacity, a.status, piece == 0 && h == 0);
     }
+    if (tid < Q) {
+        s_qrow[tid] = (unsigned char)(tid / G);
+        s_qhead[tid] = (unsigned char)(tid - (tid / G) * G);
+    }
     __syncthreads();
-    int lmax = 0;
-    for (int i = 0; i < nrows; ++i) lmax = max(lmax, s_len[i]);
+    int lmax = 0, lmin = 0x7fffffff;
+    for (int i = 0; i < nrows; ++i) {
+        lmax = max(lmax, s_len[i]);
+        lmin = min(lmin, s_len[i]);
+    }
     const int k0 = piece * P.chunk;
     const int k1 = min(k0 + P.chunk, lmax);
-    if (k0 >= k1) return;
+    if (k0 >= k1) return;                       // nothing of this piece is attended (no barrier pending)
+    const int nst = (k1 - k0 + kStKeys - 1) / kStKeys;
 
     const int reg = P.row_region[s_row[0]];
-    const uint16_t *kbase = a.kc + (int64_t)reg * a.region_stride + (int64_t)h * a.capacity * D;
-    const uint16_t *vbase = a.vc + (int64_t)reg * a.region_stride + (int64_t)h * a.capacity * D;
+    unsigned char *ring = smem;
+    unsigned char *qfrag = smem + (size_t)S * kStageBytes;
+    const uint32_t ring_s = dla::smem_u32(ring);
+    bool bad = false;
 
-    const int MT = (Q + 15) >> 4;          // 16-query tiles (1 or 2)
-    const int KS = 4 / MT;                 // warps sharing one query tile
-    const int mt = warp % MT, ksp = warp / MT;
-    const int nblk = (k1 - k0 + KB - 1) / KB;
-    const int b_begin = ksp * nblk / KS, b_end = (ksp + 1) * nblk / KS;
+    if (producer) {
+        if (lane == 0) {
+            dla::prefetch_tmap(&tk);
+            dla::prefetch_tmap(&tv);
+            // keys below the lowest slot this command writes are final before the previous kernel ends
+            const int stable = lmin - 1;
+            const int nstable = k1 <= stable ? nst : max(0, (stable - k0) / kStKeys);
+            bool waited = false;
+            int i = 0;
+            for (; i < nst; ++i) {
+                const int st = i % S;
+                if (i >= S && !dla::mbar_wait(&empty[st], (uint32_t)(((i / S) - 1) & 1))) {
+                    bad = true;
+                    break;
+                }
+                if (!waited && i >= nstable) {
+                    dl_pdl_wait();
+                    waited = true;
+                }
+                unsigned char *kd = ring + (size_t)st * kStageBytes;
+                unsigned char *vd = kd + kStageBytes / 2;
+                const int y = h * a.capacity + k0 + i * kStKeys;
+                dla::mbar_expect_tx(&full[st], kStageBytes);
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf) {
+                    dla::tma_g2s_3d(kd + hf * kHalfTile, &tk, hf * 64, y, reg, &full[st]);
+                    dla::tma_g2s_3d(vd + hf * kHalfTile, &tv, hf * 64, y, reg, &full[st]);
+                }
+            }
+            if (!waited) dl_pdl_wait();
+            if (bad) {
+                // leave no copy in flight: wait (bounded) for the stages issued last
+                for (int j = max(0, i - S); j < i; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
+            }
+        } else {
+            dl_pdl_wait();
+        }
+        dl_pdl_launch_dependents();
+        return;
+    }
 
+    dl_pdl_wait();
+    dl_pdl_launch_dependents();
+
+    const int mt = warp % MT, grp = warp / MT;
     // ---- query operand fragments (log2-domain scaled, hi + lo f16 terms) in shared memory:
     // [query tile][k-step][lane] 32 bytes = a0..a3 hi then a0..a3 lo
-    const int r0 = mt * 16 + g, r1 = r0 + 8;
-    unsigned char *qfrag = smem + (size_t)4 * 2 * 2 * BLK * 2;
-    for (int fi = tid; fi < MT * NKS * 32; fi += kAttnThreads) {
+    for (int fi = tid; fi < MT * NKS * 32; fi += kMmaConsumers * 32) {
         const int t = fi & 31, ks = (fi >> 5) % NKS, qt = (fi >> 5) / NKS;
         const int gg = t >> 2, cc = t & 3;
         const int q0i = qt * 16 + gg, q1i = q0i + 8;
-        const float *q0 = q0i < Q ? a.q + (int64_t)s_row[q0i / G] * a.q_stride + (h * G + q0i % G) * D : nullptr;
-        const float *q1 = q1i < Q ? a.q + (int64_t)s_row[q1i / G] * a.q_stride + (h * G + q1i % G) * D : nullptr;
+        const float *q0 = q0i < Q ? a.q + (int64_t)s_row[s_qrow[q0i]] * a.q_stride + (h * G + s_qhead[q0i]) * D : nullptr;
+        const float *q1 = q1i < Q ? a.q + (int64_t)s_row[s_qrow[q1i]] * a.q_stride + (h * G + s_qhead[q1i]) * D : nullptr;
         uint32_t hv[4], lv[4];
 #pragma unroll
         for (int part = 0; part < 4; ++part) {
             const float *src = (part & 1) ? q1 : q0;
             const int col = ks * 16 + 2 * cc + (part >> 1) * 8;
             float2 v = make_float2(0.f, 0.f);
-            if (src) v = *reinterpret_cast<const float2 *>(src + col);
+            if (src) v = __ldcg(reinterpret_cast<const float2 *>(src + col));
             v.x *= a.qscale;
             v.y *= a.qscale;
             const __half2 hq = __floats2half2_rn(v.x, v.y);
@@ -436,53 +510,42 @@ __global__ void __launch_bounds__(kAttnThreads, 2) decode_attn_mma_kernel(const 
         dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
         dst[1] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
     }
-    __syncthreads();
+    dla::named_sync(1, kMmaConsumers * 32);
     const unsigned char *myq = qfrag + (size_t)mt * NKS * 32 * 32 + lane * 32;
-    const int len0 = r0 < Q ? s_len[r0 / G] : 0;
-    const int len1 = r1 < Q ? s_len[r1 / G] : 0;
+    const int r0 = mt * 16 + g, r1 = r0 + 8;
+    const int len0 = r0 < Q ? s_len[s_qrow[r0]] : 0;
+    const int len1 = r1 < Q ? s_len[s_qrow[r1]] : 0;
 
     float o[NDT][4];
 #pragma unroll
     for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    uint16_t *ring = reinterpret_cast<uint16_t *>(smem) + warp * 2 * 2 * BLK;   // [stage][K, V][KB][D]
-    auto load_block = [&](int stage, int b) {
-        uint16_t *kd = ring + stage * 2 * BLK, *vd = kd + BLK;
-        const int kb0 = k0 + b * KB;
-#pragma unroll
-        for (int i = lane; i < KB * CPR; i += 32) {
-            const int key = i / CPR, ch = i - key * CPR;
-            const int off = key * D + ((ch ^ (key & 7)) << 3);
-            const int kk = kb0 + key;
-            if (kk < k1) {
-                cp_async16(kd + off, kbase + (int64_t)kk * D + ch * 8);
-                cp_async16(vd + off, vbase + (int64_t)kk * D + ch * 8);
-            } else {
-                *reinterpret_cast<uint4 *>(kd + off) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(vd + off) = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = grp; i < nst; i += KS) {
+        const int st = i % S;
+        if (!__all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((i / S) & 1)))) {
+            bad = true;
+            break;
+        }
+        const uint32_t ksm = ring_s + (uint32_t)st * kStageBytes;
+        const uint32_t vsm = ksm + kStageBytes / 2;
+        const int kb0 = k0 + i * kStKeys;
+        if (kb0 + kStKeys > k1) {
+            // keys past the piece may hold anything (even NaN) in the V rows: zero them
+            unsigned char *vrow = ring + (size_t)st * kStageBytes + kStageBytes / 2;
+            for (int e = lane; e < NH * kStKeys * 8; e += 32) {
+                const int hf = e / (kStKeys * 8), rem = e - hf * kStKeys * 8;
+                const int key = rem >> 3;
+                if (kb0 + key >= k1) *reinterpret_cast<uint4 *>(vrow + hf * kHalfTile + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
+            dla::fence_proxy_async();
+            __syncwarp();
         }
-        cp_async_commit();
-    };
 
-    if (b_begin < b_end) load_block(0, b_begin);
-    for (int b = b_begin; b < b_end; ++b) {
-        const int stage = (b - b_begin) & 1;
-        if (b + 1 < b_end) {
-            load_block(stage ^ 1, b + 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncwarp();
-        const uint32_t ksm = static_cast<uint32_t>(__cvta_generic_to_shared(ring + stage * 2 * BLK));
-        const uint32_t vsm = ksm + BLK * 2;
-
-        // scores of 16 keys: two 8-key column tiles, hi and lo terms in independent chains
-        float sc[2][4], sl[2][4];
+        // scores of 32 keys: four 8-key column tiles, hi and lo terms in independent chains
+        float sc[4][4], sl[4][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 4; ++nt) {
             sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
             sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
         }
@@ -494,32 +557,29 @@ __global__ void __launch_bounds__(kAttnThreads, 2) decode_attn_mma_kernel(const 
             const uint4 qd = *reinterpret_cast<const uint4 *>(myq + ((ks + 1) * 32) * 32 + 16);
             const uint32_t qh0[4] = {qa.x, qa.y, qa.z, qa.w}, ql0[4] = {qb.x, qb.y, qb.z, qb.w};
             const uint32_t qh1[4] = {qc.x, qc.y, qc.z, qc.w}, ql1[4] = {qd.x, qd.y, qd.z, qd.w};
+            const int ch = 2 * ks + (lane >> 3);                 // 16-byte chunk of the key row
+            const uint32_t half_off = (uint32_t)(ch >> 3) * kHalfTile;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < 4; ++nt) {
                 const int key = nt * 8 + (lane & 7);
-                const int ch = 2 * ks + (lane >> 3);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(b0, b1, b2, b3, ksm + (uint32_t)(key * D + ((ch ^ (key & 7)) << 3)) * 2u);
+                ldsm_x4(b0, b1, b2, b3, ksm + half_off + (uint32_t)(key * 128 + (((ch & 7) ^ (key & 7)) << 4)));
                 mma_f16(sc[nt], qh0, b0, b1);
                 mma_f16(sl[nt], ql0, b0, b1);
                 mma_f16(sc[nt], qh1, b2, b3);
                 mma_f16(sl[nt], ql1, b2, b3);
             }
         }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[nt][e] += sl[nt][e];
         // mask keys past each row's count, online softmax per row (quad of lanes = one row)
-        const int kb0 = k0 + b * KB;
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int key = kb0 + nt * 8 + 2 * c + e;
-                if (key >= len0) sc[nt][e] = -INFINITY;
-                if (key >= len1) sc[nt][2 + e] = -INFINITY;
+                const float v0 = sc[nt][e] + sl[nt][e], v1 = sc[nt][2 + e] + sl[nt][2 + e];
+                sc[nt][e] = key < len0 ? v0 : -INFINITY;
+                sc[nt][2 + e] = key < len1 ? v1 : -INFINITY;
                 mx0 = fmaxf(mx0, sc[nt][e]);
                 mx1 = fmaxf(mx1, sc[nt][2 + e]);
             }
@@ -530,55 +590,78 @@ __global__ void __launch_bounds__(kAttnThreads, 2) decode_attn_mma_kernel(const 
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
         const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
-        float ps[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            ps[nt][0] = sc[nt][0] == -INFINITY ? 0.f : exp2f(sc[nt][0] - mn0);
-            ps[nt][1] = sc[nt][1] == -INFINITY ? 0.f : exp2f(sc[nt][1] - mn0);
-            ps[nt][2] = sc[nt][2] == -INFINITY ? 0.f : exp2f(sc[nt][2] - mn1);
-            ps[nt][3] = sc[nt][3] == -INFINITY ? 0.f : exp2f(sc[nt][3] - mn1);
+        for (int nt = 0; nt < 4; ++nt) {
+            sc[nt][0] = sc[nt][0] == -INFINITY ? 0.f : exp2f(sc[nt][0] - mn0);
+            sc[nt][1] = sc[nt][1] == -INFINITY ? 0.f : exp2f(sc[nt][1] - mn0);
+            sc[nt][2] = sc[nt][2] == -INFINITY ? 0.f : exp2f(sc[nt][2] - mn1);
+            sc[nt][3] = sc[nt][3] == -INFINITY ? 0.f : exp2f(sc[nt][3] - mn1);
         }
-        l0 = l0 * al0 + (ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1]);
-        l1 = l1 * al1 + (ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3]);
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            ps0 += sc[nt][0] + sc[nt][1];
+            ps1 += sc[nt][2] + sc[nt][3];
+        }
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
         m0 = mn0;
         m1 = mn1;
         if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-            for (int i = 0; i < NDT; ++i) {
-                o[i][0] *= al0;
-                o[i][1] *= al0;
-                o[i][2] *= al1;
-                o[i][3] *= al1;
+            for (int j = 0; j < NDT; ++j) {
+                o[j][0] *= al0;
+                o[j][1] *= al0;
+                o[j][2] *= al1;
+                o[j][3] *= al1;
             }
         }
-        const uint32_t pa[4] = {h2_bits(ps[0][0], ps[0][1]), h2_bits(ps[0][2], ps[0][3]),
-                                h2_bits(ps[1][0], ps[1][1]), h2_bits(ps[1][2], ps[1][3])};
-        // O += P V: two 8-wide output tiles per transposed 4-matrix load
-        const int vkey = (lane & 7) + ((lane >> 3) & 1) * 8;
+        // O += P V over two 16-key steps: two 8-wide output tiles per transposed 4-matrix load
 #pragma unroll
-        for (int j = 0; j < NDT / 2; ++j) {
-            const int ch = 2 * j + (lane >> 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(b0, b1, b2, b3, vsm + (uint32_t)(vkey * D + ((ch ^ (vkey & 7)) << 3)) * 2u);
-            mma_f16(o[2 * j], pa, b0, b1);
-            mma_f16(o[2 * j + 1], pa, b2, b3);
+        for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t pa[4] = {h2_bits(sc[2 * kk][0], sc[2 * kk][1]), h2_bits(sc[2 * kk][2], sc[2 * kk][3]),
+                                    h2_bits(sc[2 * kk + 1][0], sc[2 * kk + 1][1]),
+                                    h2_bits(sc[2 * kk + 1][2], sc[2 * kk + 1][3])};
+            const int vkey = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int j = 0; j < NDT / 2; ++j) {
+                const int ch = 2 * j + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(b0, b1, b2, b3, vsm + (uint32_t)(ch >> 3) * kHalfTile +
+                                              (uint32_t)(vkey * 128 + (((ch & 7) ^ (vkey & 7)) << 4)));
+                mma_f16(o[2 * j], pa, b0, b1);
+                mma_f16(o[2 * j + 1], pa, b2, b3);
+            }
         }
         __syncwarp();
+        if (lane == 0) dla::mbar_arrive(&empty[st]);      // the stage is free for the producer
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-    // ---- combine the warps that share a query tile, then write this piece's partials
-    __syncthreads();                                   // every warp is done with its ring
+    const int ms = P.max_splits;
+    if (attn_consumers_any(bad)) {
+        // a stage never arrived: this piece's partials are marked invalid (NaN) for the merge
+        for (int e = tid; e < Q * D; e += kMmaConsumers * 32) {
+            const int qi = e / D, d = e - qi * D;
+            const int rq = s_qrow[qi], gq = s_qhead[qi];
+            if (s_len[rq] <= k0) continue;
+            const int64_t pidx = ((int64_t)s_row[rq] * P.n_q + h * G + gq) * ms + piece;
+            a.part_o[pidx * D + d] = __int_as_float(0x7fc00000);
+            if (d == 0) a.part_lse[pidx] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
+    // ---- combine the warps that share a query tile (the ring is idle now), then write partials
     float *co = reinterpret_cast<float *>(smem);       // [4 warps][16][D]
-    float *cm = co + 4 * 16 * D;                       // [4 warps][16]
-    float *cl = cm + 4 * 16;                           // [4 warps][16]
+    float *cm = co + kMmaConsumers * 16 * D;           // [4 warps][16]
+    float *cl = cm + kMmaConsumers * 16;               // [4 warps][16]
 #pragma unroll
-    for (int i = 0; i < NDT; ++i) {
-        *reinterpret_cast<float2 *>(co + (warp * 16 + g) * D + i * 8 + 2 * c) = make_float2(o[i][0], o[i][1]);
-        *reinterpret_cast<float2 *>(co + (warp * 16 + g + 8) * D + i * 8 + 2 * c) = make_float2(o[i][2], o[i][3]);
+    for (int j = 0; j < NDT; ++j) {
+        *reinterpret_cast<float2 *>(co + (warp * 16 + g) * D + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
+        *reinterpret_cast<float2 *>(co + (warp * 16 + g + 8) * D + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
     }
     if (c == 0) {
         cm[warp * 16 + g] = m0;
@@ -586,29 +669,43 @@ __global__ void __launch_bounds__(kAttnThreads, 2) decode_attn_mma_kernel(const 
         cl[warp * 16 + g] = l0;
         cl[warp * 16 + g + 8] = l1;
     }
-    __syncthreads();
-    const int ms = P.max_splits;
-    for (int e = tid; e < MT * 16 * D; e += kAttnThreads) {
-        const int qt = e / (16 * D), rem = e - qt * 16 * D;
-        const int row = rem / D, d = rem - row * D;
-        const int qi = qt * 16 + row;
-        if (qi >= Q) continue;
-        const int rq = qi / G, gq = qi - rq * G;
+    dla::named_sync(1, kMmaConsumers * 32);
+    // one query per warp at a time, lanes over the dimensions (4 each)
+    for (int qi = warp; qi < Q; qi += kMmaConsumers) {
+        const int rq = s_qrow[qi], gq = s_qhead[qi];
         if (s_len[rq] <= k0) continue;
+        const int qt = qi >> 4, row = qi & 15;
         float M = -INFINITY;
         for (int kq = 0; kq < KS; ++kq) M = fmaxf(M, cm[(kq * MT + qt) * 16 + row]);
-        float wsum = 0.f, acc = 0.f;
-        for (int kq = 0; kq < KS; ++kq) {
-            const int w = kq * MT + qt;
-            const float mw = cm[w * 16 + row];
-            const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-            wsum += f * cl[w * 16 + row];
-            acc += f * co[(w * 16 + row) * D + d];
+        float f[kMmaConsumers], wsum = 0.f;
+#pragma unroll
+        for (int kq = 0; kq < kMmaConsumers; ++kq) {
+            f[kq] = 0.f;
+            if (kq < KS) {
+                const int w = kq * MT + qt;
+                const float mw = cm[w * 16 + row];
+                f[kq] = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                wsum += f[kq] * cl[w * 16 + row];
+            }
         }
-        const int r = s_row[rq], head = h * G + gq;
-        const int64_t pidx = ((int64_t)r * P.n_q + head) * ms + piece;
-        a.part_o[pidx * D + d] = acc / wsum;
-        if (d == 0) a.part_lse[pidx] = (M + log2f(wsum)) * 0.69314718055994530942f;
+        const float inv = 1.f / wsum;
+        const int64_t pidx = ((int64_t)s_row[rq] * P.n_q + h * G + gq) * ms + piece;
+        for (int d4 = lane; d4 < D / 4; d4 += 32) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int kq = 0; kq < kMmaConsumers; ++kq) {
+                if (kq < KS) {
+                    const float4 v = *reinterpret_cast<const float4 *>(co + ((kq * MT + qt) * 16 + row) * D + d4 * 4);
+                    acc.x = fmaf(f[kq], v.x, acc.x);
+                    acc.y = fmaf(f[kq], v.y, acc.y);
+                    acc.z = fmaf(f[kq], v.z, acc.z);
+                    acc.w = fmaf(f[kq], v.w, acc.w);
+                }
+            }
+            *reinterpret_cast<float4 *>(a.part_o + pidx * D + d4 * 4) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        }
+        if (lane == 0) a.part_lse[pidx] = (M + log2f(wsum)) * 0.69314718055994530942f;
     }
 }
 
@@ -621,16 +718,20 @@ struct MergeArgs {
     int row_keys_max[DL_MAX_ROWS];
 };
 
-// One CTA per (row, head); its four warps take every fourth piece, so the pieces'
-// loads are in flight together, and combine their sums in shared memory.
+// One CTA per (row, head); its eight warps take every eighth piece and issue the loads of
+// their pieces' (lse, o) together, each warp keeping its own running maximum, so that the
+// partials cross from L2 in one round; the warps' sums are combined in shared memory.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 8;     // pieces a warp has in flight per pass
+
 template <int D>
-__global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__ MergeArgs a)
+__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const __grid_constant__ MergeArgs a)
 {
     constexpr int VPL = D / 32;              // values per lane
-    __shared__ float s_acc[4][D];
-    __shared__ float s_w[4];
-    dl_pdl_launch_dependents();
+    __shared__ float s_acc[kMergeWarps][D];
+    __shared__ float s_m[kMergeWarps], s_w[kMergeWarps];
     dl_pdl_wait();
+    dl_pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x / a.n_q, h = blockIdx.x - (blockIdx.x / a.n_q) * a.n_q;
     const int L = clip_len(a.seqlen[r], a.row_keys_max[r], a.capacity, nullptr, false);
@@ -638,52 +739,72 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__
     const float *pl = a.part_lse + ((int64_t)r * a.n_q + h) * a.max_splits;
     float *dst = a.out + r * a.out_stride + h * D;
     if (np == 0) {
-        for (int d = threadIdx.x; d < D; d += 128) dst[d] = 0.f;
+        for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) dst[d] = 0.f;
         if (a.lse && threadIdx.x == 0) a.lse[r * a.n_q + h] = -INFINITY;
         return;
     }
-    float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, pl[p]);
-    M = warp_max(M);
-    float acc[VPL];
+    const float *po = a.part_o + ((int64_t)r * a.n_q + h) * a.max_splits * D + lane * VPL;
+    float Mw = -INFINITY, Ww = 0.f, acc[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
-    float W = 0.f;
-    const float *po = a.part_o + ((int64_t)r * a.n_q + h) * a.max_splits * D + lane * VPL;
-    for (int p0 = warp; p0 < np; p0 += 16) {
-        float w[4], v[4][VPL];
+    for (int p0 = warp; p0 < np; p0 += kMergeWarps * kMergeBatch) {
+        float lv[kMergeBatch], v[kMergeBatch][VPL];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int p = p0 + 4 * u;
-            w[u] = 0.f;
+        for (int u = 0; u < kMergeBatch; ++u) {
+            const int p = p0 + kMergeWarps * u;
+            lv[u] = -INFINITY;
 #pragma unroll
             for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
             if (p < np) {
-                w[u] = __expf(pl[p] - M);
+                lv[u] = __ldcg(pl + p);
                 if constexpr (VPL == 4) {
-                    const float4 t = *reinterpret_cast<const float4 *>(po + (int64_t)p * D);
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)p * D));
                     v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
                 } else {
-                    const float2 t = *reinterpret_cast<const float2 *>(po + (int64_t)p * D);
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(po + (int64_t)p * D));
                     v[u][0] = t.x; v[u][1] = t.y;
                 }
             }
         }
+        float mb = Mw;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            W += w[u];
+        for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, lv[u]);
+        const float sc = Mw == -INFINITY ? 0.f : __expf(Mw - mb);
+        Ww *= sc;
 #pragma unroll
-            for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
+        for (int i = 0; i < VPL; ++i) acc[i] *= sc;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            const float w = lv[u] == -INFINITY ? 0.f : __expf(lv[u] - mb);
+            Ww += w;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w, v[u][i], acc[i]);
         }
+        Mw = mb;
     }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) s_acc[warp][lane * VPL + i] = acc[i];
-    if (lane == 0) s_w[warp] = W;
+    if (lane == 0) {
+        s_m[warp] = Mw;
+        s_w[warp] = Ww;
+    }
     __syncthreads();
-    const float Wt = s_w[0] + s_w[1] + s_w[2] + s_w[3];
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_m[w]);
+    float f[kMergeWarps], Wt = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) {
+        f[w] = s_m[w] == -INFINITY ? 0.f : __expf(s_m[w] - M);
+        Wt += f[w] * s_w[w];
+    }
     const float inv = 1.f / Wt;
-    for (int d = threadIdx.x; d < D; d += 128)
-        dst[d] = (s_acc[0][d] + s_acc[1][d] + s_acc[2][d] + s_acc[3][d]) * inv;
+    for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) t = fmaf(f[w], s_acc[w][d], t);
+        dst[d] = t * inv;
+    }
     if (a.lse && threadIdx.x == 0) a.lse[r * a.n_q + h] = M + logf(Wt);
 }
 
@@ -691,6 +812,41 @@ size_t attn_smem_bytes(int D)
 {
     const int pitch = D + 8;
     return (size_t)4 * kTile * pitch * 2 + (size_t)kMaxQ * D * 4 + (size_t)kMaxQ * kTile * 4 + 3 * kMaxQ * 4;
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link against the driver).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of one cache plane as [region][kv_head * capacity + slot][head_dim] f16, read in
+// boxes of 32 slots x 64 dims with the 128-byte swizzle; slots past the plane read as zero.
+int make_kv_tmap(CUtensorMap *m, const uint16_t *plane, const dl_kv_cache *kv)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+    if (!enc) return dl::fail(DL_E_CUDA, "dl_decode_attn: the driver offers no tensor-map encoder");
+    const cuuint64_t dims[3] = {(cuuint64_t)kv->head_dim, (cuuint64_t)kv->n_kv * (cuuint64_t)kv->capacity,
+                                (cuuint64_t)kv->n_regions};
+    const cuuint64_t strides[2] = {(cuuint64_t)kv->head_dim * 2u, (cuuint64_t)kv->region_stride * 2u};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)kStKeys, 1u};
+    const cuuint32_t es[3] = {1u, 1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(plane), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return dl::fail(DL_E_ARG, "dl_decode_attn: cache plane refused as a tensor map (%d)", (int)r);
+    return DL_OK;
 }
 
 int check_plan(const dl_attn_plan *P)
@@ -844,11 +1000,23 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     for (int si = 0; si < plan->n_sessions; ++si)
         qmax = std::max(qmax, (plan->sess_begin[si + 1] - plan->sess_begin[si]) * (plan->n_q / plan->n_kv));
     const bool mma = path == 2 || (path == 0 && qmax > kCudaCoreMaxQ);
-    const size_t smem = mma ? attn_mma_smem_bytes(plan->head_dim) : attn_smem_bytes(plan->head_dim);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    auto kern = mma ? (plan->head_dim == 128 ? decode_attn_mma_kernel<128> : decode_attn_mma_kernel<64>)
-                    : (plan->head_dim == 128 ? decode_attn_cc_kernel<128> : decode_attn_cc_kernel<64>);
+    if (mma) {
+        CUtensorMap tk, tv;
+        rc = make_kv_tmap(&tk, kv->k, kv);
+        if (rc != DL_OK) return rc;
+        rc = make_kv_tmap(&tv, kv->v, kv);
+        if (rc != DL_OK) return rc;
+        const size_t smem = attn_mma_smem_bytes(plan->head_dim);
+        auto kern = plan->head_dim == 128 ? decode_attn_mma_kernel<128> : decode_attn_mma_kernel<64>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
+        return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kMmaThreads), smem, st, "dl_decode_attn: launch", a, tk,
+                              tv);
+    }
+    const size_t smem = attn_smem_bytes(plan->head_dim);
+    auto kern = plan->head_dim == 128 ? decode_attn_cc_kernel<128> : decode_attn_cc_kernel<64>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
     return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kAttnThreads), smem, st, "dl_decode_attn: launch", a);
@@ -895,7 +1063,7 @@ int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t
     const unsigned grid = (unsigned)(plan->rows * plan->n_q);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto kern = plan->head_dim == 128 ? attn_merge_kernel<128> : attn_merge_kernel<64>;
-    return dl::launch_pdl(kern, dim3(grid), dim3(128), 0, st, "dl_attn_merge: launch", m);
+    return dl::launch_pdl(kern, dim3(grid), dim3(kMergeWarps * 32), 0, st, "dl_attn_merge: launch", m);
 }
 
 }  // extern "C"

@@ -54,7 +54,10 @@ inline int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 
 // Device side: wait for the previous kernel of the stream (no-op without PDL).
 __device__ __forceinline__ void dl_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Device side: let the next kernel of the stream begin launching.
+// Device side: let the next kernel of the stream begin launching.  Every kernel of the library
+// calls this only after its own dl_pdl_wait(), so a kernel that starts early may rely on every
+// kernel before its immediate predecessor having finished (the attention loads the cache slots
+// that its predecessor does not write before waiting on it).
 __device__ __forceinline__ void dl_pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 // Device side: ask L2 to fetch [p, p + bytes) (16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void dl_prefetch_l2(const void *p, uint32_t bytes)

@@ -3,43 +3,47 @@
 // router launch": eight activation columns per launch, longer launches tiled).
 //
 // Device weight form: tiles of 16 output rows x 32 inputs (one Q8_0 block per
-// row), 512 bytes each, in the A-operand order of the 16x8x32 int8 tensor-core
-// product: lane t = 4g + c owns 16 bytes = row g at inputs 4c..4c+3, row g+8 at
-// the same inputs, row g at 16+4c..16+4c+3, row g+8 at those.  The tiles of one
-// row tile are contiguous along K.  Scales: per 16 rows and 4 tiles, 128 bytes;
-// lane group g reads 16 bytes = (d[g], d[g+8]) for the 4 tiles.
+// row), 512 bytes each, in the A-operand order of two 16x8x16 f16 tensor-core
+// products, as biased bytes u = q + 128.  Lane t = 4g + c owns 16 bytes; word p
+// (p = 0..3) covers inputs kb = 16(p/2) + 8(p%2) + 2c and kb + 1 of row g (bytes
+// 0, 1) and of row g + 8 (bytes 2, 3).  One byte permute turns two bytes into the
+// f16 pair (1024 + u) = (1152 + q), exact.  The tiles of one row tile are
+// contiguous along K.  Scales: per 16 rows and 4 tiles, 128 bytes; lane group g
+// reads 16 bytes = (d[g], d[g+8]) for the 4 tiles.
 //
-// Kernel shape:
+// Kernel shape (one CTA per SM, one wave):
 //  * a CTA = one producer warp + 8 consumer warps owns a run of row tiles and one
 //    K-slice; the producer streams one row tile's slice (weights, then scales: two
-//    contiguous bulk copies) into each stage of a shared-memory ring, tracked by
-//    mbarriers, and issues the first stages before waiting on the previous kernel
-//    (programmatic dependent launch);
+//    contiguous bulk copies) into each stage of a shared-memory ring of about
+//    96 KB, tracked by mbarriers, and issues the ring before waiting on the
+//    previous kernel (programmatic dependent launch);
 //  * each consumer warp owns an eighth of the slice's k-tiles; its activations are
 //    loaded once and kept in registers as operands for the whole launch;
-//  * per row tile each warp adds its k-tiles into a 16x8 accumulator and parks it
-//    in shared memory; the warps' partials are summed once at the end in a fixed
-//    order, and the K-slices of a thread-block cluster through distributed shared
-//    memory in rank order (no atomics: results do not depend on timing).
-// Two inner products share this shape.  Tensor path: the int8 weights enter
-// 16x8x32 int8 products as they are; each activation row is quantised per warp to
-// two int8 terms, x ~ s (h + l/254) with s = max|x|/127, so that both products are
-// exact in int32 and 254 h-sum + l-sum is formed exactly before one conversion to
-// f32 (activation error <= max|x| / 64516 per element).  CUDA-core path: the
-// weights are widened to f32 and multiplied with the f32 activations by FMAs.
+//  * after each stage the 8 warps' partial 16x8 tiles are summed, in warp order, by
+//    one owner warp (stage index mod 8); the K-slices of a thread-block cluster are
+//    summed through distributed shared memory in rank order at the end (no
+//    atomics: results do not depend on timing).
+// Two inner products share this shape.  Tensor path: the f16 weights (1152 + q)
+// enter 16x8x16 f16 products with f32 accumulation; each activation row is scaled
+// per warp by a power of two (largest |x| into [2^14, 2^15)) and split into two f16
+// terms hi + lo (about 22 significant bits); the products' bias 1152 * sum(x) is
+// taken off per block and column, and the scale undone per column at the end.
+// CUDA-core path (1 or 2 rows): the weights are widened to f32 and multiplied with
+// the f32 activations by FMAs.
 #include <cuda_fp16.h>
 #include <cstdio>
-#include <type_traits>
+#include <mutex>
 
 #include "dl_common.cuh"
+#include "dl_async.cuh"
 
 namespace {
 
 enum { PATH_AUTO = 0, PATH_CUDA_CORE = 1, PATH_TENSOR = 2 };
 
 struct GemvArgs {
-    const uint4 *qs;        // packed weight tiles
-    const uint32_t *d;      // packed scales as (d[g], d[g+8]) pairs
+    const unsigned char *qs;   // packed weight tiles
+    const unsigned char *d;    // packed scales as (d[g], d[g+8]) pairs
     const float *x;
     float *y;
     int64_t x_stride, y_stride;
@@ -51,124 +55,84 @@ struct GemvArgs {
     int ksl;                // k-tiles per K-slice (multiple of 4)
     int rpr;                // row tiles per CTA
     int stages;             // ring depth
+    int l2pf;               // stages past the ring prefetched into L2 before the wait
 };
 
 constexpr int kConsumers = 8;                        // consumer warps, each a share of the K-slice
 constexpr int kThreads = (kConsumers + 1) * 32;      // and one producer warp
 constexpr int kMaxStages = 8;
+constexpr int kStageTileBytes = 512 + 32;            // weights and scales of one k-tile
+constexpr size_t kRedBytes = (size_t)2 * kConsumers * 128 * 4;   // per-stage partials, two buffers
 
-// ---- cluster and shared-memory helpers
-__device__ __forceinline__ void cluster_sync_all()
+// Shared-memory bytes of a launch: the ring, the per-stage partials and, with clusters,
+// this CTA's K-slice sums of its row tiles.
+size_t gemv_smem(int ksl, int stages, int rpr, int cs)
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
-{
-    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-// ---- asynchronous bulk copies into shared memory, tracked by mbarriers
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-    return ok != 0;
-}
-// Bounded wait: false if the phase never completed (the caller then stops using the stage).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
-{
-    for (int spin = 0; spin < (1 << 22); ++spin)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+    return (size_t)stages * ksl * kStageTileBytes + kRedBytes + (cs > 1 ? (size_t)rpr * 128 * 4 : 0);
 }
 
 // ---- arithmetic helpers
-// stored weight byte `sel` of w (int8) to float, through the biased byte q + 128 placed in
-// the low mantissa of 2^23 (2^23 + 128 subtracted)
-__device__ __forceinline__ float s8_to_f32(uint32_t w, uint32_t sel)
+// biased weight byte `sel` of w (u = q + 128) to the float q, through u placed in the low
+// mantissa of 2^23
+__device__ __forceinline__ float u8_to_f32(uint32_t w, uint32_t sel)
 {
-    return __uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | sel)) - 8388736.0f;
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | sel)) - 8388736.0f;
 }
-__device__ __forceinline__ void imma16832(int &c0, int &c1, int &c2, int &c3, const uint4 &a, uint32_t b0, uint32_t b1)
+// two biased bytes (0, 1 or 2, 3) of w to the f16 pair (1024 + u)
+__device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t w, uint32_t sel)
 {
-    asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    return __byte_perm(w, 0x64646464u, sel);
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
                  "{%0,%1,%2,%3};"
-                 : "+r"(c0), "+r"(c1), "+r"(c2), "+r"(c3)
-                 : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d)
-{
-    return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) | ((uint32_t)(d & 0xFF) << 24);
-}
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-// Shared-memory bytes of a launch: a ring of `stages` row-tile stages of `ksl` k-tiles (weights
-// then scales), per-warp partials of `rpr` row tiles, and the cluster partials.
-size_t gemv_smem(int ksl, int stages, int rpr)
+// OR of `flag` over the consumer warps, at a barrier they all reach (uniform result).
+__device__ __forceinline__ bool consumers_any(bool flag)
 {
-    const size_t sb = (size_t)ksl * 512 + (size_t)ksl * 32;
-    return (size_t)stages * sb + (size_t)rpr * kConsumers * 128 * 4 + (size_t)rpr * 128 * 4;
+    uint32_t r;
+    asm volatile("{\n .reg .pred pin, pout;\n setp.ne.u32 pin, %1, 0;\n"
+                 " bar.red.or.pred pout, 1, %2, pin;\n selp.u32 %0, 1, 0, pout;\n}"
+                 : "=r"(r) : "r"((uint32_t)flag), "r"((uint32_t)(kConsumers * 32)) : "memory");
+    return r != 0;
 }
 
 template <bool MMA, int NRC, int KWM>
-__global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
+__global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
-    __shared__ int s_fail;
+    __shared__ int s_shape_bad;
 
     const int S = a.stages;
     const int slice = blockIdx.x % a.cs;
     const int rt0 = (blockIdx.x / a.cs) * a.rpr;
     const int nrt = max(0, min(a.rpr, a.RT - rt0));      // row tiles of this CTA
     const int kt0 = slice * a.ksl, kt1 = min(a.KT, kt0 + a.ksl);
-    const int nkt = kt1 - kt0;
+    const int nkt = max(0, kt1 - kt0);
     const uint32_t wbytes = (uint32_t)nkt * 512u, dbytes = (uint32_t)nkt * 32u;
-    const size_t SB = (size_t)a.ksl * 544;
+    const size_t SB = (size_t)a.ksl * kStageTileBytes;
     unsigned char *ring = smem;
-    float *red = reinterpret_cast<float *>(smem + S * SB);          // [kConsumers][rpr][128]
-    float *cpart = red + kConsumers * a.rpr * 128;                  // [rpr][128]
+    float *red = reinterpret_cast<float *>(smem + S * SB);          // [2][kConsumers][128]
+    float *part = red + 2 * kConsumers * 128;                       // [rpr][128] (clusters)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int KG = a.KT >> 2;
     const bool producer = warp == kConsumers;
-    const unsigned char *qs = reinterpret_cast<const unsigned char *>(a.qs);
-    const unsigned char *dp = reinterpret_cast<const unsigned char *>(a.d);
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < S; ++st) {
-            mbar_init(&full[st], 1);
-            mbar_init(&empty[st], kConsumers);
+            dla::mbar_init(&full[st], 1);
+            dla::mbar_init(&empty[st], kConsumers);
         }
-        s_fail = 0;
-        mbar_init_fence();
+        s_shape_bad = 0;
+        dla::mbar_init_fence();
     }
     __syncthreads();
 
@@ -177,142 +141,177 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         const int st = j % S;
         const int rt = rt0 + j;
         unsigned char *dst = ring + st * SB;
-        mbar_expect_tx(&full[st], wbytes + dbytes);
-        bulk_g2s(dst, qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
-        bulk_g2s(dst + (size_t)a.ksl * 512, dp + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
+        dla::mbar_expect_tx(&full[st], wbytes + dbytes);
+        dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
+        dla::bulk_g2s(dst + (size_t)a.ksl * 512, a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
     };
-    // the weights do not depend on the previous kernel: start the ring before waiting on it
-    if (producer && lane == 0)
-        for (int j = 0; j < S && j < nrt; ++j) issue(j);
-    dl_pdl_launch_dependents();
+    int issued = 0;
+    // the weights do not depend on the previous kernel: fill the ring before waiting on it
+    if (producer && lane == 0) {
+        for (; issued < S && issued < nrt; ++issued) issue(issued);
+        const int pf_end = min(nrt, S + a.l2pf);
+        for (int j = S; j < pf_end; ++j) {
+            const int rt = rt0 + j;
+            dl_prefetch_l2(a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes);
+            dl_prefetch_l2(a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes);
+        }
+    }
+    // every thread waits before the next kernel may launch: kernels after this one can rely
+    // on everything before this one having finished
     dl_pdl_wait();
+    dl_pdl_launch_dependents();
 
     // ---- this warp's share of the slice and its activations, kept in registers
     const int wk0 = (warp * nkt) / kConsumers, wk1 = ((warp + 1) * nkt) / kConsumers;   // slice-local
     const int nw = producer ? 0 : min(wk1 - wk0, KWM);
-    if (!producer && lane == 0 && wk1 - wk0 > KWM) atomicExch(&s_fail, 1);   // launch shape broken: poison
-    float xv[KWM][NRC][8];
-#pragma unroll
-    for (int j = 0; j < KWM; ++j) {
-        const int kt = kt0 + wk0 + j;
-        const bool live = j < nw && kt * 32 < a.n_in;
-#pragma unroll
-        for (int r = 0; r < NRC; ++r) {
-            const int row = MMA ? g : r;
-            const bool ok = live && row < a.nr;
-            float4 lo4 = make_float4(0.f, 0.f, 0.f, 0.f), hi4 = lo4;
-            if (ok) {
-                const float *xr = a.x + (int64_t)row * a.x_stride + kt * 32;
-                lo4 = __ldg(reinterpret_cast<const float4 *>(xr + 4 * c));
-                hi4 = __ldg(reinterpret_cast<const float4 *>(xr + 16 + 4 * c));
-            }
-            xv[j][r][0] = lo4.x; xv[j][r][1] = lo4.y; xv[j][r][2] = lo4.z; xv[j][r][3] = lo4.w;
-            xv[j][r][4] = hi4.x; xv[j][r][5] = hi4.y; xv[j][r][6] = hi4.z; xv[j][r][7] = hi4.w;
-        }
-    }
-    // tensor path: activation row g quantised over this warp's inputs to two int8 terms,
-    // x ~ s (h + l/254); the products' scale s/254 is applied per accumulator column at the end
-    uint32_t bh[KWM][2], bl[KWM][2];
-    float cs0 = 0.f, cs1 = 0.f;
+    if (!producer && lane == 0 && wk1 - wk0 > KWM) atomicExch(&s_shape_bad, 1);   // broken launch shape
+    // lane (g, c) holds inputs 2c, 2c+1 / 8+2c, 9+2c / 16+2c, 17+2c / 24+2c, 25+2c of each k-tile
+    uint32_t bh[MMA ? KWM : 1][4], bl[MMA ? KWM : 1][4];
+    float2 ncorr[MMA ? KWM : 1];                 // -1152 * sum(x) of columns 2c, 2c+1 per k-tile
+    float xv[MMA ? 1 : KWM][NRC][8];
+    float us0 = 1.f, us1 = 1.f;
     if constexpr (MMA) {
+        float2 v[KWM][4];
         float m = 0.f;
 #pragma unroll
-        for (int j = 0; j < KWM; ++j)
+        for (int j = 0; j < KWM; ++j) {
+            const int kt = kt0 + wk0 + j;
+            const bool live = j < nw && kt * 32 < a.n_in && g < a.nr;
+            const float *xr = a.x + (int64_t)g * a.x_stride + kt * 32 + 2 * c;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(xv[j][0][e]));
+            for (int p = 0; p < 4; ++p) {
+                v[j][p] = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
+                               : make_float2(0.f, 0.f);
+                m = fmaxf(m, fmaxf(fabsf(v[j][p].x), fabsf(v[j][p].y)));
+            }
+        }
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        const float s = m / 127.f;
-        const float inv = m > 0.f ? 127.f / m : 0.f;
+        // power-of-two scale of activation row g over this warp's inputs: largest |x| into [2^14, 2^15)
+        float sig = 1.f;
+        if (m > 0.f) {
+            int e;
+            frexpf(m, &e);
+            sig = ldexpf(1.f, min(15 - e, 126));
+        }
 #pragma unroll
-        for (int j = 0; j < KWM; ++j)
+        for (int j = 0; j < KWM; ++j) {
+            float colsum = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                int hq[4], lq[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float t = fminf(fmaxf(xv[j][0][4 * half + e] * inv, -127.f), 127.f);
-                    const float hr = rintf(t);
-                    hq[e] = (int)hr;
-                    lq[e] = (int)rintf((t - hr) * 254.f);
-                }
-                bh[j][half] = pack_s8x4(hq[0], hq[1], hq[2], hq[3]);
-                bl[j][half] = pack_s8x4(lq[0], lq[1], lq[2], lq[3]);
+            for (int p = 0; p < 4; ++p) {
+                const float tx = v[j][p].x * sig, ty = v[j][p].y * sig;
+                const __half2 h = __floats2half2_rn(tx, ty);
+                const float2 hf = __half22float2(h);
+                const __half2 l = __floats2half2_rn(tx - hf.x, ty - hf.y);
+                const float2 lf = __half22float2(l);
+                bh[j][p] = h2_bits(h);
+                bl[j][p] = h2_bits(l);
+                colsum += (hf.x + lf.x) + (hf.y + lf.y);
             }
-        // accumulator columns of this lane are rows 2c and 2c+1 (held by lanes 8c and 8c+4)
-        const float sc = s / 254.f;
-        cs0 = __shfl_sync(0xffffffffu, sc, 8 * c);
-        cs1 = __shfl_sync(0xffffffffu, sc, 8 * c + 4);
+            colsum += __shfl_xor_sync(0xffffffffu, colsum, 1);
+            colsum += __shfl_xor_sync(0xffffffffu, colsum, 2);
+            // accumulator columns of this lane are activation rows 2c and 2c+1 (lanes 8c, 8c+4)
+            ncorr[j] = make_float2(-1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c),
+                                   -1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c + 4));
+        }
+        const float inv = 1.f / sig;
+        us0 = __shfl_sync(0xffffffffu, inv, 8 * c);
+        us1 = __shfl_sync(0xffffffffu, inv, 8 * c + 4);
+    } else {
+#pragma unroll
+        for (int j = 0; j < KWM; ++j) {
+            const int kt = kt0 + wk0 + j;
+#pragma unroll
+            for (int r = 0; r < NRC; ++r) {
+                const bool live = j < nw && kt * 32 < a.n_in && r < a.nr;
+                const float *xr = a.x + (int64_t)r * a.x_stride + kt * 32 + 2 * c;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const float2 t = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
+                                          : make_float2(0.f, 0.f);
+                    xv[j][r][2 * p] = t.x;
+                    xv[j][r][2 * p + 1] = t.y;
+                }
+            }
+        }
     }
 
+    bool bad = false;
     if (producer) {
         // refill each stage once every consumer warp has released it
         if (lane == 0) {
-            for (int j = S; j < nrt; ++j) {
-                const int st = j % S;
-                if (!mbar_wait(&empty[st], (uint32_t)(((j / S) - 1) & 1))) {
-                    atomicExch(&s_fail, 1);
+            for (; issued < nrt; ++issued) {
+                const int st = issued % S;
+                if (!dla::mbar_wait(&empty[st], (uint32_t)(((issued / S) - 1) & 1))) {
+                    bad = true;
                     break;
                 }
-                issue(j);
+                issue(issued);
             }
         }
     } else {
         for (int i = 0; i < nrt; ++i) {
             const int st = i % S;
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (uint32_t)((i / S) & 1)))) {
-                if (lane == 0) atomicExch(&s_fail, 1);
-                break;
-            }
+            const bool ok = __all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((i / S) & 1)));
             const unsigned char *sw = ring + st * SB;
             const unsigned char *sd = sw + (size_t)a.ksl * 512;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);   // rows g, g+8
             float accg[NRC], acch[NRC];
 #pragma unroll
             for (int r = 0; r < NRC; ++r) accg[r] = acch[r] = 0.f;
+            if (ok) {
 #pragma unroll
-            for (int j = 0; j < KWM; ++j) {
-                if (j >= nw) break;
-                const int kl = wk0 + j;                                  // slice-local k-tile
-                const uint4 w = *reinterpret_cast<const uint4 *>(sw + kl * 512 + lane * 16);
-                const uint32_t sp = *reinterpret_cast<const uint32_t *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4);
-                const float dg = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
-                const float dh = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
-                if constexpr (MMA) {
-                    int h0 = 0, h1 = 0, h2 = 0, h3 = 0, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
-                    imma16832(h0, h1, h2, h3, w, bh[j][0], bh[j][1]);
-                    imma16832(l0, l1, l2, l3, w, bl[j][0], bl[j][1]);
-                    // 254 h-sum + l-sum is exact in int32 (|h-sum| <= 32*127*127)
-                    acc[0] = fmaf(dg, (float)(h0 * 254 + l0), acc[0]);
-                    acc[1] = fmaf(dg, (float)(h1 * 254 + l1), acc[1]);
-                    acc[2] = fmaf(dh, (float)(h2 * 254 + l2), acc[2]);
-                    acc[3] = fmaf(dh, (float)(h3 * 254 + l3), acc[3]);
-                } else {
-                    // row g: words 0 and 2; row g+8: words 1 and 3
-                    float wg[8], wh[8];
-                    wg[0] = s8_to_f32(w.x, 0); wg[1] = s8_to_f32(w.x, 1); wg[2] = s8_to_f32(w.x, 2); wg[3] = s8_to_f32(w.x, 3);
-                    wg[4] = s8_to_f32(w.z, 0); wg[5] = s8_to_f32(w.z, 1); wg[6] = s8_to_f32(w.z, 2); wg[7] = s8_to_f32(w.z, 3);
-                    wh[0] = s8_to_f32(w.y, 0); wh[1] = s8_to_f32(w.y, 1); wh[2] = s8_to_f32(w.y, 2); wh[3] = s8_to_f32(w.y, 3);
-                    wh[4] = s8_to_f32(w.w, 0); wh[5] = s8_to_f32(w.w, 1); wh[6] = s8_to_f32(w.w, 2); wh[7] = s8_to_f32(w.w, 3);
+                for (int j = 0; j < KWM; ++j) {
+                    if (j >= nw) break;
+                    const int kl = wk0 + j;                                  // slice-local k-tile
+                    const uint4 w = *reinterpret_cast<const uint4 *>(sw + kl * 512 + lane * 16);
+                    const __half2 sp = *reinterpret_cast<const __half2 *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4);
+                    const float2 dgh = __half22float2(sp);          // (d[g], d[g+8])
+                    const float dg = dgh.x, dh = dgh.y;
+                    if constexpr (MMA) {
+                        float t[4] = {0.f, 0.f, 0.f, 0.f};
+                        const uint32_t a0 = u8x2_to_h2(w.x, 0x4140u), a1 = u8x2_to_h2(w.x, 0x4342u);
+                        const uint32_t a2 = u8x2_to_h2(w.y, 0x4140u), a3 = u8x2_to_h2(w.y, 0x4342u);
+                        mma16816(t, a0, a1, a2, a3, bh[j][0], bh[j][1]);
+                        mma16816(t, a0, a1, a2, a3, bl[j][0], bl[j][1]);
+                        const uint32_t a4 = u8x2_to_h2(w.z, 0x4140u), a5 = u8x2_to_h2(w.z, 0x4342u);
+                        const uint32_t a6 = u8x2_to_h2(w.w, 0x4140u), a7 = u8x2_to_h2(w.w, 0x4342u);
+                        mma16816(t, a4, a5, a6, a7, bh[j][2], bh[j][3]);
+                        mma16816(t, a4, a5, a6, a7, bl[j][2], bl[j][3]);
+                        acc01 = __ffma2_rn(make_float2(dg, dg), __fadd2_rn(make_float2(t[0], t[1]), ncorr[j]), acc01);
+                        acc23 = __ffma2_rn(make_float2(dh, dh), __fadd2_rn(make_float2(t[2], t[3]), ncorr[j]), acc23);
+                    } else {
+                        // row g: bytes 0, 1 of each word; row g+8: bytes 2, 3
+                        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+                        float wg[8], wh[8];
 #pragma unroll
-                    for (int r = 0; r < NRC; ++r) {
-                        float sg = wg[0] * xv[j][r][0], sh = wh[0] * xv[j][r][0];
-#pragma unroll
-                        for (int e = 1; e < 8; ++e) {
-                            sg = fmaf(wg[e], xv[j][r][e], sg);
-                            sh = fmaf(wh[e], xv[j][r][e], sh);
+                        for (int p = 0; p < 4; ++p) {
+                            wg[2 * p] = u8_to_f32(wd[p], 0);
+                            wg[2 * p + 1] = u8_to_f32(wd[p], 1);
+                            wh[2 * p] = u8_to_f32(wd[p], 2);
+                            wh[2 * p + 1] = u8_to_f32(wd[p], 3);
                         }
-                        accg[r] = fmaf(dg, sg, accg[r]);
-                        acch[r] = fmaf(dh, sh, acch[r]);
+#pragma unroll
+                        for (int r = 0; r < NRC; ++r) {
+                            float sg = wg[0] * xv[j][r][0], sh = wh[0] * xv[j][r][0];
+#pragma unroll
+                            for (int e = 1; e < 8; ++e) {
+                                sg = fmaf(wg[e], xv[j][r][e], sg);
+                                sh = fmaf(wh[e], xv[j][r][e], sh);
+                            }
+                            accg[r] = fmaf(dg, sg, accg[r]);
+                            acch[r] = fmaf(dh, sh, acch[r]);
+                        }
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);            // the stage is free for the producer
-            float *rw = red + (warp * a.rpr + i) * 128;
+            if (lane == 0) dla::mbar_arrive(&empty[st]);          // the stage is free for the producer
+            // this warp's partial of the row tile: [row 0..15][column 0..7]
+            float *rw = red + ((i & 1) * kConsumers + warp) * 128;
             if constexpr (MMA) {
-                *reinterpret_cast<float2 *>(rw + g * 8 + 2 * c) = make_float2(acc[0] * cs0, acc[1] * cs1);
-                *reinterpret_cast<float2 *>(rw + (g + 8) * 8 + 2 * c) = make_float2(acc[2] * cs0, acc[3] * cs1);
+                *reinterpret_cast<float2 *>(rw + g * 8 + 2 * c) = make_float2(acc01.x * us0, acc01.y * us1);
+                *reinterpret_cast<float2 *>(rw + (g + 8) * 8 + 2 * c) = make_float2(acc23.x * us0, acc23.y * us1);
             } else {
 #pragma unroll
                 for (int r = 0; r < NRC; ++r) {
@@ -327,40 +326,72 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
                     }
                 }
             }
-        }
-    }
-    __syncthreads();
-    const bool failed = s_fail != 0;
-
-    // ---- sum the warps' partials in a fixed order; finish here or hand to the cluster
-    for (int e = threadIdx.x; e < nrt * 128; e += kThreads) {
-        const int i = e >> 7, el = e & 127;
-        const int row = el >> 3, col = el & 7;
-        if (col >= a.nr) continue;
-        float sum = 0.f;
+            if (consumers_any(!ok)) {          // a stage that never arrived: stop (all warps alike)
+                bad = true;
+                break;
+            }
+            if (warp == i % kConsumers) {
+                // owner warp: sum the 8 partials in warp order; lane holds elements 4 lane .. 4 lane + 3
+                const float *rb = red + (i & 1) * kConsumers * 128 + lane * 4;
+                float4 s = *reinterpret_cast<const float4 *>(rb);
 #pragma unroll
-        for (int w = 0; w < kConsumers; ++w) sum += red[(w * a.rpr + i) * 128 + el];
-        if (failed) sum = __int_as_float(0x7fc00000);
-        if (a.cs == 1) {
-            const int o = (rt0 + i) * 16 + row;
-            if (o < a.n_out) a.y[(int64_t)col * a.y_stride + o] = sum;
-        } else {
-            cpart[e] = sum;
+                for (int w = 1; w < kConsumers; ++w) {
+                    const float4 t = *reinterpret_cast<const float4 *>(rb + w * 128);
+                    s.x += t.x;
+                    s.y += t.y;
+                    s.z += t.z;
+                    s.w += t.w;
+                }
+                if (a.cs == 1) {
+                    const int o = (rt0 + i) * 16 + (lane >> 1), col0 = (lane & 1) * 4;
+                    if (o < a.n_out) {
+                        const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (col0 + q < a.nr) a.y[(int64_t)(col0 + q) * a.y_stride + o] = sv[q];
+                    }
+                } else {
+                    *reinterpret_cast<float4 *>(part + i * 128 + lane * 4) = s;
+                }
+            }
         }
     }
+    if (producer && lane == 0 && bad) {
+        // do not leave with copies in flight: wait (bounded) for every stage still landing
+        for (int j = max(0, issued - S); j < issued; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
+    }
+    const bool failed = __syncthreads_or(bad || s_shape_bad) != 0;
+
     if (a.cs > 1) {
-        // every K-slice of this run of row tiles holds its partials in shared memory: sum in rank order
-        cluster_sync_all();
-        for (int e = threadIdx.x; e < nrt * 128; e += kThreads) {
-            if ((e >> 3) % a.cs != slice) continue;      // each rank finishes a share of the rows
-            const int col = e & 7;
-            if (col >= a.nr) continue;
-            float sum = 0.f;
-            for (int q = 0; q < a.cs; ++q) sum += ld_dsmem_f32(cpart + e, (uint32_t)q);
-            const int o = rt0 * 16 + (e >> 3);
-            if (o < a.n_out) a.y[(int64_t)col * a.y_stride + o] = sum;
+        // every K-slice of this run of row tiles holds its sums in shared memory: add them in rank order
+        if (failed)
+            for (int e = threadIdx.x; e < nrt * 128; e += kThreads) part[e] = __int_as_float(0x7fc00000);
+        dla::cluster_sync_all();
+        for (int e4 = threadIdx.x; e4 < nrt * 32; e4 += kThreads) {
+            const int i = e4 >> 5;
+            if (i % a.cs != slice) continue;                 // each rank finishes a share of the row tiles
+            float4 s = dla::ld_dsmem_f32x4(part + e4 * 4, 0);
+            for (int q = 1; q < a.cs; ++q) {
+                const float4 t = dla::ld_dsmem_f32x4(part + e4 * 4, (uint32_t)q);
+                s.x += t.x;
+                s.y += t.y;
+                s.z += t.z;
+                s.w += t.w;
+            }
+            const int o = (rt0 + i) * 16 + ((e4 & 31) >> 1), col0 = (e4 & 1) * 4;
+            if (o < a.n_out) {
+                const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (col0 + q < a.nr) a.y[(int64_t)(col0 + q) * a.y_stride + o] = sv[q];
+            }
         }
-        cluster_sync_all();   // keep this CTA's shared memory alive until every peer has read it
+        dla::cluster_sync_all();   // keep this CTA's shared memory alive until every peer has read it
+    } else if (failed) {
+        for (int e = threadIdx.x; e < nrt * 128; e += kThreads) {
+            const int o = rt0 * 16 + (e >> 3), col = e & 7;
+            if (o < a.n_out && col < a.nr) a.y[(int64_t)col * a.y_stride + o] = __int_as_float(0x7fc00000);
+        }
     }
 }
 
@@ -373,8 +404,8 @@ __device__ __forceinline__ uint32_t q8_byte(const uint8_t *blocks, int64_t n_out
     return blocks[(o * (n_in / 32) + k / 32) * 34 + 2 + (k % 32)];
 }
 
-// lane t = 4g + c of tile (rt, kt): word 0 = row g at inputs 4c..4c+3, word 1 = row g+8 there,
-// words 2 and 3 = the same rows at 16+4c..16+4c+3
+// lane t = 4g + c of tile (rt, kt), word p: inputs kb, kb + 1 (kb = 16(p/2) + 8(p%2) + 2c) of
+// row g, then of row g + 8, as biased bytes q + 128 (padding: q = 0)
 __global__ void q8_pack_qs_kernel(const uint8_t *blocks, int64_t n_out, int64_t n_in, int KT,
                                   int64_t units, uint4 *qs)
 {
@@ -386,13 +417,14 @@ __global__ void q8_pack_qs_kernel(const uint8_t *blocks, int64_t n_out, int64_t 
     const int g = lane >> 2, c = lane & 3;
     uint32_t w[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int row = g + (q & 1) * 8;
-        const int k0 = 4 * c + (q >> 1) * 16;
-        uint32_t v = 0u;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) v |= q8_byte(blocks, n_out, n_in, rt * 16 + row, kt * 32 + k0 + b) << (8 * b);
-        w[q] = v;
+    for (int p = 0; p < 4; ++p) {
+        const int kb = (p >> 1) * 16 + (p & 1) * 8 + 2 * c;
+        const int64_t k = kt * 32 + kb, o = rt * 16 + g;
+        const uint32_t b0 = q8_byte(blocks, n_out, n_in, o, k) ^ 0x80u;
+        const uint32_t b1 = q8_byte(blocks, n_out, n_in, o, k + 1) ^ 0x80u;
+        const uint32_t b2 = q8_byte(blocks, n_out, n_in, o + 8, k) ^ 0x80u;
+        const uint32_t b3 = q8_byte(blocks, n_out, n_in, o + 8, k + 1) ^ 0x80u;
+        w[p] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
     }
     qs[u] = make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -439,20 +471,41 @@ void *kptr() { return reinterpret_cast<void *>(gemv_q8_kernel<MMA, NRC, KWM>); }
 
 void *pick_kernel(bool mma, int nrc, int kwm)
 {
+    if (mma) {
+        switch (kwm) {
+        case 1: return kptr<true, 1, 1>();
+        case 2: return kptr<true, 1, 2>();
+        case 4: return kptr<true, 1, 4>();
+        case 6: return kptr<true, 1, 6>();
+        }
+        return nullptr;
+    }
     switch (kwm) {
-    case 1: return mma ? kptr<true, 1, 1>() : nrc == 1 ? kptr<false, 1, 1>() : kptr<false, 2, 1>();
-    case 2: return mma ? kptr<true, 1, 2>() : nrc == 1 ? kptr<false, 1, 2>() : kptr<false, 2, 2>();
-    case 4: return mma ? kptr<true, 1, 4>() : nrc == 1 ? kptr<false, 1, 4>() : kptr<false, 2, 4>();
-    case 6: return mma ? kptr<true, 1, 6>() : nullptr;
-    case 8: return mma ? kptr<true, 1, 8>() : nrc == 1 ? kptr<false, 1, 8>() : nullptr;
+    case 1: return nrc == 1 ? kptr<false, 1, 1>() : kptr<false, 2, 1>();
+    case 2: return nrc == 1 ? kptr<false, 1, 2>() : kptr<false, 2, 2>();
+    case 4: return nrc == 1 ? kptr<false, 1, 4>() : kptr<false, 2, 4>();
+    case 8: return nrc == 1 ? kptr<false, 1, 8>() : nullptr;
     }
     return nullptr;
+}
+
+int kwm_for(bool mma, int nrc, int kw)
+{
+    if (kw <= 1) return 1;
+    if (kw <= 2) return 2;
+    if (kw <= 4) return 4;
+    if (mma) return kw <= 6 ? 6 : 0;
+    return (nrc == 1 && kw <= 8) ? 8 : 0;
 }
 
 // The dynamic shared-memory limit is a per-function attribute shared by every launch of the
 // kernel (graph nodes and profilers re-launch against it): set it once to the largest size any
 // launch shape may use, never to one launch's own size.
 constexpr int kSmemLimit = 200 * 1024;
+// Two CTAs share an SM (registers are capped for it): ring bytes aimed at per CTA and the
+// largest footprint with which two fit.
+constexpr size_t kRingBudget = 80 * 1024;
+constexpr size_t kShareLimit = 110 * 1024;
 
 int prepare_kernel(const void *kern, int cs)
 {
@@ -465,13 +518,30 @@ int prepare_kernel(const void *kern, int cs)
     return DL_OK;
 }
 
-// Clusters of `cs` CTAs of this shape that are resident at once.
-int resident_clusters(const void *kern, int cs, size_t smem)
+// Clusters of `cs` CTAs resident at once with one CTA per SM (asked with a shared-memory
+// footprint that no two CTAs can share), cached per device and cluster size.
+int clusters_one_per_sm(const void *kern, int cs)
 {
+    static std::mutex mu;
+    static int cache[16][17];
+    static bool init = false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!init) {
+        for (auto &row : cache)
+            for (int &v : row) v = -1;
+        init = true;
+    }
+    if (cache[dev][cs] >= 0) return cache[dev][cs];
+    if (prepare_kernel(kern, cs) != DL_OK) return 0;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cs);
     lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = smem;
+    lc.dynamicSmemBytes = (size_t)150 * 1024;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cs;
@@ -482,85 +552,107 @@ int resident_clusters(const void *kern, int cs, size_t smem)
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) != cudaSuccess) {
         cudaGetLastError();
-        return 0;
+        clusters = 0;
     }
+    cache[dev][cs] = clusters;
     return clusters;
 }
 
-// Launch shape.  K is cut into cs slices of ksl k-tiles (whole groups of 4); each CTA takes
-// rpr consecutive row tiles of one slice and streams them one row tile per ring stage.  The
-// shape with the least work per CTA whose grid is resident in one wave wins (near-ties go
-// to fewer slices).
+// Whether two CTAs of this kernel fit on an SM at the largest shared footprint the launch shapes
+// use (registers decide), cached per device and kernel.
+bool two_per_sm(const void *kern)
+{
+    static std::mutex mu;
+    static const void *keys[16][32];
+    static int vals[16][32];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < 32; ++i) {
+        if (keys[dev][i] == kern) return vals[dev][i] >= 2;
+        if (!keys[dev][i]) {
+            int n = 0;
+            if (prepare_kernel(kern, 1) != DL_OK ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kShareLimit) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            keys[dev][i] = kern;
+            vals[dev][i] = n;
+            return n >= 2;
+        }
+    }
+    return false;
+}
+
+// Launch shape.  K is cut into cs slices of ksl k-tiles (whole groups of 4, at most 8 x kwm
+// per slice so that every warp holds its activations in registers); each CTA takes rpr
+// consecutive row tiles of one slice and streams them one row tile per ring stage.  Among the
+// shapes that run in one wave with two CTAs per SM, the least bytes per CTA wins (near-ties go
+// to fewer slices).  Matrices too tall for one wave run in several.
 int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
 {
     const bool mma = path == PATH_TENSOR || (path == PATH_AUTO && nr > 2);
     if (!mma && nr > 2) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: the CUDA-core path serves 1 or 2 rows per command");
     const int nrc = mma ? 1 : nr;
-    const int kw_max = (!mma && nrc == 2) ? 4 : 8;
     GemvCfg best{};
     long best_cost = -1;
     for (int cs = 1; cs <= 16; ++cs) {
         const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
         if ((int)dl::ceil_div(KT, ksl) != cs) continue;
-        const int kw = (int)dl::ceil_div(ksl, kConsumers);             // k-tiles per consumer warp
-        if (kw > kw_max || (size_t)ksl * 544 > 48 * 1024) continue;
-        const int kwm = kw <= 1 ? 1 : kw <= 2 ? 2 : kw <= 4 ? 4 : (mma && kw <= 6) ? 6 : 8;
-        const size_t sb = (size_t)ksl * 544;
-        // two CTAs per SM when shared memory allows, else one; the ring takes what the
-        // partials leave (2 to 8 stages)
-        for (int per_sm = 2; per_sm >= 1; --per_sm) {
-            const int ranges = (per_sm * sm) / cs;
-            if (ranges < 1) continue;
-            const int rpr = (int)dl::ceil_div(RT, ranges);
-            const size_t limit = per_sm == 2 ? (size_t)112 * 1024 : (size_t)kSmemLimit;
-            const size_t fixed = gemv_smem(ksl, 0, rpr);
-            if (fixed + 2 * sb > limit) continue;
-            int stages = (int)((limit - fixed) / sb);
-            if (stages > kMaxStages) stages = kMaxStages;
-            const size_t smem = gemv_smem(ksl, stages, rpr);
-            const long cost = (long)rpr * ksl * 100 + cs;        // bytes per CTA, then fewer slices
-            if (best_cost < 0 || cost * 100 < best_cost * 95) {
-                best_cost = cost;
-                best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs, smem};
-            }
-            break;
+        const int kwm = kwm_for(mma, nrc, (int)dl::ceil_div(ksl, kConsumers));
+        if (kwm == 0) continue;
+        const void *kern = pick_kernel(mma, nrc, kwm);
+        if (!kern) continue;
+        const int nc1 = cs == 1 ? sm : clusters_one_per_sm(kern, cs);
+        if (nc1 < 1) continue;
+        const size_t sb = (size_t)ksl * kStageTileBytes;
+        int stages = (int)(kRingBudget / sb);
+        stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
+        int per_sm = two_per_sm(kern) ? 2 : 1;
+        int rpr = (int)dl::ceil_div(RT, per_sm * nc1);
+        while (stages > 2 && gemv_smem(ksl, stages, rpr, cs) > kShareLimit) --stages;
+        if (per_sm == 2 && gemv_smem(ksl, stages, rpr, cs) > kShareLimit) {
+            // two CTAs do not fit on an SM: one CTA per SM
+            per_sm = 1;
+            rpr = (int)dl::ceil_div(RT, nc1);
+        }
+        if (gemv_smem(ksl, stages, rpr, cs) > (size_t)kSmemLimit) continue;
+        const long cost = (long)per_sm * rpr * ksl * 100 + cs;   // bytes per SM, then fewer slices
+        if (best_cost < 0 || cost * 100 < best_cost * 95) {
+            best_cost = cost;
+            best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
+                           gemv_smem(ksl, stages, rpr, cs)};
         }
     }
     if (best_cost < 0) {
-        // no single-wave shape (very many row tiles): CTAs of as many row tiles as shared memory
+        // no one-wave shape (very many row tiles): CTAs of as many row tiles as shared memory
         // holds, in several waves
         for (int cs = 1; cs <= 16 && best_cost < 0; ++cs) {
             const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
             if ((int)dl::ceil_div(KT, ksl) != cs) continue;
-            const int kw = (int)dl::ceil_div(ksl, kConsumers);
-            if (kw > kw_max || (size_t)ksl * 544 > 48 * 1024) continue;
-            const int kwm = kw <= 1 ? 1 : kw <= 2 ? 2 : kw <= 4 ? 4 : (mma && kw <= 6) ? 6 : 8;
-            const size_t sb = (size_t)ksl * 544;
-            const int stages = 3;
-            int rpr = (int)(((size_t)112 * 1024 - stages * sb) / ((size_t)kConsumers * 512 + 512));
+            const int kwm = kwm_for(mma, nrc, (int)dl::ceil_div(ksl, kConsumers));
+            if (kwm == 0 || !pick_kernel(mma, nrc, kwm)) continue;
+            const size_t sb = (size_t)ksl * kStageTileBytes;
+            int stages = (int)(kRingBudget / sb);
+            stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
+            const size_t fixed = gemv_smem(ksl, stages, 0, cs);
+            if (fixed >= (size_t)kSmemLimit) continue;
+            int rpr = cs > 1 ? (int)(((size_t)kSmemLimit - fixed) / 512) : (int)dl::ceil_div(RT, sm);
             if (rpr < 1) continue;
             if (rpr > RT) rpr = RT;
             best_cost = 0;
             best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
-                           gemv_smem(ksl, stages, rpr)};
+                           gemv_smem(ksl, stages, rpr, cs)};
         }
         if (best_cost < 0) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no launch shape for %d k-tiles", KT);
     }
     const void *kern = pick_kernel(best.mma, best.nrc, best.kwm);
-    if (!kern) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no kernel for this shape");
-    int rc = prepare_kernel(kern, best.cs);
+    const int rc = prepare_kernel(kern, best.cs);
     if (rc != DL_OK) return rc;
-    if (best.cs > 1 && best_cost > 0) {
-        // a one-wave shape stays one wave with clusters: grow the row tiles per CTA until every
-        // cluster is resident at once, within the shared-memory limit
-        while (resident_clusters(kern, best.cs, best.smem) < best.grid / best.cs && best.rpr < RT) {
-            const size_t smem = gemv_smem(best.ksl, best.stages, best.rpr + 1);
-            if (smem > (size_t)kSmemLimit) break;
-            best.rpr += 1;
-            best.smem = smem;
-            best.grid = (int)dl::ceil_div(RT, best.rpr) * best.cs;
-        }
-    }
     *out = best;
     return DL_OK;
 }
@@ -575,6 +667,7 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     a.ksl = cfg.ksl;
     a.rpr = cfg.rpr;
     a.stages = cfg.stages;
+    a.l2pf = 0;
     const void *kern = pick_kernel(cfg.mma, cfg.nrc, cfg.kwm);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid);
@@ -625,8 +718,8 @@ int gemv_impl(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
     if (rc != DL_OK) return rc;
 
     GemvArgs a{};
-    a.qs = static_cast<const uint4 *>(W->qs);
-    a.d = static_cast<const uint32_t *>(W->d);
+    a.qs = static_cast<const unsigned char *>(W->qs);
+    a.d = static_cast<const unsigned char *>(W->d);
     a.x_stride = x_stride;
     a.y_stride = y_stride;
     a.n_out = (int)W->n_out;

@@ -34,8 +34,8 @@ __device__ __forceinline__ unsigned short to_half_clamped(float v)
 
 __global__ void __launch_bounds__(256) rope_kv_store_kernel(RopeArgs a)
 {
-    dl_pdl_launch_dependents();
     dl_pdl_wait();
+    dl_pdl_launch_dependents();
     const int r = blockIdx.y;
     const int half = a.D >> 1;
     const int pairs_total = (a.n_q + a.n_kv) * half;
