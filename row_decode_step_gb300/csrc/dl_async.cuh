@@ -34,12 +34,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
                  : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase of `parity` to complete: false if it never did (the caller
-// then records a failure and stops using what the barrier guards).
+// try_wait that lets the thread sleep up to `ns` nanoseconds for the phase (it wakes as soon as
+// the phase completes), so that waiting warps leave the issue slots to working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(ns) : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of `parity` to complete (at most 2^16 sleeps of 20 us, about
+// 1.3 s): false if it never did (the caller then records a failure and stops using what the
+// barrier guards).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
-    for (int spin = 0; spin < (1 << 22); ++spin)
-        if (mbar_try_wait(bar, parity)) return true;
+    for (int spin = 0; spin < (1 << 16); ++spin)
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     return false;
 }
 

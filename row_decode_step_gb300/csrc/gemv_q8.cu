@@ -11,16 +11,17 @@
 // contiguous along K.  Scales: per 16 rows and 4 tiles, 128 bytes; lane group g
 // reads 16 bytes = (d[g], d[g+8]) for the 4 tiles.
 //
-// Kernel shape (one CTA per SM, one wave):
-//  * a CTA = one producer warp + 8 consumer warps owns a run of row tiles and one
-//    K-slice; the producer streams one row tile's slice (weights, then scales: two
-//    contiguous bulk copies) into each stage of a shared-memory ring of about
-//    96 KB, tracked by mbarriers, and issues the ring before waiting on the
-//    previous kernel (programmatic dependent launch);
-//  * each consumer warp owns an eighth of the slice's k-tiles; its activations are
-//    loaded once and kept in registers as operands for the whole launch;
+// Kernel shape (two CTAs per SM, one wave):
+//  * a CTA of 8 warps owns a run of row tiles and one K-slice; each stage of a
+//    shared-memory ring (about 80 KB, mbarrier-tracked) holds one row tile's slice
+//    (weights, then scales: two contiguous bulk copies).  Thread 0 fills the ring
+//    before waiting on the previous kernel (programmatic dependent launch: the
+//    weights do not depend on it); afterwards each slot is refilled by the warp that
+//    owns the stage just consumed, right after the CTA-wide barrier that ends it;
+//  * each warp owns an eighth of the slice's k-tiles; its activations are loaded
+//    once and kept in registers as operands for the whole launch;
 //  * after each stage the 8 warps' partial 16x8 tiles are summed, in warp order, by
-//    one owner warp (stage index mod 8); the K-slices of a thread-block cluster are
+//    the owner warp (stage index mod 8); the K-slices of a thread-block cluster are
 //    summed through distributed shared memory in rank order at the end (no
 //    atomics: results do not depend on timing).
 // Two inner products share this shape.  Tensor path: the f16 weights (1152 + q)
@@ -58,8 +59,8 @@ struct GemvArgs {
     int l2pf;               // stages past the ring prefetched into L2 before the wait
 };
 
-constexpr int kConsumers = 8;                        // consumer warps, each a share of the K-slice
-constexpr int kThreads = (kConsumers + 1) * 32;      // and one producer warp
+constexpr int kConsumers = 8;                        // warps, each a share of the K-slice
+constexpr int kThreads = kConsumers * 32;
 constexpr int kMaxStages = 8;
 constexpr int kStageTileBytes = 512 + 32;            // weights and scales of one k-tile
 constexpr size_t kRedBytes = (size_t)2 * kConsumers * 128 * 4;   // per-stage partials, two buffers
@@ -93,21 +94,11 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 }
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-// OR of `flag` over the consumer warps, at a barrier they all reach (uniform result).
-__device__ __forceinline__ bool consumers_any(bool flag)
-{
-    uint32_t r;
-    asm volatile("{\n .reg .pred pin, pout;\n setp.ne.u32 pin, %1, 0;\n"
-                 " bar.red.or.pred pout, 1, %2, pin;\n selp.u32 %0, 1, 0, pout;\n}"
-                 : "=r"(r) : "r"((uint32_t)flag), "r"((uint32_t)(kConsumers * 32)) : "memory");
-    return r != 0;
-}
-
 template <bool MMA, int NRC, int KWM>
-__global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
+__global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ int s_shape_bad;
 
     const int S = a.stages;
@@ -124,13 +115,9 @@ __global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int KG = a.KT >> 2;
-    const bool producer = warp == kConsumers;
 
     if (threadIdx.x == 0) {
-        for (int st = 0; st < S; ++st) {
-            dla::mbar_init(&full[st], 1);
-            dla::mbar_init(&empty[st], kConsumers);
-        }
+        for (int st = 0; st < S; ++st) dla::mbar_init(&full[st], 1);
         s_shape_bad = 0;
         dla::mbar_init_fence();
     }
@@ -145,10 +132,9 @@ __global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs
         dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
         dla::bulk_g2s(dst + (size_t)a.ksl * 512, a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
     };
-    int issued = 0;
     // the weights do not depend on the previous kernel: fill the ring before waiting on it
-    if (producer && lane == 0) {
-        for (; issued < S && issued < nrt; ++issued) issue(issued);
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < S && j < nrt; ++j) issue(j);
         const int pf_end = min(nrt, S + a.l2pf);
         for (int j = S; j < pf_end; ++j) {
             const int rt = rt0 + j;
@@ -163,8 +149,8 @@ __global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs
 
     // ---- this warp's share of the slice and its activations, kept in registers
     const int wk0 = (warp * nkt) / kConsumers, wk1 = ((warp + 1) * nkt) / kConsumers;   // slice-local
-    const int nw = producer ? 0 : min(wk1 - wk0, KWM);
-    if (!producer && lane == 0 && wk1 - wk0 > KWM) atomicExch(&s_shape_bad, 1);   // broken launch shape
+    const int nw = min(wk1 - wk0, KWM);
+    if (lane == 0 && wk1 - wk0 > KWM) atomicExch(&s_shape_bad, 1);   // broken launch shape
     // lane (g, c) holds inputs 2c, 2c+1 / 8+2c, 9+2c / 16+2c, 17+2c / 24+2c, 25+2c of each k-tile
     uint32_t bh[MMA ? KWM : 1][4], bl[MMA ? KWM : 1][4];
     float2 ncorr[MMA ? KWM : 1];                 // -1152 * sum(x) of columns 2c, 2c+1 per k-tile
@@ -237,19 +223,8 @@ __global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs
     }
 
     bool bad = false;
-    if (producer) {
-        // refill each stage once every consumer warp has released it
-        if (lane == 0) {
-            for (; issued < nrt; ++issued) {
-                const int st = issued % S;
-                if (!dla::mbar_wait(&empty[st], (uint32_t)(((issued / S) - 1) & 1))) {
-                    bad = true;
-                    break;
-                }
-                issue(issued);
-            }
-        }
-    } else {
+    int fail_at = nrt;                                   // first stage that never arrived
+    {
         for (int i = 0; i < nrt; ++i) {
             const int st = i % S;
             const bool ok = __all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((i / S) & 1)));
@@ -305,8 +280,6 @@ __global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) dla::mbar_arrive(&empty[st]);          // the stage is free for the producer
             // this warp's partial of the row tile: [row 0..15][column 0..7]
             float *rw = red + ((i & 1) * kConsumers + warp) * 128;
             if constexpr (MMA) {
@@ -326,11 +299,14 @@ __global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs
                     }
                 }
             }
-            if (consumers_any(!ok)) {          // a stage that never arrived: stop (all warps alike)
+            // every warp is done with stage i (its slot may be refilled) and has parked its partial
+            if (__syncthreads_or(!ok)) {       // a stage that never arrived: stop (all warps alike)
                 bad = true;
+                fail_at = i;
                 break;
             }
             if (warp == i % kConsumers) {
+                if (lane == 0 && i + S < nrt) issue(i + S);     // refill the slot
                 // owner warp: sum the 8 partials in warp order; lane holds elements 4 lane .. 4 lane + 3
                 const float *rb = red + (i & 1) * kConsumers * 128 + lane * 4;
                 float4 s = *reinterpret_cast<const float4 *>(rb);
@@ -356,9 +332,9 @@ __global__ void __maxnreg__(104) gemv_q8_kernel(const __grid_constant__ GemvArgs
             }
         }
     }
-    if (producer && lane == 0 && bad) {
-        // do not leave with copies in flight: wait (bounded) for every stage still landing
-        for (int j = max(0, issued - S); j < issued; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
+    if (bad && threadIdx.x == 0) {
+        // do not leave with copies in flight: wait (bounded) for every stage that may still land
+        for (int j = fail_at; j < nrt && j < fail_at + S; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
     }
     const bool failed = __syncthreads_or(bad || s_shape_bad) != 0;
 
@@ -511,6 +487,8 @@ int prepare_kernel(const void *kern, int cs)
 {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8: set shared memory");
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8: shared-memory carveout");
     if (cs > 8) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8: allow a large cluster");
