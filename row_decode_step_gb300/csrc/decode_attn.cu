@@ -6,10 +6,10 @@
 //
 // Work item = (session, KV head, piece).  A session's rows share a region, so
 // one CTA scores every query head of every session row that reads the KV head:
-// each key is loaded from HBM once per session and step.  KV tiles of 32 keys
-// are staged in shared memory with cp.async (16-byte copies, double-buffered);
-// scores use one lane per key, the online softmax reduces over the warp with
-// shuffles, and P.V runs with lanes over head dimensions.
+// each key is loaded from HBM once per session and step.  Stages of 32 keys of
+// K and V reach shared memory through tensor maps (below); two inner products
+// consume them: tensor cores for sessions of several rows, CUDA cores (lane = key
+// for the scores, lanes over head dimensions for P.V) for a few queries.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -23,7 +23,6 @@
 
 namespace {
 
-constexpr int kAttnThreads = 128;
 constexpr int kTile = 32;          // keys per tile
 constexpr int kMaxQ = 32;          // queries one work item serves (session rows x group)
 constexpr int kCudaCoreMaxQ = 4;   // queries per work item up to which the CUDA-core form is used
@@ -56,15 +55,6 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
-{
-    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 // Clip a row's device key count to what the plan and the cache cover.
 __device__ __forceinline__ int clip_len(int L, int planned, int capacity, int32_t *status, bool report)
 {
@@ -74,233 +64,6 @@ __device__ __forceinline__ int clip_len(int L, int planned, int capacity, int32_
         L = L < 1 ? 0 : hi;
     }
     return L;
-}
-
-template <int D>
-__global__ void __launch_bounds__(kAttnThreads) decode_attn_cc_kernel(const __grid_constant__ AttnArgs a)
-{
-    constexpr int PITCH = D + 8;                 // halves per staged row (16-byte pad: conflict-free)
-    constexpr int NQS = kAttnThreads / (D / 2);  // query slices of the P.V phase
-    constexpr int QPS = kMaxQ / NQS;             // queries per slice (upper bound)
-    const dl_attn_plan &P = a.plan;
-
-    extern __shared__ __align__(16) unsigned char smem[];
-    uint16_t *ks = reinterpret_cast<uint16_t *>(smem);            // [2][kTile][PITCH]
-    uint16_t *vs = ks + 2 * kTile * PITCH;                        // [2][kTile][PITCH]
-    float *qs = reinterpret_cast<float *>(vs + 2 * kTile * PITCH);  // [kMaxQ][D]
-    float *ps = qs + kMaxQ * D;                                   // [kMaxQ][kTile]
-    float *al = ps + kMaxQ * kTile;                               // [kMaxQ]
-    float *sm_m = al + kMaxQ;                                     // [kMaxQ]
-    float *sm_l = sm_m + kMaxQ;                                   // [kMaxQ]
-    __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS];
-
-    // ---- which (session, KV head, piece)
-    const int item = blockIdx.x;
-    int s = 0;
-    while (s + 1 < P.n_sessions && item >= P.sess_item0[s + 1]) ++s;
-    const int local = item - P.sess_item0[s];
-    const int splits = P.sess_splits[s];
-    const int h = local / splits, piece = local - h * splits;
-    const int rb = P.sess_begin[s], nrows = P.sess_begin[s + 1] - rb;
-    const int G = P.n_q / P.n_kv;
-    const int Q = nrows * G;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // ask L2 for this piece's keys and values (planned bound) before waiting on the previous kernel
-    if (tid == 0) {
-        int lplan = 0;
-        for (int i = 0; i < nrows; ++i) lplan = max(lplan, P.row_keys_max[P.sess_rows[rb + i]]);
-        lplan = min(lplan, a.capacity);
-        const int p0 = piece * P.chunk, p1 = min(p0 + P.chunk, lplan);
-        if (p1 > p0) {
-            const int64_t off = (int64_t)P.row_region[P.sess_rows[rb]] * a.region_stride +
-                                ((int64_t)h * a.capacity + p0) * D;
-            dl_prefetch_l2(a.kc + off, (uint32_t)(p1 - p0) * D * 2u);
-            dl_prefetch_l2(a.vc + off, (uint32_t)(p1 - p0) * D * 2u);
-        }
-    }
-    dl_pdl_wait();
-    dl_pdl_launch_dependents();
-
-    if (tid < nrows) {
-        const int r = P.sess_rows[rb + tid];
-        s_row[tid] = r;
-        s_len[tid] = clip_len(a.seqlen[r], P.row_keys_max[r], a.capacity, a.status, piece == 0 && h == 0);
-    }
-    __syncthreads();
-    int lmax = 0;
-    for (int i = 0; i < nrows; ++i) lmax = max(lmax, s_len[i]);
-    const int k0 = piece * P.chunk;
-    const int k1 = min(k0 + P.chunk, lmax);
-    if (k0 >= k1) return;                      // no row of the session reaches this piece
-
-    const int reg = P.row_region[s_row[0]];
-    const uint16_t *kbase = a.kc + (int64_t)reg * a.region_stride + (int64_t)h * a.capacity * D;
-    const uint16_t *vbase = a.vc + (int64_t)reg * a.region_stride + (int64_t)h * a.capacity * D;
-
-    // ---- stage the queries, pre-scaled into the log2 domain
-    for (int i = tid; i < Q * D; i += kAttnThreads) {
-        const int qi = i / D, d = i - qi * D;
-        const int rq = qi / G, gq = qi - rq * G;
-        qs[i] = a.q[s_row[rq] * a.q_stride + (h * G + gq) * D + d] * a.qscale;
-    }
-
-    auto load_tile = [&](int buf, int t0) {
-        constexpr int CH = D * 2 / 16;         // 16-byte chunks per key row
-        for (int i = tid; i < kTile * CH; i += kAttnThreads) {
-            const int t = i / CH, ch = i - t * CH;
-            uint16_t *dk = ks + (buf * kTile + t) * PITCH + ch * 8;
-            uint16_t *dv = vs + (buf * kTile + t) * PITCH + ch * 8;
-            const int key = t0 + t;
-            if (key < k1) {
-                cp_async16(dk, kbase + (int64_t)key * D + ch * 8);
-                cp_async16(dv, vbase + (int64_t)key * D + ch * 8);
-            } else {
-                *reinterpret_cast<uint4 *>(dk) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(dv) = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        cp_async_commit();
-    };
-
-    // softmax state of this warp's queries (q = warp + 4*i), replicated over lanes
-    constexpr int WQ = kMaxQ / 4;
-    float m_run[WQ], l_run[WQ];
-#pragma unroll
-    for (int i = 0; i < WQ; ++i) {
-        m_run[i] = -INFINITY;
-        l_run[i] = 0.f;
-    }
-    // P.V accumulators: dims (2*dp, 2*dp+1) of queries qslice + NQS*i
-    const int dp = tid % (D / 2), qslice = tid / (D / 2);
-    float o0[QPS], o1[QPS];
-#pragma unroll
-    for (int i = 0; i < QPS; ++i) o0[i] = o1[i] = 0.f;
-
-    const int ntiles = (k1 - k0 + kTile - 1) / kTile;
-    load_tile(0, k0);
-    for (int it = 0; it < ntiles; ++it) {
-        const int buf = it & 1;
-        const int t0 = k0 + it * kTile;
-        if (it + 1 < ntiles) {
-            load_tile(buf ^ 1, t0 + kTile);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-
-        // ---- scores: lane = key, warp's queries
-        {
-            const uint16_t *krow = ks + (buf * kTile + lane) * PITCH;
-            float acc[WQ];
-#pragma unroll
-            for (int i = 0; i < WQ; ++i) acc[i] = 0.f;
-#pragma unroll 4
-            for (int c8 = 0; c8 < D; c8 += 8) {
-                const uint4 kw = *reinterpret_cast<const uint4 *>(krow + c8);
-                const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
-                const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
-                const float2 k45 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.z));
-                const float2 k67 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.w));
-#pragma unroll
-                for (int i = 0; i < WQ; ++i) {
-                    const int qi = warp + 4 * i;
-                    if (qi < Q) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(qs + qi * D + c8);
-                        const float4 qb = *reinterpret_cast<const float4 *>(qs + qi * D + c8 + 4);
-                        float v = acc[i];
-                        v = fmaf(qa.x, k01.x, v); v = fmaf(qa.y, k01.y, v);
-                        v = fmaf(qa.z, k23.x, v); v = fmaf(qa.w, k23.y, v);
-                        v = fmaf(qb.x, k45.x, v); v = fmaf(qb.y, k45.y, v);
-                        v = fmaf(qb.z, k67.x, v); v = fmaf(qb.w, k67.y, v);
-                        acc[i] = v;
-                    }
-                }
-            }
-            const int key = t0 + lane;
-#pragma unroll
-            for (int i = 0; i < WQ; ++i) {
-                const int qi = warp + 4 * i;
-                if (qi < Q) {
-                    const bool valid = key < s_len[qi / G];
-                    const float sc = valid ? acc[i] : -INFINITY;
-                    const float mt = warp_max(sc);
-                    const float mn = fmaxf(m_run[i], mt);
-                    const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m_run[i] - mn);
-                    const float p = valid ? exp2f(sc - mn) : 0.f;
-                    l_run[i] = l_run[i] * alpha + warp_sum(p);
-                    m_run[i] = mn;
-                    ps[qi * kTile + lane] = p;
-                    if (lane == 0) al[qi] = alpha;
-                }
-            }
-        }
-        __syncthreads();
-
-        // ---- P.V: lanes over head-dimension pairs
-        {
-#pragma unroll
-            for (int i = 0; i < QPS; ++i) {
-                const int qi = qslice + NQS * i;
-                if (qi < Q) {
-                    const float alpha = al[qi];
-                    o0[i] *= alpha;
-                    o1[i] *= alpha;
-                }
-            }
-            const uint16_t *vcol = vs + buf * kTile * PITCH + 2 * dp;
-#pragma unroll 4
-            for (int t = 0; t < kTile; t += 4) {
-                float2 vv[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    vv[u] = __half22float2(*reinterpret_cast<const __half2 *>(vcol + (t + u) * PITCH));
-#pragma unroll
-                for (int i = 0; i < QPS; ++i) {
-                    const int qi = qslice + NQS * i;
-                    if (qi < Q) {
-                        const float4 p4 = *reinterpret_cast<const float4 *>(ps + qi * kTile + t);
-                        o0[i] = fmaf(p4.x, vv[0].x, o0[i]); o1[i] = fmaf(p4.x, vv[0].y, o1[i]);
-                        o0[i] = fmaf(p4.y, vv[1].x, o0[i]); o1[i] = fmaf(p4.y, vv[1].y, o1[i]);
-                        o0[i] = fmaf(p4.z, vv[2].x, o0[i]); o1[i] = fmaf(p4.z, vv[2].y, o1[i]);
-                        o0[i] = fmaf(p4.w, vv[3].x, o0[i]); o1[i] = fmaf(p4.w, vv[3].y, o1[i]);
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    // ---- publish (m, l) and write this piece's partials for rows that reach it
-    if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < WQ; ++i) {
-            const int qi = warp + 4 * i;
-            if (qi < Q) {
-                sm_m[qi] = m_run[i];
-                sm_l[qi] = l_run[i];
-            }
-        }
-    }
-    __syncthreads();
-    const int ms = P.max_splits;
-#pragma unroll
-    for (int i = 0; i < QPS; ++i) {
-        const int qi = qslice + NQS * i;
-        if (qi < Q) {
-            const int rq = qi / G, gq = qi - rq * G;
-            if (s_len[rq] > k0) {
-                const int r = s_row[rq], head = h * G + gq;
-                const float inv = 1.f / sm_l[qi];
-                float *po = a.part_o + (((int64_t)r * P.n_q + head) * ms + piece) * D;
-                *reinterpret_cast<float2 *>(po + 2 * dp) = make_float2(o0[i] * inv, o1[i] * inv);
-                if (dp == 0)
-                    a.part_lse[((int64_t)r * P.n_q + head) * ms + piece] =
-                        (sm_m[qi] + log2f(sm_l[qi])) * 0.69314718055994530942f;
-            }
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -370,9 +133,9 @@ __device__ __forceinline__ bool attn_consumers_any(bool flag)
     return r != 0;
 }
 
-template <int D>
+template <int D, bool MMA>
 __global__ void __launch_bounds__(kMmaThreads, 2)
-decode_attn_mma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tk,
+decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv)
 {
     constexpr int NKS = D / 16;     // k-steps of the score product
@@ -403,12 +166,15 @@ decode_attn_mma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     const int g = lane >> 2, c = lane & 3;
     const bool producer = warp == kMmaConsumers;
 
-    const int MT = (Q + 15) >> 4;               // 16-query tiles (1 or 2)
-    const int KS = kMmaConsumers / MT;          // warps sharing one query tile
+    // warps: NT query tiles (16 queries, tensor form; 8, CUDA-core form) x NS stage groups
+    const int TL = MMA ? 16 : 8;
+    const int NT = (Q + TL - 1) / TL;
+    const int NS = kMmaConsumers / NT;
+    const int MT = NT, KS = NS;
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             dla::mbar_init(&full[i], 1);
-            dla::mbar_init(&empty[i], (uint32_t)MT);   // released by the query tiles' warps
+            dla::mbar_init(&empty[i], (uint32_t)NT);   // released by the warps of one stage group
         }
         dla::mbar_init_fence();
     }
@@ -484,166 +250,9 @@ decode_attn_mma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     dl_pdl_launch_dependents();
 
     const int mt = warp % MT, grp = warp / MT;
-    // ---- query operand fragments (log2-domain scaled, hi + lo f16 terms) in shared memory:
-    // [query tile][k-step][lane] 32 bytes = a0..a3 hi then a0..a3 lo
-    for (int fi = tid; fi < MT * NKS * 32; fi += kMmaConsumers * 32) {
-        const int t = fi & 31, ks = (fi >> 5) % NKS, qt = (fi >> 5) / NKS;
-        const int gg = t >> 2, cc = t & 3;
-        const int q0i = qt * 16 + gg, q1i = q0i + 8;
-        const float *q0 = q0i < Q ? a.q + (int64_t)s_row[s_qrow[q0i]] * a.q_stride + (h * G + s_qhead[q0i]) * D : nullptr;
-        const float *q1 = q1i < Q ? a.q + (int64_t)s_row[s_qrow[q1i]] * a.q_stride + (h * G + s_qhead[q1i]) * D : nullptr;
-        uint32_t hv[4], lv[4];
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            const float *src = (part & 1) ? q1 : q0;
-            const int col = ks * 16 + 2 * cc + (part >> 1) * 8;
-            float2 v = make_float2(0.f, 0.f);
-            if (src) v = __ldcg(reinterpret_cast<const float2 *>(src + col));
-            v.x *= a.qscale;
-            v.y *= a.qscale;
-            const __half2 hq = __floats2half2_rn(v.x, v.y);
-            const float2 hf = __half22float2(hq);
-            hv[part] = *reinterpret_cast<const uint32_t *>(&hq);
-            lv[part] = h2_bits(v.x - hf.x, v.y - hf.y);
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(qfrag + (size_t)fi * 32);
-        dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        dst[1] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-    }
-    dla::named_sync(1, kMmaConsumers * 32);
-    const unsigned char *myq = qfrag + (size_t)mt * NKS * 32 * 32 + lane * 32;
-    const int r0 = mt * 16 + g, r1 = r0 + 8;
-    const int len0 = r0 < Q ? s_len[s_qrow[r0]] : 0;
-    const int len1 = r1 < Q ? s_len[s_qrow[r1]] : 0;
-
-    float o[NDT][4];
-#pragma unroll
-    for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    for (int i = grp; i < nst; i += KS) {
-        const int st = i % S;
-        if (!__all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((i / S) & 1)))) {
-            bad = true;
-            break;
-        }
-        const uint32_t ksm = ring_s + (uint32_t)st * kStageBytes;
-        const uint32_t vsm = ksm + kStageBytes / 2;
-        const int kb0 = k0 + i * kStKeys;
-        if (kb0 + kStKeys > k1) {
-            // keys past the piece may hold anything (even NaN) in the V rows: zero them
-            unsigned char *vrow = ring + (size_t)st * kStageBytes + kStageBytes / 2;
-            for (int e = lane; e < NH * kStKeys * 8; e += 32) {
-                const int hf = e / (kStKeys * 8), rem = e - hf * kStKeys * 8;
-                const int key = rem >> 3;
-                if (kb0 + key >= k1) *reinterpret_cast<uint4 *>(vrow + hf * kHalfTile + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            dla::fence_proxy_async();
-            __syncwarp();
-        }
-
-        // scores of 32 keys: four 8-key column tiles, hi and lo terms in independent chains
-        float sc[4][4], sl[4][4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-            sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
-        }
-#pragma unroll
-        for (int ks = 0; ks < NKS; ks += 2) {
-            const uint4 qa = *reinterpret_cast<const uint4 *>(myq + (ks * 32) * 32);
-            const uint4 qb = *reinterpret_cast<const uint4 *>(myq + (ks * 32) * 32 + 16);
-            const uint4 qc = *reinterpret_cast<const uint4 *>(myq + ((ks + 1) * 32) * 32);
-            const uint4 qd = *reinterpret_cast<const uint4 *>(myq + ((ks + 1) * 32) * 32 + 16);
-            const uint32_t qh0[4] = {qa.x, qa.y, qa.z, qa.w}, ql0[4] = {qb.x, qb.y, qb.z, qb.w};
-            const uint32_t qh1[4] = {qc.x, qc.y, qc.z, qc.w}, ql1[4] = {qd.x, qd.y, qd.z, qd.w};
-            const int ch = 2 * ks + (lane >> 3);                 // 16-byte chunk of the key row
-            const uint32_t half_off = (uint32_t)(ch >> 3) * kHalfTile;
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int key = nt * 8 + (lane & 7);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(b0, b1, b2, b3, ksm + half_off + (uint32_t)(key * 128 + (((ch & 7) ^ (key & 7)) << 4)));
-                mma_f16(sc[nt], qh0, b0, b1);
-                mma_f16(sl[nt], ql0, b0, b1);
-                mma_f16(sc[nt], qh1, b2, b3);
-                mma_f16(sl[nt], ql1, b2, b3);
-            }
-        }
-        // mask keys past each row's count, online softmax per row (quad of lanes = one row)
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int key = kb0 + nt * 8 + 2 * c + e;
-                const float v0 = sc[nt][e] + sl[nt][e], v1 = sc[nt][2 + e] + sl[nt][2 + e];
-                sc[nt][e] = key < len0 ? v0 : -INFINITY;
-                sc[nt][2 + e] = key < len1 ? v1 : -INFINITY;
-                mx0 = fmaxf(mx0, sc[nt][e]);
-                mx1 = fmaxf(mx1, sc[nt][2 + e]);
-            }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
-        const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            sc[nt][0] = sc[nt][0] == -INFINITY ? 0.f : exp2f(sc[nt][0] - mn0);
-            sc[nt][1] = sc[nt][1] == -INFINITY ? 0.f : exp2f(sc[nt][1] - mn0);
-            sc[nt][2] = sc[nt][2] == -INFINITY ? 0.f : exp2f(sc[nt][2] - mn1);
-            sc[nt][3] = sc[nt][3] == -INFINITY ? 0.f : exp2f(sc[nt][3] - mn1);
-        }
-        float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            ps0 += sc[nt][0] + sc[nt][1];
-            ps1 += sc[nt][2] + sc[nt][3];
-        }
-        l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
-        m0 = mn0;
-        m1 = mn1;
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-            for (int j = 0; j < NDT; ++j) {
-                o[j][0] *= al0;
-                o[j][1] *= al0;
-                o[j][2] *= al1;
-                o[j][3] *= al1;
-            }
-        }
-        // O += P V over two 16-key steps: two 8-wide output tiles per transposed 4-matrix load
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const uint32_t pa[4] = {h2_bits(sc[2 * kk][0], sc[2 * kk][1]), h2_bits(sc[2 * kk][2], sc[2 * kk][3]),
-                                    h2_bits(sc[2 * kk + 1][0], sc[2 * kk + 1][1]),
-                                    h2_bits(sc[2 * kk + 1][2], sc[2 * kk + 1][3])};
-            const int vkey = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-            for (int j = 0; j < NDT / 2; ++j) {
-                const int ch = 2 * j + (lane >> 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(b0, b1, b2, b3, vsm + (uint32_t)(ch >> 3) * kHalfTile +
-                                              (uint32_t)(vkey * 128 + (((ch & 7) ^ (vkey & 7)) << 4)));
-                mma_f16(o[2 * j], pa, b0, b1);
-                mma_f16(o[2 * j + 1], pa, b2, b3);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) dla::mbar_arrive(&empty[st]);      // the stage is free for the producer
-    }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
     const int ms = P.max_splits;
-    if (attn_consumers_any(bad)) {
-        // a stage never arrived: this piece's partials are marked invalid (NaN) for the merge
+    // a stage never arrived: this piece's partials are marked invalid (NaN) for the merge
+    auto poison_partials = [&]() {
         for (int e = tid; e < Q * D; e += kMmaConsumers * 32) {
             const int qi = e / D, d = e - qi * D;
             const int rq = s_qrow[qi], gq = s_qhead[qi];
@@ -652,29 +261,329 @@ decode_attn_mma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             a.part_o[pidx * D + d] = __int_as_float(0x7fc00000);
             if (d == 0) a.part_lse[pidx] = __int_as_float(0x7fc00000);
         }
-        return;
-    }
-    // ---- combine the warps that share a query tile (the ring is idle now), then write partials
-    float *co = reinterpret_cast<float *>(smem);       // [4 warps][16][D]
-    float *cm = co + kMmaConsumers * 16 * D;           // [4 warps][16]
-    float *cl = cm + kMmaConsumers * 16;               // [4 warps][16]
+    };
+    // combine area (the ring, idle once every stage is consumed): [4 warps][16 rows][CP], m, l
+    constexpr int CP = D + 8;                          // padded row: the fragment stores spread over banks
+    float *co = reinterpret_cast<float *>(smem);
+    float *cm = co + kMmaConsumers * 16 * CP;
+    float *cl = cm + kMmaConsumers * 16;
+    if constexpr (MMA) {
+        // ---- query operand fragments (log2-domain scaled, hi + lo f16 terms) in shared memory:
+        // [query tile][k-step][hi, lo][lane] 16 bytes = a0..a3
+        for (int fi = tid; fi < MT * NKS * 32; fi += kMmaConsumers * 32) {
+            const int t = fi & 31, ks = (fi >> 5) % NKS, qt = (fi >> 5) / NKS;
+            const int gg = t >> 2, cc = t & 3;
+            const int q0i = qt * 16 + gg, q1i = q0i + 8;
+            const float *q0 = q0i < Q ? a.q + (int64_t)s_row[s_qrow[q0i]] * a.q_stride + (h * G + s_qhead[q0i]) * D : nullptr;
+            const float *q1 = q1i < Q ? a.q + (int64_t)s_row[s_qrow[q1i]] * a.q_stride + (h * G + s_qhead[q1i]) * D : nullptr;
+            uint32_t hv[4], lv[4];
+    #pragma unroll
+            for (int part = 0; part < 4; ++part) {
+                const float *src = (part & 1) ? q1 : q0;
+                const int col = ks * 16 + 2 * cc + (part >> 1) * 8;
+                float2 v = make_float2(0.f, 0.f);
+                if (src) v = __ldcg(reinterpret_cast<const float2 *>(src + col));
+                v.x *= a.qscale;
+                v.y *= a.qscale;
+                const __half2 hq = __floats2half2_rn(v.x, v.y);
+                const float2 hf = __half22float2(hq);
+                hv[part] = *reinterpret_cast<const uint32_t *>(&hq);
+                lv[part] = h2_bits(v.x - hf.x, v.y - hf.y);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(qfrag + (size_t)(fi >> 5) * 1024 + t * 16);
+            dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            dst[32] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        }
+        dla::named_sync(1, kMmaConsumers * 32);
+        const unsigned char *myq = qfrag + (size_t)mt * NKS * 1024 + lane * 16;
+        const int r0 = mt * 16 + g, r1 = r0 + 8;
+        const int len0 = r0 < Q ? s_len[s_qrow[r0]] : 0;
+        const int len1 = r1 < Q ? s_len[s_qrow[r1]] : 0;
+
+        float o[NDT][4];
+    #pragma unroll
+        for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        for (int i = grp; i < nst; i += KS) {
+            const int st = i % S;
+            if (!__all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((i / S) & 1)))) {
+                bad = true;
+                break;
+            }
+            const uint32_t ksm = ring_s + (uint32_t)st * kStageBytes;
+            const uint32_t vsm = ksm + kStageBytes / 2;
+            const int kb0 = k0 + i * kStKeys;
+            if (kb0 + kStKeys > k1) {
+                // keys past the piece may hold anything (even NaN) in the V rows: zero them
+                unsigned char *vrow = ring + (size_t)st * kStageBytes + kStageBytes / 2;
+                for (int e = lane; e < NH * kStKeys * 8; e += 32) {
+                    const int hf = e / (kStKeys * 8), rem = e - hf * kStKeys * 8;
+                    const int key = rem >> 3;
+                    if (kb0 + key >= k1) *reinterpret_cast<uint4 *>(vrow + hf * kHalfTile + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                dla::fence_proxy_async();
+                __syncwarp();
+            }
+
+            // scores of 32 keys: four 8-key column tiles, hi and lo terms in independent chains
+            float sc[4][4], sl[4][4];
+    #pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
+            }
+    #pragma unroll
+            for (int ks = 0; ks < NKS; ks += 2) {
+                const uint4 qa = *reinterpret_cast<const uint4 *>(myq + ks * 1024);
+                const uint4 qb = *reinterpret_cast<const uint4 *>(myq + ks * 1024 + 512);
+                const uint4 qc = *reinterpret_cast<const uint4 *>(myq + (ks + 1) * 1024);
+                const uint4 qd = *reinterpret_cast<const uint4 *>(myq + (ks + 1) * 1024 + 512);
+                const uint32_t qh0[4] = {qa.x, qa.y, qa.z, qa.w}, ql0[4] = {qb.x, qb.y, qb.z, qb.w};
+                const uint32_t qh1[4] = {qc.x, qc.y, qc.z, qc.w}, ql1[4] = {qd.x, qd.y, qd.z, qd.w};
+                const int ch = 2 * ks + (lane >> 3);                 // 16-byte chunk of the key row
+                const uint32_t half_off = (uint32_t)(ch >> 3) * kHalfTile;
+    #pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int key = nt * 8 + (lane & 7);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(b0, b1, b2, b3, ksm + half_off + (uint32_t)(key * 128 + (((ch & 7) ^ (key & 7)) << 4)));
+                    mma_f16(sc[nt], qh0, b0, b1);
+                    mma_f16(sl[nt], ql0, b0, b1);
+                    mma_f16(sc[nt], qh1, b2, b3);
+                    mma_f16(sl[nt], ql1, b2, b3);
+                }
+            }
+            // mask keys past each row's count, online softmax per row (quad of lanes = one row)
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+    #pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+    #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = kb0 + nt * 8 + 2 * c + e;
+                    const float v0 = sc[nt][e] + sl[nt][e], v1 = sc[nt][2 + e] + sl[nt][2 + e];
+                    sc[nt][e] = key < len0 ? v0 : -INFINITY;
+                    sc[nt][2 + e] = key < len1 ? v1 : -INFINITY;
+                    mx0 = fmaxf(mx0, sc[nt][e]);
+                    mx1 = fmaxf(mx1, sc[nt][2 + e]);
+                }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
+            const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+    #pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                sc[nt][0] = sc[nt][0] == -INFINITY ? 0.f : exp2f(sc[nt][0] - mn0);
+                sc[nt][1] = sc[nt][1] == -INFINITY ? 0.f : exp2f(sc[nt][1] - mn0);
+                sc[nt][2] = sc[nt][2] == -INFINITY ? 0.f : exp2f(sc[nt][2] - mn1);
+                sc[nt][3] = sc[nt][3] == -INFINITY ? 0.f : exp2f(sc[nt][3] - mn1);
+            }
+            float ps0 = 0.f, ps1 = 0.f;
+    #pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                ps0 += sc[nt][0] + sc[nt][1];
+                ps1 += sc[nt][2] + sc[nt][3];
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+            m0 = mn0;
+            m1 = mn1;
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+    #pragma unroll
+                for (int j = 0; j < NDT; ++j) {
+                    o[j][0] *= al0;
+                    o[j][1] *= al0;
+                    o[j][2] *= al1;
+                    o[j][3] *= al1;
+                }
+            }
+            // O += P V over two 16-key steps: two 8-wide output tiles per transposed 4-matrix load
+    #pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const uint32_t pa[4] = {h2_bits(sc[2 * kk][0], sc[2 * kk][1]), h2_bits(sc[2 * kk][2], sc[2 * kk][3]),
+                                        h2_bits(sc[2 * kk + 1][0], sc[2 * kk + 1][1]),
+                                        h2_bits(sc[2 * kk + 1][2], sc[2 * kk + 1][3])};
+                const int vkey = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    #pragma unroll
+                for (int j = 0; j < NDT / 2; ++j) {
+                    const int ch = 2 * j + (lane >> 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(b0, b1, b2, b3, vsm + (uint32_t)(ch >> 3) * kHalfTile +
+                                                  (uint32_t)(vkey * 128 + (((ch & 7) ^ (vkey & 7)) << 4)));
+                    mma_f16(o[2 * j], pa, b0, b1);
+                    mma_f16(o[2 * j + 1], pa, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) dla::mbar_arrive(&empty[st]);      // the stage is free for the producer
+        }
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+        if (attn_consumers_any(bad)) {
+            poison_partials();
+            return;
+        }
+    #pragma unroll
+        for (int j = 0; j < NDT; ++j) {
+            *reinterpret_cast<float2 *>(co + (warp * 16 + g) * CP + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
+            *reinterpret_cast<float2 *>(co + (warp * 16 + g + 8) * CP + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
+        }
+        if (c == 0) {
+            cm[warp * 16 + g] = m0;
+            cm[warp * 16 + g + 8] = m1;
+            cl[warp * 16 + g] = l0;
+            cl[warp * 16 + g + 8] = l1;
+        }
+    } else {
+        // ---- CUDA-core form: warp (query group qg of up to 8 queries, stage group sg); lane = key
+        // for the scores, lanes over the dimensions for P.V
+        constexpr int QM = 8;
+        constexpr int DPL = D / 32;                 // dimensions per lane
+        const int qg = warp % NT, sg = warp / NT;
+        const int qb = qg * QM, nq = min(QM, Q - qb);
+        float *qs = reinterpret_cast<float *>(qfrag);   // [Q][D] f32, log2-domain scaled
+        for (int e = tid; e < Q * D; e += kMmaConsumers * 32) {
+            const int qi = e / D, d = e - qi * D;
+            qs[e] = __ldcg(a.q + (int64_t)s_row[s_qrow[qi]] * a.q_stride + (h * G + s_qhead[qi]) * D + d) * a.qscale;
+        }
+        dla::named_sync(1, kMmaConsumers * 32);
+        int lenq[QM];
 #pragma unroll
-    for (int j = 0; j < NDT; ++j) {
-        *reinterpret_cast<float2 *>(co + (warp * 16 + g) * D + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
-        *reinterpret_cast<float2 *>(co + (warp * 16 + g + 8) * D + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
-    }
-    if (c == 0) {
-        cm[warp * 16 + g] = m0;
-        cm[warp * 16 + g + 8] = m1;
-        cl[warp * 16 + g] = l0;
-        cl[warp * 16 + g + 8] = l1;
+        for (int q = 0; q < QM; ++q) lenq[q] = q < nq ? s_len[s_qrow[qb + q]] : 0;
+        float o[QM][DPL], mq[QM], lq[QM];
+#pragma unroll
+        for (int q = 0; q < QM; ++q) {
+            mq[q] = -INFINITY;
+            lq[q] = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[q][e] = 0.f;
+        }
+        const int d0 = DPL * lane, dch = d0 >> 3;
+        for (int i = sg; sg < NS && i < nst; i += NS) {
+            const int st = i % S;
+            if (!__all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((i / S) & 1)))) {
+                bad = true;
+                break;
+            }
+            const unsigned char *kst = ring + (size_t)st * kStageBytes;
+            const unsigned char *vst = kst + kStageBytes / 2;
+            const int kb0 = k0 + i * kStKeys;
+            if (kb0 + kStKeys > k1) {
+                // keys past the piece may hold anything (even NaN) in the V rows: zero them
+                unsigned char *vrow = ring + (size_t)st * kStageBytes + kStageBytes / 2;
+                for (int e = lane; e < NH * kStKeys * 8; e += 32) {
+                    const int hf = e / (kStKeys * 8), rem = e - hf * kStKeys * 8;
+                    if (kb0 + (rem >> 3) >= k1)
+                        *reinterpret_cast<uint4 *>(vrow + hf * kHalfTile + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                dla::fence_proxy_async();
+                __syncwarp();
+            }
+            // scores: lane = key, its row read 16 bytes at a time through the swizzle
+            float sc[QM];
+#pragma unroll
+            for (int q = 0; q < QM; ++q) sc[q] = 0.f;
+#pragma unroll 4
+            for (int ch = 0; ch < D / 8; ++ch) {
+                const uint4 kv = *reinterpret_cast<const uint4 *>(kst + (ch >> 3) * kHalfTile + lane * 128 +
+                                                                  (((ch & 7) ^ (lane & 7)) << 4));
+                const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kv.x));
+                const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kv.y));
+                const float2 k45 = __half22float2(*reinterpret_cast<const __half2 *>(&kv.z));
+                const float2 k67 = __half22float2(*reinterpret_cast<const __half2 *>(&kv.w));
+#pragma unroll
+                for (int q = 0; q < QM; ++q) {
+                    if (q < nq) {
+                        const float4 qa = *reinterpret_cast<const float4 *>(qs + (qb + q) * D + ch * 8);
+                        const float4 qc = *reinterpret_cast<const float4 *>(qs + (qb + q) * D + ch * 8 + 4);
+                        float t = sc[q];
+                        t = fmaf(qa.x, k01.x, t);
+                        t = fmaf(qa.y, k01.y, t);
+                        t = fmaf(qa.z, k23.x, t);
+                        t = fmaf(qa.w, k23.y, t);
+                        t = fmaf(qc.x, k45.x, t);
+                        t = fmaf(qc.y, k45.y, t);
+                        t = fmaf(qc.z, k67.x, t);
+                        t = fmaf(qc.w, k67.y, t);
+                        sc[q] = t;
+                    }
+                }
+            }
+            // online softmax per query over the stage's 32 keys
+            const int key = kb0 + lane;
+            float ps[QM];
+#pragma unroll
+            for (int q = 0; q < QM; ++q) {
+                ps[q] = 0.f;
+                if (q >= nq) continue;
+                const float sv = key < lenq[q] ? sc[q] : -INFINITY;
+                const float mn = fmaxf(mq[q], warp_max(sv));
+                if (mn == -INFINITY) continue;             // no attended key yet (warp-uniform)
+                const float al = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mn);
+                ps[q] = sv == -INFINITY ? 0.f : exp2f(sv - mn);
+                lq[q] = lq[q] * al + warp_sum(ps[q]);
+                mq[q] = mn;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[q][e] *= al;
+            }
+            // O += P V: lane holds dimensions d0 .. d0 + DPL - 1
+            const unsigned char *vcol = vst + (dch >> 3) * kHalfTile + (d0 & 7) * 2;
+#pragma unroll 4
+            for (int j = 0; j < kStKeys; ++j) {
+                const unsigned char *vp = vcol + j * 128 + (((dch & 7) ^ (j & 7)) << 4);
+                float v[DPL];
+                if constexpr (DPL == 4) {
+                    const uint2 w = *reinterpret_cast<const uint2 *>(vp);
+                    const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+                    const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+                    v[0] = v01.x; v[1] = v01.y; v[2] = v23.x; v[3] = v23.y;
+                } else {
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(vp);
+                    const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+                    v[0] = v01.x; v[1] = v01.y;
+                }
+#pragma unroll
+                for (int q = 0; q < QM; ++q) {
+                    if (q < nq) {
+                        const float pj = __shfl_sync(0xffffffffu, ps[q], j);
+#pragma unroll
+                        for (int e = 0; e < DPL; ++e) o[q][e] = fmaf(pj, v[e], o[q][e]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) dla::mbar_arrive(&empty[st]);      // the stage is free for the producer
+        }
+        if (attn_consumers_any(bad)) {
+            poison_partials();
+            return;
+        }
+        if (sg < NS) {
+#pragma unroll
+            for (int q = 0; q < QM; ++q) {
+                if (q < nq) {
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) co[(warp * 16 + q) * CP + d0 + e] = o[q][e];
+                    if (lane == 0) {
+                        cm[warp * 16 + q] = mq[q];
+                        cl[warp * 16 + q] = lq[q];
+                    }
+                }
+            }
+        }
     }
     dla::named_sync(1, kMmaConsumers * 32);
     // one query per warp at a time, lanes over the dimensions (4 each)
     for (int qi = warp; qi < Q; qi += kMmaConsumers) {
         const int rq = s_qrow[qi], gq = s_qhead[qi];
         if (s_len[rq] <= k0) continue;
-        const int qt = qi >> 4, row = qi & 15;
+        const int qt = qi / TL, row = qi - qt * TL;
         float M = -INFINITY;
         for (int kq = 0; kq < KS; ++kq) M = fmaxf(M, cm[(kq * MT + qt) * 16 + row]);
         float f[kMmaConsumers], wsum = 0.f;
@@ -695,7 +604,7 @@ decode_attn_mma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
 #pragma unroll
             for (int kq = 0; kq < kMmaConsumers; ++kq) {
                 if (kq < KS) {
-                    const float4 v = *reinterpret_cast<const float4 *>(co + ((kq * MT + qt) * 16 + row) * D + d4 * 4);
+                    const float4 v = *reinterpret_cast<const float4 *>(co + ((kq * MT + qt) * 16 + row) * CP + d4 * 4);
                     acc.x = fmaf(f[kq], v.x, acc.x);
                     acc.y = fmaf(f[kq], v.y, acc.y);
                     acc.z = fmaf(f[kq], v.z, acc.z);
@@ -806,12 +715,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const __gr
         dst[d] = t * inv;
     }
     if (a.lse && threadIdx.x == 0) a.lse[r * a.n_q + h] = M + logf(Wt);
-}
-
-size_t attn_smem_bytes(int D)
-{
-    const int pitch = D + 8;
-    return (size_t)4 * kTile * pitch * 2 + (size_t)kMaxQ * D * 4 + (size_t)kMaxQ * kTile * 4 + 3 * kMaxQ * 4;
 }
 
 // The driver's tensor-map encoder, looked up once through the runtime (no link against the driver).
@@ -1001,25 +904,17 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
         qmax = std::max(qmax, (plan->sess_begin[si + 1] - plan->sess_begin[si]) * (plan->n_q / plan->n_kv));
     const bool mma = path == 2 || (path == 0 && qmax > kCudaCoreMaxQ);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (mma) {
-        CUtensorMap tk, tv;
-        rc = make_kv_tmap(&tk, kv->k, kv);
-        if (rc != DL_OK) return rc;
-        rc = make_kv_tmap(&tv, kv->v, kv);
-        if (rc != DL_OK) return rc;
-        const size_t smem = attn_mma_smem_bytes(plan->head_dim);
-        auto kern = plan->head_dim == 128 ? decode_attn_mma_kernel<128> : decode_attn_mma_kernel<64>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
-        return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kMmaThreads), smem, st, "dl_decode_attn: launch", a, tk,
-                              tv);
-    }
-    const size_t smem = attn_smem_bytes(plan->head_dim);
-    auto kern = plan->head_dim == 128 ? decode_attn_cc_kernel<128> : decode_attn_cc_kernel<64>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    CUtensorMap tk, tv;
+    rc = make_kv_tmap(&tk, kv->k, kv);
+    if (rc != DL_OK) return rc;
+    rc = make_kv_tmap(&tv, kv->v, kv);
+    if (rc != DL_OK) return rc;
+    const size_t smem = attn_mma_smem_bytes(plan->head_dim);
+    auto kern = plan->head_dim == 128 ? (mma ? decode_attn_tma_kernel<128, true> : decode_attn_tma_kernel<128, false>)
+                                      : (mma ? decode_attn_tma_kernel<64, true> : decode_attn_tma_kernel<64, false>);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
-    return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kAttnThreads), smem, st, "dl_decode_attn: launch", a);
+    return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kMmaThreads), smem, st, "dl_decode_attn: launch", a, tk, tv);
 }
 
 int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
