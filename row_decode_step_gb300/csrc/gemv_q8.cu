@@ -63,7 +63,9 @@ constexpr int kConsumers = 8;                        // warps, each a share of t
 constexpr int kThreads = kConsumers * 32;
 constexpr int kMaxStages = 8;
 constexpr int kStageTileBytes = 512 + 32;            // weights and scales of one k-tile
-constexpr size_t kRedBytes = (size_t)2 * kConsumers * 128 * 4;   // per-stage partials, two buffers
+constexpr int kRowBatch = 4;                         // row tiles whose partials a warp holds at once
+constexpr size_t kRedBytes = (size_t)kRowBatch * kConsumers * 128 * 4;   // one batch of per-warp partials
+constexpr int kPreWaitStages = 1;                    // ring stages requested before the wait
 
 // Shared-memory bytes of a launch: the ring, the per-stage partials and, with clusters,
 // this CTA's K-slice sums of its row tiles.
@@ -97,9 +99,11 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cas
 template <bool MMA, int NRC, int KWM>
 __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
 {
+    constexpr int RB = kRowBatch;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
-    __shared__ int s_shape_bad;
+    __shared__ int s_shape_bad, s_issued;
+    __shared__ int s_cnt[kMaxStages];                 // warps done with the stage in each slot
 
     const int S = a.stages;
     const int slice = blockIdx.x % a.cs;
@@ -110,17 +114,29 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     const uint32_t wbytes = (uint32_t)nkt * 512u, dbytes = (uint32_t)nkt * 32u;
     const size_t SB = (size_t)a.ksl * kStageTileBytes;
     unsigned char *ring = smem;
-    float *red = reinterpret_cast<float *>(smem + S * SB);          // [2][kConsumers][128]
-    float *part = red + 2 * kConsumers * 128;                       // [rpr][128] (clusters)
+    float *red = reinterpret_cast<float *>(smem + S * SB);          // [kRowBatch][kConsumers][128]
+    float *part = red + kRowBatch * kConsumers * 128;                // [rpr][128] (clusters)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int KG = a.KT >> 2;
 
     if (threadIdx.x == 0) {
-        for (int st = 0; st < S; ++st) dla::mbar_init(&full[st], 1);
+        for (int st = 0; st < S; ++st) {
+            dla::mbar_init(&full[st], 1);
+            s_cnt[st] = 0;
+        }
         s_shape_bad = 0;
+        s_issued = min(S, nrt);
         dla::mbar_init_fence();
     }
+    // a slice shorter than the stage (the last one of K): the scales of the missing k-tiles
+    // read as zero, so that whatever the stage holds there contributes nothing (never written
+    // by the copies, which carry this slice's k-tiles only)
+    if (nkt < a.ksl)
+        for (int e = threadIdx.x; e < S * (a.ksl - nkt) * 8; e += kThreads) {
+            const int st = e / ((a.ksl - nkt) * 8), w = e - st * (a.ksl - nkt) * 8;
+            reinterpret_cast<uint32_t *>(ring + st * SB + (size_t)a.ksl * 512 + (size_t)nkt * 32)[w] = 0u;
+        }
     __syncthreads();
 
     // stage j: row tile rt0 + j, this slice's k-tiles (contiguous), then their scales (contiguous)
@@ -132,9 +148,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
         dla::bulk_g2s(dst + (size_t)a.ksl * 512, a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
     };
-    // the weights do not depend on the previous kernel: fill the ring before waiting on it
+    // the weights do not depend on the previous kernel: the first stage is requested before
+    // waiting on it; the rest of the ring only after the activations' loads are in flight, so
+    // that those few latency-critical loads do not queue behind the whole ring
     if (threadIdx.x == 0) {
-        for (int j = 0; j < S && j < nrt; ++j) issue(j);
+        for (int j = 0; j < kPreWaitStages && j < S && j < nrt; ++j) issue(j);
         const int pf_end = min(nrt, S + a.l2pf);
         for (int j = S; j < pf_end; ++j) {
             const int rt = rt0 + j;
@@ -147,10 +165,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     dl_pdl_wait();
     dl_pdl_launch_dependents();
 
-    // ---- this warp's share of the slice and its activations, kept in registers
-    const int wk0 = (warp * nkt) / kConsumers, wk1 = ((warp + 1) * nkt) / kConsumers;   // slice-local
-    const int nw = min(wk1 - wk0, KWM);
-    if (lane == 0 && wk1 - wk0 > KWM) atomicExch(&s_shape_bad, 1);   // broken launch shape
+    // ---- this warp's window of KWM k-tiles of the slice and its activations, kept in registers;
+    // k-tiles past the slice (the last slice of K may be short) have zero activations and scales
+    const int wk0 = warp * KWM;                                  // slice-local
+    const int nw = max(0, min(KWM, nkt - wk0));
+    if (lane == 0 && kConsumers * KWM != a.ksl) atomicExch(&s_shape_bad, 1);   // broken launch shape
     // lane (g, c) holds inputs 2c, 2c+1 / 8+2c, 9+2c / 16+2c, 17+2c / 24+2c, 25+2c of each k-tile
     uint32_t bh[MMA ? KWM : 1][4], bl[MMA ? KWM : 1][4];
     float2 ncorr[MMA ? KWM : 1];                 // -1152 * sum(x) of columns 2c, 2c+1 per k-tile
@@ -165,12 +184,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
             const bool live = j < nw && kt * 32 < a.n_in && g < a.nr;
             const float *xr = a.x + (int64_t)g * a.x_stride + kt * 32 + 2 * c;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
+            for (int p = 0; p < 4; ++p)
                 v[j][p] = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
                                : make_float2(0.f, 0.f);
-                m = fmaxf(m, fmaxf(fabsf(v[j][p].x), fabsf(v[j][p].y)));
-            }
         }
+        if (threadIdx.x == 0)
+            for (int j = kPreWaitStages; j < S && j < nrt; ++j) issue(j);
+#pragma unroll
+        for (int j = 0; j < KWM; ++j)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) m = fmaxf(m, fmaxf(fabsf(v[j][p].x), fabsf(v[j][p].y)));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
         // power-of-two scale of activation row g over this warp's inputs: largest |x| into [2^14, 2^15)
@@ -220,24 +243,35 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
                 }
             }
         }
+        if (threadIdx.x == 0)
+            for (int j = kPreWaitStages; j < S && j < nrt; ++j) issue(j);
     }
 
+    // ---- stages in batches of RB row tiles: each warp keeps its partial of every row tile of
+    // the batch in registers; no barrier between stages (the last warp done with a stage refills
+    // its slot), one CTA-wide reduction per batch
     bool bad = false;
-    int fail_at = nrt;                                   // first stage that never arrived
-    {
-        for (int i = 0; i < nrt; ++i) {
-            const int st = i % S;
+    for (int b0 = 0; b0 < nrt; b0 += RB) {
+        const int nb = min(RB, nrt - b0);
+        float2 acc01[RB], acc23[RB];                 // tensor path: rows g, g+8 x columns 2c, 2c+1
+        float accg[RB][NRC], acch[RB][NRC];          // CUDA-core path: rows g, g+8 x activation rows
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            acc01[r] = acc23[r] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NRC; ++q) accg[r][q] = acch[r][q] = 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            if (r >= nb) break;                                      // CTA-uniform
+            const int i = b0 + r, st = i % S;
             const bool ok = __all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((i / S) & 1)));
+            if (!ok) bad = true;
             const unsigned char *sw = ring + st * SB;
             const unsigned char *sd = sw + (size_t)a.ksl * 512;
-            float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);   // rows g, g+8
-            float accg[NRC], acch[NRC];
-#pragma unroll
-            for (int r = 0; r < NRC; ++r) accg[r] = acch[r] = 0.f;
             if (ok) {
 #pragma unroll
                 for (int j = 0; j < KWM; ++j) {
-                    if (j >= nw) break;
                     const int kl = wk0 + j;                                  // slice-local k-tile
                     const uint4 w = *reinterpret_cast<const uint4 *>(sw + kl * 512 + lane * 16);
                     const __half2 sp = *reinterpret_cast<const __half2 *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4);
@@ -253,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
                         const uint32_t a6 = u8x2_to_h2(w.w, 0x4140u), a7 = u8x2_to_h2(w.w, 0x4342u);
                         mma16816(t, a4, a5, a6, a7, bh[j][2], bh[j][3]);
                         mma16816(t, a4, a5, a6, a7, bl[j][2], bl[j][3]);
-                        acc01 = __ffma2_rn(make_float2(dg, dg), __fadd2_rn(make_float2(t[0], t[1]), ncorr[j]), acc01);
-                        acc23 = __ffma2_rn(make_float2(dh, dh), __fadd2_rn(make_float2(t[2], t[3]), ncorr[j]), acc23);
+                        acc01[r] = __ffma2_rn(make_float2(dg, dg), __fadd2_rn(make_float2(t[0], t[1]), ncorr[j]), acc01[r]);
+                        acc23[r] = __ffma2_rn(make_float2(dh, dh), __fadd2_rn(make_float2(t[2], t[3]), ncorr[j]), acc23[r]);
                     } else {
                         // row g: bytes 0, 1 of each word; row g+8: bytes 2, 3
                         const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
@@ -267,74 +301,89 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
                             wh[2 * p + 1] = u8_to_f32(wd[p], 3);
                         }
 #pragma unroll
-                        for (int r = 0; r < NRC; ++r) {
-                            float sg = wg[0] * xv[j][r][0], sh = wh[0] * xv[j][r][0];
+                        for (int q = 0; q < NRC; ++q) {
+                            float sg = wg[0] * xv[j][q][0], sh = wh[0] * xv[j][q][0];
 #pragma unroll
                             for (int e = 1; e < 8; ++e) {
-                                sg = fmaf(wg[e], xv[j][r][e], sg);
-                                sh = fmaf(wh[e], xv[j][r][e], sh);
+                                sg = fmaf(wg[e], xv[j][q][e], sg);
+                                sh = fmaf(wh[e], xv[j][q][e], sh);
                             }
-                            accg[r] = fmaf(dg, sg, accg[r]);
-                            acch[r] = fmaf(dh, sh, acch[r]);
+                            accg[r][q] = fmaf(dg, sg, accg[r][q]);
+                            acch[r][q] = fmaf(dh, sh, acch[r][q]);
                         }
                     }
                 }
             }
-            // this warp's partial of the row tile: [row 0..15][column 0..7]
-            float *rw = red + ((i & 1) * kConsumers + warp) * 128;
+            // the last warp done with this stage refills its slot (every warp has read it: the
+            // values sit in registers)
+            __syncwarp();
+            if (lane == 0 && atomicAdd(&s_cnt[st], 1) == kConsumers - 1) {
+                s_cnt[st] = 0;
+                if (i + S < nrt) {
+                    issue(i + S);
+                    s_issued = i + S + 1;
+                }
+            }
+        }
+        // this warp's partials of the batch: [row tile][warp][row 0..15][column 0..7]
+        __syncthreads();                                   // the previous batch's reduction is done
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            if (r >= nb) break;
+            float *rw = red + (r * kConsumers + warp) * 128;
             if constexpr (MMA) {
-                *reinterpret_cast<float2 *>(rw + g * 8 + 2 * c) = make_float2(acc01.x * us0, acc01.y * us1);
-                *reinterpret_cast<float2 *>(rw + (g + 8) * 8 + 2 * c) = make_float2(acc23.x * us0, acc23.y * us1);
+                *reinterpret_cast<float2 *>(rw + g * 8 + 2 * c) = make_float2(acc01[r].x * us0, acc01[r].y * us1);
+                *reinterpret_cast<float2 *>(rw + (g + 8) * 8 + 2 * c) = make_float2(acc23[r].x * us0, acc23[r].y * us1);
             } else {
 #pragma unroll
-                for (int r = 0; r < NRC; ++r) {
-                    float vg = accg[r], vh = acch[r];
+                for (int q = 0; q < NRC; ++q) {
+                    float vg = accg[r][q], vh = acch[r][q];
                     vg += __shfl_xor_sync(0xffffffffu, vg, 1);
                     vg += __shfl_xor_sync(0xffffffffu, vg, 2);
                     vh += __shfl_xor_sync(0xffffffffu, vh, 1);
                     vh += __shfl_xor_sync(0xffffffffu, vh, 2);
                     if (c == 0) {
-                        rw[g * 8 + r] = vg;
-                        rw[(g + 8) * 8 + r] = vh;
+                        rw[g * 8 + q] = vg;
+                        rw[(g + 8) * 8 + q] = vh;
                     }
                 }
             }
-            // every warp is done with stage i (its slot may be refilled) and has parked its partial
-            if (__syncthreads_or(!ok)) {       // a stage that never arrived: stop (all warps alike)
-                bad = true;
-                fail_at = i;
-                break;
+        }
+        if (__syncthreads_or(bad)) {                       // a stage that never arrived: stop
+            bad = true;
+            break;
+        }
+        // sum the 8 warps' partials in warp order: thread -> 4 consecutive elements of a row tile
+        for (int e4 = threadIdx.x; e4 < nb * 32; e4 += kThreads) {
+            const int r = e4 >> 5, el = (e4 & 31) * 4;
+            const float *rb = red + r * kConsumers * 128 + el;
+            float4 sum = *reinterpret_cast<const float4 *>(rb);
+#pragma unroll
+            for (int w = 1; w < kConsumers; ++w) {
+                const float4 t = *reinterpret_cast<const float4 *>(rb + w * 128);
+                sum.x += t.x;
+                sum.y += t.y;
+                sum.z += t.z;
+                sum.w += t.w;
             }
-            if (warp == i % kConsumers) {
-                if (lane == 0 && i + S < nrt) issue(i + S);     // refill the slot
-                // owner warp: sum the 8 partials in warp order; lane holds elements 4 lane .. 4 lane + 3
-                const float *rb = red + (i & 1) * kConsumers * 128 + lane * 4;
-                float4 s = *reinterpret_cast<const float4 *>(rb);
+            const int i = b0 + r;
+            if (a.cs == 1) {
+                const int o = (rt0 + i) * 16 + (el >> 3), col0 = el & 7;
+                if (o < a.n_out) {
+                    const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-                for (int w = 1; w < kConsumers; ++w) {
-                    const float4 t = *reinterpret_cast<const float4 *>(rb + w * 128);
-                    s.x += t.x;
-                    s.y += t.y;
-                    s.z += t.z;
-                    s.w += t.w;
+                    for (int q = 0; q < 4; ++q)
+                        if (col0 + q < a.nr) a.y[(int64_t)(col0 + q) * a.y_stride + o] = sv[q];
                 }
-                if (a.cs == 1) {
-                    const int o = (rt0 + i) * 16 + (lane >> 1), col0 = (lane & 1) * 4;
-                    if (o < a.n_out) {
-                        const float sv[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (col0 + q < a.nr) a.y[(int64_t)(col0 + q) * a.y_stride + o] = sv[q];
-                    }
-                } else {
-                    *reinterpret_cast<float4 *>(part + i * 128 + lane * 4) = s;
-                }
+            } else {
+                *reinterpret_cast<float4 *>(part + i * 128 + el) = sum;
             }
         }
     }
     if (bad && threadIdx.x == 0) {
         // do not leave with copies in flight: wait (bounded) for every stage that may still land
-        for (int j = fail_at; j < nrt && j < fail_at + S; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
+        const int hi = s_issued;
+        for (int j = max(0, hi - S); j < hi; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
     }
     const bool failed = __syncthreads_or(bad || s_shape_bad) != 0;
 
@@ -465,15 +514,6 @@ void *pick_kernel(bool mma, int nrc, int kwm)
     return nullptr;
 }
 
-int kwm_for(bool mma, int nrc, int kw)
-{
-    if (kw <= 1) return 1;
-    if (kw <= 2) return 2;
-    if (kw <= 4) return 4;
-    if (mma) return kw <= 6 ? 6 : 0;
-    return (nrc == 1 && kw <= 8) ? 8 : 0;
-}
-
 // The dynamic shared-memory limit is a per-function attribute shared by every launch of the
 // kernel (graph nodes and profilers re-launch against it): set it once to the largest size any
 // launch shape may use, never to one launch's own size.
@@ -566,8 +606,8 @@ bool two_per_sm(const void *kern)
     return false;
 }
 
-// Launch shape.  K is cut into cs slices of ksl k-tiles (whole groups of 4, at most 8 x kwm
-// per slice so that every warp holds its activations in registers); each CTA takes rpr
+// Launch shape.  K is cut into cs slices of ksl = 8 x kwm k-tiles (every warp holds the
+// activations of its kwm k-tiles in registers; the last slice may be short); each CTA takes rpr
 // consecutive row tiles of one slice and streams them one row tile per ring stage.  Among the
 // shapes that run in one wave with two CTAs per SM, the least bytes per CTA wins (near-ties go
 // to fewer slices).  Matrices too tall for one wave run in several.
@@ -578,13 +618,12 @@ int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
     const int nrc = mma ? 1 : nr;
     GemvCfg best{};
     long best_cost = -1;
-    for (int cs = 1; cs <= 16; ++cs) {
-        const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
-        if ((int)dl::ceil_div(KT, ksl) != cs) continue;
-        const int kwm = kwm_for(mma, nrc, (int)dl::ceil_div(ksl, kConsumers));
-        if (kwm == 0) continue;
+    for (int kwm : {8, 6, 4, 2, 1}) {                           // fewer slices first
         const void *kern = pick_kernel(mma, nrc, kwm);
         if (!kern) continue;
+        const int ksl = kConsumers * kwm;
+        const int cs = (int)dl::ceil_div(KT, ksl);
+        if (cs > 16) continue;
         const int nc1 = cs == 1 ? sm : clusters_one_per_sm(kern, cs);
         if (nc1 < 1) continue;
         const size_t sb = (size_t)ksl * kStageTileBytes;
@@ -609,11 +648,12 @@ int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
     if (best_cost < 0) {
         // no one-wave shape (very many row tiles): CTAs of as many row tiles as shared memory
         // holds, in several waves
-        for (int cs = 1; cs <= 16 && best_cost < 0; ++cs) {
-            const int ksl = (int)dl::ceil_div(dl::ceil_div(KT, cs), 4) * 4;
-            if ((int)dl::ceil_div(KT, ksl) != cs) continue;
-            const int kwm = kwm_for(mma, nrc, (int)dl::ceil_div(ksl, kConsumers));
-            if (kwm == 0 || !pick_kernel(mma, nrc, kwm)) continue;
+        for (int kwm : {8, 6, 4, 2, 1}) {
+            if (best_cost >= 0) break;
+            if (!pick_kernel(mma, nrc, kwm)) continue;
+            const int ksl = kConsumers * kwm;
+            const int cs = (int)dl::ceil_div(KT, ksl);
+            if (cs > 16) continue;
             const size_t sb = (size_t)ksl * kStageTileBytes;
             int stages = (int)(kRingBudget / sb);
             stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
