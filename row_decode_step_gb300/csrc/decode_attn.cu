@@ -112,6 +112,7 @@ constexpr int kMmaConsumers = 4;             // consumer warps
 constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 constexpr int kMmaMaxStages = 8;
 constexpr int kHalfTile = kStKeys * 128;     // bytes of 32 keys x 64 dims (one swizzled box)
+constexpr int kAttnPreWaitStages = 2;        // stages requested before the wait on the previous kernel
 
 // Ring depth per head dimension: two CTAs fit on an SM.
 __host__ __device__ constexpr int mma_stages(int D) { return D == 128 ? 5 : 8; }
@@ -133,7 +134,7 @@ __device__ __forceinline__ bool attn_consumers_any(bool flag)
     return r != 0;
 }
 
-template <int D, bool MMA>
+template <int D, bool MMA, int QM>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv)
@@ -146,7 +147,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     const dl_attn_plan &P = a.plan;
 
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t full[kMmaMaxStages], empty[kMmaMaxStages];
+    __shared__ __align__(8) uint64_t full[kMmaMaxStages], empty[kMmaMaxStages], qbar;
     __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS];
     __shared__ unsigned char s_qrow[kMaxQ], s_qhead[kMaxQ];   // query -> (session row, head in group)
     // the swizzled boxes want 1024-byte aligned destinations
@@ -167,7 +168,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     const bool producer = warp == kMmaConsumers;
 
     // warps: NT query tiles (16 queries, tensor form; 8, CUDA-core form) x NS stage groups
-    const int TL = MMA ? 16 : 8;
+    const int TL = MMA ? 16 : QM;
     const int NT = (Q + TL - 1) / TL;
     const int NS = kMmaConsumers / NT;
     const int MT = NT, KS = NS;
@@ -176,6 +177,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             dla::mbar_init(&full[i], 1);
             dla::mbar_init(&empty[i], (uint32_t)NT);   // released by the warps of one stage group
         }
+        dla::mbar_init(&qbar, kMmaConsumers);          // every consumer warp has its queries
         dla::mbar_init_fence();
     }
     // the key counts come from the caller, not from the previous kernel: read them now
@@ -209,9 +211,13 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         if (lane == 0) {
             dla::prefetch_tmap(&tk);
             dla::prefetch_tmap(&tv);
-            // keys below the lowest slot this command writes are final before the previous kernel ends
+            // keys below the lowest slot this command writes are final before the previous kernel ends:
+            // the first few such stages are requested before waiting on it; the rest only once the
+            // consumers hold their queries, so that those latency-critical loads do not queue behind
+            // the whole ring
             const int stable = lmin - 1;
             const int nstable = k1 <= stable ? nst : max(0, (stable - k0) / kStKeys);
+            const int npre = min(nstable, kAttnPreWaitStages);
             bool waited = false;
             int i = 0;
             for (; i < nst; ++i) {
@@ -220,9 +226,13 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     bad = true;
                     break;
                 }
-                if (!waited && i >= nstable) {
+                if (!waited && i >= npre) {
                     dl_pdl_wait();
                     waited = true;
+                    if (!dla::mbar_wait(&qbar, 0u)) {
+                        bad = true;
+                        break;
+                    }
                 }
                 unsigned char *kd = ring + (size_t)st * kStageBytes;
                 unsigned char *vd = kd + kStageBytes / 2;
@@ -294,6 +304,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             dst[32] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
         }
+        __syncwarp();
+        if (lane == 0) dla::mbar_arrive(&qbar);
         dla::named_sync(1, kMmaConsumers * 32);
         const unsigned char *myq = qfrag + (size_t)mt * NKS * 1024 + lane * 16;
         const int r0 = mt * 16 + g, r1 = r0 + 8;
@@ -441,9 +453,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             cl[warp * 16 + g + 8] = l1;
         }
     } else {
-        // ---- CUDA-core form: warp (query group qg of up to 8 queries, stage group sg); lane = key
+        // ---- CUDA-core form: warp (query group qg of up to QM queries, stage group sg); lane = key
         // for the scores, lanes over the dimensions for P.V
-        constexpr int QM = 8;
         constexpr int DPL = D / 32;                 // dimensions per lane
         const int qg = warp % NT, sg = warp / NT;
         const int qb = qg * QM, nq = min(QM, Q - qb);
@@ -452,6 +463,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             const int qi = e / D, d = e - qi * D;
             qs[e] = __ldcg(a.q + (int64_t)s_row[s_qrow[qi]] * a.q_stride + (h * G + s_qhead[qi]) * D + d) * a.qscale;
         }
+        __syncwarp();
+        if (lane == 0) dla::mbar_arrive(&qbar);
         dla::named_sync(1, kMmaConsumers * 32);
         int lenq[QM];
 #pragma unroll
@@ -486,10 +499,10 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 __syncwarp();
             }
             // scores: lane = key, its row read 16 bytes at a time through the swizzle
-            float sc[QM];
+            float sc[QM], sd[QM];                  // two partial sums per score: even, odd chunks
 #pragma unroll
-            for (int q = 0; q < QM; ++q) sc[q] = 0.f;
-#pragma unroll 4
+            for (int q = 0; q < QM; ++q) sc[q] = sd[q] = 0.f;
+#pragma unroll 2
             for (int ch = 0; ch < D / 8; ++ch) {
                 const uint4 kv = *reinterpret_cast<const uint4 *>(kst + (ch >> 3) * kHalfTile + lane * 128 +
                                                                   (((ch & 7) ^ (lane & 7)) << 4));
@@ -502,7 +515,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     if (q < nq) {
                         const float4 qa = *reinterpret_cast<const float4 *>(qs + (qb + q) * D + ch * 8);
                         const float4 qc = *reinterpret_cast<const float4 *>(qs + (qb + q) * D + ch * 8 + 4);
-                        float t = sc[q];
+                        float t = (ch & 1) ? sd[q] : sc[q];
                         t = fmaf(qa.x, k01.x, t);
                         t = fmaf(qa.y, k01.y, t);
                         t = fmaf(qa.z, k23.x, t);
@@ -511,7 +524,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                         t = fmaf(qc.y, k45.y, t);
                         t = fmaf(qc.z, k67.x, t);
                         t = fmaf(qc.w, k67.y, t);
-                        sc[q] = t;
+                        if (ch & 1) sd[q] = t; else sc[q] = t;
                     }
                 }
             }
@@ -522,7 +535,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             for (int q = 0; q < QM; ++q) {
                 ps[q] = 0.f;
                 if (q >= nq) continue;
-                const float sv = key < lenq[q] ? sc[q] : -INFINITY;
+                const float sv = key < lenq[q] ? sc[q] + sd[q] : -INFINITY;
                 const float mn = fmaxf(mq[q], warp_max(sv));
                 if (mn == -INFINITY) continue;             // no attended key yet (warp-uniform)
                 const float al = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mn);
@@ -579,42 +592,52 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         }
     }
     dla::named_sync(1, kMmaConsumers * 32);
-    // one query per warp at a time, lanes over the dimensions (4 each)
-    for (int qi = warp; qi < Q; qi += kMmaConsumers) {
-        const int rq = s_qrow[qi], gq = s_qhead[qi];
-        if (s_len[rq] <= k0) continue;
+    // per query: the warps' weights and the normaliser (one thread each), then the weighted
+    // sums with every thread on independent (query, 4 dimensions) elements
+    float *cf = cl + kMmaConsumers * 16;               // [kMaxQ][kMmaConsumers + 1]: weights, 1/sum
+    if (tid < Q) {
+        const int qi = tid;
         const int qt = qi / TL, row = qi - qt * TL;
         float M = -INFINITY;
         for (int kq = 0; kq < KS; ++kq) M = fmaxf(M, cm[(kq * MT + qt) * 16 + row]);
-        float f[kMmaConsumers], wsum = 0.f;
+        float wsum = 0.f;
+        for (int kq = 0; kq < kMmaConsumers; ++kq) {
+            float f = 0.f;
+            if (kq < KS) {
+                const float mw = cm[(kq * MT + qt) * 16 + row];
+                f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                wsum += f * cl[(kq * MT + qt) * 16 + row];
+            }
+            cf[qi * (kMmaConsumers + 1) + kq] = f;
+        }
+        cf[qi * (kMmaConsumers + 1) + kMmaConsumers] = 1.f / wsum;
+        const int rq = s_qrow[qi];
+        if (s_len[rq] > k0)
+            a.part_lse[((int64_t)s_row[rq] * P.n_q + h * G + s_qhead[qi]) * ms + piece] =
+                (M + log2f(wsum)) * 0.69314718055994530942f;
+    }
+    dla::named_sync(1, kMmaConsumers * 32);
+    for (int e = tid; e < Q * (D / 4); e += kMmaConsumers * 32) {
+        const int qi = e / (D / 4), d4 = e - qi * (D / 4);
+        const int rq = s_qrow[qi];
+        if (s_len[rq] <= k0) continue;
+        const int qt = qi / TL, row = qi - qt * TL;
+        const float *f = cf + qi * (kMmaConsumers + 1);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int kq = 0; kq < kMmaConsumers; ++kq) {
-            f[kq] = 0.f;
             if (kq < KS) {
-                const int w = kq * MT + qt;
-                const float mw = cm[w * 16 + row];
-                f[kq] = mw == -INFINITY ? 0.f : exp2f(mw - M);
-                wsum += f[kq] * cl[w * 16 + row];
+                const float4 v = *reinterpret_cast<const float4 *>(co + ((kq * MT + qt) * 16 + row) * CP + d4 * 4);
+                acc.x = fmaf(f[kq], v.x, acc.x);
+                acc.y = fmaf(f[kq], v.y, acc.y);
+                acc.z = fmaf(f[kq], v.z, acc.z);
+                acc.w = fmaf(f[kq], v.w, acc.w);
             }
         }
-        const float inv = 1.f / wsum;
-        const int64_t pidx = ((int64_t)s_row[rq] * P.n_q + h * G + gq) * ms + piece;
-        for (int d4 = lane; d4 < D / 4; d4 += 32) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int kq = 0; kq < kMmaConsumers; ++kq) {
-                if (kq < KS) {
-                    const float4 v = *reinterpret_cast<const float4 *>(co + ((kq * MT + qt) * 16 + row) * CP + d4 * 4);
-                    acc.x = fmaf(f[kq], v.x, acc.x);
-                    acc.y = fmaf(f[kq], v.y, acc.y);
-                    acc.z = fmaf(f[kq], v.z, acc.z);
-                    acc.w = fmaf(f[kq], v.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4 *>(a.part_o + pidx * D + d4 * 4) =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        }
-        if (lane == 0) a.part_lse[pidx] = (M + log2f(wsum)) * 0.69314718055994530942f;
+        const float inv = f[kMmaConsumers];
+        const int64_t pidx = ((int64_t)s_row[rq] * P.n_q + h * G + s_qhead[qi]) * ms + piece;
+        *reinterpret_cast<float4 *>(a.part_o + pidx * D + d4 * 4) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
 }
 
@@ -910,8 +933,13 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     rc = make_kv_tmap(&tv, kv->v, kv);
     if (rc != DL_OK) return rc;
     const size_t smem = attn_mma_smem_bytes(plan->head_dim);
-    auto kern = plan->head_dim == 128 ? (mma ? decode_attn_tma_kernel<128, true> : decode_attn_tma_kernel<128, false>)
-                                      : (mma ? decode_attn_tma_kernel<64, true> : decode_attn_tma_kernel<64, false>);
+    // the CUDA-core form holds the queries of a warp in registers: 4 for one-row sessions, else 8
+    const bool few = qmax <= 4;
+    auto kern = plan->head_dim == 128
+                    ? (mma ? decode_attn_tma_kernel<128, true, 8>
+                           : few ? decode_attn_tma_kernel<128, false, 4> : decode_attn_tma_kernel<128, false, 8>)
+                    : (mma ? decode_attn_tma_kernel<64, true, 8>
+                           : few ? decode_attn_tma_kernel<64, false, 4> : decode_attn_tma_kernel<64, false, 8>);
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
     return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kMmaThreads), smem, st, "dl_decode_attn: launch", a, tk, tv);

@@ -56,6 +56,8 @@ struct GemvArgs {
     int ksl;                // k-tiles per K-slice (multiple of 4)
     int rpr;                // row tiles per CTA
     int stages;             // ring depth
+    int pre;                // ring stages requested before the wait (0 or 1)
+    int xpitch;             // bytes between activation rows staged in shared memory
     int l2pf;               // stages past the ring prefetched into L2 before the wait
 };
 
@@ -65,7 +67,6 @@ constexpr int kMaxStages = 8;
 constexpr int kStageTileBytes = 512 + 32;            // weights and scales of one k-tile
 constexpr int kRowBatch = 4;                         // row tiles whose partials a warp holds at once
 constexpr size_t kRedBytes = (size_t)kRowBatch * kConsumers * 128 * 4;   // one batch of per-warp partials
-constexpr int kPreWaitStages = 1;                    // ring stages requested before the wait
 
 // Shared-memory bytes of a launch: the ring, the per-stage partials and, with clusters,
 // this CTA's K-slice sums of its row tiles.
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
 {
     constexpr int RB = kRowBatch;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ __align__(8) uint64_t full[kMaxStages], xbar;
     __shared__ int s_shape_bad, s_issued;
     __shared__ int s_cnt[kMaxStages];                 // warps done with the stage in each slot
 
@@ -125,18 +126,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
             dla::mbar_init(&full[st], 1);
             s_cnt[st] = 0;
         }
+        dla::mbar_init(&xbar, 1);
         s_shape_bad = 0;
         s_issued = min(S, nrt);
         dla::mbar_init_fence();
     }
     // a slice shorter than the stage (the last one of K): the scales of the missing k-tiles
-    // read as zero, so that whatever the stage holds there contributes nothing (never written
-    // by the copies, which carry this slice's k-tiles only)
-    if (nkt < a.ksl)
-        for (int e = threadIdx.x; e < S * (a.ksl - nkt) * 8; e += kThreads) {
-            const int st = e / ((a.ksl - nkt) * 8), w = e - st * (a.ksl - nkt) * 8;
-            reinterpret_cast<uint32_t *>(ring + st * SB + (size_t)a.ksl * 512 + (size_t)nkt * 32)[w] = 0u;
-        }
+    // read as zero, so that whatever the stage holds there contributes nothing (the copies carry
+    // this slice's k-tiles only).  Slots at and past `pre` hold the staged activations first and
+    // are cleared later, before their first stage is requested.
+    auto zero_scale_tail = [&](int st, int t0, int nt) {
+        uint32_t *z = reinterpret_cast<uint32_t *>(ring + st * SB + (size_t)a.ksl * 512 + (size_t)nkt * 32);
+        for (int w = t0; w < (a.ksl - nkt) * 8; w += nt) z[w] = 0u;
+    };
+    if (nkt < a.ksl && a.pre > 0) zero_scale_tail(0, threadIdx.x, kThreads);
     __syncthreads();
 
     // stage j: row tile rt0 + j, this slice's k-tiles (contiguous), then their scales (contiguous)
@@ -148,11 +151,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
         dla::bulk_g2s(dst + (size_t)a.ksl * 512, a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
     };
-    // the weights do not depend on the previous kernel: the first stage is requested before
-    // waiting on it; the rest of the ring only after the activations' loads are in flight, so
-    // that those few latency-critical loads do not queue behind the whole ring
+    // the weights do not depend on the previous kernel: the first stage may be requested before
+    // waiting on it.  The activations of this K-slice then arrive as whole lines (one bulk copy
+    // per activation row) in ring slots not yet in use, ahead of the rest of the ring: activation
+    // lines are read by every CTA of the slice, and line-sized requests keep that traffic small
     if (threadIdx.x == 0) {
-        for (int j = 0; j < kPreWaitStages && j < S && j < nrt; ++j) issue(j);
+        for (int j = 0; j < a.pre && j < nrt; ++j) issue(j);
         const int pf_end = min(nrt, S + a.l2pf);
         for (int j = S; j < pf_end; ++j) {
             const int rt = rt0 + j;
@@ -165,11 +169,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     dl_pdl_wait();
     dl_pdl_launch_dependents();
 
+    const unsigned char *xs = ring + (size_t)a.pre * SB;        // staged activation rows
+    const int xfl = max(0, min(nkt * 32, a.n_in - kt0 * 32));   // valid inputs of the slice
+    if (threadIdx.x == 0) {
+        dla::mbar_expect_tx(&xbar, (uint32_t)(a.nr * xfl * 4));
+        if (xfl > 0)
+            for (int r = 0; r < a.nr; ++r)
+                dla::bulk_g2s(ring + (size_t)a.pre * SB + (size_t)r * a.xpitch, a.x + (int64_t)r * a.x_stride + kt0 * 32,
+                              (uint32_t)(xfl * 4), &xbar);
+    }
+    const bool xok = __all_sync(0xffffffffu, dla::mbar_wait(&xbar, 0u));
+
     // ---- this warp's window of KWM k-tiles of the slice and its activations, kept in registers;
     // k-tiles past the slice (the last slice of K may be short) have zero activations and scales
     const int wk0 = warp * KWM;                                  // slice-local
     const int nw = max(0, min(KWM, nkt - wk0));
-    if (lane == 0 && kConsumers * KWM != a.ksl) atomicExch(&s_shape_bad, 1);   // broken launch shape
+    if (lane == 0 && (kConsumers * KWM != a.ksl || !xok)) atomicExch(&s_shape_bad, 1);   // broken shape
     // lane (g, c) holds inputs 2c, 2c+1 / 8+2c, 9+2c / 16+2c, 17+2c / 24+2c, 25+2c of each k-tile
     uint32_t bh[MMA ? KWM : 1][4], bl[MMA ? KWM : 1][4];
     float2 ncorr[MMA ? KWM : 1];                 // -1152 * sum(x) of columns 2c, 2c+1 per k-tile
@@ -180,20 +195,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         float m = 0.f;
 #pragma unroll
         for (int j = 0; j < KWM; ++j) {
-            const int kt = kt0 + wk0 + j;
-            const bool live = j < nw && kt * 32 < a.n_in && g < a.nr;
-            const float *xr = a.x + (int64_t)g * a.x_stride + kt * 32 + 2 * c;
+            const int kl = wk0 + j;
+            const bool live = xok && kl * 32 < xfl && g < a.nr;
+            const float *xr = reinterpret_cast<const float *>(xs + (size_t)g * a.xpitch) + kl * 32 + 2 * c;
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
-                v[j][p] = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
-                               : make_float2(0.f, 0.f);
+            for (int p = 0; p < 4; ++p) {
+                v[j][p] = live ? *reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8) : make_float2(0.f, 0.f);
+                m = fmaxf(m, fmaxf(fabsf(v[j][p].x), fabsf(v[j][p].y)));
+            }
         }
-        if (threadIdx.x == 0)
-            for (int j = kPreWaitStages; j < S && j < nrt; ++j) issue(j);
-#pragma unroll
-        for (int j = 0; j < KWM; ++j)
-#pragma unroll
-            for (int p = 0; p < 4; ++p) m = fmaxf(m, fmaxf(fabsf(v[j][p].x), fabsf(v[j][p].y)));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
         // power-of-two scale of activation row g over this warp's inputs: largest |x| into [2^14, 2^15)
@@ -229,22 +239,29 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     } else {
 #pragma unroll
         for (int j = 0; j < KWM; ++j) {
-            const int kt = kt0 + wk0 + j;
+            const int kl = wk0 + j;
 #pragma unroll
             for (int r = 0; r < NRC; ++r) {
-                const bool live = j < nw && kt * 32 < a.n_in && r < a.nr;
-                const float *xr = a.x + (int64_t)r * a.x_stride + kt * 32 + 2 * c;
+                const bool live = xok && kl * 32 < xfl && r < a.nr;
+                const float *xr = reinterpret_cast<const float *>(xs + (size_t)r * a.xpitch) + kl * 32 + 2 * c;
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    const float2 t = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
+                    const float2 t = live ? *reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8)
                                           : make_float2(0.f, 0.f);
                     xv[j][r][2 * p] = t.x;
                     xv[j][r][2 * p + 1] = t.y;
                 }
             }
         }
-        if (threadIdx.x == 0)
-            for (int j = kPreWaitStages; j < S && j < nrt; ++j) issue(j);
+    }
+    // every warp holds its activations: the slots they were staged in join the ring
+    __syncthreads();
+    if (warp == 0) {
+        if (nkt < a.ksl)
+            for (int st = a.pre; st < S; ++st) zero_scale_tail(st, lane, 32);
+        __syncwarp();
+        if (lane == 0)
+            for (int j = a.pre; j < S && j < nrt; ++j) issue(j);
     }
 
     // ---- stages in batches of RB row tiles: each warp keeps its partial of every row tile of
@@ -686,6 +703,13 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     a.rpr = cfg.rpr;
     a.stages = cfg.stages;
     a.l2pf = 0;
+    // the activation rows are staged in the ring slots after the pre-issued one (16-byte pad per
+    // row: the fragment reads spread over the banks); without room, nothing is pre-issued
+    a.xpitch = cfg.ksl * 128 + 16;
+    const size_t sb = (size_t)cfg.ksl * kStageTileBytes;
+    a.pre = (size_t)(cfg.stages - 1) * sb >= (size_t)nr * a.xpitch ? 1 : 0;
+    if ((size_t)cfg.stages * sb < (size_t)nr * a.xpitch)
+        return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no room to stage the activations");
     const void *kern = pick_kernel(cfg.mma, cfg.nrc, cfg.kwm);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid);
