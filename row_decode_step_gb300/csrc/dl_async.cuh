@@ -59,6 +59,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
+// Bulk copy delivered to the same shared-memory offset in every CTA of `mask` (cluster ranks),
+// each completing its own mbarrier at `bar`'s offset.
+__device__ __forceinline__ void bulk_g2s_multicast(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                                   uint16_t mask)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+                 " [%0], [%1], %2, [%3], %4;"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(mask) : "memory");
+}
 // Two-dimensional tiled copy through a tensor map (x = innermost coordinate, in elements).
 __device__ __forceinline__ void tma_g2s_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar)
 {
@@ -91,6 +100,13 @@ __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// Cluster barrier with no memory ordering: only keeps every CTA of the cluster running until
+// all have arrived (for example so that peers may still read this CTA's shared memory).
+__device__ __forceinline__ void cluster_sync_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n"
+                 "barrier.cluster.wait.aligned;\n" ::: "memory");
 }
 __device__ __forceinline__ float4 ld_dsmem_f32x4(const float *local, uint32_t rank)
 {

@@ -33,6 +33,7 @@
 // the f32 activations by FMAs.
 #include <cuda_fp16.h>
 #include <cstdio>
+#include <algorithm>
 #include <mutex>
 
 #include "dl_common.cuh"
@@ -52,7 +53,8 @@ struct GemvArgs {
     int nr;                 // rows of this command, 1..8
     int KT;                 // k-tiles, padded to a multiple of 4
     int RT;                 // row tiles
-    int cs;                 // K-slices (= cluster size)
+    int cs;                 // K-slices
+    int R;                  // row groups per cluster (a cluster is cs x R CTAs, ranks slice + cs * group)
     int ksl;                // k-tiles per K-slice (multiple of 4)
     int rpr;                // row tiles per CTA
     int stages;             // ring depth
@@ -107,8 +109,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     __shared__ int s_cnt[kMaxStages];                 // warps done with the stage in each slot
 
     const int S = a.stages;
-    const int slice = blockIdx.x % a.cs;
-    const int rt0 = (blockIdx.x / a.cs) * a.rpr;
+    const int csz = a.cs * a.R;                          // cluster size
+    const int crank = blockIdx.x % csz;
+    const int slice = crank % a.cs, rg = crank / a.cs;
+    const int rt0 = ((blockIdx.x / csz) * a.R + rg) * a.rpr;
     const int nrt = max(0, min(a.rpr, a.RT - rt0));      // row tiles of this CTA
     const int kt0 = slice * a.ksl, kt1 = min(a.KT, kt0 + a.ksl);
     const int nkt = max(0, kt1 - kt0);
@@ -140,7 +144,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         for (int w = t0; w < (a.ksl - nkt) * 8; w += nt) z[w] = 0u;
     };
     if (nkt < a.ksl && a.pre > 0) zero_scale_tail(0, threadIdx.x, kThreads);
-    __syncthreads();
+    if (a.R > 1)
+        dla::cluster_sync_all();          // every CTA's mbarriers exist before a multicast lands
+    else
+        __syncthreads();
 
     // stage j: row tile rt0 + j, this slice's k-tiles (contiguous), then their scales (contiguous)
     auto issue = [&](int j) {
@@ -173,10 +180,18 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     const int xfl = max(0, min(nkt * 32, a.n_in - kt0 * 32));   // valid inputs of the slice
     if (threadIdx.x == 0) {
         dla::mbar_expect_tx(&xbar, (uint32_t)(a.nr * xfl * 4));
-        if (xfl > 0)
+        if (xfl > 0 && a.R == 1) {
             for (int r = 0; r < a.nr; ++r)
                 dla::bulk_g2s(ring + (size_t)a.pre * SB + (size_t)r * a.xpitch, a.x + (int64_t)r * a.x_stride + kt0 * 32,
                               (uint32_t)(xfl * 4), &xbar);
+        } else if (xfl > 0 && rg == 0) {
+            // one read of the slice's activation lines for every row group of the cluster
+            uint16_t mask = 0;
+            for (int q = 0; q < a.R; ++q) mask |= (uint16_t)(1u << (slice + a.cs * q));
+            for (int r = 0; r < a.nr; ++r)
+                dla::bulk_g2s_multicast(ring + (size_t)a.pre * SB + (size_t)r * a.xpitch,
+                                        a.x + (int64_t)r * a.x_stride + kt0 * 32, (uint32_t)(xfl * 4), &xbar, mask);
+        }
     }
     const bool xok = __all_sync(0xffffffffu, dla::mbar_wait(&xbar, 0u));
 
@@ -412,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         for (int e4 = threadIdx.x; e4 < nrt * 32; e4 += kThreads) {
             const int i = e4 >> 5;
             if (i % a.cs != slice) continue;                 // each rank finishes a share of the row tiles
-            float4 s = dla::ld_dsmem_f32x4(part + e4 * 4, 0);
+            float4 s = dla::ld_dsmem_f32x4(part + e4 * 4, (uint32_t)(a.cs * rg));
             for (int q = 1; q < a.cs; ++q) {
-                const float4 t = dla::ld_dsmem_f32x4(part + e4 * 4, (uint32_t)q);
+                const float4 t = dla::ld_dsmem_f32x4(part + e4 * 4, (uint32_t)(q + a.cs * rg));
                 s.x += t.x;
                 s.y += t.y;
                 s.z += t.z;
@@ -428,7 +443,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
                     if (col0 + q < a.nr) a.y[(int64_t)(col0 + q) * a.y_stride + o] = sv[q];
             }
         }
-        dla::cluster_sync_all();   // keep this CTA's shared memory alive until every peer has read it
+        // keep this CTA's shared memory alive until every peer has read it (no ordering of the
+        // output stores is needed, so the arrive does not wait for them)
+        dla::cluster_sync_relaxed();
     } else if (failed) {
         for (int e = threadIdx.x; e < nrt * 128; e += kThreads) {
             const int o = rt0 * 16 + (e >> 3), col = e & 7;
@@ -504,7 +521,7 @@ __global__ void q8_pack_d_kernel(const uint8_t *blocks, int64_t n_out, int64_t n
 
 struct GemvCfg {
     bool mma;
-    int nrc, kwm, cs, ksl, rpr, stages, grid;
+    int nrc, kwm, cs, R, ksl, rpr, stages, grid;
     size_t smem;
 };
 
@@ -623,6 +640,44 @@ bool two_per_sm(const void *kern)
     return false;
 }
 
+// Clusters of `csz` CTAs with `smem` bytes each that are resident at once, cached per device.
+int max_clusters(const void *kern, int csz, size_t smem)
+{
+    struct Key { int dev; const void *kern; int csz; size_t smem; int val; };
+    static std::mutex mu;
+    static Key cache[64];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].dev == dev && cache[i].kern == kern && cache[i].csz == csz && cache[i].smem == smem)
+            return cache[i].val;
+    int clusters = 0;
+    if (prepare_kernel(kern, csz) == DL_OK) {
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3((unsigned)csz);
+        lc.blockDim = dim3(kThreads);
+        lc.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)csz;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) != cudaSuccess) {
+            cudaGetLastError();
+            clusters = 0;
+        }
+    }
+    if (used < 64) cache[used++] = Key{dev, kern, csz, smem, clusters};
+    return clusters;
+}
+
 // Launch shape.  K is cut into cs slices of ksl = 8 x kwm k-tiles (every warp holds the
 // activations of its kwm k-tiles in registers; the last slice may be short); each CTA takes rpr
 // consecutive row tiles of one slice and streams them one row tile per ring stage.  Among the
@@ -641,25 +696,35 @@ int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
         const int ksl = kConsumers * kwm;
         const int cs = (int)dl::ceil_div(KT, ksl);
         if (cs > 16) continue;
-        const int nc1 = cs == 1 ? sm : clusters_one_per_sm(kern, cs);
-        if (nc1 < 1) continue;
         const size_t sb = (size_t)ksl * kStageTileBytes;
-        int stages = (int)(kRingBudget / sb);
-        stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
-        int per_sm = two_per_sm(kern) ? 2 : 1;
-        int rpr = (int)dl::ceil_div(RT, per_sm * nc1);
-        while (stages > 2 && gemv_smem(ksl, stages, rpr, cs) > kShareLimit) --stages;
-        if (per_sm == 2 && gemv_smem(ksl, stages, rpr, cs) > kShareLimit) {
-            // two CTAs do not fit on an SM: one CTA per SM
-            per_sm = 1;
-            rpr = (int)dl::ceil_div(RT, nc1);
-        }
-        if (gemv_smem(ksl, stages, rpr, cs) > (size_t)kSmemLimit) continue;
-        const long cost = (long)per_sm * rpr * ksl * 100 + cs;   // bytes per SM, then fewer slices
-        if (best_cost < 0 || cost * 100 < best_cost * 95) {
-            best_cost = cost;
-            best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
-                           gemv_smem(ksl, stages, rpr, cs)};
+        const int per_sm = two_per_sm(kern) ? 2 : 1;
+        for (int R : {4, 2, 1}) {                               // more row groups sharing activations first
+            const int csz = cs * R;
+            if (R > 1 && csz > 8) continue;
+            if (csz > 1 && clusters_one_per_sm(kern, csz) < 1) continue;
+            // footprint for an even spread of the row tiles over per_sm CTAs per SM, then the real
+            // number of resident clusters at that footprint
+            int stages = (int)(kRingBudget / sb);
+            stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
+            const int groups_est = std::max(1, (per_sm * sm) / csz) * R;
+            int rpr = (int)dl::ceil_div(RT, groups_est);
+            const size_t limit = per_sm == 2 ? kShareLimit : (size_t)kSmemLimit;
+            while (stages > 2 && gemv_smem(ksl, stages, rpr, cs) > limit) --stages;
+            size_t smem = gemv_smem(ksl, stages, rpr, cs);
+            if (smem > (size_t)kSmemLimit) continue;
+            const int nclu = csz == 1 ? per_sm * sm : max_clusters(kern, csz, smem);
+            if (nclu < 1) continue;
+            rpr = (int)dl::ceil_div(RT, nclu * R);
+            smem = gemv_smem(ksl, stages, rpr, cs);
+            if (smem > (size_t)kSmemLimit) continue;
+            const int groups = (int)dl::ceil_div(RT, rpr);          // row groups in use
+            const int ctas = (int)dl::ceil_div(groups, R) * csz;
+            const int ctas_per_sm = (int)dl::ceil_div(ctas, sm);
+            const long cost = (long)ctas_per_sm * rpr * ksl * 100 + cs;   // bytes per SM, then fewer slices
+            if (best_cost < 0 || cost * 100 < best_cost * 95) {
+                best_cost = cost;
+                best = GemvCfg{mma, nrc, kwm, cs, R, ksl, rpr, stages, ctas, smem};
+            }
         }
     }
     if (best_cost < 0) {
@@ -680,13 +745,13 @@ int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
             if (rpr < 1) continue;
             if (rpr > RT) rpr = RT;
             best_cost = 0;
-            best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
+            best = GemvCfg{mma, nrc, kwm, cs, 1, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
                            gemv_smem(ksl, stages, rpr, cs)};
         }
         if (best_cost < 0) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no launch shape for %d k-tiles", KT);
     }
     const void *kern = pick_kernel(best.mma, best.nrc, best.kwm);
-    const int rc = prepare_kernel(kern, best.cs);
+    const int rc = prepare_kernel(kern, best.cs * best.R);
     if (rc != DL_OK) return rc;
     *out = best;
     return DL_OK;
@@ -699,6 +764,7 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     if (rc != DL_OK) return rc;
     a.nr = nr;
     a.cs = cfg.cs;
+    a.R = cfg.R;
     a.ksl = cfg.ksl;
     a.rpr = cfg.rpr;
     a.stages = cfg.stages;
@@ -721,9 +787,9 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if (cfg.cs > 1) {
+    if (cfg.cs * cfg.R > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = (unsigned)cfg.cs;
+        attr[na].val.clusterDim.x = (unsigned)(cfg.cs * cfg.R);
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
