@@ -107,6 +107,21 @@ __device__ __forceinline__ uint32_t h2_bits(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// 2^x and log2 x through the special-function unit (PTX ex2.approx / lg2.approx: relative error
+// about 2^-22, far below the f16 probabilities and the tolerances of the partials)
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fast_log2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 constexpr int kStKeys = 32;                  // keys per stage
 constexpr int kMmaConsumers = 4;             // consumer warps
 constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
@@ -115,13 +130,14 @@ constexpr int kHalfTile = kStKeys * 128;     // bytes of 32 keys x 64 dims (one 
 constexpr int kAttnPreWaitStages = 2;        // stages requested before the wait on the previous kernel
 
 // Ring depth per head dimension: two CTAs fit on an SM.
-__host__ __device__ constexpr int mma_stages(int D) { return D == 128 ? 5 : 8; }
+__host__ __device__ constexpr int mma_stages(int D) { return D == 128 ? 4 : 8; }
 
 size_t attn_mma_smem_bytes(int D)
 {
     const size_t stage = (size_t)2 * kStKeys * D * 2;                    // K and V of 32 keys
     const size_t qf = (size_t)2 * (D / 16) * 32 * 32;                    // query fragments, 2 tiles
-    return 1024 + (size_t)mma_stages(D) * stage + qf;                   // + alignment slack
+    const size_t qr = (size_t)kMaxQ * D * 4;                             // the queries as they arrive
+    return 1024 + (size_t)mma_stages(D) * stage + qf + qr;              // + alignment slack
 }
 
 // OR of `flag` over the consumer warps (uniform result).
@@ -168,7 +184,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     const bool producer = warp == kMmaConsumers;
 
     // warps: NT query tiles (16 queries, tensor form; 8, CUDA-core form) x NS stage groups
-    const int TL = MMA ? 16 : QM;
+    constexpr int TL = MMA ? 16 : QM;
     const int NT = (Q + TL - 1) / TL;
     const int NS = kMmaConsumers / NT;
     const int MT = NT, KS = NS;
@@ -177,7 +193,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             dla::mbar_init(&full[i], 1);
             dla::mbar_init(&empty[i], (uint32_t)NT);   // released by the warps of one stage group
         }
-        dla::mbar_init(&qbar, kMmaConsumers);          // every consumer warp has its queries
+        dla::mbar_init(&qbar, 1);                       // the session's queries have arrived
         dla::mbar_init_fence();
     }
     // the key counts come from the caller, not from the previous kernel: read them now
@@ -204,17 +220,25 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     const int reg = P.row_region[s_row[0]];
     unsigned char *ring = smem;
     unsigned char *qfrag = smem + (size_t)S * kStageBytes;
+    float *qraw = reinterpret_cast<float *>(qfrag + (size_t)2 * (D / 16) * 32 * 32);   // [Q][D] as stored
     const uint32_t ring_s = dla::smem_u32(ring);
     bool bad = false;
 
+    // the session's queries of this KV head: row r's G heads are contiguous in q
+    auto issue_queries = [&]() {
+        dla::mbar_expect_tx(&qbar, (uint32_t)(Q * D * 4));
+        for (int r = 0; r < nrows; ++r)
+            dla::bulk_g2s(qraw + r * G * D, a.q + (int64_t)s_row[r] * a.q_stride + (int64_t)h * G * D,
+                          (uint32_t)(G * D * 4), &qbar);
+    };
     if (producer) {
         if (lane == 0) {
             dla::prefetch_tmap(&tk);
             dla::prefetch_tmap(&tv);
             // keys below the lowest slot this command writes are final before the previous kernel ends:
-            // the first few such stages are requested before waiting on it; the rest only once the
-            // consumers hold their queries, so that those latency-critical loads do not queue behind
-            // the whole ring
+            // the first few such stages are requested before waiting on it; after the wait come the
+            // session's queries (one bulk copy per row: the G heads of this KV head are contiguous),
+            // then the rest of the ring, so that those latency-critical lines go first
             const int stable = lmin - 1;
             const int nstable = k1 <= stable ? nst : max(0, (stable - k0) / kStKeys);
             const int npre = min(nstable, kAttnPreWaitStages);
@@ -229,10 +253,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 if (!waited && i >= npre) {
                     dl_pdl_wait();
                     waited = true;
-                    if (!dla::mbar_wait(&qbar, 0u)) {
-                        bad = true;
-                        break;
-                    }
+                    issue_queries();
                 }
                 unsigned char *kd = ring + (size_t)st * kStageBytes;
                 unsigned char *vd = kd + kStageBytes / 2;
@@ -244,9 +265,13 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     dla::tma_g2s_3d(vd + hf * kHalfTile, &tv, hf * 64, y, reg, &full[st]);
                 }
             }
-            if (!waited) dl_pdl_wait();
+            if (!waited) {
+                dl_pdl_wait();
+                issue_queries();
+            }
             if (bad) {
-                // leave no copy in flight: wait (bounded) for the stages issued last
+                // leave no copy in flight: wait (bounded) for the queries and the stages issued last
+                dla::mbar_wait(&qbar, 0u);
                 for (int j = max(0, i - S); j < i; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
             }
         } else {
@@ -280,19 +305,21 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     if constexpr (MMA) {
         // ---- query operand fragments (log2-domain scaled, hi + lo f16 terms) in shared memory:
         // [query tile][k-step][hi, lo][lane] 16 bytes = a0..a3
+        const bool qok = __all_sync(0xffffffffu, dla::mbar_wait(&qbar, 0u));
+        if (!qok) bad = true;
         for (int fi = tid; fi < MT * NKS * 32; fi += kMmaConsumers * 32) {
             const int t = fi & 31, ks = (fi >> 5) % NKS, qt = (fi >> 5) / NKS;
             const int gg = t >> 2, cc = t & 3;
             const int q0i = qt * 16 + gg, q1i = q0i + 8;
-            const float *q0 = q0i < Q ? a.q + (int64_t)s_row[s_qrow[q0i]] * a.q_stride + (h * G + s_qhead[q0i]) * D : nullptr;
-            const float *q1 = q1i < Q ? a.q + (int64_t)s_row[s_qrow[q1i]] * a.q_stride + (h * G + s_qhead[q1i]) * D : nullptr;
+            const float *q0 = q0i < Q ? qraw + q0i * D : nullptr;
+            const float *q1 = q1i < Q ? qraw + q1i * D : nullptr;
             uint32_t hv[4], lv[4];
     #pragma unroll
             for (int part = 0; part < 4; ++part) {
                 const float *src = (part & 1) ? q1 : q0;
                 const int col = ks * 16 + 2 * cc + (part >> 1) * 8;
                 float2 v = make_float2(0.f, 0.f);
-                if (src) v = __ldcg(reinterpret_cast<const float2 *>(src + col));
+                if (src) v = *reinterpret_cast<const float2 *>(src + col);
                 v.x *= a.qscale;
                 v.y *= a.qscale;
                 const __half2 hq = __floats2half2_rn(v.x, v.y);
@@ -304,8 +331,6 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             dst[32] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
         }
-        __syncwarp();
-        if (lane == 0) dla::mbar_arrive(&qbar);
         dla::named_sync(1, kMmaConsumers * 32);
         const unsigned char *myq = qfrag + (size_t)mt * NKS * 1024 + lane * 16;
         const int r0 = mt * 16 + g, r1 = r0 + 8;
@@ -384,14 +409,14 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
             const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
-            const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+            const float al0 = (mn0 == -INFINITY) ? 1.f : fast_exp2(m0 - mn0);
+            const float al1 = (mn1 == -INFINITY) ? 1.f : fast_exp2(m1 - mn1);
     #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
-                sc[nt][0] = sc[nt][0] == -INFINITY ? 0.f : exp2f(sc[nt][0] - mn0);
-                sc[nt][1] = sc[nt][1] == -INFINITY ? 0.f : exp2f(sc[nt][1] - mn0);
-                sc[nt][2] = sc[nt][2] == -INFINITY ? 0.f : exp2f(sc[nt][2] - mn1);
-                sc[nt][3] = sc[nt][3] == -INFINITY ? 0.f : exp2f(sc[nt][3] - mn1);
+                sc[nt][0] = sc[nt][0] == -INFINITY ? 0.f : fast_exp2(sc[nt][0] - mn0);
+                sc[nt][1] = sc[nt][1] == -INFINITY ? 0.f : fast_exp2(sc[nt][1] - mn0);
+                sc[nt][2] = sc[nt][2] == -INFINITY ? 0.f : fast_exp2(sc[nt][2] - mn1);
+                sc[nt][3] = sc[nt][3] == -INFINITY ? 0.f : fast_exp2(sc[nt][3] - mn1);
             }
             float ps0 = 0.f, ps1 = 0.f;
     #pragma unroll
@@ -458,14 +483,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         constexpr int DPL = D / 32;                 // dimensions per lane
         const int qg = warp % NT, sg = warp / NT;
         const int qb = qg * QM, nq = min(QM, Q - qb);
-        float *qs = reinterpret_cast<float *>(qfrag);   // [Q][D] f32, log2-domain scaled
-        for (int e = tid; e < Q * D; e += kMmaConsumers * 32) {
-            const int qi = e / D, d = e - qi * D;
-            qs[e] = __ldcg(a.q + (int64_t)s_row[s_qrow[qi]] * a.q_stride + (h * G + s_qhead[qi]) * D + d) * a.qscale;
-        }
-        __syncwarp();
-        if (lane == 0) dla::mbar_arrive(&qbar);
-        dla::named_sync(1, kMmaConsumers * 32);
+        const float *qs = qraw;                      // [Q][D] f32 as stored; the scale goes on the score
+        if (!__all_sync(0xffffffffu, dla::mbar_wait(&qbar, 0u))) bad = true;
         int lenq[QM];
 #pragma unroll
         for (int q = 0; q < QM; ++q) lenq[q] = q < nq ? s_len[s_qrow[qb + q]] : 0;
@@ -535,11 +554,11 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             for (int q = 0; q < QM; ++q) {
                 ps[q] = 0.f;
                 if (q >= nq) continue;
-                const float sv = key < lenq[q] ? sc[q] + sd[q] : -INFINITY;
+                const float sv = key < lenq[q] ? (sc[q] + sd[q]) * a.qscale : -INFINITY;
                 const float mn = fmaxf(mq[q], warp_max(sv));
                 if (mn == -INFINITY) continue;             // no attended key yet (warp-uniform)
-                const float al = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mn);
-                ps[q] = sv == -INFINITY ? 0.f : exp2f(sv - mn);
+                const float al = mq[q] == -INFINITY ? 0.f : fast_exp2(mq[q] - mn);
+                ps[q] = sv == -INFINITY ? 0.f : fast_exp2(sv - mn);
                 lq[q] = lq[q] * al + warp_sum(ps[q]);
                 mq[q] = mn;
 #pragma unroll
@@ -605,7 +624,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             float f = 0.f;
             if (kq < KS) {
                 const float mw = cm[(kq * MT + qt) * 16 + row];
-                f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
                 wsum += f * cl[(kq * MT + qt) * 16 + row];
             }
             cf[qi * (kMmaConsumers + 1) + kq] = f;
@@ -614,7 +633,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         const int rq = s_qrow[qi];
         if (s_len[rq] > k0)
             a.part_lse[((int64_t)s_row[rq] * P.n_q + h * G + s_qhead[qi]) * ms + piece] =
-                (M + log2f(wsum)) * 0.69314718055994530942f;
+                (M + fast_log2(wsum)) * 0.69314718055994530942f;
     }
     dla::named_sync(1, kMmaConsumers * 32);
     for (int e = tid; e < Q * (D / 4); e += kMmaConsumers * 32) {
