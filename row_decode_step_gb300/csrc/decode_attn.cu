@@ -484,6 +484,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         const int qg = warp % NT, sg = warp / NT;
         const int qb = qg * QM, nq = min(QM, Q - qb);
         const float *qs = qraw;                      // [Q][D] f32 as stored; the scale goes on the score
+        float *pb = reinterpret_cast<float *>(qfrag) + warp * QM * kStKeys;   // this warp's probabilities
         if (!__all_sync(0xffffffffu, dla::mbar_wait(&qbar, 0u))) bad = true;
         int lenq[QM];
 #pragma unroll
@@ -564,28 +565,39 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
 #pragma unroll
                 for (int e = 0; e < DPL; ++e) o[q][e] *= al;
             }
-            // O += P V: lane holds dimensions d0 .. d0 + DPL - 1
+            // O += P V: lane holds dimensions d0 .. d0 + DPL - 1; the probabilities go through this
+            // warp's shared buffer and come back four keys per broadcast load
+            for (int q = 0; q < QM; ++q)
+                if (q < nq) pb[q * kStKeys + lane] = ps[q];
+            __syncwarp();
             const unsigned char *vcol = vst + (dch >> 3) * kHalfTile + (d0 & 7) * 2;
-#pragma unroll 4
-            for (int j = 0; j < kStKeys; ++j) {
-                const unsigned char *vp = vcol + j * 128 + (((dch & 7) ^ (j & 7)) << 4);
-                float v[DPL];
-                if constexpr (DPL == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(vp);
-                    const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
-                    const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
-                    v[0] = v01.x; v[1] = v01.y; v[2] = v23.x; v[3] = v23.y;
-                } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(vp);
-                    const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w));
-                    v[0] = v01.x; v[1] = v01.y;
+#pragma unroll 2
+            for (int j4 = 0; j4 < kStKeys; j4 += 4) {
+                float v[4][DPL];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int j = j4 + kk;
+                    const unsigned char *vp = vcol + j * 128 + (((dch & 7) ^ (j & 7)) << 4);
+                    if constexpr (DPL == 4) {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(vp);
+                        const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+                        const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+                        v[kk][0] = v01.x; v[kk][1] = v01.y; v[kk][2] = v23.x; v[kk][3] = v23.y;
+                    } else {
+                        const uint32_t w = *reinterpret_cast<const uint32_t *>(vp);
+                        const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+                        v[kk][0] = v01.x; v[kk][1] = v01.y;
+                    }
                 }
 #pragma unroll
                 for (int q = 0; q < QM; ++q) {
                     if (q < nq) {
-                        const float pj = __shfl_sync(0xffffffffu, ps[q], j);
+                        const float4 p4 = *reinterpret_cast<const float4 *>(pb + q * kStKeys + j4);
+                        const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
-                        for (int e = 0; e < DPL; ++e) o[q][e] = fmaf(pj, v[e], o[q][e]);
+                        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                            for (int e = 0; e < DPL; ++e) o[q][e] = fmaf(pk[kk], v[kk][e], o[q][e]);
                     }
                 }
             }

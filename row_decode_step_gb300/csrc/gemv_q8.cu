@@ -208,26 +208,29 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     if constexpr (MMA) {
         float2 v[KWM][4];
         float m = 0.f;
+        float mj[KWM];
 #pragma unroll
         for (int j = 0; j < KWM; ++j) {
             const int kl = wk0 + j;
             const bool live = xok && kl * 32 < xfl && g < a.nr;
             const float *xr = reinterpret_cast<const float *>(xs + (size_t)g * a.xpitch) + kl * 32 + 2 * c;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
+            for (int p = 0; p < 4; ++p)
                 v[j][p] = live ? *reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8) : make_float2(0.f, 0.f);
-                m = fmaxf(m, fmaxf(fabsf(v[j][p].x), fabsf(v[j][p].y)));
-            }
+            mj[j] = fmaxf(fmaxf(fmaxf(fabsf(v[j][0].x), fabsf(v[j][0].y)), fmaxf(fabsf(v[j][1].x), fabsf(v[j][1].y))),
+                          fmaxf(fmaxf(fabsf(v[j][2].x), fabsf(v[j][2].y)), fmaxf(fabsf(v[j][3].x), fabsf(v[j][3].y))));
         }
+#pragma unroll
+        for (int j = 0; j < KWM; ++j) m = fmaxf(m, mj[j]);
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        // power-of-two scale of activation row g over this warp's inputs: largest |x| into [2^14, 2^15)
-        float sig = 1.f;
-        if (m > 0.f) {
-            int e;
-            frexpf(m, &e);
-            sig = ldexpf(1.f, min(15 - e, 126));
-        }
+        // power-of-two scale of activation row g over this warp's inputs: largest |x| into [2^14, 2^15),
+        // built from the exponent field of m (m in [2^(E-127), 2^(E-126)) -> scale 2^(141-E), at most
+        // 2^126; m = 0 keeps 1)
+        const int ebits = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+        const int sexp = m > 0.f ? min(268 - ebits, 253) : 127;
+        const float sig = __uint_as_float((uint32_t)sexp << 23);
+        const float inv = __uint_as_float((uint32_t)(254 - sexp) << 23);
 #pragma unroll
         for (int j = 0; j < KWM; ++j) {
             float colsum = 0.f;
@@ -248,7 +251,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
             ncorr[j] = make_float2(-1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c),
                                    -1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c + 4));
         }
-        const float inv = 1.f / sig;
         us0 = __shfl_sync(0xffffffffu, inv, 8 * c);
         us1 = __shfl_sync(0xffffffffu, inv, 8 * c + 4);
     } else {
