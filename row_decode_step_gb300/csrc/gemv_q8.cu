@@ -53,13 +53,10 @@ struct GemvArgs {
     int nr;                 // rows of this command, 1..8
     int KT;                 // k-tiles, padded to a multiple of 4
     int RT;                 // row tiles
-    int cs;                 // K-slices
-    int R;                  // row groups per cluster (a cluster is cs x R CTAs, ranks slice + cs * group)
+    int cs;                 // K-slices (= cluster size)
     int ksl;                // k-tiles per K-slice (multiple of 4)
     int rpr;                // row tiles per CTA
     int stages;             // ring depth
-    int pre;                // ring stages requested before the wait (0 or 1)
-    int xpitch;             // bytes between activation rows staged in shared memory
     int l2pf;               // stages past the ring prefetched into L2 before the wait
 };
 
@@ -104,15 +101,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
 {
     constexpr int RB = kRowBatch;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t full[kMaxStages], xbar;
+    __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ int s_shape_bad, s_issued;
     __shared__ int s_cnt[kMaxStages];                 // warps done with the stage in each slot
 
     const int S = a.stages;
-    const int csz = a.cs * a.R;                          // cluster size
-    const int crank = blockIdx.x % csz;
-    const int slice = crank % a.cs, rg = crank / a.cs;
-    const int rt0 = ((blockIdx.x / csz) * a.R + rg) * a.rpr;
+    const int slice = blockIdx.x % a.cs;
+    const int rt0 = (blockIdx.x / a.cs) * a.rpr;
     const int nrt = max(0, min(a.rpr, a.RT - rt0));      // row tiles of this CTA
     const int kt0 = slice * a.ksl, kt1 = min(a.KT, kt0 + a.ksl);
     const int nkt = max(0, kt1 - kt0);
@@ -130,24 +125,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
             dla::mbar_init(&full[st], 1);
             s_cnt[st] = 0;
         }
-        dla::mbar_init(&xbar, 1);
         s_shape_bad = 0;
         s_issued = min(S, nrt);
         dla::mbar_init_fence();
     }
     // a slice shorter than the stage (the last one of K): the scales of the missing k-tiles
     // read as zero, so that whatever the stage holds there contributes nothing (the copies carry
-    // this slice's k-tiles only).  Slots at and past `pre` hold the staged activations first and
-    // are cleared later, before their first stage is requested.
-    auto zero_scale_tail = [&](int st, int t0, int nt) {
-        uint32_t *z = reinterpret_cast<uint32_t *>(ring + st * SB + (size_t)a.ksl * 512 + (size_t)nkt * 32);
-        for (int w = t0; w < (a.ksl - nkt) * 8; w += nt) z[w] = 0u;
-    };
-    if (nkt < a.ksl && a.pre > 0) zero_scale_tail(0, threadIdx.x, kThreads);
-    if (a.R > 1)
-        dla::cluster_sync_all();          // every CTA's mbarriers exist before a multicast lands
-    else
-        __syncthreads();
+    // this slice's k-tiles only, so these bytes are never overwritten)
+    if (nkt < a.ksl)
+        for (int e = threadIdx.x; e < S * (a.ksl - nkt) * 8; e += kThreads) {
+            const int st = e / ((a.ksl - nkt) * 8), w = e - st * (a.ksl - nkt) * 8;
+            reinterpret_cast<uint32_t *>(ring + st * SB + (size_t)a.ksl * 512 + (size_t)nkt * 32)[w] = 0u;
+        }
+    __syncthreads();
 
     // stage j: row tile rt0 + j, this slice's k-tiles (contiguous), then their scales (contiguous)
     auto issue = [&](int j) {
@@ -158,12 +148,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
         dla::bulk_g2s(dst + (size_t)a.ksl * 512, a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
     };
-    // the weights do not depend on the previous kernel: the first stage may be requested before
-    // waiting on it.  The activations of this K-slice then arrive as whole lines (one bulk copy
-    // per activation row) in ring slots not yet in use, ahead of the rest of the ring: activation
-    // lines are read by every CTA of the slice, and line-sized requests keep that traffic small
+    // the weights do not depend on the previous kernel: the whole ring is requested before waiting
+    // on it, so that the weights stream while that kernel finishes and the activations load
     if (threadIdx.x == 0) {
-        for (int j = 0; j < a.pre && j < nrt; ++j) issue(j);
+        for (int j = 0; j < S && j < nrt; ++j) issue(j);
         const int pf_end = min(nrt, S + a.l2pf);
         for (int j = S; j < pf_end; ++j) {
             const int rt = rt0 + j;
@@ -175,31 +163,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     // on everything before this one having finished
     dl_pdl_wait();
     dl_pdl_launch_dependents();
-
-    const unsigned char *xs = ring + (size_t)a.pre * SB;        // staged activation rows
     const int xfl = max(0, min(nkt * 32, a.n_in - kt0 * 32));   // valid inputs of the slice
-    if (threadIdx.x == 0) {
-        dla::mbar_expect_tx(&xbar, (uint32_t)(a.nr * xfl * 4));
-        if (xfl > 0 && a.R == 1) {
-            for (int r = 0; r < a.nr; ++r)
-                dla::bulk_g2s(ring + (size_t)a.pre * SB + (size_t)r * a.xpitch, a.x + (int64_t)r * a.x_stride + kt0 * 32,
-                              (uint32_t)(xfl * 4), &xbar);
-        } else if (xfl > 0 && rg == 0) {
-            // one read of the slice's activation lines for every row group of the cluster
-            uint16_t mask = 0;
-            for (int q = 0; q < a.R; ++q) mask |= (uint16_t)(1u << (slice + a.cs * q));
-            for (int r = 0; r < a.nr; ++r)
-                dla::bulk_g2s_multicast(ring + (size_t)a.pre * SB + (size_t)r * a.xpitch,
-                                        a.x + (int64_t)r * a.x_stride + kt0 * 32, (uint32_t)(xfl * 4), &xbar, mask);
-        }
-    }
-    const bool xok = __all_sync(0xffffffffu, dla::mbar_wait(&xbar, 0u));
 
     // ---- this warp's window of KWM k-tiles of the slice and its activations, kept in registers;
     // k-tiles past the slice (the last slice of K may be short) have zero activations and scales
     const int wk0 = warp * KWM;                                  // slice-local
     const int nw = max(0, min(KWM, nkt - wk0));
-    if (lane == 0 && (kConsumers * KWM != a.ksl || !xok)) atomicExch(&s_shape_bad, 1);   // broken shape
+    if (lane == 0 && kConsumers * KWM != a.ksl) atomicExch(&s_shape_bad, 1);   // broken launch shape
     // lane (g, c) holds inputs 2c, 2c+1 / 8+2c, 9+2c / 16+2c, 17+2c / 24+2c, 25+2c of each k-tile
     uint32_t bh[MMA ? KWM : 1][4], bl[MMA ? KWM : 1][4];
     float2 ncorr[MMA ? KWM : 1];                 // -1152 * sum(x) of columns 2c, 2c+1 per k-tile
@@ -212,11 +182,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
 #pragma unroll
         for (int j = 0; j < KWM; ++j) {
             const int kl = wk0 + j;
-            const bool live = xok && kl * 32 < xfl && g < a.nr;
-            const float *xr = reinterpret_cast<const float *>(xs + (size_t)g * a.xpitch) + kl * 32 + 2 * c;
+            const bool live = kl * 32 < xfl && g < a.nr;
+            const float *xr = a.x + (int64_t)g * a.x_stride + (kt0 + kl) * 32 + 2 * c;
 #pragma unroll
             for (int p = 0; p < 4; ++p)
-                v[j][p] = live ? *reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8) : make_float2(0.f, 0.f);
+                v[j][p] = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
+                               : make_float2(0.f, 0.f);
             mj[j] = fmaxf(fmaxf(fmaxf(fabsf(v[j][0].x), fabsf(v[j][0].y)), fmaxf(fabsf(v[j][1].x), fabsf(v[j][1].y))),
                           fmaxf(fmaxf(fabsf(v[j][2].x), fabsf(v[j][2].y)), fmaxf(fabsf(v[j][3].x), fabsf(v[j][3].y))));
         }
@@ -259,26 +230,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
             const int kl = wk0 + j;
 #pragma unroll
             for (int r = 0; r < NRC; ++r) {
-                const bool live = xok && kl * 32 < xfl && r < a.nr;
-                const float *xr = reinterpret_cast<const float *>(xs + (size_t)r * a.xpitch) + kl * 32 + 2 * c;
+                const bool live = kl * 32 < xfl && r < a.nr;
+                const float *xr = a.x + (int64_t)r * a.x_stride + (kt0 + kl) * 32 + 2 * c;
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    const float2 t = live ? *reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8)
+                    const float2 t = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
                                           : make_float2(0.f, 0.f);
                     xv[j][r][2 * p] = t.x;
                     xv[j][r][2 * p + 1] = t.y;
                 }
             }
         }
-    }
-    // every warp holds its activations: the slots they were staged in join the ring
-    __syncthreads();
-    if (warp == 0) {
-        if (nkt < a.ksl)
-            for (int st = a.pre; st < S; ++st) zero_scale_tail(st, lane, 32);
-        __syncwarp();
-        if (lane == 0)
-            for (int j = a.pre; j < S && j < nrt; ++j) issue(j);
     }
 
     // ---- stages in batches of RB row tiles: each warp keeps its partial of every row tile of
@@ -429,9 +391,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         for (int e4 = threadIdx.x; e4 < nrt * 32; e4 += kThreads) {
             const int i = e4 >> 5;
             if (i % a.cs != slice) continue;                 // each rank finishes a share of the row tiles
-            float4 s = dla::ld_dsmem_f32x4(part + e4 * 4, (uint32_t)(a.cs * rg));
+            float4 s = dla::ld_dsmem_f32x4(part + e4 * 4, 0);
             for (int q = 1; q < a.cs; ++q) {
-                const float4 t = dla::ld_dsmem_f32x4(part + e4 * 4, (uint32_t)(q + a.cs * rg));
+                const float4 t = dla::ld_dsmem_f32x4(part + e4 * 4, (uint32_t)q);
                 s.x += t.x;
                 s.y += t.y;
                 s.z += t.z;
@@ -523,7 +485,7 @@ __global__ void q8_pack_d_kernel(const uint8_t *blocks, int64_t n_out, int64_t n
 
 struct GemvCfg {
     bool mma;
-    int nrc, kwm, cs, R, ksl, rpr, stages, grid;
+    int nrc, kwm, cs, ksl, rpr, stages, grid;
     size_t smem;
 };
 
@@ -700,33 +662,27 @@ int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
         if (cs > 16) continue;
         const size_t sb = (size_t)ksl * kStageTileBytes;
         const int per_sm = two_per_sm(kern) ? 2 : 1;
-        for (int R : {4, 2, 1}) {                               // more row groups sharing activations first
-            const int csz = cs * R;
-            if (R > 1 && csz > 8) continue;
-            if (csz > 1 && clusters_one_per_sm(kern, csz) < 1) continue;
-            // footprint for an even spread of the row tiles over per_sm CTAs per SM, then the real
-            // number of resident clusters at that footprint
-            int stages = (int)(kRingBudget / sb);
-            stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
-            const int groups_est = std::max(1, (per_sm * sm) / csz) * R;
-            int rpr = (int)dl::ceil_div(RT, groups_est);
-            const size_t limit = per_sm == 2 ? kShareLimit : (size_t)kSmemLimit;
-            while (stages > 2 && gemv_smem(ksl, stages, rpr, cs) > limit) --stages;
-            size_t smem = gemv_smem(ksl, stages, rpr, cs);
-            if (smem > (size_t)kSmemLimit) continue;
-            const int nclu = csz == 1 ? per_sm * sm : max_clusters(kern, csz, smem);
-            if (nclu < 1) continue;
-            rpr = (int)dl::ceil_div(RT, nclu * R);
-            smem = gemv_smem(ksl, stages, rpr, cs);
-            if (smem > (size_t)kSmemLimit) continue;
-            const int groups = (int)dl::ceil_div(RT, rpr);          // row groups in use
-            const int ctas = (int)dl::ceil_div(groups, R) * csz;
-            const int ctas_per_sm = (int)dl::ceil_div(ctas, sm);
-            const long cost = (long)ctas_per_sm * rpr * ksl * 100 + cs;   // bytes per SM, then fewer slices
-            if (best_cost < 0 || cost * 100 < best_cost * 95) {
-                best_cost = cost;
-                best = GemvCfg{mma, nrc, kwm, cs, R, ksl, rpr, stages, ctas, smem};
-            }
+        if (cs > 1 && clusters_one_per_sm(kern, cs) < 1) continue;
+        // footprint for an even spread of the row tiles over per_sm CTAs per SM, then the real
+        // number of resident clusters at that footprint
+        int stages = (int)(kRingBudget / sb);
+        stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
+        int rpr = (int)dl::ceil_div(RT, std::max(1, (per_sm * sm) / cs));
+        const size_t limit = per_sm == 2 ? kShareLimit : (size_t)kSmemLimit;
+        while (stages > 2 && gemv_smem(ksl, stages, rpr, cs) > limit) --stages;
+        size_t smem = gemv_smem(ksl, stages, rpr, cs);
+        if (smem > (size_t)kSmemLimit) continue;
+        const int nclu = cs == 1 ? per_sm * sm : max_clusters(kern, cs, smem);
+        if (nclu < 1) continue;
+        rpr = (int)dl::ceil_div(RT, nclu);
+        smem = gemv_smem(ksl, stages, rpr, cs);
+        if (smem > (size_t)kSmemLimit) continue;
+        const int ctas = (int)dl::ceil_div(RT, rpr) * cs;
+        const int ctas_per_sm = (int)dl::ceil_div(ctas, sm);
+        const long cost = (long)ctas_per_sm * rpr * ksl * 100 + cs;   // bytes per SM, then fewer slices
+        if (best_cost < 0 || cost * 100 < best_cost * 95) {
+            best_cost = cost;
+            best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, ctas, smem};
         }
     }
     if (best_cost < 0) {
@@ -747,13 +703,13 @@ int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
             if (rpr < 1) continue;
             if (rpr > RT) rpr = RT;
             best_cost = 0;
-            best = GemvCfg{mma, nrc, kwm, cs, 1, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
+            best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
                            gemv_smem(ksl, stages, rpr, cs)};
         }
         if (best_cost < 0) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no launch shape for %d k-tiles", KT);
     }
     const void *kern = pick_kernel(best.mma, best.nrc, best.kwm);
-    const int rc = prepare_kernel(kern, best.cs * best.R);
+    const int rc = prepare_kernel(kern, best.cs);
     if (rc != DL_OK) return rc;
     *out = best;
     return DL_OK;
@@ -766,18 +722,10 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     if (rc != DL_OK) return rc;
     a.nr = nr;
     a.cs = cfg.cs;
-    a.R = cfg.R;
     a.ksl = cfg.ksl;
     a.rpr = cfg.rpr;
     a.stages = cfg.stages;
     a.l2pf = 0;
-    // the activation rows are staged in the ring slots after the pre-issued one (16-byte pad per
-    // row: the fragment reads spread over the banks); without room, nothing is pre-issued
-    a.xpitch = cfg.ksl * 128 + 16;
-    const size_t sb = (size_t)cfg.ksl * kStageTileBytes;
-    a.pre = (size_t)(cfg.stages - 1) * sb >= (size_t)nr * a.xpitch ? 1 : 0;
-    if ((size_t)cfg.stages * sb < (size_t)nr * a.xpitch)
-        return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no room to stage the activations");
     const void *kern = pick_kernel(cfg.mma, cfg.nrc, cfg.kwm);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid);
@@ -789,9 +737,9 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if (cfg.cs * cfg.R > 1) {
+    if (cfg.cs > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = (unsigned)(cfg.cs * cfg.R);
+        attr[na].val.clusterDim.x = (unsigned)cfg.cs;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
