@@ -489,13 +489,14 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         int lenq[QM];
 #pragma unroll
         for (int q = 0; q < QM; ++q) lenq[q] = q < nq ? s_len[s_qrow[qb + q]] : 0;
-        float o[QM][DPL], mq[QM], lq[QM];
+        float2 o[QM][DPL];                           // (even keys, odd keys) of each dimension
+        float mq[QM], lq[QM];
 #pragma unroll
         for (int q = 0; q < QM; ++q) {
             mq[q] = -INFINITY;
             lq[q] = 0.f;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) o[q][e] = 0.f;
+            for (int e = 0; e < DPL; ++e) o[q][e] = make_float2(0.f, 0.f);
         }
         const int d0 = DPL * lane, dch = d0 >> 3;
         for (int i = sg; sg < NS && i < nst; i += NS) {
@@ -519,9 +520,9 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 __syncwarp();
             }
             // scores: lane = key, its row read 16 bytes at a time through the swizzle
-            float sc[QM], sd[QM];                  // two partial sums per score: even, odd chunks
-#pragma unroll
-            for (int q = 0; q < QM; ++q) sc[q] = sd[q] = 0.f;
+            float2 sc[QM], sd[QM];                 // partial sums per score: even, odd chunks x
+#pragma unroll                                     // even, odd dimensions
+            for (int q = 0; q < QM; ++q) sc[q] = sd[q] = make_float2(0.f, 0.f);
 #pragma unroll 2
             for (int ch = 0; ch < D / 8; ++ch) {
                 const uint4 kv = *reinterpret_cast<const uint4 *>(kst + (ch >> 3) * kHalfTile + lane * 128 +
@@ -535,15 +536,11 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     if (q < nq) {
                         const float4 qa = *reinterpret_cast<const float4 *>(qs + (qb + q) * D + ch * 8);
                         const float4 qc = *reinterpret_cast<const float4 *>(qs + (qb + q) * D + ch * 8 + 4);
-                        float t = (ch & 1) ? sd[q] : sc[q];
-                        t = fmaf(qa.x, k01.x, t);
-                        t = fmaf(qa.y, k01.y, t);
-                        t = fmaf(qa.z, k23.x, t);
-                        t = fmaf(qa.w, k23.y, t);
-                        t = fmaf(qc.x, k45.x, t);
-                        t = fmaf(qc.y, k45.y, t);
-                        t = fmaf(qc.z, k67.x, t);
-                        t = fmaf(qc.w, k67.y, t);
+                        float2 t = (ch & 1) ? sd[q] : sc[q];
+                        t = __ffma2_rn(make_float2(qa.x, qa.y), k01, t);
+                        t = __ffma2_rn(make_float2(qa.z, qa.w), k23, t);
+                        t = __ffma2_rn(make_float2(qc.x, qc.y), k45, t);
+                        t = __ffma2_rn(make_float2(qc.z, qc.w), k67, t);
                         if (ch & 1) sd[q] = t; else sc[q] = t;
                     }
                 }
@@ -555,7 +552,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             for (int q = 0; q < QM; ++q) {
                 ps[q] = 0.f;
                 if (q >= nq) continue;
-                const float sv = key < lenq[q] ? (sc[q] + sd[q]) * a.qscale : -INFINITY;
+                const float sv = key < lenq[q] ? ((sc[q].x + sd[q].x) + (sc[q].y + sd[q].y)) * a.qscale : -INFINITY;
                 const float mn = fmaxf(mq[q], warp_max(sv));
                 if (mn == -INFINITY) continue;             // no attended key yet (warp-uniform)
                 const float al = mq[q] == -INFINITY ? 0.f : fast_exp2(mq[q] - mn);
@@ -563,7 +560,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 lq[q] = lq[q] * al + warp_sum(ps[q]);
                 mq[q] = mn;
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) o[q][e] *= al;
+                for (int e = 0; e < DPL; ++e) o[q][e] = __fmul2_rn(o[q][e], make_float2(al, al));
             }
             // O += P V: lane holds dimensions d0 .. d0 + DPL - 1; the probabilities go through this
             // warp's shared buffer and come back four keys per broadcast load
@@ -593,11 +590,12 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 for (int q = 0; q < QM; ++q) {
                     if (q < nq) {
                         const float4 p4 = *reinterpret_cast<const float4 *>(pb + q * kStKeys + j4);
-                        const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
+                        const float2 p01 = make_float2(p4.x, p4.y), p23 = make_float2(p4.z, p4.w);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                            for (int e = 0; e < DPL; ++e) o[q][e] = fmaf(pk[kk], v[kk][e], o[q][e]);
+                        for (int e = 0; e < DPL; ++e) {
+                            o[q][e] = __ffma2_rn(p01, make_float2(v[0][e], v[1][e]), o[q][e]);
+                            o[q][e] = __ffma2_rn(p23, make_float2(v[2][e], v[3][e]), o[q][e]);
+                        }
                     }
                 }
             }
@@ -613,7 +611,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             for (int q = 0; q < QM; ++q) {
                 if (q < nq) {
 #pragma unroll
-                    for (int e = 0; e < DPL; ++e) co[(warp * 16 + q) * CP + d0 + e] = o[q][e];
+                    for (int e = 0; e < DPL; ++e) co[(warp * 16 + q) * CP + d0 + e] = o[q][e].x + o[q][e].y;
                     if (lane == 0) {
                         cm[warp * 16 + q] = mq[q];
                         cl[warp * 16 + q] = lq[q];

@@ -75,11 +75,13 @@ size_t gemv_smem(int ksl, int stages, int rpr, int cs)
 }
 
 // ---- arithmetic helpers
-// biased weight byte `sel` of w (u = q + 128) to the float q, through u placed in the low
-// mantissa of 2^23
-__device__ __forceinline__ float u8_to_f32(uint32_t w, uint32_t sel)
+// biased weight bytes `lo`, `lo + 1` of w (u = q + 128) to the float pair (q, q'): each u is placed
+// in the low mantissa of 2^23, and one packed subtraction takes 2^23 + 128 off both
+__device__ __forceinline__ float2 u8x2_to_f32x2(uint32_t w, uint32_t lo)
 {
-    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | sel)) - 8388736.0f;
+    const float2 b = make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | lo)),
+                                 __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541u | lo)));
+    return __fadd2_rn(b, make_float2(-8388736.0f, -8388736.0f));
 }
 // two biased bytes (0, 1 or 2, 3) of w to the f16 pair (1024 + u)
 __device__ __forceinline__ uint32_t u8x2_to_h2(uint32_t w, uint32_t sel)
@@ -250,12 +252,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     for (int b0 = 0; b0 < nrt; b0 += RB) {
         const int nb = min(RB, nrt - b0);
         float2 acc01[RB], acc23[RB];                 // tensor path: rows g, g+8 x columns 2c, 2c+1
-        float accg[RB][NRC], acch[RB][NRC];          // CUDA-core path: rows g, g+8 x activation rows
+        float2 accg[RB][NRC], acch[RB][NRC];         // CUDA-core path: rows g, g+8 x activation rows
+                                                     // (even and odd inputs summed apart)
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
             acc01[r] = acc23[r] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < NRC; ++q) accg[r][q] = acch[r][q] = 0.f;
+            for (int q = 0; q < NRC; ++q) accg[r][q] = acch[r][q] = make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
@@ -286,26 +289,27 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
                         acc01[r] = __ffma2_rn(make_float2(dg, dg), __fadd2_rn(make_float2(t[0], t[1]), ncorr[j]), acc01[r]);
                         acc23[r] = __ffma2_rn(make_float2(dh, dh), __fadd2_rn(make_float2(t[2], t[3]), ncorr[j]), acc23[r]);
                     } else {
-                        // row g: bytes 0, 1 of each word; row g+8: bytes 2, 3
+                        // row g: bytes 0, 1 of each word; row g+8: bytes 2, 3 (inputs 2p, 2p+1 of
+                        // the lane's eight), multiplied pairwise with the activation pairs
                         const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
-                        float wg[8], wh[8];
+                        float2 wg[4], wh[4];
 #pragma unroll
                         for (int p = 0; p < 4; ++p) {
-                            wg[2 * p] = u8_to_f32(wd[p], 0);
-                            wg[2 * p + 1] = u8_to_f32(wd[p], 1);
-                            wh[2 * p] = u8_to_f32(wd[p], 2);
-                            wh[2 * p + 1] = u8_to_f32(wd[p], 3);
+                            wg[p] = u8x2_to_f32x2(wd[p], 0);
+                            wh[p] = u8x2_to_f32x2(wd[p], 2);
                         }
 #pragma unroll
                         for (int q = 0; q < NRC; ++q) {
-                            float sg = wg[0] * xv[j][q][0], sh = wh[0] * xv[j][q][0];
+                            const float2 x0 = make_float2(xv[j][q][0], xv[j][q][1]);
+                            float2 sg = __fmul2_rn(wg[0], x0), sh = __fmul2_rn(wh[0], x0);
 #pragma unroll
-                            for (int e = 1; e < 8; ++e) {
-                                sg = fmaf(wg[e], xv[j][q][e], sg);
-                                sh = fmaf(wh[e], xv[j][q][e], sh);
+                            for (int p = 1; p < 4; ++p) {
+                                const float2 xp = make_float2(xv[j][q][2 * p], xv[j][q][2 * p + 1]);
+                                sg = __ffma2_rn(wg[p], xp, sg);
+                                sh = __ffma2_rn(wh[p], xp, sh);
                             }
-                            accg[r][q] = fmaf(dg, sg, accg[r][q]);
-                            acch[r][q] = fmaf(dh, sh, acch[r][q]);
+                            accg[r][q] = __ffma2_rn(make_float2(dg, dg), sg, accg[r][q]);
+                            acch[r][q] = __ffma2_rn(make_float2(dh, dh), sh, acch[r][q]);
                         }
                     }
                 }
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
             } else {
 #pragma unroll
                 for (int q = 0; q < NRC; ++q) {
-                    float vg = accg[r][q], vh = acch[r][q];
+                    float vg = accg[r][q].x + accg[r][q].y, vh = acch[r][q].x + acch[r][q].y;
                     vg += __shfl_xor_sync(0xffffffffu, vg, 1);
                     vg += __shfl_xor_sync(0xffffffffu, vg, 2);
                     vh += __shfl_xor_sync(0xffffffffu, vh, 1);
