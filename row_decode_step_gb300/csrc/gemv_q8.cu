@@ -57,7 +57,7 @@ struct GemvArgs {
     int ksl;                // k-tiles per K-slice (multiple of 4)
     int rpr;                // row tiles per CTA
     int stages;             // ring depth
-    int l2pf;               // stages past the ring prefetched into L2 before the wait
+    int pre;                // ring stages requested before waiting on the previous kernel
 };
 
 constexpr int kConsumers = 8;                        // warps, each a share of the K-slice
@@ -150,17 +150,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
         dla::bulk_g2s(dst + (size_t)a.ksl * 512, a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
     };
-    // the weights do not depend on the previous kernel: the whole ring is requested before waiting
-    // on it, so that the weights stream while that kernel finishes and the activations load
-    if (threadIdx.x == 0) {
-        for (int j = 0; j < S && j < nrt; ++j) issue(j);
-        const int pf_end = min(nrt, S + a.l2pf);
-        for (int j = S; j < pf_end; ++j) {
-            const int rt = rt0 + j;
-            dl_prefetch_l2(a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes);
-            dl_prefetch_l2(a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes);
-        }
-    }
+    // the weights do not depend on the previous kernel: the first stages are requested before
+    // waiting on it, the rest once the activations are requested (an SM's requests are served
+    // roughly in order, and the activations gate every stage)
+    if (threadIdx.x == 0)
+        for (int j = 0; j < a.pre && j < S && j < nrt; ++j) issue(j);
+    auto issue_rest = [&]() {
+        if (threadIdx.x == 0)
+            for (int j = a.pre; j < S && j < nrt; ++j) issue(j);
+    };
     // every thread waits before the next kernel may launch: kernels after this one can rely
     // on everything before this one having finished
     dl_pdl_wait();
@@ -190,6 +188,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
             for (int p = 0; p < 4; ++p)
                 v[j][p] = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
                                : make_float2(0.f, 0.f);
+        }
+        issue_rest();
+#pragma unroll
+        for (int j = 0; j < KWM; ++j) {
             mj[j] = fmaxf(fmaxf(fmaxf(fabsf(v[j][0].x), fabsf(v[j][0].y)), fmaxf(fabsf(v[j][1].x), fabsf(v[j][1].y))),
                           fmaxf(fmaxf(fabsf(v[j][2].x), fabsf(v[j][2].y)), fmaxf(fabsf(v[j][3].x), fabsf(v[j][3].y))));
         }
@@ -243,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
                 }
             }
         }
+        issue_rest();
     }
 
     // ---- stages in batches of RB row tiles: each warp keeps its partial of every row tile of
@@ -729,7 +732,9 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     a.ksl = cfg.ksl;
     a.rpr = cfg.rpr;
     a.stages = cfg.stages;
-    a.l2pf = 0;
+    // two stages per CTA ahead of the activations: about what an SM receives while the previous
+    // kernel drains
+    a.pre = 2;
     const void *kern = pick_kernel(cfg.mma, cfg.nrc, cfg.kwm);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid);
