@@ -46,6 +46,7 @@ def lib():
         L.orc_double_to_half.restype = ctypes.c_uint16
         L.orc_gemv_q8.argtypes = [P, I64, I64, P, I, I64, P, I64]
         L.orc_q8_dequant.argtypes = [P, I64, I64, P]
+        L.orc_gemv_f16w.argtypes = [P, I64, I64, P, I, I64, P, I64]
         L.orc_matmul.argtypes = [P, I64, I64, P, I, I64, P, I64]
         L.orc_rope_vec.argtypes = [P, I, I, D, D]
         L.orc_rope_vec.restype = None
@@ -55,7 +56,7 @@ def lib():
         L.orc_attn_merge.argtypes = [P, P, I, I, I, I, P, I64, P]
         L.orc_attn_full.argtypes = [P, I64, I, I, I, I, P, P, I64, I, P, P, P, I64, P]
         L.orc_plan_groups.argtypes = [I, I, P]
-        for f in ("orc_gemv_q8", "orc_q8_dequant", "orc_matmul", "orc_rope_kv_store",
+        for f in ("orc_gemv_q8", "orc_gemv_f16w", "orc_q8_dequant", "orc_matmul", "orc_rope_kv_store",
                   "orc_attn_split", "orc_attn_merge", "orc_attn_full", "orc_plan_groups"):
             getattr(L, f).restype = I
         _lib = L
@@ -99,6 +100,25 @@ def gemv_q8(blocks, x) -> np.ndarray:
     assert xx.shape[1] == n_in
     y = np.zeros((rows, n_out), np.float64)
     _check(lib().orc_gemv_q8(_p(b), n_out, n_in, _p(xx), rows, n_in, _p(y), n_out), "gemv_q8")
+    return y
+
+
+def gemv_f16w(w, x) -> np.ndarray:
+    """y[r][o] (float64) of an f16 weight matrix [n_out][n_in] (float16 values or their uint16
+    bits) against x float32 [rows][n_in]."""
+    if hasattr(w, "detach"):
+        w = w.detach().cpu().numpy()
+    ww = np.ascontiguousarray(w)
+    if ww.dtype == np.float16:
+        ww = ww.view(np.uint16)
+    if ww.dtype != np.uint16:
+        raise TypeError("expected float16 values or uint16 bits, got %s" % ww.dtype)
+    xx = _np(x, np.float32)
+    n_out, n_in = ww.shape
+    rows = xx.shape[0]
+    assert xx.shape[1] == n_in
+    y = np.zeros((rows, n_out), np.float64)
+    _check(lib().orc_gemv_f16w(_p(ww), n_out, n_in, _p(xx), rows, n_in, _p(y), n_out), "gemv_f16w")
     return y
 
 

@@ -182,6 +182,27 @@ int orc_matmul(const double *w, int64_t n_out, int64_t n_in,
     return ORC_OK;
 }
 
+/*
+ * f16-weight GEMV (the halfword-weight "reference lane" of daScript PR #4473, where a
+ * lane reads half-precision weights and accumulates in f32): y[r][o] = sum_i w[o][i] * x[r][i]
+ * with w the binary16 values of a row-major [n_out][n_in] array, every product and sum in double.
+ */
+int orc_gemv_f16w(const uint16_t *w, int64_t n_out, int64_t n_in,
+                  const float *x, int rows, int64_t x_stride,
+                  double *y, int64_t y_stride)
+{
+    if (!w || !x || !y || n_in <= 0 || rows < 0)
+        return ORC_EARG;
+    for (int r = 0; r < rows; ++r)
+        for (int64_t o = 0; o < n_out; ++o) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < n_in; ++i)
+                acc += orc_half_to_double(w[o * n_in + i]) * (double)x[r * x_stride + i];
+            y[r * y_stride + o] = acc;
+        }
+    return ORC_OK;
+}
+
 /* ---------------------------------------------------------------- RoPE --- */
 
 /*

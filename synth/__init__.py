@@ -179,6 +179,19 @@ def q8_0_blocks_from_normal(seed: int, label: str, n_out: int, n_in: int, std: f
     return out
 
 
+def f16_weights_from_normal(seed: int, label: str, n_out: int, n_in: int, std: float = 0.02,
+                            device="cpu", rows_per_chunk: int = 2048) -> torch.Tensor:
+    """An f16 [n_out, n_in] weight matrix drawn w ~ N(0, std^2) and rounded to f16 (RNE), element
+    (o, i) being normal draw o*n_in + i of stream `label`."""
+    sid = stream_id(label)
+    out = torch.empty(n_out, n_in, dtype=torch.float16, device=device)
+    for r0 in range(0, n_out, rows_per_chunk):
+        r1 = min(n_out, r0 + rows_per_chunk)
+        z = _normal_range(seed, sid, r0 * n_in, (r1 - r0) * n_in, device)
+        out[r0:r1] = (z * std).to(torch.float32).view(r1 - r0, n_in).to(torch.float16)
+    return out
+
+
 def _normal_range(seed: int, stream: int, first: int, n: int, device) -> torch.Tensor:
     """Normal draws first..first+n-1 of a stream (Box-Muller pairs aligned to even indices)."""
     p0 = first // 2

@@ -136,6 +136,44 @@ def test_gemv_rows_independent():
         np.testing.assert_array_equal(y[r], oracle.gemv_q8(blocks, x[r:r + 1])[0])
 
 
+@pytest.mark.parametrize("n_out,n_in,rows", [(5, 32, 1), (37, 224, 3), (64, 512, 8)])
+def test_gemv_f16w_matches_numpy_half_matmul(n_out, n_in, rows):
+    """The f16-weight GEMV equals numpy's float16 -> float64 widening followed by a dense product."""
+    w = synth.f16_weights_from_normal(7, "pin/w16", n_out, n_in)
+    x = synth.normal_f32(7, "pin/x16", (rows, n_in))
+    y = oracle.gemv_f16w(w, x)
+    want = x.numpy().astype(np.float64) @ w.numpy().astype(np.float64).T
+    np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-13)
+    # the weight bits and the float16 values give the same result
+    np.testing.assert_array_equal(oracle.gemv_f16w(w.numpy().view(np.uint16), x), y)
+
+
+def test_gemv_f16w_extremes_exact():
+    """Single weights at the ends of the f16 range give exact products: the largest normal
+    65504, the smallest subnormal 2^-24, a negative normal and -0; all others zero."""
+    x = synth.normal_f32(3, "pin/w16x", (2, 64))
+    w = np.zeros((5, 64), np.uint16)
+    w[0, 3] = 0x7BFF          # 65504
+    w[1, 63] = 0x0001         # 2^-24
+    w[2, 10] = 0xC500         # -5.0
+    w[3, 20] = 0x8000         # -0.0
+    y = oracle.gemv_f16w(w, x)
+    for r in range(2):
+        assert y[r, 0] == 65504.0 * float(x[r, 3])
+        assert y[r, 1] == 2.0 ** -24 * float(x[r, 63])
+        assert y[r, 2] == -5.0 * float(x[r, 10])
+        assert y[r, 3] == 0.0 and y[r, 4] == 0.0
+
+
+def test_gemv_f16w_ones_is_row_sum():
+    """w = 1 everywhere: every output is the plain sum of its activation row."""
+    x = synth.normal_f32(4, "pin/w16ones", (3, 96))
+    w = np.full((4, 96), 0x3C00, np.uint16)
+    y = oracle.gemv_f16w(w, x)
+    for r in range(3):
+        assert np.allclose(y[r], math.fsum(float(v) for v in x[r]), rtol=0, atol=1e-12)
+
+
 def test_quantizer_bytes():
     """Q8_0 input encoding: scale max|w|/127 as f16, values rounded half away from zero."""
     w = torch.zeros(1, 32)
@@ -392,6 +430,12 @@ def test_controls_catch_planted_mistakes():
     x = synth.normal_f32(8, "ctl/x", (1, 64))
     y = oracle.gemv_q8(blocks, x)
     assert not np.allclose(y, x.numpy().astype(np.float64) @ _numpy_dequant(blocks), rtol=1e-3)
+    # the f16-weight pin catches a transposed operand and weights read as bf16 instead of f16
+    w16 = synth.f16_weights_from_normal(8, "ctl/w16", 64, 64)
+    y16 = oracle.gemv_f16w(w16, x)
+    assert not np.allclose(y16, x.numpy().astype(np.float64) @ w16.numpy().astype(np.float64), rtol=1e-3)
+    as_bf16 = (w16.numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert not np.allclose(y16, x.numpy().astype(np.float64) @ as_bf16.T, rtol=1e-3)
     # a sign flip in the rotation is caught by the complex-multiplication pin
     xr = np.random.default_rng(0).standard_normal(64)
     yr = oracle.rope_vec(xr, 64, True, 500000.0, 3.0)
