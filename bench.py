@@ -319,6 +319,48 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
                 launches_per_step=step.launches, e2e=e2e)
 
 
+def measure_f16w(dev, peak, n_out=16384, n_in=3072, mats=4, reps=50):
+    """The f16-weight lane on the 3B gate/up shape: `mats` distinct matrices (> L2 together)
+    multiplied back to back in one CUDA graph, per row count; bytes = the f16 weights + x + y."""
+    import synth
+    import torch
+    import row_decode_step_gb300 as dl
+    stream = torch.cuda.Stream(device=dev)
+    Ws = []
+    for m in range(mats):
+        w = synth.f16_weights_from_normal(0, "bench/f16w/%d" % m, n_out, n_in, device=dev)
+        Ws.append(dl.dl_f16w_pack(w))
+        del w
+    out = {"shape": [n_out, n_in], "matrices_cycled": mats}
+    for rows in (1, 8):
+        x = synth.normal_f32(0, "bench/f16w/x/%d" % rows, (rows, n_in), device=dev)
+        y = torch.empty(rows, n_out, device=dev)
+        with torch.cuda.stream(stream):
+            for W in Ws:
+                dl.dl_gemv_f16w(W, x, y, stream=stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for W in Ws:
+                dl.dl_gemv_f16w(W, x, y, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            k0 = torch.cuda.Event(enable_timing=True)
+            k1 = torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            k1.record(stream)
+        torch.cuda.synchronize()
+        ms = k0.elapsed_time(k1) / (reps * mats)
+        b = n_out * n_in * 2 + rows * (n_in + n_out) * 4
+        out["rows_%d" % rows] = {"launch_us": ms * 1e3, "achieved_gbs": b / (ms / 1e3) / 1e9,
+                                 "frac": b / (ms / 1e3) / 1e9 / peak}
+        del g
+    return out
+
+
 def measure_e2e(step, graphs, L, steps, stream, dev):
     """Same steps through host buffers: per step, the activation rows and positions are copied
     from pinned host memory, the graph runs, and the step's outputs are read back."""
@@ -443,6 +485,9 @@ def run_ours(args):
                             "commands": len(r2["step"].commands), "status": r2["status"]}
             del r2
             torch.cuda.empty_cache()
+    if not args.no_extras and args.workload == "3b-8":
+        extras["f16w_gemv"] = measure_f16w(dev, peak)
+        torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(wl)

@@ -12,6 +12,7 @@
  *   dl_decode_attn    split-KV decode attention with GQA, the split sized by the
  *                     command's rows
  *   dl_attn_merge     log-sum-exp merge of the split pieces
+ *   dl_gemv_f16w      the same projection GEMV on f16 weights (the reference lane)
  *
  * plus host-side helpers (weight packing, RoPE tables, the row-grouping and
  * split planner, status words).
@@ -35,6 +36,9 @@
  *         on every GPU home", commit "cud_router_enc_cols tiles every router
  *         launch": a projection launch holds eight activation columns, longer
  *         launches are tiled, every row equal to the row stepped alone.
+ *  [F16W] the same PR #4473, its description: every GPU home serves two weight
+ *         lanes, q8 by default and f16 (halfword weights, f32 accumulate) as the
+ *         reference lane.
  *  [ROPE] daScript PR #4293 "dasLLAMA llama leg ...", commit "The decode
  *         rope-and-store rides one template on both homes" (GkRopeKvStore).
  *  [GRP]  the same PR, commit "The Vulkan batched step past eight rows runs in
@@ -147,6 +151,51 @@ int dl_gemv_q8(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride
  */
 int dl_gemv_q8_ex(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
                   float *y, int64_t y_stride, int path, dl_stream_t stream);
+
+/* ------------------------------------------------- f16 weights (reference lane)
+ *
+ * The halfword-weight lane [F16W]: y[r][o] = sum_i w[o][i] * x[r][i] with w in
+ * binary16, accumulated in f32.
+ *
+ * Interchange form: a row-major [n_out][n_in] array of f16 bit patterns.
+ * Device form (written by dl_f16w_pack, read by dl_gemv_f16w): tiles of 16 output
+ * rows x 32 inputs, 1024 bytes, tile (rt, kt) at byte ((rt * KT) + kt) * 1024 with
+ * KT = 4 * ceil(n_in / 128); the 32 bytes of lane t = 4g + c are eight words,
+ * word m holding inputs kb and kb + 1 (kb = 16*(p/2) + 8*(p%2) + 2c, p = m/2) of
+ * row g + 8*(m%2) (the A operands of two 16x8x16 f16 tensor-core products).
+ * Rows past n_out and inputs past n_in hold 0.  The plane must be 16-byte aligned.
+ */
+typedef struct dl_f16_weight {
+    const void *w;      /* device, packed f16 tiles */
+    int64_t n_out;      /* output features */
+    int64_t n_in;       /* input features, a multiple of 32 */
+} dl_f16_weight;
+
+/* Size in bytes of the device plane for an [n_out][n_in] f16 weight.  Host only. */
+int dl_f16w_packed_size(int64_t n_out, int64_t n_in, size_t *bytes);
+
+/*
+ * Convert an interchange f16 matrix (device, n_out * n_in halves, 2-byte aligned)
+ * into the device form (packed: device, dl_f16w_packed_size bytes, 16-byte
+ * aligned).  One-time preparation, not part of a decode step.
+ */
+int dl_f16w_pack(const uint16_t *w, int64_t n_out, int64_t n_in, void *packed, dl_stream_t stream);
+
+/*
+ * f16-weight GEMV [F16W]: y[r][o] = sum_i w[o][i] * x[r][i] for r < rows, o < n_out.
+ * Arguments, strides, alignment, row grouping and error codes as dl_gemv_q8.
+ * Arithmetic: CUDA cores for commands of 1 or 2 rows (the f16 weights widened
+ * to f32, f32 FMAs); tensor cores for 3 to 8 (16x8x16 f16 products of the
+ * weights as stored with each activation row scaled per warp by a power of two
+ * and split into two f16 terms, f32 accumulation).
+ */
+int dl_gemv_f16w(const dl_f16_weight *W, const float *x, int rows, int64_t x_stride,
+                 float *y, int64_t y_stride, dl_stream_t stream);
+
+/* dl_gemv_f16w with the inner product chosen by the caller: path 0 automatic,
+ * 1 CUDA cores (1 or 2 rows only, else DL_E_SHAPE), 2 tensor cores. */
+int dl_gemv_f16w_ex(const dl_f16_weight *W, const float *x, int rows, int64_t x_stride,
+                    float *y, int64_t y_stride, int path, dl_stream_t stream);
 
 /* ---------------------------------------------------------------- KV cache */
 

@@ -96,7 +96,7 @@ uint16_t orc_double_to_half(double x)
 
 /*
  * Decoded value of every binary16 pattern, filled on first use from
- * orc_half_to_double (a speed-up of the attention loops only; same values).
+ * orc_half_to_double (a speed-up of the attention and f16-weight loops only; same values).
  */
 static double orc_h2d_table[65536];
 static int orc_h2d_ready = 0;
@@ -185,7 +185,8 @@ int orc_matmul(const double *w, int64_t n_out, int64_t n_in,
 /*
  * f16-weight GEMV (the halfword-weight "reference lane" of daScript PR #4473, where a
  * lane reads half-precision weights and accumulates in f32): y[r][o] = sum_i w[o][i] * x[r][i]
- * with w the binary16 values of a row-major [n_out][n_in] array, every product and sum in double.
+ * with w the binary16 values of a row-major [n_out][n_in] array, every product and sum in double
+ * (the values come from the decode table of orc_half_to_double).
  */
 int orc_gemv_f16w(const uint16_t *w, int64_t n_out, int64_t n_in,
                   const float *x, int rows, int64_t x_stride,
@@ -197,7 +198,7 @@ int orc_gemv_f16w(const uint16_t *w, int64_t n_out, int64_t n_in,
         for (int64_t o = 0; o < n_out; ++o) {
             double acc = 0.0;
             for (int64_t i = 0; i < n_in; ++i)
-                acc += orc_half_to_double(w[o * n_in + i]) * (double)x[r * x_stride + i];
+                acc += orc_h2d(w[o * n_in + i]) * (double)x[r * x_stride + i];
             y[r * y_stride + o] = acc;
         }
     return ORC_OK;

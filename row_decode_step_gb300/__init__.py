@@ -47,6 +47,10 @@ class dl_q8_weight(ctypes.Structure):
                 ("n_out", ctypes.c_int64), ("n_in", ctypes.c_int64)]
 
 
+class dl_f16_weight(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("n_out", ctypes.c_int64), ("n_in", ctypes.c_int64)]
+
+
 class dl_kv_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("region_stride", ctypes.c_int64),
                 ("n_regions", ctypes.c_int), ("n_kv", ctypes.c_int), ("head_dim", ctypes.c_int),
@@ -91,6 +95,10 @@ def lib() -> ctypes.CDLL:
             "dl_q8_pack": ([P, I64, I64, P, P, P], I),
             "dl_gemv_q8": ([P, P, I, I64, P, I64, P], I),
             "dl_gemv_q8_ex": ([P, P, I, I64, P, I64, I, P], I),
+            "dl_f16w_packed_size": ([I64, I64, P], I),
+            "dl_f16w_pack": ([P, I64, I64, P, P], I),
+            "dl_gemv_f16w": ([P, P, I, I64, P, I64, P], I),
+            "dl_gemv_f16w_ex": ([P, P, I, I64, P, I64, I, P], I),
             "dl_rope_table_bytes": ([I, I, P], I),
             "dl_rope_table_build": ([ctypes.c_double, I, I, P], I),
             "dl_rope_kv_store": ([P, I64, P, I64, P, I64, P, P, P, I, I, P, P, P, P], I),
@@ -165,6 +173,36 @@ def dl_q8_pack(blocks: torch.Tensor, n_out: int, n_in: int, stream=None) -> Pack
     return PackedQ8(qs, d, n_out, n_in)
 
 
+class PackedF16W:
+    """An f16 weight in the library's device form (the plane kept alive here)."""
+
+    def __init__(self, w: torch.Tensor, n_out: int, n_in: int):
+        self.w, self.n_out, self.n_in = w, int(n_out), int(n_in)
+        self.c = dl_f16_weight(w.data_ptr(), self.n_out, self.n_in)
+
+    @property
+    def nbytes_f16(self) -> int:
+        """Bytes of the matrix as f16 values."""
+        return self.n_out * self.n_in * 2
+
+
+def dl_f16w_packed_size(n_out: int, n_in: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().dl_f16w_packed_size(n_out, n_in, ctypes.byref(b)))
+    return b.value
+
+
+def dl_f16w_pack(w: torch.Tensor, stream=None) -> PackedF16W:
+    """Pack a row-major f16 weight matrix (float16 CUDA tensor [n_out][n_in])."""
+    _dev(w, torch.float16, "w")
+    if w.dim() != 2 or not w.is_contiguous():
+        raise ValueError("w must be a contiguous [n_out][n_in] float16 tensor")
+    n_out, n_in = w.shape
+    packed = torch.empty(dl_f16w_packed_size(n_out, n_in), dtype=torch.uint8, device=w.device)
+    _check(lib().dl_f16w_pack(_ptr(w), n_out, n_in, _ptr(packed), _stream(stream)))
+    return PackedF16W(packed, n_out, n_in)
+
+
 GEMV_PATH_AUTO, GEMV_PATH_CUDA_CORE, GEMV_PATH_TENSOR = 0, 1, 2
 
 
@@ -185,6 +223,25 @@ def dl_gemv_q8(W: PackedQ8, x: torch.Tensor, y: Optional[torch.Tensor] = None, s
     else:
         _check(lib().dl_gemv_q8_ex(ctypes.byref(W.c), _ptr(x), rows, x.stride(0), _ptr(y), y.stride(0),
                                    path, _stream(stream)))
+    return y
+
+
+def dl_gemv_f16w(W: PackedF16W, x: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None,
+                 path: int = GEMV_PATH_AUTO) -> torch.Tensor:
+    """y[r] = W x[r] for every row of x with f16 weights (f32 [rows][>= n_in], rows may exceed eight)."""
+    _dev(x, torch.float32, "x")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit inner stride")
+    rows = x.shape[0]
+    if y is None:
+        y = torch.empty(rows, W.n_out, dtype=torch.float32, device=x.device)
+    _dev(y, torch.float32, "y")
+    if path == GEMV_PATH_AUTO:
+        _check(lib().dl_gemv_f16w(ctypes.byref(W.c), _ptr(x), rows, x.stride(0), _ptr(y), y.stride(0),
+                                  _stream(stream)))
+    else:
+        _check(lib().dl_gemv_f16w_ex(ctypes.byref(W.c), _ptr(x), rows, x.stride(0), _ptr(y), y.stride(0),
+                                     path, _stream(stream)))
     return y
 
 

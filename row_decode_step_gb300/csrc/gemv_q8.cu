@@ -63,15 +63,16 @@ struct GemvArgs {
 constexpr int kConsumers = 8;                        // warps, each a share of the K-slice
 constexpr int kThreads = kConsumers * 32;
 constexpr int kMaxStages = 8;
-constexpr int kStageTileBytes = 512 + 32;            // weights and scales of one k-tile
+constexpr int kTileBytesQ8 = 512 + 32;               // Q8_0: weights and scales of one k-tile
+constexpr int kTileBytesF16 = 1024;                  // f16 weights of one k-tile
 constexpr int kRowBatch = 4;                         // row tiles whose partials a warp holds at once
 constexpr size_t kRedBytes = (size_t)kRowBatch * kConsumers * 128 * 4;   // one batch of per-warp partials
 
 // Shared-memory bytes of a launch: the ring, the per-stage partials and, with clusters,
 // this CTA's K-slice sums of its row tiles.
-size_t gemv_smem(int ksl, int stages, int rpr, int cs)
+size_t gemv_smem(int ksl, int stages, int rpr, int cs, int tile_bytes)
 {
-    return (size_t)stages * ksl * kStageTileBytes + kRedBytes + (cs > 1 ? (size_t)rpr * 128 * 4 : 0);
+    return (size_t)stages * ksl * tile_bytes + kRedBytes + (cs > 1 ? (size_t)rpr * 128 * 4 : 0);
 }
 
 // ---- arithmetic helpers
@@ -98,10 +99,12 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 }
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-template <bool MMA, int NRC, int KWM>
+// W16: the weights are f16 (the halfword-weight lane) instead of Q8_0 biased bytes and scales.
+template <bool W16, bool MMA, int NRC, int KWM>
 __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_constant__ GemvArgs a)
 {
     constexpr int RB = kRowBatch;
+    constexpr int TB = W16 ? kTileBytesF16 : kTileBytesQ8;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ int s_shape_bad, s_issued;
@@ -113,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     const int nrt = max(0, min(a.rpr, a.RT - rt0));      // row tiles of this CTA
     const int kt0 = slice * a.ksl, kt1 = min(a.KT, kt0 + a.ksl);
     const int nkt = max(0, kt1 - kt0);
-    const uint32_t wbytes = (uint32_t)nkt * 512u, dbytes = (uint32_t)nkt * 32u;
-    const size_t SB = (size_t)a.ksl * kStageTileBytes;
+    const uint32_t wbytes = (uint32_t)nkt * (W16 ? 1024u : 512u), dbytes = W16 ? 0u : (uint32_t)nkt * 32u;
+    const size_t SB = (size_t)a.ksl * TB;
     unsigned char *ring = smem;
     float *red = reinterpret_cast<float *>(smem + S * SB);          // [kRowBatch][kConsumers][128]
     float *part = red + kRowBatch * kConsumers * 128;                // [rpr][128] (clusters)
@@ -131,14 +134,18 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         s_issued = min(S, nrt);
         dla::mbar_init_fence();
     }
-    // a slice shorter than the stage (the last one of K): the scales of the missing k-tiles
-    // read as zero, so that whatever the stage holds there contributes nothing (the copies carry
-    // this slice's k-tiles only, so these bytes are never overwritten)
-    if (nkt < a.ksl)
-        for (int e = threadIdx.x; e < S * (a.ksl - nkt) * 8; e += kThreads) {
-            const int st = e / ((a.ksl - nkt) * 8), w = e - st * (a.ksl - nkt) * 8;
-            reinterpret_cast<uint32_t *>(ring + st * SB + (size_t)a.ksl * 512 + (size_t)nkt * 32)[w] = 0u;
+    // a slice shorter than the stage (the last one of K): the missing k-tiles' scales (Q8_0) or
+    // weights (f16, where stale bytes could read as Inf or NaN and poison 0 * w) read as zero, so
+    // that they contribute nothing (the copies carry this slice's k-tiles only, so these bytes
+    // are never overwritten)
+    if (nkt < a.ksl) {
+        const int zw = (a.ksl - nkt) * (W16 ? 256 : 8);              // words per slot
+        const size_t z0 = W16 ? (size_t)nkt * 1024 : (size_t)a.ksl * 512 + (size_t)nkt * 32;
+        for (int e = threadIdx.x; e < S * zw; e += kThreads) {
+            const int st = e / zw, w = e - st * zw;
+            reinterpret_cast<uint32_t *>(ring + st * SB + z0)[w] = 0u;
         }
+    }
     __syncthreads();
 
     // stage j: row tile rt0 + j, this slice's k-tiles (contiguous), then their scales (contiguous)
@@ -147,8 +154,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         const int rt = rt0 + j;
         unsigned char *dst = ring + st * SB;
         dla::mbar_expect_tx(&full[st], wbytes + dbytes);
-        dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
-        dla::bulk_g2s(dst + (size_t)a.ksl * 512, a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes, &full[st]);
+        if constexpr (W16) {
+            dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 1024, wbytes, &full[st]);
+        } else {
+            dla::bulk_g2s(dst, a.qs + ((size_t)rt * a.KT + kt0) * 512, wbytes, &full[st]);
+            dla::bulk_g2s(dst + (size_t)a.ksl * 512, a.d + ((size_t)rt * KG + (kt0 >> 2)) * 128, dbytes,
+                          &full[st]);
+        }
     };
     // the weights do not depend on the previous kernel: the first stages are requested before
     // waiting on it, the rest once the activations are requested (an SM's requests are served
@@ -172,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     if (lane == 0 && kConsumers * KWM != a.ksl) atomicExch(&s_shape_bad, 1);   // broken launch shape
     // lane (g, c) holds inputs 2c, 2c+1 / 8+2c, 9+2c / 16+2c, 17+2c / 24+2c, 25+2c of each k-tile
     uint32_t bh[MMA ? KWM : 1][4], bl[MMA ? KWM : 1][4];
-    float2 ncorr[MMA ? KWM : 1];                 // -1152 * sum(x) of columns 2c, 2c+1 per k-tile
+    float2 ncorr[MMA && !W16 ? KWM : 1];         // -1152 * sum(x) of columns 2c, 2c+1 per k-tile (Q8_0)
     float xv[MMA ? 1 : KWM][NRC][8];
     float us0 = 1.f, us1 = 1.f;
     if constexpr (MMA) {
@@ -220,11 +232,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
                 bl[j][p] = h2_bits(l);
                 colsum += (hf.x + lf.x) + (hf.y + lf.y);
             }
-            colsum += __shfl_xor_sync(0xffffffffu, colsum, 1);
-            colsum += __shfl_xor_sync(0xffffffffu, colsum, 2);
-            // accumulator columns of this lane are activation rows 2c and 2c+1 (lanes 8c, 8c+4)
-            ncorr[j] = make_float2(-1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c),
-                                   -1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c + 4));
+            if constexpr (!W16) {
+                colsum += __shfl_xor_sync(0xffffffffu, colsum, 1);
+                colsum += __shfl_xor_sync(0xffffffffu, colsum, 2);
+                // accumulator columns of this lane are activation rows 2c and 2c+1 (lanes 8c, 8c+4)
+                ncorr[j] = make_float2(-1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c),
+                                       -1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c + 4));
+            }
         }
         us0 = __shfl_sync(0xffffffffu, inv, 8 * c);
         us1 = __shfl_sync(0xffffffffu, inv, 8 * c + 4);
@@ -275,44 +289,80 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
 #pragma unroll
                 for (int j = 0; j < KWM; ++j) {
                     const int kl = wk0 + j;                                  // slice-local k-tile
-                    const uint4 w = *reinterpret_cast<const uint4 *>(sw + kl * 512 + lane * 16);
-                    const __half2 sp = *reinterpret_cast<const __half2 *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4);
-                    const float2 dgh = __half22float2(sp);          // (d[g], d[g+8])
-                    const float dg = dgh.x, dh = dgh.y;
-                    if constexpr (MMA) {
-                        float t[4] = {0.f, 0.f, 0.f, 0.f};
-                        const uint32_t a0 = u8x2_to_h2(w.x, 0x4140u), a1 = u8x2_to_h2(w.x, 0x4342u);
-                        const uint32_t a2 = u8x2_to_h2(w.y, 0x4140u), a3 = u8x2_to_h2(w.y, 0x4342u);
-                        mma16816(t, a0, a1, a2, a3, bh[j][0], bh[j][1]);
-                        mma16816(t, a0, a1, a2, a3, bl[j][0], bl[j][1]);
-                        const uint32_t a4 = u8x2_to_h2(w.z, 0x4140u), a5 = u8x2_to_h2(w.z, 0x4342u);
-                        const uint32_t a6 = u8x2_to_h2(w.w, 0x4140u), a7 = u8x2_to_h2(w.w, 0x4342u);
-                        mma16816(t, a4, a5, a6, a7, bh[j][2], bh[j][3]);
-                        mma16816(t, a4, a5, a6, a7, bl[j][2], bl[j][3]);
-                        acc01[r] = __ffma2_rn(make_float2(dg, dg), __fadd2_rn(make_float2(t[0], t[1]), ncorr[j]), acc01[r]);
-                        acc23[r] = __ffma2_rn(make_float2(dh, dh), __fadd2_rn(make_float2(t[2], t[3]), ncorr[j]), acc23[r]);
-                    } else {
-                        // row g: bytes 0, 1 of each word; row g+8: bytes 2, 3 (inputs 2p, 2p+1 of
-                        // the lane's eight), multiplied pairwise with the activation pairs
-                        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
-                        float2 wg[4], wh[4];
+                    if constexpr (W16) {
+                        // lane's 32 bytes: the A operands of the two 16x8x16 products, f16 as stored
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(sw + kl * 1024 + lane * 32);
+                        const uint4 w1 = *reinterpret_cast<const uint4 *>(sw + kl * 1024 + lane * 32 + 16);
+                        if constexpr (MMA) {
+                            float t[4] = {acc01[r].x, acc01[r].y, acc23[r].x, acc23[r].y};
+                            mma16816(t, w0.x, w0.y, w0.z, w0.w, bh[j][0], bh[j][1]);
+                            mma16816(t, w0.x, w0.y, w0.z, w0.w, bl[j][0], bl[j][1]);
+                            mma16816(t, w1.x, w1.y, w1.z, w1.w, bh[j][2], bh[j][3]);
+                            mma16816(t, w1.x, w1.y, w1.z, w1.w, bl[j][2], bl[j][3]);
+                            acc01[r] = make_float2(t[0], t[1]);
+                            acc23[r] = make_float2(t[2], t[3]);
+                        } else {
+                            // word 2p: row g, inputs of pair p; word 2p + 1: row g + 8
+                            const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                            float2 wg[4], wh[4];
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            wg[p] = u8x2_to_f32x2(wd[p], 0);
-                            wh[p] = u8x2_to_f32x2(wd[p], 2);
-                        }
-#pragma unroll
-                        for (int q = 0; q < NRC; ++q) {
-                            const float2 x0 = make_float2(xv[j][q][0], xv[j][q][1]);
-                            float2 sg = __fmul2_rn(wg[0], x0), sh = __fmul2_rn(wh[0], x0);
-#pragma unroll
-                            for (int p = 1; p < 4; ++p) {
-                                const float2 xp = make_float2(xv[j][q][2 * p], xv[j][q][2 * p + 1]);
-                                sg = __ffma2_rn(wg[p], xp, sg);
-                                sh = __ffma2_rn(wh[p], xp, sh);
+                            for (int p = 0; p < 4; ++p) {
+                                wg[p] = __half22float2(*reinterpret_cast<const __half2 *>(&wd[2 * p]));
+                                wh[p] = __half22float2(*reinterpret_cast<const __half2 *>(&wd[2 * p + 1]));
                             }
-                            accg[r][q] = __ffma2_rn(make_float2(dg, dg), sg, accg[r][q]);
-                            acch[r][q] = __ffma2_rn(make_float2(dh, dh), sh, acch[r][q]);
+#pragma unroll
+                            for (int q = 0; q < NRC; ++q) {
+                                float2 sg = accg[r][q], sh = acch[r][q];
+#pragma unroll
+                                for (int p = 0; p < 4; ++p) {
+                                    const float2 xp = make_float2(xv[j][q][2 * p], xv[j][q][2 * p + 1]);
+                                    sg = __ffma2_rn(wg[p], xp, sg);
+                                    sh = __ffma2_rn(wh[p], xp, sh);
+                                }
+                                accg[r][q] = sg;
+                                acch[r][q] = sh;
+                            }
+                        }
+                    } else {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(sw + kl * 512 + lane * 16);
+                        const __half2 sp = *reinterpret_cast<const __half2 *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4);
+                        const float2 dgh = __half22float2(sp);          // (d[g], d[g+8])
+                        const float dg = dgh.x, dh = dgh.y;
+                        if constexpr (MMA) {
+                            float t[4] = {0.f, 0.f, 0.f, 0.f};
+                            const uint32_t a0 = u8x2_to_h2(w.x, 0x4140u), a1 = u8x2_to_h2(w.x, 0x4342u);
+                            const uint32_t a2 = u8x2_to_h2(w.y, 0x4140u), a3 = u8x2_to_h2(w.y, 0x4342u);
+                            mma16816(t, a0, a1, a2, a3, bh[j][0], bh[j][1]);
+                            mma16816(t, a0, a1, a2, a3, bl[j][0], bl[j][1]);
+                            const uint32_t a4 = u8x2_to_h2(w.z, 0x4140u), a5 = u8x2_to_h2(w.z, 0x4342u);
+                            const uint32_t a6 = u8x2_to_h2(w.w, 0x4140u), a7 = u8x2_to_h2(w.w, 0x4342u);
+                            mma16816(t, a4, a5, a6, a7, bh[j][2], bh[j][3]);
+                            mma16816(t, a4, a5, a6, a7, bl[j][2], bl[j][3]);
+                            acc01[r] = __ffma2_rn(make_float2(dg, dg), __fadd2_rn(make_float2(t[0], t[1]), ncorr[j]), acc01[r]);
+                            acc23[r] = __ffma2_rn(make_float2(dh, dh), __fadd2_rn(make_float2(t[2], t[3]), ncorr[j]), acc23[r]);
+                        } else {
+                            // row g: bytes 0, 1 of each word; row g+8: bytes 2, 3 (inputs 2p, 2p+1 of
+                            // the lane's eight), multiplied pairwise with the activation pairs
+                            const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+                            float2 wg[4], wh[4];
+#pragma unroll
+                            for (int p = 0; p < 4; ++p) {
+                                wg[p] = u8x2_to_f32x2(wd[p], 0);
+                                wh[p] = u8x2_to_f32x2(wd[p], 2);
+                            }
+#pragma unroll
+                            for (int q = 0; q < NRC; ++q) {
+                                const float2 x0 = make_float2(xv[j][q][0], xv[j][q][1]);
+                                float2 sg = __fmul2_rn(wg[0], x0), sh = __fmul2_rn(wh[0], x0);
+#pragma unroll
+                                for (int p = 1; p < 4; ++p) {
+                                    const float2 xp = make_float2(xv[j][q][2 * p], xv[j][q][2 * p + 1]);
+                                    sg = __ffma2_rn(wg[p], xp, sg);
+                                    sh = __ffma2_rn(wh[p], xp, sh);
+                                }
+                                accg[r][q] = __ffma2_rn(make_float2(dg, dg), sg, accg[r][q]);
+                                acch[r][q] = __ffma2_rn(make_float2(dh, dh), sh, acch[r][q]);
+                            }
                         }
                     }
                 }
@@ -491,30 +541,39 @@ __global__ void q8_pack_d_kernel(const uint8_t *blocks, int64_t n_out, int64_t n
 // ---------------------------------------------------------------- launch
 
 struct GemvCfg {
-    bool mma;
+    bool w16, mma;
     int nrc, kwm, cs, ksl, rpr, stages, grid;
     size_t smem;
 };
 
-template <bool MMA, int NRC, int KWM>
-void *kptr() { return reinterpret_cast<void *>(gemv_q8_kernel<MMA, NRC, KWM>); }
+template <bool W16, bool MMA, int NRC, int KWM>
+void *kptr() { return reinterpret_cast<void *>(gemv_q8_kernel<W16, MMA, NRC, KWM>); }
 
-void *pick_kernel(bool mma, int nrc, int kwm)
+void *pick_kernel(bool w16, bool mma, int nrc, int kwm)
 {
+    if (w16) {
+        // a k-tile is 1 KB: windows of up to 4 k-tiles per warp keep two stages per CTA in reach
+        switch (kwm) {
+        case 1: return mma ? kptr<true, true, 1, 1>() : nrc == 1 ? kptr<true, false, 1, 1>() : kptr<true, false, 2, 1>();
+        case 2: return mma ? kptr<true, true, 1, 2>() : nrc == 1 ? kptr<true, false, 1, 2>() : kptr<true, false, 2, 2>();
+        case 4: return mma ? kptr<true, true, 1, 4>() : nrc == 1 ? kptr<true, false, 1, 4>() : kptr<true, false, 2, 4>();
+        }
+        return nullptr;
+    }
     if (mma) {
         switch (kwm) {
-        case 1: return kptr<true, 1, 1>();
-        case 2: return kptr<true, 1, 2>();
-        case 4: return kptr<true, 1, 4>();
-        case 6: return kptr<true, 1, 6>();
+        case 1: return kptr<false, true, 1, 1>();
+        case 2: return kptr<false, true, 1, 2>();
+        case 4: return kptr<false, true, 1, 4>();
+        case 6: return kptr<false, true, 1, 6>();
         }
         return nullptr;
     }
     switch (kwm) {
-    case 1: return nrc == 1 ? kptr<false, 1, 1>() : kptr<false, 2, 1>();
-    case 2: return nrc == 1 ? kptr<false, 1, 2>() : kptr<false, 2, 2>();
-    case 4: return nrc == 1 ? kptr<false, 1, 4>() : kptr<false, 2, 4>();
-    case 8: return nrc == 1 ? kptr<false, 1, 8>() : nullptr;
+    case 1: return nrc == 1 ? kptr<false, false, 1, 1>() : kptr<false, false, 2, 1>();
+    case 2: return nrc == 1 ? kptr<false, false, 1, 2>() : kptr<false, false, 2, 2>();
+    case 4: return nrc == 1 ? kptr<false, false, 1, 4>() : kptr<false, false, 2, 4>();
+    case 8: return nrc == 1 ? kptr<false, false, 1, 8>() : nullptr;
     }
     return nullptr;
 }
@@ -654,20 +713,21 @@ int max_clusters(const void *kern, int csz, size_t smem)
 // consecutive row tiles of one slice and streams them one row tile per ring stage.  Among the
 // shapes that run in one wave with two CTAs per SM, the least bytes per CTA wins (near-ties go
 // to fewer slices).  Matrices too tall for one wave run in several.
-int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
+int choose_cfg(bool w16, int nr, int RT, int KT, int sm, int path, GemvCfg *out)
 {
     const bool mma = path == PATH_TENSOR || (path == PATH_AUTO && nr > 2);
     if (!mma && nr > 2) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: the CUDA-core path serves 1 or 2 rows per command");
     const int nrc = mma ? 1 : nr;
+    const int tb = w16 ? kTileBytesF16 : kTileBytesQ8;
     GemvCfg best{};
     long best_cost = -1;
     for (int kwm : {8, 6, 4, 2, 1}) {                           // fewer slices first
-        const void *kern = pick_kernel(mma, nrc, kwm);
+        const void *kern = pick_kernel(w16, mma, nrc, kwm);
         if (!kern) continue;
         const int ksl = kConsumers * kwm;
         const int cs = (int)dl::ceil_div(KT, ksl);
         if (cs > 16) continue;
-        const size_t sb = (size_t)ksl * kStageTileBytes;
+        const size_t sb = (size_t)ksl * tb;
         const int per_sm = two_per_sm(kern) ? 2 : 1;
         if (cs > 1 && clusters_one_per_sm(kern, cs) < 1) continue;
         // footprint for an even spread of the row tiles over per_sm CTAs per SM, then the real
@@ -676,20 +736,20 @@ int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
         stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
         int rpr = (int)dl::ceil_div(RT, std::max(1, (per_sm * sm) / cs));
         const size_t limit = per_sm == 2 ? kShareLimit : (size_t)kSmemLimit;
-        while (stages > 2 && gemv_smem(ksl, stages, rpr, cs) > limit) --stages;
-        size_t smem = gemv_smem(ksl, stages, rpr, cs);
+        while (stages > 2 && gemv_smem(ksl, stages, rpr, cs, tb) > limit) --stages;
+        size_t smem = gemv_smem(ksl, stages, rpr, cs, tb);
         if (smem > (size_t)kSmemLimit) continue;
         const int nclu = cs == 1 ? per_sm * sm : max_clusters(kern, cs, smem);
         if (nclu < 1) continue;
         rpr = (int)dl::ceil_div(RT, nclu);
-        smem = gemv_smem(ksl, stages, rpr, cs);
+        smem = gemv_smem(ksl, stages, rpr, cs, tb);
         if (smem > (size_t)kSmemLimit) continue;
         const int ctas = (int)dl::ceil_div(RT, rpr) * cs;
         const int ctas_per_sm = (int)dl::ceil_div(ctas, sm);
         const long cost = (long)ctas_per_sm * rpr * ksl * 100 + cs;   // bytes per SM, then fewer slices
         if (best_cost < 0 || cost * 100 < best_cost * 95) {
             best_cost = cost;
-            best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, ctas, smem};
+            best = GemvCfg{w16, mma, nrc, kwm, cs, ksl, rpr, stages, ctas, smem};
         }
     }
     if (best_cost < 0) {
@@ -697,35 +757,35 @@ int choose_cfg(int nr, int RT, int KT, int sm, int path, GemvCfg *out)
         // holds, in several waves
         for (int kwm : {8, 6, 4, 2, 1}) {
             if (best_cost >= 0) break;
-            if (!pick_kernel(mma, nrc, kwm)) continue;
+            if (!pick_kernel(w16, mma, nrc, kwm)) continue;
             const int ksl = kConsumers * kwm;
             const int cs = (int)dl::ceil_div(KT, ksl);
             if (cs > 16) continue;
-            const size_t sb = (size_t)ksl * kStageTileBytes;
+            const size_t sb = (size_t)ksl * tb;
             int stages = (int)(kRingBudget / sb);
             stages = stages < 2 ? 2 : stages > kMaxStages ? kMaxStages : stages;
-            const size_t fixed = gemv_smem(ksl, stages, 0, cs);
+            const size_t fixed = gemv_smem(ksl, stages, 0, cs, tb);
             if (fixed >= (size_t)kSmemLimit) continue;
             int rpr = cs > 1 ? (int)(((size_t)kSmemLimit - fixed) / 512) : (int)dl::ceil_div(RT, sm);
             if (rpr < 1) continue;
             if (rpr > RT) rpr = RT;
             best_cost = 0;
-            best = GemvCfg{mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
-                           gemv_smem(ksl, stages, rpr, cs)};
+            best = GemvCfg{w16, mma, nrc, kwm, cs, ksl, rpr, stages, (int)dl::ceil_div(RT, rpr) * cs,
+                           gemv_smem(ksl, stages, rpr, cs, tb)};
         }
         if (best_cost < 0) return dl::fail(DL_E_SHAPE, "dl_gemv_q8: no launch shape for %d k-tiles", KT);
     }
-    const void *kern = pick_kernel(best.mma, best.nrc, best.kwm);
+    const void *kern = pick_kernel(best.w16, best.mma, best.nrc, best.kwm);
     const int rc = prepare_kernel(kern, best.cs);
     if (rc != DL_OK) return rc;
     *out = best;
     return DL_OK;
 }
 
-int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
+int gemv_group(GemvArgs a, bool w16, int nr, int sm, int path, cudaStream_t st)
 {
     GemvCfg cfg;
-    int rc = choose_cfg(nr, a.RT, a.KT, sm, path, &cfg);
+    int rc = choose_cfg(w16, nr, a.RT, a.KT, sm, path, &cfg);
     if (rc != DL_OK) return rc;
     a.nr = nr;
     a.cs = cfg.cs;
@@ -735,7 +795,7 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     // two stages per CTA ahead of the activations: about what an SM receives while the previous
     // kernel drains
     a.pre = 2;
-    const void *kern = pick_kernel(cfg.mma, cfg.nrc, cfg.kwm);
+    const void *kern = pick_kernel(cfg.w16, cfg.mma, cfg.nrc, cfg.kwm);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid);
     lc.blockDim = dim3(kThreads);
@@ -761,38 +821,36 @@ int gemv_group(GemvArgs a, int nr, int sm, int path, cudaStream_t st)
     return DL_OK;
 }
 
-int gemv_impl(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride, float *y, int64_t y_stride,
-              int path, dl_stream_t stream)
+// Shared launch path of both weight kinds (the caller has checked the matrix shape).
+int gemv_run(const char *name, const void *wq, const void *wd, int64_t n_out, int64_t n_in, bool w16,
+             const float *x, int rows, int64_t x_stride, float *y, int64_t y_stride, int path, dl_stream_t stream)
 {
-    dl::clear_error();
-    if (!W || !x || !y || !W->qs || !W->d) return dl::fail(DL_E_ARG, "dl_gemv_q8: null pointer");
-    if (rows < 0) return dl::fail(DL_E_ARG, "dl_gemv_q8: rows=%d", rows);
-    if (path < PATH_AUTO || path > PATH_TENSOR) return dl::fail(DL_E_ARG, "dl_gemv_q8: path=%d", path);
-    int rc = dl_q8_packed_size(W->n_out, W->n_in, nullptr, nullptr);
-    if (rc != DL_OK) return rc;
+    if (!x || !y) return dl::fail(DL_E_ARG, "%s: null pointer", name);
+    if (rows < 0) return dl::fail(DL_E_ARG, "%s: rows=%d", name, rows);
+    if (path < PATH_AUTO || path > PATH_TENSOR) return dl::fail(DL_E_ARG, "%s: path=%d", name, path);
     if (rows == 0) return DL_OK;
-    if (x_stride < W->n_in || y_stride < W->n_out)
-        return dl::fail(DL_E_ARG, "dl_gemv_q8: strides %lld/%lld below the row widths",
+    if (x_stride < n_in || y_stride < n_out)
+        return dl::fail(DL_E_ARG, "%s: strides %lld/%lld below the row widths", name,
                         (long long)x_stride, (long long)y_stride);
-    if (!dl::aligned16(x) || (x_stride % 4) != 0 || !dl::aligned16(W->qs) || !dl::aligned16(W->d))
-        return dl::fail(DL_E_ALIGN, "dl_gemv_q8: x, its stride and the weight planes must be 16-byte aligned");
+    if (!dl::aligned16(x) || (x_stride % 4) != 0 || !dl::aligned16(wq) || (wd && !dl::aligned16(wd)))
+        return dl::fail(DL_E_ALIGN, "%s: x, its stride and the weight planes must be 16-byte aligned", name);
     const char *xb = reinterpret_cast<const char *>(x), *yb = reinterpret_cast<const char *>(y);
-    const char *xe = xb + ((size_t)(rows - 1) * x_stride + W->n_in) * 4;
-    const char *ye = yb + ((size_t)(rows - 1) * y_stride + W->n_out) * 4;
-    if (xb < ye && yb < xe) return dl::fail(DL_E_ARG, "dl_gemv_q8: y overlaps x");
+    const char *xe = xb + ((size_t)(rows - 1) * x_stride + n_in) * 4;
+    const char *ye = yb + ((size_t)(rows - 1) * y_stride + n_out) * 4;
+    if (xb < ye && yb < xe) return dl::fail(DL_E_ARG, "%s: y overlaps x", name);
     int sm = 0;
-    rc = dl::device_sm_count(&sm);
+    int rc = dl::device_sm_count(&sm);
     if (rc != DL_OK) return rc;
 
     GemvArgs a{};
-    a.qs = static_cast<const unsigned char *>(W->qs);
-    a.d = static_cast<const unsigned char *>(W->d);
+    a.qs = static_cast<const unsigned char *>(wq);
+    a.d = static_cast<const unsigned char *>(wd);
     a.x_stride = x_stride;
     a.y_stride = y_stride;
-    a.n_out = (int)W->n_out;
-    a.n_in = (int)W->n_in;
-    a.KT = (int)(dl::ceil_div(W->n_in, 128) * 4);
-    a.RT = (int)dl::ceil_div(W->n_out, 16);
+    a.n_out = (int)n_out;
+    a.n_in = (int)n_in;
+    a.KT = (int)(dl::ceil_div(n_in, 128) * 4);
+    a.RT = (int)dl::ceil_div(n_out, 16);
 
     int sizes[64];
     int done = 0;
@@ -804,12 +862,59 @@ int gemv_impl(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
         for (int gi = 0; gi < ng; ++gi) {
             a.x = x + (size_t)done * x_stride;
             a.y = y + (size_t)done * y_stride;
-            rc = gemv_group(a, sizes[gi], sm, path, static_cast<cudaStream_t>(stream));
+            rc = gemv_group(a, w16, sizes[gi], sm, path, static_cast<cudaStream_t>(stream));
             if (rc != DL_OK) return rc;
             done += sizes[gi];
         }
     }
     return DL_OK;
+}
+
+int gemv_impl(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride, float *y, int64_t y_stride,
+              int path, dl_stream_t stream)
+{
+    dl::clear_error();
+    if (!W || !W->qs || !W->d) return dl::fail(DL_E_ARG, "dl_gemv_q8: null pointer");
+    const int rc = dl_q8_packed_size(W->n_out, W->n_in, nullptr, nullptr);
+    if (rc != DL_OK) return rc;
+    return gemv_run("dl_gemv_q8", W->qs, W->d, W->n_out, W->n_in, false, x, rows, x_stride, y, y_stride, path,
+                    stream);
+}
+
+int gemv_f16w_impl(const dl_f16_weight *W, const float *x, int rows, int64_t x_stride, float *y,
+                   int64_t y_stride, int path, dl_stream_t stream)
+{
+    dl::clear_error();
+    if (!W || !W->w) return dl::fail(DL_E_ARG, "dl_gemv_f16w: null pointer");
+    const int rc = dl_f16w_packed_size(W->n_out, W->n_in, nullptr);
+    if (rc != DL_OK) return rc;
+    return gemv_run("dl_gemv_f16w", W->w, nullptr, W->n_out, W->n_in, true, x, rows, x_stride, y, y_stride, path,
+                    stream);
+}
+
+// f16 weights [n_out][n_in] (row-major) to the tile form: one thread per 16 bytes, the half
+// `hf` of lane t's 32 bytes = words 4hf .. 4hf + 3; word m holds inputs kb, kb + 1
+// (kb = 16(p/2) + 8(p%2) + 2c, p = m/2) of row g + 8(m%2).  Out-of-range weights are zero.
+__global__ void f16w_pack_kernel(const uint16_t *w, int64_t n_out, int64_t n_in, int KT, int64_t units, uint4 *out)
+{
+    const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= units) return;
+    const int hf = (int)(u & 1), lane = (int)((u >> 1) & 31);
+    const int64_t t = u >> 6;
+    const int64_t kt = t % KT, rt = t / KT;
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t word[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int m = 4 * hf + e, p = m >> 1;
+        const int64_t o = rt * 16 + g + 8 * (m & 1);
+        const int64_t k = kt * 32 + (p >> 1) * 16 + (p & 1) * 8 + 2 * c;
+        uint32_t lo = 0u, hi = 0u;
+        if (o < n_out && k < n_in) lo = w[o * n_in + k];
+        if (o < n_out && k + 1 < n_in) hi = w[o * n_in + k + 1];
+        word[e] = lo | (hi << 16);
+    }
+    out[u] = make_uint4(word[0], word[1], word[2], word[3]);
 }
 
 }  // namespace
@@ -859,6 +964,45 @@ int dl_gemv_q8_ex(const dl_q8_weight *W, const float *x, int rows, int64_t x_str
                   float *y, int64_t y_stride, int path, dl_stream_t stream)
 {
     return gemv_impl(W, x, rows, x_stride, y, y_stride, path, stream);
+}
+
+int dl_f16w_packed_size(int64_t n_out, int64_t n_in, size_t *bytes)
+{
+    if (n_out <= 0 || n_in <= 0 || n_in % 32 != 0)
+        return dl::fail(DL_E_SHAPE, "dl_f16w_packed_size: n_out=%lld n_in=%lld (n_in must be a positive multiple of 32)",
+                        (long long)n_out, (long long)n_in);
+    if (n_out > (1LL << 30) || n_in > (1LL << 24))
+        return dl::fail(DL_E_SHAPE, "dl_f16w_packed_size: matrix too large");
+    const int64_t RT = dl::ceil_div(n_out, 16), KT = dl::ceil_div(n_in, 128) * 4;
+    if (bytes) *bytes = (size_t)(RT * KT * 1024);
+    return DL_OK;
+}
+
+int dl_f16w_pack(const uint16_t *w, int64_t n_out, int64_t n_in, void *packed, dl_stream_t stream)
+{
+    dl::clear_error();
+    size_t bytes = 0;
+    const int rc = dl_f16w_packed_size(n_out, n_in, &bytes);
+    if (rc != DL_OK) return rc;
+    if (!w || !packed) return dl::fail(DL_E_ARG, "dl_f16w_pack: null pointer");
+    if (!dl::aligned16(packed)) return dl::fail(DL_E_ALIGN, "dl_f16w_pack: the packed plane must be 16-byte aligned");
+    const int KT = (int)(dl::ceil_div(n_in, 128) * 4);
+    const int64_t units = (int64_t)(bytes / 16);
+    f16w_pack_kernel<<<(unsigned)dl::ceil_div(units, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        w, n_out, n_in, KT, units, static_cast<uint4 *>(packed));
+    return dl::check_launch("dl_f16w_pack");
+}
+
+int dl_gemv_f16w(const dl_f16_weight *W, const float *x, int rows, int64_t x_stride,
+                 float *y, int64_t y_stride, dl_stream_t stream)
+{
+    return gemv_f16w_impl(W, x, rows, x_stride, y, y_stride, PATH_AUTO, stream);
+}
+
+int dl_gemv_f16w_ex(const dl_f16_weight *W, const float *x, int rows, int64_t x_stride,
+                    float *y, int64_t y_stride, int path, dl_stream_t stream)
+{
+    return gemv_f16w_impl(W, x, rows, x_stride, y, y_stride, path, stream);
 }
 
 }  // extern "C"

@@ -54,6 +54,17 @@ def test_packed_sizes_match_q8_bytes(dl):
     assert qb == 3 * 4 * 512 and db == 3 * 4 * 32
 
 
+def test_f16w_packed_sizes(dl):
+    """The f16 device plane is the matrix's f16 bytes on full tiles, padded to whole tiles else;
+    widths that are not a multiple of 32 are refused."""
+    for n_out, n_in in ((5120, 3072), (16384, 3072), (3072, 8192)):
+        assert dl.dl_f16w_packed_size(n_out, n_in) == n_out * n_in * 2
+    assert dl.dl_f16w_packed_size(37, 96) == 3 * 4 * 1024
+    with pytest.raises(dl.DLError) as e:
+        dl.dl_f16w_packed_size(16, 48)
+    assert e.value.code == dl.DL_E_SHAPE
+
+
 def test_grouping_matches_oracle_and_golden(dl):
     for n in range(0, 70):
         assert dl.dl_plan_groups(n) == (oracle.plan_groups(n) if n else [])
