@@ -337,6 +337,31 @@ int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv,
                       int32_t *status, int path, dl_stream_t stream);
 
 /*
+ * Split-KV decode attention with the rope and KV store fused in: one launch does
+ * what dl_rope_kv_store followed by dl_decode_attn_ex do, for a command whose
+ * rows carry their new token [ROPE][SPL].  The bias (optional, laid out as for
+ * dl_rope_kv_store) is added first; every work item rotates its queries in
+ * shared memory (q itself is only read, never rotated in place); the work item
+ * whose keys hold pos[r] (the last one, for a position past every row's keys)
+ * rotates k, clamps k and v into +-65504, stores both as f16 (round to nearest
+ * even) in slot pos[r] of region plan->row_region[r], and reads them back from
+ * the mirror after its own stores.  The stored halves, the queries and the
+ * results equal those of the two separate calls.
+ *   q        device f32, row r at q + r*q_stride: n_q heads as projected (unrotated)
+ *   k, v     device f32 rows, n_kv heads each; k_stride, v_stride >= n_kv*head_dim
+ *   bias     device f32 [(n_q + 2*n_kv) * head_dim] or NULL
+ *   pos      device int32 [rows]: the new token's slot; a row whose pos is outside
+ *            the cache or the table is not stored and DL_STATUS_POS_RANGE is set
+ *   rope     rotary table (16-byte aligned) and pairing (rot_dim even, <= head_dim)
+ * The other arguments, the path and the error codes are those of dl_decode_attn_ex.
+ */
+int dl_decode_attn_rope(const float *q, int64_t q_stride, const float *k, int64_t k_stride,
+                        const float *v, int64_t v_stride, const float *bias, const int32_t *pos,
+                        const dl_rope *rope, const dl_kv_cache *kv, const int32_t *seqlen,
+                        const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
+                        int32_t *status, int path, dl_stream_t stream);
+
+/*
  * Log-sum-exp merge of the pieces of every (row, head):
  *   M = max_p lse_p, w_p = exp(lse_p - M), out = sum w_p o_p / sum w_p,
  *   LSE = M + ln sum w_p  (natural log of the scaled scores' exp-sum).

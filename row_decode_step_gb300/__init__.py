@@ -106,6 +106,7 @@ def lib() -> ctypes.CDLL:
             "dl_attn_plan_build": ([I, P, P, I, I, I, I, I, P], I),
             "dl_decode_attn": ([P, I64, P, P, P, P, SZ, P, P], I),
             "dl_decode_attn_ex": ([P, I64, P, P, P, P, SZ, P, I, P], I),
+            "dl_decode_attn_rope": ([P, I64, P, I64, P, I64, P, P, P, P, P, P, P, SZ, P, I, P], I),
             "dl_attn_merge": ([P, P, P, P, I64, P, P], I),
             "dl_decode_attention_noalloc_max_bytes": ([], SZ),
             "dl_decode_attention_noalloc": ([P, I64, P, P, P, P, I64, P, P, P], I),
@@ -344,6 +345,28 @@ def dl_decode_attn(q: torch.Tensor, kv: KVCache, seqlen: torch.Tensor, plan: dl_
         _check(lib().dl_decode_attn_ex(_ptr(q), q.stride(0), ctypes.byref(kv.c), _ptr(seqlen),
                                        ctypes.byref(plan), _ptr(workspace), workspace.numel(), _ptr(status),
                                        path, _stream(stream)))
+
+
+def dl_decode_attn_rope(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos: torch.Tensor, rope: "Rope",
+                        kv: KVCache, seqlen: torch.Tensor, plan: dl_attn_plan, workspace: torch.Tensor,
+                        bias: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                        stream=None, path: int = ATTN_PATH_AUTO) -> None:
+    """dl_rope_kv_store followed by dl_decode_attn_ex in one launch; q stays as projected."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev(t, torch.float32, n)
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("%s must be 2-D rows with unit inner stride" % n)
+    _dev(pos, torch.int32, "pos")
+    _dev(seqlen, torch.int32, "seqlen")
+    _dev(workspace, torch.uint8, "workspace")
+    if bias is not None:
+        _dev(bias, torch.float32, "bias")
+    if status is not None:
+        _dev(status, torch.int32, "status")
+    _check(lib().dl_decode_attn_rope(_ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(v), v.stride(0),
+                                     _ptr(bias), _ptr(pos), ctypes.byref(rope.c), ctypes.byref(kv.c),
+                                     _ptr(seqlen), ctypes.byref(plan), _ptr(workspace), workspace.numel(),
+                                     _ptr(status), path, _stream(stream)))
 
 
 def dl_attn_merge(workspace: torch.Tensor, plan: dl_attn_plan, seqlen: torch.Tensor,

@@ -39,7 +39,37 @@ struct AttnArgs {
     int32_t *status;
     float qscale;        // log2(e) / sqrt(D)
     dl_attn_plan plan;
+    // rope and KV store fused into the launch (fused = 1): q holds the rows as projected, every
+    // work item rotates its queries, and the item whose keys hold a row's position stores that
+    // row's rotated k and its v into the mirror before reading them
+    int fused;
+    const float *k_new, *v_new, *bias;
+    int64_t k_stride, v_stride;
+    const int32_t *pos;
+    const float2 *cs;    // [max_pos][rot/2] (cos, sin)
+    uint16_t *kc_w, *vc_w;
+    int rot, neox, max_pos;
 };
+
+__device__ __forceinline__ unsigned short attn_half_clamped(float v)
+{
+    v = fminf(fmaxf(v, -65504.0f), 65504.0f);
+    return __half_as_ushort(__float2half_rn(v));
+}
+
+// Channels (i0, i1) of rotary pair j (pairs past rot/2 pass through two at a time).
+__device__ __forceinline__ bool rope_pair(int j, int rot, int neox, int &i0, int &i1)
+{
+    const int rh = rot >> 1;
+    if (j < rh) {
+        i0 = neox ? j : 2 * j;
+        i1 = neox ? j + rh : 2 * j + 1;
+        return true;
+    }
+    i0 = rot + 2 * (j - rh);
+    i1 = i0 + 1;
+    return false;
+}
 
 __device__ __forceinline__ float warp_max(float v)
 {
@@ -137,7 +167,8 @@ size_t attn_mma_smem_bytes(int D)
     const size_t stage = (size_t)2 * kStKeys * D * 2;                    // K and V of 32 keys
     const size_t qf = (size_t)2 * (D / 16) * 32 * 32;                    // query fragments, 2 tiles
     const size_t qr = (size_t)kMaxQ * D * 4;                             // the queries as they arrive
-    return 1024 + (size_t)mma_stages(D) * stage + qf + qr;              // + alignment slack
+    const size_t cs = (size_t)DL_MAX_ROWS * (D / 2) * 8;                 // rotary rows (fused form)
+    return 1024 + (size_t)mma_stages(D) * stage + qf + qr + cs;         // + alignment slack
 }
 
 // OR of `flag` over the consumer warps (uniform result).
@@ -163,8 +194,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     const dl_attn_plan &P = a.plan;
 
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t full[kMmaMaxStages], empty[kMmaMaxStages], qbar;
-    __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS];
+    __shared__ __align__(8) uint64_t full[kMmaMaxStages], empty[kMmaMaxStages], qbar, csbar;
+    __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS], s_pos[DL_MAX_ROWS];
     __shared__ unsigned char s_qrow[kMaxQ], s_qhead[kMaxQ];   // query -> (session row, head in group)
     // the swizzled boxes want 1024-byte aligned destinations
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -194,6 +225,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             dla::mbar_init(&empty[i], (uint32_t)NT);   // released by the warps of one stage group
         }
         dla::mbar_init(&qbar, 1);                       // the session's queries have arrived
+        dla::mbar_init(&csbar, 1);                      // the rows' rotary table rows have arrived (fused)
         dla::mbar_init_fence();
     }
     // the key counts come from the caller, not from the previous kernel: read them now
@@ -201,6 +233,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         const int r = P.sess_rows[rb + tid];
         s_row[tid] = r;
         s_len[tid] = clip_len(a.seqlen[r], P.row_keys_max[r], a.capacity, a.status, piece == 0 && h == 0);
+        s_pos[tid] = a.fused ? a.pos[r] : 0;            // a caller input as well
     }
     if (tid < Q) {
         s_qrow[tid] = (unsigned char)(tid / G);
@@ -221,6 +254,14 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     unsigned char *ring = smem;
     unsigned char *qfrag = smem + (size_t)S * kStageBytes;
     float *qraw = reinterpret_cast<float *>(qfrag + (size_t)2 * (D / 16) * 32 * 32);   // [Q][D] as stored
+    float2 *s_cs = reinterpret_cast<float2 *>(qraw + (size_t)kMaxQ * D);              // [rows][rot/2] (fused)
+    // the fused form copies each row's table row (rot/2 (cos, sin) pairs) into shared memory when
+    // it is a whole number of 16-byte units; otherwise the rotations read the table in place
+    const int rh = a.rot >> 1;
+    const bool cs_staged = a.fused && (rh % 2) == 0 && rh > 0;
+    auto cs_at = [&](int i, int p, int jp) -> float2 {
+        return cs_staged ? s_cs[i * rh + jp] : a.cs[(size_t)p * rh + jp];
+    };
     const uint32_t ring_s = dla::smem_u32(ring);
     bool bad = false;
 
@@ -231,51 +272,113 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             dla::bulk_g2s(qraw + r * G * D, a.q + (int64_t)s_row[r] * a.q_stride + (int64_t)h * G * D,
                           (uint32_t)(G * D * 4), &qbar);
     };
+    // fused form: this piece stores the new rows whose positions fall in its keys (a position past
+    // every piece goes to the last one); every thread of the CTA a share of the (row, channel pair)
+    // elements, each fencing its writes so that the copies issued after the CTA barrier that
+    // follows read them
+    auto store_new_rows = [&]() {
+        const int owner_last = (lmax - 1) / P.chunk;
+        const int hp = D / 2;
+        if (cs_staged && !dla::mbar_wait(&csbar, 0u)) bad = true;
+        if (!bad) {
+#pragma unroll 4
+            for (int e = tid; e < nrows * hp; e += kMmaThreads) {
+                const int i = e / hp, jp = e - i * hp;
+                const int p = s_pos[i];
+                if (min(max(p, 0) / P.chunk, owner_last) != piece) continue;
+                if (p < 0 || p >= a.capacity || p >= a.max_pos) {
+                    if (jp == 0) dl_status_or(a.status, DL_STATUS_POS_RANGE);
+                    continue;
+                }
+                const int r = s_row[i];
+                const float *kr = a.k_new + (int64_t)r * a.k_stride + (int64_t)h * D;
+                const float *vr = a.v_new + (int64_t)r * a.v_stride + (int64_t)h * D;
+                int i0, i1;
+                const bool rotate = rope_pair(jp, a.rot, a.neox, i0, i1);
+                float k0 = kr[i0], k1 = kr[i1], v0 = vr[i0], v1 = vr[i1];
+                if (a.bias) {
+                    const float *bk = a.bias + (int64_t)(P.n_q + h) * D;
+                    const float *bv = a.bias + (int64_t)(P.n_q + P.n_kv + h) * D;
+                    k0 += bk[i0];
+                    k1 += bk[i1];
+                    v0 += bv[i0];
+                    v1 += bv[i1];
+                }
+                if (rotate) {
+                    const float2 t = cs_at(i, p, jp);
+                    const float y0 = fmaf(k0, t.x, -k1 * t.y);
+                    const float y1 = fmaf(k0, t.y, k1 * t.x);
+                    k0 = y0;
+                    k1 = y1;
+                }
+                const int64_t base = (int64_t)reg * a.region_stride + ((int64_t)h * a.capacity + p) * D;
+                a.kc_w[base + i0] = attn_half_clamped(k0);
+                a.kc_w[base + i1] = attn_half_clamped(k1);
+                a.vc_w[base + i0] = attn_half_clamped(v0);
+                a.vc_w[base + i1] = attn_half_clamped(v1);
+            }
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    };
     if (producer) {
+        // keys below the lowest slot this command writes are final before the previous kernel ends:
+        // the first few such stages are requested before waiting on it; after the wait come the
+        // session's queries (one bulk copy per row: the G heads of this KV head are contiguous),
+        // then the rest of the ring, so that those latency-critical lines go first
+        const int stable = lmin - 1;
+        const int nstable = k1 <= stable ? nst : max(0, (stable - k0) / kStKeys);
+        const int npre = min(min(nstable, kAttnPreWaitStages), nst);
+        auto issue_stage = [&](int i) {
+            const int st = i % S;
+            unsigned char *kd = ring + (size_t)st * kStageBytes;
+            unsigned char *vd = kd + kStageBytes / 2;
+            const int y = h * a.capacity + k0 + i * kStKeys;
+            dla::mbar_expect_tx(&full[st], kStageBytes);
+#pragma unroll
+            for (int hf = 0; hf < NH; ++hf) {
+                dla::tma_g2s_3d(kd + hf * kHalfTile, &tk, hf * 64, y, reg, &full[st]);
+                dla::tma_g2s_3d(vd + hf * kHalfTile, &tv, hf * 64, y, reg, &full[st]);
+            }
+        };
         if (lane == 0) {
             dla::prefetch_tmap(&tk);
             dla::prefetch_tmap(&tv);
-            // keys below the lowest slot this command writes are final before the previous kernel ends:
-            // the first few such stages are requested before waiting on it; after the wait come the
-            // session's queries (one bulk copy per row: the G heads of this KV head are contiguous),
-            // then the rest of the ring, so that those latency-critical lines go first
-            const int stable = lmin - 1;
-            const int nstable = k1 <= stable ? nst : max(0, (stable - k0) / kStKeys);
-            const int npre = min(nstable, kAttnPreWaitStages);
-            bool waited = false;
-            int i = 0;
+            if (cs_staged) {
+                // the rows' table rows (a caller input, not the previous kernel's): one bulk copy
+                // each; a row whose position is outside the table gets none (and no rotation)
+                uint32_t bytes = 0;
+                for (int i = 0; i < nrows; ++i)
+                    if (s_pos[i] >= 0 && s_pos[i] < a.max_pos) bytes += (uint32_t)rh * 8u;
+                dla::mbar_expect_tx(&csbar, bytes);
+                for (int i = 0; i < nrows; ++i)
+                    if (s_pos[i] >= 0 && s_pos[i] < a.max_pos)
+                        dla::bulk_g2s(s_cs + i * rh, a.cs + (size_t)s_pos[i] * rh, (uint32_t)rh * 8u, &csbar);
+            }
+            for (int i = 0; i < npre; ++i) issue_stage(i);      // npre <= S: every slot is free
+        }
+        dl_pdl_wait();
+        if (lane == 0) issue_queries();
+        if (a.fused) {
+            store_new_rows();
+            dla::named_sync(2, kMmaThreads);                 // every new row is stored and fenced
+        }
+        if (lane == 0) {
+            int i = npre;
             for (; i < nst; ++i) {
                 const int st = i % S;
                 if (i >= S && !dla::mbar_wait(&empty[st], (uint32_t)(((i / S) - 1) & 1))) {
                     bad = true;
                     break;
                 }
-                if (!waited && i >= npre) {
-                    dl_pdl_wait();
-                    waited = true;
-                    issue_queries();
-                }
-                unsigned char *kd = ring + (size_t)st * kStageBytes;
-                unsigned char *vd = kd + kStageBytes / 2;
-                const int y = h * a.capacity + k0 + i * kStKeys;
-                dla::mbar_expect_tx(&full[st], kStageBytes);
-#pragma unroll
-                for (int hf = 0; hf < NH; ++hf) {
-                    dla::tma_g2s_3d(kd + hf * kHalfTile, &tk, hf * 64, y, reg, &full[st]);
-                    dla::tma_g2s_3d(vd + hf * kHalfTile, &tv, hf * 64, y, reg, &full[st]);
-                }
-            }
-            if (!waited) {
-                dl_pdl_wait();
-                issue_queries();
+                issue_stage(i);
             }
             if (bad) {
-                // leave no copy in flight: wait (bounded) for the queries and the stages issued last
+                // leave no copy in flight: wait (bounded) for the queries, the table rows and the
+                // stages issued last
                 dla::mbar_wait(&qbar, 0u);
+                if (cs_staged) dla::mbar_wait(&csbar, 0u);
                 for (int j = max(0, i - S); j < i; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
             }
-        } else {
-            dl_pdl_wait();
         }
         dl_pdl_launch_dependents();
         return;
@@ -283,6 +386,10 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
 
     dl_pdl_wait();
     dl_pdl_launch_dependents();
+    if (a.fused) {
+        store_new_rows();
+        dla::named_sync(2, kMmaThreads);
+    }
 
     const int mt = warp % MT, grp = warp / MT;
     const int ms = P.max_splits;
@@ -297,6 +404,39 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             if (d == 0) a.part_lse[pidx] = __int_as_float(0x7fc00000);
         }
     };
+    // fused form: rotate the session's queries in shared memory (bias first), every consumer
+    // thread a share of the (query, channel pair) elements, before any of them is read
+    auto rotate_queries = [&](bool qok) {
+        if (a.fused && qok && cs_staged && !__all_sync(0xffffffffu, dla::mbar_wait(&csbar, 0u))) {
+            qok = false;
+            bad = true;
+        }
+        if (a.fused && qok) {
+            for (int e = tid; e < Q * (D / 2); e += kMmaConsumers * 32) {
+                const int qi = e / (D / 2), jp = e - qi * (D / 2);
+                const int ri = s_qrow[qi], head = h * G + s_qhead[qi];
+                const int p = s_pos[ri];
+                int i0, i1;
+                const bool rotate = rope_pair(jp, a.rot, a.neox, i0, i1);
+                float *qv = qraw + qi * D;
+                float x0 = qv[i0], x1 = qv[i1];
+                if (a.bias) {
+                    x0 += a.bias[(int64_t)head * D + i0];
+                    x1 += a.bias[(int64_t)head * D + i1];
+                }
+                if (rotate && p >= 0 && p < a.max_pos) {
+                    const float2 t = cs_at(ri, p, jp);
+                    const float y0 = fmaf(x0, t.x, -x1 * t.y);
+                    const float y1 = fmaf(x0, t.y, x1 * t.x);
+                    x0 = y0;
+                    x1 = y1;
+                }
+                qv[i0] = x0;
+                qv[i1] = x1;
+            }
+        }
+        if (a.fused) dla::named_sync(1, kMmaConsumers * 32);
+    };
     // combine area (the ring, idle once every stage is consumed): [4 warps][16 rows][CP], m, l
     constexpr int CP = D + 8;                          // padded row: the fragment stores spread over banks
     float *co = reinterpret_cast<float *>(smem);
@@ -307,6 +447,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         // [query tile][k-step][hi, lo][lane] 16 bytes = a0..a3
         const bool qok = __all_sync(0xffffffffu, dla::mbar_wait(&qbar, 0u));
         if (!qok) bad = true;
+        rotate_queries(qok);
         for (int fi = tid; fi < MT * NKS * 32; fi += kMmaConsumers * 32) {
             const int t = fi & 31, ks = (fi >> 5) % NKS, qt = (fi >> 5) / NKS;
             const int gg = t >> 2, cc = t & 3;
@@ -486,6 +627,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         const float *qs = qraw;                      // [Q][D] f32 as stored; the scale goes on the score
         float *pb = reinterpret_cast<float *>(qfrag) + warp * QM * kStKeys;   // this warp's probabilities
         if (!__all_sync(0xffffffffu, dla::mbar_wait(&qbar, 0u))) bad = true;
+        rotate_queries(!bad);
         int lenq[QM];
 #pragma unroll
         for (int q = 0; q < QM; ++q) lenq[q] = q < nq ? s_len[s_qrow[qb + q]] : 0;
@@ -911,9 +1053,17 @@ int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *regi
     return DL_OK;
 }
 
+// The new rows of the fused form: raw k and v rows, optional bias, positions and the rope table.
+struct FusedIn {
+    const float *k, *v, *bias;
+    int64_t k_stride, v_stride;
+    const int32_t *pos;
+    const dl_rope *rope;
+};
+
 static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
                             const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
-                            int32_t *status, int path, dl_stream_t stream)
+                            int32_t *status, int path, dl_stream_t stream, const FusedIn *f = nullptr)
 {
     dl::clear_error();
     if (!q || !kv || !kv->k || !kv->v || !seqlen || !workspace) return dl::fail(DL_E_ARG, "dl_decode_attn: null pointer");
@@ -950,6 +1100,30 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     a.status = status;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)plan->head_dim));
     a.plan = *plan;
+    if (f) {
+        const int D = plan->head_dim;
+        if (!f->k || !f->v || !f->pos || !f->rope || !f->rope->cos_sin)
+            return dl::fail(DL_E_ARG, "dl_decode_attn_rope: null pointer");
+        if (f->rope->rot_dim < 0 || f->rope->rot_dim % 2 != 0 || f->rope->rot_dim > D || f->rope->max_pos <= 0)
+            return dl::fail(DL_E_SHAPE, "dl_decode_attn_rope: rot_dim=%d head_dim=%d", f->rope->rot_dim, D);
+        if (f->k_stride < (int64_t)plan->n_kv * D || f->v_stride < (int64_t)plan->n_kv * D)
+            return dl::fail(DL_E_ARG, "dl_decode_attn_rope: k/v strides below the row widths");
+        if (!dl::aligned16(f->rope->cos_sin))
+            return dl::fail(DL_E_ALIGN, "dl_decode_attn_rope: the rotary table must be 16-byte aligned");
+        a.fused = 1;
+        a.k_new = f->k;
+        a.v_new = f->v;
+        a.bias = f->bias;
+        a.k_stride = f->k_stride;
+        a.v_stride = f->v_stride;
+        a.pos = f->pos;
+        a.cs = reinterpret_cast<const float2 *>(f->rope->cos_sin);
+        a.kc_w = kv->k;
+        a.vc_w = kv->v;
+        a.rot = f->rope->rot_dim;
+        a.neox = f->rope->neox ? 1 : 0;
+        a.max_pos = f->rope->max_pos;
+    }
     if (path < 0 || path > 2) return dl::fail(DL_E_ARG, "dl_decode_attn: path=%d", path);
     int qmax = 0;
     for (int si = 0; si < plan->n_sessions; ++si)
@@ -986,6 +1160,16 @@ int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv, c
                       int32_t *status, int path, dl_stream_t stream)
 {
     return decode_attn_impl(q, q_stride, kv, seqlen, plan, workspace, workspace_bytes, status, path, stream);
+}
+
+int dl_decode_attn_rope(const float *q, int64_t q_stride, const float *k, int64_t k_stride,
+                        const float *v, int64_t v_stride, const float *bias, const int32_t *pos,
+                        const dl_rope *rope, const dl_kv_cache *kv, const int32_t *seqlen,
+                        const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
+                        int32_t *status, int path, dl_stream_t stream)
+{
+    const FusedIn f{k, v, bias, k_stride, v_stride, pos, rope};
+    return decode_attn_impl(q, q_stride, kv, seqlen, plan, workspace, workspace_bytes, status, path, stream, &f);
 }
 
 int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t *seqlen,

@@ -26,7 +26,7 @@ def dl():
     return m
 
 
-def _step(dl, S, positions, regions, n_regions, capacity, label):
+def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=False):
     from row_decode_step_gb300.step import LayerStep, LayerWeights
     D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
     blocks = layer_blocks(S.name)
@@ -41,7 +41,7 @@ def _step(dl, S, positions, regions, n_regions, capacity, label):
     x = synth.normal_f32(0, label + "/x", (n, H))
     xf = synth.normal_f32(0, label + "/xf", (n, H)) if F else None
     h = synth.normal_f32(0, label + "/h", (n, F)) if F else None
-    step = LayerStep(positions, regions, n_q, n_kv, D, H, F, "cuda")
+    step = LayerStep(positions, regions, n_q, n_kv, D, H, F, "cuda", fused_rope=fused_rope)
     r0 = 0
     for c in step.commands:
         c.x.copy_(x[r0:r0 + c.n].cuda())
@@ -66,7 +66,9 @@ def _step(dl, S, positions, regions, n_regions, capacity, label):
         assert_gemv_close(c.qkv.cpu().numpy()[:, qd:], ref["qkv"][:, qd:])
         # roped q carries the GEMV's error through a rotation of channel pairs, which keeps each
         # pair's error norm: at most sqrt(2) times the GEMV bar per element
-        assert gemv_err(c.q.cpu().numpy(), ref["q"]) < 1e-3 * np.sqrt(2)
+        # (the fused launch rotates its queries in shared memory and leaves q as projected)
+        if not fused_rope:
+            assert gemv_err(c.q.cpu().numpy(), ref["q"]) < 1e-3 * np.sqrt(2)
         assert_attn_close(c.attn.cpu().numpy(), c.lse.cpu().numpy(), ref["attn"], ref["lse"])
         # the O projection's input differs by the attention error; allow that share on top of the bar
         assert gemv_err(c.y_o.cpu().numpy(), ref["y_o"]) < 1e-2
@@ -98,12 +100,15 @@ def test_step_1b(dl):
     _step(dl, synth.LLAMA_1B, [4096], [0], 1, 4097, "step/1b")
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("rows", [1, 8])
-def test_step_3b(dl, rows):
-    _step(dl, synth.LLAMA_3B, list(range(5120, 5120 + rows)), [0] * rows, 1, 5128, "step/3b%d" % rows)
+def test_step_3b(dl, rows, fused):
+    _step(dl, synth.LLAMA_3B, list(range(5120, 5120 + rows)), [0] * rows, 1, 5128, "step/3b%d" % rows,
+          fused_rope=fused)
 
 
-def test_step_twelve_streams(dl):
+@pytest.mark.parametrize("fused", [False, True])
+def test_step_twelve_streams(dl, fused):
     lens = synth.twelve_stream_lengths(0)
-    step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams")
+    step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams", fused_rope=fused)
     assert step.group_sizes == [6, 6]
