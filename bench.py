@@ -51,8 +51,9 @@ def parse_args():
                    help="inner product of the GEMVs: 0 library choice, 1 CUDA cores (<= 2 rows), 2 tensor cores")
     p.add_argument("--attn-path", type=int, default=0, choices=[0, 1, 2],
                    help="inner product of the attention: 0 library choice, 1 CUDA cores, 2 tensor cores")
-    p.add_argument("--fused-rope", type=int, default=0, choices=[0, 1],
-                   help="1: the rope/store runs inside the attention launch (dl_decode_attn_rope)")
+    p.add_argument("--fused-rope", type=int, default=1, choices=[0, 1],
+                   help="1: the rope/store runs inside the attention launch (dl_decode_attn_rope); "
+                        "0: separate dl_rope_kv_store and dl_decode_attn launches")
     return p.parse_args()
 
 
@@ -490,6 +491,16 @@ def run_ours(args):
             del r2
             torch.cuda.empty_cache()
     if not args.no_extras and args.workload == "3b-8":
+        # the same step with the rope/store as its own launch (the other form of the path)
+        r2 = measure(wl, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
+                     want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
+                     fused=not args.fused_rope)
+        extras["3b-8 rope %s" % ("separate" if args.fused_rope else "in attention")] = {
+            "layer_steps_per_s": 1e3 / r2["ms_per_step"], "ms_per_step": r2["ms_per_step"],
+            "algorithmic_gbs": sb / (r2["ms_per_step"] / 1e3) / 1e9,
+            "hbm_frac": sb / (r2["ms_per_step"] / 1e3) / 1e9 / peak, "status": r2["status"]}
+        del r2
+        torch.cuda.empty_cache()
         extras["f16w_gemv"] = measure_f16w(dev, peak)
         torch.cuda.empty_cache()
     cpu = None
