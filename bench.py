@@ -51,6 +51,8 @@ def parse_args():
                    help="inner product of the GEMVs: 0 library choice, 1 CUDA cores (<= 2 rows), 2 tensor cores")
     p.add_argument("--attn-path", type=int, default=0, choices=[0, 1, 2],
                    help="inner product of the attention: 0 library choice, 1 CUDA cores, 2 tensor cores")
+    p.add_argument("--cluster-merge", type=int, default=0, choices=[0, 1],
+                   help="1: the pieces of a KV head merge inside their thread-block cluster (no merge launch)")
     p.add_argument("--fused-rope", type=int, default=1, choices=[0, 1],
                    help="1: the rope/store runs inside the attention launch (dl_decode_attn_rope); "
                         "0: separate dl_rope_kv_store and dl_decode_attn launches")
@@ -219,7 +221,8 @@ def build_layers(wl, L, dev, seed=0):
     return layers, caches
 
 
-def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0), fused=False):
+def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0), fused=False,
+            cluster=False):
     import synth
     import torch
     import row_decode_step_gb300 as dl
@@ -228,7 +231,7 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
     layers, caches = build_layers(wl, L, dev)
     rope = dl.make_rope(S.rope_theta, S.head_dim, wl["capacity"], device=dev)
     step = LayerStep(wl["positions"], wl["regions"], S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, dev,
-                     gemv_path=paths[0], attn_path=paths[1], fused_rope=fused)
+                     gemv_path=paths[0], attn_path=paths[1], fused_rope=fused, cluster_merge=cluster)
     for i, c in enumerate(step.commands):
         c.x.copy_(synth.normal_f32(0, "bench/x%d" % i, tuple(c.x.shape), device=dev))
         if c.x_ffn is not None:
@@ -464,7 +467,7 @@ def run_ours(args):
 
     wl = workload(args.workload)
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path),
-                  fused=bool(args.fused_rope))
+                  fused=bool(args.fused_rope), cluster=bool(args.cluster_merge))
     steps = args.steps
     ms, value = combine_ranks(res["ms_total"], steps, world, dev)
     step = res["step"]
@@ -480,7 +483,7 @@ def run_ours(args):
             w2 = workload(name)
             r2 = measure(w2, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
                          want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
-                         fused=bool(args.fused_rope))
+                         fused=bool(args.fused_rope), cluster=bool(args.cluster_merge))
             sb2 = step_bytes(w2, r2["step"])
             extras[name] = {"rows": len(w2["positions"]), "layer_steps_per_s": 1e3 / r2["ms_per_step"],
                             "ms_per_step": r2["ms_per_step"],
@@ -521,7 +524,7 @@ def run_ours(args):
                    "attn_chunk": [c.plan.chunk for c in step.commands],
                    "attn_work_items": [c.plan.n_work for c in step.commands],
                    "gemv_path": args.gemv_path, "attn_path": args.attn_path,
-                   "rope_in_attention": bool(args.fused_rope)},
+                   "rope_in_attention": bool(args.fused_rope), "merge_in_cluster": bool(args.cluster_merge)},
         "tokens_per_s": rows * value,
         "step": {"algorithmic_bytes": sb, "algorithmic_gbs": step_gbs, "hbm_frac": step_gbs / peak,
                  "peak_gbs": peak, "peak_source": peak_src},

@@ -39,6 +39,9 @@
  *  [F16W] the same PR #4473, its description: every GPU home serves two weight
  *         lanes, q8 by default and f16 (halfword weights, f32 accumulate) as the
  *         reference lane.
+ *  [CLU]  TensorFold PR #926 "drama: the tower's one-row projections ...": a CTA
+ *         cluster shares a head, its CTAs exchanging their pieces' results over
+ *         distributed shared memory instead of a separate merge pass.
  *  [ROPE] daScript PR #4293 "dasLLAMA llama leg ...", commit "The decode
  *         rope-and-store rides one template on both homes" (GkRopeKvStore).
  *  [GRP]  the same PR, commit "The Vulkan batched step past eight rows runs in
@@ -285,6 +288,9 @@ typedef struct dl_attn_plan {
     int n_sessions;
     int n_work;                    /* work items (CTAs) of dl_decode_attn */
     int sm_count;                  /* SMs the plan was sized for */
+    int cluster;                   /* 0: pieces write partials for dl_attn_merge; C > 0: the C pieces
+                                      of every (session, KV head) form one thread-block cluster that
+                                      merges itself (dl_decode_attn_cluster) */
     int row_region[DL_MAX_ROWS];   /* region of each row */
     int row_keys_max[DL_MAX_ROWS]; /* planned key bound of each row (host seqlen) */
     int sess_rows[DL_MAX_ROWS];    /* rows sorted by session */
@@ -306,6 +312,18 @@ typedef struct dl_attn_plan {
 int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *region_host,
                        int n_q, int n_kv, int head_dim, int sm_count, int force_chunk,
                        dl_attn_plan *out);
+
+/*
+ * A plan for dl_decode_attn_cluster [SPL][CLU]: every (session, KV head) gets the
+ * same number C <= max_cluster (<= 16; 0 = 16) of pieces, sized like
+ * dl_attn_plan_build's (about two work items per SM, the longest session's keys
+ * split into C pieces of a multiple of 32 keys); sessions with fewer keys leave
+ * their last pieces empty.  No workspace is needed (workspace_bytes = 0).
+ * Host only (plus one device attribute query when sm_count == 0).
+ */
+int dl_attn_plan_build_cluster(int rows, const int32_t *seqlen_host, const int32_t *region_host,
+                               int n_q, int n_kv, int head_dim, int sm_count, int max_cluster,
+                               dl_attn_plan *out);
 
 /*
  * Split-KV decode attention [SPL].  For row r, query head h (KV head
@@ -360,6 +378,38 @@ int dl_decode_attn_rope(const float *q, int64_t q_stride, const float *k, int64_
                         const dl_rope *rope, const dl_kv_cache *kv, const int32_t *seqlen,
                         const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
                         int32_t *status, int path, dl_stream_t stream);
+
+/* The new rows of a command for the attention launches that store them: as dl_decode_attn_rope. */
+typedef struct dl_attn_rope_in {
+    const float *k;
+    int64_t k_stride;
+    const float *v;
+    int64_t v_stride;
+    const float *bias;             /* or NULL */
+    const int32_t *pos;            /* device int32 [rows] */
+    const dl_rope *rope;           /* table 16-byte aligned */
+} dl_attn_rope_in;
+
+/*
+ * Split-KV decode attention with the merge inside the launch [SPL][CLU]: the C
+ * pieces of a (session, KV head) (plan from dl_attn_plan_build_cluster) run as one
+ * thread-block cluster; each keeps its (o, lse) in shared memory, and after a
+ * cluster barrier every CTA merges a share of the group's outputs by reading its
+ * peers' pieces through distributed shared memory, with the arithmetic of
+ * dl_attn_merge (pieces holding none of a row's keys weigh nothing; a row with
+ * no keys gets out = 0, lse = -inf).  No partials reach global memory.
+ *   rope_in  NULL: q is already rotated and the new rows stored (dl_rope_kv_store);
+ *            else the rope and store happen in the launch, as in dl_decode_attn_rope
+ *   out      device f32, row r at out + r*out_stride, n_q*head_dim values
+ *   lse      device f32 [rows][n_q] or NULL
+ * Other arguments, the path and the error codes as dl_decode_attn_ex; a plan
+ * without clusters is refused (DL_E_ARG), as is a cluster plan handed to
+ * dl_decode_attn / dl_decode_attn_rope.
+ */
+int dl_decode_attn_cluster(const float *q, int64_t q_stride, const dl_attn_rope_in *rope_in,
+                           const dl_kv_cache *kv, const int32_t *seqlen, const dl_attn_plan *plan,
+                           float *out, int64_t out_stride, float *lse, int32_t *status, int path,
+                           dl_stream_t stream);
 
 /*
  * Log-sum-exp merge of the pieces of every (row, head):

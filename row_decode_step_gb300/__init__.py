@@ -69,6 +69,7 @@ class dl_attn_plan(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int), ("n_q", ctypes.c_int), ("n_kv", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("chunk", ctypes.c_int), ("max_splits", ctypes.c_int),
                 ("n_sessions", ctypes.c_int), ("n_work", ctypes.c_int), ("sm_count", ctypes.c_int),
+                ("cluster", ctypes.c_int),
                 ("row_region", ctypes.c_int * _R), ("row_keys_max", ctypes.c_int * _R),
                 ("sess_rows", ctypes.c_int * _R), ("sess_begin", ctypes.c_int * (_R + 1)),
                 ("sess_splits", ctypes.c_int * _R), ("sess_item0", ctypes.c_int * (_R + 1)),
@@ -107,6 +108,8 @@ def lib() -> ctypes.CDLL:
             "dl_decode_attn": ([P, I64, P, P, P, P, SZ, P, P], I),
             "dl_decode_attn_ex": ([P, I64, P, P, P, P, SZ, P, I, P], I),
             "dl_decode_attn_rope": ([P, I64, P, I64, P, I64, P, P, P, P, P, P, P, SZ, P, I, P], I),
+            "dl_attn_plan_build_cluster": ([I, P, P, I, I, I, I, I, P], I),
+            "dl_decode_attn_cluster": ([P, I64, P, P, P, P, P, I64, P, P, I, P], I),
             "dl_attn_merge": ([P, P, P, P, I64, P, P], I),
             "dl_decode_attention_noalloc_max_bytes": ([], SZ),
             "dl_decode_attention_noalloc": ([P, I64, P, P, P, P, I64, P, P, P], I),
@@ -367,6 +370,51 @@ def dl_decode_attn_rope(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos: 
                                      _ptr(bias), _ptr(pos), ctypes.byref(rope.c), ctypes.byref(kv.c),
                                      _ptr(seqlen), ctypes.byref(plan), _ptr(workspace), workspace.numel(),
                                      _ptr(status), path, _stream(stream)))
+
+
+class dl_attn_rope_in(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("k_stride", ctypes.c_int64), ("v", ctypes.c_void_p),
+                ("v_stride", ctypes.c_int64), ("bias", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("rope", ctypes.c_void_p)]
+
+
+def dl_attn_plan_build_cluster(seqlen: Sequence[int], n_q: int, n_kv: int, head_dim: int,
+                               regions: Optional[Sequence[int]] = None, sm_count: int = 0,
+                               max_cluster: int = 0) -> dl_attn_plan:
+    rows = len(seqlen)
+    sl = (ctypes.c_int32 * rows)(*[int(s) for s in seqlen])
+    rg = None if regions is None else (ctypes.c_int32 * rows)(*[int(r) for r in regions])
+    plan = dl_attn_plan()
+    _check(lib().dl_attn_plan_build_cluster(rows, sl, rg, n_q, n_kv, head_dim, sm_count, max_cluster,
+                                            ctypes.byref(plan)))
+    return plan
+
+
+def dl_decode_attn_cluster(q: torch.Tensor, kv: KVCache, seqlen: torch.Tensor, plan: dl_attn_plan,
+                           out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                           k: Optional[torch.Tensor] = None, v: Optional[torch.Tensor] = None,
+                           pos: Optional[torch.Tensor] = None, rope: Optional["Rope"] = None,
+                           bias: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                           stream=None, path: int = ATTN_PATH_AUTO) -> None:
+    """Attention with the merge inside the launch (a plan from dl_attn_plan_build_cluster); with
+    k, v, pos and rope given, the rope and store happen in the launch too."""
+    _dev(q, torch.float32, "q")
+    _dev(seqlen, torch.int32, "seqlen")
+    _dev(out, torch.float32, "out")
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+    rin = None
+    if k is not None:
+        for t, n in ((k, "k"), (v, "v")):
+            _dev(t, torch.float32, n)
+        _dev(pos, torch.int32, "pos")
+        if bias is not None:
+            _dev(bias, torch.float32, "bias")
+        rin = dl_attn_rope_in(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(bias), _ptr(pos),
+                              ctypes.cast(ctypes.pointer(rope.c), ctypes.c_void_p))
+    _check(lib().dl_decode_attn_cluster(_ptr(q), q.stride(0), None if rin is None else ctypes.byref(rin),
+                                        ctypes.byref(kv.c), _ptr(seqlen), ctypes.byref(plan), _ptr(out),
+                                        out.stride(0), _ptr(lse), _ptr(status), path, _stream(stream)))
 
 
 def dl_attn_merge(workspace: torch.Tensor, plan: dl_attn_plan, seqlen: torch.Tensor,

@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kTile = 32;          // keys per tile
 constexpr int kMaxQ = 32;          // queries one work item serves (session rows x group)
+constexpr int kMaxCluster = 16;    // pieces of a (session, KV head) merged inside one cluster
 constexpr int kCudaCoreMaxQ = 4;   // queries per work item up to which the CUDA-core form is used
 
 struct AttnArgs {
@@ -49,6 +50,9 @@ struct AttnArgs {
     const float2 *cs;    // [max_pos][rot/2] (cos, sin)
     uint16_t *kc_w, *vc_w;
     int rot, neox, max_pos;
+    // merge inside the launch (plan.cluster = C > 0): the results go straight to out / lse_out
+    float *out, *lse_out;
+    int64_t out_stride;
 };
 
 __device__ __forceinline__ unsigned short attn_half_clamped(float v)
@@ -197,6 +201,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     __shared__ __align__(8) uint64_t full[kMmaMaxStages], empty[kMmaMaxStages], qbar, csbar;
     __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS], s_pos[DL_MAX_ROWS];
     __shared__ unsigned char s_qrow[kMaxQ], s_qhead[kMaxQ];   // query -> (session row, head in group)
+    __shared__ float s_plse[kMaxQ], s_mM[kMaxQ], s_mW[kMaxQ];   // cluster merge: this piece's lse, weights
     // the swizzled boxes want 1024-byte aligned destinations
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~static_cast<uintptr_t>(1023));
@@ -247,8 +252,10 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     }
     const int k0 = piece * P.chunk;
     const int k1 = min(k0 + P.chunk, lmax);
-    if (k0 >= k1) return;                       // nothing of this piece is attended (no barrier pending)
-    const int nst = (k1 - k0 + kStKeys - 1) / kStKeys;
+    const bool idle = k0 >= k1;                 // nothing of this piece is attended
+    // (no barrier pending; with a cluster merge the CTA stays to merge its share of the group)
+    if (idle && !P.cluster) return;
+    const int nst = idle ? 0 : (k1 - k0 + kStKeys - 1) / kStKeys;
 
     const int reg = P.row_region[s_row[0]];
     unsigned char *ring = smem;
@@ -320,6 +327,15 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         }
         asm volatile("fence.proxy.async.global;" ::: "memory");
     };
+    if (producer && idle) {
+        dl_pdl_wait();
+        dl_pdl_launch_dependents();
+        if (P.cluster) {                                 // the group's two cluster barriers
+            dla::cluster_sync_all();
+            dla::cluster_sync_relaxed();
+        }
+        return;
+    }
     if (producer) {
         // keys below the lowest slot this command writes are final before the previous kernel ends:
         // the first few such stages are requested before waiting on it; after the wait come the
@@ -358,7 +374,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         }
         dl_pdl_wait();
         if (lane == 0) issue_queries();
-        if (a.fused) {
+        if (a.fused) {                                       // (an idle piece returned above)
             store_new_rows();
             dla::named_sync(2, kMmaThreads);                 // every new row is stored and fenced
         }
@@ -381,12 +397,17 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             }
         }
         dl_pdl_launch_dependents();
+        __syncwarp();
+        if (P.cluster) {                                 // the group's two cluster barriers
+            dla::cluster_sync_all();
+            dla::cluster_sync_relaxed();
+        }
         return;
     }
 
     dl_pdl_wait();
     dl_pdl_launch_dependents();
-    if (a.fused) {
+    if (a.fused && !idle) {
         store_new_rows();
         dla::named_sync(2, kMmaThreads);
     }
@@ -399,11 +420,67 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             const int qi = e / D, d = e - qi * D;
             const int rq = s_qrow[qi], gq = s_qhead[qi];
             if (s_len[rq] <= k0) continue;
+            if (P.cluster) {
+                qraw[qi * D + d] = __int_as_float(0x7fc00000);
+                if (d == 0) s_plse[qi] = __int_as_float(0x7fc00000);
+                continue;
+            }
             const int64_t pidx = ((int64_t)s_row[rq] * P.n_q + h * G + gq) * ms + piece;
             a.part_o[pidx * D + d] = __int_as_float(0x7fc00000);
             if (d == 0) a.part_lse[pidx] = __int_as_float(0x7fc00000);
         }
     };
+    // cluster merge: every piece of the group holds (o, lse) of the rows it covers in its shared
+    // memory (o in the query area, lse in s_plse); after the release/acquire cluster barrier each
+    // CTA (rank = piece) merges the queries' weights over the pieces that hold keys of their row,
+    // then writes every C-th (query, 4-dimension) element; the closing barrier keeps this CTA's
+    // results alive until its peers have read them
+    auto cluster_merge = [&]() {
+        const int C = P.cluster;
+        __syncwarp();                                // the barrier instructions are warp-aligned
+        dla::cluster_sync_all();
+        for (int qi = tid; qi < Q; qi += kMmaConsumers * 32) {
+            const int rq = s_qrow[qi];
+            const int np = min(C, (s_len[rq] + P.chunk - 1) / P.chunk);
+            float M = -INFINITY;
+            for (int pp = 0; pp < np; ++pp) M = fmaxf(M, dla::ld_dsmem_f32(&s_plse[qi], (uint32_t)pp));
+            float W = 0.f;
+            for (int pp = 0; pp < np; ++pp) {
+                const float l = dla::ld_dsmem_f32(&s_plse[qi], (uint32_t)pp);
+                W += l == -INFINITY ? 0.f : __expf(l - M);
+            }
+            s_mM[qi] = M;
+            s_mW[qi] = W;
+            if (a.lse_out && qi % C == piece)
+                a.lse_out[(int64_t)s_row[rq] * P.n_q + h * G + s_qhead[qi]] = np == 0 ? -INFINITY : M + logf(W);
+        }
+        dla::named_sync(1, kMmaConsumers * 32);
+        for (int e = piece + C * tid; e < Q * (D / 4); e += C * kMmaConsumers * 32) {
+            const int qi = e / (D / 4), d4 = e - qi * (D / 4);
+            const int rq = s_qrow[qi];
+            const int np = min(C, (s_len[rq] + P.chunk - 1) / P.chunk);
+            const float M = s_mM[qi];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int pp = 0; pp < np; ++pp) {
+                const float l = dla::ld_dsmem_f32(&s_plse[qi], (uint32_t)pp);
+                const float w = l == -INFINITY ? 0.f : __expf(l - M);
+                const float4 v = dla::ld_dsmem_f32x4(qraw + qi * D + d4 * 4, (uint32_t)pp);
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
+            const float inv = np == 0 ? 0.f : 1.f / s_mW[qi];
+            *reinterpret_cast<float4 *>(a.out + (int64_t)s_row[rq] * a.out_stride +
+                                        (int64_t)(h * G + s_qhead[qi]) * D + d4 * 4) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        }
+        dla::cluster_sync_relaxed();
+    };
+    if (idle) {                                      // (cluster plans only: the others returned)
+        cluster_merge();
+        return;
+    }
     // fused form: rotate the session's queries in shared memory (bias first), every consumer
     // thread a share of the (query, channel pair) elements, before any of them is read
     auto rotate_queries = [&](bool qok) {
@@ -605,6 +682,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
 
         if (attn_consumers_any(bad)) {
             poison_partials();
+            if (P.cluster) cluster_merge();
             return;
         }
     #pragma unroll
@@ -746,6 +824,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         }
         if (attn_consumers_any(bad)) {
             poison_partials();
+            if (P.cluster) cluster_merge();
             return;
         }
         if (sg < NS) {
@@ -783,9 +862,13 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         }
         cf[qi * (kMmaConsumers + 1) + kMmaConsumers] = 1.f / wsum;
         const int rq = s_qrow[qi];
-        if (s_len[rq] > k0)
-            a.part_lse[((int64_t)s_row[rq] * P.n_q + h * G + s_qhead[qi]) * ms + piece] =
-                (M + fast_log2(wsum)) * 0.69314718055994530942f;
+        if (s_len[rq] > k0) {
+            const float lse_piece = (M + fast_log2(wsum)) * 0.69314718055994530942f;
+            if (P.cluster)
+                s_plse[qi] = lse_piece;
+            else
+                a.part_lse[((int64_t)s_row[rq] * P.n_q + h * G + s_qhead[qi]) * ms + piece] = lse_piece;
+        }
     }
     dla::named_sync(1, kMmaConsumers * 32);
     for (int e = tid; e < Q * (D / 4); e += kMmaConsumers * 32) {
@@ -806,10 +889,15 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             }
         }
         const float inv = f[kMmaConsumers];
-        const int64_t pidx = ((int64_t)s_row[rq] * P.n_q + h * G + s_qhead[qi]) * ms + piece;
-        *reinterpret_cast<float4 *>(a.part_o + pidx * D + d4 * 4) =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        const float4 res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (P.cluster) {
+            *reinterpret_cast<float4 *>(qraw + qi * D + d4 * 4) = res;
+        } else {
+            const int64_t pidx = ((int64_t)s_row[rq] * P.n_q + h * G + s_qhead[qi]) * ms + piece;
+            *reinterpret_cast<float4 *>(a.part_o + pidx * D + d4 * 4) = res;
+        }
     }
+    if (P.cluster) cluster_merge();
 }
 
 struct MergeArgs {
@@ -969,11 +1057,12 @@ int dl_plan_groups(int n, int max_rows, int *sizes)
     return g;
 }
 
-int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *region_host,
-                       int n_q, int n_kv, int head_dim, int sm_count, int force_chunk,
-                       dl_attn_plan *out)
+// max_cluster == 0: pieces sized per session from the command's total keys (partials + merge);
+// max_cluster > 0: every (session, KV head) gets the same C <= max_cluster pieces (one cluster).
+static int plan_build(int rows, const int32_t *seqlen_host, const int32_t *region_host,
+                      int n_q, int n_kv, int head_dim, int sm_count, int force_chunk, int max_cluster,
+                      dl_attn_plan *out)
 {
-    dl::clear_error();
     if (!out || !seqlen_host) return dl::fail(DL_E_ARG, "dl_attn_plan_build: null pointer");
     if (rows < 1 || rows > DL_MAX_ROWS)
         return dl::fail(DL_E_SHAPE, "dl_attn_plan_build: rows=%d (a command steps 1..%d rows)", rows, DL_MAX_ROWS);
@@ -1026,6 +1115,28 @@ int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *regi
         for (int i = P.sess_begin[s]; i < P.sess_begin[s + 1]; ++i) lmax[s] = std::max(lmax[s], seqlen_host[P.sess_rows[i]]);
         total += (int64_t)lmax[s] * n_kv;
     }
+    if (max_cluster > 0) {
+        // one cluster of C pieces per (session, KV head): about two work items per SM, the
+        // longest session's keys in C pieces
+        const int groups = ns * n_kv;
+        int maxl = 1;
+        for (int s = 0; s < ns; ++s) maxl = std::max(maxl, lmax[s]);
+        int C = (int)std::min<int64_t>(max_cluster, std::max<int64_t>(1, dl::ceil_div(2LL * sm_count, groups)));
+        const int chunk = (int)(dl::ceil_div(dl::ceil_div(maxl, C), kTile) * kTile);
+        C = (int)dl::ceil_div(maxl, chunk);
+        P.chunk = chunk;
+        P.cluster = C;
+        for (int s = 0; s < ns; ++s) {
+            P.sess_splits[s] = C;
+            P.sess_item0[s] = s * n_kv * C;
+        }
+        P.sess_item0[ns] = groups * C;
+        P.n_work = groups * C;
+        P.max_splits = C;
+        P.workspace_bytes = 0;
+        *out = P;
+        return DL_OK;
+    }
     // pieces sized from this command's own work: about two work items per SM
     int chunk;
     if (force_chunk > 0) {
@@ -1053,6 +1164,25 @@ int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *regi
     return DL_OK;
 }
 
+int dl_attn_plan_build(int rows, const int32_t *seqlen_host, const int32_t *region_host,
+                       int n_q, int n_kv, int head_dim, int sm_count, int force_chunk,
+                       dl_attn_plan *out)
+{
+    dl::clear_error();
+    return plan_build(rows, seqlen_host, region_host, n_q, n_kv, head_dim, sm_count, force_chunk, 0, out);
+}
+
+int dl_attn_plan_build_cluster(int rows, const int32_t *seqlen_host, const int32_t *region_host,
+                               int n_q, int n_kv, int head_dim, int sm_count, int max_cluster,
+                               dl_attn_plan *out)
+{
+    dl::clear_error();
+    if (max_cluster < 0 || max_cluster > kMaxCluster)
+        return dl::fail(DL_E_ARG, "dl_attn_plan_build_cluster: max_cluster=%d (0..%d)", max_cluster, kMaxCluster);
+    return plan_build(rows, seqlen_host, region_host, n_q, n_kv, head_dim, sm_count, 0,
+                      max_cluster == 0 ? kMaxCluster : max_cluster, out);
+}
+
 // The new rows of the fused form: raw k and v rows, optional bias, positions and the rope table.
 struct FusedIn {
     const float *k, *v, *bias;
@@ -1061,14 +1191,36 @@ struct FusedIn {
     const dl_rope *rope;
 };
 
+// Results of a cluster plan: written by the launch itself.
+struct ClusterOut {
+    float *out;
+    int64_t out_stride;
+    float *lse;
+};
+
 static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
                             const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
-                            int32_t *status, int path, dl_stream_t stream, const FusedIn *f = nullptr)
+                            int32_t *status, int path, dl_stream_t stream, const FusedIn *f = nullptr,
+                            const ClusterOut *co = nullptr)
 {
     dl::clear_error();
-    if (!q || !kv || !kv->k || !kv->v || !seqlen || !workspace) return dl::fail(DL_E_ARG, "dl_decode_attn: null pointer");
+    if (!q || !kv || !kv->k || !kv->v || !seqlen || (!co && !workspace))
+        return dl::fail(DL_E_ARG, "dl_decode_attn: null pointer");
     int rc = check_plan(plan);
     if (rc != DL_OK) return rc;
+    if ((plan->cluster > 0) != (co != nullptr))
+        return dl::fail(DL_E_ARG, plan->cluster > 0 ? "dl_decode_attn: a cluster plan goes to dl_decode_attn_cluster"
+                                                    : "dl_decode_attn_cluster: the plan has no clusters");
+    if (co) {
+        if (!co->out) return dl::fail(DL_E_ARG, "dl_decode_attn_cluster: null output");
+        if (plan->cluster > kMaxCluster || plan->n_work != plan->n_sessions * plan->n_kv * plan->cluster)
+            return dl::fail(DL_E_ARG, "dl_decode_attn_cluster: cluster of %d", plan->cluster);
+        for (int si = 0; si < plan->n_sessions; ++si)
+            if (plan->sess_splits[si] != plan->cluster || plan->sess_item0[si] != si * plan->n_kv * plan->cluster)
+                return dl::fail(DL_E_ARG, "dl_decode_attn_cluster: session %d is not laid out in clusters", si);
+        if (co->out_stride < (int64_t)plan->n_q * plan->head_dim || !dl::aligned16(co->out) || (co->out_stride % 4) != 0)
+            return dl::fail(DL_E_ALIGN, "dl_decode_attn_cluster: out must be 16-byte aligned rows of n_q*head_dim");
+    }
     if (kv->head_dim != plan->head_dim || kv->n_kv != plan->n_kv)
         return dl::fail(DL_E_SHAPE, "dl_decode_attn: cache heads/dim differ from the plan");
     if (kv->capacity <= 0 || kv->region_stride < (int64_t)kv->n_kv * kv->capacity * kv->head_dim)
@@ -1079,9 +1231,9 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
             return dl::fail(DL_E_ARG, "dl_decode_attn: plan covers %d keys of row %d, the cache holds %d",
                             plan->row_keys_max[r], r, kv->capacity);
     }
-    if (workspace_bytes < plan->workspace_bytes)
+    if (!co && workspace_bytes < plan->workspace_bytes)
         return dl::fail(DL_E_WORKSPACE, "dl_decode_attn: workspace %zu < %zu bytes", workspace_bytes, plan->workspace_bytes);
-    if (!dl::aligned16(workspace) || !dl::aligned16(kv->k) || !dl::aligned16(kv->v) || !dl::aligned16(q) ||
+    if ((!co && !dl::aligned16(workspace)) || !dl::aligned16(kv->k) || !dl::aligned16(kv->v) || !dl::aligned16(q) ||
         (q_stride % 4) != 0 || (kv->region_stride % 8) != 0)
         return dl::fail(DL_E_ALIGN, "dl_decode_attn: q, cache planes and workspace must be 16-byte aligned");
     if (q_stride < (int64_t)plan->n_q * plan->head_dim) return dl::fail(DL_E_ARG, "dl_decode_attn: q_stride too small");
@@ -1095,8 +1247,14 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     a.capacity = kv->capacity;
     a.seqlen = seqlen;
     const size_t po = (size_t)plan->rows * plan->n_q * plan->max_splits * plan->head_dim * 4;
-    a.part_o = static_cast<float *>(workspace);
-    a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((po + 15) / 16) * 16);
+    if (!co) {
+        a.part_o = static_cast<float *>(workspace);
+        a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((po + 15) / 16) * 16);
+    } else {
+        a.out = co->out;
+        a.out_stride = co->out_stride;
+        a.lse_out = co->lse;
+    }
     a.status = status;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)plan->head_dim));
     a.plan = *plan;
@@ -1143,9 +1301,39 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
                            : few ? decode_attn_tma_kernel<128, false, 4> : decode_attn_tma_kernel<128, false, 8>)
                     : (mma ? decode_attn_tma_kernel<64, true, 8>
                            : few ? decode_attn_tma_kernel<64, false, 4> : decode_attn_tma_kernel<64, false, 8>);
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
-    return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kMmaThreads), smem, st, "dl_decode_attn: launch", a, tk, tv);
+    if (!co)
+        return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kMmaThreads), smem, st, "dl_decode_attn: launch", a, tk, tv);
+    // one thread-block cluster per (session, KV head): its pieces are consecutive work items
+    if (plan->cluster > 8) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn_cluster: allow a large cluster");
+    }
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)plan->n_work);
+    lc.blockDim = dim3(kMmaThreads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)plan->cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 2;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(kern), &lc);
+    if (e != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        return dl::fail(DL_E_SHAPE, "dl_decode_attn_cluster: a cluster of %d does not fit on the device", plan->cluster);
+    }
+    void *args[3] = {&a, &tk, &tv};
+    e = cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(kern), args);
+    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn_cluster: launch");
+    return DL_OK;
 }
 
 int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
@@ -1160,6 +1348,19 @@ int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv, c
                       int32_t *status, int path, dl_stream_t stream)
 {
     return decode_attn_impl(q, q_stride, kv, seqlen, plan, workspace, workspace_bytes, status, path, stream);
+}
+
+int dl_decode_attn_cluster(const float *q, int64_t q_stride, const dl_attn_rope_in *rope_in,
+                           const dl_kv_cache *kv, const int32_t *seqlen, const dl_attn_plan *plan,
+                           float *out, int64_t out_stride, float *lse, int32_t *status, int path,
+                           dl_stream_t stream)
+{
+    const ClusterOut co{out, out_stride, lse};
+    if (!rope_in)
+        return decode_attn_impl(q, q_stride, kv, seqlen, plan, nullptr, 0, status, path, stream, nullptr, &co);
+    const FusedIn f{rope_in->k, rope_in->v, rope_in->bias, rope_in->k_stride, rope_in->v_stride, rope_in->pos,
+                    rope_in->rope};
+    return decode_attn_impl(q, q_stride, kv, seqlen, plan, nullptr, 0, status, path, stream, &f, &co);
 }
 
 int dl_decode_attn_rope(const float *q, int64_t q_stride, const float *k, int64_t k_stride,
@@ -1179,6 +1380,7 @@ int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t
     if (!workspace || !seqlen || !out) return dl::fail(DL_E_ARG, "dl_attn_merge: null pointer");
     int rc = check_plan(plan);
     if (rc != DL_OK) return rc;
+    if (plan->cluster > 0) return dl::fail(DL_E_ARG, "dl_attn_merge: a cluster plan merges inside its attention launch");
     if (out_stride < (int64_t)plan->n_q * plan->head_dim) return dl::fail(DL_E_ARG, "dl_attn_merge: out_stride too small");
     if (!dl::aligned16(out) || (out_stride % 4) != 0 || !dl::aligned16(workspace))
         return dl::fail(DL_E_ALIGN, "dl_attn_merge: out and workspace must be 16-byte aligned");

@@ -119,4 +119,14 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(const float *local, uint32_t ra
     return v;
 }
 
+__device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
+{
+    const uint32_t a = smem_u32(local);
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+    return v;
+}
+
 }  // namespace dla

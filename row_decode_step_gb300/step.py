@@ -7,7 +7,9 @@ most eight rows:
     ->  dl_gemv_q8(Wo)  ->  dl_gemv_q8(Wgate|up)  ->  dl_gemv_q8(Wdown)
 
 or, with `fused_rope`, dl_decode_attn_rope in place of the rope/store and the
-attention (one launch fewer, the same stored halves and results).
+attention (one launch fewer, the same stored halves and results); with
+`cluster_merge`, dl_decode_attn_cluster in place of the attention and the merge
+(the pieces of a KV head merge inside their thread-block cluster).
 
 Norms, SwiGLU and residual adds are not part of the path: the gate/up and down
 projections read their own activation buffers (filled by the caller).  More
@@ -21,8 +23,9 @@ from typing import Dict, List, Optional, Sequence
 
 import torch
 
-from . import (KVCache, PackedQ8, Rope, dl_attn_merge, dl_attn_plan_build, dl_decode_attn, dl_decode_attn_rope,
-               dl_gemv_q8, dl_plan_groups, dl_rope_kv_store, workspace_for)
+from . import (KVCache, PackedQ8, Rope, dl_attn_merge, dl_attn_plan_build, dl_attn_plan_build_cluster,
+               dl_decode_attn, dl_decode_attn_cluster, dl_decode_attn_rope, dl_gemv_q8, dl_plan_groups,
+               dl_rope_kv_store, workspace_for)
 
 
 @dataclasses.dataclass
@@ -42,11 +45,13 @@ class Command:
 
     def __init__(self, rows: Sequence[int], positions: Sequence[int], regions: Sequence[int],
                  n_q: int, n_kv: int, head_dim: int, hidden: int, ffn: int, device, sm_count: int = 0,
-                 force_chunk: int = 0, gemv_path: int = 0, attn_path: int = 0, fused_rope: bool = False):
+                 force_chunk: int = 0, gemv_path: int = 0, attn_path: int = 0, fused_rope: bool = False,
+                 cluster_merge: bool = False):
         n = len(rows)
         assert 1 <= n <= 8
         self.gemv_path, self.attn_path = gemv_path, attn_path
         self.fused_rope = bool(fused_rope)
+        self.cluster_merge = bool(cluster_merge)
         self.rows = list(rows)
         self.n = n
         D = head_dim
@@ -54,8 +59,12 @@ class Command:
         self.positions = [int(p) for p in positions]
         self.regions = [int(r) for r in regions]
         self.seqlen_host = [p + 1 for p in self.positions]
-        self.plan = dl_attn_plan_build(self.seqlen_host, n_q, n_kv, D, regions=self.regions,
-                                       sm_count=sm_count, force_chunk=force_chunk)
+        if self.cluster_merge:
+            self.plan = dl_attn_plan_build_cluster(self.seqlen_host, n_q, n_kv, D, regions=self.regions,
+                                                   sm_count=sm_count)
+        else:
+            self.plan = dl_attn_plan_build(self.seqlen_host, n_q, n_kv, D, regions=self.regions,
+                                           sm_count=sm_count, force_chunk=force_chunk)
         dev = device
         f32 = dict(dtype=torch.float32, device=dev)
         self.x = torch.zeros(n, hidden, **f32)
@@ -81,7 +90,17 @@ class Command:
     def run(self, W: LayerWeights, rope: Rope, kv: KVCache, stream=None):
         gp = self.gemv_path if (self.gemv_path != 1 or self.n <= 2) else 0
         dl_gemv_q8(W.wqkv, self.x, self.qkv, stream=stream, path=gp)
-        if self.fused_rope:
+        if self.cluster_merge:
+            if self.fused_rope:
+                dl_decode_attn_cluster(self.q, kv, self.seqlen, self.plan, self.attn, self.lse, k=self.k, v=self.v,
+                                       pos=self.pos, rope=rope, status=self.status, stream=stream,
+                                       path=self.attn_path)
+            else:
+                dl_rope_kv_store(self.q, self.k, self.v, self.pos, rope, kv, self.n_q, row_region=self.region,
+                                 status=self.status, stream=stream)
+                dl_decode_attn_cluster(self.q, kv, self.seqlen, self.plan, self.attn, self.lse, status=self.status,
+                                       stream=stream, path=self.attn_path)
+        elif self.fused_rope:
             dl_decode_attn_rope(self.q, self.k, self.v, self.pos, rope, kv, self.seqlen, self.plan,
                                 self.workspace, status=self.status, stream=stream, path=self.attn_path)
         else:
@@ -89,7 +108,8 @@ class Command:
                              status=self.status, stream=stream)
             dl_decode_attn(self.q, kv, self.seqlen, self.plan, self.workspace, status=self.status, stream=stream,
                            path=self.attn_path)
-        dl_attn_merge(self.workspace, self.plan, self.seqlen, self.attn, self.lse, stream=stream)
+        if not self.cluster_merge:
+            dl_attn_merge(self.workspace, self.plan, self.seqlen, self.attn, self.lse, stream=stream)
         dl_gemv_q8(W.wo, self.attn, self.y_o, stream=stream, path=gp)
         if W.wgu is not None:
             dl_gemv_q8(W.wgu, self.x_ffn, self.gu, stream=stream, path=gp)
@@ -97,7 +117,7 @@ class Command:
 
     @property
     def launches(self) -> int:
-        return 6 if self.fused_rope else 7
+        return 7 - int(self.fused_rope) - int(self.cluster_merge)
 
 
 class LayerStep:
@@ -105,7 +125,7 @@ class LayerStep:
 
     def __init__(self, positions: Sequence[int], regions: Sequence[int], n_q: int, n_kv: int, head_dim: int,
                  hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0, gemv_path: int = 0,
-                 attn_path: int = 0, fused_rope: bool = False):
+                 attn_path: int = 0, fused_rope: bool = False, cluster_merge: bool = False):
         n = len(positions)
         sizes = dl_plan_groups(n)
         self.commands: List[Command] = []
@@ -114,7 +134,7 @@ class LayerStep:
             idx = list(range(r0, r0 + s))
             self.commands.append(Command(idx, [positions[i] for i in idx], [regions[i] for i in idx],
                                          n_q, n_kv, head_dim, hidden, ffn, device, sm_count, force_chunk,
-                                         gemv_path, attn_path, fused_rope))
+                                         gemv_path, attn_path, fused_rope, cluster_merge))
             r0 += s
         self.group_sizes = sizes
 

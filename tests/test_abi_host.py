@@ -99,6 +99,22 @@ def test_attn_plan_sessions(dl):
     assert p.n_sessions == 2
 
 
+def test_attn_plan_cluster_shapes(dl):
+    """Cluster plans: every (session, KV head) has the same C <= max_cluster pieces of a multiple of
+    32 keys covering the longest session, laid out as consecutive work items, with no workspace."""
+    for lens, regions, mc in (([5121], None, 0), ([5121 + r for r in range(8)], None, 0),
+                              ([513, 8192, 1500, 64, 4097, 2900], list(range(6)), 8), ([32761], None, 4)):
+        P = dl.dl_attn_plan_build_cluster(lens, 24, 8, 128, regions=regions, sm_count=152, max_cluster=mc)
+        C = P.cluster
+        assert 1 <= C <= (mc or 16) and P.workspace_bytes == 0
+        assert P.chunk % 32 == 0 and C * P.chunk >= max(lens) > (C - 1) * P.chunk
+        assert P.n_work == P.n_sessions * 8 * C and P.max_splits == C
+        for s in range(P.n_sessions):
+            assert P.sess_splits[s] == C and P.sess_item0[s] == s * 8 * C
+    with pytest.raises(dl.DLError):
+        dl.dl_attn_plan_build_cluster([100], 24, 8, 128, max_cluster=17)
+
+
 def test_attn_plan_refusals(dl):
     for args, code in ((([5] * 9, 24, 8, 128), dl.DL_E_SHAPE),
                        (([0], 24, 8, 128), dl.DL_E_ARG),
