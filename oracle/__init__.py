@@ -52,12 +52,16 @@ def lib():
         L.orc_rope_vec.restype = None
         L.orc_rope_kv_store.argtypes = [P, I64, P, I64, P, I64, P, P, P, I,
                                         I, I, I, I, I, D, P, I64, P, P, I64, I]
+        L.orc_rope_kv_store_f32.argtypes = L.orc_rope_kv_store.argtypes
         L.orc_attn_split.argtypes = [P, I64, I, I, I, I, P, P, I64, I, P, P, I, I, P, P]
+        L.orc_attn_split_f32.argtypes = L.orc_attn_split.argtypes
         L.orc_attn_merge.argtypes = [P, P, I, I, I, I, P, I64, P]
         L.orc_attn_full.argtypes = [P, I64, I, I, I, I, P, P, I64, I, P, P, P, I64, P]
+        L.orc_attn_full_f32.argtypes = L.orc_attn_full.argtypes
         L.orc_plan_groups.argtypes = [I, I, P]
         for f in ("orc_gemv_q8", "orc_gemv_f16w", "orc_q8_dequant", "orc_matmul", "orc_rope_kv_store",
-                  "orc_attn_split", "orc_attn_merge", "orc_attn_full", "orc_plan_groups"):
+                  "orc_rope_kv_store_f32", "orc_attn_split", "orc_attn_split_f32", "orc_attn_merge",
+                  "orc_attn_full", "orc_attn_full_f32", "orc_plan_groups"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -148,19 +152,22 @@ def rope_vec(x, rot_dim: int, neox: bool, theta: float, pos: float) -> np.ndarra
 
 def rope_kv_store(q, k, v, pos, kcache, vcache, *, n_q, n_kv, head_dim, rot_dim, theta,
                   neox=True, bias=None, row_region=None):
-    """Returns q' (float64 [rows][n_q*D]); writes kcache/vcache (uint16 [reg][n_kv][cap][D]) in place."""
+    """Returns q' (float64 [rows][n_q*D]); writes kcache/vcache in place: uint16 [reg][n_kv][cap][D]
+    (the f16 mirror) or float32 (the f32 mirror)."""
     qq = _np(q, np.float32).reshape(q.shape[0], -1)
     kk = _np(k, np.float32).reshape(k.shape[0], -1)
     vv = _np(v, np.float32).reshape(v.shape[0], -1)
     pp = _np(pos, np.int32)
     bb = None if bias is None else _np(bias, np.float32)
     rr = None if row_region is None else _np(row_region, np.int32)
-    assert kcache.dtype == np.uint16 and kcache.flags.c_contiguous and vcache.flags.c_contiguous
+    assert kcache.dtype in (np.uint16, np.float32) and vcache.dtype == kcache.dtype
+    assert kcache.flags.c_contiguous and vcache.flags.c_contiguous
     rows = qq.shape[0]
     cap = kcache.shape[2]
     region_stride = kcache.shape[1] * cap * head_dim
     qo = np.zeros((rows, n_q * head_dim), np.float64)
-    _check(lib().orc_rope_kv_store(_p(qq), qq.shape[1], _p(kk), kk.shape[1], _p(vv), vv.shape[1],
+    fn = lib().orc_rope_kv_store_f32 if kcache.dtype == np.float32 else lib().orc_rope_kv_store
+    _check(fn(_p(qq), qq.shape[1], _p(kk), kk.shape[1], _p(vv), vv.shape[1],
                                    _p(bb), _p(pp), _p(rr), rows, n_q, n_kv, head_dim, rot_dim,
                                    1 if neox else 0, float(theta), _p(qo), n_q * head_dim,
                                    _p(kcache), _p(vcache), region_stride, cap), "rope_kv_store")
@@ -177,7 +184,8 @@ def attn_split(q, kcache, vcache, seqlen, *, n_q, n_kv, head_dim, chunk, n_split
     region_stride = kcache.shape[1] * cap * head_dim
     po = np.zeros((rows, n_q, n_splits, head_dim), np.float64)
     pl = np.zeros((rows, n_q, n_splits), np.float64)
-    _check(lib().orc_attn_split(_p(qq), n_q * head_dim, rows, n_q, n_kv, head_dim,
+    fn = lib().orc_attn_split_f32 if np.asarray(kcache).dtype == np.float32 else lib().orc_attn_split
+    _check(fn(_p(qq), n_q * head_dim, rows, n_q, n_kv, head_dim,
                                 _p(np.ascontiguousarray(kcache)), _p(np.ascontiguousarray(vcache)),
                                 region_stride, cap, _p(rr), _p(sl), chunk, n_splits,
                                 _p(po), _p(pl)), "attn_split")
@@ -204,7 +212,8 @@ def attn_full(q, kcache, vcache, seqlen, *, n_q, n_kv, head_dim, row_region=None
     region_stride = kcache.shape[1] * cap * head_dim
     out = np.zeros((rows, n_q * head_dim), np.float64)
     lse = np.zeros((rows, n_q), np.float64)
-    _check(lib().orc_attn_full(_p(qq), n_q * head_dim, rows, n_q, n_kv, head_dim,
+    fn = lib().orc_attn_full_f32 if np.asarray(kcache).dtype == np.float32 else lib().orc_attn_full
+    _check(fn(_p(qq), n_q * head_dim, rows, n_q, n_kv, head_dim,
                                _p(np.ascontiguousarray(kcache)), _p(np.ascontiguousarray(vcache)),
                                region_stride, cap, _p(rr), _p(sl), _p(out), n_q * head_dim, _p(lse)),
            "attn_full")

@@ -242,13 +242,13 @@ static double orc_clamp_half(double v)
  * Row r writes slot pos[r] of region row_region[r] (NULL: region 0) of each KV head:
  *   K[(reg*region_stride) + (h*capacity + pos)*D + d].
  */
-int orc_rope_kv_store(const float *q_in, int64_t q_stride,
-                      const float *k_in, int64_t k_stride,
-                      const float *v_in, int64_t v_stride,
-                      const float *bias, const int32_t *pos, const int32_t *row_region, int rows,
-                      int n_q, int n_kv, int head_dim, int rot_dim, int neox, double theta,
-                      double *q_out, int64_t qo_stride,
-                      uint16_t *kcache, uint16_t *vcache, int64_t region_stride, int capacity)
+static int orc_rope_kv_store_any(const float *q_in, int64_t q_stride,
+                                 const float *k_in, int64_t k_stride,
+                                 const float *v_in, int64_t v_stride,
+                                 const float *bias, const int32_t *pos, const int32_t *row_region, int rows,
+                                 int n_q, int n_kv, int head_dim, int rot_dim, int neox, double theta,
+                                 double *q_out, int64_t qo_stride,
+                                 void *kcache, void *vcache, int elem, int64_t region_stride, int capacity)
 {
     if (!q_in || !k_in || !v_in || !pos || !q_out || !kcache || !vcache)
         return ORC_EARG;
@@ -277,11 +277,18 @@ int orc_rope_kv_store(const float *q_in, int64_t q_stride,
             for (int d = 0; d < D; ++d)
                 tmp[d] = (double)k_in[r * k_stride + h * D + d] + (bias ? (double)bias[(n_q + h) * D + d] : 0.0);
             orc_rope_vec(tmp, rot_dim, neox, theta, (double)p);
-            for (int d = 0; d < D; ++d)
-                kcache[base + d] = orc_double_to_half(orc_clamp_half(tmp[d]));
+            for (int d = 0; d < D; ++d) {
+                if (elem == 4)
+                    ((float *)kcache)[base + d] = (float)tmp[d];      /* f32 mirror: round to nearest */
+                else
+                    ((uint16_t *)kcache)[base + d] = orc_double_to_half(orc_clamp_half(tmp[d]));
+            }
             for (int d = 0; d < D; ++d) {
                 double v = (double)v_in[r * v_stride + h * D + d] + (bias ? (double)bias[(n_q + n_kv + h) * D + d] : 0.0);
-                vcache[base + d] = orc_double_to_half(orc_clamp_half(v));
+                if (elem == 4)
+                    ((float *)vcache)[base + d] = (float)v;
+                else
+                    ((uint16_t *)vcache)[base + d] = orc_double_to_half(orc_clamp_half(v));
             }
         }
     }
@@ -289,14 +296,47 @@ int orc_rope_kv_store(const float *q_in, int64_t q_stride,
     return ORC_OK;
 }
 
+/* The rope-and-store into the f16 mirror (clamped into the half range, round to nearest even). */
+int orc_rope_kv_store(const float *q_in, int64_t q_stride, const float *k_in, int64_t k_stride,
+                      const float *v_in, int64_t v_stride, const float *bias, const int32_t *pos,
+                      const int32_t *row_region, int rows, int n_q, int n_kv, int head_dim, int rot_dim,
+                      int neox, double theta, double *q_out, int64_t qo_stride,
+                      uint16_t *kcache, uint16_t *vcache, int64_t region_stride, int capacity)
+{
+    return orc_rope_kv_store_any(q_in, q_stride, k_in, k_stride, v_in, v_stride, bias, pos, row_region, rows,
+                                 n_q, n_kv, head_dim, rot_dim, neox, theta, q_out, qo_stride, kcache, vcache, 2,
+                                 region_stride, capacity);
+}
+
+/* The same into the f32 mirror (each value rounded once to f32). */
+int orc_rope_kv_store_f32(const float *q_in, int64_t q_stride, const float *k_in, int64_t k_stride,
+                          const float *v_in, int64_t v_stride, const float *bias, const int32_t *pos,
+                          const int32_t *row_region, int rows, int n_q, int n_kv, int head_dim, int rot_dim,
+                          int neox, double theta, double *q_out, int64_t qo_stride,
+                          float *kcache, float *vcache, int64_t region_stride, int capacity)
+{
+    return orc_rope_kv_store_any(q_in, q_stride, k_in, k_stride, v_in, v_stride, bias, pos, row_region, rows,
+                                 n_q, n_kv, head_dim, rot_dim, neox, theta, q_out, qo_stride, kcache, vcache, 4,
+                                 region_stride, capacity);
+}
+
 /* ----------------------------------------------------------- attention --- */
 
 /* Score of query q (D doubles) against cached key (kv head h, slot j): (q . k_j) / sqrt(D). */
-static double orc_score(const double *q, const uint16_t *kc, int64_t kbase, int D)
+/*
+ * A KV plane of either mirror: binary16 patterns (elem = 2, the default f16 mirror) or f32
+ * values (elem = 4, the f32 mirror of the same rope-and-store template).
+ */
+static double orc_kv_get(const void *plane, int elem, int64_t i)
+{
+    return elem == 4 ? (double)((const float *)plane)[i] : orc_h2d(((const uint16_t *)plane)[i]);
+}
+
+static double orc_score(const double *q, const void *kc, int elem, int64_t kbase, int D)
 {
     double s = 0.0;
     for (int d = 0; d < D; ++d)
-        s += q[d] * orc_h2d(kc[kbase + d]);
+        s += q[d] * orc_kv_get(kc, elem, kbase + d);
     return s / sqrt((double)D);
 }
 
@@ -310,8 +350,8 @@ static double orc_score(const double *q, const uint16_t *kc, int64_t kbase, int 
  *   part_o   [rows][n_q][n_splits][D]
  *   part_lse [rows][n_q][n_splits]
  */
-int orc_attn_split(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
-                   const uint16_t *kcache, const uint16_t *vcache, int64_t region_stride, int capacity,
+static int orc_attn_split_any(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
+                   const void *kcache, const void *vcache, int elem, int64_t region_stride, int capacity,
                    const int32_t *row_region, const int32_t *seqlen, int chunk, int n_splits,
                    double *part_o, double *part_lse)
 {
@@ -341,15 +381,15 @@ int orc_attn_split(const double *q, int64_t q_stride, int rows, int n_q, int n_k
                 }
                 double m = -INFINITY;
                 for (int j = k0; j < k1; ++j) {
-                    double sc = orc_score(qv, kcache, hbase + (int64_t)j * D, D);
+                    double sc = orc_score(qv, kcache, elem, hbase + (int64_t)j * D, D);
                     if (sc > m) m = sc;
                 }
                 double l = 0.0;
                 for (int j = k0; j < k1; ++j) {
-                    double w = exp(orc_score(qv, kcache, hbase + (int64_t)j * D, D) - m);
+                    double w = exp(orc_score(qv, kcache, elem, hbase + (int64_t)j * D, D) - m);
                     l += w;
                     for (int d = 0; d < D; ++d)
-                        o[d] += w * orc_h2d(vcache[hbase + (int64_t)j * D + d]);
+                        o[d] += w * orc_kv_get(vcache, elem, hbase + (int64_t)j * D + d);
                 }
                 for (int d = 0; d < D; ++d) o[d] /= l;
                 *lse = m + log(l);
@@ -398,8 +438,8 @@ int orc_attn_merge(const double *part_o, const double *part_lse, int rows, int n
  * Written without the running maximum of the split form: the scores are first
  * collected, then exponentiated against their exact maximum.
  */
-int orc_attn_full(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
-                  const uint16_t *kcache, const uint16_t *vcache, int64_t region_stride, int capacity,
+static int orc_attn_full_any(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
+                  const void *kcache, const void *vcache, int elem, int64_t region_stride, int capacity,
                   const int32_t *row_region, const int32_t *seqlen,
                   double *out, int64_t out_stride, double *lse)
 {
@@ -421,7 +461,7 @@ int orc_attn_full(const double *q, int64_t q_stride, int rows, int n_q, int n_kv
             const double *qv = q + r * q_stride + (int64_t)h * D;
             double M = -INFINITY;
             for (int j = 0; j < L; ++j) {
-                sc[j] = orc_score(qv, kcache, hbase + (int64_t)j * D, D);
+                sc[j] = orc_score(qv, kcache, elem, hbase + (int64_t)j * D, D);
                 if (sc[j] > M) M = sc[j];
             }
             double Z = 0.0;
@@ -431,12 +471,46 @@ int orc_attn_full(const double *q, int64_t q_stride, int rows, int n_q, int n_kv
             for (int d = 0; d < D; ++d) ov[d] = 0.0;
             for (int j = 0; j < L; ++j)
                 for (int d = 0; d < D; ++d)
-                    ov[d] += sc[j] * orc_h2d(vcache[hbase + (int64_t)j * D + d]);
+                    ov[d] += sc[j] * orc_kv_get(vcache, elem, hbase + (int64_t)j * D + d);
             lse[(int64_t)r * n_q + h] = M + log(Z);
         }
         free(sc);
     }
     return ORC_OK;
+}
+
+int orc_attn_split(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
+                   const uint16_t *kcache, const uint16_t *vcache, int64_t region_stride, int capacity,
+                   const int32_t *row_region, const int32_t *seqlen, int chunk, int n_splits,
+                   double *part_o, double *part_lse)
+{
+    return orc_attn_split_any(q, q_stride, rows, n_q, n_kv, head_dim, kcache, vcache, 2, region_stride, capacity,
+                              row_region, seqlen, chunk, n_splits, part_o, part_lse);
+}
+
+int orc_attn_split_f32(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
+                       const float *kcache, const float *vcache, int64_t region_stride, int capacity,
+                       const int32_t *row_region, const int32_t *seqlen, int chunk, int n_splits,
+                       double *part_o, double *part_lse)
+{
+    return orc_attn_split_any(q, q_stride, rows, n_q, n_kv, head_dim, kcache, vcache, 4, region_stride, capacity,
+                              row_region, seqlen, chunk, n_splits, part_o, part_lse);
+}
+
+int orc_attn_full(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
+                  const uint16_t *kcache, const uint16_t *vcache, int64_t region_stride, int capacity,
+                  const int32_t *row_region, const int32_t *seqlen, double *out, int64_t out_stride, double *lse)
+{
+    return orc_attn_full_any(q, q_stride, rows, n_q, n_kv, head_dim, kcache, vcache, 2, region_stride, capacity,
+                             row_region, seqlen, out, out_stride, lse);
+}
+
+int orc_attn_full_f32(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
+                      const float *kcache, const float *vcache, int64_t region_stride, int capacity,
+                      const int32_t *row_region, const int32_t *seqlen, double *out, int64_t out_stride, double *lse)
+{
+    return orc_attn_full_any(q, q_stride, rows, n_q, n_kv, head_dim, kcache, vcache, 4, region_stride, capacity,
+                             row_region, seqlen, out, out_stride, lse);
 }
 
 /* ------------------------------------------------------------- grouping --- */

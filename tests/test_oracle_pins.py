@@ -397,6 +397,66 @@ def test_empty_split_weighs_nothing():
 
 # ------------------------------------------------------------------ grouping
 
+def test_f32_mirror_store():
+    """The f32 mirror: k rotated as a complex product and rounded once to f32, v (plus bias) rounded
+    once to f32, no clamp to the half range; the slot layout is the f16 mirror's."""
+    n_q, n_kv, D, cap = 2, 2, 64, 16
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, n_q * D)).astype(np.float32)
+    k = rng.standard_normal((1, n_kv * D)).astype(np.float32)
+    v = rng.standard_normal((1, n_kv * D)).astype(np.float32)
+    k[0, 3] = 1.0e5                    # past the half range: kept in the f32 mirror
+    b = rng.standard_normal((n_q + 2 * n_kv) * D).astype(np.float32)
+    kc = np.zeros((1, n_kv, cap, D), np.float32)
+    vc = np.zeros((1, n_kv, cap, D), np.float32)
+    pos = 11
+    oracle.rope_kv_store(q, k, v, np.array([pos], np.int32), kc, vc, n_q=n_q, n_kv=n_kv, head_dim=D, rot_dim=D,
+                         theta=500000.0, neox=True, bias=b)
+    j = np.arange(D // 2)
+    ang = pos * 500000.0 ** (-2.0 * j / D)
+    for h in range(n_kv):
+        kb = k[0, h * D:(h + 1) * D].astype(np.float64) + b[(n_q + h) * D:(n_q + h + 1) * D]
+        z = (kb[:D // 2] + 1j * kb[D // 2:]) * np.exp(1j * ang)
+        want = np.concatenate([z.real, z.imag]).astype(np.float32)
+        got = kc[0, h, pos]
+        assert np.max(np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))) <= 1
+        vb = (v[0, h * D:(h + 1) * D].astype(np.float64) + b[(n_q + n_kv + h) * D:(n_q + n_kv + h + 1) * D])
+        np.testing.assert_array_equal(vc[0, h, pos], vb.astype(np.float32))
+    # the pair holding 1e5 keeps its norm: one of its two channels is past 65504 (nothing clamped)
+    assert max(abs(float(kc[0, 0, pos, 3])), abs(float(kc[0, 0, pos, 3 + D // 2]))) > 65504.0
+    assert np.count_nonzero(kc) == n_kv * D and np.count_nonzero(vc) == n_kv * D
+
+
+def test_f32_mirror_attention():
+    """Attention over f32 planes equals scipy's softmax over the same values, and f16-valued
+    f32 planes give exactly the f16 mirror's result."""
+    n_q, n_kv, D = 6, 2, 64
+    q, kc16, vc16, sl = _attn_inputs(3, 3, n_q, n_kv, D, 200, [200, 57, 1])
+    rng = np.random.default_rng(7)
+    kc32 = rng.standard_normal(kc16.shape).astype(np.float32)
+    vc32 = rng.standard_normal(vc16.shape).astype(np.float32)
+    out, lse = oracle.attn_full(q, kc32, vc32, sl, n_q=n_q, n_kv=n_kv, head_dim=D)
+    from scipy.special import logsumexp
+    K, V = kc32.astype(np.float64), vc32.astype(np.float64)
+    for r in range(3):
+        for h in range(n_q):
+            s_ = K[0, h // 3, :sl[r]] @ q[r, h * D:(h + 1) * D] / math.sqrt(D)
+            assert abs(lse[r, h] - logsumexp(s_)) < 1e-12
+            np.testing.assert_allclose(out[r, h * D:(h + 1) * D], np.exp(s_ - logsumexp(s_)) @ V[0, h // 3, :sl[r]],
+                                       rtol=0, atol=1e-12)
+    po, pl = oracle.attn_split(q, kc32, vc32, sl, n_q=n_q, n_kv=n_kv, head_dim=D, chunk=32, n_splits=7)
+    mo, ml = oracle.attn_merge(po, pl)
+    np.testing.assert_allclose(mo, out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ml, lse, rtol=0, atol=1e-12)
+    # the f16 values widened into an f32 mirror: identical to the f16 mirror's result
+    k_w = kc16.view(np.float16).astype(np.float32)
+    v_w = vc16.view(np.float16).astype(np.float32)
+    o16, l16 = oracle.attn_full(q, kc16, vc16, sl, n_q=n_q, n_kv=n_kv, head_dim=D)
+    o32, l32 = oracle.attn_full(q, k_w, v_w, sl, n_q=n_q, n_kv=n_kv, head_dim=D)
+    np.testing.assert_array_equal(o16, o32)
+    np.testing.assert_array_equal(l16, l32)
+
+
 def test_grouping_golden():
     """The pages' twelve streams run as two commands of six (tests/golden/grouping.txt)."""
     for n, sizes in _read_golden("grouping.txt"):
