@@ -42,6 +42,10 @@
  *  [CLU]  TensorFold PR #926 "drama: the tower's one-row projections ...": a CTA
  *         cluster shares a head, its CTAs exchanging their pieces' results over
  *         distributed shared memory instead of a separate merge pass.
+ *  [KV32] daScript PR #4293, "Tests": the rope-and-store template also serves an
+ *         f32 mirror (RopeKvStore's f32 stamp) beside the default f16 one.  With
+ *         it every stored value is rounded once to f32 (no clamp), and the
+ *         attention runs on CUDA cores (the tensor form reads f16 operands).
  *  [ROPE] daScript PR #4293 "dasLLAMA llama leg ...", commit "The decode
  *         rope-and-store rides one template on both homes" (GkRopeKvStore).
  *  [GRP]  the same PR, commit "The Vulkan batched step past eight rows runs in
@@ -209,13 +213,14 @@ int dl_gemv_f16w_ex(const dl_f16_weight *W, const float *x, int rows, int64_t x_
  * Each session (stream) owns one region.
  */
 typedef struct dl_kv_cache {
-    uint16_t *k;              /* device f16 K plane */
-    uint16_t *v;              /* device f16 V plane */
+    void *k;                  /* device K plane: f16 patterns, or f32 values (elem_bytes 4) */
+    void *v;                  /* device V plane, same element type */
     int64_t region_stride;    /* elements between regions, >= n_kv*capacity*head_dim */
     int n_regions;
     int n_kv;                 /* KV heads */
     int head_dim;             /* 64 or 128 */
     int capacity;             /* slots per head and region */
+    int elem_bytes;           /* 2 (or 0): the f16 mirror; 4: the f32 mirror [KV32] */
 } dl_kv_cache;
 
 /* ------------------------------------------------------------------- RoPE */

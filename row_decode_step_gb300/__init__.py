@@ -54,7 +54,7 @@ class dl_f16_weight(ctypes.Structure):
 class dl_kv_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("region_stride", ctypes.c_int64),
                 ("n_regions", ctypes.c_int), ("n_kv", ctypes.c_int), ("head_dim", ctypes.c_int),
-                ("capacity", ctypes.c_int)]
+                ("capacity", ctypes.c_int), ("elem_bytes", ctypes.c_int)]
 
 
 class dl_rope(ctypes.Structure):
@@ -252,21 +252,22 @@ def dl_gemv_f16w(W: PackedF16W, x: torch.Tensor, y: Optional[torch.Tensor] = Non
 # ------------------------------------------------------------------ KV cache
 
 class KVCache:
-    """An f16 mirror [n_regions][n_kv][capacity][head_dim] for K and V."""
+    """A K/V mirror [n_regions][n_kv][capacity][head_dim]: float16 (the default) or float32."""
 
     def __init__(self, k: torch.Tensor, v: torch.Tensor):
         assert k.shape == v.shape and k.dim() == 4
-        _dev(k, torch.float16, "k")
-        _dev(v, torch.float16, "v")
+        dt = torch.float32 if k.dtype == torch.float32 else torch.float16
+        _dev(k, dt, "k")
+        _dev(v, dt, "v")
         self.k, self.v = k, v
         n_reg, n_kv, cap, D = k.shape
-        self.c = dl_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), n_reg, n_kv, D, cap)
+        self.c = dl_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), n_reg, n_kv, D, cap,
+                             4 if dt == torch.float32 else 2)
 
     @classmethod
-    def empty(cls, n_regions, n_kv, capacity, head_dim, device="cuda"):
+    def empty(cls, n_regions, n_kv, capacity, head_dim, device="cuda", dtype=torch.float16):
         shape = (n_regions, n_kv, capacity, head_dim)
-        return cls(torch.empty(shape, dtype=torch.float16, device=device),
-                   torch.empty(shape, dtype=torch.float16, device=device))
+        return cls(torch.empty(shape, dtype=dtype, device=device), torch.empty(shape, dtype=dtype, device=device))
 
 
 class Rope:

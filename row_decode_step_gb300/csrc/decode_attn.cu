@@ -31,7 +31,7 @@ constexpr int kCudaCoreMaxQ = 4;   // queries per work item up to which the CUDA
 struct AttnArgs {
     const float *q;
     int64_t q_stride;
-    const uint16_t *kc, *vc;
+    const void *kc, *vc;
     int64_t region_stride;
     int capacity;
     const int32_t *seqlen;
@@ -48,7 +48,7 @@ struct AttnArgs {
     int64_t k_stride, v_stride;
     const int32_t *pos;
     const float2 *cs;    // [max_pos][rot/2] (cos, sin)
-    uint16_t *kc_w, *vc_w;
+    void *kc_w, *vc_w;  // f16 patterns, or f32 values in the f32 mirror
     int rot, neox, max_pos;
     // merge inside the launch (plan.cluster = C > 0): the results go straight to out / lse_out
     float *out, *lse_out;
@@ -165,14 +165,19 @@ constexpr int kAttnPreWaitStages = 2;        // stages requested before the wait
 
 // Ring depth per head dimension: two CTAs fit on an SM.
 __host__ __device__ constexpr int mma_stages(int D) { return D == 128 ? 4 : 8; }
+// Stages of the ring.  Stage i sits in slot i % S and the consumer warps' stage groups take
+// stages round robin, so S must be at least the number of groups (kMmaConsumers): a warp must
+// never wait on a slot two fills ahead of what it holds (a parity wait cannot tell the phases
+// apart).  The f32 mirror keeps four stages of twice the bytes (one CTA per SM at D = 128).
+__host__ __device__ constexpr int attn_stages(int D, bool kv32) { return kv32 ? 4 : mma_stages(D); }
 
-size_t attn_mma_smem_bytes(int D)
+size_t attn_mma_smem_bytes(int D, bool kv32 = false)
 {
-    const size_t stage = (size_t)2 * kStKeys * D * 2;                    // K and V of 32 keys
+    const size_t stage = (size_t)2 * kStKeys * D * (kv32 ? 4 : 2);       // K and V of 32 keys
     const size_t qf = (size_t)2 * (D / 16) * 32 * 32;                    // query fragments, 2 tiles
     const size_t qr = (size_t)kMaxQ * D * 4;                             // the queries as they arrive
     const size_t cs = (size_t)DL_MAX_ROWS * (D / 2) * 8;                 // rotary rows (fused form)
-    return 1024 + (size_t)mma_stages(D) * stage + qf + qr + cs;         // + alignment slack
+    return 1024 + (size_t)attn_stages(D, kv32) * stage + qf + qr + cs;  // + alignment slack
 }
 
 // OR of `flag` over the consumer warps (uniform result).
@@ -185,16 +190,21 @@ __device__ __forceinline__ bool attn_consumers_any(bool flag)
     return r != 0;
 }
 
-template <int D, bool MMA, int QM>
+// KV32: the f32 mirror (CUDA-core form only: the tensor form reads f16 operands).
+template <int D, bool MMA, int QM, bool KV32 = false>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv)
 {
     constexpr int NKS = D / 16;     // k-steps of the score product
     constexpr int NDT = D / 8;      // 8-wide column tiles of the output
-    constexpr int NH = D / 64;      // 64-dim boxes per key row
-    constexpr int S = mma_stages(D);
-    constexpr uint32_t kStageBytes = 2u * kStKeys * D * 2u;
+    static_assert(!(MMA && KV32), "the tensor form reads the f16 mirror");
+    constexpr int EB = KV32 ? 4 : 2;          // bytes per element of the mirror
+    constexpr int EPB = 128 / EB;             // elements per 128-byte swizzled box row
+    constexpr int NH = D / EPB;               // boxes per key row
+    constexpr int S = attn_stages(D, KV32);
+    static_assert(S >= kMmaConsumers, "every stage group needs a slot of its own in flight");
+    constexpr uint32_t kStageBytes = 2u * kStKeys * D * EB;
     const dl_attn_plan &P = a.plan;
 
     extern __shared__ unsigned char smem_raw[];
@@ -319,10 +329,19 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     k1 = y1;
                 }
                 const int64_t base = (int64_t)reg * a.region_stride + ((int64_t)h * a.capacity + p) * D;
-                a.kc_w[base + i0] = attn_half_clamped(k0);
-                a.kc_w[base + i1] = attn_half_clamped(k1);
-                a.vc_w[base + i0] = attn_half_clamped(v0);
-                a.vc_w[base + i1] = attn_half_clamped(v1);
+                if constexpr (KV32) {
+                    float *kcw = static_cast<float *>(a.kc_w), *vcw = static_cast<float *>(a.vc_w);
+                    kcw[base + i0] = k0;
+                    kcw[base + i1] = k1;
+                    vcw[base + i0] = v0;
+                    vcw[base + i1] = v1;
+                } else {
+                    uint16_t *kcw = static_cast<uint16_t *>(a.kc_w), *vcw = static_cast<uint16_t *>(a.vc_w);
+                    kcw[base + i0] = attn_half_clamped(k0);
+                    kcw[base + i1] = attn_half_clamped(k1);
+                    vcw[base + i0] = attn_half_clamped(v0);
+                    vcw[base + i1] = attn_half_clamped(v1);
+                }
             }
         }
         asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -352,8 +371,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             dla::mbar_expect_tx(&full[st], kStageBytes);
 #pragma unroll
             for (int hf = 0; hf < NH; ++hf) {
-                dla::tma_g2s_3d(kd + hf * kHalfTile, &tk, hf * 64, y, reg, &full[st]);
-                dla::tma_g2s_3d(vd + hf * kHalfTile, &tv, hf * 64, y, reg, &full[st]);
+                dla::tma_g2s_3d(kd + hf * kHalfTile, &tk, hf * EPB, y, reg, &full[st]);
+                dla::tma_g2s_3d(vd + hf * kHalfTile, &tv, hf * EPB, y, reg, &full[st]);
             }
         };
         if (lane == 0) {
@@ -718,7 +737,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
 #pragma unroll
             for (int e = 0; e < DPL; ++e) o[q][e] = make_float2(0.f, 0.f);
         }
-        const int d0 = DPL * lane, dch = d0 >> 3;
+        const int d0 = DPL * lane, dch = d0 / (16 / EB);     // 16-byte chunk of the lane's dimensions
         for (int i = sg; sg < NS && i < nst; i += NS) {
             const int st = i % S;
             if (!__all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((i / S) & 1)))) {
@@ -743,6 +762,24 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             float2 sc[QM], sd[QM];                 // partial sums per score: even, odd chunks x
 #pragma unroll                                     // even, odd dimensions
             for (int q = 0; q < QM; ++q) sc[q] = sd[q] = make_float2(0.f, 0.f);
+            if constexpr (KV32) {
+                // 16 bytes = 4 dimensions per chunk
+#pragma unroll 2
+                for (int ch = 0; ch < D / 4; ++ch) {
+                    const float4 kf = *reinterpret_cast<const float4 *>(kst + (ch >> 3) * kHalfTile + lane * 128 +
+                                                                        (((ch & 7) ^ (lane & 7)) << 4));
+#pragma unroll
+                    for (int q = 0; q < QM; ++q) {
+                        if (q < nq) {
+                            const float4 qa = *reinterpret_cast<const float4 *>(qs + (qb + q) * D + ch * 4);
+                            float2 t = (ch & 1) ? sd[q] : sc[q];
+                            t = __ffma2_rn(make_float2(qa.x, qa.y), make_float2(kf.x, kf.y), t);
+                            t = __ffma2_rn(make_float2(qa.z, qa.w), make_float2(kf.z, kf.w), t);
+                            if (ch & 1) sd[q] = t; else sc[q] = t;
+                        }
+                    }
+                }
+            } else
 #pragma unroll 2
             for (int ch = 0; ch < D / 8; ++ch) {
                 const uint4 kv = *reinterpret_cast<const uint4 *>(kst + (ch >> 3) * kHalfTile + lane * 128 +
@@ -787,7 +824,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             for (int q = 0; q < QM; ++q)
                 if (q < nq) pb[q * kStKeys + lane] = ps[q];
             __syncwarp();
-            const unsigned char *vcol = vst + (dch >> 3) * kHalfTile + (d0 & 7) * 2;
+            const unsigned char *vcol = vst + (dch >> 3) * kHalfTile + (d0 & (16 / EB - 1)) * EB;
 #pragma unroll 2
             for (int j4 = 0; j4 < kStKeys; j4 += 4) {
                 float v[4][DPL];
@@ -795,7 +832,13 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 for (int kk = 0; kk < 4; ++kk) {
                     const int j = j4 + kk;
                     const unsigned char *vp = vcol + j * 128 + (((dch & 7) ^ (j & 7)) << 4);
-                    if constexpr (DPL == 4) {
+                    if constexpr (KV32 && DPL == 4) {
+                        const float4 w = *reinterpret_cast<const float4 *>(vp);
+                        v[kk][0] = w.x; v[kk][1] = w.y; v[kk][2] = w.z; v[kk][3] = w.w;
+                    } else if constexpr (KV32) {
+                        const float2 w = *reinterpret_cast<const float2 *>(vp);
+                        v[kk][0] = w.x; v[kk][1] = w.y;
+                    } else if constexpr (DPL == 4) {
                         const uint2 w = *reinterpret_cast<const uint2 *>(vp);
                         const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
                         const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
@@ -1018,16 +1061,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
 
 // Tensor map of one cache plane as [region][kv_head * capacity + slot][head_dim] f16, read in
 // boxes of 32 slots x 64 dims with the 128-byte swizzle; slots past the plane read as zero.
-int make_kv_tmap(CUtensorMap *m, const uint16_t *plane, const dl_kv_cache *kv)
+int make_kv_tmap(CUtensorMap *m, const void *plane, const dl_kv_cache *kv)
 {
+    const bool f32 = kv->elem_bytes == 4;
+    const cuuint64_t eb = f32 ? 4u : 2u;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
     if (!enc) return dl::fail(DL_E_CUDA, "dl_decode_attn: the driver offers no tensor-map encoder");
     const cuuint64_t dims[3] = {(cuuint64_t)kv->head_dim, (cuuint64_t)kv->n_kv * (cuuint64_t)kv->capacity,
                                 (cuuint64_t)kv->n_regions};
-    const cuuint64_t strides[2] = {(cuuint64_t)kv->head_dim * 2u, (cuuint64_t)kv->region_stride * 2u};
-    const cuuint32_t box[3] = {64u, (cuuint32_t)kStKeys, 1u};
+    const cuuint64_t strides[2] = {(cuuint64_t)kv->head_dim * eb, (cuuint64_t)kv->region_stride * eb};
+    const cuuint32_t box[3] = {(cuuint32_t)(128u / eb), (cuuint32_t)kStKeys, 1u};    // 128-byte box rows
     const cuuint32_t es[3] = {1u, 1u, 1u};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(plane), dims, strides, box, es,
+    const CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                           const_cast<void *>(plane), dims, strides, box, es,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return dl::fail(DL_E_ARG, "dl_decode_attn: cache plane refused as a tensor map (%d)", (int)r);
@@ -1225,6 +1271,8 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
         return dl::fail(DL_E_SHAPE, "dl_decode_attn: cache heads/dim differ from the plan");
     if (kv->capacity <= 0 || kv->region_stride < (int64_t)kv->n_kv * kv->capacity * kv->head_dim)
         return dl::fail(DL_E_ARG, "dl_decode_attn: bad cache geometry");
+    if (kv->elem_bytes != 0 && kv->elem_bytes != 2 && kv->elem_bytes != 4)
+        return dl::fail(DL_E_ARG, "dl_decode_attn: elem_bytes=%d (2 or 4)", kv->elem_bytes);
     for (int r = 0; r < plan->rows; ++r) {
         if (plan->row_region[r] >= kv->n_regions) return dl::fail(DL_E_ARG, "dl_decode_attn: plan region past the cache");
         if (plan->row_keys_max[r] > kv->capacity)
@@ -1234,7 +1282,7 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     if (!co && workspace_bytes < plan->workspace_bytes)
         return dl::fail(DL_E_WORKSPACE, "dl_decode_attn: workspace %zu < %zu bytes", workspace_bytes, plan->workspace_bytes);
     if ((!co && !dl::aligned16(workspace)) || !dl::aligned16(kv->k) || !dl::aligned16(kv->v) || !dl::aligned16(q) ||
-        (q_stride % 4) != 0 || (kv->region_stride % 8) != 0)
+        (q_stride % 4) != 0 || (kv->region_stride * (kv->elem_bytes == 4 ? 4 : 2)) % 16 != 0)
         return dl::fail(DL_E_ALIGN, "dl_decode_attn: q, cache planes and workspace must be 16-byte aligned");
     if (q_stride < (int64_t)plan->n_q * plan->head_dim) return dl::fail(DL_E_ARG, "dl_decode_attn: q_stride too small");
 
@@ -1286,17 +1334,23 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     int qmax = 0;
     for (int si = 0; si < plan->n_sessions; ++si)
         qmax = std::max(qmax, (plan->sess_begin[si + 1] - plan->sess_begin[si]) * (plan->n_q / plan->n_kv));
-    const bool mma = path == 2 || (path == 0 && qmax > kCudaCoreMaxQ);
+    // the f32 mirror is read on CUDA cores (the tensor form takes f16 operands)
+    const bool kv32 = kv->elem_bytes == 4;
+    if (kv32 && path == 2) return dl::fail(DL_E_SHAPE, "dl_decode_attn: the tensor form reads the f16 mirror only");
+    const bool mma = !kv32 && (path == 2 || (path == 0 && qmax > kCudaCoreMaxQ));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     CUtensorMap tk, tv;
     rc = make_kv_tmap(&tk, kv->k, kv);
     if (rc != DL_OK) return rc;
     rc = make_kv_tmap(&tv, kv->v, kv);
     if (rc != DL_OK) return rc;
-    const size_t smem = attn_mma_smem_bytes(plan->head_dim);
+    const size_t smem = attn_mma_smem_bytes(plan->head_dim, kv32);
     // the CUDA-core form holds the queries of a warp in registers: 4 for one-row sessions, else 8
     const bool few = qmax <= 4;
-    auto kern = plan->head_dim == 128
+    auto kern = kv32 ? (plan->head_dim == 128
+                            ? (few ? decode_attn_tma_kernel<128, false, 4, true> : decode_attn_tma_kernel<128, false, 8, true>)
+                            : (few ? decode_attn_tma_kernel<64, false, 4, true> : decode_attn_tma_kernel<64, false, 8, true>))
+         : plan->head_dim == 128
                     ? (mma ? decode_attn_tma_kernel<128, true, 8>
                            : few ? decode_attn_tma_kernel<128, false, 4> : decode_attn_tma_kernel<128, false, 8>)
                     : (mma ? decode_attn_tma_kernel<64, true, 8>

@@ -20,8 +20,9 @@ struct RopeArgs {
     int64_t q_stride, k_stride, v_stride;
     const int32_t *pos, *row_region;
     const float2 *cs;       // [max_pos][rot/2] (cos, sin)
-    uint16_t *kc, *vc;
+    void *kc, *vc;           // f16 patterns, or f32 values when f32 is set
     int64_t region_stride;
+    int f32;
     int32_t *status;
     int n_q, n_kv, D, rot, neox, max_pos, capacity, n_regions;
 };
@@ -108,10 +109,20 @@ __global__ void __launch_bounds__(256) rope_kv_store_kernel(RopeArgs a)
             k1 = y1;
         }
         const int64_t base = (int64_t)reg * a.region_stride + ((int64_t)h * a.capacity + p) * a.D;
-        a.kc[base + i0] = to_half_clamped(k0);
-        a.kc[base + i1] = to_half_clamped(k1);
-        a.vc[base + i0] = to_half_clamped(v0);
-        a.vc[base + i1] = to_half_clamped(v1);
+        if (a.f32) {
+            // the f32 mirror: each value rounded once, nothing clamped
+            float *kc = static_cast<float *>(a.kc), *vc = static_cast<float *>(a.vc);
+            kc[base + i0] = k0;
+            kc[base + i1] = k1;
+            vc[base + i0] = v0;
+            vc[base + i1] = v1;
+        } else {
+            uint16_t *kc = static_cast<uint16_t *>(a.kc), *vc = static_cast<uint16_t *>(a.vc);
+            kc[base + i0] = to_half_clamped(k0);
+            kc[base + i1] = to_half_clamped(k1);
+            vc[base + i0] = to_half_clamped(v0);
+            vc[base + i1] = to_half_clamped(v1);
+        }
     }
 }
 
@@ -159,6 +170,8 @@ int dl_rope_kv_store(float *q, int64_t q_stride, const float *k, int64_t k_strid
         return dl::fail(DL_E_SHAPE, "dl_rope_kv_store: head_dim=%d n_q=%d n_kv=%d", D, n_q, kv->n_kv);
     if (rope->rot_dim < 0 || rope->rot_dim % 2 != 0 || rope->rot_dim > D || rope->max_pos <= 0)
         return dl::fail(DL_E_SHAPE, "dl_rope_kv_store: rot_dim=%d head_dim=%d", rope->rot_dim, D);
+    if (kv->elem_bytes != 0 && kv->elem_bytes != 2 && kv->elem_bytes != 4)
+        return dl::fail(DL_E_ARG, "dl_rope_kv_store: elem_bytes=%d (2 or 4)", kv->elem_bytes);
     if (kv->capacity <= 0 || kv->n_regions <= 0 ||
         kv->region_stride < (int64_t)kv->n_kv * kv->capacity * D)
         return dl::fail(DL_E_ARG, "dl_rope_kv_store: bad cache geometry");
@@ -172,6 +185,7 @@ int dl_rope_kv_store(float *q, int64_t q_stride, const float *k, int64_t k_strid
     a.pos = pos; a.row_region = row_region;
     a.cs = reinterpret_cast<const float2 *>(rope->cos_sin);
     a.kc = kv->k; a.vc = kv->v; a.region_stride = kv->region_stride;
+    a.f32 = kv->elem_bytes == 4 ? 1 : 0;
     a.status = status;
     a.n_q = n_q; a.n_kv = kv->n_kv; a.D = D; a.rot = rope->rot_dim; a.neox = rope->neox ? 1 : 0;
     a.max_pos = rope->max_pos; a.capacity = kv->capacity; a.n_regions = kv->n_regions;
