@@ -367,6 +367,63 @@ def measure_f16w(dev, peak, n_out=16384, n_in=3072, mats=4, reps=50):
     return out
 
 
+def measure_attn_mirrors(dev, peak, caches=4, reps=30):
+    """The attention alone (work items + merge) of the 3B shape at 1 and 8 rows on the f16 and the
+    f32 mirror: `caches` distinct caches (> L2 together) cycled in one CUDA graph; bytes = the keys
+    and values read + queries + outputs."""
+    import synth
+    import torch
+    import row_decode_step_gb300 as dl
+    S = synth.LLAMA_3B
+    cap, D = 5128, S.head_dim
+    stream = torch.cuda.Stream(device=dev)
+    out = {}
+    for name, dt in (("f16", torch.float16), ("f32", torch.float32)):
+        kvs = []
+        for c in range(caches):
+            k = synth.normal_f32(0, "bench/mir/k%d" % c, (1, S.n_kv, cap, D), device=dev).to(dt)
+            v = synth.normal_f32(0, "bench/mir/v%d" % c, (1, S.n_kv, cap, D), device=dev).to(dt)
+            kvs.append(dl.KVCache(k, v))
+        for rows in (1, 8):
+            seqlen = list(range(5121, 5121 + rows))
+            plan = dl.dl_attn_plan_build(seqlen, S.n_q, S.n_kv, D)
+            ws = dl.workspace_for(plan, dev)
+            q = synth.normal_f32(0, "bench/mir/q%d" % rows, (rows, S.n_q * D), device=dev)
+            sl = torch.tensor(seqlen, dtype=torch.int32, device=dev)
+            o = torch.empty(rows, S.n_q * D, device=dev)
+            lse = torch.empty(rows, S.n_q, device=dev)
+
+            def run():
+                for kv in kvs:
+                    dl.dl_decode_attn(q, kv, sl, plan, ws, stream=stream)
+                    dl.dl_attn_merge(ws, plan, sl, o, lse, stream=stream)
+            with torch.cuda.stream(stream):
+                run()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                run()
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                k0 = torch.cuda.Event(enable_timing=True)
+                k1 = torch.cuda.Event(enable_timing=True)
+                k0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                k1.record(stream)
+            torch.cuda.synchronize()
+            ms = k0.elapsed_time(k1) / (reps * caches)
+            eb = 4 if dt == torch.float32 else 2
+            b = max(seqlen) * S.n_kv * D * 2 * eb + rows * S.n_q * D * 4 * 2
+            out["%s_rows_%d" % (name, rows)] = {"attention_us": ms * 1e3, "achieved_gbs": b / (ms / 1e3) / 1e9,
+                                                 "frac": b / (ms / 1e3) / 1e9 / peak}
+            del g
+        del kvs
+        torch.cuda.empty_cache()
+    return out
+
+
 def measure_e2e(step, graphs, L, steps, stream, dev):
     """Same steps through host buffers: per step, the activation rows and positions are copied
     from pinned host memory, the graph runs, and the step's outputs are read back."""
@@ -505,6 +562,8 @@ def run_ours(args):
         del r2
         torch.cuda.empty_cache()
         extras["f16w_gemv"] = measure_f16w(dev, peak)
+        torch.cuda.empty_cache()
+        extras["attention_kv_mirrors"] = measure_attn_mirrors(dev, peak)
         torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
