@@ -53,6 +53,12 @@ def lib():
         L.orc_rope_kv_store.argtypes = [P, I64, P, I64, P, I64, P, P, P, I,
                                         I, I, I, I, I, D, P, I64, P, P, I64, I]
         L.orc_rope_kv_store_f32.argtypes = L.orc_rope_kv_store.argtypes
+        L.orc_rope_kv_store_q8.argtypes = [P, I64, P, I64, P, I64, P, P, P, I,
+                                           I, I, I, I, I, D, P, I64, P, P, P, P, I64, I]
+        L.orc_q8_encode_block.argtypes = [P, P, P]
+        L.orc_q8_encode_block.restype = None
+        L.orc_attn_split_q8.argtypes = [P, I64, I, I, I, I, P, P, P, P, I64, I, P, P, I, I, P, P]
+        L.orc_attn_full_q8.argtypes = [P, I64, I, I, I, I, P, P, P, P, I64, I, P, P, P, I64, P]
         L.orc_attn_split.argtypes = [P, I64, I, I, I, I, P, P, I64, I, P, P, I, I, P, P]
         L.orc_attn_split_f32.argtypes = L.orc_attn_split.argtypes
         L.orc_attn_merge.argtypes = [P, P, I, I, I, I, P, I64, P]
@@ -60,8 +66,9 @@ def lib():
         L.orc_attn_full_f32.argtypes = L.orc_attn_full.argtypes
         L.orc_plan_groups.argtypes = [I, I, P]
         for f in ("orc_gemv_q8", "orc_gemv_f16w", "orc_q8_dequant", "orc_matmul", "orc_rope_kv_store",
-                  "orc_rope_kv_store_f32", "orc_attn_split", "orc_attn_split_f32", "orc_attn_merge",
-                  "orc_attn_full", "orc_attn_full_f32", "orc_plan_groups"):
+                  "orc_rope_kv_store_f32", "orc_rope_kv_store_q8", "orc_attn_split", "orc_attn_split_f32",
+                  "orc_attn_split_q8", "orc_attn_merge", "orc_attn_full", "orc_attn_full_f32", "orc_attn_full_q8",
+                  "orc_plan_groups"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -150,6 +157,32 @@ def rope_vec(x, rot_dim: int, neox: bool, theta: float, pos: float) -> np.ndarra
     return v
 
 
+class Q8Plane:
+    """A q8_0 mirror plane: int8 codes [reg][n_kv][cap][D] and f16 scale bits [reg][n_kv][cap][D/32]."""
+
+    def __init__(self, codes: np.ndarray, scales: np.ndarray):
+        assert codes.dtype == np.int8 and scales.dtype == np.uint16
+        assert codes.flags.c_contiguous and scales.flags.c_contiguous
+        assert codes.shape[:3] == scales.shape[:3] and codes.shape[3] == 32 * scales.shape[3]
+        self.codes, self.scales = codes, scales
+        self.shape = codes.shape
+
+    def values(self) -> np.ndarray:
+        """Decoded values (float64): scale * code."""
+        d = self.scales.view(np.float16).astype(np.float64)
+        return self.codes.astype(np.float64) * np.repeat(d, 32, axis=3)
+
+
+def q8_encode_block(x) -> tuple:
+    """The q8_0 mirror's encoding of 32 float32 values: (codes int8[32], scale bits uint16)."""
+    xx = _np(np.asarray(x, np.float32), np.float32)
+    assert xx.shape == (32,)
+    q = np.zeros(32, np.int8)
+    d = np.zeros(1, np.uint16)
+    lib().orc_q8_encode_block(_p(xx), _p(q), _p(d))
+    return q, int(d[0])
+
+
 def rope_kv_store(q, k, v, pos, kcache, vcache, *, n_q, n_kv, head_dim, rot_dim, theta,
                   neox=True, bias=None, row_region=None):
     """Returns q' (float64 [rows][n_q*D]); writes kcache/vcache in place: uint16 [reg][n_kv][cap][D]
@@ -160,6 +193,17 @@ def rope_kv_store(q, k, v, pos, kcache, vcache, *, n_q, n_kv, head_dim, rot_dim,
     pp = _np(pos, np.int32)
     bb = None if bias is None else _np(bias, np.float32)
     rr = None if row_region is None else _np(row_region, np.int32)
+    if isinstance(kcache, Q8Plane):
+        rows = qq.shape[0]
+        cap = kcache.shape[2]
+        region_stride = kcache.shape[1] * cap * head_dim
+        qo = np.zeros((rows, n_q * head_dim), np.float64)
+        _check(lib().orc_rope_kv_store_q8(_p(qq), qq.shape[1], _p(kk), kk.shape[1], _p(vv), vv.shape[1],
+                                          _p(bb), _p(pp), _p(rr), rows, n_q, n_kv, head_dim, rot_dim,
+                                          1 if neox else 0, float(theta), _p(qo), n_q * head_dim,
+                                          _p(kcache.codes), _p(kcache.scales), _p(vcache.codes), _p(vcache.scales),
+                                          region_stride, cap), "rope_kv_store_q8")
+        return qo
     assert kcache.dtype in (np.uint16, np.float32) and vcache.dtype == kcache.dtype
     assert kcache.flags.c_contiguous and vcache.flags.c_contiguous
     rows = qq.shape[0]
@@ -184,6 +228,12 @@ def attn_split(q, kcache, vcache, seqlen, *, n_q, n_kv, head_dim, chunk, n_split
     region_stride = kcache.shape[1] * cap * head_dim
     po = np.zeros((rows, n_q, n_splits, head_dim), np.float64)
     pl = np.zeros((rows, n_q, n_splits), np.float64)
+    if isinstance(kcache, Q8Plane):
+        _check(lib().orc_attn_split_q8(_p(qq), n_q * head_dim, rows, n_q, n_kv, head_dim,
+                                       _p(kcache.codes), _p(kcache.scales), _p(vcache.codes), _p(vcache.scales),
+                                       region_stride, cap, _p(rr), _p(sl), chunk, n_splits, _p(po), _p(pl)),
+               "attn_split_q8")
+        return po, pl
     fn = lib().orc_attn_split_f32 if np.asarray(kcache).dtype == np.float32 else lib().orc_attn_split
     _check(fn(_p(qq), n_q * head_dim, rows, n_q, n_kv, head_dim,
                                 _p(np.ascontiguousarray(kcache)), _p(np.ascontiguousarray(vcache)),
@@ -212,6 +262,12 @@ def attn_full(q, kcache, vcache, seqlen, *, n_q, n_kv, head_dim, row_region=None
     region_stride = kcache.shape[1] * cap * head_dim
     out = np.zeros((rows, n_q * head_dim), np.float64)
     lse = np.zeros((rows, n_q), np.float64)
+    if isinstance(kcache, Q8Plane):
+        _check(lib().orc_attn_full_q8(_p(qq), n_q * head_dim, rows, n_q, n_kv, head_dim,
+                                      _p(kcache.codes), _p(kcache.scales), _p(vcache.codes), _p(vcache.scales),
+                                      region_stride, cap, _p(rr), _p(sl), _p(out), n_q * head_dim, _p(lse)),
+               "attn_full_q8")
+        return out, lse
     fn = lib().orc_attn_full_f32 if np.asarray(kcache).dtype == np.float32 else lib().orc_attn_full
     _check(fn(_p(qq), n_q * head_dim, rows, n_q, n_kv, head_dim,
                                _p(np.ascontiguousarray(kcache)), _p(np.ascontiguousarray(vcache)),

@@ -204,6 +204,8 @@ int orc_gemv_f16w(const uint16_t *w, int64_t n_out, int64_t n_in,
     return ORC_OK;
 }
 
+void orc_q8_encode_block(const float *x, int8_t *q, uint16_t *d);   /* the q8_0 mirror's encoder, below */
+
 /* ---------------------------------------------------------------- RoPE --- */
 
 /*
@@ -320,6 +322,63 @@ int orc_rope_kv_store_f32(const float *q_in, int64_t q_stride, const float *k_in
                                  region_stride, capacity);
 }
 
+/*
+ * The same into the q8_0 mirror: every stored value is first rounded to f32 (the values the
+ * rope produces), then each block of 32 channels of a key row is encoded by orc_q8_encode_block
+ * into the code plane (laid out as the f16 mirror) and the scale plane (one per 32 values).
+ */
+int orc_rope_kv_store_q8(const float *q_in, int64_t q_stride, const float *k_in, int64_t k_stride,
+                         const float *v_in, int64_t v_stride, const float *bias, const int32_t *pos,
+                         const int32_t *row_region, int rows, int n_q, int n_kv, int head_dim, int rot_dim,
+                         int neox, double theta, double *q_out, int64_t qo_stride,
+                         int8_t *kq, uint16_t *kd, int8_t *vq, uint16_t *vd, int64_t region_stride, int capacity)
+{
+    if (!q_in || !k_in || !v_in || !pos || !q_out || !kq || !kd || !vq || !vd)
+        return ORC_EARG;
+    if (rot_dim < 0 || rot_dim > head_dim || rot_dim % 2 != 0 || head_dim % 32 != 0 || region_stride % 32 != 0)
+        return ORC_EARG;
+    int D = head_dim;
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!tmp)
+        return ORC_EARG;
+    float blk[32];
+    for (int r = 0; r < rows; ++r) {
+        int p = pos[r];
+        int reg = row_region ? row_region[r] : 0;
+        if (p < 0 || p >= capacity) {
+            free(tmp);
+            return ORC_EARG;
+        }
+        for (int h = 0; h < n_q; ++h) {
+            for (int d = 0; d < D; ++d)
+                tmp[d] = (double)q_in[r * q_stride + h * D + d] + (bias ? (double)bias[h * D + d] : 0.0);
+            orc_rope_vec(tmp, rot_dim, neox, theta, (double)p);
+            for (int d = 0; d < D; ++d)
+                q_out[r * qo_stride + h * D + d] = tmp[d];
+        }
+        for (int h = 0; h < n_kv; ++h) {
+            int64_t base = (int64_t)reg * region_stride + ((int64_t)h * capacity + p) * D;
+            for (int d = 0; d < D; ++d)
+                tmp[d] = (double)k_in[r * k_stride + h * D + d] + (bias ? (double)bias[(n_q + h) * D + d] : 0.0);
+            orc_rope_vec(tmp, rot_dim, neox, theta, (double)p);
+            for (int b = 0; b < D / 32; ++b) {
+                for (int i = 0; i < 32; ++i) blk[i] = (float)tmp[32 * b + i];
+                orc_q8_encode_block(blk, kq + base + 32 * b, kd + (base + 32 * b) / 32);
+            }
+            for (int b = 0; b < D / 32; ++b) {
+                for (int i = 0; i < 32; ++i) {
+                    int d = 32 * b + i;
+                    blk[i] = (float)((double)v_in[r * v_stride + h * D + d] +
+                                     (bias ? (double)bias[(n_q + n_kv + h) * D + d] : 0.0));
+                }
+                orc_q8_encode_block(blk, vq + base + 32 * b, vd + (base + 32 * b) / 32);
+            }
+        }
+    }
+    free(tmp);
+    return ORC_OK;
+}
+
 /* ----------------------------------------------------------- attention --- */
 
 /* Score of query q (D doubles) against cached key (kv head h, slot j): (q . k_j) / sqrt(D). */
@@ -327,9 +386,52 @@ int orc_rope_kv_store_f32(const float *q_in, int64_t q_stride, const float *k_in
  * A KV plane of either mirror: binary16 patterns (elem = 2, the default f16 mirror) or f32
  * values (elem = 4, the f32 mirror of the same rope-and-store template).
  */
+
+/*
+ * The block-codec (q8_0) mirror: a plane of int8 codes shaped like the f16 mirror and a plane
+ * of f16 scales, one per 32 consecutive values of a key row (scale index = value index / 32).
+ * Value i = scale[i / 32] * code[i].
+ */
+typedef struct { const int8_t *q; const uint16_t *d; } orc_q8kv;
+
+static double orc_q8kv_get(orc_q8kv p, int64_t i)
+{
+    return orc_h2d(p.d[i / 32]) * (double)p.q[i];
+}
+
+/* Value i of a KV plane: f16 (elem 2), f32 (elem 4) or q8_0 (elem 1, `plane` an orc_q8kv). */
 static double orc_kv_get(const void *plane, int elem, int64_t i)
 {
+    if (elem == 1)
+        return orc_q8kv_get(*(const orc_q8kv *)plane, i);
     return elem == 4 ? (double)((const float *)plane)[i] : orc_h2d(((const uint16_t *)plane)[i]);
+}
+
+/*
+ * Q8_0 encoding of one block of 32 f32 values, decided in f32 (the stored precision of the
+ * values): d = max|x| / 127, code = x / d rounded half away from zero and clamped to +-127,
+ * the scale stored as f16 (round to nearest even); an all-zero block has d = 0 and codes 0.
+ */
+void orc_q8_encode_block(const float *x, int8_t *q, uint16_t *d)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float d32 = amax / 127.0f;
+    for (int i = 0; i < 32; ++i) {
+        int c = 0;
+        if (d32 > 0.0f) {
+            float t = x[i] / d32;
+            float r = floorf(fabsf(t) + 0.5f);
+            c = (int)(t < 0.0f ? -r : r);
+            if (c > 127) c = 127;
+            if (c < -127) c = -127;
+        }
+        q[i] = (int8_t)c;
+    }
+    *d = orc_double_to_half((double)d32);
 }
 
 static double orc_score(const double *q, const void *kc, int elem, int64_t kbase, int D)
@@ -510,6 +612,30 @@ int orc_attn_full_f32(const double *q, int64_t q_stride, int rows, int n_q, int 
                       const int32_t *row_region, const int32_t *seqlen, double *out, int64_t out_stride, double *lse)
 {
     return orc_attn_full_any(q, q_stride, rows, n_q, n_kv, head_dim, kcache, vcache, 4, region_stride, capacity,
+                             row_region, seqlen, out, out_stride, lse);
+}
+
+int orc_attn_split_q8(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
+                      const int8_t *kq, const uint16_t *kd, const int8_t *vq, const uint16_t *vd,
+                      int64_t region_stride, int capacity, const int32_t *row_region, const int32_t *seqlen,
+                      int chunk, int n_splits, double *part_o, double *part_lse)
+{
+    const orc_q8kv K = {kq, kd}, V = {vq, vd};
+    if (!kq || !kd || !vq || !vd)
+        return ORC_EARG;
+    return orc_attn_split_any(q, q_stride, rows, n_q, n_kv, head_dim, &K, &V, 1, region_stride, capacity,
+                              row_region, seqlen, chunk, n_splits, part_o, part_lse);
+}
+
+int orc_attn_full_q8(const double *q, int64_t q_stride, int rows, int n_q, int n_kv, int head_dim,
+                     const int8_t *kq, const uint16_t *kd, const int8_t *vq, const uint16_t *vd,
+                     int64_t region_stride, int capacity, const int32_t *row_region, const int32_t *seqlen,
+                     double *out, int64_t out_stride, double *lse)
+{
+    const orc_q8kv K = {kq, kd}, V = {vq, vd};
+    if (!kq || !kd || !vq || !vd)
+        return ORC_EARG;
+    return orc_attn_full_any(q, q_stride, rows, n_q, n_kv, head_dim, &K, &V, 1, region_stride, capacity,
                              row_region, seqlen, out, out_stride, lse);
 }
 

@@ -457,6 +457,80 @@ def test_f32_mirror_attention():
     np.testing.assert_array_equal(l16, l32)
 
 
+def _numpy_q8_encode(x):
+    """Q8_0 encoding in numpy float32 (independent of the oracle's C)."""
+    x = np.asarray(x, np.float32)
+    amax = np.float32(np.max(np.abs(x)))
+    d32 = np.float32(amax / np.float32(127.0))
+    if d32 == 0:
+        return np.zeros(32, np.int8), 0
+    t = (x / d32).astype(np.float32)
+    r = np.floor(np.abs(t) + np.float32(0.5)).astype(np.float32)
+    q = np.clip(np.where(t < 0, -r, r), -127, 127).astype(np.int8)
+    return q, int(np.array([d32], np.float32).astype(np.float16).view(np.uint16)[0])
+
+
+def test_q8_encode_block():
+    """The q8_0 mirror's block encoding: numpy float32 agrees; ties round away from zero; an
+    all-zero block has scale 0 and codes 0; the largest magnitude takes code +-127."""
+    rng = np.random.default_rng(11)
+    for scale in (1e-3, 1.0, 3e4):
+        x = (rng.standard_normal(32) * scale).astype(np.float32)
+        q, d = oracle.q8_encode_block(x)
+        wq, wd = _numpy_q8_encode(x)
+        np.testing.assert_array_equal(q, wq)
+        assert d == wd
+        assert np.max(np.abs(q.astype(int))) == 127
+    ties = np.zeros(32, np.float32)
+    ties[:6] = [127.0, 2.5, -2.5, 0.5, -0.5, -126.5]      # d = 127 / 127 = 1: t = x exactly
+    q, d = oracle.q8_encode_block(ties)
+    assert list(q[:6]) == [127, 3, -3, 1, -1, -127] and d == 0x3C00
+    q, d = oracle.q8_encode_block(np.zeros(32, np.float32))
+    assert d == 0 and not q.any()
+
+
+def test_q8_mirror_store_and_attention():
+    """The q8_0 mirror: the stored codes and scales are numpy's rotation rounded to f32 and encoded
+    per block; attention over the planes equals scipy's softmax over the decoded values."""
+    n_q, n_kv, D, cap = 4, 2, 64, 40
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((1, n_q * D)).astype(np.float32)
+    k = rng.standard_normal((1, n_kv * D)).astype(np.float32)
+    v = rng.standard_normal((1, n_kv * D)).astype(np.float32)
+    kp = oracle.Q8Plane(rng.integers(-127, 128, (1, n_kv, cap, D)).astype(np.int8),
+                        np.full((1, n_kv, cap, D // 32), 0x2C00, np.uint16))          # scale 1/16
+    vp = oracle.Q8Plane(rng.integers(-127, 128, (1, n_kv, cap, D)).astype(np.int8),
+                        np.full((1, n_kv, cap, D // 32), 0x2C00, np.uint16))
+    pos = 33
+    qo = oracle.rope_kv_store(q, k, v, np.array([pos], np.int32), kp, vp, n_q=n_q, n_kv=n_kv, head_dim=D,
+                              rot_dim=D, theta=500000.0, neox=True)
+    ang = pos * 500000.0 ** (-2.0 * np.arange(D // 2) / D)
+    for h in range(n_kv):
+        kh = k[0, h * D:(h + 1) * D].astype(np.float64)
+        z = (kh[:D // 2] + 1j * kh[D // 2:]) * np.exp(1j * ang)
+        kr = np.concatenate([z.real, z.imag]).astype(np.float32)
+        for b in range(D // 32):
+            wq, wd = _numpy_q8_encode(kr[32 * b:32 * (b + 1)])
+            np.testing.assert_array_equal(kp.codes[0, h, pos, 32 * b:32 * (b + 1)], wq)
+            assert kp.scales[0, h, pos, b] == wd
+            wq, wd = _numpy_q8_encode(v[0, h * D + 32 * b:h * D + 32 * (b + 1)])
+            np.testing.assert_array_equal(vp.codes[0, h, pos, 32 * b:32 * (b + 1)], wq)
+            assert vp.scales[0, h, pos, b] == wd
+    from scipy.special import logsumexp
+    sl = np.array([pos + 1], np.int32)
+    out, lse = oracle.attn_full(qo, kp, vp, sl, n_q=n_q, n_kv=n_kv, head_dim=D)
+    K, V = kp.values(), vp.values()
+    for h in range(n_q):
+        s_ = K[0, h // 2, :pos + 1] @ qo[0, h * D:(h + 1) * D] / math.sqrt(D)
+        assert abs(lse[0, h] - logsumexp(s_)) < 1e-12
+        np.testing.assert_allclose(out[0, h * D:(h + 1) * D], np.exp(s_ - logsumexp(s_)) @ V[0, h // 2, :pos + 1],
+                                   rtol=0, atol=1e-12)
+    po, pl = oracle.attn_split(qo, kp, vp, sl, n_q=n_q, n_kv=n_kv, head_dim=D, chunk=32, n_splits=2)
+    mo, ml = oracle.attn_merge(po, pl)
+    np.testing.assert_allclose(mo, out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ml, lse, rtol=0, atol=1e-12)
+
+
 def test_grouping_golden():
     """The pages' twelve streams run as two commands of six (tests/golden/grouping.txt)."""
     for n, sizes in _read_golden("grouping.txt"):
