@@ -46,6 +46,12 @@
  *         f32 mirror (RopeKvStore's f32 stamp) beside the default f16 one.  With
  *         it every stored value is rounded once to f32 (no clamp), and the
  *         attention runs on CUDA cores (the tensor form reads f16 operands).
+ *  [KVQ8] daScript PR #4293 ("_regions_q8kv" and the block-codec mirror): K and V
+ *         kept as Q8_0 blocks of 32 values.  Here: per block the scale d = max|x| / 127
+ *         (f32, stored as f16) and codes round(x / d) half away from zero, both decided
+ *         in f32; the attention decodes d * code on CUDA cores (no tensor form, no
+ *         rope fused into the attention).  Requires capacity % 4 == 0 and the
+ *         region stride a multiple of 256 values (16-byte aligned scale rows).
  *  [ROPE] daScript PR #4293 "dasLLAMA llama leg ...", commit "The decode
  *         rope-and-store rides one template on both homes" (GkRopeKvStore).
  *  [GRP]  the same PR, commit "The Vulkan batched step past eight rows runs in
@@ -220,7 +226,10 @@ typedef struct dl_kv_cache {
     int n_kv;                 /* KV heads */
     int head_dim;             /* 64 or 128 */
     int capacity;             /* slots per head and region */
-    int elem_bytes;           /* 2 (or 0): the f16 mirror; 4: the f32 mirror [KV32] */
+    int elem_bytes;           /* 2 (or 0): the f16 mirror; 4: the f32 mirror [KV32];
+                                 1: the q8_0 mirror [KVQ8]: k and v hold int8 codes */
+    void *k_scale;            /* q8_0 mirror only: device f16 scales of K, one per 32 values: */
+    void *v_scale;            /*   scale of value index i (as above) at index i / 32 */
 } dl_kv_cache;
 
 /* ------------------------------------------------------------------- RoPE */

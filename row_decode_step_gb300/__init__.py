@@ -54,7 +54,8 @@ class dl_f16_weight(ctypes.Structure):
 class dl_kv_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("region_stride", ctypes.c_int64),
                 ("n_regions", ctypes.c_int), ("n_kv", ctypes.c_int), ("head_dim", ctypes.c_int),
-                ("capacity", ctypes.c_int), ("elem_bytes", ctypes.c_int)]
+                ("capacity", ctypes.c_int), ("elem_bytes", ctypes.c_int),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 class dl_rope(ctypes.Structure):
@@ -262,7 +263,25 @@ class KVCache:
         self.k, self.v = k, v
         n_reg, n_kv, cap, D = k.shape
         self.c = dl_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), n_reg, n_kv, D, cap,
-                             4 if dt == torch.float32 else 2)
+                             4 if dt == torch.float32 else 2, None, None)
+
+    @classmethod
+    def q8(cls, k_codes: torch.Tensor, k_scale: torch.Tensor, v_codes: torch.Tensor, v_scale: torch.Tensor):
+        """The q8_0 mirror: int8 codes [n_regions][n_kv][capacity][head_dim] and float16 scales
+        [n_regions][n_kv][capacity][head_dim / 32]."""
+        assert k_codes.shape == v_codes.shape and k_codes.dim() == 4
+        assert k_scale.shape == v_scale.shape and tuple(k_scale.shape) == tuple(k_codes.shape[:3]) + (
+            k_codes.shape[3] // 32,)
+        for t, n in ((k_codes, "k_codes"), (v_codes, "v_codes")):
+            _dev(t, torch.int8, n)
+        for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+            _dev(t, torch.float16, n)
+        self = cls.__new__(cls)
+        self.k, self.v, self.k_scale, self.v_scale = k_codes, v_codes, k_scale, v_scale
+        n_reg, n_kv, cap, D = k_codes.shape
+        self.c = dl_kv_cache(k_codes.data_ptr(), v_codes.data_ptr(), k_codes.stride(0), n_reg, n_kv, D, cap, 1,
+                             k_scale.data_ptr(), v_scale.data_ptr())
+        return self
 
     @classmethod
     def empty(cls, n_regions, n_kv, capacity, head_dim, device="cuda", dtype=torch.float16):

@@ -50,10 +50,22 @@ struct AttnArgs {
     const float2 *cs;    // [max_pos][rot/2] (cos, sin)
     void *kc_w, *vc_w;  // f16 patterns, or f32 values in the f32 mirror
     int rot, neox, max_pos;
+    // the q8_0 mirror's f16 scale planes (one scale per 32 values of a key row)
+    const uint16_t *ksc, *vsc;
     // merge inside the launch (plan.cluster = C > 0): the results go straight to out / lse_out
     float *out, *lse_out;
     int64_t out_stride;
 };
+
+// Signed bytes `lo`, `lo + 1` of w to floats: the byte flipped to u = q + 128 sits in the low
+// mantissa of 2^23; one packed subtraction of 2^23 + 128 leaves q exactly.
+__device__ __forceinline__ float2 s8x2_to_f32x2(uint32_t w, uint32_t lo)
+{
+    w ^= 0x80808080u;
+    const float2 b = make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | lo)),
+                                 __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541u | lo)));
+    return __fadd2_rn(b, make_float2(-8388736.0f, -8388736.0f));
+}
 
 __device__ __forceinline__ unsigned short attn_half_clamped(float v)
 {
@@ -169,15 +181,22 @@ __host__ __device__ constexpr int mma_stages(int D) { return D == 128 ? 4 : 8; }
 // stages round robin, so S must be at least the number of groups (kMmaConsumers): a warp must
 // never wait on a slot two fills ahead of what it holds (a parity wait cannot tell the phases
 // apart).  The f32 mirror keeps four stages of twice the bytes (one CTA per SM at D = 128).
-__host__ __device__ constexpr int attn_stages(int D, bool kv32) { return kv32 ? 4 : mma_stages(D); }
-
-size_t attn_mma_smem_bytes(int D, bool kv32 = false)
+__host__ __device__ constexpr int attn_stages(int D, int eb) { return eb != 2 ? 4 : mma_stages(D); }
+// Bytes of one ring slot: K and V of 32 keys; for the q8_0 mirror the codes, then the K and V
+// scales, padded to 1024 bytes (the swizzled destinations' alignment).
+__host__ __device__ constexpr uint32_t attn_slot_bytes(int D, int eb)
 {
-    const size_t stage = (size_t)2 * kStKeys * D * (kv32 ? 4 : 2);       // K and V of 32 keys
+    return eb == 1 ? ((uint32_t)(2 * kStKeys * D + 2 * kStKeys * (D / 16)) + 1023u) & ~1023u
+                   : (uint32_t)(2 * kStKeys * D * eb);
+}
+
+size_t attn_mma_smem_bytes(int D, int eb = 2)
+{
+    const size_t stage = attn_slot_bytes(D, eb);                         // K and V of 32 keys
     const size_t qf = (size_t)2 * (D / 16) * 32 * 32;                    // query fragments, 2 tiles
     const size_t qr = (size_t)kMaxQ * D * 4;                             // the queries as they arrive
     const size_t cs = (size_t)DL_MAX_ROWS * (D / 2) * 8;                 // rotary rows (fused form)
-    return 1024 + (size_t)attn_stages(D, kv32) * stage + qf + qr + cs;  // + alignment slack
+    return 1024 + (size_t)attn_stages(D, eb) * stage + qf + qr + cs;    // + alignment slack
 }
 
 // OR of `flag` over the consumer warps (uniform result).
@@ -190,21 +209,28 @@ __device__ __forceinline__ bool attn_consumers_any(bool flag)
     return r != 0;
 }
 
-// KV32: the f32 mirror (CUDA-core form only: the tensor form reads f16 operands).
-template <int D, bool MMA, int QM, bool KV32 = false>
+// EB: bytes per element of the mirror: 2 the f16 mirror, 4 the f32 mirror, 1 the q8_0 mirror
+// (codes; the scales ride along). The f32 and q8_0 mirrors take the CUDA-core form only, since
+// the tensor form reads f16 operands.
+template <int D, bool MMA, int QM, int EB = 2>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv)
 {
     constexpr int NKS = D / 16;     // k-steps of the score product
     constexpr int NDT = D / 8;      // 8-wide column tiles of the output
-    static_assert(!(MMA && KV32), "the tensor form reads the f16 mirror");
-    constexpr int EB = KV32 ? 4 : 2;          // bytes per element of the mirror
-    constexpr int EPB = 128 / EB;             // elements per 128-byte swizzled box row
+    static_assert(!(MMA && EB != 2), "the tensor form reads the f16 mirror");
+    constexpr bool KV32 = EB == 4, KVQ8 = EB == 1;
+    constexpr int EPB = KVQ8 ? D : 128 / EB;  // elements per box row (q8_0: the whole key row)
     constexpr int NH = D / EPB;               // boxes per key row
-    constexpr int S = attn_stages(D, KV32);
+    constexpr int S = attn_stages(D, EB);
     static_assert(S >= kMmaConsumers, "every stage group needs a slot of its own in flight");
-    constexpr uint32_t kStageBytes = 2u * kStKeys * D * EB;
+    constexpr uint32_t kStageBytes = attn_slot_bytes(D, EB);
+    constexpr uint32_t kCodeBytes = kStKeys * D;                  // q8_0: codes of 32 keys
+    constexpr uint32_t kScaleBytes = kStKeys * (D / 16);          // q8_0: scales of 32 keys
+    constexpr uint32_t kVOff = KVQ8 ? kCodeBytes : kStageBytes / 2;   // V within a slot
+    constexpr int kRowB = KVQ8 ? D : 128;    // bytes of a box row in shared memory
+    constexpr bool kSwz = kRowB == 128;      // 128-byte rows are swizzled, 64-byte rows are not
     const dl_attn_plan &P = a.plan;
 
     extern __shared__ unsigned char smem_raw[];
@@ -329,7 +355,9 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     k1 = y1;
                 }
                 const int64_t base = (int64_t)reg * a.region_stride + ((int64_t)h * a.capacity + p) * D;
-                if constexpr (KV32) {
+                if constexpr (KVQ8) {
+                    // (the fused form is refused for the q8_0 mirror before any launch)
+                } else if constexpr (KV32) {
                     float *kcw = static_cast<float *>(a.kc_w), *vcw = static_cast<float *>(a.vc_w);
                     kcw[base + i0] = k0;
                     kcw[base + i1] = k1;
@@ -366,13 +394,27 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         auto issue_stage = [&](int i) {
             const int st = i % S;
             unsigned char *kd = ring + (size_t)st * kStageBytes;
-            unsigned char *vd = kd + kStageBytes / 2;
-            const int y = h * a.capacity + k0 + i * kStKeys;
-            dla::mbar_expect_tx(&full[st], kStageBytes);
+            unsigned char *vd = kd + kVOff;
+            const int key0 = k0 + i * kStKeys;
+            const int y = h * a.capacity + key0;
+            if constexpr (KVQ8) {
+                // codes: one box per key row (keys past the cache read as zero); scales: the
+                // stage's keys up to the capacity (a multiple of 4: whole 16-byte units)
+                const int nk = min(kStKeys, a.capacity - key0);
+                const uint32_t sb = (uint32_t)nk * (D / 16);
+                const int64_t s0 = ((int64_t)reg * a.region_stride + (int64_t)y * D) / 32;
+                dla::mbar_expect_tx(&full[st], 2 * kCodeBytes + 2 * sb);
+                dla::tma_g2s_3d(kd, &tk, 0, y, reg, &full[st]);
+                dla::tma_g2s_3d(vd, &tv, 0, y, reg, &full[st]);
+                dla::bulk_g2s(kd + 2 * kCodeBytes, a.ksc + s0, sb, &full[st]);
+                dla::bulk_g2s(kd + 2 * kCodeBytes + kScaleBytes, a.vsc + s0, sb, &full[st]);
+            } else {
+                dla::mbar_expect_tx(&full[st], kStageBytes);
 #pragma unroll
-            for (int hf = 0; hf < NH; ++hf) {
-                dla::tma_g2s_3d(kd + hf * kHalfTile, &tk, hf * EPB, y, reg, &full[st]);
-                dla::tma_g2s_3d(vd + hf * kHalfTile, &tv, hf * EPB, y, reg, &full[st]);
+                for (int hf = 0; hf < NH; ++hf) {
+                    dla::tma_g2s_3d(kd + hf * kHalfTile, &tk, hf * EPB, y, reg, &full[st]);
+                    dla::tma_g2s_3d(vd + hf * kHalfTile, &tv, hf * EPB, y, reg, &full[st]);
+                }
             }
         };
         if (lane == 0) {
@@ -586,7 +628,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 break;
             }
             const uint32_t ksm = ring_s + (uint32_t)st * kStageBytes;
-            const uint32_t vsm = ksm + kStageBytes / 2;
+            const uint32_t vsm = ksm + kVOff;
             const int kb0 = k0 + i * kStKeys;
             if (kb0 + kStKeys > k1) {
                 // keys past the piece may hold anything (even NaN) in the V rows: zero them
@@ -745,15 +787,23 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 break;
             }
             const unsigned char *kst = ring + (size_t)st * kStageBytes;
-            const unsigned char *vst = kst + kStageBytes / 2;
+            const unsigned char *vst = kst + kVOff;
             const int kb0 = k0 + i * kStKeys;
             if (kb0 + kStKeys > k1) {
-                // keys past the piece may hold anything (even NaN) in the V rows: zero them
-                unsigned char *vrow = ring + (size_t)st * kStageBytes + kStageBytes / 2;
-                for (int e = lane; e < NH * kStKeys * 8; e += 32) {
-                    const int hf = e / (kStKeys * 8), rem = e - hf * kStKeys * 8;
-                    if (kb0 + (rem >> 3) >= k1)
-                        *reinterpret_cast<uint4 *>(vrow + hf * kHalfTile + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
+                // keys past the piece may hold anything (even NaN) in the V rows: zero them (the
+                // q8_0 mirror's codes are finite; zeroing their scales is enough)
+                if constexpr (KVQ8) {
+                    uint16_t *vs = reinterpret_cast<uint16_t *>(ring + (size_t)st * kStageBytes + 2 * kCodeBytes +
+                                                                kScaleBytes);
+                    for (int e = lane; e < kStKeys * (D / 32); e += 32)
+                        if (kb0 + e / (D / 32) >= k1) vs[e] = 0;
+                } else {
+                    unsigned char *vrow = ring + (size_t)st * kStageBytes + kVOff;
+                    for (int e = lane; e < NH * kStKeys * 8; e += 32) {
+                        const int hf = e / (kStKeys * 8), rem = e - hf * kStKeys * 8;
+                        if (kb0 + (rem >> 3) >= k1)
+                            *reinterpret_cast<uint4 *>(vrow + hf * kHalfTile + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 dla::fence_proxy_async();
                 __syncwarp();
@@ -762,7 +812,46 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             float2 sc[QM], sd[QM];                 // partial sums per score: even, odd chunks x
 #pragma unroll                                     // even, odd dimensions
             for (int q = 0; q < QM; ++q) sc[q] = sd[q] = make_float2(0.f, 0.f);
-            if constexpr (KV32) {
+            if constexpr (KVQ8) {
+                // the key's row of D codes, 16 per chunk, two chunks per block of 32; each block's
+                // dot product is scaled by the key's scale of that block
+                const unsigned char *krow = kst + lane * kRowB;
+                const uint16_t *ksr = reinterpret_cast<const uint16_t *>(kst + 2 * kCodeBytes) + lane * (D / 32);
+#pragma unroll 1
+                for (int b = 0; b < D / 32; ++b) {
+                    float2 tq[QM];
+#pragma unroll
+                    for (int q = 0; q < QM; ++q) tq[q] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int ch = 2 * b + hh;
+                        const uint4 w = *reinterpret_cast<const uint4 *>(
+                            krow + ((kSwz ? (ch ^ (lane & 7)) : ch) << 4));
+                        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+                        float2 kf[8];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            kf[2 * u] = s8x2_to_f32x2(wd[u], 0);
+                            kf[2 * u + 1] = s8x2_to_f32x2(wd[u], 2);
+                        }
+#pragma unroll
+                        for (int q = 0; q < QM; ++q) {
+                            if (q < nq) {
+                                const float *qv = qs + (qb + q) * D + ch * 16;
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const float4 qa = *reinterpret_cast<const float4 *>(qv + 4 * u);
+                                    tq[q] = __ffma2_rn(make_float2(qa.x, qa.y), kf[2 * u], tq[q]);
+                                    tq[q] = __ffma2_rn(make_float2(qa.z, qa.w), kf[2 * u + 1], tq[q]);
+                                }
+                            }
+                        }
+                    }
+                    const float dk = __half2float(__ushort_as_half(ksr[b]));
+#pragma unroll
+                    for (int q = 0; q < QM; ++q) sc[q] = __ffma2_rn(make_float2(dk, dk), tq[q], sc[q]);
+                }
+            } else if constexpr (KV32) {
                 // 16 bytes = 4 dimensions per chunk
 #pragma unroll 2
                 for (int ch = 0; ch < D / 4; ++ch) {
@@ -824,15 +913,29 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             for (int q = 0; q < QM; ++q)
                 if (q < nq) pb[q * kStKeys + lane] = ps[q];
             __syncwarp();
-            const unsigned char *vcol = vst + (dch >> 3) * kHalfTile + (d0 & (16 / EB - 1)) * EB;
+            const unsigned char *vcol = KVQ8 ? vst + (d0 & 15) : vst + (dch >> 3) * kHalfTile + (d0 & (16 / EB - 1)) * EB;
+            const uint16_t *vsr = reinterpret_cast<const uint16_t *>(kst + 2 * kCodeBytes + kScaleBytes) + d0 / 32;
 #pragma unroll 2
             for (int j4 = 0; j4 < kStKeys; j4 += 4) {
                 float v[4][DPL];
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const int j = j4 + kk;
-                    const unsigned char *vp = vcol + j * 128 + (((dch & 7) ^ (j & 7)) << 4);
-                    if constexpr (KV32 && DPL == 4) {
+                    const unsigned char *vp = KVQ8 ? vcol + j * kRowB + ((kSwz ? ((d0 >> 4) ^ (j & 7)) : (d0 >> 4)) << 4)
+                                                   : vcol + j * 128 + (((dch & 7) ^ (j & 7)) << 4);
+                    if constexpr (KVQ8) {
+                        // DPL codes of key j, times the key's scale of their block
+                        const float dv = __half2float(__ushort_as_half(vsr[j * (D / 32)]));
+                        if constexpr (DPL == 4) {
+                            const uint32_t w = *reinterpret_cast<const uint32_t *>(vp);
+                            const float2 c01 = s8x2_to_f32x2(w, 0), c23 = s8x2_to_f32x2(w, 2);
+                            v[kk][0] = dv * c01.x; v[kk][1] = dv * c01.y; v[kk][2] = dv * c23.x; v[kk][3] = dv * c23.y;
+                        } else {
+                            const uint32_t w = *reinterpret_cast<const uint16_t *>(vp);
+                            const float2 c01 = s8x2_to_f32x2(w, 0);
+                            v[kk][0] = dv * c01.x; v[kk][1] = dv * c01.y;
+                        }
+                    } else if constexpr (KV32 && DPL == 4) {
                         const float4 w = *reinterpret_cast<const float4 *>(vp);
                         v[kk][0] = w.x; v[kk][1] = w.y; v[kk][2] = w.z; v[kk][3] = w.w;
                     } else if constexpr (KV32) {
@@ -1063,18 +1166,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
 // boxes of 32 slots x 64 dims with the 128-byte swizzle; slots past the plane read as zero.
 int make_kv_tmap(CUtensorMap *m, const void *plane, const dl_kv_cache *kv)
 {
-    const bool f32 = kv->elem_bytes == 4;
-    const cuuint64_t eb = f32 ? 4u : 2u;
+    const bool f32 = kv->elem_bytes == 4, q8 = kv->elem_bytes == 1;
+    const cuuint64_t eb = f32 ? 4u : q8 ? 1u : 2u;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
     if (!enc) return dl::fail(DL_E_CUDA, "dl_decode_attn: the driver offers no tensor-map encoder");
     const cuuint64_t dims[3] = {(cuuint64_t)kv->head_dim, (cuuint64_t)kv->n_kv * (cuuint64_t)kv->capacity,
                                 (cuuint64_t)kv->n_regions};
     const cuuint64_t strides[2] = {(cuuint64_t)kv->head_dim * eb, (cuuint64_t)kv->region_stride * eb};
-    const cuuint32_t box[3] = {(cuuint32_t)(128u / eb), (cuuint32_t)kStKeys, 1u};    // 128-byte box rows
+    // box rows of 128 bytes (swizzled); the q8_0 mirror's rows are whole key rows of codes,
+    // swizzled when they are 128 bytes (head_dim 128), plain when 64
+    const cuuint32_t inner = q8 ? (cuuint32_t)kv->head_dim : (cuuint32_t)(128u / eb);
+    const cuuint32_t box[3] = {inner, (cuuint32_t)kStKeys, 1u};
     const cuuint32_t es[3] = {1u, 1u, 1u};
-    const CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+    const CUtensorMapSwizzle swz = (q8 && kv->head_dim != 128) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    const CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                            const_cast<void *>(plane), dims, strides, box, es,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return dl::fail(DL_E_ARG, "dl_decode_attn: cache plane refused as a tensor map (%d)", (int)r);
     return DL_OK;
@@ -1271,8 +1379,17 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
         return dl::fail(DL_E_SHAPE, "dl_decode_attn: cache heads/dim differ from the plan");
     if (kv->capacity <= 0 || kv->region_stride < (int64_t)kv->n_kv * kv->capacity * kv->head_dim)
         return dl::fail(DL_E_ARG, "dl_decode_attn: bad cache geometry");
-    if (kv->elem_bytes != 0 && kv->elem_bytes != 2 && kv->elem_bytes != 4)
-        return dl::fail(DL_E_ARG, "dl_decode_attn: elem_bytes=%d (2 or 4)", kv->elem_bytes);
+    if (kv->elem_bytes != 0 && kv->elem_bytes != 1 && kv->elem_bytes != 2 && kv->elem_bytes != 4)
+        return dl::fail(DL_E_ARG, "dl_decode_attn: elem_bytes=%d (1, 2 or 4)", kv->elem_bytes);
+    if (kv->elem_bytes == 1) {
+        if (!kv->k_scale || !kv->v_scale || !dl::aligned16(kv->k_scale) || !dl::aligned16(kv->v_scale))
+            return dl::fail(DL_E_ALIGN, "dl_decode_attn: the q8_0 mirror wants 16-byte aligned scale planes");
+        if (kv->capacity % 4 != 0 || kv->region_stride % 256 != 0)
+            return dl::fail(DL_E_SHAPE, "dl_decode_attn: the q8_0 mirror wants capacity %% 4 == 0 and a region "
+                                        "stride that is a multiple of 256 (capacity %d, stride %lld)",
+                            kv->capacity, (long long)kv->region_stride);
+        if (f) return dl::fail(DL_E_SHAPE, "dl_decode_attn_rope: the rope is not fused for the q8_0 mirror");
+    }
     for (int r = 0; r < plan->rows; ++r) {
         if (plan->row_region[r] >= kv->n_regions) return dl::fail(DL_E_ARG, "dl_decode_attn: plan region past the cache");
         if (plan->row_keys_max[r] > kv->capacity)
@@ -1282,7 +1399,7 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     if (!co && workspace_bytes < plan->workspace_bytes)
         return dl::fail(DL_E_WORKSPACE, "dl_decode_attn: workspace %zu < %zu bytes", workspace_bytes, plan->workspace_bytes);
     if ((!co && !dl::aligned16(workspace)) || !dl::aligned16(kv->k) || !dl::aligned16(kv->v) || !dl::aligned16(q) ||
-        (q_stride % 4) != 0 || (kv->region_stride * (kv->elem_bytes == 4 ? 4 : 2)) % 16 != 0)
+        (q_stride % 4) != 0 || (kv->region_stride * (kv->elem_bytes == 4 ? 4 : kv->elem_bytes == 1 ? 1 : 2)) % 16 != 0)
         return dl::fail(DL_E_ALIGN, "dl_decode_attn: q, cache planes and workspace must be 16-byte aligned");
     if (q_stride < (int64_t)plan->n_q * plan->head_dim) return dl::fail(DL_E_ARG, "dl_decode_attn: q_stride too small");
 
@@ -1334,22 +1451,27 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     int qmax = 0;
     for (int si = 0; si < plan->n_sessions; ++si)
         qmax = std::max(qmax, (plan->sess_begin[si + 1] - plan->sess_begin[si]) * (plan->n_q / plan->n_kv));
-    // the f32 mirror is read on CUDA cores (the tensor form takes f16 operands)
-    const bool kv32 = kv->elem_bytes == 4;
-    if (kv32 && path == 2) return dl::fail(DL_E_SHAPE, "dl_decode_attn: the tensor form reads the f16 mirror only");
-    const bool mma = !kv32 && (path == 2 || (path == 0 && qmax > kCudaCoreMaxQ));
+    // the f32 and q8_0 mirrors are read on CUDA cores (the tensor form takes f16 operands)
+    const int eb = kv->elem_bytes == 0 ? 2 : kv->elem_bytes;
+    if (eb != 2 && path == 2) return dl::fail(DL_E_SHAPE, "dl_decode_attn: the tensor form reads the f16 mirror only");
+    const bool mma = eb == 2 && (path == 2 || (path == 0 && qmax > kCudaCoreMaxQ));
+    a.ksc = static_cast<const uint16_t *>(kv->k_scale);
+    a.vsc = static_cast<const uint16_t *>(kv->v_scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     CUtensorMap tk, tv;
     rc = make_kv_tmap(&tk, kv->k, kv);
     if (rc != DL_OK) return rc;
     rc = make_kv_tmap(&tv, kv->v, kv);
     if (rc != DL_OK) return rc;
-    const size_t smem = attn_mma_smem_bytes(plan->head_dim, kv32);
+    const size_t smem = attn_mma_smem_bytes(plan->head_dim, eb);
     // the CUDA-core form holds the queries of a warp in registers: 4 for one-row sessions, else 8
     const bool few = qmax <= 4;
-    auto kern = kv32 ? (plan->head_dim == 128
-                            ? (few ? decode_attn_tma_kernel<128, false, 4, true> : decode_attn_tma_kernel<128, false, 8, true>)
-                            : (few ? decode_attn_tma_kernel<64, false, 4, true> : decode_attn_tma_kernel<64, false, 8, true>))
+    auto kern = eb == 4 ? (plan->head_dim == 128
+                            ? (few ? decode_attn_tma_kernel<128, false, 4, 4> : decode_attn_tma_kernel<128, false, 8, 4>)
+                            : (few ? decode_attn_tma_kernel<64, false, 4, 4> : decode_attn_tma_kernel<64, false, 8, 4>))
+         : eb == 1 ? (plan->head_dim == 128
+                            ? (few ? decode_attn_tma_kernel<128, false, 4, 1> : decode_attn_tma_kernel<128, false, 8, 1>)
+                            : (few ? decode_attn_tma_kernel<64, false, 4, 1> : decode_attn_tma_kernel<64, false, 8, 1>))
          : plan->head_dim == 128
                     ? (mma ? decode_attn_tma_kernel<128, true, 8>
                            : few ? decode_attn_tma_kernel<128, false, 4> : decode_attn_tma_kernel<128, false, 8>)

@@ -212,6 +212,19 @@ def kv_cache_normal(seed: int, label: str, n_regions: int, n_kv: int, capacity: 
     return z.to(torch.float32).to(torch.float16).view(n_regions, n_kv, capacity, head_dim)
 
 
+def kv_q8_random_planes(seed: int, label: str, n_regions: int, n_kv: int, capacity: int, head_dim: int,
+                        device="cpu"):
+    """Random q8_0-mirror planes: int8 codes uniform in [-127, 127] and f16 scales uniform in
+    [0.005, 0.015), one per 32 values (plain draws, no encoding)."""
+    n = n_regions * n_kv * capacity * head_dim
+    u = uniform(seed, stream_id(label + "/codes"), n, device=device)
+    codes = (torch.floor(u * 255.0) - 127.0).clamp_(-127, 127).to(torch.int8)
+    us = uniform(seed, stream_id(label + "/scales"), n // 32, device=device)
+    scales = (0.005 + 0.01 * us).to(torch.float32).to(torch.float16)
+    return (codes.view(n_regions, n_kv, capacity, head_dim),
+            scales.view(n_regions, n_kv, capacity, head_dim // 32))
+
+
 def normal_f32(seed: int, label: str, shape: Sequence[int], std: float = 1.0, device="cpu") -> torch.Tensor:
     """float32 N(0, std^2) draws of the given shape from stream `label`."""
     n = 1
