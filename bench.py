@@ -368,9 +368,9 @@ def measure_f16w(dev, peak, n_out=16384, n_in=3072, mats=4, reps=50):
 
 
 def measure_attn_mirrors(dev, peak, caches=4, reps=30):
-    """The attention alone (work items + merge) of the 3B shape at 1 and 8 rows on the f16 and the
-    f32 mirror: `caches` distinct caches (> L2 together) cycled in one CUDA graph; bytes = the keys
-    and values read + queries + outputs."""
+    """The attention alone (work items + merge) of the 3B shape at 1 and 8 rows on the f16, f32 and
+    q8_0 mirrors: `caches` distinct caches (> L2 together) cycled in one CUDA graph; bytes = the
+    keys and values read + queries + outputs."""
     import synth
     import torch
     import row_decode_step_gb300 as dl
@@ -378,9 +378,14 @@ def measure_attn_mirrors(dev, peak, caches=4, reps=30):
     cap, D = 5128, S.head_dim
     stream = torch.cuda.Stream(device=dev)
     out = {}
-    for name, dt in (("f16", torch.float16), ("f32", torch.float32)):
+    for name, dt in (("f16", torch.float16), ("f32", torch.float32), ("q8_0", torch.int8)):
         kvs = []
         for c in range(caches):
+            if dt == torch.int8:
+                kc, ks = synth.kv_q8_random_planes(0, "bench/mir/k%d" % c, 1, S.n_kv, cap, D, device=dev)
+                vc, vs = synth.kv_q8_random_planes(0, "bench/mir/v%d" % c, 1, S.n_kv, cap, D, device=dev)
+                kvs.append(dl.KVCache.q8(kc, ks, vc, vs))
+                continue
             k = synth.normal_f32(0, "bench/mir/k%d" % c, (1, S.n_kv, cap, D), device=dev).to(dt)
             v = synth.normal_f32(0, "bench/mir/v%d" % c, (1, S.n_kv, cap, D), device=dev).to(dt)
             kvs.append(dl.KVCache(k, v))
@@ -414,8 +419,8 @@ def measure_attn_mirrors(dev, peak, caches=4, reps=30):
                 k1.record(stream)
             torch.cuda.synchronize()
             ms = k0.elapsed_time(k1) / (reps * caches)
-            eb = 4 if dt == torch.float32 else 2
-            b = max(seqlen) * S.n_kv * D * 2 * eb + rows * S.n_q * D * 4 * 2
+            eb = 4 if dt == torch.float32 else 34 / 32 if dt == torch.int8 else 2    # q8_0: codes + a scale per 32
+            b = int(max(seqlen) * S.n_kv * D * 2 * eb) + rows * S.n_q * D * 4 * 2
             out["%s_rows_%d" % (name, rows)] = {"attention_us": ms * 1e3, "achieved_gbs": b / (ms / 1e3) / 1e9,
                                                  "frac": b / (ms / 1e3) / 1e9 / peak}
             del g
