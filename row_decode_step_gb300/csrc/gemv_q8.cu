@@ -11,26 +11,28 @@
 // contiguous along K.  Scales: per 16 rows and 4 tiles, 128 bytes; lane group g
 // reads 16 bytes = (d[g], d[g+8]) for the 4 tiles.
 //
+// The same kernel serves f16 weights (the halfword-weight reference lane of the same PR's
+// description): 1024-byte tiles of 16 rows x 32 inputs in the same A-operand order, no scales.
+//
 // Kernel shape (two CTAs per SM, one wave):
-//  * a CTA of 8 warps owns a run of row tiles and one K-slice; each stage of a
-//    shared-memory ring (about 80 KB, mbarrier-tracked) holds one row tile's slice
-//    (weights, then scales: two contiguous bulk copies).  Thread 0 fills the ring
-//    before waiting on the previous kernel (programmatic dependent launch: the
-//    weights do not depend on it); afterwards each slot is refilled by the warp that
-//    owns the stage just consumed, right after the CTA-wide barrier that ends it;
-//  * each warp owns an eighth of the slice's k-tiles; its activations are loaded
-//    once and kept in registers as operands for the whole launch;
-//  * after each stage the 8 warps' partial 16x8 tiles are summed, in warp order, by
-//    the owner warp (stage index mod 8); the K-slices of a thread-block cluster are
-//    summed through distributed shared memory in rank order at the end (no
-//    atomics: results do not depend on timing).
-// Two inner products share this shape.  Tensor path: the f16 weights (1152 + q)
-// enter 16x8x16 f16 products with f32 accumulation; each activation row is scaled
-// per warp by a power of two (largest |x| into [2^14, 2^15)) and split into two f16
-// terms hi + lo (about 22 significant bits); the products' bias 1152 * sum(x) is
-// taken off per block and column, and the scale undone per column at the end.
-// CUDA-core path (1 or 2 rows): the weights are widened to f32 and multiplied with
-// the f32 activations by FMAs.
+//  * a CTA of 8 warps owns a run of row tiles and one K-slice; each stage of a shared-memory
+//    ring (about 80 KB, mbarrier-tracked) holds one row tile's slice (weights, then scales: two
+//    contiguous bulk copies; f16 weights: one).  Thread 0 requests two stages before waiting on
+//    the previous kernel (programmatic dependent launch: the weights do not depend on it) and the
+//    rest right after the warps have requested their activations;
+//  * each warp owns an eighth of the slice's k-tiles; its activations are loaded once, per lane
+//    from L2, and kept in registers as operands for the whole launch;
+//  * warps run free over the stages: each keeps its partials of a batch of 4 row tiles in
+//    registers, the last warp done with a stage refills its slot, one CTA-wide reduction per batch
+//    sums the 8 warps' 16x8 partials in warp order; the K-slices of a thread-block cluster are
+//    summed through distributed shared memory in rank order at the end (no atomics: results do
+//    not depend on timing).
+// Two inner products share this shape.  Tensor path: the f16 weights (1152 + q for Q8_0, as
+// stored for f16 weights) enter 16x8x16 f16 products with f32 accumulation; each activation row
+// is scaled per warp by a power of two (largest |x| into [2^14, 2^15)) and split into two f16
+// terms hi + lo (about 22 significant bits); for Q8_0 the products' bias 1152 * sum(x) is taken
+// off per block and column; the scale is undone per column at the end.  CUDA-core path (1 or 2
+// rows): the weights are widened to f32 and multiplied with the f32 activations by packed FMAs.
 #include <cuda_fp16.h>
 #include <cstdio>
 #include <algorithm>
