@@ -51,6 +51,8 @@ def parse_args():
                    help="inner product of the GEMVs: 0 library choice, 1 CUDA cores (<= 2 rows), 2 tensor cores")
     p.add_argument("--attn-path", type=int, default=0, choices=[0, 1, 2],
                    help="inner product of the attention: 0 library choice, 1 CUDA cores, 2 tensor cores")
+    p.add_argument("--gemv-chain", type=int, default=0, choices=[0, 1],
+                   help="1: the O, gate/up and down projections as the phases of one persistent launch")
     p.add_argument("--cluster-merge", type=int, default=0, choices=[0, 1],
                    help="1: the pieces of a KV head merge inside their thread-block cluster (no merge launch)")
     p.add_argument("--fused-rope", type=int, default=1, choices=[0, 1],
@@ -222,7 +224,7 @@ def build_layers(wl, L, dev, seed=0):
 
 
 def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0), fused=False,
-            cluster=False):
+            cluster=False, chain=False):
     import synth
     import torch
     import row_decode_step_gb300 as dl
@@ -231,7 +233,8 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
     layers, caches = build_layers(wl, L, dev)
     rope = dl.make_rope(S.rope_theta, S.head_dim, wl["capacity"], device=dev)
     step = LayerStep(wl["positions"], wl["regions"], S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, dev,
-                     gemv_path=paths[0], attn_path=paths[1], fused_rope=fused, cluster_merge=cluster)
+                     gemv_path=paths[0], attn_path=paths[1], fused_rope=fused, cluster_merge=cluster,
+                     gemv_chain=chain)
     for i, c in enumerate(step.commands):
         c.x.copy_(synth.normal_f32(0, "bench/x%d" % i, tuple(c.x.shape), device=dev))
         if c.x_ffn is not None:
@@ -529,7 +532,7 @@ def run_ours(args):
 
     wl = workload(args.workload)
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path),
-                  fused=bool(args.fused_rope), cluster=bool(args.cluster_merge))
+                  fused=bool(args.fused_rope), cluster=bool(args.cluster_merge), chain=bool(args.gemv_chain))
     steps = args.steps
     ms, value = combine_ranks(res["ms_total"], steps, world, dev)
     step = res["step"]
@@ -545,7 +548,8 @@ def run_ours(args):
             w2 = workload(name)
             r2 = measure(w2, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
                          want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
-                         fused=bool(args.fused_rope), cluster=bool(args.cluster_merge))
+                         fused=bool(args.fused_rope), cluster=bool(args.cluster_merge),
+                         chain=bool(args.gemv_chain))
             sb2 = step_bytes(w2, r2["step"])
             extras[name] = {"rows": len(w2["positions"]), "layer_steps_per_s": 1e3 / r2["ms_per_step"],
                             "ms_per_step": r2["ms_per_step"],
@@ -588,7 +592,8 @@ def run_ours(args):
                    "attn_chunk": [c.plan.chunk for c in step.commands],
                    "attn_work_items": [c.plan.n_work for c in step.commands],
                    "gemv_path": args.gemv_path, "attn_path": args.attn_path,
-                   "rope_in_attention": bool(args.fused_rope), "merge_in_cluster": bool(args.cluster_merge)},
+                   "rope_in_attention": bool(args.fused_rope), "merge_in_cluster": bool(args.cluster_merge),
+                   "gemv_chain": bool(args.gemv_chain)},
         "tokens_per_s": rows * value,
         "step": {"algorithmic_bytes": sb, "algorithmic_gbs": step_gbs, "hbm_frac": step_gbs / peak,
                  "peak_gbs": peak, "peak_source": peak_src},

@@ -85,6 +85,7 @@ extern "C" {
 #define DL_STATUS_POS_RANGE     0x1  /* rope/store: pos < 0 or pos >= capacity (row skipped) */
 #define DL_STATUS_REGION_RANGE  0x2  /* rope/store: region outside the cache (row skipped) */
 #define DL_STATUS_SEQLEN_RANGE  0x4  /* attention: seqlen < 1 or past the plan (keys clipped) */
+#define DL_STATUS_SYNC_TIMEOUT  0x8  /* a bounded wait of a persistent launch gave up (outputs invalid) */
 
 #define DL_MAX_ROWS 8          /* rows one command steps at once */
 
@@ -164,6 +165,24 @@ int dl_gemv_q8(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride
  */
 int dl_gemv_q8_ex(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
                   float *y, int64_t y_stride, int path, dl_stream_t stream);
+
+/*
+ * Chained Q8_0 GEMVs in one persistent launch: phase p computes
+ * y_p[r] = W_p x_p[r] (as dl_gemv_q8) for r < rows (1..8), the phases in order,
+ * each complete before the next starts (x_{p+1} may be y_p).  The weights of a
+ * phase stream while the previous one finishes.  Requirements: 1 <= n_phases <= 4,
+ * every n_in a multiple of 1024 and every n_out of 16, x/y 16-byte aligned with
+ * strides multiples of 4, y_p overlapping no x_q.
+ *   sync     device uint32[2], zero before the first call; every successful call
+ *            leaves it ready for the next (its own grid barrier's words)
+ *   status   device int32 or NULL: DL_STATUS_SYNC_TIMEOUT if a bounded wait gave up
+ *   path     as dl_gemv_q8_ex
+ * The K-slices of a row tile are added into the outputs (zeroed by the launch), so
+ * the summation order, and the last bits of a result, may vary from call to call.
+ */
+int dl_gemv_q8_chain(const dl_q8_weight *const *W, const float *const *x, const int64_t *x_stride,
+                     float *const *y, const int64_t *y_stride, int n_phases, int rows,
+                     uint32_t *sync, int32_t *status, int path, dl_stream_t stream);
 
 /* ------------------------------------------------- f16 weights (reference lane)
  *

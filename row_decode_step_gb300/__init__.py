@@ -30,6 +30,7 @@ DL_E_RANGE = -6
 DL_STATUS_POS_RANGE = 0x1
 DL_STATUS_REGION_RANGE = 0x2
 DL_STATUS_SEQLEN_RANGE = 0x4
+DL_STATUS_SYNC_TIMEOUT = 0x8
 DL_MAX_ROWS = 8
 
 _ERRNAMES = {DL_E_ARG: "DL_E_ARG", DL_E_SHAPE: "DL_E_SHAPE", DL_E_ALIGN: "DL_E_ALIGN",
@@ -97,6 +98,7 @@ def lib() -> ctypes.CDLL:
             "dl_q8_pack": ([P, I64, I64, P, P, P], I),
             "dl_gemv_q8": ([P, P, I, I64, P, I64, P], I),
             "dl_gemv_q8_ex": ([P, P, I, I64, P, I64, I, P], I),
+            "dl_gemv_q8_chain": ([P, P, P, P, P, I, I, P, P, I, P], I),
             "dl_f16w_packed_size": ([I64, I64, P], I),
             "dl_f16w_pack": ([P, I64, I64, P, P], I),
             "dl_gemv_f16w": ([P, P, I, I64, P, I64, P], I),
@@ -248,6 +250,28 @@ def dl_gemv_f16w(W: PackedF16W, x: torch.Tensor, y: Optional[torch.Tensor] = Non
         _check(lib().dl_gemv_f16w_ex(ctypes.byref(W.c), _ptr(x), rows, x.stride(0), _ptr(y), y.stride(0),
                                      path, _stream(stream)))
     return y
+
+
+def dl_gemv_q8_chain(Ws: Sequence[PackedQ8], xs: Sequence[torch.Tensor], ys: Sequence[torch.Tensor],
+                     sync: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None,
+                     path: int = GEMV_PATH_AUTO) -> None:
+    """Phases y_p = W_p x_p in one persistent launch, in order (x_{p+1} may be y_p); `sync` is a
+    zeroed int32 CUDA tensor of at least 4 elements, reused call after call."""
+    n = len(Ws)
+    assert len(xs) == n and len(ys) == n and n >= 1
+    rows = xs[0].shape[0]
+    for t in list(xs) + list(ys):
+        _dev(t, torch.float32, "x/y")
+        if t.dim() != 2 or t.stride(1) != 1 or t.shape[0] != rows:
+            raise ValueError("x and y must be 2-D rows with unit inner stride, the same row count")
+    _dev(sync, torch.int32, "sync")
+    Warr = (ctypes.c_void_p * n)(*[ctypes.cast(ctypes.pointer(W.c), ctypes.c_void_p) for W in Ws])
+    xarr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in xs])
+    yarr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in ys])
+    xst = (ctypes.c_int64 * n)(*[t.stride(0) for t in xs])
+    yst = (ctypes.c_int64 * n)(*[t.stride(0) for t in ys])
+    _check(lib().dl_gemv_q8_chain(Warr, xarr, xst, yarr, yst, n, rows, _ptr(sync), _ptr(status), path,
+                                  _stream(stream)))
 
 
 # ------------------------------------------------------------------ KV cache

@@ -540,6 +540,331 @@ __global__ void q8_pack_d_kernel(const uint8_t *blocks, int64_t n_out, int64_t n
     d[u] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// ---------------------------------------------------------------- chained GEMVs
+// A sequence of Q8_0 GEMVs (say O -> gate/up -> down) in one persistent launch: the grid is
+// exactly the CTAs resident at once (two per SM), the phases are separated by grid barriers
+// (phase p + 1 may read phase p's outputs), and each CTA's stages of all phases form one
+// sequence through its ring, so the weights of phase p + 1 stream while phase p finishes and
+// the barrier settles.  Every slice is 32 k-tiles (four per warp); the K-slices of a row tile
+// add their sums into outputs zeroed before the first barrier.
+constexpr int kChainKWM = 4;
+constexpr int kChainKsl = kConsumers * kChainKWM;
+constexpr int kChainMaxPhases = 4;
+constexpr int kBarrierSpins = 1 << 20;               // x 256 ns: a barrier gives up after ~0.3 s
+
+struct ChainPhase {
+    const unsigned char *qs, *d;
+    const float *x;
+    float *y;
+    int64_t x_stride, y_stride;
+    int n_out, n_in, KT, RT, cs, rpr;
+};
+
+struct ChainArgs {
+    ChainPhase ph[kChainMaxPhases];
+    int nph, nr, stages;
+    unsigned *sync;                                  // [0] arrivals, [1] generation
+    int32_t *status;
+};
+
+template <bool MMA, int NRC>
+__global__ void __launch_bounds__(kThreads, 2) gemv_chain_kernel(const __grid_constant__ ChainArgs a)
+{
+    constexpr int RB = kRowBatch, KWM = kChainKWM;
+    constexpr size_t SB = (size_t)kChainKsl * kTileBytesQ8;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ int s_issued, s_fail;
+    __shared__ int s_cnt[kMaxStages];
+    __shared__ int s_off[kChainMaxPhases + 1], s_rt0[kChainMaxPhases], s_slice[kChainMaxPhases];
+
+    const int S = a.stages;
+    unsigned char *ring = smem;
+    float *red = reinterpret_cast<float *>(smem + S * SB);          // [kRowBatch][kConsumers][128]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const unsigned G = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        int off = 0;
+        for (int p = 0; p < a.nph; ++p) {
+            const ChainPhase &P = a.ph[p];
+            const int rt0 = (int)(blockIdx.x / P.cs) * P.rpr;
+            s_off[p] = off;
+            s_rt0[p] = rt0;
+            s_slice[p] = (int)(blockIdx.x % P.cs);
+            off += max(0, min(P.rpr, P.RT - rt0));
+        }
+        s_off[a.nph] = off;
+        for (int st = 0; st < S; ++st) {
+            dla::mbar_init(&full[st], 1);
+            s_cnt[st] = 0;
+        }
+        s_issued = min(S, off);
+        s_fail = 0;
+        dla::mbar_init_fence();
+    }
+    __syncthreads();
+    const int total = s_off[a.nph];
+
+    // stage gi of this CTA's sequence: phase p's row tile, its slice's k-tiles, then their scales
+    auto issue = [&](int gi) {
+        int p = 0;
+        while (gi >= s_off[p + 1]) ++p;
+        const ChainPhase &P = a.ph[p];
+        const int rt = s_rt0[p] + (gi - s_off[p]);
+        const int kt0 = s_slice[p] * kChainKsl;
+        unsigned char *dst = ring + (size_t)(gi % S) * SB;
+        dla::mbar_expect_tx(&full[gi % S], (uint32_t)(kChainKsl * kTileBytesQ8));
+        dla::bulk_g2s(dst, P.qs + ((size_t)rt * P.KT + kt0) * 512, kChainKsl * 512u, &full[gi % S]);
+        dla::bulk_g2s(dst + kChainKsl * 512, P.d + ((size_t)rt * (P.KT >> 2) + (kt0 >> 2)) * 128, kChainKsl * 32u,
+                      &full[gi % S]);
+    };
+    // grid barrier (every CTA resident: the grid is the resident capacity); bounded: a CTA that
+    // waits too long records the failure and the launch winds down
+    auto grid_barrier = [&]() -> bool {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            volatile unsigned *gen = a.sync + 1;
+            const unsigned g0 = *gen;
+            __threadfence();
+            const unsigned arrived = atomicAdd(a.sync, 1u);
+            bool ok = true;
+            if (arrived == G - 1) {
+                atomicExch(a.sync, 0u);
+                __threadfence();
+                atomicAdd(a.sync + 1, 1u);
+            } else {
+                for (int it = 0; *gen == g0; ++it) {
+                    if (it > kBarrierSpins) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+            __threadfence();
+            if (!ok) {
+                s_fail = 1;
+                dl_status_or(a.status, DL_STATUS_SYNC_TIMEOUT);
+            }
+        }
+        __syncthreads();
+        return s_fail == 0;
+    };
+
+    if (threadIdx.x == 0)
+        for (int gi = 0; gi < S && gi < total; ++gi) issue(gi);     // weights: not the previous kernel's
+    dl_pdl_wait();
+    // every phase's outputs start at zero (the K-slices add into them)
+    for (int p = 0; p < a.nph; ++p) {
+        const ChainPhase &P = a.ph[p];
+        const int n4 = P.n_out / 4;
+        for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < (int64_t)a.nr * n4;
+             e += (int64_t)G * kThreads) {
+            const int r = (int)(e / n4), o4 = (int)(e - (int64_t)r * n4);
+            reinterpret_cast<float4 *>(P.y + r * P.y_stride)[o4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    bool bad = !grid_barrier();
+    for (int p = 0; p < a.nph && !bad; ++p) {
+        if (p > 0 && !grid_barrier()) {
+            bad = true;
+            break;
+        }
+        const ChainPhase &P = a.ph[p];
+        const int base = s_off[p], nrt = s_off[p + 1] - base;
+        const int kt0 = s_slice[p] * kChainKsl;
+        const int wk0 = warp * KWM;
+        // this warp's activations (every slice is whole: K is a multiple of 32 k-tiles)
+        uint32_t bh[MMA ? KWM : 1][4], bl[MMA ? KWM : 1][4];
+        float2 ncorr[MMA ? KWM : 1];
+        float xv[MMA ? 1 : KWM][NRC][8];
+        float us0 = 1.f, us1 = 1.f;
+        if constexpr (MMA) {
+            float2 v[KWM][4];
+#pragma unroll
+            for (int j = 0; j < KWM; ++j) {
+                const float *xr = P.x + (int64_t)g * P.x_stride + (kt0 + wk0 + j) * 32 + 2 * c;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    v[j][q] = g < a.nr ? __ldcg(reinterpret_cast<const float2 *>(xr + (q >> 1) * 16 + (q & 1) * 8))
+                                       : make_float2(0.f, 0.f);
+            }
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < KWM; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(v[j][q].x), fabsf(v[j][q].y)));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const int ebits = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+            const int sexp = m > 0.f ? min(268 - ebits, 253) : 127;
+            const float sig = __uint_as_float((uint32_t)sexp << 23);
+            const float inv = __uint_as_float((uint32_t)(254 - sexp) << 23);
+#pragma unroll
+            for (int j = 0; j < KWM; ++j) {
+                float colsum = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float tx = v[j][q].x * sig, ty = v[j][q].y * sig;
+                    const __half2 hh = __floats2half2_rn(tx, ty);
+                    const float2 hf = __half22float2(hh);
+                    const __half2 ll = __floats2half2_rn(tx - hf.x, ty - hf.y);
+                    const float2 lf = __half22float2(ll);
+                    bh[j][q] = h2_bits(hh);
+                    bl[j][q] = h2_bits(ll);
+                    colsum += (hf.x + lf.x) + (hf.y + lf.y);
+                }
+                colsum += __shfl_xor_sync(0xffffffffu, colsum, 1);
+                colsum += __shfl_xor_sync(0xffffffffu, colsum, 2);
+                ncorr[j] = make_float2(-1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c),
+                                       -1152.f * __shfl_sync(0xffffffffu, colsum, 8 * c + 4));
+            }
+            us0 = __shfl_sync(0xffffffffu, inv, 8 * c);
+            us1 = __shfl_sync(0xffffffffu, inv, 8 * c + 4);
+        } else {
+#pragma unroll
+            for (int j = 0; j < KWM; ++j)
+#pragma unroll
+                for (int r = 0; r < NRC; ++r) {
+                    const float *xr = P.x + (int64_t)r * P.x_stride + (kt0 + wk0 + j) * 32 + 2 * c;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 t = r < a.nr ? __ldcg(reinterpret_cast<const float2 *>(xr + (q >> 1) * 16 + (q & 1) * 8))
+                                                  : make_float2(0.f, 0.f);
+                        xv[j][r][2 * q] = t.x;
+                        xv[j][r][2 * q + 1] = t.y;
+                    }
+                }
+        }
+        for (int b0 = 0; b0 < nrt && !bad; b0 += RB) {
+            const int nb = min(RB, nrt - b0);
+            float2 acc01[RB], acc23[RB];
+            float2 accg[RB][NRC], acch[RB][NRC];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                acc01[r] = acc23[r] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < NRC; ++q) accg[r][q] = acch[r][q] = make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                if (r >= nb) break;                                     // CTA-uniform
+                const int gi = base + b0 + r, st = gi % S;
+                const bool ok = __all_sync(0xffffffffu, dla::mbar_wait(&full[st], (uint32_t)((gi / S) & 1)));
+                if (!ok) bad = true;
+                const unsigned char *sw = ring + (size_t)st * SB;
+                const unsigned char *sd = sw + kChainKsl * 512;
+                if (ok) {
+#pragma unroll
+                    for (int j = 0; j < KWM; ++j) {
+                        const int kl = wk0 + j;
+                        const uint4 w = *reinterpret_cast<const uint4 *>(sw + kl * 512 + lane * 16);
+                        const __half2 sp = *reinterpret_cast<const __half2 *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4);
+                        const float2 dgh = __half22float2(sp);
+                        if constexpr (MMA) {
+                            float t[4] = {0.f, 0.f, 0.f, 0.f};
+                            const uint32_t a0 = u8x2_to_h2(w.x, 0x4140u), a1 = u8x2_to_h2(w.x, 0x4342u);
+                            const uint32_t a2 = u8x2_to_h2(w.y, 0x4140u), a3 = u8x2_to_h2(w.y, 0x4342u);
+                            mma16816(t, a0, a1, a2, a3, bh[j][0], bh[j][1]);
+                            mma16816(t, a0, a1, a2, a3, bl[j][0], bl[j][1]);
+                            const uint32_t a4 = u8x2_to_h2(w.z, 0x4140u), a5 = u8x2_to_h2(w.z, 0x4342u);
+                            const uint32_t a6 = u8x2_to_h2(w.w, 0x4140u), a7 = u8x2_to_h2(w.w, 0x4342u);
+                            mma16816(t, a4, a5, a6, a7, bh[j][2], bh[j][3]);
+                            mma16816(t, a4, a5, a6, a7, bl[j][2], bl[j][3]);
+                            acc01[r] = __ffma2_rn(make_float2(dgh.x, dgh.x), __fadd2_rn(make_float2(t[0], t[1]), ncorr[j]), acc01[r]);
+                            acc23[r] = __ffma2_rn(make_float2(dgh.y, dgh.y), __fadd2_rn(make_float2(t[2], t[3]), ncorr[j]), acc23[r]);
+                        } else {
+                            const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+                            float2 wg[4], wh[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                wg[q] = u8x2_to_f32x2(wd[q], 0);
+                                wh[q] = u8x2_to_f32x2(wd[q], 2);
+                            }
+#pragma unroll
+                            for (int q = 0; q < NRC; ++q) {
+                                float2 sg = __fmul2_rn(wg[0], make_float2(xv[j][q][0], xv[j][q][1]));
+                                float2 sh = __fmul2_rn(wh[0], make_float2(xv[j][q][0], xv[j][q][1]));
+#pragma unroll
+                                for (int u = 1; u < 4; ++u) {
+                                    const float2 xp = make_float2(xv[j][q][2 * u], xv[j][q][2 * u + 1]);
+                                    sg = __ffma2_rn(wg[u], xp, sg);
+                                    sh = __ffma2_rn(wh[u], xp, sh);
+                                }
+                                accg[r][q] = __ffma2_rn(make_float2(dgh.x, dgh.x), sg, accg[r][q]);
+                                acch[r][q] = __ffma2_rn(make_float2(dgh.y, dgh.y), sh, acch[r][q]);
+                            }
+                        }
+                    }
+                }
+                // the last warp done with this stage refills its slot, possibly with the next
+                // phase's weights
+                __syncwarp();
+                if (lane == 0 && atomicAdd(&s_cnt[st], 1) == kConsumers - 1) {
+                    s_cnt[st] = 0;
+                    if (gi + S < total) {
+                        issue(gi + S);
+                        s_issued = gi + S + 1;
+                    }
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                if (r >= nb) break;
+                float *rw = red + (r * kConsumers + warp) * 128;
+                if constexpr (MMA) {
+                    *reinterpret_cast<float2 *>(rw + g * 8 + 2 * c) = make_float2(acc01[r].x * us0, acc01[r].y * us1);
+                    *reinterpret_cast<float2 *>(rw + (g + 8) * 8 + 2 * c) = make_float2(acc23[r].x * us0, acc23[r].y * us1);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < NRC; ++q) {
+                        float vg = accg[r][q].x + accg[r][q].y, vh = acch[r][q].x + acch[r][q].y;
+                        vg += __shfl_xor_sync(0xffffffffu, vg, 1);
+                        vg += __shfl_xor_sync(0xffffffffu, vg, 2);
+                        vh += __shfl_xor_sync(0xffffffffu, vh, 1);
+                        vh += __shfl_xor_sync(0xffffffffu, vh, 2);
+                        if (c == 0) {
+                            rw[g * 8 + q] = vg;
+                            rw[(g + 8) * 8 + q] = vh;
+                        }
+                    }
+                }
+            }
+            if (__syncthreads_or(bad)) {
+                bad = true;
+                break;
+            }
+            // this slice's sums, four consecutive outputs of one activation row per thread, added
+            // into the phase's outputs
+            for (int e = threadIdx.x; e < nb * 32; e += kThreads) {
+                const int r = e >> 5, col = (e & 31) >> 2, o4 = (e & 3) * 4;
+                if (col >= a.nr) continue;
+                const float *rb = red + r * kConsumers * 128 + col;
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int w = 0; w < kConsumers; ++w)
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2) s4[i2] += rb[w * 128 + (o4 + i2) * 8];
+                const int o = (s_rt0[p] + b0 + r) * 16 + o4;
+                atomicAdd(reinterpret_cast<float4 *>(P.y + (int64_t)col * P.y_stride + o),
+                          make_float4(s4[0], s4[1], s4[2], s4[3]));
+            }
+        }
+    }
+    // a failure: leave no copy in flight (bounded waits on the stages issued last)
+    if (__syncthreads_or(bad) && threadIdx.x == 0) {
+        dl_status_or(a.status, DL_STATUS_SYNC_TIMEOUT);
+        const int hi = s_issued;
+        for (int j = max(0, hi - S); j < hi; ++j) dla::mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
+    }
+    // the next kernel may only launch now: before this, a later kernel's CTAs could take the slots
+    // of CTAs of this grid not yet resident, which the barriers wait for
+    dl_pdl_launch_dependents();
+}
+
 // ---------------------------------------------------------------- launch
 
 struct GemvCfg {
@@ -894,6 +1219,101 @@ int gemv_f16w_impl(const dl_f16_weight *W, const float *x, int rows, int64_t x_s
                     stream);
 }
 
+// Chained GEMVs: grid = the CTAs resident at once (the grid barriers need every CTA running).
+int gemv_chain_impl(const dl_q8_weight *const *W, const float *const *x, const int64_t *x_stride,
+                    float *const *y, const int64_t *y_stride, int nph, int rows, uint32_t *sync,
+                    int32_t *status, int path, dl_stream_t stream)
+{
+    dl::clear_error();
+    if (!W || !x || !x_stride || !y || !y_stride || !sync) return dl::fail(DL_E_ARG, "dl_gemv_q8_chain: null pointer");
+    if (nph < 1 || nph > kChainMaxPhases) return dl::fail(DL_E_ARG, "dl_gemv_q8_chain: %d phases", nph);
+    if (rows < 1 || rows > DL_MAX_ROWS) return dl::fail(DL_E_SHAPE, "dl_gemv_q8_chain: rows=%d (1..%d)", rows, DL_MAX_ROWS);
+    if (path < PATH_AUTO || path > PATH_TENSOR) return dl::fail(DL_E_ARG, "dl_gemv_q8_chain: path=%d", path);
+    const bool mma = path == PATH_TENSOR || (path == PATH_AUTO && rows > 2);
+    if (!mma && rows > 2) return dl::fail(DL_E_SHAPE, "dl_gemv_q8_chain: the CUDA-core path serves 1 or 2 rows");
+    if (!dl::aligned16(sync)) return dl::fail(DL_E_ALIGN, "dl_gemv_q8_chain: sync must be 16-byte aligned");
+    ChainArgs a{};
+    for (int p = 0; p < nph; ++p) {
+        const dl_q8_weight *w = W[p];
+        if (!w || !w->qs || !w->d || !x[p] || !y[p]) return dl::fail(DL_E_ARG, "dl_gemv_q8_chain: null pointer");
+        int rc = dl_q8_packed_size(w->n_out, w->n_in, nullptr, nullptr);
+        if (rc != DL_OK) return rc;
+        if (w->n_in % 1024 != 0 || w->n_out % 16 != 0)
+            return dl::fail(DL_E_SHAPE, "dl_gemv_q8_chain: phase %d is %lld x %lld (n_in a multiple of 1024, n_out of 16)",
+                            p, (long long)w->n_out, (long long)w->n_in);
+        if (x_stride[p] < w->n_in || y_stride[p] < w->n_out || x_stride[p] % 4 || y_stride[p] % 4)
+            return dl::fail(DL_E_ARG, "dl_gemv_q8_chain: phase %d strides", p);
+        if (!dl::aligned16(x[p]) || !dl::aligned16(y[p]) || !dl::aligned16(w->qs) || !dl::aligned16(w->d))
+            return dl::fail(DL_E_ALIGN, "dl_gemv_q8_chain: phase %d pointers must be 16-byte aligned", p);
+        ChainPhase &P = a.ph[p];
+        P.qs = static_cast<const unsigned char *>(w->qs);
+        P.d = static_cast<const unsigned char *>(w->d);
+        P.x = x[p];
+        P.y = y[p];
+        P.x_stride = x_stride[p];
+        P.y_stride = y_stride[p];
+        P.n_out = (int)w->n_out;
+        P.n_in = (int)w->n_in;
+        P.KT = (int)(w->n_in / 32);
+        P.RT = (int)(w->n_out / 16);
+        P.cs = P.KT / kChainKsl;
+    }
+    for (int p = 0; p < nph; ++p)
+        for (int q = 0; q < nph; ++q) {
+            const char *yb = reinterpret_cast<const char *>(a.ph[p].y), *xb = reinterpret_cast<const char *>(a.ph[q].x);
+            const char *ye = yb + ((size_t)(rows - 1) * a.ph[p].y_stride + a.ph[p].n_out) * 4;
+            const char *xe = xb + ((size_t)(rows - 1) * a.ph[q].x_stride + a.ph[q].n_in) * 4;
+            if (q <= p && xb < ye && yb < xe)
+                return dl::fail(DL_E_ARG, "dl_gemv_q8_chain: phase %d's output overlaps phase %d's input", p, q);
+        }
+    int sm = 0;
+    int rc = dl::device_sm_count(&sm);
+    if (rc != DL_OK) return rc;
+    const void *kern = mma ? reinterpret_cast<const void *>(gemv_chain_kernel<true, 1>)
+                           : rows == 1 ? reinterpret_cast<const void *>(gemv_chain_kernel<false, 1>)
+                                       : reinterpret_cast<const void *>(gemv_chain_kernel<false, 2>);
+    const size_t sb = (size_t)kChainKsl * kTileBytesQ8;
+    const int stages = std::min(kMaxStages, std::max(2, (int)(kRingBudget / sb)));
+    const size_t smem = (size_t)stages * sb + kRedBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8_chain: set shared memory");
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8_chain: shared-memory carveout");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        return dl::fail(DL_E_SHAPE, "dl_gemv_q8_chain: no CTA fits an SM");
+    }
+    per_sm = std::min(per_sm, 2);
+    const int G = per_sm * sm;
+    for (int p = 0; p < nph; ++p) {
+        ChainPhase &P = a.ph[p];
+        if (P.cs > G) return dl::fail(DL_E_SHAPE, "dl_gemv_q8_chain: phase %d needs %d K-slices", p, P.cs);
+        const int runs = G / P.cs;
+        P.rpr = (int)dl::ceil_div(P.RT, runs);
+    }
+    a.nph = nph;
+    a.nr = rows;
+    a.stages = stages;
+    a.sync = reinterpret_cast<unsigned *>(sync);
+    a.status = status;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)G);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    void *args[1] = {&a};
+    e = cudaLaunchKernelExC(&lc, kern, args);
+    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_gemv_q8_chain: launch");
+    return DL_OK;
+}
+
 // f16 weights [n_out][n_in] (row-major) to the tile form: one thread per 16 bytes, the half
 // `hf` of lane t's 32 bytes = words 4hf .. 4hf + 3; word m holds inputs kb, kb + 1
 // (kb = 16(p/2) + 8(p%2) + 2c, p = m/2) of row g + 8(m%2).  Out-of-range weights are zero.
@@ -966,6 +1386,13 @@ int dl_gemv_q8_ex(const dl_q8_weight *W, const float *x, int rows, int64_t x_str
                   float *y, int64_t y_stride, int path, dl_stream_t stream)
 {
     return gemv_impl(W, x, rows, x_stride, y, y_stride, path, stream);
+}
+
+int dl_gemv_q8_chain(const dl_q8_weight *const *W, const float *const *x, const int64_t *x_stride,
+                     float *const *y, const int64_t *y_stride, int n_phases, int rows,
+                     uint32_t *sync, int32_t *status, int path, dl_stream_t stream)
+{
+    return gemv_chain_impl(W, x, x_stride, y, y_stride, n_phases, rows, sync, status, path, stream);
 }
 
 int dl_f16w_packed_size(int64_t n_out, int64_t n_in, size_t *bytes)

@@ -9,7 +9,9 @@ most eight rows:
 or, with `fused_rope`, dl_decode_attn_rope in place of the rope/store and the
 attention (one launch fewer, the same stored halves and results); with
 `cluster_merge`, dl_decode_attn_cluster in place of the attention and the merge
-(the pieces of a KV head merge inside their thread-block cluster).
+(the pieces of a KV head merge inside their thread-block cluster); with
+`gemv_chain`, the O, gate/up and down projections as the phases of one
+dl_gemv_q8_chain launch.
 
 Norms, SwiGLU and residual adds are not part of the path: the gate/up and down
 projections read their own activation buffers (filled by the caller).  More
@@ -24,8 +26,8 @@ from typing import Dict, List, Optional, Sequence
 import torch
 
 from . import (KVCache, PackedQ8, Rope, dl_attn_merge, dl_attn_plan_build, dl_attn_plan_build_cluster,
-               dl_decode_attn, dl_decode_attn_cluster, dl_decode_attn_rope, dl_gemv_q8, dl_plan_groups,
-               dl_rope_kv_store, workspace_for)
+               dl_decode_attn, dl_decode_attn_cluster, dl_decode_attn_rope, dl_gemv_q8, dl_gemv_q8_chain,
+               dl_plan_groups, dl_rope_kv_store, workspace_for)
 
 
 @dataclasses.dataclass
@@ -46,12 +48,13 @@ class Command:
     def __init__(self, rows: Sequence[int], positions: Sequence[int], regions: Sequence[int],
                  n_q: int, n_kv: int, head_dim: int, hidden: int, ffn: int, device, sm_count: int = 0,
                  force_chunk: int = 0, gemv_path: int = 0, attn_path: int = 0, fused_rope: bool = False,
-                 cluster_merge: bool = False):
+                 cluster_merge: bool = False, gemv_chain: bool = False):
         n = len(rows)
         assert 1 <= n <= 8
         self.gemv_path, self.attn_path = gemv_path, attn_path
         self.fused_rope = bool(fused_rope)
         self.cluster_merge = bool(cluster_merge)
+        self.gemv_chain = bool(gemv_chain) and ffn > 0
         self.rows = list(rows)
         self.n = n
         D = head_dim
@@ -82,6 +85,7 @@ class Command:
         self.region = torch.tensor(self.regions, **i32)
         self.status = torch.zeros(1, **i32)
         self.workspace = workspace_for(self.plan, dev)
+        self.sync = torch.zeros(4, **i32)                    # the chain launch's barrier words
         qd, kd = n_q * D, n_kv * D
         self.q = self.qkv[:, :qd]
         self.k = self.qkv[:, qd:qd + kd]
@@ -110,6 +114,10 @@ class Command:
                            path=self.attn_path)
         if not self.cluster_merge:
             dl_attn_merge(self.workspace, self.plan, self.seqlen, self.attn, self.lse, stream=stream)
+        if self.gemv_chain and W.wgu is not None:
+            dl_gemv_q8_chain([W.wo, W.wgu, W.wdown], [self.attn, self.x_ffn, self.h], [self.y_o, self.gu, self.y_down],
+                             self.sync, status=self.status, stream=stream, path=gp)
+            return
         dl_gemv_q8(W.wo, self.attn, self.y_o, stream=stream, path=gp)
         if W.wgu is not None:
             dl_gemv_q8(W.wgu, self.x_ffn, self.gu, stream=stream, path=gp)
@@ -117,7 +125,7 @@ class Command:
 
     @property
     def launches(self) -> int:
-        return 7 - int(self.fused_rope) - int(self.cluster_merge)
+        return 7 - int(self.fused_rope) - int(self.cluster_merge) - 2 * int(self.gemv_chain)
 
 
 class LayerStep:
@@ -125,7 +133,8 @@ class LayerStep:
 
     def __init__(self, positions: Sequence[int], regions: Sequence[int], n_q: int, n_kv: int, head_dim: int,
                  hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0, gemv_path: int = 0,
-                 attn_path: int = 0, fused_rope: bool = False, cluster_merge: bool = False):
+                 attn_path: int = 0, fused_rope: bool = False, cluster_merge: bool = False,
+                 gemv_chain: bool = False):
         n = len(positions)
         sizes = dl_plan_groups(n)
         self.commands: List[Command] = []
@@ -134,7 +143,7 @@ class LayerStep:
             idx = list(range(r0, r0 + s))
             self.commands.append(Command(idx, [positions[i] for i in idx], [regions[i] for i in idx],
                                          n_q, n_kv, head_dim, hidden, ffn, device, sm_count, force_chunk,
-                                         gemv_path, attn_path, fused_rope, cluster_merge))
+                                         gemv_path, attn_path, fused_rope, cluster_merge, gemv_chain))
             r0 += s
         self.group_sizes = sizes
 

@@ -26,7 +26,8 @@ def dl():
     return m
 
 
-def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=False, cluster_merge=False):
+def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=False, cluster_merge=False,
+          gemv_chain=False):
     from row_decode_step_gb300.step import LayerStep, LayerWeights
     D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
     blocks = layer_blocks(S.name)
@@ -42,7 +43,7 @@ def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=Fals
     xf = synth.normal_f32(0, label + "/xf", (n, H)) if F else None
     h = synth.normal_f32(0, label + "/h", (n, F)) if F else None
     step = LayerStep(positions, regions, n_q, n_kv, D, H, F, "cuda", fused_rope=fused_rope,
-                     cluster_merge=cluster_merge)
+                     cluster_merge=cluster_merge, gemv_chain=gemv_chain)
     r0 = 0
     for c in step.commands:
         c.x.copy_(x[r0:r0 + c.n].cuda())
@@ -101,16 +102,18 @@ def test_step_1b(dl):
     _step(dl, synth.LLAMA_1B, [4096], [0], 1, 4097, "step/1b")
 
 
-@pytest.mark.parametrize("fused,cluster", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("fused,cluster,chain", [(False, False, False), (True, False, False), (True, True, False),
+                                                 (True, False, True)])
 @pytest.mark.parametrize("rows", [1, 8])
-def test_step_3b(dl, rows, fused, cluster):
+def test_step_3b(dl, rows, fused, cluster, chain):
     _step(dl, synth.LLAMA_3B, list(range(5120, 5120 + rows)), [0] * rows, 1, 5128, "step/3b%d" % rows,
-          fused_rope=fused, cluster_merge=cluster)
+          fused_rope=fused, cluster_merge=cluster, gemv_chain=chain)
 
 
-@pytest.mark.parametrize("fused,cluster", [(False, False), (True, False), (True, True)])
-def test_step_twelve_streams(dl, fused, cluster):
+@pytest.mark.parametrize("fused,cluster,chain", [(False, False, False), (True, False, False), (True, True, False),
+                                                 (True, False, True)])
+def test_step_twelve_streams(dl, fused, cluster, chain):
     lens = synth.twelve_stream_lengths(0)
     step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams", fused_rope=fused,
-                 cluster_merge=cluster)
+                 cluster_merge=cluster, gemv_chain=chain)
     assert step.group_sizes == [6, 6]
