@@ -47,6 +47,9 @@ def parse_args():
     p.add_argument("--workload", default="3b-8", choices=["3b-8", "3b-1", "3b-12", "1b-1", "3b-8-32k"])
     p.add_argument("--no-extras", action="store_true", help="skip the 1-row and 12-stream side measurements")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--side-only", action="store_true",
+                   help="only the side measurements (f16-weight GEMV, attention on each KV mirror), a few "
+                        "repetitions each: a small program for profilers")
     p.add_argument("--gemv-path", type=int, default=0, choices=[0, 1, 2],
                    help="inner product of the GEMVs: 0 library choice, 1 CUDA cores (<= 2 rows), 2 tensor cores")
     p.add_argument("--attn-path", type=int, default=0, choices=[0, 1, 2],
@@ -529,6 +532,13 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     dl.lib()
+    if args.side_only:
+        peak, _ = hbm_peak()
+        side = {"f16w_gemv": measure_f16w(dev, peak, mats=2, reps=2),
+                "attention_kv_mirrors": measure_attn_mirrors(dev, peak, caches=2, reps=2)}
+        if rank == 0:
+            print(json.dumps({"side_only": True, "side_workloads": side}))
+        return
 
     wl = workload(args.workload)
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path),
