@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode layer-steps/sec and achieved HBM GB/s (% of GB300 peak) at 1/8/12 rows"
 UNIT = "layer-steps/s"
 FALLBACK_HBM_GBS = 6800.0
+L2_CYCLE_BYTES = 260_000_000          # about twice the 129 MB L2: bytes one pass over cycled inputs exceeds
 
 
 def parse_args():
@@ -58,6 +59,9 @@ def parse_args():
                    help="1: the O, gate/up and down projections as the phases of one persistent launch")
     p.add_argument("--cluster-merge", type=int, default=0, choices=[0, 1],
                    help="1: the pieces of a KV head merge inside their thread-block cluster (no merge launch)")
+    p.add_argument("--l2-prefetch", type=int, default=0, choices=[0, 1],
+                   help="1: each launch asks L2 for the weights or keys of a later kernel while it runs "
+                        "(dl_l2_prefetch_next)")
     p.add_argument("--fused-rope", type=int, default=1, choices=[0, 1],
                    help="1: the rope/store runs inside the attention launch (dl_decode_attn_rope); "
                         "0: separate dl_rope_kv_store and dl_decode_attn launches")
@@ -227,7 +231,7 @@ def build_layers(wl, L, dev, seed=0):
 
 
 def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0), fused=False,
-            cluster=False, chain=False):
+            cluster=False, chain=False, prefetch=False):
     import synth
     import torch
     import row_decode_step_gb300 as dl
@@ -237,7 +241,7 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
     rope = dl.make_rope(S.rope_theta, S.head_dim, wl["capacity"], device=dev)
     step = LayerStep(wl["positions"], wl["regions"], S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, dev,
                      gemv_path=paths[0], attn_path=paths[1], fused_rope=fused, cluster_merge=cluster,
-                     gemv_chain=chain)
+                     gemv_chain=chain, l2_prefetch=prefetch)
     for i, c in enumerate(step.commands):
         c.x.copy_(synth.normal_f32(0, "bench/x%d" % i, tuple(c.x.shape), device=dev))
         if c.x_ffn is not None:
@@ -383,10 +387,14 @@ def measure_attn_mirrors(dev, peak, caches=4, reps=30):
     S = synth.LLAMA_3B
     cap, D = 5128, S.head_dim
     stream = torch.cuda.Stream(device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out = {}
     for name, dt in (("f16", torch.float16), ("f32", torch.float32), ("q8_0", torch.int8)):
+        eb = 4 if dt == torch.float32 else 34 / 32 if dt == torch.int8 else 2    # q8_0: codes + a scale per 32
+        # enough distinct caches that one pass over them exceeds L2 about twice
+        n_caches = max(caches, -(-L2_CYCLE_BYTES // int(S.n_kv * cap * D * 2 * eb)))
         kvs = []
-        for c in range(caches):
+        for c in range(n_caches):
             if dt == torch.int8:
                 kc, ks = synth.kv_q8_random_planes(0, "bench/mir/k%d" % c, 1, S.n_kv, cap, D, device=dev)
                 vc, vs = synth.kv_q8_random_planes(0, "bench/mir/v%d" % c, 1, S.n_kv, cap, D, device=dev)
@@ -397,7 +405,9 @@ def measure_attn_mirrors(dev, peak, caches=4, reps=30):
             kvs.append(dl.KVCache(k, v))
         for rows in (1, 8):
             seqlen = list(range(5121, 5121 + rows))
-            plan = dl.dl_attn_plan_build(seqlen, S.n_q, S.n_kv, D)
+            # the f32 mirror's ring holds one CTA per SM at D = 128: half the SMs' worth of pieces
+            plan = dl.dl_attn_plan_build(seqlen, S.n_q, S.n_kv, D,
+                                         sm_count=sms // 2 if dt == torch.float32 and D == 128 else 0)
             ws = dl.workspace_for(plan, dev)
             q = synth.normal_f32(0, "bench/mir/q%d" % rows, (rows, S.n_q * D), device=dev)
             sl = torch.tensor(seqlen, dtype=torch.int32, device=dev)
@@ -424,11 +434,11 @@ def measure_attn_mirrors(dev, peak, caches=4, reps=30):
                     g.replay()
                 k1.record(stream)
             torch.cuda.synchronize()
-            ms = k0.elapsed_time(k1) / (reps * caches)
-            eb = 4 if dt == torch.float32 else 34 / 32 if dt == torch.int8 else 2    # q8_0: codes + a scale per 32
+            ms = k0.elapsed_time(k1) / (reps * n_caches)
             b = int(max(seqlen) * S.n_kv * D * 2 * eb) + rows * S.n_q * D * 4 * 2
             out["%s_rows_%d" % (name, rows)] = {"attention_us": ms * 1e3, "achieved_gbs": b / (ms / 1e3) / 1e9,
-                                                 "frac": b / (ms / 1e3) / 1e9 / peak}
+                                                 "frac": b / (ms / 1e3) / 1e9 / peak, "caches_cycled": n_caches,
+                                                 "work_items": plan.n_work}
             del g
         del kvs
         torch.cuda.empty_cache()
@@ -542,7 +552,8 @@ def run_ours(args):
 
     wl = workload(args.workload)
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path),
-                  fused=bool(args.fused_rope), cluster=bool(args.cluster_merge), chain=bool(args.gemv_chain))
+                  fused=bool(args.fused_rope), cluster=bool(args.cluster_merge), chain=bool(args.gemv_chain),
+                  prefetch=bool(args.l2_prefetch))
     steps = args.steps
     ms, value = combine_ranks(res["ms_total"], steps, world, dev)
     step = res["step"]
@@ -559,7 +570,7 @@ def run_ours(args):
             r2 = measure(w2, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
                          want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
                          fused=bool(args.fused_rope), cluster=bool(args.cluster_merge),
-                         chain=bool(args.gemv_chain))
+                         chain=bool(args.gemv_chain), prefetch=bool(args.l2_prefetch))
             sb2 = step_bytes(w2, r2["step"])
             extras[name] = {"rows": len(w2["positions"]), "layer_steps_per_s": 1e3 / r2["ms_per_step"],
                             "ms_per_step": r2["ms_per_step"],
@@ -573,7 +584,7 @@ def run_ours(args):
         # the same step with the rope/store as its own launch (the other form of the path)
         r2 = measure(wl, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
                      want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
-                     fused=not args.fused_rope)
+                     fused=not args.fused_rope, prefetch=bool(args.l2_prefetch))
         extras["3b-8 rope %s" % ("separate" if args.fused_rope else "in attention")] = {
             "layer_steps_per_s": 1e3 / r2["ms_per_step"], "ms_per_step": r2["ms_per_step"],
             "algorithmic_gbs": sb / (r2["ms_per_step"] / 1e3) / 1e9,
@@ -603,6 +614,7 @@ def run_ours(args):
                    "attn_work_items": [c.plan.n_work for c in step.commands],
                    "gemv_path": args.gemv_path, "attn_path": args.attn_path,
                    "rope_in_attention": bool(args.fused_rope), "merge_in_cluster": bool(args.cluster_merge),
+                   "l2_prefetch": bool(args.l2_prefetch),
                    "gemv_chain": bool(args.gemv_chain)},
         "tokens_per_s": rows * value,
         "step": {"algorithmic_bytes": sb, "algorithmic_gbs": step_gbs, "hbm_frac": step_gbs / peak,

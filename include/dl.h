@@ -49,9 +49,11 @@
  *  [KVQ8] daScript PR #4293 ("_regions_q8kv" and the block-codec mirror): K and V
  *         kept as Q8_0 blocks of 32 values.  Here: per block the scale d = max|x| / 127
  *         (f32, stored as f16) and codes round(x / d) half away from zero, both decided
- *         in f32; the attention decodes d * code on CUDA cores (no tensor form, no
- *         rope fused into the attention).  Requires capacity % 4 == 0 and the
- *         region stride a multiple of 256 values (16-byte aligned scale rows).
+ *         in f32; the attention decodes d * code on CUDA cores, or on tensor cores
+ *         with the codes as exact f16 operands, each key's block scale applied to
+ *         its 32-dimension score sums (f32) and to the V operand (rounded once to
+ *         f16); no rope fused into the attention.  Requires capacity % 4 == 0 and
+ *         the region stride a multiple of 256 values (16-byte aligned scale rows).
  *  [ROPE] daScript PR #4293 "dasLLAMA llama leg ...", commit "The decode
  *         rope-and-store rides one template on both homes" (GkRopeKvStore).
  *  [GRP]  the same PR, commit "The Vulkan batched step past eight rows runs in
@@ -102,6 +104,31 @@ int dl_version(void);
  * debug use).  Returns DL_OK and stores the word, or DL_E_CUDA.
  */
 int dl_status_read(const int32_t *status_dev, int32_t *host_out);
+
+/*
+ * L2 prefetch on behalf of a later kernel.  No page defines this: it is a
+ * scheduling hint of this library.  The decode step's launches are latency
+ * bound, so HBM idles while they run.  The step can use that time to bring the
+ * weights or keys of the kernels after them into L2.
+ *
+ * The next launching call this host thread makes among dl_gemv_q8,
+ * dl_gemv_q8_ex, dl_gemv_f16w, dl_gemv_f16w_ex, dl_rope_kv_store, dl_decode_attn,
+ * dl_decode_attn_ex, dl_decode_attn_rope, dl_decode_attn_cluster and
+ * dl_attn_merge takes the ranges, whether or not it launches.  Its kernel then
+ * splits them over its CTAs and issues bulk L2 prefetches for them before
+ * waiting on the previous kernel.
+ *
+ *   n       0..16 ranges (0 clears what is pending)
+ *   ptrs    host array of n device pointers, each 16-byte aligned
+ *   bytes   host array of n sizes, each a multiple of 16 (0 skips the range)
+ *
+ * Results do not change.  The ranges must lie inside live device allocations
+ * until that kernel ends; the library keeps no reference past it.  A new call
+ * replaces what is pending.
+ * Errors: DL_E_ARG (n out of range, null arrays), DL_E_ALIGN (a range breaks
+ * the 16-byte rule); either leaves nothing pending.  Host only, no CUDA call.
+ */
+int dl_l2_prefetch_next(int n, const void *const *ptrs, const size_t *bytes);
 
 /* ------------------------------------------------------------ Q8_0 weights
  *
@@ -380,7 +407,8 @@ int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv,
  * measurement): path 0 = automatic (what dl_decode_attn does: CUDA cores when a
  * work item serves at most 4 queries, tensor cores above), 1 = f32 CUDA-core
  * dot products, 2 = 16x8x16 f16 tensor-core products with q split into two f16
- * terms (hi + lo) and probabilities in f16, f32 accumulation and softmax.
+ * terms (hi + lo) and probabilities in f16, f32 accumulation and softmax.  The
+ * f32 mirror refuses path 2 (DL_E_SHAPE) and takes path 1 whatever path 0 sees.
  */
 int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv,
                       const int32_t *seqlen, const dl_attn_plan *plan,

@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
             "dl_last_error": ([], ctypes.c_char_p),
             "dl_version": ([], I),
             "dl_status_read": ([P, P], I),
+            "dl_l2_prefetch_next": ([I, P, P], I),
             "dl_q8_packed_size": ([I64, I64, P, P], I),
             "dl_q8_pack": ([P, I64, I64, P, P, P], I),
             "dl_gemv_q8": ([P, P, I, I64, P, I64, P], I),
@@ -466,6 +467,24 @@ def dl_attn_merge(workspace: torch.Tensor, plan: dl_attn_plan, seqlen: torch.Ten
     _dev(out, torch.float32, "out")
     _check(lib().dl_attn_merge(_ptr(workspace), ctypes.byref(plan), _ptr(seqlen), _ptr(out), out.stride(0),
                                _ptr(lse), _stream(stream)))
+
+
+def dl_l2_prefetch_next(ranges) -> None:
+    """Byte ranges the next launching call of this thread asks L2 to fetch for a later kernel:
+    each a device tensor (its elements) or a (device pointer, bytes) pair."""
+    ptrs, sizes = [], []
+    for r in ranges:
+        if isinstance(r, torch.Tensor):
+            if not r.is_cuda or not r.is_contiguous():
+                raise ValueError("dl_l2_prefetch_next: ranges must be contiguous device tensors")
+            ptrs.append(r.data_ptr())
+            sizes.append(r.numel() * r.element_size())
+        else:
+            ptrs.append(int(r[0]))
+            sizes.append(int(r[1]))
+    n = len(ptrs)
+    _check(lib().dl_l2_prefetch_next(n, (ctypes.c_void_p * max(1, n))(*ptrs),
+                                     (ctypes.c_size_t * max(1, n))(*sizes)))
 
 
 def dl_status_read(status: torch.Tensor) -> int:

@@ -55,6 +55,7 @@ struct AttnArgs {
     // merge inside the launch (plan.cluster = C > 0): the results go straight to out / lse_out
     float *out, *lse_out;
     int64_t out_stride;
+    DlPrefetch pf;       // L2 prefetches for a later kernel (the producer issues its share)
 };
 
 // Signed bytes `lo`, `lo + 1` of w to floats: the byte flipped to u = q + 128 sits in the low
@@ -65,6 +66,16 @@ __device__ __forceinline__ float2 s8x2_to_f32x2(uint32_t w, uint32_t lo)
     const float2 b = make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | lo)),
                                  __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541u | lo)));
     return __fadd2_rn(b, make_float2(-8388736.0f, -8388736.0f));
+}
+
+// Two signed codes as an f16 pair for the tensor form: `t` holds them flipped to u = q + 128 in
+// bytes 0 and 2; with 0x64 above each, the halves read 1024 + u = 1152 + q, and one exact
+// subtraction of 1152 leaves q.
+__device__ __forceinline__ uint32_t q8_pair_h2(uint32_t t)
+{
+    const uint32_t b = (t & 0x00FF00FFu) ^ 0x64806480u;         // bytes 1, 3 <- 0x64; u = q ^ 0x80
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&b), __half2half2(__ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 __device__ __forceinline__ unsigned short attn_half_clamped(float v)
@@ -210,8 +221,9 @@ __device__ __forceinline__ bool attn_consumers_any(bool flag)
 }
 
 // EB: bytes per element of the mirror: 2 the f16 mirror, 4 the f32 mirror, 1 the q8_0 mirror
-// (codes; the scales ride along). The f32 and q8_0 mirrors take the CUDA-core form only, since
-// the tensor form reads f16 operands.
+// (codes; the scales ride along). The f32 mirror takes the CUDA-core form only, since the
+// tensor form reads f16 operands; the q8_0 codes are exact f16 operands, with each key's block
+// scales applied to the score sums and to the V operand.
 template <int D, bool MMA, int QM, int EB = 2>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tk,
@@ -219,7 +231,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
 {
     constexpr int NKS = D / 16;     // k-steps of the score product
     constexpr int NDT = D / 8;      // 8-wide column tiles of the output
-    static_assert(!(MMA && EB != 2), "the tensor form reads the f16 mirror");
+    static_assert(!(MMA && EB == 4), "the tensor form reads f16 values or q8_0 codes");
     constexpr bool KV32 = EB == 4, KVQ8 = EB == 1;
     constexpr int EPB = KVQ8 ? D : 128 / EB;  // elements per box row (q8_0: the whole key row)
     constexpr int NH = D / EPB;               // boxes per key row
@@ -375,6 +387,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         asm volatile("fence.proxy.async.global;" ::: "memory");
     };
     if (producer && idle) {
+        if (lane == 0 && a.pf.n > 0) dl_issue_prefetch(a.pf);
         dl_pdl_wait();
         dl_pdl_launch_dependents();
         if (P.cluster) {                                 // the group's two cluster barriers
@@ -432,6 +445,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                         dla::bulk_g2s(s_cs + i * rh, a.cs + (size_t)s_pos[i] * rh, (uint32_t)rh * 8u, &csbar);
             }
             for (int i = 0; i < npre; ++i) issue_stage(i);      // npre <= S: every slot is free
+            if (a.pf.n > 0) dl_issue_prefetch(a.pf);
         }
         dl_pdl_wait();
         if (lane == 0) issue_queries();
@@ -582,7 +596,11 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     float *cl = cm + kMmaConsumers * 16;
     if constexpr (MMA) {
         // ---- query operand fragments (log2-domain scaled, hi + lo f16 terms) in shared memory:
-        // [query tile][k-step][hi, lo][lane] 16 bytes = a0..a3
+        // [query tile][k-step][hi, lo][lane] 16 bytes = a0..a3.  On the q8_0 mirror the
+        // dimensions are permuted within each 32-dimension block (the order of a sum is free when
+        // both operands follow it): k-step 2b + e, column pair p of lane quad c holds dimensions
+        // 32b + 8c + 4e + 2p + {0, 1}, so that a key's codes of both k-steps of block b are the 8
+        // contiguous bytes at 32b + 8c of its row
         const bool qok = __all_sync(0xffffffffu, dla::mbar_wait(&qbar, 0u));
         if (!qok) bad = true;
         rotate_queries(qok);
@@ -596,7 +614,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     #pragma unroll
             for (int part = 0; part < 4; ++part) {
                 const float *src = (part & 1) ? q1 : q0;
-                const int col = ks * 16 + 2 * cc + (part >> 1) * 8;
+                const int col = KVQ8 ? 32 * (ks >> 1) + 8 * cc + 4 * (ks & 1) + (part >> 1) * 2
+                                     : ks * 16 + 2 * cc + (part >> 1) * 8;
                 float2 v = make_float2(0.f, 0.f);
                 if (src) v = *reinterpret_cast<const float2 *>(src + col);
                 v.x *= a.qscale;
@@ -631,12 +650,21 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             const uint32_t vsm = ksm + kVOff;
             const int kb0 = k0 + i * kStKeys;
             if (kb0 + kStKeys > k1) {
-                // keys past the piece may hold anything (even NaN) in the V rows: zero them
-                unsigned char *vrow = ring + (size_t)st * kStageBytes + kStageBytes / 2;
-                for (int e = lane; e < NH * kStKeys * 8; e += 32) {
-                    const int hf = e / (kStKeys * 8), rem = e - hf * kStKeys * 8;
-                    const int key = rem >> 3;
-                    if (kb0 + key >= k1) *reinterpret_cast<uint4 *>(vrow + hf * kHalfTile + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
+                // keys past the piece may hold anything (even NaN) in the V rows: zero them (the
+                // q8_0 mirror's codes are finite; zeroing their scales is enough)
+                if constexpr (KVQ8) {
+                    uint16_t *vs = reinterpret_cast<uint16_t *>(ring + (size_t)st * kStageBytes + 2 * kCodeBytes +
+                                                                kScaleBytes);
+                    for (int e = lane; e < kStKeys * (D / 32); e += 32)
+                        if (kb0 + e / (D / 32) >= k1) vs[e] = 0;
+                } else {
+                    unsigned char *vrow = ring + (size_t)st * kStageBytes + kStageBytes / 2;
+                    for (int e = lane; e < NH * kStKeys * 8; e += 32) {
+                        const int hf = e / (kStKeys * 8), rem = e - hf * kStKeys * 8;
+                        const int key = rem >> 3;
+                        if (kb0 + key >= k1)
+                            *reinterpret_cast<uint4 *>(vrow + hf * kHalfTile + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 dla::fence_proxy_async();
                 __syncwarp();
@@ -649,6 +677,45 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
                 sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
             }
+            if constexpr (KVQ8) {
+                // per 32-dimension block b: lane (g, c) takes key g's 8 codes at 32b + 8c (both
+                // k-steps of the block), the block's products accumulate apart and are scaled by
+                // the key's scale of that block (the columns 2c, 2c + 1 of the fragment)
+                const unsigned char *kcs = ring + (size_t)st * kStageBytes;
+                const uint16_t *ksc = reinterpret_cast<const uint16_t *>(kcs + 2 * kCodeBytes);
+    #pragma unroll
+                for (int b = 0; b < D / 32; ++b) {
+                    const uint4 qa = *reinterpret_cast<const uint4 *>(myq + (2 * b) * 1024);
+                    const uint4 qb = *reinterpret_cast<const uint4 *>(myq + (2 * b) * 1024 + 512);
+                    const uint4 qc = *reinterpret_cast<const uint4 *>(myq + (2 * b + 1) * 1024);
+                    const uint4 qd = *reinterpret_cast<const uint4 *>(myq + (2 * b + 1) * 1024 + 512);
+                    const uint32_t qh0[4] = {qa.x, qa.y, qa.z, qa.w}, ql0[4] = {qb.x, qb.y, qb.z, qb.w};
+                    const uint32_t qh1[4] = {qc.x, qc.y, qc.z, qc.w}, ql1[4] = {qd.x, qd.y, qd.z, qd.w};
+                    const int byte = 32 * b + 8 * c, ch = byte >> 4;
+    #pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const int key = nt * 8 + g;
+                        const uint2 w = *reinterpret_cast<const uint2 *>(
+                            kcs + key * kRowB + ((kSwz ? (ch ^ (key & 7)) : ch) << 4) + (byte & 8));
+                        const uint32_t b0 = q8_pair_h2(__byte_perm(w.x, 0u, 0x3120u));   // dims +0, +1
+                        const uint32_t b1 = q8_pair_h2(__byte_perm(w.x, 0u, 0x1302u));   // dims +2, +3
+                        const uint32_t b2 = q8_pair_h2(__byte_perm(w.y, 0u, 0x3120u));
+                        const uint32_t b3 = q8_pair_h2(__byte_perm(w.y, 0u, 0x1302u));
+                        float th[4] = {0.f, 0.f, 0.f, 0.f}, tl[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_f16(th, qh0, b0, b1);
+                        mma_f16(tl, ql0, b0, b1);
+                        mma_f16(th, qh1, b2, b3);
+                        mma_f16(tl, ql1, b2, b3);
+                        const int kc0 = nt * 8 + 2 * c;
+                        const float d0 = __half2float(__ushort_as_half(ksc[kc0 * (D / 32) + b]));
+                        const float d1 = __half2float(__ushort_as_half(ksc[(kc0 + 1) * (D / 32) + b]));
+                        sc[nt][0] = fmaf(d0, th[0] + tl[0], sc[nt][0]);
+                        sc[nt][1] = fmaf(d1, th[1] + tl[1], sc[nt][1]);
+                        sc[nt][2] = fmaf(d0, th[2] + tl[2], sc[nt][2]);
+                        sc[nt][3] = fmaf(d1, th[3] + tl[3], sc[nt][3]);
+                    }
+                }
+            } else
     #pragma unroll
             for (int ks = 0; ks < NKS; ks += 2) {
                 const uint4 qa = *reinterpret_cast<const uint4 *>(myq + ks * 1024);
@@ -717,6 +784,53 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 }
             }
             // O += P V over two 16-key steps: two 8-wide output tiles per transposed 4-matrix load
+            if constexpr (KVQ8) {
+                // output column n of tile j is dimension (D / 8) n + j, so that lane (g, c) reads
+                // the D / 8 contiguous codes at (D / 8) g of its keys 2c, 2c + 1, 2c + 8, 2c + 9 (all
+                // in block g / (256 / D)) and takes byte j of them for tile j; each pair is scaled
+                // by its keys' scales of that block as it becomes an f16 operand
+                const unsigned char *vcs = ring + (size_t)st * kStageBytes + kCodeBytes;
+                const uint16_t *vsc =
+                    reinterpret_cast<const uint16_t *>(ring + (size_t)st * kStageBytes + 2 * kCodeBytes + kScaleBytes);
+                constexpr int VB = D / 8;                 // codes per lane and key
+                const int blk = (VB * g) >> 5;
+    #pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint32_t pa[4] = {h2_bits(sc[2 * kk][0], sc[2 * kk][1]), h2_bits(sc[2 * kk][2], sc[2 * kk][3]),
+                                            h2_bits(sc[2 * kk + 1][0], sc[2 * kk + 1][1]),
+                                            h2_bits(sc[2 * kk + 1][2], sc[2 * kk + 1][3])};
+                    uint32_t wv[4][VB / 4];
+                    __half2 dv[2];
+    #pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int key = kk * 16 + 2 * c + (u & 1) + (u >> 1) * 8;
+                        const unsigned char *row = vcs + key * kRowB;
+                        if constexpr (VB == 16) {
+                            const uint4 w = *reinterpret_cast<const uint4 *>(row + ((kSwz ? (g ^ (key & 7)) : g) << 4));
+                            wv[u][0] = w.x; wv[u][1] = w.y; wv[u][2] = w.z; wv[u][3] = w.w;
+                        } else {
+                            const uint2 w = *reinterpret_cast<const uint2 *>(row + VB * g);
+                            wv[u][0] = w.x; wv[u][1] = w.y;
+                        }
+                    }
+    #pragma unroll
+                    for (int u2 = 0; u2 < 2; ++u2) {
+                        const int key = kk * 16 + 2 * c + u2 * 8;
+                        dv[u2] = __halves2half2(__ushort_as_half(vsc[key * (D / 32) + blk]),
+                                                __ushort_as_half(vsc[(key + 1) * (D / 32) + blk]));
+                    }
+    #pragma unroll
+                    for (int j = 0; j < NDT; ++j) {
+                        const uint32_t sel = (uint32_t)(j & 3) | ((uint32_t)(4 + (j & 3)) << 8);
+                        uint32_t b01 = q8_pair_h2(__byte_perm(wv[0][j >> 2], wv[1][j >> 2], sel));
+                        uint32_t b23 = q8_pair_h2(__byte_perm(wv[2][j >> 2], wv[3][j >> 2], sel));
+                        const __half2 v01 = __hmul2(*reinterpret_cast<const __half2 *>(&b01), dv[0]);
+                        const __half2 v23 = __hmul2(*reinterpret_cast<const __half2 *>(&b23), dv[1]);
+                        mma_f16(o[j], pa, *reinterpret_cast<const uint32_t *>(&v01),
+                                *reinterpret_cast<const uint32_t *>(&v23));
+                    }
+                }
+            } else
     #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const uint32_t pa[4] = {h2_bits(sc[2 * kk][0], sc[2 * kk][1]), h2_bits(sc[2 * kk][2], sc[2 * kk][3]),
@@ -748,8 +862,17 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         }
     #pragma unroll
         for (int j = 0; j < NDT; ++j) {
-            *reinterpret_cast<float2 *>(co + (warp * 16 + g) * CP + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
-            *reinterpret_cast<float2 *>(co + (warp * 16 + g + 8) * CP + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
+            if constexpr (KVQ8) {                    // column n of tile j is dimension (D / 8) n + j
+                const int d0 = (D / 8) * 2 * c + j, d1 = d0 + D / 8;
+                co[(warp * 16 + g) * CP + d0] = o[j][0];
+                co[(warp * 16 + g) * CP + d1] = o[j][1];
+                co[(warp * 16 + g + 8) * CP + d0] = o[j][2];
+                co[(warp * 16 + g + 8) * CP + d1] = o[j][3];
+            } else {
+                *reinterpret_cast<float2 *>(co + (warp * 16 + g) * CP + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
+                *reinterpret_cast<float2 *>(co + (warp * 16 + g + 8) * CP + j * 8 + 2 * c) =
+                    make_float2(o[j][2], o[j][3]);
+            }
         }
         if (c == 0) {
             cm[warp * 16 + g] = m0;
@@ -1053,6 +1176,7 @@ struct MergeArgs {
     int64_t out_stride;
     int rows, n_q, chunk, max_splits, capacity;
     int row_keys_max[DL_MAX_ROWS];
+    DlPrefetch pf;       // L2 prefetches for a later kernel
 };
 
 // One CTA per (row, head); its eight warps take every eighth piece and issue the loads of
@@ -1067,6 +1191,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const __gr
     constexpr int VPL = D / 32;              // values per lane
     __shared__ float s_acc[kMergeWarps][D];
     __shared__ float s_m[kMergeWarps], s_w[kMergeWarps];
+    if (threadIdx.x == 0 && a.pf.n > 0) dl_issue_prefetch(a.pf);
     dl_pdl_wait();
     dl_pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1195,6 +1320,19 @@ int check_plan(const dl_attn_plan *P)
         P->n_kv < 1 || P->n_q % P->n_kv != 0 || (P->head_dim != 64 && P->head_dim != 128))
         return dl::fail(DL_E_ARG, "dl attention: invalid plan");
     return DL_OK;
+}
+
+using AttnKernel = void (*)(AttnArgs, CUtensorMap, CUtensorMap);
+
+// The instantiation for a head dimension and mirror: the tensor form (f16 and q8_0 mirrors), or
+// the CUDA-core form with qm queries per warp.
+template <int D, int EB>
+AttnKernel pick_attn_kernel(bool mma, int qm)
+{
+    if constexpr (EB != 4)
+        if (mma) return decode_attn_tma_kernel<D, true, 8, EB>;
+    return qm == 4 ? decode_attn_tma_kernel<D, false, 4, EB>
+         : qm == 6 ? decode_attn_tma_kernel<D, false, 6, EB> : decode_attn_tma_kernel<D, false, 8, EB>;
 }
 
 }  // namespace
@@ -1358,6 +1496,8 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
                             const ClusterOut *co = nullptr)
 {
     dl::clear_error();
+    DlPrefetch pf;
+    dl::take_prefetch(&pf);
     if (!q || !kv || !kv->k || !kv->v || !seqlen || (!co && !workspace))
         return dl::fail(DL_E_ARG, "dl_decode_attn: null pointer");
     int rc = check_plan(plan);
@@ -1423,6 +1563,7 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     a.status = status;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)plan->head_dim));
     a.plan = *plan;
+    a.pf = pf;
     if (f) {
         const int D = plan->head_dim;
         if (!f->k || !f->v || !f->pos || !f->rope || !f->rope->cos_sin)
@@ -1451,10 +1592,12 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     int qmax = 0;
     for (int si = 0; si < plan->n_sessions; ++si)
         qmax = std::max(qmax, (plan->sess_begin[si + 1] - plan->sess_begin[si]) * (plan->n_q / plan->n_kv));
-    // the f32 and q8_0 mirrors are read on CUDA cores (the tensor form takes f16 operands)
+    // the f32 mirror is read on CUDA cores only (the tensor form takes f16 operands; q8_0 codes
+    // are exact in f16)
     const int eb = kv->elem_bytes == 0 ? 2 : kv->elem_bytes;
-    if (eb != 2 && path == 2) return dl::fail(DL_E_SHAPE, "dl_decode_attn: the tensor form reads the f16 mirror only");
-    const bool mma = eb == 2 && (path == 2 || (path == 0 && qmax > kCudaCoreMaxQ));
+    if (eb == 4 && path == 2)
+        return dl::fail(DL_E_SHAPE, "dl_decode_attn: the tensor form reads the f16 and q8_0 mirrors only");
+    const bool mma = eb != 4 && (path == 2 || (path == 0 && qmax > kCudaCoreMaxQ));
     a.ksc = static_cast<const uint16_t *>(kv->k_scale);
     a.vsc = static_cast<const uint16_t *>(kv->v_scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1464,19 +1607,13 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     rc = make_kv_tmap(&tv, kv->v, kv);
     if (rc != DL_OK) return rc;
     const size_t smem = attn_mma_smem_bytes(plan->head_dim, eb);
-    // the CUDA-core form holds the queries of a warp in registers: 4 for one-row sessions, else 8
-    const bool few = qmax <= 4;
-    auto kern = eb == 4 ? (plan->head_dim == 128
-                            ? (few ? decode_attn_tma_kernel<128, false, 4, 4> : decode_attn_tma_kernel<128, false, 8, 4>)
-                            : (few ? decode_attn_tma_kernel<64, false, 4, 4> : decode_attn_tma_kernel<64, false, 8, 4>))
-         : eb == 1 ? (plan->head_dim == 128
-                            ? (few ? decode_attn_tma_kernel<128, false, 4, 1> : decode_attn_tma_kernel<128, false, 8, 1>)
-                            : (few ? decode_attn_tma_kernel<64, false, 4, 1> : decode_attn_tma_kernel<64, false, 8, 1>))
-         : plan->head_dim == 128
-                    ? (mma ? decode_attn_tma_kernel<128, true, 8>
-                           : few ? decode_attn_tma_kernel<128, false, 4> : decode_attn_tma_kernel<128, false, 8>)
-                    : (mma ? decode_attn_tma_kernel<64, true, 8>
-                           : few ? decode_attn_tma_kernel<64, false, 4> : decode_attn_tma_kernel<64, false, 8>);
+    // the CUDA-core form holds the queries of a warp in registers: 4 for one-row sessions; 6 when
+    // a work item serves 17..24 queries (four query groups keep all four consumer warps busy,
+    // where groups of 8 would leave one idle); else 8
+    const int qm = qmax <= 4 ? 4 : (qmax > 16 && qmax <= 24) ? 6 : 8;
+    auto kern = eb == 4 ? (plan->head_dim == 128 ? pick_attn_kernel<128, 4>(false, qm) : pick_attn_kernel<64, 4>(false, qm))
+              : eb == 1 ? (plan->head_dim == 128 ? pick_attn_kernel<128, 1>(mma, qm) : pick_attn_kernel<64, 1>(mma, qm))
+                        : (plan->head_dim == 128 ? pick_attn_kernel<128, 2>(mma, qm) : pick_attn_kernel<64, 2>(mma, qm));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
     if (!co)
@@ -1553,6 +1690,8 @@ int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t
                   float *out, int64_t out_stride, float *lse, dl_stream_t stream)
 {
     dl::clear_error();
+    MergeArgs m{};
+    dl::take_prefetch(&m.pf);
     if (!workspace || !seqlen || !out) return dl::fail(DL_E_ARG, "dl_attn_merge: null pointer");
     int rc = check_plan(plan);
     if (rc != DL_OK) return rc;
@@ -1560,7 +1699,6 @@ int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t
     if (out_stride < (int64_t)plan->n_q * plan->head_dim) return dl::fail(DL_E_ARG, "dl_attn_merge: out_stride too small");
     if (!dl::aligned16(out) || (out_stride % 4) != 0 || !dl::aligned16(workspace))
         return dl::fail(DL_E_ALIGN, "dl_attn_merge: out and workspace must be 16-byte aligned");
-    MergeArgs m{};
     const size_t po = (size_t)plan->rows * plan->n_q * plan->max_splits * plan->head_dim * 4;
     m.part_o = static_cast<const float *>(workspace);
     m.part_lse = reinterpret_cast<const float *>(static_cast<const char *>(workspace) + ((po + 15) / 16) * 16);

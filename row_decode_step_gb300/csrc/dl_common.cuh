@@ -27,6 +27,22 @@ int device_sm_count(int *out);
 // Check the launch that was just issued; returns DL_OK or DL_E_CUDA.
 int check_launch(const char *what);
 
+}  // namespace dl
+
+// Byte ranges a launch asks L2 to fetch on behalf of a later kernel (dl_l2_prefetch_next): every
+// pointer 16-byte aligned, every size a multiple of 16.
+constexpr int kMaxPrefetch = 16;
+struct DlPrefetch {
+    const char *p[kMaxPrefetch];
+    uint64_t bytes[kMaxPrefetch];
+    int n;
+};
+
+namespace dl {
+
+// Move the calling thread's pending prefetch ranges into `out` (n = 0 if none) and clear them.
+void take_prefetch(DlPrefetch *out);
+
 
 // Launch `kern` on `st` as a programmatic dependent of the previous kernel in the
 // stream (it may start before that kernel ends and must call dl_pdl_wait()
@@ -63,6 +79,25 @@ __device__ __forceinline__ void dl_pdl_launch_dependents() { asm volatile("gridd
 __device__ __forceinline__ void dl_prefetch_l2(const void *p, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Device side: this CTA's share of every prefetch range (ranges split evenly over the grid in
+// 16-byte units, at most 64 KB per request); one thread per CTA calls it.
+__device__ __forceinline__ void dl_issue_prefetch(const DlPrefetch &pf)
+{
+    const uint64_t nb = (uint64_t)gridDim.x * gridDim.y * gridDim.z;
+    const uint64_t b = blockIdx.x + (uint64_t)gridDim.x * (blockIdx.y + (uint64_t)gridDim.y * blockIdx.z);
+    for (int i = 0; i < pf.n; ++i) {
+        const uint64_t total = pf.bytes[i];
+        const uint64_t per = ((total + nb - 1) / nb + 15) & ~(uint64_t)15;
+        uint64_t off = per * b;
+        const uint64_t end = off + per < total ? off + per : total;
+        while (off < end) {
+            const uint32_t len = (uint32_t)(end - off < 65536 ? end - off : 65536);
+            dl_prefetch_l2(pf.p[i] + off, len);
+            off += len;
+        }
+    }
 }
 
 // Device side: OR bits into a status word (no trap, no assert).

@@ -60,6 +60,7 @@ struct GemvArgs {
     int rpr;                // row tiles per CTA
     int stages;             // ring depth
     int pre;                // ring stages requested before waiting on the previous kernel
+    DlPrefetch pf;          // L2 prefetches for a later kernel, issued after those stages
 };
 
 constexpr int kConsumers = 8;                        // warps, each a share of the K-slice
@@ -167,8 +168,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     // the weights do not depend on the previous kernel: the first stages are requested before
     // waiting on it, the rest once the activations are requested (an SM's requests are served
     // roughly in order, and the activations gate every stage)
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         for (int j = 0; j < a.pre && j < S && j < nrt; ++j) issue(j);
+        if (a.pf.n > 0) dl_issue_prefetch(a.pf);
+    }
     auto issue_rest = [&]() {
         if (threadIdx.x == 0)
             for (int j = a.pre; j < S && j < nrt; ++j) issue(j);
@@ -1150,7 +1153,8 @@ int gemv_group(GemvArgs a, bool w16, int nr, int sm, int path, cudaStream_t st)
 
 // Shared launch path of both weight kinds (the caller has checked the matrix shape).
 int gemv_run(const char *name, const void *wq, const void *wd, int64_t n_out, int64_t n_in, bool w16,
-             const float *x, int rows, int64_t x_stride, float *y, int64_t y_stride, int path, dl_stream_t stream)
+             const float *x, int rows, int64_t x_stride, float *y, int64_t y_stride, int path, dl_stream_t stream,
+             const DlPrefetch &pf)
 {
     if (!x || !y) return dl::fail(DL_E_ARG, "%s: null pointer", name);
     if (rows < 0) return dl::fail(DL_E_ARG, "%s: rows=%d", name, rows);
@@ -1179,6 +1183,7 @@ int gemv_run(const char *name, const void *wq, const void *wd, int64_t n_out, in
     a.KT = (int)(dl::ceil_div(n_in, 128) * 4);
     a.RT = (int)dl::ceil_div(n_out, 16);
 
+    a.pf = pf;                                 // the first command's launch issues them
     int sizes[64];
     int done = 0;
     while (done < rows) {
@@ -1191,6 +1196,7 @@ int gemv_run(const char *name, const void *wq, const void *wd, int64_t n_out, in
             a.y = y + (size_t)done * y_stride;
             rc = gemv_group(a, w16, sizes[gi], sm, path, static_cast<cudaStream_t>(stream));
             if (rc != DL_OK) return rc;
+            a.pf.n = 0;
             done += sizes[gi];
         }
     }
@@ -1201,22 +1207,26 @@ int gemv_impl(const dl_q8_weight *W, const float *x, int rows, int64_t x_stride,
               int path, dl_stream_t stream)
 {
     dl::clear_error();
+    DlPrefetch pf;
+    dl::take_prefetch(&pf);
     if (!W || !W->qs || !W->d) return dl::fail(DL_E_ARG, "dl_gemv_q8: null pointer");
     const int rc = dl_q8_packed_size(W->n_out, W->n_in, nullptr, nullptr);
     if (rc != DL_OK) return rc;
     return gemv_run("dl_gemv_q8", W->qs, W->d, W->n_out, W->n_in, false, x, rows, x_stride, y, y_stride, path,
-                    stream);
+                    stream, pf);
 }
 
 int gemv_f16w_impl(const dl_f16_weight *W, const float *x, int rows, int64_t x_stride, float *y,
                    int64_t y_stride, int path, dl_stream_t stream)
 {
     dl::clear_error();
+    DlPrefetch pf;
+    dl::take_prefetch(&pf);
     if (!W || !W->w) return dl::fail(DL_E_ARG, "dl_gemv_f16w: null pointer");
     const int rc = dl_f16w_packed_size(W->n_out, W->n_in, nullptr);
     if (rc != DL_OK) return rc;
     return gemv_run("dl_gemv_f16w", W->w, nullptr, W->n_out, W->n_in, true, x, rows, x_stride, y, y_stride, path,
-                    stream);
+                    stream, pf);
 }
 
 // Chained GEMVs: grid = the CTAs resident at once (the grid barriers need every CTA running).

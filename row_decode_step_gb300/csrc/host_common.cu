@@ -44,6 +44,14 @@ int check_launch(const char *what)
     return DL_OK;
 }
 
+static thread_local DlPrefetch g_pf = {};
+
+void take_prefetch(DlPrefetch *out)
+{
+    *out = g_pf;
+    g_pf.n = 0;
+}
+
 }  // namespace dl
 
 extern "C" {
@@ -51,6 +59,26 @@ extern "C" {
 const char *dl_last_error(void) { return dl::g_err; }
 
 int dl_version(void) { return 100; }
+
+int dl_l2_prefetch_next(int n, const void *const *ptrs, const size_t *bytes)
+{
+    dl::clear_error();
+    dl::g_pf.n = 0;
+    if (n < 0 || n > kMaxPrefetch) return dl::fail(DL_E_ARG, "dl_l2_prefetch_next: n=%d (0..%d)", n, kMaxPrefetch);
+    if (n > 0 && (!ptrs || !bytes)) return dl::fail(DL_E_ARG, "dl_l2_prefetch_next: null pointer");
+    DlPrefetch pf = {};
+    for (int i = 0; i < n; ++i) {
+        if (!ptrs[i] || !dl::aligned16(ptrs[i]) || bytes[i] % 16 != 0)
+            return dl::fail(DL_E_ALIGN, "dl_l2_prefetch_next: range %d must start 16-byte aligned and span a "
+                                        "multiple of 16 bytes", i);
+        if (bytes[i] == 0) continue;
+        pf.p[pf.n] = static_cast<const char *>(ptrs[i]);
+        pf.bytes[pf.n] = bytes[i];
+        ++pf.n;
+    }
+    dl::g_pf = pf;
+    return DL_OK;
+}
 
 int dl_status_read(const int32_t *status_dev, int32_t *host_out)
 {

@@ -26,6 +26,7 @@ struct RopeArgs {
     int f32, q8;
     int32_t *status;
     int n_q, n_kv, D, rot, neox, max_pos, capacity, n_regions;
+    DlPrefetch pf;           // L2 prefetches for a later kernel (first launch only)
 };
 
 __device__ __forceinline__ unsigned short to_half_clamped(float v)
@@ -34,8 +35,9 @@ __device__ __forceinline__ unsigned short to_half_clamped(float v)
     return __half_as_ushort(__float2half_rn(v));
 }
 
-__global__ void __launch_bounds__(256) rope_kv_store_kernel(RopeArgs a)
+__global__ void __launch_bounds__(256) rope_kv_store_kernel(const __grid_constant__ RopeArgs a)
 {
+    if (threadIdx.x == 0 && a.pf.n > 0) dl_issue_prefetch(a.pf);
     dl_pdl_wait();
     dl_pdl_launch_dependents();
     const int r = blockIdx.y;
@@ -224,6 +226,8 @@ int dl_rope_kv_store(float *q, int64_t q_stride, const float *k, int64_t k_strid
                      const dl_kv_cache *kv, int32_t *status, dl_stream_t stream)
 {
     dl::clear_error();
+    DlPrefetch pf;
+    dl::take_prefetch(&pf);
     if (!q || !k || !v || !pos || !rope || !kv || !kv->k || !kv->v || !rope->cos_sin)
         return dl::fail(DL_E_ARG, "dl_rope_kv_store: null pointer");
     if (rows < 0 || n_q <= 0) return dl::fail(DL_E_ARG, "dl_rope_kv_store: rows=%d n_q=%d", rows, n_q);
@@ -257,12 +261,14 @@ int dl_rope_kv_store(float *q, int64_t q_stride, const float *k, int64_t k_strid
     a.status = status;
     a.n_q = n_q; a.n_kv = kv->n_kv; a.D = D; a.rot = rope->rot_dim; a.neox = rope->neox ? 1 : 0;
     a.max_pos = rope->max_pos; a.capacity = kv->capacity; a.n_regions = kv->n_regions;
+    a.pf = pf;
     // q heads and the f16 / f32 mirrors' k and v heads: one thread per channel pair
     const int pairs = (a.q8 ? n_q : n_q + kv->n_kv) * (D / 2);
     dim3 grid((unsigned)dl::ceil_div(pairs, 256), (unsigned)rows);
     int rc = dl::launch_pdl(rope_kv_store_kernel, grid, dim3(256), 0, static_cast<cudaStream_t>(stream),
                             "dl_rope_kv_store: launch", a);
     if (rc != DL_OK || !a.q8) return rc;
+    a.pf.n = 0;
     // the q8_0 mirror's k and v: a warp per block of 32 channels, four warps a CTA
     dim3 grid8((unsigned)dl::ceil_div(2 * kv->n_kv * (D / 32), 4), (unsigned)rows);
     return dl::launch_pdl(rope_kv_store_q8_kernel, grid8, dim3(128), 0, static_cast<cudaStream_t>(stream),

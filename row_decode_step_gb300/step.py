@@ -8,6 +8,11 @@ most eight rows:
 
 or, with `fused_rope`, dl_decode_attn_rope in place of the rope/store and the
 attention (one launch fewer, the same stored halves and results); with
+`l2_prefetch`, two launches ask L2 for part of a later kernel's weights while
+they run (dl_l2_prefetch_next; results unchanged): the merge for the first
+half of the gate/up tiles, the O projection for the first quarter of the down
+tiles (the schedule that measured best at eight rows; it is off by default,
+since at one row it measured slower); with
 `cluster_merge`, dl_decode_attn_cluster in place of the attention and the merge
 (the pieces of a KV head merge inside their thread-block cluster); with
 `gemv_chain`, the O, gate/up and down projections as the phases of one
@@ -27,7 +32,16 @@ import torch
 
 from . import (KVCache, PackedQ8, Rope, dl_attn_merge, dl_attn_plan_build, dl_attn_plan_build_cluster,
                dl_decode_attn, dl_decode_attn_cluster, dl_decode_attn_rope, dl_gemv_q8, dl_gemv_q8_chain,
-               dl_plan_groups, dl_rope_kv_store, workspace_for)
+               dl_l2_prefetch_next, dl_plan_groups, dl_rope_kv_store, workspace_for)
+
+
+
+def _prefetch_head(w: Optional[PackedQ8], frac: float) -> None:
+    """Hand the first `frac` of w's weight tiles (whole 16-byte units) to the next launch."""
+    if w is None:
+        dl_l2_prefetch_next([])
+        return
+    dl_l2_prefetch_next([(w.qs.data_ptr(), int(w.qs.numel() * frac) // 16 * 16)])
 
 
 @dataclasses.dataclass
@@ -48,9 +62,10 @@ class Command:
     def __init__(self, rows: Sequence[int], positions: Sequence[int], regions: Sequence[int],
                  n_q: int, n_kv: int, head_dim: int, hidden: int, ffn: int, device, sm_count: int = 0,
                  force_chunk: int = 0, gemv_path: int = 0, attn_path: int = 0, fused_rope: bool = False,
-                 cluster_merge: bool = False, gemv_chain: bool = False):
+                 cluster_merge: bool = False, gemv_chain: bool = False, l2_prefetch: bool = False):
         n = len(rows)
         assert 1 <= n <= 8
+        self.l2_prefetch = bool(l2_prefetch)
         self.gemv_path, self.attn_path = gemv_path, attn_path
         self.fused_rope = bool(fused_rope)
         self.cluster_merge = bool(cluster_merge)
@@ -93,6 +108,7 @@ class Command:
 
     def run(self, W: LayerWeights, rope: Rope, kv: KVCache, stream=None):
         gp = self.gemv_path if (self.gemv_path != 1 or self.n <= 2) else 0
+        pf = self.l2_prefetch and not self.gemv_chain
         dl_gemv_q8(W.wqkv, self.x, self.qkv, stream=stream, path=gp)
         if self.cluster_merge:
             if self.fused_rope:
@@ -113,11 +129,15 @@ class Command:
             dl_decode_attn(self.q, kv, self.seqlen, self.plan, self.workspace, status=self.status, stream=stream,
                            path=self.attn_path)
         if not self.cluster_merge:
+            if pf:
+                _prefetch_head(W.wgu, 0.5)
             dl_attn_merge(self.workspace, self.plan, self.seqlen, self.attn, self.lse, stream=stream)
         if self.gemv_chain and W.wgu is not None:
             dl_gemv_q8_chain([W.wo, W.wgu, W.wdown], [self.attn, self.x_ffn, self.h], [self.y_o, self.gu, self.y_down],
                              self.sync, status=self.status, stream=stream, path=gp)
             return
+        if pf:
+            _prefetch_head(W.wdown, 0.25)
         dl_gemv_q8(W.wo, self.attn, self.y_o, stream=stream, path=gp)
         if W.wgu is not None:
             dl_gemv_q8(W.wgu, self.x_ffn, self.gu, stream=stream, path=gp)
@@ -134,7 +154,7 @@ class LayerStep:
     def __init__(self, positions: Sequence[int], regions: Sequence[int], n_q: int, n_kv: int, head_dim: int,
                  hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0, gemv_path: int = 0,
                  attn_path: int = 0, fused_rope: bool = False, cluster_merge: bool = False,
-                 gemv_chain: bool = False):
+                 gemv_chain: bool = False, l2_prefetch: bool = False):
         n = len(positions)
         sizes = dl_plan_groups(n)
         self.commands: List[Command] = []
@@ -143,7 +163,8 @@ class LayerStep:
             idx = list(range(r0, r0 + s))
             self.commands.append(Command(idx, [positions[i] for i in idx], [regions[i] for i in idx],
                                          n_q, n_kv, head_dim, hidden, ffn, device, sm_count, force_chunk,
-                                         gemv_path, attn_path, fused_rope, cluster_merge, gemv_chain))
+                                         gemv_path, attn_path, fused_rope, cluster_merge, gemv_chain,
+                                         l2_prefetch))
             r0 += s
         self.group_sizes = sizes
 

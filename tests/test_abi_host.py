@@ -143,3 +143,21 @@ def test_null_and_shape_refusals_before_any_launch(dl):
     w = dl.dl_q8_weight(16, 16, 64, 100)   # n_in not a multiple of 32
     x = ctypes.c_float(0)
     assert L.dl_gemv_q8(ctypes.byref(w), ctypes.byref(x), 1, 128, ctypes.byref(x), 64, None) == dl.DL_E_SHAPE
+
+
+def test_l2_prefetch_next_arguments(dl):
+    """The prefetch ranges are checked on the host: count, null arrays, 16-byte starts and sizes
+    (pointers are host integers here: nothing is dereferenced or launched)."""
+    L = dl.lib()
+    P, SZ = ctypes.c_void_p, ctypes.c_size_t
+    assert L.dl_l2_prefetch_next(0, None, None) == dl.DL_OK
+    assert L.dl_l2_prefetch_next(-1, None, None) == dl.DL_E_ARG
+    assert L.dl_l2_prefetch_next(17, (P * 17)(*([4096] * 17)), (SZ * 17)(*([16] * 17))) == dl.DL_E_ARG
+    assert L.dl_l2_prefetch_next(1, None, None) == dl.DL_E_ARG
+    assert L.dl_l2_prefetch_next(2, (P * 2)(4096, 4104), (SZ * 2)(16, 16)) == dl.DL_E_ALIGN   # start
+    assert L.dl_l2_prefetch_next(1, (P * 1)(4096), (SZ * 1)(24)) == dl.DL_E_ALIGN            # size
+    assert L.dl_l2_prefetch_next(1, (P * 1)(None), (SZ * 1)(16)) == dl.DL_E_ALIGN            # null range
+    assert L.dl_l2_prefetch_next(16, (P * 16)(*([4096] * 16)), (SZ * 16)(*([0, 32] * 8))) == dl.DL_OK
+    # the next launching call takes them even when it refuses its own arguments
+    assert L.dl_gemv_q8(None, None, 1, 0, None, 0, None) == dl.DL_E_ARG
+    assert L.dl_l2_prefetch_next(0, None, None) == dl.DL_OK

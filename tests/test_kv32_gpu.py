@@ -60,13 +60,16 @@ def test_kv32_rope_store(dl):
     np.testing.assert_allclose(qd.cpu().numpy(), qo, rtol=1e-6, atol=2e-6)
 
 
-@pytest.mark.parametrize("rows,n_q,n_kv,D,cap", [(1, 32, 8, 64, 4097), (1, 24, 8, 128, 5128), (8, 24, 8, 128, 5128)])
-@pytest.mark.parametrize("path", [0, 1])
-def test_kv32_attention(dl, rows, n_q, n_kv, D, cap, path):
+@pytest.mark.parametrize("rows,n_q,n_kv,D,cap", [(1, 32, 8, 64, 4097), (1, 24, 8, 128, 5128), (8, 24, 8, 128, 5128),
+                                                (4, 32, 8, 64, 3000)])
+@pytest.mark.parametrize("path,sm_count", [(0, 0), (1, 0), (0, 76)])
+def test_kv32_attention(dl, rows, n_q, n_kv, D, cap, path, sm_count):
+    """Queries per warp 4 (one row), 6 (24 queries per work item) and 8 (32); sm_count 76 is the
+    one-wave plan for the mirror's one CTA per SM at D = 128."""
     seqlen = list(range(cap - 7, cap - 7 + rows)) if rows > 1 else [cap]
     kc, vc = _planes("kv32/attn/%d/%d" % (rows, D), 1, n_kv, cap, D)
     q = synth.normal_f32(2, "kv32/attn/q/%d/%d" % (rows, D), (rows, n_q * D))
-    plan = dl.dl_attn_plan_build(seqlen, n_q, n_kv, D)
+    plan = dl.dl_attn_plan_build(seqlen, n_q, n_kv, D, sm_count=sm_count)
     ws = dl.workspace_for(plan)
     kv = dl.KVCache(kc.cuda(), vc.cuda())
     status = torch.zeros(1, dtype=torch.int32, device="cuda")

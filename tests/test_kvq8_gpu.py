@@ -81,9 +81,14 @@ def test_q8_store(dl, D, neox, rot, bias):
     (1, 4, 2, 64, 128, 128),
     (1, 32, 8, 64, 4100, 4097),
     (1, 24, 8, 128, 5128, 5121),
+    (2, 24, 8, 128, 5128, 5121),
     (8, 24, 8, 128, 5128, 5121),
+    (8, 32, 8, 64, 4100, 4090),
 ])
-def test_q8_attention(dl, rows, n_q, n_kv, D, cap, first):
+@pytest.mark.parametrize("path", [0, 1, 2])
+def test_q8_attention(dl, rows, n_q, n_kv, D, cap, first, path):
+    """Both inner products (CUDA cores; tensor cores with the codes as exact f16 operands and
+    the block scales on the score sums and the V operand) and the library's choice."""
     seqlen = list(range(first, first + rows))
     kc, ks, vc, vs = _planes("q8a/%d/%d" % (rows, D), 1, n_kv, cap, D)
     q = synth.normal_f32(2, "q8a/q/%d/%d" % (rows, D), (rows, n_q * D))
@@ -91,7 +96,8 @@ def test_q8_attention(dl, rows, n_q, n_kv, D, cap, first):
     ws = dl.workspace_for(plan)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = dl.decode_attention(q.cuda(), _cache(dl, kc, ks, vc, vs),
-                                   torch.tensor(seqlen, dtype=torch.int32, device="cuda"), plan, ws, status=status)
+                                   torch.tensor(seqlen, dtype=torch.int32, device="cuda"), plan, ws, status=status,
+                                   path=path)
     torch.cuda.synchronize()
     assert dl.dl_status_read(status) == 0
     kp, vp = _oracle_planes(kc, ks, vc, vs)
@@ -100,9 +106,10 @@ def test_q8_attention(dl, rows, n_q, n_kv, D, cap, first):
     assert_attn_close(out.cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse)
 
 
-def test_q8_sessions_and_cluster(dl):
+@pytest.mark.parametrize("path", [0, 2])
+def test_q8_sessions_and_cluster(dl, path):
     """Six sessions of different lengths in their own regions, through the partials path and the
-    cluster merge."""
+    cluster merge, on the library's choice (CUDA cores for one-row sessions) and tensor cores."""
     lens = [513, 4000, 1500, 64, 2049, 2900]
     n_q, n_kv, D, cap = 24, 8, 128, 4000
     kc, ks, vc, vs = _planes("q8a/sess", 6, n_kv, cap, D)
@@ -115,10 +122,10 @@ def test_q8_sessions_and_cluster(dl):
             plan = dl.dl_attn_plan_build_cluster(lens, n_q, n_kv, D, regions=list(range(6)))
             out = torch.empty(6, n_q * D, device="cuda")
             lse = torch.empty(6, n_q, device="cuda")
-            dl.dl_decode_attn_cluster(q.cuda(), kv, sl, plan, out, lse)
+            dl.dl_decode_attn_cluster(q.cuda(), kv, sl, plan, out, lse, path=path)
         else:
             plan = dl.dl_attn_plan_build(lens, n_q, n_kv, D, regions=list(range(6)))
-            out, lse = dl.decode_attention(q.cuda(), kv, sl, plan, dl.workspace_for(plan))
+            out, lse = dl.decode_attention(q.cuda(), kv, sl, plan, dl.workspace_for(plan), path=path)
         torch.cuda.synchronize()
         ref_out, ref_lse = oracle.attention(q.numpy().astype(np.float64), kp, vp, np.array(lens, np.int32), n_q=n_q,
                                             n_kv=n_kv, head_dim=D, chunk=plan.chunk, n_splits=plan.max_splits,
@@ -127,17 +134,14 @@ def test_q8_sessions_and_cluster(dl):
 
 
 def test_q8_refusals(dl):
-    """The tensor form, the fused rope and a capacity that is not a multiple of 4 are refused
-    before anything launches."""
+    """The fused rope and a capacity that is not a multiple of 4 are refused before anything
+    launches."""
     kc, ks, vc, vs = _planes("q8a/refuse", 1, 2, 64, 64)
     kv = _cache(dl, kc, ks, vc, vs)
     plan = dl.dl_attn_plan_build([64], 4, 2, 64)
     ws = dl.workspace_for(plan)
     q = torch.zeros(1, 256, device="cuda")
     sl = torch.tensor([64], dtype=torch.int32, device="cuda")
-    with pytest.raises(dl.DLError) as e:
-        dl.dl_decode_attn(q, kv, sl, plan, ws, path=2)
-    assert e.value.code == dl.DL_E_SHAPE
     rope = dl.make_rope(500000.0, 64, 64)
     with pytest.raises(dl.DLError) as e:
         dl.dl_decode_attn_rope(q, torch.zeros(1, 128, device="cuda"), torch.zeros(1, 128, device="cuda"),

@@ -27,7 +27,7 @@ def dl():
 
 
 def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=False, cluster_merge=False,
-          gemv_chain=False):
+          gemv_chain=False, l2_prefetch=False):
     from row_decode_step_gb300.step import LayerStep, LayerWeights
     D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
     blocks = layer_blocks(S.name)
@@ -43,7 +43,7 @@ def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=Fals
     xf = synth.normal_f32(0, label + "/xf", (n, H)) if F else None
     h = synth.normal_f32(0, label + "/h", (n, F)) if F else None
     step = LayerStep(positions, regions, n_q, n_kv, D, H, F, "cuda", fused_rope=fused_rope,
-                     cluster_merge=cluster_merge, gemv_chain=gemv_chain)
+                     cluster_merge=cluster_merge, gemv_chain=gemv_chain, l2_prefetch=l2_prefetch)
     r0 = 0
     for c in step.commands:
         c.x.copy_(x[r0:r0 + c.n].cuda())
@@ -102,18 +102,22 @@ def test_step_1b(dl):
     _step(dl, synth.LLAMA_1B, [4096], [0], 1, 4097, "step/1b")
 
 
-@pytest.mark.parametrize("fused,cluster,chain", [(False, False, False), (True, False, False), (True, True, False),
-                                                 (True, False, True)])
+FORMS = [(False, False, False, False), (True, False, False, False), (True, True, False, False),
+         (True, False, True, False), (True, False, False, True), (False, False, False, True)]
+
+
+@pytest.mark.parametrize("fused,cluster,chain,prefetch", FORMS)
 @pytest.mark.parametrize("rows", [1, 8])
-def test_step_3b(dl, rows, fused, cluster, chain):
+def test_step_3b(dl, rows, fused, cluster, chain, prefetch):
+    """Every form of the step (rope in the attention, cluster merge, GEMV chain, L2 prefetches)
+    against the oracle's layer step."""
     _step(dl, synth.LLAMA_3B, list(range(5120, 5120 + rows)), [0] * rows, 1, 5128, "step/3b%d" % rows,
-          fused_rope=fused, cluster_merge=cluster, gemv_chain=chain)
+          fused_rope=fused, cluster_merge=cluster, gemv_chain=chain, l2_prefetch=prefetch)
 
 
-@pytest.mark.parametrize("fused,cluster,chain", [(False, False, False), (True, False, False), (True, True, False),
-                                                 (True, False, True)])
-def test_step_twelve_streams(dl, fused, cluster, chain):
+@pytest.mark.parametrize("fused,cluster,chain,prefetch", FORMS)
+def test_step_twelve_streams(dl, fused, cluster, chain, prefetch):
     lens = synth.twelve_stream_lengths(0)
     step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams", fused_rope=fused,
-                 cluster_merge=cluster, gemv_chain=chain)
+                 cluster_merge=cluster, gemv_chain=chain, l2_prefetch=prefetch)
     assert step.group_sizes == [6, 6]
