@@ -16,7 +16,9 @@ since at one row it measured slower); with
 `cluster_merge`, dl_decode_attn_cluster in place of the attention and the merge
 (the pieces of a KV head merge inside their thread-block cluster); with
 `gemv_chain`, the O, gate/up and down projections as the phases of one
-dl_gemv_q8_chain launch.
+dl_gemv_q8_chain launch.  A step of several commands (sessions past eight rows)
+may run them on streams of their own (`concurrent`), since they share nothing
+but the weights.
 
 Norms, SwiGLU and residual adds are not part of the path: the gate/up and down
 projections read their own activation buffers (filled by the caller).  More
@@ -154,7 +156,10 @@ class LayerStep:
     def __init__(self, positions: Sequence[int], regions: Sequence[int], n_q: int, n_kv: int, head_dim: int,
                  hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0, gemv_path: int = 0,
                  attn_path: int = 0, fused_rope: bool = False, cluster_merge: bool = False,
-                 gemv_chain: bool = False, l2_prefetch: bool = False):
+                 gemv_chain: bool = False, l2_prefetch: bool = False, concurrent: bool = False):
+        """concurrent: the commands (independent sessions) run on streams of their own, forked
+        from the caller's stream and joined back into it, so that one command's launch latencies
+        overlap another's work."""
         n = len(positions)
         sizes = dl_plan_groups(n)
         self.commands: List[Command] = []
@@ -167,10 +172,23 @@ class LayerStep:
                                          l2_prefetch))
             r0 += s
         self.group_sizes = sizes
+        self.concurrent = bool(concurrent) and len(self.commands) > 1
+        self.side_streams = ([torch.cuda.Stream(device=device) for _ in self.commands] if self.concurrent
+                             else [])
 
     def run(self, W: LayerWeights, rope: Rope, kv: KVCache, stream=None):
-        for c in self.commands:
-            c.run(W, rope, kv, stream)
+        if not self.concurrent:
+            for c in self.commands:
+                c.run(W, rope, kv, stream)
+            return
+        main = stream if stream is not None else torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        for c, s in zip(self.commands, self.side_streams):
+            s.wait_event(fork)
+            c.run(W, rope, kv, s)
+        for s in self.side_streams:
+            main.wait_stream(s)
 
     @property
     def launches(self) -> int:

@@ -27,7 +27,7 @@ def dl():
 
 
 def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=False, cluster_merge=False,
-          gemv_chain=False, l2_prefetch=False):
+          gemv_chain=False, l2_prefetch=False, concurrent=False):
     from row_decode_step_gb300.step import LayerStep, LayerWeights
     D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
     blocks = layer_blocks(S.name)
@@ -43,7 +43,8 @@ def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=Fals
     xf = synth.normal_f32(0, label + "/xf", (n, H)) if F else None
     h = synth.normal_f32(0, label + "/h", (n, F)) if F else None
     step = LayerStep(positions, regions, n_q, n_kv, D, H, F, "cuda", fused_rope=fused_rope,
-                     cluster_merge=cluster_merge, gemv_chain=gemv_chain, l2_prefetch=l2_prefetch)
+                     cluster_merge=cluster_merge, gemv_chain=gemv_chain, l2_prefetch=l2_prefetch,
+                     concurrent=concurrent)
     r0 = 0
     for c in step.commands:
         c.x.copy_(x[r0:r0 + c.n].cuda())
@@ -121,3 +122,11 @@ def test_step_twelve_streams(dl, fused, cluster, chain, prefetch):
     step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams", fused_rope=fused,
                  cluster_merge=cluster, gemv_chain=chain, l2_prefetch=prefetch)
     assert step.group_sizes == [6, 6]
+
+
+def test_step_twelve_streams_concurrent(dl):
+    """The two 6-row commands on streams of their own (forked and joined around them)."""
+    lens = synth.twelve_stream_lengths(0)
+    step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams", fused_rope=True,
+                 concurrent=True)
+    assert step.concurrent and step.group_sizes == [6, 6]
