@@ -59,6 +59,9 @@ def parse_args():
                    help="1: the O, gate/up and down projections as the phases of one persistent launch")
     p.add_argument("--cluster-merge", type=int, default=0, choices=[0, 1],
                    help="1: the pieces of a KV head merge inside their thread-block cluster (no merge launch)")
+    p.add_argument("--tail-merge", type=int, default=0, choices=[0, 1],
+                   help="1: commands of at most 8 queries per KV head merge in the attention launch "
+                        "(dl_decode_attn_merged: the last piece of each KV head merges)")
     p.add_argument("--concurrent-commands", type=int, default=1, choices=[0, 1],
                    help="1: the commands of a step (independent sessions) run on streams of their own, "
                         "forked and joined inside the step's graph (twelve streams: two 6-row commands)")
@@ -234,7 +237,7 @@ def build_layers(wl, L, dev, seed=0):
 
 
 def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0), fused=False,
-            cluster=False, chain=False, prefetch=False, concurrent=False):
+            cluster=False, chain=False, prefetch=False, concurrent=False, tail=False):
     import synth
     import torch
     import row_decode_step_gb300 as dl
@@ -244,7 +247,7 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
     rope = dl.make_rope(S.rope_theta, S.head_dim, wl["capacity"], device=dev)
     step = LayerStep(wl["positions"], wl["regions"], S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, dev,
                      gemv_path=paths[0], attn_path=paths[1], fused_rope=fused, cluster_merge=cluster,
-                     gemv_chain=chain, l2_prefetch=prefetch, concurrent=concurrent)
+                     gemv_chain=chain, l2_prefetch=prefetch, concurrent=concurrent, tail_merge=tail)
     for i, c in enumerate(step.commands):
         c.x.copy_(synth.normal_f32(0, "bench/x%d" % i, tuple(c.x.shape), device=dev))
         if c.x_ffn is not None:
@@ -556,7 +559,8 @@ def run_ours(args):
     wl = workload(args.workload)
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path),
                   fused=bool(args.fused_rope), cluster=bool(args.cluster_merge), chain=bool(args.gemv_chain),
-                  prefetch=bool(args.l2_prefetch), concurrent=bool(args.concurrent_commands))
+                  prefetch=bool(args.l2_prefetch), concurrent=bool(args.concurrent_commands),
+                  tail=bool(args.tail_merge))
     steps = args.steps
     ms, value = combine_ranks(res["ms_total"], steps, world, dev)
     step = res["step"]
@@ -574,7 +578,7 @@ def run_ours(args):
                          want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
                          fused=bool(args.fused_rope), cluster=bool(args.cluster_merge),
                          chain=bool(args.gemv_chain), prefetch=bool(args.l2_prefetch),
-                         concurrent=bool(args.concurrent_commands))
+                         concurrent=bool(args.concurrent_commands), tail=bool(args.tail_merge))
             sb2 = step_bytes(w2, r2["step"])
             extras[name] = {"rows": len(w2["positions"]), "layer_steps_per_s": 1e3 / r2["ms_per_step"],
                             "ms_per_step": r2["ms_per_step"],
@@ -619,6 +623,7 @@ def run_ours(args):
                    "gemv_path": args.gemv_path, "attn_path": args.attn_path,
                    "rope_in_attention": bool(args.fused_rope), "merge_in_cluster": bool(args.cluster_merge),
                    "l2_prefetch": bool(args.l2_prefetch), "concurrent_commands": bool(args.concurrent_commands),
+                   "tail_merge": bool(args.tail_merge),
                    "gemv_chain": bool(args.gemv_chain)},
         "tokens_per_s": rows * value,
         "step": {"algorithmic_bytes": sb, "algorithmic_gbs": step_gbs, "hbm_frac": step_gbs / peak,

@@ -113,8 +113,8 @@ int dl_status_read(const int32_t *status_dev, int32_t *host_out);
  *
  * The next launching call this host thread makes among dl_gemv_q8,
  * dl_gemv_q8_ex, dl_gemv_f16w, dl_gemv_f16w_ex, dl_rope_kv_store, dl_decode_attn,
- * dl_decode_attn_ex, dl_decode_attn_rope, dl_decode_attn_cluster and
- * dl_attn_merge takes the ranges, whether or not it launches.  Its kernel then
+ * dl_decode_attn_ex, dl_decode_attn_rope, dl_decode_attn_cluster,
+ * dl_decode_attn_merged and dl_attn_merge takes the ranges, whether or not it launches.  Its kernel then
  * splits them over its CTAs and issues bulk L2 prefetches for them before
  * waiting on the previous kernel.
  *
@@ -357,7 +357,8 @@ typedef struct dl_attn_plan {
     int sess_begin[DL_MAX_ROWS + 1];  /* session s owns sess_rows[sess_begin[s] .. sess_begin[s+1]) */
     int sess_splits[DL_MAX_ROWS];  /* pieces of session s */
     int sess_item0[DL_MAX_ROWS + 1];  /* first work item of session s (items = n_kv * splits) */
-    size_t workspace_bytes;        /* bytes of the partials workspace */
+    size_t workspace_bytes;        /* bytes of the workspace: partials (o, lse), then the
+                                      last-piece merge's counters */
 } dl_attn_plan;
 
 /*
@@ -471,6 +472,29 @@ int dl_decode_attn_cluster(const float *q, int64_t q_stride, const dl_attn_rope_
                            const dl_kv_cache *kv, const int32_t *seqlen, const dl_attn_plan *plan,
                            float *out, int64_t out_stride, float *lse, int32_t *status, int path,
                            dl_stream_t stream);
+
+/*
+ * Split-KV decode attention with the merge done by the last piece [SPL]: every
+ * piece writes its (o, lse) to the workspace as dl_decode_attn does, then counts
+ * itself in a per-(session, KV head) counter kept in the workspace; the piece
+ * that completes the count merges the group's partials into out / lse with the
+ * arithmetic of dl_attn_merge, operation for operation (the results are
+ * bit-identical to dl_decode_attn_ex + dl_attn_merge), and clears the counter.
+ * One launch instead of two; for commands of few queries per KV head (the
+ * merge of a group runs in one CTA).
+ *   plan       from dl_attn_plan_build; at most 8 queries per work item (rows of
+ *              a session x n_q / n_kv), else DL_E_SHAPE
+ *   workspace  plan->workspace_bytes, 16-byte aligned; its counters (the last
+ *              16-byte-rounded n_sessions * n_kv int32) must be zero before the
+ *              first call (zero the whole workspace once); every call leaves
+ *              them zero
+ *   rope_in, out, lse   as dl_decode_attn_cluster
+ * Other arguments, the path and the error codes as dl_decode_attn_ex.
+ */
+int dl_decode_attn_merged(const float *q, int64_t q_stride, const dl_attn_rope_in *rope_in,
+                          const dl_kv_cache *kv, const int32_t *seqlen, const dl_attn_plan *plan,
+                          void *workspace, size_t workspace_bytes, float *out, int64_t out_stride,
+                          float *lse, int32_t *status, int path, dl_stream_t stream);
 
 /*
  * Log-sum-exp merge of the pieces of every (row, head):

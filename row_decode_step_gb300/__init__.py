@@ -114,6 +114,7 @@ def lib() -> ctypes.CDLL:
             "dl_decode_attn_rope": ([P, I64, P, I64, P, I64, P, P, P, P, P, P, P, SZ, P, I, P], I),
             "dl_attn_plan_build_cluster": ([I, P, P, I, I, I, I, I, P], I),
             "dl_decode_attn_cluster": ([P, I64, P, P, P, P, P, I64, P, P, I, P], I),
+            "dl_decode_attn_merged": ([P, I64, P, P, P, P, P, SZ, P, I64, P, P, I, P], I),
             "dl_attn_merge": ([P, P, P, P, I64, P, P], I),
             "dl_decode_attention_noalloc_max_bytes": ([], SZ),
             "dl_decode_attention_noalloc": ([P, I64, P, P, P, P, I64, P, P, P], I),
@@ -374,7 +375,8 @@ def dl_attn_plan_build(seqlen: Sequence[int], n_q: int, n_kv: int, head_dim: int
 
 
 def workspace_for(plan: dl_attn_plan, device="cuda") -> torch.Tensor:
-    return torch.empty(max(16, plan.workspace_bytes), dtype=torch.uint8, device=device)
+    """A workspace for the plan, zeroed (the last-piece merge's counters start at zero)."""
+    return torch.zeros(max(16, plan.workspace_bytes), dtype=torch.uint8, device=device)
 
 
 ATTN_PATH_AUTO, ATTN_PATH_CUDA_CORE, ATTN_PATH_TENSOR = 0, 1, 2
@@ -460,6 +462,40 @@ def dl_decode_attn_cluster(q: torch.Tensor, kv: KVCache, seqlen: torch.Tensor, p
     _check(lib().dl_decode_attn_cluster(_ptr(q), q.stride(0), None if rin is None else ctypes.byref(rin),
                                         ctypes.byref(kv.c), _ptr(seqlen), ctypes.byref(plan), _ptr(out),
                                         out.stride(0), _ptr(lse), _ptr(status), path, _stream(stream)))
+
+
+def _rope_in(k, v, pos, rope, bias):
+    if k is None:
+        return None
+    for t, n in ((k, "k"), (v, "v")):
+        _dev(t, torch.float32, n)
+    _dev(pos, torch.int32, "pos")
+    if bias is not None:
+        _dev(bias, torch.float32, "bias")
+    return dl_attn_rope_in(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(bias), _ptr(pos),
+                           ctypes.cast(ctypes.pointer(rope.c), ctypes.c_void_p))
+
+
+def dl_decode_attn_merged(q: torch.Tensor, kv: KVCache, seqlen: torch.Tensor, plan: dl_attn_plan,
+                          workspace: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                          k: Optional[torch.Tensor] = None, v: Optional[torch.Tensor] = None,
+                          pos: Optional[torch.Tensor] = None, rope: Optional["Rope"] = None,
+                          bias: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                          stream=None, path: int = ATTN_PATH_AUTO) -> None:
+    """Attention whose last piece per (session, KV head) merges the partials (one launch; a
+    workspace from workspace_for, zeroed once); with k, v, pos and rope given, the rope and
+    store happen in the launch too."""
+    _dev(q, torch.float32, "q")
+    _dev(seqlen, torch.int32, "seqlen")
+    _dev(workspace, torch.uint8, "workspace")
+    _dev(out, torch.float32, "out")
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+    rin = _rope_in(k, v, pos, rope, bias)
+    _check(lib().dl_decode_attn_merged(_ptr(q), q.stride(0), None if rin is None else ctypes.byref(rin),
+                                       ctypes.byref(kv.c), _ptr(seqlen), ctypes.byref(plan), _ptr(workspace),
+                                       workspace.numel(), _ptr(out), out.stride(0), _ptr(lse), _ptr(status), path,
+                                       _stream(stream)))
 
 
 def dl_attn_merge(workspace: torch.Tensor, plan: dl_attn_plan, seqlen: torch.Tensor,

@@ -27,6 +27,9 @@ constexpr int kTile = 32;          // keys per tile
 constexpr int kMaxQ = 32;          // queries one work item serves (session rows x group)
 constexpr int kMaxCluster = 16;    // pieces of a (session, KV head) merged inside one cluster
 constexpr int kCudaCoreMaxQ = 4;   // queries per work item up to which the CUDA-core form is used
+constexpr int kMergeWarps = 8;     // the merge's warps per (row, head), as the merge kernel runs them
+constexpr int kMergeBatch = 8;     // pieces a merge warp has in flight per pass
+constexpr int kTailMaxQ = 8;       // queries per work item up to which the last piece may merge
 
 struct AttnArgs {
     const float *q;
@@ -56,6 +59,11 @@ struct AttnArgs {
     float *out, *lse_out;
     int64_t out_stride;
     DlPrefetch pf;       // L2 prefetches for a later kernel (the producer issues its share)
+    // merge by the last piece (tail_merge = 1): every piece writes its partials, counts itself in
+    // counters[session][kv head] and the piece that completes the count merges the group's
+    // partials into out / lse_out, then clears the count
+    int tail_merge;
+    int *counters;
 };
 
 // Signed bytes `lo`, `lo + 1` of w to floats: the byte flipped to u = q + 128 sits in the low
@@ -237,6 +245,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     constexpr int NH = D / EPB;               // boxes per key row
     constexpr int S = attn_stages(D, EB);
     static_assert(S >= kMmaConsumers, "every stage group needs a slot of its own in flight");
+    static_assert((size_t)kTailMaxQ * kMergeWarps * (D + 2) * 4 <= (size_t)S * attn_slot_bytes(D, EB),
+                  "the tail merge's per-warp sums fit in the idle ring");
     constexpr uint32_t kStageBytes = attn_slot_bytes(D, EB);
     constexpr uint32_t kCodeBytes = kStKeys * D;                  // q8_0: codes of 32 keys
     constexpr uint32_t kScaleBytes = kStKeys * (D / 16);          // q8_0: scales of 32 keys
@@ -250,6 +260,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     __shared__ int s_len[DL_MAX_ROWS], s_row[DL_MAX_ROWS], s_pos[DL_MAX_ROWS];
     __shared__ unsigned char s_qrow[kMaxQ], s_qhead[kMaxQ];   // query -> (session row, head in group)
     __shared__ float s_plse[kMaxQ], s_mM[kMaxQ], s_mW[kMaxQ];   // cluster merge: this piece's lse, weights
+    __shared__ int s_last;                                      // tail merge: this piece completes the count
     // the swizzled boxes want 1024-byte aligned destinations
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~static_cast<uintptr_t>(1023));
@@ -302,7 +313,19 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     const int k1 = min(k0 + P.chunk, lmax);
     const bool idle = k0 >= k1;                 // nothing of this piece is attended
     // (no barrier pending; with a cluster merge the CTA stays to merge its share of the group)
-    if (idle && !P.cluster) return;
+    if (idle && !P.cluster) {
+        // tail merge with no keys in any row of the session: no piece counts, so the first one
+        // writes the merge's empty result (out = 0, lse = -inf)
+        if (a.tail_merge && piece == 0 && lmax == 0) {
+            for (int e = tid; e < Q * D; e += kMmaThreads) {
+                const int qi = e / D, d = e - qi * D;
+                const int r = s_row[s_qrow[qi]], hq = h * G + s_qhead[qi];
+                a.out[(int64_t)r * a.out_stride + (int64_t)hq * D + d] = 0.f;
+                if (d == 0 && a.lse_out) a.lse_out[(int64_t)r * P.n_q + hq] = -INFINITY;
+            }
+        }
+        return;
+    }
     const int nst = idle ? 0 : (k1 - k0 + kStKeys - 1) / kStKeys;
 
     const int reg = P.row_region[s_row[0]];
@@ -551,6 +574,110 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
         dla::cluster_sync_relaxed();
+    };
+    // tail merge: after this piece's partials are written and fenced, one thread counts the piece
+    // in; the piece that completes the count of the (session, KV head) (its pieces with keys)
+    // clears it for the next launch and merges the group's partials with the merge kernel's
+    // arithmetic, operation for operation: per query, eight virtual merge warps (each on every
+    // eighth piece, in batches of eight, with its own running maximum) in the ring's shared
+    // memory, then their combination
+    auto tail_merge = [&]() {
+        __threadfence();
+        dla::named_sync(1, kMmaConsumers * 32);
+        if (tid == 0) {
+            const int np_act = min(splits, (lmax + P.chunk - 1) / P.chunk);
+            int *cnt = a.counters + ((int64_t)s * P.n_kv + h);
+            const int prev = atomicAdd(cnt, 1);
+            s_last = prev == np_act - 1 ? 1 : 0;
+            if (s_last) atomicExch(cnt, 0);
+        }
+        dla::named_sync(1, kMmaConsumers * 32);
+        if (!s_last) return;
+        __threadfence();
+        constexpr int VPL = D / 32;
+        float *t_acc = reinterpret_cast<float *>(smem);             // [Q][8][D]
+        float *t_m = t_acc + (size_t)kTailMaxQ * kMergeWarps * D;   // [Q][8]
+        float *t_w = t_m + kTailMaxQ * kMergeWarps;
+        for (int pr = warp; pr < Q * kMergeWarps; pr += kMmaConsumers) {
+            const int qi = pr / kMergeWarps, vw = pr - qi * kMergeWarps;
+            const int rq = s_qrow[qi];
+            const int hq = h * G + s_qhead[qi];
+            const int np = (s_len[rq] + P.chunk - 1) / P.chunk;
+            const float *pl = a.part_lse + ((int64_t)s_row[rq] * P.n_q + hq) * ms;
+            const float *po = a.part_o + ((int64_t)s_row[rq] * P.n_q + hq) * ms * D + lane * VPL;
+            float Mw = -INFINITY, Ww = 0.f, acc[VPL];
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
+            for (int p0 = vw; p0 < np; p0 += kMergeWarps * kMergeBatch) {
+                float lv[kMergeBatch], v[kMergeBatch][VPL];
+#pragma unroll
+                for (int u = 0; u < kMergeBatch; ++u) {
+                    const int p = p0 + kMergeWarps * u;
+                    lv[u] = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
+                    if (p < np) {
+                        lv[u] = __ldcg(pl + p);
+                        if constexpr (VPL == 4) {
+                            const float4 t = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)p * D));
+                            v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+                        } else {
+                            const float2 t = __ldcg(reinterpret_cast<const float2 *>(po + (int64_t)p * D));
+                            v[u][0] = t.x; v[u][1] = t.y;
+                        }
+                    }
+                }
+                float mb = Mw;
+#pragma unroll
+                for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, lv[u]);
+                const float sc = Mw == -INFINITY ? 0.f : __expf(Mw - mb);
+                Ww *= sc;
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) acc[i] *= sc;
+#pragma unroll
+                for (int u = 0; u < kMergeBatch; ++u) {
+                    const float w = lv[u] == -INFINITY ? 0.f : __expf(lv[u] - mb);
+                    Ww += w;
+#pragma unroll
+                    for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w, v[u][i], acc[i]);
+                }
+                Mw = mb;
+            }
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) t_acc[((size_t)qi * kMergeWarps + vw) * D + lane * VPL + i] = acc[i];
+            if (lane == 0) {
+                t_m[qi * kMergeWarps + vw] = Mw;
+                t_w[qi * kMergeWarps + vw] = Ww;
+            }
+        }
+        dla::named_sync(1, kMmaConsumers * 32);
+        for (int e = tid; e < Q * D; e += kMmaConsumers * 32) {
+            const int qi = e / D, d = e - qi * D;
+            const int rq = s_qrow[qi];
+            const int r = s_row[rq], hq = h * G + s_qhead[qi];
+            float *dst = a.out + (int64_t)r * a.out_stride + (int64_t)hq * D;
+            if (s_len[rq] == 0) {
+                dst[d] = 0.f;
+                if (d == 0 && a.lse_out) a.lse_out[(int64_t)r * P.n_q + hq] = -INFINITY;
+                continue;
+            }
+            const float *mq = t_m + qi * kMergeWarps, *wq = t_w + qi * kMergeWarps;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, mq[w]);
+            float f[kMergeWarps], Wt = 0.f;
+#pragma unroll
+            for (int w = 0; w < kMergeWarps; ++w) {
+                f[w] = mq[w] == -INFINITY ? 0.f : __expf(mq[w] - M);
+                Wt += f[w] * wq[w];
+            }
+            const float inv = 1.f / Wt;
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < kMergeWarps; ++w) t = fmaf(f[w], t_acc[((size_t)qi * kMergeWarps + w) * D + d], t);
+            dst[d] = t * inv;
+            if (d == 0 && a.lse_out) a.lse_out[(int64_t)r * P.n_q + hq] = M + logf(Wt);
+        }
     };
     if (idle) {                                      // (cluster plans only: the others returned)
         cluster_merge();
@@ -858,6 +985,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         if (attn_consumers_any(bad)) {
             poison_partials();
             if (P.cluster) cluster_merge();
+            else if (a.tail_merge) tail_merge();
             return;
         }
     #pragma unroll
@@ -1094,6 +1222,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         if (attn_consumers_any(bad)) {
             poison_partials();
             if (P.cluster) cluster_merge();
+            else if (a.tail_merge) tail_merge();
             return;
         }
         if (sg < NS) {
@@ -1167,6 +1296,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         }
     }
     if (P.cluster) cluster_merge();
+    else if (a.tail_merge) tail_merge();
 }
 
 struct MergeArgs {
@@ -1182,8 +1312,6 @@ struct MergeArgs {
 // One CTA per (row, head); its eight warps take every eighth piece and issue the loads of
 // their pieces' (lse, o) together, each warp keeping its own running maximum, so that the
 // partials cross from L2 in one round; the warps' sums are combined in shared memory.
-constexpr int kMergeWarps = 8;
-constexpr int kMergeBatch = 8;     // pieces a warp has in flight per pass
 
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const __grid_constant__ MergeArgs a)
@@ -1451,7 +1579,8 @@ static int plan_build(int rows, const int32_t *seqlen_host, const int32_t *regio
     P.max_splits = ms;
     const size_t po = (size_t)rows * n_q * ms * head_dim * 4;
     const size_t pl = (size_t)rows * n_q * ms * 4;
-    P.workspace_bytes = ((po + 15) / 16) * 16 + ((pl + 15) / 16) * 16;
+    const size_t pc = (size_t)ns * n_kv * 4;          // the tail merge's piece counts
+    P.workspace_bytes = ((po + 15) / 16) * 16 + ((pl + 15) / 16) * 16 + ((pc + 15) / 16) * 16;
     *out = P;
     return DL_OK;
 }
@@ -1483,7 +1612,7 @@ struct FusedIn {
     const dl_rope *rope;
 };
 
-// Results of a cluster plan: written by the launch itself.
+// Results written by the attention launch itself: a cluster plan's, or the last piece's merge.
 struct ClusterOut {
     float *out;
     int64_t out_stride;
@@ -1493,19 +1622,21 @@ struct ClusterOut {
 static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache *kv, const int32_t *seqlen,
                             const dl_attn_plan *plan, void *workspace, size_t workspace_bytes,
                             int32_t *status, int path, dl_stream_t stream, const FusedIn *f = nullptr,
-                            const ClusterOut *co = nullptr)
+                            const ClusterOut *co = nullptr, bool tail = false)
 {
     dl::clear_error();
     DlPrefetch pf;
     dl::take_prefetch(&pf);
-    if (!q || !kv || !kv->k || !kv->v || !seqlen || (!co && !workspace))
+    if (!q || !kv || !kv->k || !kv->v || !seqlen || ((!co || tail) && !workspace) || (co && !co->out))
         return dl::fail(DL_E_ARG, "dl_decode_attn: null pointer");
     int rc = check_plan(plan);
     if (rc != DL_OK) return rc;
-    if ((plan->cluster > 0) != (co != nullptr))
+    if (tail && plan->cluster > 0)
+        return dl::fail(DL_E_ARG, "dl_decode_attn_merged: a cluster plan goes to dl_decode_attn_cluster");
+    if (!tail && (plan->cluster > 0) != (co != nullptr))
         return dl::fail(DL_E_ARG, plan->cluster > 0 ? "dl_decode_attn: a cluster plan goes to dl_decode_attn_cluster"
                                                     : "dl_decode_attn_cluster: the plan has no clusters");
-    if (co) {
+    if (co && !tail) {
         if (!co->out) return dl::fail(DL_E_ARG, "dl_decode_attn_cluster: null output");
         if (plan->cluster > kMaxCluster || plan->n_work != plan->n_sessions * plan->n_kv * plan->cluster)
             return dl::fail(DL_E_ARG, "dl_decode_attn_cluster: cluster of %d", plan->cluster);
@@ -1536,9 +1667,10 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
             return dl::fail(DL_E_ARG, "dl_decode_attn: plan covers %d keys of row %d, the cache holds %d",
                             plan->row_keys_max[r], r, kv->capacity);
     }
-    if (!co && workspace_bytes < plan->workspace_bytes)
+    const bool partials = !co || tail;           // pieces write partials to the workspace
+    if (partials && workspace_bytes < plan->workspace_bytes)
         return dl::fail(DL_E_WORKSPACE, "dl_decode_attn: workspace %zu < %zu bytes", workspace_bytes, plan->workspace_bytes);
-    if ((!co && !dl::aligned16(workspace)) || !dl::aligned16(kv->k) || !dl::aligned16(kv->v) || !dl::aligned16(q) ||
+    if ((partials && !dl::aligned16(workspace)) || !dl::aligned16(kv->k) || !dl::aligned16(kv->v) || !dl::aligned16(q) ||
         (q_stride % 4) != 0 || (kv->region_stride * (kv->elem_bytes == 4 ? 4 : kv->elem_bytes == 1 ? 1 : 2)) % 16 != 0)
         return dl::fail(DL_E_ALIGN, "dl_decode_attn: q, cache planes and workspace must be 16-byte aligned");
     if (q_stride < (int64_t)plan->n_q * plan->head_dim) return dl::fail(DL_E_ARG, "dl_decode_attn: q_stride too small");
@@ -1552,13 +1684,21 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     a.capacity = kv->capacity;
     a.seqlen = seqlen;
     const size_t po = (size_t)plan->rows * plan->n_q * plan->max_splits * plan->head_dim * 4;
-    if (!co) {
+    const size_t pl = (size_t)plan->rows * plan->n_q * plan->max_splits * 4;
+    if (partials) {
         a.part_o = static_cast<float *>(workspace);
         a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((po + 15) / 16) * 16);
-    } else {
+        a.counters = reinterpret_cast<int *>(static_cast<char *>(workspace) + ((po + 15) / 16) * 16 +
+                                             ((pl + 15) / 16) * 16);
+    }
+    if (co) {
+        if (co->out_stride < (int64_t)plan->n_q * plan->head_dim || !dl::aligned16(co->out) || co->out_stride % 4)
+            return dl::fail(DL_E_ARG, "dl_decode_attn: out must be 16-byte aligned with a stride of at least "
+                                      "n_q * head_dim (a multiple of 4)");
         a.out = co->out;
         a.out_stride = co->out_stride;
         a.lse_out = co->lse;
+        a.tail_merge = tail ? 1 : 0;
     }
     a.status = status;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)plan->head_dim));
@@ -1592,6 +1732,9 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     int qmax = 0;
     for (int si = 0; si < plan->n_sessions; ++si)
         qmax = std::max(qmax, (plan->sess_begin[si + 1] - plan->sess_begin[si]) * (plan->n_q / plan->n_kv));
+    if (tail && qmax > kTailMaxQ)
+        return dl::fail(DL_E_SHAPE, "dl_decode_attn_merged: %d queries per work item (the last piece merges at "
+                                    "most %d)", qmax, kTailMaxQ);
     // the f32 mirror is read on CUDA cores only (the tensor form takes f16 operands; q8_0 codes
     // are exact in f16)
     const int eb = kv->elem_bytes == 0 ? 2 : kv->elem_bytes;
@@ -1616,7 +1759,7 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
                         : (plan->head_dim == 128 ? pick_attn_kernel<128, 2>(mma, qm) : pick_attn_kernel<64, 2>(mma, qm));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attn: set shared memory");
-    if (!co)
+    if (!co || tail)
         return dl::launch_pdl(kern, dim3(plan->n_work), dim3(kMmaThreads), smem, st, "dl_decode_attn: launch", a, tk, tv);
     // one thread-block cluster per (session, KV head): its pieces are consecutive work items
     if (plan->cluster > 8) {
@@ -1674,6 +1817,21 @@ int dl_decode_attn_cluster(const float *q, int64_t q_stride, const dl_attn_rope_
     const FusedIn f{rope_in->k, rope_in->v, rope_in->bias, rope_in->k_stride, rope_in->v_stride, rope_in->pos,
                     rope_in->rope};
     return decode_attn_impl(q, q_stride, kv, seqlen, plan, nullptr, 0, status, path, stream, &f, &co);
+}
+
+int dl_decode_attn_merged(const float *q, int64_t q_stride, const dl_attn_rope_in *rope_in,
+                          const dl_kv_cache *kv, const int32_t *seqlen, const dl_attn_plan *plan,
+                          void *workspace, size_t workspace_bytes, float *out, int64_t out_stride, float *lse,
+                          int32_t *status, int path, dl_stream_t stream)
+{
+    const ClusterOut co{out, out_stride, lse};
+    if (!rope_in)
+        return decode_attn_impl(q, q_stride, kv, seqlen, plan, workspace, workspace_bytes, status, path, stream,
+                                nullptr, &co, true);
+    const FusedIn f{rope_in->k, rope_in->v, rope_in->bias, rope_in->k_stride, rope_in->v_stride, rope_in->pos,
+                    rope_in->rope};
+    return decode_attn_impl(q, q_stride, kv, seqlen, plan, workspace, workspace_bytes, status, path, stream, &f,
+                            &co, true);
 }
 
 int dl_decode_attn_rope(const float *q, int64_t q_stride, const float *k, int64_t k_stride,

@@ -15,6 +15,8 @@ tiles (the schedule that measured best at eight rows; it is off by default,
 since at one row it measured slower); with
 `cluster_merge`, dl_decode_attn_cluster in place of the attention and the merge
 (the pieces of a KV head merge inside their thread-block cluster); with
+`tail_merge`, dl_decode_attn_merged in place of them for commands whose work
+items serve at most eight queries (the last piece of a KV head merges); with
 `gemv_chain`, the O, gate/up and down projections as the phases of one
 dl_gemv_q8_chain launch.  A step of several commands (sessions past eight rows)
 may run them on streams of their own (`concurrent`), since they share nothing
@@ -33,7 +35,8 @@ from typing import Dict, List, Optional, Sequence
 import torch
 
 from . import (KVCache, PackedQ8, Rope, dl_attn_merge, dl_attn_plan_build, dl_attn_plan_build_cluster,
-               dl_decode_attn, dl_decode_attn_cluster, dl_decode_attn_rope, dl_gemv_q8, dl_gemv_q8_chain,
+               dl_decode_attn, dl_decode_attn_cluster, dl_decode_attn_merged, dl_decode_attn_rope, dl_gemv_q8,
+               dl_gemv_q8_chain,
                dl_l2_prefetch_next, dl_plan_groups, dl_rope_kv_store, workspace_for)
 
 
@@ -64,7 +67,8 @@ class Command:
     def __init__(self, rows: Sequence[int], positions: Sequence[int], regions: Sequence[int],
                  n_q: int, n_kv: int, head_dim: int, hidden: int, ffn: int, device, sm_count: int = 0,
                  force_chunk: int = 0, gemv_path: int = 0, attn_path: int = 0, fused_rope: bool = False,
-                 cluster_merge: bool = False, gemv_chain: bool = False, l2_prefetch: bool = False):
+                 cluster_merge: bool = False, gemv_chain: bool = False, l2_prefetch: bool = False,
+                 tail_merge: bool = False):
         n = len(rows)
         assert 1 <= n <= 8
         self.l2_prefetch = bool(l2_prefetch)
@@ -79,6 +83,9 @@ class Command:
         self.positions = [int(p) for p in positions]
         self.regions = [int(r) for r in regions]
         self.seqlen_host = [p + 1 for p in self.positions]
+        # the last piece merges when a work item serves at most 8 queries (sessions of few rows)
+        sess_rows = max(self.regions.count(r) for r in set(self.regions))
+        self.tail_merge = bool(tail_merge) and not cluster_merge and sess_rows * (n_q // n_kv) <= 8
         if self.cluster_merge:
             self.plan = dl_attn_plan_build_cluster(self.seqlen_host, n_q, n_kv, D, regions=self.regions,
                                                    sm_count=sm_count)
@@ -122,6 +129,13 @@ class Command:
                                  status=self.status, stream=stream)
                 dl_decode_attn_cluster(self.q, kv, self.seqlen, self.plan, self.attn, self.lse, status=self.status,
                                        stream=stream, path=self.attn_path)
+        elif self.tail_merge:
+            rin = dict(k=self.k, v=self.v, pos=self.pos, rope=rope) if self.fused_rope else {}
+            if not self.fused_rope:
+                dl_rope_kv_store(self.q, self.k, self.v, self.pos, rope, kv, self.n_q, row_region=self.region,
+                                 status=self.status, stream=stream)
+            dl_decode_attn_merged(self.q, kv, self.seqlen, self.plan, self.workspace, self.attn, self.lse,
+                                  status=self.status, stream=stream, path=self.attn_path, **rin)
         elif self.fused_rope:
             dl_decode_attn_rope(self.q, self.k, self.v, self.pos, rope, kv, self.seqlen, self.plan,
                                 self.workspace, status=self.status, stream=stream, path=self.attn_path)
@@ -130,7 +144,7 @@ class Command:
                              status=self.status, stream=stream)
             dl_decode_attn(self.q, kv, self.seqlen, self.plan, self.workspace, status=self.status, stream=stream,
                            path=self.attn_path)
-        if not self.cluster_merge:
+        if not self.cluster_merge and not self.tail_merge:
             if pf:
                 _prefetch_head(W.wgu, 0.5)
             dl_attn_merge(self.workspace, self.plan, self.seqlen, self.attn, self.lse, stream=stream)
@@ -147,7 +161,8 @@ class Command:
 
     @property
     def launches(self) -> int:
-        return 7 - int(self.fused_rope) - int(self.cluster_merge) - 2 * int(self.gemv_chain)
+        return (7 - int(self.fused_rope) - int(self.cluster_merge or self.tail_merge) -
+                2 * int(self.gemv_chain))
 
 
 class LayerStep:
@@ -156,7 +171,8 @@ class LayerStep:
     def __init__(self, positions: Sequence[int], regions: Sequence[int], n_q: int, n_kv: int, head_dim: int,
                  hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0, gemv_path: int = 0,
                  attn_path: int = 0, fused_rope: bool = False, cluster_merge: bool = False,
-                 gemv_chain: bool = False, l2_prefetch: bool = False, concurrent: bool = False):
+                 gemv_chain: bool = False, l2_prefetch: bool = False, concurrent: bool = False,
+                 tail_merge: bool = False):
         """concurrent: the commands (independent sessions) run on streams of their own, forked
         from the caller's stream and joined back into it, so that one command's launch latencies
         overlap another's work."""
@@ -169,7 +185,7 @@ class LayerStep:
             self.commands.append(Command(idx, [positions[i] for i in idx], [regions[i] for i in idx],
                                          n_q, n_kv, head_dim, hidden, ffn, device, sm_count, force_chunk,
                                          gemv_path, attn_path, fused_rope, cluster_merge, gemv_chain,
-                                         l2_prefetch))
+                                         l2_prefetch, tail_merge))
             r0 += s
         self.group_sizes = sizes
         self.concurrent = bool(concurrent) and len(self.commands) > 1

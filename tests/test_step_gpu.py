@@ -27,7 +27,7 @@ def dl():
 
 
 def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=False, cluster_merge=False,
-          gemv_chain=False, l2_prefetch=False, concurrent=False):
+          gemv_chain=False, l2_prefetch=False, concurrent=False, tail_merge=False):
     from row_decode_step_gb300.step import LayerStep, LayerWeights
     D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
     blocks = layer_blocks(S.name)
@@ -44,7 +44,7 @@ def _step(dl, S, positions, regions, n_regions, capacity, label, fused_rope=Fals
     h = synth.normal_f32(0, label + "/h", (n, F)) if F else None
     step = LayerStep(positions, regions, n_q, n_kv, D, H, F, "cuda", fused_rope=fused_rope,
                      cluster_merge=cluster_merge, gemv_chain=gemv_chain, l2_prefetch=l2_prefetch,
-                     concurrent=concurrent)
+                     concurrent=concurrent, tail_merge=tail_merge)
     r0 = 0
     for c in step.commands:
         c.x.copy_(x[r0:r0 + c.n].cuda())
@@ -130,3 +130,19 @@ def test_step_twelve_streams_concurrent(dl):
     step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams", fused_rope=True,
                  concurrent=True)
     assert step.concurrent and step.group_sizes == [6, 6]
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("rows", [1, 2])
+def test_step_3b_tail_merge(dl, rows, fused):
+    """The attention's last piece merges (one launch fewer) at 3 and 6 queries per KV head."""
+    step = _step(dl, synth.LLAMA_3B, list(range(5120, 5120 + rows)), [0] * rows, 1, 5128, "step/3b%d" % rows,
+                 fused_rope=fused, tail_merge=True)
+    assert step.commands[0].tail_merge
+
+
+def test_step_twelve_streams_tail_merge(dl):
+    lens = synth.twelve_stream_lengths(0)
+    step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams", fused_rope=True,
+                 tail_merge=True, concurrent=True)
+    assert all(c.tail_merge for c in step.commands)
