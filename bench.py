@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--workload", default="3b-8", choices=["3b-8", "3b-1", "3b-12", "1b-1", "3b-8-32k"])
     p.add_argument("--no-extras", action="store_true", help="skip the 1-row and 12-stream side measurements")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--breakdown", action="store_true",
+                   help="only the step breakdown: each launch timed alone and the step without it (3B, 8 and 1 rows)")
     p.add_argument("--side-only", action="store_true",
                    help="only the side measurements (f16-weight GEMV, attention on each KV mirror), a few "
                         "repetitions each: a small program for profilers")
@@ -532,6 +534,63 @@ def combine_ranks(ms_local, steps, world, device):
     return ms, world * steps / (ms / 1e3)
 
 
+def measure_breakdown(wl, L, dev, reps=50):
+    """Where the step's time goes: each launch of the default step form timed alone (its L
+    layers back to back in one CUDA graph) and the step timed without it, us per layer."""
+    import synth
+    import torch
+    import row_decode_step_gb300 as dl
+    from row_decode_step_gb300.step import LayerStep
+    S = wl["shape"]
+    layers, caches = build_layers(wl, L, dev)
+    rope = dl.make_rope(S.rope_theta, S.head_dim, wl["capacity"], device=dev)
+    c = LayerStep(wl["positions"], wl["regions"], S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, dev).commands[0]
+    c.x.copy_(synth.normal_f32(0, "bench/x0", tuple(c.x.shape), device=dev))
+    c.x_ffn.copy_(synth.normal_f32(0, "bench/xf0", tuple(c.x_ffn.shape), device=dev))
+    c.h.copy_(synth.normal_f32(0, "bench/h0", tuple(c.h.shape), device=dev))
+    launch = {
+        "qkv": lambda l: dl.dl_gemv_q8(layers[l].wqkv, c.x, c.qkv),
+        "attention+rope": lambda l: dl.dl_decode_attn_rope(c.q, c.k, c.v, c.pos, rope, caches[l], c.seqlen, c.plan,
+                                                           c.workspace, status=c.status),
+        "merge": lambda l: dl.dl_attn_merge(c.workspace, c.plan, c.seqlen, c.attn, c.lse),
+        "o": lambda l: dl.dl_gemv_q8(layers[l].wo, c.attn, c.y_o),
+        "gate/up": lambda l: dl.dl_gemv_q8(layers[l].wgu, c.x_ffn, c.gu),
+        "down": lambda l: dl.dl_gemv_q8(layers[l].wdown, c.h, c.y_down),
+    }
+    order = list(launch)
+    stream = torch.cuda.Stream(device=dev)
+
+    def timed(names):
+        with torch.cuda.stream(stream):
+            for l in range(L):
+                for n in names:
+                    launch[n](l)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(L):
+                for n in names:
+                    launch[n](l)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (reps * L)
+
+    full = timed(order)
+    out = {"workload": wl["desc"], "step_us": full, "launches": {}}
+    for n in order:
+        alone, without = timed([n]), timed([o for o in order if o != n])
+        out["launches"][n] = {"alone_us": alone, "step_without_us": without, "share_of_step_us": full - without}
+    return out
+
+
 def run_ours(args):
     import torch
     import row_decode_step_gb300 as dl
@@ -548,6 +607,11 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     dl.lib()
+    if args.breakdown:
+        if rank == 0:
+            for name in ("3b-8", "3b-1"):
+                print(json.dumps({"breakdown": measure_breakdown(workload(name), args.layers, dev)}))
+        return
     if args.side_only:
         peak, _ = hbm_peak()
         side = {"f16w_gemv": measure_f16w(dev, peak, mats=2, reps=2),
