@@ -52,8 +52,9 @@
  *         in f32; the attention decodes d * code on CUDA cores, or on tensor cores
  *         with the codes as exact f16 operands, each key's block scale applied to
  *         its 32-dimension score sums (f32) and to the V operand (rounded once to
- *         f16); no rope fused into the attention.  Requires capacity % 4 == 0 and
- *         the region stride a multiple of 256 values (16-byte aligned scale rows).
+ *         f16).  The rope/store inside the attention launch encodes the new rows
+ *         exactly as dl_rope_kv_store does.  Requires capacity % 4 == 0 and the
+ *         region stride a multiple of 256 values (16-byte aligned scale rows).
  *  [ROPE] daScript PR #4293 "dasLLAMA llama leg ...", commit "The decode
  *         rope-and-store rides one template on both homes" (GkRopeKvStore).
  *  [GRP]  the same PR, commit "The Vulkan batched step past eight rows runs in

@@ -55,6 +55,7 @@ struct AttnArgs {
     int rot, neox, max_pos;
     // the q8_0 mirror's f16 scale planes (one scale per 32 values of a key row)
     const uint16_t *ksc, *vsc;
+    uint16_t *ksc_w, *vsc_w;    // the same planes, written by the fused store
     // merge inside the launch (plan.cluster = C > 0): the results go straight to out / lse_out
     float *out, *lse_out;
     int64_t out_stride;
@@ -358,7 +359,53 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         const int owner_last = (lmax - 1) / P.chunk;
         const int hp = D / 2;
         if (cs_staged && !dla::mbar_wait(&csbar, 0u)) bad = true;
-        if (!bad) {
+        if (KVQ8 && !bad) {
+            // the q8_0 mirror: a warp per (row, k or v, block of 32 channels), lane = channel, with
+            // the separate store's arithmetic (bias, then the rotation of the channel's pair from
+            // the unrotated input; d = max|x| / 127 in f32, codes rounded half away from zero)
+            constexpr int NB = D / 32;
+            for (int t = warp; t < nrows * 2 * NB; t += kMmaConsumers + 1) {
+                const int i = t / (2 * NB), rem = t - i * (2 * NB), isv = rem / NB, b = rem - isv * NB;
+                const int p = s_pos[i];
+                if (min(max(p, 0) / P.chunk, owner_last) != piece) continue;
+                if (p < 0 || p >= a.capacity || p >= a.max_pos) {
+                    if (rem == 0 && lane == 0) dl_status_or(a.status, DL_STATUS_POS_RANGE);
+                    continue;
+                }
+                const int r = s_row[i];
+                const int c = 32 * b + lane;
+                float x;
+                if (isv) {
+                    x = a.v_new[(int64_t)r * a.v_stride + (int64_t)h * D + c];
+                    if (a.bias) x += a.bias[(int64_t)(P.n_q + P.n_kv + h) * D + c];
+                } else {
+                    const float *kr = a.k_new + (int64_t)r * a.k_stride + (int64_t)h * D;
+                    const float *bk = a.bias ? a.bias + (int64_t)(P.n_q + h) * D : nullptr;
+                    x = kr[c] + (bk ? bk[c] : 0.f);
+                    if (c < a.rot) {
+                        const int j = a.neox ? (c < rh ? c : c - rh) : (c >> 1);
+                        const int i0 = a.neox ? j : 2 * j, i1 = a.neox ? j + rh : 2 * j + 1;
+                        const float x0 = kr[i0] + (bk ? bk[i0] : 0.f), x1 = kr[i1] + (bk ? bk[i1] : 0.f);
+                        const float2 cs = cs_at(i, p, j);
+                        x = c == i0 ? fmaf(x0, cs.x, -x1 * cs.y) : fmaf(x0, cs.y, x1 * cs.x);
+                    }
+                }
+                float m = fabsf(x);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                const float d32 = m / 127.0f;
+                int code = 0;
+                if (d32 > 0.f) {
+                    const float tq = x / d32;
+                    const float rr = floorf(fabsf(tq) + 0.5f);
+                    code = (int)(tq < 0.f ? -rr : rr);
+                    code = max(-127, min(127, code));
+                }
+                const int64_t base = (int64_t)reg * a.region_stride + ((int64_t)h * a.capacity + p) * D;
+                static_cast<int8_t *>(isv ? a.vc_w : a.kc_w)[base + c] = (int8_t)code;
+                if (lane == 0) (isv ? a.vsc_w : a.ksc_w)[(base + 32 * b) / 32] = __half_as_ushort(__float2half_rn(d32));
+            }
+        } else if (!bad) {
 #pragma unroll 4
             for (int e = tid; e < nrows * hp; e += kMmaThreads) {
                 const int i = e / hp, jp = e - i * hp;
@@ -390,9 +437,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     k1 = y1;
                 }
                 const int64_t base = (int64_t)reg * a.region_stride + ((int64_t)h * a.capacity + p) * D;
-                if constexpr (KVQ8) {
-                    // (the fused form is refused for the q8_0 mirror before any launch)
-                } else if constexpr (KV32) {
+                if constexpr (KV32) {
                     float *kcw = static_cast<float *>(a.kc_w), *vcw = static_cast<float *>(a.vc_w);
                     kcw[base + i0] = k0;
                     kcw[base + i1] = k1;
@@ -1659,7 +1704,6 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
             return dl::fail(DL_E_SHAPE, "dl_decode_attn: the q8_0 mirror wants capacity %% 4 == 0 and a region "
                                         "stride that is a multiple of 256 (capacity %d, stride %lld)",
                             kv->capacity, (long long)kv->region_stride);
-        if (f) return dl::fail(DL_E_SHAPE, "dl_decode_attn_rope: the rope is not fused for the q8_0 mirror");
     }
     for (int r = 0; r < plan->rows; ++r) {
         if (plan->row_region[r] >= kv->n_regions) return dl::fail(DL_E_ARG, "dl_decode_attn: plan region past the cache");
@@ -1743,6 +1787,8 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     const bool mma = eb != 4 && (path == 2 || (path == 0 && qmax > kCudaCoreMaxQ));
     a.ksc = static_cast<const uint16_t *>(kv->k_scale);
     a.vsc = static_cast<const uint16_t *>(kv->v_scale);
+    a.ksc_w = static_cast<uint16_t *>(kv->k_scale);
+    a.vsc_w = static_cast<uint16_t *>(kv->v_scale);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     CUtensorMap tk, tv;
     rc = make_kv_tmap(&tk, kv->k, kv);

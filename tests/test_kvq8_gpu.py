@@ -133,20 +133,78 @@ def test_q8_sessions_and_cluster(dl, path):
         assert_attn_close(out.cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse)
 
 
+@pytest.mark.parametrize("form", ["partials", "cluster", "merged"])
+@pytest.mark.parametrize("rows,D,neox,rot,bias", [(1, 128, True, 128, False), (8, 128, True, 128, True),
+                                                  (2, 64, False, 32, False)])
+def test_q8_fused_rope(dl, form, rows, D, neox, rot, bias):
+    """The rope/store inside the attention launch on the q8_0 mirror: stored codes and scales,
+    outputs and lse bit-identical to dl_rope_kv_store followed by the attention; outputs within
+    the oracle's bars."""
+    n_kv = 8
+    n_q = 24 if D == 128 else 32
+    if form == "merged" and rows * n_q // n_kv > 8:
+        pytest.skip("the last piece merges at most 8 queries")
+    cap = 5128
+    pos = list(range(5120, 5120 + rows))
+    seqlen = [p + 1 for p in pos]
+    kc, ks, vc, vs = _planes("q8f/%d/%d" % (rows, D), 1, n_kv, cap, D)
+    q = synth.normal_f32(4, "q8f/q/%d/%d" % (rows, D), (rows, n_q * D))
+    k = synth.normal_f32(4, "q8f/k/%d/%d" % (rows, D), (rows, n_kv * D))
+    v = synth.normal_f32(4, "q8f/v/%d/%d" % (rows, D), (rows, n_kv * D))
+    b = synth.normal_f32(4, "q8f/b/%d" % D, ((n_q + 2 * n_kv) * D,)).cuda() if bias else None
+    rope = dl.make_rope(500000.0, rot, cap, neox=neox)
+    dpos = torch.tensor(pos, dtype=torch.int32, device="cuda")
+    sl = torch.tensor(seqlen, dtype=torch.int32, device="cuda")
+    plan = (dl.dl_attn_plan_build_cluster(seqlen, n_q, n_kv, D) if form == "cluster"
+            else dl.dl_attn_plan_build(seqlen, n_q, n_kv, D))
+    res = {}
+    for mode in ("fused", "separate"):
+        kv = _cache(dl, kc, ks, vc, vs)
+        qd = q.clone().cuda()
+        out = torch.full((rows, n_q * D), float("nan"), device="cuda")
+        lse = torch.full((rows, n_q), float("nan"), device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        rin = dict(k=k.cuda(), v=v.cuda(), pos=dpos, rope=rope, bias=b) if mode == "fused" else {}
+        if mode == "separate":
+            dl.dl_rope_kv_store(qd, k.cuda(), v.cuda(), dpos, rope, kv, n_q, bias=b, status=status)
+        if form == "cluster":
+            dl.dl_decode_attn_cluster(qd, kv, sl, plan, out, lse, status=status, **rin)
+        elif form == "merged":
+            dl.dl_decode_attn_merged(qd, kv, sl, plan, dl.workspace_for(plan), out, lse, status=status, **rin)
+        else:
+            ws = dl.workspace_for(plan)
+            if mode == "fused":
+                dl.dl_decode_attn_rope(qd, k.cuda(), v.cuda(), dpos, rope, kv, sl, plan, ws, bias=b, status=status)
+            else:
+                dl.dl_decode_attn(qd, kv, sl, plan, ws, status=status)
+            dl.dl_attn_merge(ws, plan, sl, out, lse)
+        torch.cuda.synchronize()
+        assert dl.dl_status_read(status) == 0
+        res[mode] = [kv.k.cpu().numpy(), kv.k_scale.cpu().numpy().view(np.uint16), kv.v.cpu().numpy(),
+                     kv.v_scale.cpu().numpy().view(np.uint16), out.cpu().numpy(), lse.cpu().numpy()]
+    for x, y in zip(res["fused"], res["separate"]):
+        assert np.array_equal(x, y)
+    kp, vp = _oracle_planes(torch.from_numpy(res["fused"][0]), torch.from_numpy(res["fused"][1].view(np.float16)),
+                            torch.from_numpy(res["fused"][2]), torch.from_numpy(res["fused"][3].view(np.float16)))
+    qo = q.numpy().astype(np.float64).copy()
+    ko = oracle.Q8Plane(kc.numpy().copy(), ks.numpy().view(np.uint16).copy())
+    vo = oracle.Q8Plane(vc.numpy().copy(), vs.numpy().view(np.uint16).copy())
+    qo = oracle.rope_kv_store(q, k, v, np.array(pos, np.int32), ko, vo, n_q=n_q, n_kv=n_kv, head_dim=D, rot_dim=rot,
+                              theta=500000.0, neox=neox, bias=None if b is None else b.cpu().numpy())
+    # the attention is checked on the mirror as the GPU stored it (the stored k codes may differ
+    # from the oracle's by one: rotation in f32 against double)
+    ref_out, ref_lse = oracle.attention(np.asarray(qo, np.float64), kp, vp, np.array(seqlen, np.int32), n_q=n_q,
+                                        n_kv=n_kv, head_dim=D, chunk=plan.chunk, n_splits=plan.max_splits)
+    assert_attn_close(res["fused"][4], res["fused"][5], ref_out, ref_lse)
+
+
 def test_q8_refusals(dl):
-    """The fused rope and a capacity that is not a multiple of 4 are refused before anything
-    launches."""
+    """A capacity that is not a multiple of 4 is refused before anything launches."""
     kc, ks, vc, vs = _planes("q8a/refuse", 1, 2, 64, 64)
-    kv = _cache(dl, kc, ks, vc, vs)
-    plan = dl.dl_attn_plan_build([64], 4, 2, 64)
-    ws = dl.workspace_for(plan)
     q = torch.zeros(1, 256, device="cuda")
     sl = torch.tensor([64], dtype=torch.int32, device="cuda")
-    rope = dl.make_rope(500000.0, 64, 64)
-    with pytest.raises(dl.DLError) as e:
-        dl.dl_decode_attn_rope(q, torch.zeros(1, 128, device="cuda"), torch.zeros(1, 128, device="cuda"),
-                               torch.tensor([63], dtype=torch.int32, device="cuda"), rope, kv, sl, plan, ws)
-    assert e.value.code == dl.DL_E_SHAPE
+    plan = dl.dl_attn_plan_build([64], 4, 2, 64)
+    ws = dl.workspace_for(plan)
     kc2, ks2, vc2, vs2 = _planes("q8a/refuse2", 1, 2, 66, 64)
     kv2 = _cache(dl, kc2, ks2, vc2, vs2)
     with pytest.raises(dl.DLError) as e:
