@@ -44,8 +44,9 @@
  *         distributed shared memory instead of a separate merge pass.
  *  [KV32] daScript PR #4293, "Tests": the rope-and-store template also serves an
  *         f32 mirror (RopeKvStore's f32 stamp) beside the default f16 one.  With
- *         it every stored value is rounded once to f32 (no clamp), and the
- *         attention runs on CUDA cores (the tensor form reads f16 operands).
+ *         it every stored value is rounded once to f32 (no clamp).  The
+ *         attention's tensor form splits the values (and the probabilities)
+ *         into bf16 hi + lo pairs, keeping f32's exponent range.
  *  [KVQ8] daScript PR #4293 ("_regions_q8kv" and the block-codec mirror): K and V
  *         kept as Q8_0 blocks of 32 values.  Here: per block the scale d = max|x| / 127
  *         (f32, stored as f16) and codes round(x / d) half away from zero, both decided
@@ -409,8 +410,9 @@ int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv,
  * measurement): path 0 = automatic (what dl_decode_attn does: CUDA cores when a
  * work item serves at most 4 queries, tensor cores above), 1 = f32 CUDA-core
  * dot products, 2 = 16x8x16 f16 tensor-core products with q split into two f16
- * terms (hi + lo) and probabilities in f16, f32 accumulation and softmax.  The
- * f32 mirror refuses path 2 (DL_E_SHAPE) and takes path 1 whatever path 0 sees.
+ * terms (hi + lo) and probabilities in f16, f32 accumulation and softmax.  On
+ * the f32 mirror path 2 takes q, the keys, the probabilities and the values as
+ * bf16 hi + lo pairs (three products per pair of operands, f32 accumulation).
  */
 int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv,
                       const int32_t *seqlen, const dl_attn_plan *plan,

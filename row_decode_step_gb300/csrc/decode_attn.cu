@@ -13,6 +13,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
+#include <cuda_bf16.h>
 #include <cmath>
 #include <cstring>
 #include <algorithm>
@@ -167,6 +168,25 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two f32 values as bf16 pairs: hi = the values rounded to bf16, lo = the remainders rounded
+// to bf16 (hi + lo carries 16 bits of each significand, over f32's whole exponent range).
+__device__ __forceinline__ void bf16x2_split(float x, float y, uint32_t &hi, uint32_t &lo)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
 __device__ __forceinline__ uint32_t h2_bits(float lo, float hi)
 {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -230,9 +250,10 @@ __device__ __forceinline__ bool attn_consumers_any(bool flag)
 }
 
 // EB: bytes per element of the mirror: 2 the f16 mirror, 4 the f32 mirror, 1 the q8_0 mirror
-// (codes; the scales ride along). The f32 mirror takes the CUDA-core form only, since the
-// tensor form reads f16 operands; the q8_0 codes are exact f16 operands, with each key's block
-// scales applied to the score sums and to the V operand.
+// (codes; the scales ride along). In the tensor form the f32 mirror's values and the
+// probabilities enter as bf16 hi + lo pairs (f32's range, about 16 bits of each significand),
+// and the q8_0 codes as exact f16 operands, with each key's block scales applied to the score
+// sums and to the V operand.
 template <int D, bool MMA, int QM, int EB = 2>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tk,
@@ -240,7 +261,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
 {
     constexpr int NKS = D / 16;     // k-steps of the score product
     constexpr int NDT = D / 8;      // 8-wide column tiles of the output
-    static_assert(!(MMA && EB == 4), "the tensor form reads f16 values or q8_0 codes");
+
     constexpr bool KV32 = EB == 4, KVQ8 = EB == 1;
     constexpr int EPB = KVQ8 ? D : 128 / EB;  // elements per box row (q8_0: the whole key row)
     constexpr int NH = D / EPB;               // boxes per key row
@@ -768,7 +789,9 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
     float *cl = cm + kMmaConsumers * 16;
     if constexpr (MMA) {
         // ---- query operand fragments (log2-domain scaled, hi + lo f16 terms) in shared memory:
-        // [query tile][k-step][hi, lo][lane] 16 bytes = a0..a3.  On the q8_0 mirror the
+        // [query tile][k-step][hi, lo][lane] 16 bytes = a0..a3.  On the f32 mirror the terms are
+        // bf16 (f32's exponent range) and the lane quad c of k-step ks holds dimensions
+        // 16 ks + 4c .. 16 ks + 4c + 3 (one 16-byte read of a key row).  On the q8_0 mirror the
         // dimensions are permuted within each 32-dimension block (the order of a sum is free when
         // both operands follow it): k-step 2b + e, column pair p of lane quad c holds dimensions
         // 32b + 8c + 4e + 2p + {0, 1}, so that a key's codes of both k-steps of block b are the 8
@@ -787,15 +810,20 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             for (int part = 0; part < 4; ++part) {
                 const float *src = (part & 1) ? q1 : q0;
                 const int col = KVQ8 ? 32 * (ks >> 1) + 8 * cc + 4 * (ks & 1) + (part >> 1) * 2
+                              : KV32 ? ks * 16 + 4 * cc + (part >> 1) * 2
                                      : ks * 16 + 2 * cc + (part >> 1) * 8;
                 float2 v = make_float2(0.f, 0.f);
                 if (src) v = *reinterpret_cast<const float2 *>(src + col);
                 v.x *= a.qscale;
                 v.y *= a.qscale;
-                const __half2 hq = __floats2half2_rn(v.x, v.y);
-                const float2 hf = __half22float2(hq);
-                hv[part] = *reinterpret_cast<const uint32_t *>(&hq);
-                lv[part] = h2_bits(v.x - hf.x, v.y - hf.y);
+                if constexpr (KV32) {
+                    bf16x2_split(v.x, v.y, hv[part], lv[part]);
+                } else {
+                    const __half2 hq = __floats2half2_rn(v.x, v.y);
+                    const float2 hf = __half22float2(hq);
+                    hv[part] = *reinterpret_cast<const uint32_t *>(&hq);
+                    lv[part] = h2_bits(v.x - hf.x, v.y - hf.y);
+                }
             }
             uint4 *dst = reinterpret_cast<uint4 *>(qfrag + (size_t)(fi >> 5) * 1024 + t * 16);
             dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
@@ -849,7 +877,31 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
                 sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
             }
-            if constexpr (KVQ8) {
+            if constexpr (KV32) {
+                // lane (g, c) reads key g's four dimensions 16 ks + 4c .. + 3 (one 16-byte chunk
+                // of its swizzled 128-byte box row) and splits them into bf16 hi + lo; the products
+                // q_hi k_hi, q_lo k_hi and q_hi k_lo keep about 16 bits of each operand
+                const unsigned char *kst = ring + (size_t)st * kStageBytes;
+    #pragma unroll
+                for (int ks = 0; ks < NKS; ++ks) {
+                    const uint4 qa = *reinterpret_cast<const uint4 *>(myq + ks * 1024);
+                    const uint4 qb = *reinterpret_cast<const uint4 *>(myq + ks * 1024 + 512);
+                    const uint32_t qh[4] = {qa.x, qa.y, qa.z, qa.w}, ql[4] = {qb.x, qb.y, qb.z, qb.w};
+                    const int chunk = 4 * (ks & 1) + c;
+    #pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const int key = nt * 8 + g;
+                        const float4 kf = *reinterpret_cast<const float4 *>(
+                            kst + (ks >> 1) * kHalfTile + key * 128 + ((chunk ^ (key & 7)) << 4));
+                        uint32_t h0, l0, h1, l1;
+                        bf16x2_split(kf.x, kf.y, h0, l0);
+                        bf16x2_split(kf.z, kf.w, h1, l1);
+                        mma_bf16(sc[nt], qh, h0, h1);
+                        mma_bf16(sl[nt], ql, h0, h1);
+                        mma_bf16(sl[nt], qh, l0, l1);
+                    }
+                }
+            } else if constexpr (KVQ8) {
                 // per 32-dimension block b: lane (g, c) takes key g's 8 codes at 32b + 8c (both
                 // k-steps of the block), the block's products accumulate apart and are scaled by
                 // the key's scale of that block (the columns 2c, 2c + 1 of the fragment)
@@ -956,7 +1008,45 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                 }
             }
             // O += P V over two 16-key steps: two 8-wide output tiles per transposed 4-matrix load
-            if constexpr (KVQ8) {
+            if constexpr (KV32) {
+                // output column n of tile j is dimension (D / 8) n + j: lane (g, c) reads the D / 8
+                // contiguous values at (D / 8) g of its keys 2c, 2c + 1, 2c + 8, 2c + 9, four at a
+                // time, and P and V enter as bf16 hi + lo (P_hi V_hi + P_lo V_hi + P_hi V_lo)
+                const unsigned char *vst = ring + (size_t)st * kStageBytes + kVOff;
+                constexpr int VB = D / 8;
+                const int d0 = VB * g;
+                const unsigned char *vbox = vst + (d0 >> 5) * kHalfTile;
+                const int ch0 = (d0 & 31) >> 2;
+    #pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    uint32_t ph[4], pl[4];
+                    bf16x2_split(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
+                    bf16x2_split(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
+                    bf16x2_split(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
+                    bf16x2_split(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
+    #pragma unroll
+                    for (int m = 0; m < VB / 4; ++m) {
+                        float4 w[4];
+    #pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int key = kk * 16 + 2 * c + (u & 1) + (u >> 1) * 8;
+                            w[u] = *reinterpret_cast<const float4 *>(vbox + key * 128 + (((ch0 + m) ^ (key & 7)) << 4));
+                        }
+                        const float v0[4] = {w[0].x, w[0].y, w[0].z, w[0].w}, v1[4] = {w[1].x, w[1].y, w[1].z, w[1].w};
+                        const float v2[4] = {w[2].x, w[2].y, w[2].z, w[2].w}, v3[4] = {w[3].x, w[3].y, w[3].z, w[3].w};
+    #pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            uint32_t bh0, bl0, bh1, bl1;
+                            bf16x2_split(v0[jj], v1[jj], bh0, bl0);
+                            bf16x2_split(v2[jj], v3[jj], bh1, bl1);
+                            float (&oj)[4] = o[4 * m + jj];
+                            mma_bf16(oj, ph, bh0, bh1);
+                            mma_bf16(oj, pl, bh0, bh1);
+                            mma_bf16(oj, ph, bl0, bl1);
+                        }
+                    }
+                }
+            } else if constexpr (KVQ8) {
                 // output column n of tile j is dimension (D / 8) n + j, so that lane (g, c) reads
                 // the D / 8 contiguous codes at (D / 8) g of its keys 2c, 2c + 1, 2c + 8, 2c + 9 (all
                 // in block g / (256 / D)) and takes byte j of them for tile j; each pair is scaled
@@ -1035,7 +1125,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         }
     #pragma unroll
         for (int j = 0; j < NDT; ++j) {
-            if constexpr (KVQ8) {                    // column n of tile j is dimension (D / 8) n + j
+            if constexpr (KVQ8 || KV32) {            // column n of tile j is dimension (D / 8) n + j
                 const int d0 = (D / 8) * 2 * c + j, d1 = d0 + D / 8;
                 co[(warp * 16 + g) * CP + d0] = o[j][0];
                 co[(warp * 16 + g) * CP + d1] = o[j][1];
@@ -1497,13 +1587,12 @@ int check_plan(const dl_attn_plan *P)
 
 using AttnKernel = void (*)(AttnArgs, CUtensorMap, CUtensorMap);
 
-// The instantiation for a head dimension and mirror: the tensor form (f16 and q8_0 mirrors), or
-// the CUDA-core form with qm queries per warp.
+// The instantiation for a head dimension and mirror: the tensor form, or the CUDA-core form with
+// qm queries per warp.
 template <int D, int EB>
 AttnKernel pick_attn_kernel(bool mma, int qm)
 {
-    if constexpr (EB != 4)
-        if (mma) return decode_attn_tma_kernel<D, true, 8, EB>;
+    if (mma) return decode_attn_tma_kernel<D, true, 8, EB>;
     return qm == 4 ? decode_attn_tma_kernel<D, false, 4, EB>
          : qm == 6 ? decode_attn_tma_kernel<D, false, 6, EB> : decode_attn_tma_kernel<D, false, 8, EB>;
 }
@@ -1779,12 +1868,8 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     if (tail && qmax > kTailMaxQ)
         return dl::fail(DL_E_SHAPE, "dl_decode_attn_merged: %d queries per work item (the last piece merges at "
                                     "most %d)", qmax, kTailMaxQ);
-    // the f32 mirror is read on CUDA cores only (the tensor form takes f16 operands; q8_0 codes
-    // are exact in f16)
     const int eb = kv->elem_bytes == 0 ? 2 : kv->elem_bytes;
-    if (eb == 4 && path == 2)
-        return dl::fail(DL_E_SHAPE, "dl_decode_attn: the tensor form reads the f16 and q8_0 mirrors only");
-    const bool mma = eb != 4 && (path == 2 || (path == 0 && qmax > kCudaCoreMaxQ));
+    const bool mma = path == 2 || (path == 0 && qmax > kCudaCoreMaxQ);
     a.ksc = static_cast<const uint16_t *>(kv->k_scale);
     a.vsc = static_cast<const uint16_t *>(kv->v_scale);
     a.ksc_w = static_cast<uint16_t *>(kv->k_scale);
@@ -1800,7 +1885,7 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     // a work item serves 17..24 queries (four query groups keep all four consumer warps busy,
     // where groups of 8 would leave one idle); else 8
     const int qm = qmax <= 4 ? 4 : (qmax > 16 && qmax <= 24) ? 6 : 8;
-    auto kern = eb == 4 ? (plan->head_dim == 128 ? pick_attn_kernel<128, 4>(false, qm) : pick_attn_kernel<64, 4>(false, qm))
+    auto kern = eb == 4 ? (plan->head_dim == 128 ? pick_attn_kernel<128, 4>(mma, qm) : pick_attn_kernel<64, 4>(mma, qm))
               : eb == 1 ? (plan->head_dim == 128 ? pick_attn_kernel<128, 1>(mma, qm) : pick_attn_kernel<64, 1>(mma, qm))
                         : (plan->head_dim == 128 ? pick_attn_kernel<128, 2>(mma, qm) : pick_attn_kernel<64, 2>(mma, qm));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

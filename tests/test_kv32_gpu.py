@@ -62,10 +62,11 @@ def test_kv32_rope_store(dl):
 
 @pytest.mark.parametrize("rows,n_q,n_kv,D,cap", [(1, 32, 8, 64, 4097), (1, 24, 8, 128, 5128), (8, 24, 8, 128, 5128),
                                                 (4, 32, 8, 64, 3000)])
-@pytest.mark.parametrize("path,sm_count", [(0, 0), (1, 0), (0, 76)])
+@pytest.mark.parametrize("path,sm_count", [(0, 0), (1, 0), (2, 0), (0, 76)])
 def test_kv32_attention(dl, rows, n_q, n_kv, D, cap, path, sm_count):
-    """Queries per warp 4 (one row), 6 (24 queries per work item) and 8 (32); sm_count 76 is the
-    one-wave plan for the mirror's one CTA per SM at D = 128."""
+    """Both inner products: CUDA cores with 4 (one row), 6 (24 queries per work item) or 8 (32)
+    queries per warp; tensor cores on bf16 hi + lo terms (the library's choice above 4 queries).
+    sm_count 76 is the one-wave plan for the mirror's one CTA per SM at D = 128."""
     seqlen = list(range(cap - 7, cap - 7 + rows)) if rows > 1 else [cap]
     kc, vc = _planes("kv32/attn/%d/%d" % (rows, D), 1, n_kv, cap, D)
     q = synth.normal_f32(2, "kv32/attn/q/%d/%d" % (rows, D), (rows, n_q * D))
@@ -134,12 +135,23 @@ def test_kv32_fused_rope_and_cluster(dl, cluster):
     assert_attn_close(res["fused"][2], res["fused"][3], ref_out, ref_lse)
 
 
-def test_kv32_tensor_form_refused(dl):
-    kc, vc = _planes("kv32/refuse", 1, 2, 64, 64)
+@pytest.mark.parametrize("path", [1, 2])
+def test_kv32_keys_past_the_f16_range(dl, path):
+    """Keys of magnitude 1e5 (past the f16 range, the reason for the f32 mirror) with small
+    queries: both inner products against the oracle (the tensor form's bf16 terms keep f32's
+    exponent range)."""
+    rows, n_q, n_kv, D, cap = 8, 24, 8, 128, 1024
+    seqlen = list(range(cap - 7, cap + 1))
+    kc = synth.normal_f32(0, "kv32/wide/K", (1, n_kv, cap, D)) * 1e5
+    vc = synth.normal_f32(0, "kv32/wide/V", (1, n_kv, cap, D))
+    q = synth.normal_f32(5, "kv32/wide/q", (rows, n_q * D)) * 1e-5
+    assert float(kc.abs().max()) > 65504.0
+    plan = dl.dl_attn_plan_build(seqlen, n_q, n_kv, D)
     kv = dl.KVCache(kc.cuda(), vc.cuda())
-    plan = dl.dl_attn_plan_build([64], 4, 2, 64)
-    ws = dl.workspace_for(plan)
-    with pytest.raises(dl.DLError) as e:
-        dl.dl_decode_attn(torch.zeros(1, 256, device="cuda"), kv, torch.tensor([64], dtype=torch.int32, device="cuda"),
-                          plan, ws, path=2)
-    assert e.value.code == dl.DL_E_SHAPE
+    out, lse = dl.decode_attention(q.cuda(), kv, torch.tensor(seqlen, dtype=torch.int32, device="cuda"), plan,
+                                   dl.workspace_for(plan), path=path)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.attention(q.numpy().astype(np.float64), kc.numpy(), vc.numpy(),
+                                        np.array(seqlen, np.int32), n_q=n_q, n_kv=n_kv, head_dim=D,
+                                        chunk=plan.chunk, n_splits=plan.max_splits)
+    assert_attn_close(out.cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse)
