@@ -385,7 +385,7 @@ def measure_f16w(dev, peak, n_out=16384, n_in=3072, mats=4, reps=50):
     return out
 
 
-def measure_attn_mirrors(dev, peak, caches=4, reps=30):
+def measure_attn_mirrors(dev, peak, caches=4, reps=30, path=0):
     """The attention alone (work items + merge) of the 3B shape at 1 and 8 rows on the f16, f32 and
     q8_0 mirrors: `caches` distinct caches (> L2 together) cycled in one CUDA graph; bytes = the
     keys and values read + queries + outputs."""
@@ -424,7 +424,7 @@ def measure_attn_mirrors(dev, peak, caches=4, reps=30):
 
             def run():
                 for kv in kvs:
-                    dl.dl_decode_attn(q, kv, sl, plan, ws, stream=stream)
+                    dl.dl_decode_attn(q, kv, sl, plan, ws, stream=stream, path=path)
                     dl.dl_attn_merge(ws, plan, sl, o, lse, stream=stream)
             with torch.cuda.stream(stream):
                 run()
@@ -615,7 +615,7 @@ def run_ours(args):
     if args.side_only:
         peak, _ = hbm_peak()
         side = {"f16w_gemv": measure_f16w(dev, peak, mats=2, reps=2),
-                "attention_kv_mirrors": measure_attn_mirrors(dev, peak, caches=2, reps=2)}
+                "attention_kv_mirrors": measure_attn_mirrors(dev, peak, caches=2, reps=2, path=args.attn_path)}
         if rank == 0:
             print(json.dumps({"side_only": True, "side_workloads": side}))
         return
@@ -665,7 +665,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         extras["f16w_gemv"] = measure_f16w(dev, peak)
         torch.cuda.empty_cache()
-        extras["attention_kv_mirrors"] = measure_attn_mirrors(dev, peak)
+        extras["attention_kv_mirrors"] = measure_attn_mirrors(dev, peak, path=args.attn_path)
         torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
