@@ -675,7 +675,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "q8_0 weights x f32 activations, f16 KV, f32 accumulate",
+        "vs_baseline": None, "dtype": "f32",
+        "operands": "q8_0 weights, f32 activations, f16 KV mirror; f32 accumulation (tensor-core operands f16)",
         "data": "synthetic (seeded N(0,0.02) Q8_0 weights, N(0,1) activations and f16 KV; no trained weights)",
         "config": {"workload": wl["desc"], "rows": rows, "layers_cycled": args.layers,
                    "l2": "inputs larger than L2: %d distinct layers cycled (%.2f GB)" % (
