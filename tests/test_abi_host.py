@@ -87,6 +87,10 @@ def test_attn_plan_fills_sms(dl):
         total_tiles = sum(8 * math.ceil(max(sl) / 32) for _ in range(1))
         assert p.n_work >= min(148, total_tiles)
         assert p.workspace_bytes >= rows * 24 * p.max_splits * 129 * 4
+        # partial outputs, partial LSEs, then the last-piece merge's counters, each 16-byte rounded
+        r16 = lambda b: (b + 15) // 16 * 16
+        assert p.workspace_bytes == (r16(rows * 24 * p.max_splits * 128 * 4) + r16(rows * 24 * p.max_splits * 4) +
+                                     r16(p.n_sessions * 8 * 4))
 
 
 def test_attn_plan_sessions(dl):
@@ -140,6 +144,7 @@ def test_null_and_shape_refusals_before_any_launch(dl):
     assert L.dl_rope_kv_store(None, 0, None, 0, None, 0, None, None, None, 1, 8, None, None, None, None) == dl.DL_E_ARG
     assert L.dl_plan_groups(-1, 8, None) == dl.DL_E_ARG
     assert L.dl_status_read(None, None) == dl.DL_E_ARG
+    assert L.dl_decode_attn_merged(None, 0, None, None, None, None, None, 0, None, 0, None, None, 0, None) == dl.DL_E_ARG
     w = dl.dl_q8_weight(16, 16, 64, 100)   # n_in not a multiple of 32
     x = ctypes.c_float(0)
     assert L.dl_gemv_q8(ctypes.byref(w), ctypes.byref(x), 1, 128, ctypes.byref(x), 64, None) == dl.DL_E_SHAPE
