@@ -308,6 +308,9 @@ int dl_rope_table_build(double theta, int rot_dim, int max_pos, float *host_out)
  *    nearest even) in slot pos[r] of its KV head in region row_region[r];
  *  - every v head is clamped and stored as f16 the same way;
  *  - channels >= rot_dim pass through unrotated.
+ * On the f32 mirror [KV32] k and v are rounded once to f32 (no clamp); on the
+ * q8_0 mirror [KVQ8] each block of 32 values of k (rotated) and v is encoded
+ * as codes and a scale.
  *   q        device f32, row r at q + r*q_stride, n_q heads of head_dim
  *   k, v     device f32, rows at k + r*k_stride / v + r*v_stride, n_kv heads
  *   bias     device f32 or NULL
@@ -412,7 +415,9 @@ int dl_decode_attn(const float *q, int64_t q_stride, const dl_kv_cache *kv,
  * dot products, 2 = 16x8x16 f16 tensor-core products with q split into two f16
  * terms (hi + lo) and probabilities in f16, f32 accumulation and softmax.  On
  * the f32 mirror path 2 takes q, the keys, the probabilities and the values as
- * bf16 hi + lo pairs (three products per pair of operands, f32 accumulation).
+ * bf16 hi + lo pairs (three products per pair of operands, f32 accumulation);
+ * on the q8_0 mirror the codes are exact f16 operands, each key's block scale
+ * multiplies its score sums (f32) and its values (rounded once to f16).
  */
 int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv,
                       const int32_t *seqlen, const dl_attn_plan *plan,
@@ -426,9 +431,10 @@ int dl_decode_attn_ex(const float *q, int64_t q_stride, const dl_kv_cache *kv,
  * dl_rope_kv_store) is added first; every work item rotates its queries in
  * shared memory (q itself is only read, never rotated in place); the work item
  * whose keys hold pos[r] (the last one, for a position past every row's keys)
- * rotates k, clamps k and v into +-65504, stores both as f16 (round to nearest
- * even) in slot pos[r] of region plan->row_region[r], and reads them back from
- * the mirror after its own stores.  The stored halves, the queries and the
+ * rotates k and stores k and v in slot pos[r] of region plan->row_region[r] as
+ * dl_rope_kv_store does for the mirror (f16: clamped into +-65504, round to
+ * nearest even; f32: rounded once; q8_0: block-encoded), then reads them back
+ * from the mirror after its own stores.  The stored values, the queries and the
  * results equal those of the two separate calls.
  *   q        device f32, row r at q + r*q_stride: n_q heads as projected (unrotated)
  *   k, v     device f32 rows, n_kv heads each; k_stride, v_stride >= n_kv*head_dim
