@@ -61,6 +61,8 @@ def parse_args():
                    help="1: the O, gate/up and down projections as the phases of one persistent launch")
     p.add_argument("--cluster-merge", type=int, default=0, choices=[0, 1],
                    help="1: the pieces of a KV head merge inside their thread-block cluster (no merge launch)")
+    p.add_argument("--kv", default="f16", choices=["f16", "f32", "q8_0"],
+                   help="the KV mirror of the measured step (f16: the path's; q8_0: the block-codec mirror)")
     p.add_argument("--tail-merge", type=int, default=0, choices=[0, 1],
                    help="1: commands of at most 8 queries per KV head merge in the attention launch "
                         "(dl_decode_attn_merged: the last piece of each KV head merges)")
@@ -102,9 +104,11 @@ def workload(name):
     raise ValueError(name)
 
 
-def step_bytes(wl, step):
+def step_bytes(wl, step, kv="f16"):
     """Algorithmic HBM bytes of one layer step: weights once per command, each session's keys
-    once, the new K/V rows, and every call's activation rows in and out (f32)."""
+    once, the new K/V rows (at the mirror's bytes per value), and every call's activation rows
+    in and out (f32)."""
+    eb = KV_ELEM_BYTES[kv]
     S = wl["shape"]
     D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
     w_bytes = sum(no * ni // 32 * 34 for no, ni in S.projections().values())
@@ -117,8 +121,8 @@ def step_bytes(wl, step):
         for s in range(p.n_sessions):
             rows = [p.sess_rows[i] for i in range(p.sess_begin[s], p.sess_begin[s + 1])]
             keys += max(c.seqlen_host[r] for r in rows)
-        total += keys * n_kv * D * 2 * 2                  # K and V read
-        total += n * n_kv * D * 2 * 2                     # new K and V rows
+        total += int(keys * n_kv * D * 2 * eb)           # K and V read
+        total += int(n * n_kv * D * 2 * eb)              # new K and V rows
         qkv = (n_q + 2 * n_kv) * D
         act = n * (H + qkv) + n * (qkv + n_q * D)         # QKV GEMV in/out; rope q in/out, k, v in
         act += n * n_q * D * 2 + n * n_q                  # attention q in, merge out + lse
@@ -215,7 +219,10 @@ def traffic_for(kernel_tag):
 
 # ----------------------------------------------------------------------------- our arm
 
-def build_layers(wl, L, dev, seed=0):
+KV_ELEM_BYTES = {"f16": 2.0, "f32": 4.0, "q8_0": 34 / 32}     # HBM bytes per cached value
+
+
+def build_layers(wl, L, dev, seed=0, kv="f16"):
     import synth
     import torch
     import row_decode_step_gb300 as dl
@@ -229,23 +236,32 @@ def build_layers(wl, L, dev, seed=0):
             packed[name] = dl.dl_q8_pack(blocks, n_out, n_in)
             del blocks
         layers.append(LayerWeights(packed["wqkv"], packed["wo"], packed.get("wgu"), packed.get("wdown")))
-        k = synth.kv_cache_normal(seed, "%s/L%d/K" % (S.name, l), wl["n_regions"], S.n_kv, wl["capacity"],
-                                  S.head_dim, device=dev)
-        v = synth.kv_cache_normal(seed, "%s/L%d/V" % (S.name, l), wl["n_regions"], S.n_kv, wl["capacity"],
-                                  S.head_dim, device=dev)
+        shape = (wl["n_regions"], S.n_kv, wl["capacity"], S.head_dim)
+        if kv == "q8_0":
+            shape = shape[:2] + ((wl["capacity"] + 3) // 4 * 4,) + shape[3:]    # the mirror's capacity rule
+            kc, ks = synth.kv_q8_random_planes(seed, "%s/L%d/K" % (S.name, l), *shape, device=dev)
+            vc, vs = synth.kv_q8_random_planes(seed, "%s/L%d/V" % (S.name, l), *shape, device=dev)
+            caches.append(dl.KVCache.q8(kc, ks, vc, vs))
+            continue
+        if kv == "f32":
+            k = synth.normal_f32(seed, "%s/L%d/K32" % (S.name, l), shape, device=dev)
+            v = synth.normal_f32(seed, "%s/L%d/V32" % (S.name, l), shape, device=dev)
+        else:
+            k = synth.kv_cache_normal(seed, "%s/L%d/K" % (S.name, l), *shape, device=dev)
+            v = synth.kv_cache_normal(seed, "%s/L%d/V" % (S.name, l), *shape, device=dev)
         caches.append(dl.KVCache(k, v))
     torch.cuda.synchronize()
     return layers, caches
 
 
 def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0), fused=False,
-            cluster=False, chain=False, prefetch=False, concurrent=False, tail=False):
+            cluster=False, chain=False, prefetch=False, concurrent=False, tail=False, kv="f16"):
     import synth
     import torch
     import row_decode_step_gb300 as dl
     from row_decode_step_gb300.step import LayerStep
     S = wl["shape"]
-    layers, caches = build_layers(wl, L, dev)
+    layers, caches = build_layers(wl, L, dev, kv=kv)
     rope = dl.make_rope(S.rope_theta, S.head_dim, wl["capacity"], device=dev)
     step = LayerStep(wl["positions"], wl["regions"], S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, dev,
                      gemv_path=paths[0], attn_path=paths[1], fused_rope=fused, cluster_merge=cluster,
@@ -624,12 +640,12 @@ def run_ours(args):
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path),
                   fused=bool(args.fused_rope), cluster=bool(args.cluster_merge), chain=bool(args.gemv_chain),
                   prefetch=bool(args.l2_prefetch), concurrent=bool(args.concurrent_commands),
-                  tail=bool(args.tail_merge))
+                  tail=bool(args.tail_merge), kv=args.kv)
     steps = args.steps
     ms, value = combine_ranks(res["ms_total"], steps, world, dev)
     step = res["step"]
     rows = len(wl["positions"])
-    sb = step_bytes(wl, step)
+    sb = step_bytes(wl, step, args.kv)
     peak, peak_src = hbm_peak()
     step_gbs = sb / (ms / steps / 1e3) / 1e9
     gu_avg_ms = res["gu_ms"]
@@ -642,8 +658,8 @@ def run_ours(args):
                          want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
                          fused=bool(args.fused_rope), cluster=bool(args.cluster_merge),
                          chain=bool(args.gemv_chain), prefetch=bool(args.l2_prefetch),
-                         concurrent=bool(args.concurrent_commands), tail=bool(args.tail_merge))
-            sb2 = step_bytes(w2, r2["step"])
+                         concurrent=bool(args.concurrent_commands), tail=bool(args.tail_merge), kv=args.kv)
+            sb2 = step_bytes(w2, r2["step"], args.kv)
             extras[name] = {"rows": len(w2["positions"]), "layer_steps_per_s": 1e3 / r2["ms_per_step"],
                             "ms_per_step": r2["ms_per_step"],
                             "tokens_per_s": len(w2["positions"]) * 1e3 / r2["ms_per_step"],
@@ -652,6 +668,18 @@ def run_ours(args):
                             "commands": len(r2["step"].commands), "status": r2["status"]}
             del r2
             torch.cuda.empty_cache()
+    if not args.no_extras and args.workload == "3b-8" and args.kv == "f16":
+        # the same step over the block-codec (q8_0) mirror: half the key and value bytes
+        r2 = measure(wl, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
+                     want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
+                     fused=bool(args.fused_rope), prefetch=bool(args.l2_prefetch), kv="q8_0")
+        sbq = step_bytes(wl, r2["step"], "q8_0")
+        extras["3b-8 q8_0 KV"] = {
+            "layer_steps_per_s": 1e3 / r2["ms_per_step"], "ms_per_step": r2["ms_per_step"],
+            "algorithmic_bytes": sbq, "algorithmic_gbs": sbq / (r2["ms_per_step"] / 1e3) / 1e9,
+            "hbm_frac": sbq / (r2["ms_per_step"] / 1e3) / 1e9 / peak, "status": r2["status"]}
+        del r2
+        torch.cuda.empty_cache()
     if not args.no_extras and args.workload == "3b-8":
         # the same step with the rope/store as its own launch (the other form of the path)
         r2 = measure(wl, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
@@ -688,7 +716,7 @@ def run_ours(args):
                    "gemv_path": args.gemv_path, "attn_path": args.attn_path,
                    "rope_in_attention": bool(args.fused_rope), "merge_in_cluster": bool(args.cluster_merge),
                    "l2_prefetch": bool(args.l2_prefetch), "concurrent_commands": bool(args.concurrent_commands),
-                   "tail_merge": bool(args.tail_merge),
+                   "tail_merge": bool(args.tail_merge), "kv_mirror": args.kv,
                    "gemv_chain": bool(args.gemv_chain)},
         "tokens_per_s": rows * value,
         "step": {"algorithmic_bytes": sb, "algorithmic_gbs": step_gbs, "hbm_frac": step_gbs / peak,

@@ -146,3 +146,71 @@ def test_step_twelve_streams_tail_merge(dl):
     step = _step(dl, synth.LLAMA_3B, lens, list(range(12)), 12, max(lens) + 1, "step/streams", fused_rope=True,
                  tail_merge=True, concurrent=True)
     assert all(c.tail_merge for c in step.commands)
+
+
+@pytest.mark.parametrize("mirror", ["f32", "q8_0"])
+@pytest.mark.parametrize("rows", [1, 8])
+def test_step_3b_mirrors(dl, mirror, rows):
+    """The default step (rope/store inside the attention) over the f32 and the q8_0 mirrors
+    against the oracle's layer step on the same planes.  Stored rows: f32 within the GEMV bar of
+    their values; q8_0 codes within one and scales within two f16 steps (the stored values carry
+    the QKV GEMV's rounding); unwritten slots identical."""
+    from row_decode_step_gb300.step import LayerStep, LayerWeights
+    S = synth.LLAMA_3B
+    D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
+    blocks = layer_blocks(S.name)
+    packed = {n: dl.dl_q8_pack(b.cuda(), b.shape[0], b.shape[1] * 32) for n, b in blocks.items()}
+    W = LayerWeights(packed["wqkv"], packed["wo"], packed.get("wgu"), packed.get("wdown"))
+    cap = 5128
+    positions = list(range(5120, 5120 + rows))
+    regions = [0] * rows
+    label = "stepm/%s/%d" % (mirror, rows)
+    if mirror == "q8_0":
+        kc, ks = synth.kv_q8_random_planes(0, label + "/K", 1, n_kv, cap, D)
+        vc, vs = synth.kv_q8_random_planes(0, label + "/V", 1, n_kv, cap, D)
+        kv = dl.KVCache.q8(kc.cuda(), ks.cuda(), vc.cuda(), vs.cuda())
+        ko = oracle.Q8Plane(kc.numpy().copy(), ks.numpy().view(np.uint16).copy())
+        vo = oracle.Q8Plane(vc.numpy().copy(), vs.numpy().view(np.uint16).copy())
+    else:
+        k = synth.normal_f32(0, label + "/K", (1, n_kv, cap, D))
+        v = synth.normal_f32(0, label + "/V", (1, n_kv, cap, D))
+        kv = dl.KVCache(k.cuda(), v.cuda())
+        ko, vo = k.numpy().copy(), v.numpy().copy()
+    rope = dl.make_rope(S.rope_theta, D, cap)
+    x = synth.normal_f32(0, label + "/x", (rows, H))
+    xf = synth.normal_f32(0, label + "/xf", (rows, H))
+    h = synth.normal_f32(0, label + "/h", (rows, F))
+    step = LayerStep(positions, regions, n_q, n_kv, D, H, F, "cuda", fused_rope=True)
+    c = step.commands[0]
+    c.x.copy_(x.cuda())
+    c.x_ffn.copy_(xf.cuda())
+    c.h.copy_(h.cuda())
+    step.run(W, rope, kv)
+    torch.cuda.synchronize()
+    assert dl.dl_status_read(c.status) == 0
+    ref = oracle.layer_step(blocks, x, ko, vo, positions, n_q=n_q, n_kv=n_kv, head_dim=D, theta=S.rope_theta,
+                            chunk=c.plan.chunk, n_splits=c.plan.max_splits, regions=regions, x_ffn=xf, h=h)
+    qd = n_q * D
+    assert_gemv_close(c.qkv.cpu().numpy()[:, qd:], ref["qkv"][:, qd:])
+    assert_attn_close(c.attn.cpu().numpy(), c.lse.cpu().numpy(), ref["attn"], ref["lse"])
+    assert gemv_err(c.y_o.cpu().numpy(), ref["y_o"]) < 1e-2
+    assert_gemv_close(c.gu.cpu().numpy(), ref["gu"])
+    assert_gemv_close(c.y_down.cpu().numpy(), ref["y_down"])
+    slots = np.zeros((1, n_kv, cap), bool)
+    slots[0, :, positions] = True
+    if mirror == "q8_0":
+        for got_c, got_s, o, (c0, s0) in ((kv.k, kv.k_scale, ko, (kc, ks)), (kv.v, kv.v_scale, vo, (vc, vs))):
+            gc = got_c.cpu().numpy().astype(np.int64)
+            gs = got_s.cpu().numpy().view(np.uint16).astype(np.int64)
+            assert np.array_equal(gc[~slots], c0.numpy().astype(np.int64)[~slots])
+            assert np.array_equal(gs[~slots], s0.numpy().view(np.uint16).astype(np.int64)[~slots])
+            assert int(np.abs(gc[slots] - o.codes.astype(np.int64)[slots]).max()) <= 1
+            assert int(np.abs(gs[slots] - o.scales.astype(np.int64)[slots]).max()) <= 2
+    else:
+        for got, o, init in ((kv.k, ko, k), (kv.v, vo, v)):
+            g = got.cpu().numpy()
+            assert np.array_equal(g[~slots], init.numpy()[~slots])
+            ref_w = o[slots].astype(np.float64)
+            rms = float(np.sqrt(np.mean(ref_w ** 2)))
+            # the GEMV bar per element, times sqrt(2) for the rotation of a pair
+            assert np.all(np.abs(g[slots] - ref_w) <= 1.5e-3 * np.maximum(np.abs(ref_w), rms))
