@@ -59,15 +59,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
-// Bulk copy delivered to the same shared-memory offset in every CTA of `mask` (cluster ranks),
-// each completing its own mbarrier at `bar`'s offset.
-__device__ __forceinline__ void bulk_g2s_multicast(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                                   uint16_t mask)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-                 " [%0], [%1], %2, [%3], %4;"
-                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(mask) : "memory");
-}
 // Two-dimensional tiled copy through a tensor map (x = innermost coordinate, in elements).
 __device__ __forceinline__ void tma_g2s_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar)
 {
