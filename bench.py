@@ -72,6 +72,8 @@ def parse_args():
     p.add_argument("--l2-prefetch", type=int, default=0, choices=[0, 1],
                    help="1: each launch asks L2 for the weights or keys of a later kernel while it runs "
                         "(dl_l2_prefetch_next)")
+    p.add_argument("--one-launch", type=int, default=0, choices=[0, 1],
+                   help="1: each command's whole layer step as one persistent launch (dl_layer_step)")
     p.add_argument("--fused-rope", type=int, default=1, choices=[0, 1],
                    help="1: the rope/store runs inside the attention launch (dl_decode_attn_rope); "
                         "0: separate dl_rope_kv_store and dl_decode_attn launches")
@@ -255,7 +257,7 @@ def build_layers(wl, L, dev, seed=0, kv="f16"):
 
 
 def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0), fused=False,
-            cluster=False, chain=False, prefetch=False, concurrent=False, tail=False, kv="f16"):
+            cluster=False, chain=False, prefetch=False, concurrent=False, tail=False, kv="f16", one=False):
     import synth
     import torch
     import row_decode_step_gb300 as dl
@@ -265,7 +267,8 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
     rope = dl.make_rope(S.rope_theta, S.head_dim, wl["capacity"], device=dev)
     step = LayerStep(wl["positions"], wl["regions"], S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, dev,
                      gemv_path=paths[0], attn_path=paths[1], fused_rope=fused, cluster_merge=cluster,
-                     gemv_chain=chain, l2_prefetch=prefetch, concurrent=concurrent, tail_merge=tail)
+                     gemv_chain=chain, l2_prefetch=prefetch, concurrent=concurrent and not one, tail_merge=tail,
+                     one_launch=one)
     for i, c in enumerate(step.commands):
         c.x.copy_(synth.normal_f32(0, "bench/x%d" % i, tuple(c.x.shape), device=dev))
         if c.x_ffn is not None:
@@ -640,7 +643,7 @@ def run_ours(args):
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path),
                   fused=bool(args.fused_rope), cluster=bool(args.cluster_merge), chain=bool(args.gemv_chain),
                   prefetch=bool(args.l2_prefetch), concurrent=bool(args.concurrent_commands),
-                  tail=bool(args.tail_merge), kv=args.kv)
+                  tail=bool(args.tail_merge), kv=args.kv, one=bool(args.one_launch))
     steps = args.steps
     ms, value = combine_ranks(res["ms_total"], steps, world, dev)
     step = res["step"]
@@ -658,7 +661,8 @@ def run_ours(args):
                          want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
                          fused=bool(args.fused_rope), cluster=bool(args.cluster_merge),
                          chain=bool(args.gemv_chain), prefetch=bool(args.l2_prefetch),
-                         concurrent=bool(args.concurrent_commands), tail=bool(args.tail_merge), kv=args.kv)
+                         concurrent=bool(args.concurrent_commands), tail=bool(args.tail_merge), kv=args.kv,
+                         one=bool(args.one_launch))
             sb2 = step_bytes(w2, r2["step"], args.kv)
             extras[name] = {"rows": len(w2["positions"]), "layer_steps_per_s": 1e3 / r2["ms_per_step"],
                             "ms_per_step": r2["ms_per_step"],

@@ -516,6 +516,81 @@ int dl_decode_attn_merged(const float *q, int64_t q_stride, const dl_attn_rope_i
 int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t *seqlen,
                   float *out, int64_t out_stride, float *lse, dl_stream_t stream);
 
+/* ------------------------------------------------------------- whole layer step
+ *
+ * One decoder layer's decode step for one command (1..8 rows) in a single
+ * launch [ENC][ROPE][SPL][GRP]: the QKV projection, the rope and store of the
+ * rows' new k and v into the f16 mirror, split-KV attention over the plan's
+ * pieces, their log-sum-exp merge, then the O, gate/up and down projections.
+ * Each part has the arithmetic of its separate call (dl_gemv_q8_ex,
+ * dl_decode_attn_rope, dl_attn_merge); the projections' K is cut into slices of
+ * 1024 inputs whose sums are added in slice order, so a projection's last bits
+ * may differ from dl_gemv_q8's (not from call to call: results are
+ * deterministic).
+ *
+ * The launch holds one CTA per SM for the whole step.  A CTA streams its share
+ * of every projection's weights and of the keys ahead of use, and each part
+ * waits only for the outputs it reads: the attention for the whole QKV
+ * projection, the merge for every piece, O for every merged head, gate/up for
+ * the whole O output and down for the whole gate/up output (in a decoder layer
+ * a norm reads all of O's output and the SwiGLU all of gate/up's, between
+ * them; neither is computed here).
+ */
+typedef struct dl_layer_weights {
+    dl_q8_weight qkv;    /* [(n_q + 2 n_kv) head_dim][hidden]: q, then k, then v rows */
+    dl_q8_weight o;      /* [hidden][n_q head_dim] */
+    dl_q8_weight gu;     /* [2 ffn][hidden] (gate and up concatenated); qs == NULL: no FFN */
+    dl_q8_weight down;   /* [hidden][ffn] (ignored without FFN) */
+} dl_layer_weights;
+
+/* Row buffers of a layer step: device f32, row r of a buffer at ptr + r*stride (in elements). */
+typedef struct dl_layer_bufs {
+    const float *x;      int64_t x_stride;       /* layer input [rows][hidden], read by QKV */
+    float *qkv;          int64_t qkv_stride;     /* QKV output (q | k | v), unrotated */
+    float *attn;         int64_t attn_stride;    /* merged attention [rows][n_q head_dim]: O's input */
+    float *lse;                                  /* [rows][n_q] or NULL */
+    float *o;            int64_t o_stride;       /* O output [rows][hidden] */
+    const float *x_ffn;  int64_t x_ffn_stride;   /* gate/up input; may be o */
+    float *gu;           int64_t gu_stride;      /* gate/up output [rows][2 ffn] */
+    const float *x_down; int64_t x_down_stride;  /* down input [rows][ffn]; may point into gu */
+    float *down;         int64_t down_stride;    /* down output [rows][hidden] */
+} dl_layer_bufs;
+
+/*
+ * Bytes of the workspace dl_layer_step needs for these weights and plan: its
+ * own counters, the projections' slice sums and the attention pieces' (o, lse).
+ * Host only.
+ */
+int dl_layer_step_workspace_size(const dl_layer_weights *W, const dl_attn_plan *plan, size_t *bytes);
+
+/*
+ * The layer step of one command.
+ *   W, B      weights (device planes) and row buffers as above; the inputs x,
+ *             x_ffn, x_down, the planes and qkv/attn must be 16-byte aligned with
+ *             strides a multiple of 4; every output apart from every other, from
+ *             its own input and from the workspace
+ *   bias, pos, rope, kv, seqlen, plan    as dl_decode_attn_rope; the plan from
+ *             dl_attn_plan_build for this command (about one work item per SM
+ *             fills the launch: build it with sm_count = SMs / 2), no cluster
+ *   workspace device, >= dl_layer_step_workspace_size bytes, 16-byte aligned,
+ *             zero before the first call (zero it once); every completed call
+ *             leaves its counters zero again
+ *   status    device int32 or NULL: the bits of the separate calls, plus
+ *             DL_STATUS_SYNC_TIMEOUT if a bounded wait gave up (outputs invalid;
+ *             zero the workspace again before the next call)
+ *   path      0 automatic (tensor-core projections for 3..8 rows, CUDA cores for
+ *             1..2), 1 CUDA-core projections (1..2 rows only), 2 tensor cores;
+ *             the attention takes tensor cores for work items of more than four
+ *             queries, CUDA cores otherwise
+ * The f16 mirror only (elem_bytes 0 or 2), head_dim 64 or 128.  The launch holds
+ * every SM until it ends and its CTAs wait on one another: never run two of
+ * these launches (or one beside other work that fills SMs and waits on it) at
+ * the same time; issue a step's commands one after another on one stream.
+ */
+int dl_layer_step(const dl_layer_weights *W, const dl_layer_bufs *B, const float *bias, const int32_t *pos,
+                  const dl_rope *rope, const dl_kv_cache *kv, const int32_t *seqlen, const dl_attn_plan *plan,
+                  void *workspace, size_t workspace_bytes, int32_t *status, int path, dl_stream_t stream);
+
 /* ------------------------------------------------------------- no-allocation form
  *
  * (No counterpart on the pages: an addition for callers that cannot allocate

@@ -116,6 +116,8 @@ def lib() -> ctypes.CDLL:
             "dl_decode_attn_cluster": ([P, I64, P, P, P, P, P, I64, P, P, I, P], I),
             "dl_decode_attn_merged": ([P, I64, P, P, P, P, P, SZ, P, I64, P, P, I, P], I),
             "dl_attn_merge": ([P, P, P, P, I64, P, P], I),
+            "dl_layer_step_workspace_size": ([P, P, P], I),
+            "dl_layer_step": ([P, P, P, P, P, P, P, P, P, SZ, P, I, P], I),
             "dl_decode_attention_noalloc_max_bytes": ([], SZ),
             "dl_decode_attention_noalloc": ([P, I64, P, P, P, P, I64, P, P, P], I),
         }
@@ -539,3 +541,82 @@ def decode_attention(q, kv, seqlen, plan, workspace, out=None, lse=None, status=
     dl_decode_attn(q, kv, seqlen, plan, workspace, status=status, stream=stream, path=path)
     dl_attn_merge(workspace, plan, seqlen, out, lse, stream=stream)
     return out, lse
+
+
+# ------------------------------------------------------------------ whole layer step
+
+class dl_layer_weights(ctypes.Structure):
+    _fields_ = [("qkv", dl_q8_weight), ("o", dl_q8_weight), ("gu", dl_q8_weight), ("down", dl_q8_weight)]
+
+
+class dl_layer_bufs(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("x_stride", ctypes.c_int64),
+                ("qkv", ctypes.c_void_p), ("qkv_stride", ctypes.c_int64),
+                ("attn", ctypes.c_void_p), ("attn_stride", ctypes.c_int64),
+                ("lse", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("o_stride", ctypes.c_int64),
+                ("x_ffn", ctypes.c_void_p), ("x_ffn_stride", ctypes.c_int64),
+                ("gu", ctypes.c_void_p), ("gu_stride", ctypes.c_int64),
+                ("x_down", ctypes.c_void_p), ("x_down_stride", ctypes.c_int64),
+                ("down", ctypes.c_void_p), ("down_stride", ctypes.c_int64)]
+
+
+def _q8c(W: Optional[PackedQ8]) -> dl_q8_weight:
+    return dl_q8_weight(None, None, 0, 0) if W is None else W.c
+
+
+def layer_weights_c(wqkv: PackedQ8, wo: PackedQ8, wgu: Optional[PackedQ8] = None,
+                    wdown: Optional[PackedQ8] = None) -> dl_layer_weights:
+    return dl_layer_weights(_q8c(wqkv), _q8c(wo), _q8c(wgu), _q8c(wdown))
+
+
+def dl_layer_step_workspace_size(Wc: dl_layer_weights, plan: dl_attn_plan) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().dl_layer_step_workspace_size(ctypes.byref(Wc), ctypes.byref(plan), ctypes.byref(b)))
+    return b.value
+
+
+def _rows2d(t: Optional[torch.Tensor], name: str):
+    if t is None:
+        return None, 0
+    _dev(t, torch.float32, name)
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("%s must be 2-D rows with unit inner stride" % name)
+    return t.data_ptr(), t.stride(0)
+
+
+def dl_layer_step(Wc: dl_layer_weights, x: torch.Tensor, qkv: torch.Tensor, attn: torch.Tensor,
+                  lse: Optional[torch.Tensor], o: torch.Tensor, x_ffn: Optional[torch.Tensor],
+                  gu: Optional[torch.Tensor], x_down: Optional[torch.Tensor], down: Optional[torch.Tensor],
+                  pos: torch.Tensor, rope: Rope, kv: KVCache, seqlen: torch.Tensor, plan: dl_attn_plan,
+                  workspace: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                  status: Optional[torch.Tensor] = None, stream=None, path: int = GEMV_PATH_AUTO) -> None:
+    """One command's whole layer step in one launch (weights from layer_weights_c; the workspace
+    zeroed once, dl_layer_step_workspace_size bytes)."""
+    B = dl_layer_bufs()
+    B.x, B.x_stride = _rows2d(x, "x")
+    B.qkv, B.qkv_stride = _rows2d(qkv, "qkv")
+    B.attn, B.attn_stride = _rows2d(attn, "attn")
+    if lse is not None:
+        _dev(lse, torch.float32, "lse")
+        B.lse = lse.data_ptr()
+    B.o, B.o_stride = _rows2d(o, "o")
+    B.x_ffn, B.x_ffn_stride = _rows2d(x_ffn, "x_ffn")
+    B.gu, B.gu_stride = _rows2d(gu, "gu")
+    B.x_down, B.x_down_stride = _rows2d(x_down, "x_down")
+    B.down, B.down_stride = _rows2d(down, "down")
+    _dev(pos, torch.int32, "pos")
+    _dev(seqlen, torch.int32, "seqlen")
+    _dev(workspace, torch.uint8, "workspace")
+    if bias is not None:
+        _dev(bias, torch.float32, "bias")
+    if status is not None:
+        _dev(status, torch.int32, "status")
+    _check(lib().dl_layer_step(ctypes.byref(Wc), ctypes.byref(B), _ptr(bias), _ptr(pos), ctypes.byref(rope.c),
+                               ctypes.byref(kv.c), _ptr(seqlen), ctypes.byref(plan), _ptr(workspace),
+                               workspace.numel(), _ptr(status), path, _stream(stream)))
+
+
+def device_sm_count(device=None) -> int:
+    return torch.cuda.get_device_properties(device if device is not None else torch.cuda.current_device()).multi_processor_count
+

@@ -1599,6 +1599,14 @@ AttnKernel pick_attn_kernel(bool mma, int qm)
 
 }  // namespace
 
+namespace dl {
+// The f16/f32/q8_0 mirror plane as a tensor map (boxes of 32 slots): shared with the layer-step launch.
+int make_kv_tmap(CUtensorMap *m, const void *plane, const dl_kv_cache *kv)
+{
+    return ::make_kv_tmap(m, plane, kv);
+}
+}  // namespace dl
+
 extern "C" {
 
 int dl_plan_groups(int n, int max_rows, int *sizes)

@@ -18,9 +18,13 @@ since at one row it measured slower); with
 `tail_merge`, dl_decode_attn_merged in place of them for commands whose work
 items serve at most eight queries (the last piece of a KV head merges); with
 `gemv_chain`, the O, gate/up and down projections as the phases of one
-dl_gemv_q8_chain launch.  A step of several commands (sessions past eight rows)
-may run them on streams of their own (`concurrent`), since they share nothing
-but the weights.
+dl_gemv_q8_chain launch; with `one_launch`, the whole step of a command as one
+dl_layer_step launch (the f16 mirror; its plan sized for about one attention
+work item per SM).  A step of several commands (sessions past eight rows) may
+run them on streams of their own (`concurrent`), since they share nothing but
+the weights; not with `one_launch` or `gemv_chain`, whose launches hold every
+SM while their CTAs wait on one another, so that two side by side could wait on
+each other.
 
 Norms, SwiGLU and residual adds are not part of the path: the gate/up and down
 projections read their own activation buffers (filled by the caller).  More
@@ -34,10 +38,10 @@ from typing import Dict, List, Optional, Sequence
 
 import torch
 
-from . import (KVCache, PackedQ8, Rope, dl_attn_merge, dl_attn_plan_build, dl_attn_plan_build_cluster,
-               dl_decode_attn, dl_decode_attn_cluster, dl_decode_attn_merged, dl_decode_attn_rope, dl_gemv_q8,
-               dl_gemv_q8_chain,
-               dl_l2_prefetch_next, dl_plan_groups, dl_rope_kv_store, workspace_for)
+from . import (KVCache, PackedQ8, Rope, device_sm_count, dl_attn_merge, dl_attn_plan_build,
+               dl_attn_plan_build_cluster, dl_decode_attn, dl_decode_attn_cluster, dl_decode_attn_merged,
+               dl_decode_attn_rope, dl_gemv_q8, dl_gemv_q8_chain, dl_l2_prefetch_next, dl_layer_step,
+               dl_layer_step_workspace_size, dl_plan_groups, dl_rope_kv_store, layer_weights_c, workspace_for)
 
 
 
@@ -60,6 +64,12 @@ class LayerWeights:
     def q8_bytes(self) -> int:
         return sum(w.nbytes_q8_0 for w in (self.wqkv, self.wo, self.wgu, self.wdown) if w is not None)
 
+    def c(self):
+        """The weights as the C struct of dl_layer_step (built once)."""
+        if getattr(self, "_c", None) is None:
+            self._c = layer_weights_c(self.wqkv, self.wo, self.wgu, self.wdown)
+        return self._c
+
 
 class Command:
     """Buffers and plan of one command (1..8 rows) of a layer step."""
@@ -68,9 +78,16 @@ class Command:
                  n_q: int, n_kv: int, head_dim: int, hidden: int, ffn: int, device, sm_count: int = 0,
                  force_chunk: int = 0, gemv_path: int = 0, attn_path: int = 0, fused_rope: bool = False,
                  cluster_merge: bool = False, gemv_chain: bool = False, l2_prefetch: bool = False,
-                 tail_merge: bool = False):
+                 tail_merge: bool = False, one_launch: bool = False, chain_ffn: bool = False):
+        """one_launch: the whole step as one dl_layer_step launch.  chain_ffn: the gate/up
+        projection reads the O output and the down projection the first `ffn` columns of the
+        gate/up output (instead of buffers of their own), the order a decoder layer imposes."""
         n = len(rows)
         assert 1 <= n <= 8
+        self.one_launch = bool(one_launch)
+        if self.one_launch and (cluster_merge or gemv_chain or l2_prefetch or tail_merge):
+            raise ValueError("one_launch runs the whole step in one launch: no other step form applies")
+        self.chain_ffn = bool(chain_ffn) and ffn > 0
         self.l2_prefetch = bool(l2_prefetch)
         self.gemv_path, self.attn_path = gemv_path, attn_path
         self.fused_rope = bool(fused_rope)
@@ -89,6 +106,11 @@ class Command:
         if self.cluster_merge:
             self.plan = dl_attn_plan_build_cluster(self.seqlen_host, n_q, n_kv, D, regions=self.regions,
                                                    sm_count=sm_count)
+        elif self.one_launch:
+            # about one work item per SM: the launch holds one CTA per SM
+            sms = sm_count if sm_count > 0 else device_sm_count(device)
+            self.plan = dl_attn_plan_build(self.seqlen_host, n_q, n_kv, D, regions=self.regions,
+                                           sm_count=max(1, sms // 2), force_chunk=force_chunk)
         else:
             self.plan = dl_attn_plan_build(self.seqlen_host, n_q, n_kv, D, regions=self.regions,
                                            sm_count=sm_count, force_chunk=force_chunk)
@@ -110,13 +132,34 @@ class Command:
         self.status = torch.zeros(1, **i32)
         self.workspace = workspace_for(self.plan, dev)
         self.sync = torch.zeros(4, **i32)                    # the chain launch's barrier words
+        self.step_ws = None                                  # dl_layer_step's workspace (sized at first run)
         qd, kd = n_q * D, n_kv * D
         self.q = self.qkv[:, :qd]
         self.k = self.qkv[:, qd:qd + kd]
         self.v = self.qkv[:, qd + kd:]
 
+    def ffn_inputs(self):
+        """The gate/up and down inputs: buffers of their own, or (chain_ffn) the O output and the
+        gate half of the gate/up output."""
+        if self.x_ffn is None:
+            return None, None
+        if self.chain_ffn:
+            return self.y_o, self.gu[:, :self.h.shape[1]]
+        return self.x_ffn, self.h
+
     def run(self, W: LayerWeights, rope: Rope, kv: KVCache, stream=None):
         gp = self.gemv_path if (self.gemv_path != 1 or self.n <= 2) else 0
+        if self.one_launch:
+            Wc = W.c()
+            if self.step_ws is None:
+                self.step_ws = torch.zeros(dl_layer_step_workspace_size(Wc, self.plan), dtype=torch.uint8,
+                                           device=self.x.device)
+            xf, xd = self.ffn_inputs() if W.wgu is not None else (None, None)
+            dl_layer_step(Wc, self.x, self.qkv, self.attn, self.lse, self.y_o, xf,
+                          self.gu if W.wgu is not None else None, xd,
+                          self.y_down if W.wgu is not None else None, self.pos, rope, kv, self.seqlen,
+                          self.plan, self.step_ws, status=self.status, stream=stream, path=gp)
+            return
         pf = self.l2_prefetch and not self.gemv_chain
         dl_gemv_q8(W.wqkv, self.x, self.qkv, stream=stream, path=gp)
         if self.cluster_merge:
@@ -156,11 +199,14 @@ class Command:
             _prefetch_head(W.wdown, 0.25)
         dl_gemv_q8(W.wo, self.attn, self.y_o, stream=stream, path=gp)
         if W.wgu is not None:
-            dl_gemv_q8(W.wgu, self.x_ffn, self.gu, stream=stream, path=gp)
-            dl_gemv_q8(W.wdown, self.h, self.y_down, stream=stream, path=gp)
+            xf, xd = self.ffn_inputs()
+            dl_gemv_q8(W.wgu, xf, self.gu, stream=stream, path=gp)
+            dl_gemv_q8(W.wdown, xd, self.y_down, stream=stream, path=gp)
 
     @property
     def launches(self) -> int:
+        if self.one_launch:
+            return 1
         return (7 - int(self.fused_rope) - int(self.cluster_merge or self.tail_merge) -
                 2 * int(self.gemv_chain))
 
@@ -172,10 +218,14 @@ class LayerStep:
                  hidden: int, ffn: int, device, sm_count: int = 0, force_chunk: int = 0, gemv_path: int = 0,
                  attn_path: int = 0, fused_rope: bool = False, cluster_merge: bool = False,
                  gemv_chain: bool = False, l2_prefetch: bool = False, concurrent: bool = False,
-                 tail_merge: bool = False):
+                 tail_merge: bool = False, one_launch: bool = False, chain_ffn: bool = False):
         """concurrent: the commands (independent sessions) run on streams of their own, forked
         from the caller's stream and joined back into it, so that one command's launch latencies
-        overlap another's work."""
+        overlap another's work.  Refused with one_launch and gemv_chain: those launches hold every
+        SM and their CTAs wait on one another, so two of them at once could each hold SMs the
+        other waits for."""
+        if concurrent and (one_launch or gemv_chain):
+            raise ValueError("concurrent commands cannot run as one_launch or gemv_chain launches")
         n = len(positions)
         sizes = dl_plan_groups(n)
         self.commands: List[Command] = []
@@ -185,7 +235,7 @@ class LayerStep:
             self.commands.append(Command(idx, [positions[i] for i in idx], [regions[i] for i in idx],
                                          n_q, n_kv, head_dim, hidden, ffn, device, sm_count, force_chunk,
                                          gemv_path, attn_path, fused_rope, cluster_merge, gemv_chain,
-                                         l2_prefetch, tail_merge))
+                                         l2_prefetch, tail_merge, one_launch, chain_ffn))
             r0 += s
         self.group_sizes = sizes
         self.concurrent = bool(concurrent) and len(self.commands) > 1
