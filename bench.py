@@ -45,7 +45,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--layers", type=int, default=8)
-    p.add_argument("--workload", default="3b-8", choices=["3b-8", "3b-1", "3b-12", "1b-1", "3b-8-32k"])
+    p.add_argument("--workload", default="3b-8", choices=["3b-8", "3b-1", "3b-2", "3b-4", "3b-12", "1b-1", "3b-8-32k"])
     p.add_argument("--no-extras", action="store_true", help="skip the 1-row and 12-stream side measurements")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--breakdown", action="store_true",
@@ -91,6 +91,11 @@ def workload(name):
     if name == "3b-1":
         return dict(shape=synth.LLAMA_3B, positions=[5120], regions=[0], n_regions=1, capacity=5128,
                     desc="Llama-3.2-3B-shaped layer step, 1 row at position 5120 over 5120 cached keys")
+    if name in ("3b-2", "3b-4"):
+        n = int(name[3:])
+        return dict(shape=synth.LLAMA_3B, positions=list(range(5120, 5120 + n)), regions=[0] * n, n_regions=1,
+                    capacity=5128, desc="Llama-3.2-3B-shaped layer step, %d rows of one session at positions "
+                    "5120-%d over 5120 cached keys" % (n, 5119 + n))
     if name == "3b-12":
         lens = synth.twelve_stream_lengths(0)
         return dict(shape=synth.LLAMA_3B, positions=lens, regions=list(range(12)), n_regions=12,

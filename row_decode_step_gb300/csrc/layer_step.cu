@@ -238,6 +238,25 @@ __device__ __forceinline__ void share(int64_t n, int c, int C, int &b, int &e)
     e = (int)(n * (c + 1) / C);
 }
 
+// This CTA's projection units [b, e) of RT row tiles x cs K-parts (unit u = row tile u % RT of part
+// u / RT).  With no more parts than CTAs, the CTAs split into one run per part and each takes an even
+// share of its part's row tiles, so that no CTA spans two parts (a part's activations are prepared
+// once per CTA); with more parts, an even share of all units.
+__device__ __forceinline__ void unit_share(int RT, int cs, int c, int C, int &b, int &e)
+{
+    if (cs > C) {
+        share((int64_t)RT * cs, c, C, b, e);
+        return;
+    }
+    const int s = (int)((int64_t)c * cs / C);                     // this CTA's part
+    const int f = (int)(((int64_t)s * C + cs - 1) / cs);          // the part's first CTA
+    const int l = (int)(((int64_t)(s + 1) * C + cs - 1) / cs);    // the next part's first CTA
+    int rb, re;
+    share(RT, c - f, l - f, rb, re);
+    b = s * RT + rb;
+    e = s * RT + re;
+}
+
 // ---------------------------------------------------------------- attention work items
 
 struct Item {
@@ -434,7 +453,7 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                 }
                 const SGemv &G = gemv_of(ph);
                 int ub, ue;
-                share((int64_t)G.RT * G.cs, cta, C, ub, ue);
+                unit_share(G.RT, G.cs, cta, C, ub, ue);
                 int s = ub / G.RT, rt = ub - s * G.RT;
                 for (int u = ub; u < ue && ok; ++u) {
                     // unit u: row tile rt over K part s, one slot per kKsl k-tiles
@@ -1217,7 +1236,7 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                 break;
             }
             int ub, ue;
-            share((int64_t)Gv.RT * Gv.cs, cta, C, ub, ue);
+            unit_share(Gv.RT, Gv.cs, cta, C, ub, ue);
             float *red = reinterpret_cast<float *>(scr);                     // [kRB][kCW][128]: 16 KB
             float *xs = reinterpret_cast<float *>(scr + 16 * 1024);          // CUDA-core path: [NRC][kPartKT * 32]: 32 KB
             float *snc = reinterpret_cast<float *>(scr + 16 * 1024);         // tensor path: [kCW][KPW][bias, 1/scale][8]

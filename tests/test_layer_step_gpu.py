@@ -20,7 +20,7 @@ import torch
 
 import oracle
 import synth
-from tests.workloads import assert_attn_close, assert_gemv_close, as_u16, f16_ulp_dist, kv_planes, layer_blocks
+from tests.workloads import assert_attn_close, assert_gemv_close, as_u16, kv_planes, layer_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -85,16 +85,19 @@ def _check(dl, S, blocks, step, positions, regions, x, k, v, kv, chain_ffn):
             assert_gemv_close(c.y_down.cpu().numpy(), oracle.gemv_q8(blocks["wdown"], h_used))
         r0 += c.n
     # stored rows within one f16 ulp plus the GEMV bar of their row; everything else untouched
-    kg, vg = as_u16(kv.k), as_u16(kv.v)
-    k0, v0 = as_u16(k), as_u16(v)
-    for got, ref, init in ((kg, kc_o, k0), (vg, vc_o, v0)):
-        written = ref != init
-        assert np.array_equal(got[~written], ref[~written])
-        gf = got.view(np.float16).astype(np.float64)
-        rf = ref.view(np.float16).astype(np.float64)
-        rms = np.sqrt(np.mean(rf[written] ** 2))
-        ulp = np.abs(np.spacing(rf.astype(np.float16)).astype(np.float64))
-        assert np.all(np.abs(gf - rf)[written] <= ulp[written] + 1e-3 * rms)
+    for got, ref, init in ((as_u16(kv.k), kc_o, as_u16(k)), (as_u16(kv.v), vc_o, as_u16(v))):
+        _cache_close(got, ref, ref != init)
+
+
+def _cache_close(got, ref, written):
+    """f16 cache planes (as u16): bit-identical outside `written`, within one ulp plus 1e-3 of the
+    written values' rms inside (a stored row is the f16 rounding of a projected, rotated value)."""
+    assert np.array_equal(got[~written], ref[~written])
+    gf = got.view(np.float16).astype(np.float64)
+    rf = ref.view(np.float16).astype(np.float64)
+    rms = np.sqrt(np.mean(rf[written] ** 2))
+    ulp = np.abs(np.spacing(rf.astype(np.float16)).astype(np.float64))
+    assert np.all(np.abs(gf - rf)[written] <= ulp[written] + 1e-3 * rms)
 
 
 def _case(dl, S, positions, regions, n_regions, capacity, label, chain_ffn=False, path=0, repeat=True):
@@ -131,8 +134,8 @@ def _case(dl, S, positions, regions, n_regions, capacity, label, chain_ffn=False
                 assert_gemv_close(c.gu.cpu().numpy(), g1.cpu().numpy())
                 assert_gemv_close(c.y_down.cpu().numpy(), d1.cpu().numpy())
             assert dl.dl_status_read(c.status) == 0
-        for got, ref in ((kv.k, kv1[0]), (kv.v, kv1[1])):
-            assert int(f16_ulp_dist(as_u16(got), as_u16(ref)).max()) <= 1
+        for got, ref, init in ((kv.k, kv1[0], k), (kv.v, kv1[1], v)):
+            _cache_close(as_u16(got), as_u16(ref), as_u16(ref) != as_u16(init))
     return step
 
 
