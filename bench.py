@@ -45,6 +45,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--layers", type=int, default=8)
+    p.add_argument("--repeats", type=int, default=5,
+                   help="timed regions of --steps steps each; the line reports the median region")
     p.add_argument("--workload", default="3b-8", choices=["3b-8", "3b-1", "3b-2", "3b-4", "3b-12", "1b-1", "3b-8-32k"])
     p.add_argument("--no-extras", action="store_true", help="skip the 1-row and 12-stream side measurements")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -111,18 +113,20 @@ def workload(name):
     raise ValueError(name)
 
 
-def step_bytes(wl, step, kv="f16"):
-    """Algorithmic HBM bytes of one layer step: weights once per command, each session's keys
-    once, the new K/V rows (at the mirror's bytes per value), and every call's activation rows
-    in and out (f32)."""
+def step_bytes(wl, step, kv="f16", weights_once=False):
+    """Algorithmic HBM bytes of one layer step: weights once per command (once per step with
+    `weights_once`: commands that run at the same time can share one pass through L2), each
+    session's keys once, the new K/V rows (at the mirror's bytes per value), and every call's
+    activation rows in and out (f32)."""
     eb = KV_ELEM_BYTES[kv]
     S = wl["shape"]
     D, n_q, n_kv, H, F = S.head_dim, S.n_q, S.n_kv, S.hidden, S.ffn
     w_bytes = sum(no * ni // 32 * 34 for no, ni in S.projections().values())
-    total = 0
+    total = w_bytes if weights_once else 0
     for c in step.commands:
         n = c.n
-        total += w_bytes
+        if not weights_once:
+            total += w_bytes
         p = c.plan
         keys = 0
         for s in range(p.n_sessions):
@@ -262,7 +266,8 @@ def build_layers(wl, L, dev, seed=0, kv="f16"):
 
 
 def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=True, paths=(0, 0), fused=False,
-            cluster=False, chain=False, prefetch=False, concurrent=False, tail=False, kv="f16", one=False):
+            cluster=False, chain=False, prefetch=False, concurrent=False, tail=False, kv="f16", one=False,
+            repeats=5):
     import synth
     import torch
     import row_decode_step_gb300 as dl
@@ -315,21 +320,26 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
         while time.time() - t_soak < 1.0:
             replay(4 * L)
             stream.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    # `repeats` timed regions of exactly `steps` layer steps, each bracketed by a barrier and a
+    # device synchronisation; the median region is the result
+    region_ms = []
     t0 = time.time()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        replay(steps)
-        e1.record(stream)
-    torch.cuda.synchronize()
+    for _ in range(max(1, repeats)):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            replay(steps)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        region_ms.append(e0.elapsed_time(e1))
     t1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = e0.elapsed_time(e1)
+    ms = statistics.median(region_ms)
     clocks = None
     if sampler:
         time.sleep(0.25)
@@ -364,7 +374,7 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
     if want_e2e:
         e2e = measure_e2e(step, graphs, L, max(10, min(steps, 500)), stream, dev)
     return dict(ms_total=ms, ms_per_step=ms / steps, status=status, gu_ms=gu_ms, clocks=clocks, step=step,
-                launches_per_step=step.launches, e2e=e2e)
+                launches_per_step=step.launches, e2e=e2e, region_ms=region_ms)
 
 
 def measure_f16w(dev, peak, n_out=16384, n_in=3072, mats=4, reps=50):
@@ -509,10 +519,33 @@ def measure_e2e(step, graphs, L, steps, stream, dev):
             "steps": steps}
 
 
-def cpu_baseline_sample(wl, budget_s=12.0):
-    """The oracle, as it stands, on one full layer step of the workload (host cores, one thread)."""
+def host_info():
+    """The host's core count (all of them and those this process may use) and CPU model."""
+    import platform
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":", 1)[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.split(":", 1)[0].strip() in ("model name", "CPU part"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "usable_cores": cores, "model": model, "machine": platform.machine()}
+
+
+def oracle_step_inputs(wl):
+    """Layer 0 of the workload for the oracle: Q8_0 blocks, caches and activation rows (seeded)."""
     import numpy as np
-    import oracle
     import synth
     S = wl["shape"]
     D = S.head_dim
@@ -525,21 +558,52 @@ def cpu_baseline_sample(wl, budget_s=12.0):
     x = synth.normal_f32(0, "bench/x0", (n, S.hidden)).numpy()
     xf = synth.normal_f32(0, "bench/xf0", (n, S.hidden)).numpy()
     h = synth.normal_f32(0, "bench/h0", (n, S.ffn)).numpy()
-    oracle.lib()
+    return blocks, k, v, x, xf, h
+
+
+def oracle_step_seconds(wl, inp):
+    """One full layer step of the workload in the oracle (the caches restored first, untimed)."""
+    import numpy as np
+    import oracle
+    S = wl["shape"]
+    blocks, k, v, x, xf, h = inp
+    n = len(wl["positions"])
+    kc, vc = k.copy(), v.copy()
+    t0 = time.perf_counter()
+    for g0 in range(0, n, 8):
+        sl = slice(g0, min(n, g0 + 8))
+        pos = np.array(wl["positions"][sl], np.int32)
+        oracle.layer_step(blocks, x[sl], kc, vc, pos, n_q=S.n_q, n_kv=S.n_kv, head_dim=S.head_dim,
+                          theta=S.rope_theta, chunk=256, n_splits=-(-int(pos.max() + 1) // 256),
+                          regions=np.array(wl["regions"][sl], np.int32), x_ffn=xf[sl], h=h[sl])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_sample(wl, threads=1, budget_s=12.0, max_reps=5, inp=None):
+    """The oracle, as it stands, on full layer steps of the workload on the host's cores: `threads`
+    threads over its (row, output) and (row, head) loops (OpenMP), up to `max_reps` steps within
+    about `budget_s` seconds."""
+    import oracle
+    inp = inp if inp is not None else oracle_step_inputs(wl)
+    used = oracle.set_threads(threads)
     reps, t_total = 0, 0.0
-    while reps < 5 and t_total < budget_s:
-        kc, vc = k.copy(), v.copy()
-        t0 = time.perf_counter()
-        for g0 in range(0, n, 8):
-            sl = slice(g0, min(n, g0 + 8))
-            pos = np.array(wl["positions"][sl], np.int32)
-            oracle.layer_step(blocks, x[sl], kc, vc, pos, n_q=S.n_q, n_kv=S.n_kv, head_dim=D,
-                              theta=S.rope_theta, chunk=256, n_splits=-(-int(pos.max() + 1) // 256),
-                              regions=np.array(wl["regions"][sl], np.int32), x_ffn=xf[sl], h=h[sl])
-        t_total += time.perf_counter() - t0
+    while reps < max_reps and (reps == 0 or t_total < budget_s):
+        t_total += oracle_step_seconds(wl, inp)
         reps += 1
-    return {"value": reps / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d full layer step(s) of the workload on layer 0, single-threaded C oracle (double)" % reps}
+    oracle.set_threads(1)
+    return {"value": reps / t_total, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": "%d full layer step(s) of the workload on layer 0, C oracle (double), %d thread(s)"
+                      % (reps, used)}
+
+
+def cpu_baselines(wl):
+    """The oracle on all the host's usable cores (the reported baseline) and on one core."""
+    host = host_info()
+    inp = oracle_step_inputs(wl)
+    allc = cpu_baseline_sample(wl, threads=host["usable_cores"], budget_s=8.0, max_reps=5, inp=inp)
+    one = cpu_baseline_sample(wl, threads=1, budget_s=4.0, max_reps=2, inp=inp)
+    allc.update({"host_cores": host["usable_cores"], "host": host, "single_thread": one})
+    return allc
 
 
 def combine_ranks(ms_local, steps, world, device):
@@ -648,7 +712,7 @@ def run_ours(args):
     res = measure(wl, args.layers, args.steps, args.warmup, dev, rank, world, paths=(args.gemv_path, args.attn_path),
                   fused=bool(args.fused_rope), cluster=bool(args.cluster_merge), chain=bool(args.gemv_chain),
                   prefetch=bool(args.l2_prefetch), concurrent=bool(args.concurrent_commands),
-                  tail=bool(args.tail_merge), kv=args.kv, one=bool(args.one_launch))
+                  tail=bool(args.tail_merge), kv=args.kv, one=bool(args.one_launch), repeats=args.repeats)
     steps = args.steps
     ms, value = combine_ranks(res["ms_total"], steps, world, dev)
     step = res["step"]
@@ -660,21 +724,31 @@ def run_ours(args):
     gu_gbs = gu_bytes(wl, step.commands[0].n) / (gu_avg_ms / 1e3) / 1e9 if gu_avg_ms else None
     extras = {}
     if not args.no_extras and args.workload == "3b-8":
-        for name in ("3b-1", "3b-12"):
+        # the other configurations, each its own line: median of the repeated timed regions
+        for name in ("3b-1", "3b-2", "3b-4", "1b-1", "3b-8-32k", "3b-12"):
             w2 = workload(name)
-            r2 = measure(w2, args.layers, max(20, min(args.steps, 2000)), args.warmup, dev, rank, world,
+            st2 = max(20, min(args.steps, 2000))
+            r2 = measure(w2, args.layers, st2, args.warmup, dev, rank, world,
                          want_clocks=False, want_e2e=False, paths=(args.gemv_path, args.attn_path),
                          fused=bool(args.fused_rope), cluster=bool(args.cluster_merge),
                          chain=bool(args.gemv_chain), prefetch=bool(args.l2_prefetch),
                          concurrent=bool(args.concurrent_commands), tail=bool(args.tail_merge), kv=args.kv,
-                         one=bool(args.one_launch))
+                         one=bool(args.one_launch), repeats=args.repeats)
             sb2 = step_bytes(w2, r2["step"], args.kv)
-            extras[name] = {"rows": len(w2["positions"]), "layer_steps_per_s": 1e3 / r2["ms_per_step"],
-                            "ms_per_step": r2["ms_per_step"],
-                            "tokens_per_s": len(w2["positions"]) * 1e3 / r2["ms_per_step"],
-                            "algorithmic_gbs": sb2 / (r2["ms_per_step"] / 1e3) / 1e9,
-                            "hbm_frac": sb2 / (r2["ms_per_step"] / 1e3) / 1e9 / peak,
-                            "commands": len(r2["step"].commands), "status": r2["status"]}
+            sec = r2["ms_per_step"] / 1e3
+            line2 = {"workload": w2["desc"], "rows": len(w2["positions"]), "layer_steps_per_s": 1 / sec,
+                     "ms_per_step": r2["ms_per_step"], "tokens_per_s": len(w2["positions"]) / sec,
+                     "algorithmic_bytes": sb2, "algorithmic_gbs": sb2 / sec / 1e9, "hbm_frac": sb2 / sec / 1e9 / peak,
+                     "commands": [c.n for c in r2["step"].commands], "status": r2["status"],
+                     "timed_regions_ms_per_step": [m / st2 for m in r2["region_ms"]], "steps_per_region": st2}
+            if len(r2["step"].commands) > 1 and bool(args.concurrent_commands):
+                # commands that run at the same time may share the weights' pass through L2: the
+                # fraction with the weights counted once is the one to hold against the peak
+                sb1 = step_bytes(w2, r2["step"], args.kv, weights_once=True)
+                line2.update({"algorithmic_bytes_weights_per_command": sb2, "algorithmic_bytes": sb1,
+                              "algorithmic_gbs": sb1 / sec / 1e9, "hbm_frac": sb1 / sec / 1e9 / peak,
+                              "hbm_frac_weights_per_command": sb2 / sec / 1e9 / peak})
+            extras[name] = line2
             del r2
             torch.cuda.empty_cache()
     if not args.no_extras and args.workload == "3b-8" and args.kv == "f16":
@@ -706,13 +780,15 @@ def run_ours(args):
         torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_sample(wl)
+        cpu = cpu_baselines(wl)
     if rank != 0:
         return
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
+        "timing": {"timed_regions": len(res["region_ms"]), "steps_per_region": steps,
+                   "ms_per_step_each": [m / steps for m in res["region_ms"]], "reported": "median region"},
         "operands": "q8_0 weights, f32 activations, f16 KV mirror; f32 accumulation (tensor-core operands f16)",
         "data": "synthetic (seeded N(0,0.02) Q8_0 weights, N(0,1) activations and f16 KV; no trained weights)",
         "config": {"workload": wl["desc"], "rows": rows, "layers_cycled": args.layers,
@@ -735,10 +811,13 @@ def run_ours(args):
                      "bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s",
                      "frac": (gu_gbs / peak) if gu_gbs else None,
                      "traffic": traffic_for("gemv_gu_%drows" % step.commands[0].n),
+                     "traffic_source": "stored: ncu --set full capture of this kernel (profiles/ncu_traffic.txt), "
+                                       "null when gemv_q8.cu changed since",
                      "launch_ms": gu_avg_ms, "peak_source": peak_src},
         "cpu_baseline": cpu,
         "e2e": res["e2e"],
         "gpu_launches": res["launches_per_step"] * steps,
+        "gpu_launches_note": "per timed region (%d regions timed)" % len(res["region_ms"]),
         "clocks": res["clocks"],
         "device_status": res["status"],
         "side_workloads": extras,
@@ -749,65 +828,38 @@ def run_ours(args):
 # ----------------------------------------------------------------------------- reference arm (CPU oracle)
 
 def run_reference(args):
+    """The oracle as it stands on the host's cores: whole layer steps of the workload, each timed.
+    Warm-up and timed steps stop early once they pass a time budget (the line then reports the
+    steps it timed)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import numpy as np
     import oracle
-    import synth
     wl = workload(args.workload)
-    S = wl["shape"]
-    D = S.head_dim
-    n = len(wl["positions"])
-    # a bounded sample of the step: every 32nd output row of each projection and the
-    # attention of one KV head (its query heads) for every row; scaled to a whole step
-    FR = 32
-    blocks = {}
-    for name, (n_out, n_in) in S.projections().items():
-        b = synth.q8_0_blocks_from_normal(0, "%s/L0/%s" % (S.name, name), n_out, n_in).numpy()
-        blocks[name] = np.ascontiguousarray(b[::FR])
-    kc = synth.kv_cache_normal(0, "%s/L0/K" % S.name, wl["n_regions"], S.n_kv, wl["capacity"], D)
-    vc = synth.kv_cache_normal(0, "%s/L0/V" % S.name, wl["n_regions"], S.n_kv, wl["capacity"], D)
-    k1 = np.ascontiguousarray(kc.numpy().view(np.uint16)[:, :1])
-    v1 = np.ascontiguousarray(vc.numpy().view(np.uint16)[:, :1])
-    G = S.n_q // S.n_kv
-    x = synth.normal_f32(0, "bench/x0", (n, S.hidden)).numpy()
-    xf = synth.normal_f32(0, "bench/xf0", (n, S.hidden)).numpy()
-    h = synth.normal_f32(0, "bench/h0", (n, S.ffn)).numpy()
-    q = synth.normal_f32(0, "bench/q0", (n, G * D)).numpy().astype(np.float64)
-    seqlen = np.array([p + 1 for p in wl["positions"]], np.int32)
-    regions = np.array(wl["regions"], np.int32)
-    oracle.lib()
-
-    def one():
-        tg = time.perf_counter()
-        for g0 in range(0, n, 8):
-            sl = slice(g0, min(n, g0 + 8))
-            oracle.gemv_q8(blocks["wqkv"], x[sl])
-            oracle.gemv_q8(blocks["wo"], x[sl])
-            oracle.gemv_q8(blocks["wgu"], xf[sl])
-            oracle.gemv_q8(blocks["wdown"], h[sl])
-        t_gemv = time.perf_counter() - tg
-        ta = time.perf_counter()
-        oracle.attention(q, k1, v1, seqlen, n_q=G, n_kv=1, head_dim=D, chunk=256,
-                         n_splits=-(-int(seqlen.max()) // 256), row_region=regions)
-        t_attn = time.perf_counter() - ta
-        return t_gemv * FR + t_attn * S.n_kv
-
-    for _ in range(args.warmup):
-        one()
-    est = [one() for _ in range(args.steps)]
-    sec_per_step = sum(est) / len(est)
-    value = 1.0 / sec_per_step
-    sample = ("per step: 1/%d of every projection's output rows and 1 of %d KV heads' attention, "
-              "scaled to the whole layer step; single-threaded C oracle (double)" % (FR, S.n_kv))
+    host = host_info()
+    inp = oracle_step_inputs(wl)
+    used = oracle.set_threads(host["usable_cores"])
+    t_w = 0.0
+    for _ in range(min(args.warmup, 3)):
+        t_w += oracle_step_seconds(wl, inp)
+        if t_w > 20.0:
+            break
+    times = []
+    while len(times) < args.steps and (not times or sum(times) < 90.0):
+        times.append(oracle_step_seconds(wl, inp))
+    oracle.set_threads(1)
+    sec = sum(times) / len(times)
+    value = 1.0 / sec
+    sample = ("%d whole layer steps of the workload on layer 0, each timed; C oracle (double) on %d threads "
+              "(OpenMP over (row, output) and (row, head))" % (len(times), used))
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": sec_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": wl["desc"], "rows": n},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": len(times),
+        "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": wl["desc"], "rows": len(wl["positions"])},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample,
+                         "host_cores": host["usable_cores"], "host": host},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

@@ -611,7 +611,13 @@ int dl_layer_step(const dl_layer_weights *W, const dl_layer_bufs *B, const float
  *    Calls whose kernels overlap on the GPU (other streams, other threads) race
  *    on the array; serialise them.
  *  - A plan whose workspace_bytes exceeds the array is refused with
- *    DL_E_WORKSPACE before anything is launched.
+ *    DL_E_WORKSPACE before anything is launched.  A cluster plan
+ *    (dl_attn_plan_build_cluster: no partials) is refused with DL_E_ARG; it
+ *    goes to dl_decode_attn_cluster, which needs no workspace either.
+ *  - The array's device address is asked of the runtime on every call made
+ *    outside stream capture; a call under capture uses the address asked last
+ *    on that device.  After cudaDeviceReset (a new context, so a new address)
+ *    make one call outside capture before capturing another.
  */
 size_t dl_decode_attention_noalloc_max_bytes(void);
 int dl_decode_attention_noalloc(const float *q, int64_t q_stride, const dl_kv_cache *kv,

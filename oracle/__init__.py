@@ -22,10 +22,11 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so with plain -O2 (no fast-math, no vector intrinsics)."""
+    """Compile oracle.c into liboracle.so with plain -O2 (no fast-math, no vector intrinsics), OpenMP
+    for its (row, output) and (row, head) loops."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp.%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math", "-fopenmp",
                                "-Wall", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -65,6 +66,9 @@ def lib():
         L.orc_attn_full.argtypes = [P, I64, I, I, I, I, P, P, I64, I, P, P, P, I64, P]
         L.orc_attn_full_f32.argtypes = L.orc_attn_full.argtypes
         L.orc_plan_groups.argtypes = [I, I, P]
+        L.orc_set_threads.argtypes = [I]
+        L.orc_set_threads.restype = I
+        L.orc_set_threads(1)
         for f in ("orc_gemv_q8", "orc_gemv_f16w", "orc_q8_dequant", "orc_matmul", "orc_rope_kv_store",
                   "orc_rope_kv_store_f32", "orc_rope_kv_store_q8", "orc_attn_split", "orc_attn_split_f32",
                   "orc_attn_split_q8", "orc_attn_merge", "orc_attn_full", "orc_attn_full_f32", "orc_attn_full_q8",
@@ -72,6 +76,12 @@ def lib():
             getattr(L, f).restype = I
         _lib = L
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Threads of the oracle's parallel (row, output) and (row, head) loops from now on; returns the
+    number in effect.  Results do not depend on it."""
+    return int(lib().orc_set_threads(int(n)))
 
 
 def _np(a, dtype) -> np.ndarray:

@@ -33,14 +33,35 @@
  * identity, rotation composition, full-softmax attention, seqlen-1 and equal-key
  * attention, and split invariance of the merge.  No function here is "parity
  * unpinned".
+ *
+ * Threads: built with OpenMP, the GEMV runs its (row, output) pairs and the split
+ * attention its (row, head) pairs on several threads (orc_set_threads; one by
+ * default).  Each result is still computed by one thread in the order above, so
+ * the values do not depend on the thread count.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_OK 0
 #define ORC_EARG (-1)
+
+/* Threads the parallel loops use from now on (at least 1); returns the number in effect
+ * (always 1 without OpenMP). */
+int orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    omp_set_num_threads(n < 1 ? 1 : n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 /* ---------------------------------------------------------------- f16 ---- */
 
@@ -134,6 +155,7 @@ int orc_gemv_q8(const uint8_t *blocks, int64_t n_out, int64_t n_in,
     if (!blocks || !x || !y || n_in % 32 != 0 || rows < 0)
         return ORC_EARG;
     int64_t nb = n_in / 32;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int r = 0; r < rows; ++r) {
         for (int64_t o = 0; o < n_out; ++o) {
             double acc = 0.0;
@@ -463,11 +485,15 @@ static int orc_attn_split_any(const double *q, int64_t q_stride, int rows, int n
         return ORC_EARG;
     int D = head_dim, G = n_q / n_kv;
     for (int r = 0; r < rows; ++r) {
-        int reg = row_region ? row_region[r] : 0;
         int L = seqlen[r];
         if (L < 1 || L > capacity || (int64_t)n_splits * chunk < L)
             return ORC_EARG;
+    }
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int r = 0; r < rows; ++r) {
         for (int h = 0; h < n_q; ++h) {
+            int reg = row_region ? row_region[r] : 0;
+            int L = seqlen[r];
             int kvh = h / G;
             int64_t hbase = (int64_t)reg * region_stride + (int64_t)kvh * capacity * D;
             const double *qv = q + r * q_stride + (int64_t)h * D;

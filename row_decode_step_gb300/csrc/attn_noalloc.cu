@@ -20,19 +20,24 @@ constexpr size_t kScratchBytes = (size_t)8 << 20;    // 8 MiB of partials
 __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
-void *g_scratch_dev[256] = {};   // the array's device address, per device ordinal
+void *g_scratch_dev[256] = {};   // the array's device address asked last, per device ordinal
 
 // Device address of the array on the current device.  In host code the array's
-// name is only a host-side stand-in, so the address is asked of the runtime, once
-// per device, with that device current.
-int scratch_address(void **out)
+// name is only a host-side stand-in, so the address is asked of the runtime.  It is
+// asked again on every call made outside stream capture (a cudaDeviceReset gives the
+// device a new context and the array a new address); a call under capture uses the
+// address asked last on that device.
+int scratch_address(cudaStream_t st, void **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attention_noalloc: cudaGetDevice");
     if (dev < 0 || dev >= 256) return dl::fail(DL_E_ARG, "dl_decode_attention_noalloc: device %d", dev);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attention_noalloc: cudaStreamIsCapturing");
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_dev[dev]) {
+    if (cs == cudaStreamCaptureStatusNone || !g_scratch_dev[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_attn_scratch);
         if (e != cudaSuccess) return dl::cuda_fail(e, "dl_decode_attention_noalloc: cudaGetSymbolAddress");
@@ -55,13 +60,16 @@ int dl_decode_attention_noalloc(const float *q, int64_t q_stride, const dl_kv_ca
 {
     dl::clear_error();
     if (!plan) return dl::fail(DL_E_ARG, "dl_decode_attention_noalloc: null plan");
+    if (plan->cluster > 0)
+        return dl::fail(DL_E_ARG, "dl_decode_attention_noalloc: a cluster plan merges inside its clusters and keeps "
+                                  "no partials; call dl_decode_attn_cluster, which needs no workspace either");
     if (plan->workspace_bytes > kScratchBytes)
         return dl::fail(DL_E_WORKSPACE,
                         "dl_decode_attention_noalloc: the plan needs %zu bytes of partials, the library's "
                         "fixed buffer holds %zu; use dl_decode_attn with a caller workspace",
                         plan->workspace_bytes, kScratchBytes);
     void *scratch = nullptr;
-    int rc = scratch_address(&scratch);
+    int rc = scratch_address(static_cast<cudaStream_t>(stream), &scratch);
     if (rc != DL_OK) return rc;
     rc = dl_decode_attn(q, q_stride, kv, seqlen, plan, scratch, kScratchBytes, status, stream);
     if (rc != DL_OK) return rc;

@@ -166,3 +166,59 @@ def test_l2_prefetch_next_arguments(dl):
     # the next launching call takes them even when it refuses its own arguments
     assert L.dl_gemv_q8(None, None, 1, 0, None, 0, None) == dl.DL_E_ARG
     assert L.dl_l2_prefetch_next(0, None, None) == dl.DL_OK
+
+
+def test_layer_step_refusals_before_any_launch(dl):
+    """dl_layer_step checks its plan and cache on the host first: a cluster plan (no partials in
+    the workspace) and a mirror other than f16 are refused before anything is read on the device
+    (pointers are host integers here: nothing is dereferenced or launched)."""
+    L = dl.lib()
+    P = ctypes.c_void_p
+    assert L.dl_layer_step(None, None, None, None, None, None, None, None, None, 0, None, 0, None) == dl.DL_E_ARG
+    n_q, n_kv, D = 24, 8, 128
+    W = dl.dl_layer_weights()
+    B = dl.dl_layer_bufs()
+    rope = dl.dl_rope()
+    kv = dl.dl_kv_cache()
+    kv.k, kv.v, kv.head_dim, kv.n_kv, kv.capacity, kv.n_regions = 4096, 8192, D, n_kv, 5128, 1
+    kv.region_stride, kv.elem_bytes = n_kv * 5128 * D, 2
+    fake = P(4096)
+    cplan = dl.dl_attn_plan_build_cluster([5128] * 8, n_q, n_kv, D, regions=[0] * 8, sm_count=152)
+    rc = L.dl_layer_step(ctypes.byref(W), ctypes.byref(B), None, fake, ctypes.byref(rope), ctypes.byref(kv),
+                         fake, ctypes.byref(cplan), fake, 1 << 20, None, 0, None)
+    assert rc == dl.DL_E_ARG and "cluster" in L.dl_last_error().decode()
+    plan = dl.dl_attn_plan_build([5128] * 8, n_q, n_kv, D, regions=[0] * 8, sm_count=152)
+    kv.elem_bytes = 4
+    rc = L.dl_layer_step(ctypes.byref(W), ctypes.byref(B), None, fake, ctypes.byref(rope), ctypes.byref(kv),
+                         fake, ctypes.byref(plan), fake, 1 << 20, None, 0, None)
+    assert rc == dl.DL_E_SHAPE and "f16" in L.dl_last_error().decode()
+
+
+@pytest.mark.parametrize("kw", [dict(one_launch=True), dict(gemv_chain=True)])
+def test_layer_step_refuses_concurrent_grid_wide_launches(kw):
+    """Launches that hold every SM and wait across their CTAs cannot run as concurrent commands:
+    the refusal comes before anything is allocated."""
+    from row_decode_step_gb300.step import LayerStep
+    with pytest.raises(ValueError):
+        LayerStep([5120] * 12, list(range(12)), 24, 8, 128, 3072, 8192, "cpu", concurrent=True, **kw)
+
+
+def test_oracle_results_do_not_depend_on_threads():
+    """The oracle's parallel loops give each result to one thread in the stated order: any thread
+    count returns the same bits."""
+    import synth
+    blocks = synth.q8_0_blocks_from_normal(4, "thr/w", 96, 256).numpy()
+    x = synth.normal_f32(4, "thr/x", (3, 256)).numpy()
+    k = synth.kv_cache_normal(4, "thr/K", 1, 2, 300, 64).numpy().view(np.uint16)
+    v = synth.kv_cache_normal(4, "thr/V", 1, 2, 300, 64).numpy().view(np.uint16)
+    q = synth.normal_f32(4, "thr/q", (3, 8 * 64)).numpy().astype(np.float64)
+    sl = np.array([300, 171, 1], np.int32)
+    got = []
+    for t in (1, 4):
+        oracle.set_threads(t)
+        y = oracle.gemv_q8(blocks, x)
+        o, l = oracle.attention(q, k, v, sl, n_q=8, n_kv=2, head_dim=64, chunk=64, n_splits=5)
+        got.append((y, o, l))
+    oracle.set_threads(1)
+    for a, b in zip(got[0], got[1]):
+        assert np.array_equal(a, b)

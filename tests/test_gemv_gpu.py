@@ -81,11 +81,13 @@ def test_gemv_cuda_core_path_refuses_wide_commands(dl):
 def test_gemv_rows_match_single_rows(dl):
     """Rows stepped together agree with the same rows stepped one at a time (tails of 2, 9, 16).
 
-    One row takes the CUDA-core inner product (activations in f32); a command of 2 or
-    more rows takes the int8 tensor path, whose two-term activation code x ~ s(h + l/254),
-    s = max|x|/127 over a warp's inputs, is off by at most s/508 per element.  Summed
-    against N(0, 0.02) weights that stays near 1e-4 of the output scale, so the two agree
-    at 3e-4, well inside the 1e-3 bar each of them meets against the oracle.
+    One or two rows take the CUDA-core inner product (f32 activations and sums); a command
+    of more rows takes the tensor-core path, whose activations enter as an f16 hi + lo pair
+    after a power-of-two scale per k-tile (about 22 significant bits) and whose products
+    are summed in f32.  Both are close to an f32 dot product, so they agree with each other
+    at 3e-4 of the output scale (summation order and the lo term's rounding), well inside
+    the 1e-3 bar each of them meets against the oracle.  A 9-row command is stepped as
+    balanced groups (5 + 4), a 16-row one as 8 + 8.
     """
     n_out, n_in = 384, 1024
     blocks = synth.q8_0_blocks_from_normal(2, "gemv/tail", n_out, n_in)
