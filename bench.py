@@ -349,7 +349,7 @@ def measure(wl, L, steps, warmup, dev, rank, world, want_clocks=True, want_e2e=T
 
     # the dominant kernel on its own: the gate/up GEMV of every layer, back to back, timed on its stream
     gu_ms = None
-    if S.ffn:
+    if S.ffn and not one:
         c0 = step.commands[0]
         g_gu = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_gu, stream=stream):

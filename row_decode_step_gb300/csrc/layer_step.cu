@@ -1238,9 +1238,9 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
             int ub, ue;
             unit_share(Gv.RT, Gv.cs, cta, C, ub, ue);
             float *red = reinterpret_cast<float *>(scr);                     // [kRB][kCW][128]: 16 KB
-            float *xs = reinterpret_cast<float *>(scr + 16 * 1024);          // CUDA-core path: [NRC][kPartKT * 32]: 32 KB
+            float *xs = reinterpret_cast<float *>(scr + 16 * 1024);          // CUDA-core path: [NRC][kPartKT * 32]
             float *snc = reinterpret_cast<float *>(scr + 16 * 1024);         // tensor path: [kCW][KPW][bias, 1/scale][8]
-            static_assert(16 * 1024 + 2 * kPartKT * 32 * 4 <= (int)kScratch &&
+            static_assert(16 * 1024 + NRC * kPartKT * 32 * 4 <= (int)kScratch &&
                           16 * 1024 + kCW * kPartSlots * kKWM * 2 * 8 * 4 <= (int)kScratch, "projection scratch fits");
             const int wk0 = warp * kKWM;
             constexpr int KPW = kPartSlots * kKWM;                             // k-tiles of a part per warp
@@ -1314,12 +1314,22 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                     } else {
                         // the part's activation rows in shared memory (zero past n_in)
                         csync();                                 // the previous part's rows are read
-                        for (int e = ctid; e < NRC * nkt * 8; e += kCT) {
+                        // every load of the thread first (one round trip), then the stores
+                        static_assert(kPartKT * 8 == kCT, "a row of a part is one float4 per thread");
+                        float4 v[NRC];
+#pragma unroll
+                        for (int i = 0; i < NRC; ++i) {
+                            const int e = ctid + i * kCT;
                             const int r = e / (nkt * 8), q = e - r * (nkt * 8);       // q: float4 of the part
-                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (r < a.nr && (kt0 * 32 + q * 4) < Gv.n_in)
-                                v = __ldcg(reinterpret_cast<const float4 *>(Gv.x + (int64_t)r * Gv.x_stride + kt0 * 32) + q);
-                            *reinterpret_cast<float4 *>(xs + r * (kPartKT * 32) + q * 4) = v;
+                            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (e < NRC * nkt * 8 && r < a.nr && (kt0 * 32 + q * 4) < Gv.n_in)
+                                v[i] = __ldcg(reinterpret_cast<const float4 *>(Gv.x + (int64_t)r * Gv.x_stride + kt0 * 32) + q);
+                        }
+#pragma unroll
+                        for (int i = 0; i < NRC; ++i) {
+                            const int e = ctid + i * kCT;
+                            const int r = e / (nkt * 8), q = e - r * (nkt * 8);
+                            if (e < NRC * nkt * 8) *reinterpret_cast<float4 *>(xs + r * (kPartKT * 32) + q * 4) = v[i];
                         }
                         csync();
                     }
@@ -1496,6 +1506,11 @@ template <int D>
 StepKernel pick_step_d(bool mma, int nrc)
 {
     if (mma) return layer_step_kernel<D, true, 1>;
+    if constexpr (D == 128) {
+        // the CUDA-core projections of wider commands: an option, to compare the two inner products
+        if (nrc > 4) return layer_step_kernel<D, false, 8>;
+        if (nrc > 2) return layer_step_kernel<D, false, 4>;
+    }
     return nrc == 1 ? layer_step_kernel<D, false, 1> : layer_step_kernel<D, false, 2>;
 }
 
@@ -1588,7 +1603,8 @@ int dl_layer_step(const dl_layer_weights *W, const dl_layer_bufs *B, const float
         return dl::fail(DL_E_ARG, "dl_layer_step: rope table");
     if (path < 0 || path > 2) return dl::fail(DL_E_ARG, "dl_layer_step: path=%d", path);
     const bool mma = path == 2 || (path == 0 && rows > 2);
-    if (!mma && rows > 2) return dl::fail(DL_E_SHAPE, "dl_layer_step: the CUDA-core projections serve 1 or 2 rows");
+    if (!mma && rows > 2 && D != 128)
+        return dl::fail(DL_E_SHAPE, "dl_layer_step: the CUDA-core projections serve more than 2 rows at head_dim 128 only");
     const bool ffn = W->gu.qs != nullptr;
     const dl_q8_weight *w[4] = {&W->qkv, &W->o, &W->gu, &W->down};
     const int ng = ffn ? 4 : 2;
@@ -1634,7 +1650,7 @@ int dl_layer_step(const dl_layer_weights *W, const dl_layer_bufs *B, const float
     if (rc != DL_OK) return rc;
     if (dl::ceil_div(P.n_work, sm) > kMaxIt)
         return dl::fail(DL_E_SHAPE, "dl_layer_step: %d work items exceed %d per SM", P.n_work, kMaxIt);
-    const StepKernel kern = pick_step(D, mma, mma ? 1 : rows);
+    const StepKernel kern = pick_step(D, mma, mma ? 1 : rows);   // rows 3, 4 -> 4; 5..8 -> 8
     {
         static std::mutex mu;
         static const void *ready[16][8];

@@ -148,7 +148,8 @@ class Command:
         return self.x_ffn, self.h
 
     def run(self, W: LayerWeights, rope: Rope, kv: KVCache, stream=None):
-        gp = self.gemv_path if (self.gemv_path != 1 or self.n <= 2) else 0
+        # the separate GEMV's CUDA-core form serves 1 or 2 rows; the one launch's serves up to 8
+        gp = self.gemv_path if (self.gemv_path != 1 or self.n <= 2 or self.one_launch) else 0
         if self.one_launch:
             Wc = W.c()
             if self.step_ws is None:

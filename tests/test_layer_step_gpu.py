@@ -206,3 +206,10 @@ def test_layer_step_refuses_concurrent(dl):
     with pytest.raises(ValueError):
         LayerStep(lens, list(range(12)), S.n_q, S.n_kv, S.head_dim, S.hidden, S.ffn, "cuda", one_launch=True,
                   concurrent=True)
+
+
+@pytest.mark.parametrize("rows", [3, 4, 8])
+def test_layer_step_3b_cuda_core_wide(dl, rows):
+    """The CUDA-core projections asked for explicitly on 3 to 8 rows (the option that compares the
+    two inner products on the same launch)."""
+    _case(dl, synth.LLAMA_3B, list(range(5120, 5120 + rows)), [0] * rows, 1, 5128, "ls/3bcc%d" % rows, path=1)
