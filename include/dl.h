@@ -13,6 +13,8 @@
  *                     command's rows
  *   dl_attn_merge     log-sum-exp merge of the split pieces
  *   dl_gemv_f16w      the same projection GEMV on f16 weights (the reference lane)
+ *   dl_layer_step     the whole layer step of one command as one launch (an option:
+ *                     it reads the same bytes and is not yet faster than the calls)
  *
  * plus host-side helpers (weight packing, RoPE tables, the row-grouping and
  * split planner, status words).
@@ -523,10 +525,11 @@ int dl_attn_merge(const void *workspace, const dl_attn_plan *plan, const int32_t
  * rows' new k and v into the f16 mirror, split-KV attention over the plan's
  * pieces, their log-sum-exp merge, then the O, gate/up and down projections.
  * Each part has the arithmetic of its separate call (dl_gemv_q8_ex,
- * dl_decode_attn_rope, dl_attn_merge); the projections' K is cut into slices of
- * 1024 inputs whose sums are added in slice order, so a projection's last bits
- * may differ from dl_gemv_q8's (not from call to call: results are
- * deterministic).
+ * dl_decode_attn_rope, dl_attn_merge); the projections' K is cut into parts of
+ * 1024 inputs whose sums are added (atomically, in the order they arrive) into
+ * outputs the launch zeroes first, so a projection's last bits may differ from
+ * dl_gemv_q8's and, with three or more parts, from one call to the next; the
+ * stored k and v rows follow them within one f16 ulp.
  *
  * The launch holds one CTA per SM for the whole step.  A CTA streams its share
  * of every projection's weights and of the keys ahead of use, and each part
@@ -558,7 +561,7 @@ typedef struct dl_layer_bufs {
 
 /*
  * Bytes of the workspace dl_layer_step needs for these weights and plan: its
- * own counters, the projections' slice sums and the attention pieces' (o, lse).
+ * own counters and the attention pieces' (o, lse).
  * Host only.
  */
 int dl_layer_step_workspace_size(const dl_layer_weights *W, const dl_attn_plan *plan, size_t *bytes);
@@ -579,7 +582,8 @@ int dl_layer_step_workspace_size(const dl_layer_weights *W, const dl_attn_plan *
  *             DL_STATUS_SYNC_TIMEOUT if a bounded wait gave up (outputs invalid;
  *             zero the workspace again before the next call)
  *   path      0 automatic (tensor-core projections for 3..8 rows, CUDA cores for
- *             1..2), 1 CUDA-core projections (1..2 rows only), 2 tensor cores;
+ *             1..2), 1 CUDA-core projections (3..8 rows at head_dim 128 only:
+ *             slower, kept to compare the two), 2 tensor cores;
  *             the attention takes tensor cores for work items of more than four
  *             queries, CUDA cores otherwise
  * The f16 mirror only (elem_bytes 0 or 2), head_dim 64 or 128.  The launch holds
