@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
     const int wk0 = warp * KWM;                                  // slice-local
     const int nw = max(0, min(KWM, nkt - wk0));
     if (lane == 0 && kConsumers * KWM != a.ksl) atomicExch(&s_shape_bad, 1);   // broken launch shape
-    // lane (g, c) holds inputs 2c, 2c+1 / 8+2c, 9+2c / 16+2c, 17+2c / 24+2c, 25+2c of each k-tile
+    // lane (g, c) holds inputs 8c .. 8c + 7 of each k-tile (pairs 8c + 2p, 8c + 2p + 1): the packed
+    // weights put the same inputs in the MMA slots 2c, 2c+1 / 2c+8, 2c+9 / 16+2c, 17+2c / 24+2c, 25+2c
     uint32_t bh[MMA ? KWM : 1][4], bl[MMA ? KWM : 1][4];
     float2 ncorr[MMA && !W16 ? KWM : 1];         // -1152 * sum(x) of columns 2c, 2c+1 per k-tile (Q8_0)
     float xv[MMA ? 1 : KWM][NRC][8];
@@ -200,11 +201,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
         for (int j = 0; j < KWM; ++j) {
             const int kl = wk0 + j;
             const bool live = kl * 32 < xfl && g < a.nr;
-            const float *xr = a.x + (int64_t)g * a.x_stride + (kt0 + kl) * 32 + 2 * c;
-#pragma unroll
-            for (int p = 0; p < 4; ++p)
-                v[j][p] = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
-                               : make_float2(0.f, 0.f);
+            const float4 *xr = reinterpret_cast<const float4 *>(a.x + (int64_t)g * a.x_stride + (kt0 + kl) * 32 + 8 * c);
+            const float4 lo = live ? __ldcg(xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 hi = live ? __ldcg(xr + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j][0] = make_float2(lo.x, lo.y);
+            v[j][1] = make_float2(lo.z, lo.w);
+            v[j][2] = make_float2(hi.x, hi.y);
+            v[j][3] = make_float2(hi.z, hi.w);
         }
         issue_rest();
 #pragma unroll
@@ -254,14 +257,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_q8_kernel(const __grid_const
 #pragma unroll
             for (int r = 0; r < NRC; ++r) {
                 const bool live = kl * 32 < xfl && r < a.nr;
-                const float *xr = a.x + (int64_t)r * a.x_stride + (kt0 + kl) * 32 + 2 * c;
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const float2 t = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
-                                          : make_float2(0.f, 0.f);
-                    xv[j][r][2 * p] = t.x;
-                    xv[j][r][2 * p + 1] = t.y;
-                }
+                const float4 *xr = reinterpret_cast<const float4 *>(a.x + (int64_t)r * a.x_stride + (kt0 + kl) * 32 + 8 * c);
+                const float4 lo = live ? __ldcg(xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 hi = live ? __ldcg(xr + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xv[j][r][0] = lo.x;
+                xv[j][r][1] = lo.y;
+                xv[j][r][2] = lo.z;
+                xv[j][r][3] = lo.w;
+                xv[j][r][4] = hi.x;
+                xv[j][r][5] = hi.y;
+                xv[j][r][6] = hi.z;
+                xv[j][r][7] = hi.w;
             }
         }
         issue_rest();
@@ -489,8 +495,11 @@ __device__ __forceinline__ uint32_t q8_byte(const uint8_t *blocks, int64_t n_out
     return blocks[(o * (n_in / 32) + k / 32) * 34 + 2 + (k % 32)];
 }
 
-// lane t = 4g + c of tile (rt, kt), word p: inputs kb, kb + 1 (kb = 16(p/2) + 8(p%2) + 2c) of
-// row g, then of row g + 8, as biased bytes q + 128 (padding: q = 0)
+// lane t = 4g + c of tile (rt, kt), word p: inputs kb, kb + 1 (kb = 8c + 2p) of row g, then of
+// row g + 8, as biased bytes q + 128 (padding: q = 0).  In the tensor path word p fills the MMA
+// A slots of pair p of the lane (2c, 2c+1 / 2c+8, 2c+9 / 16+2c, 17+2c / 24+2c, 25+2c): the order
+// of the 32 inputs inside a k-tile is permuted alike for the weights and the activations, so a
+// lane's activations are eight consecutive floats (two 16-byte loads)
 __global__ void q8_pack_qs_kernel(const uint8_t *blocks, int64_t n_out, int64_t n_in, int KT,
                                   int64_t units, uint4 *qs)
 {
@@ -503,7 +512,7 @@ __global__ void q8_pack_qs_kernel(const uint8_t *blocks, int64_t n_out, int64_t 
     uint32_t w[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        const int kb = (p >> 1) * 16 + (p & 1) * 8 + 2 * c;
+        const int kb = 8 * c + 2 * p;
         const int64_t k = kt * 32 + kb, o = rt * 16 + g;
         const uint32_t b0 = q8_byte(blocks, n_out, n_in, o, k) ^ 0x80u;
         const uint32_t b1 = q8_byte(blocks, n_out, n_in, o, k + 1) ^ 0x80u;
@@ -688,11 +697,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_chain_kernel(const __grid_co
             float2 v[KWM][4];
 #pragma unroll
             for (int j = 0; j < KWM; ++j) {
-                const float *xr = P.x + (int64_t)g * P.x_stride + (kt0 + wk0 + j) * 32 + 2 * c;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    v[j][q] = g < a.nr ? __ldcg(reinterpret_cast<const float2 *>(xr + (q >> 1) * 16 + (q & 1) * 8))
-                                       : make_float2(0.f, 0.f);
+                const float4 *xr = reinterpret_cast<const float4 *>(P.x + (int64_t)g * P.x_stride + (kt0 + wk0 + j) * 32 + 8 * c);
+                const float4 lo = g < a.nr ? __ldcg(xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 hi = g < a.nr ? __ldcg(xr + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[j][0] = make_float2(lo.x, lo.y);
+                v[j][1] = make_float2(lo.z, lo.w);
+                v[j][2] = make_float2(hi.x, hi.y);
+                v[j][3] = make_float2(hi.z, hi.w);
             }
             float m = 0.f;
 #pragma unroll
@@ -731,14 +742,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_chain_kernel(const __grid_co
             for (int j = 0; j < KWM; ++j)
 #pragma unroll
                 for (int r = 0; r < NRC; ++r) {
-                    const float *xr = P.x + (int64_t)r * P.x_stride + (kt0 + wk0 + j) * 32 + 2 * c;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 t = r < a.nr ? __ldcg(reinterpret_cast<const float2 *>(xr + (q >> 1) * 16 + (q & 1) * 8))
-                                                  : make_float2(0.f, 0.f);
-                        xv[j][r][2 * q] = t.x;
-                        xv[j][r][2 * q + 1] = t.y;
-                    }
+                    const float4 *xr = reinterpret_cast<const float4 *>(P.x + (int64_t)r * P.x_stride + (kt0 + wk0 + j) * 32 + 8 * c);
+                    const float4 lo = r < a.nr ? __ldcg(xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 hi = r < a.nr ? __ldcg(xr + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    xv[j][r][0] = lo.x;
+                    xv[j][r][1] = lo.y;
+                    xv[j][r][2] = lo.z;
+                    xv[j][r][3] = lo.w;
+                    xv[j][r][4] = hi.x;
+                    xv[j][r][5] = hi.y;
+                    xv[j][r][6] = hi.z;
+                    xv[j][r][7] = hi.w;
                 }
         }
         for (int b0 = 0; b0 < nrt && !bad; b0 += RB) {
@@ -1340,7 +1354,7 @@ __global__ void f16w_pack_kernel(const uint16_t *w, int64_t n_out, int64_t n_in,
     for (int e = 0; e < 4; ++e) {
         const int m = 4 * hf + e, p = m >> 1;
         const int64_t o = rt * 16 + g + 8 * (m & 1);
-        const int64_t k = kt * 32 + (p >> 1) * 16 + (p & 1) * 8 + 2 * c;
+        const int64_t k = kt * 32 + 8 * c + 2 * p;
         uint32_t lo = 0u, hi = 0u;
         if (o < n_out && k < n_in) lo = w[o * n_in + k];
         if (o < n_out && k + 1 < n_in) hi = w[o * n_in + k + 1];

@@ -1269,14 +1269,17 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                         for (int jj = 0; jj < KPW; ++jj) {              // every load first (raw bits)
                             const int kl = (jj / kKWM) * kKsl + wk0 + (jj % kKWM);      // part-local k-tile
                             const bool live = kl < nkt && (kt0 + kl) * 32 < Gv.n_in && g < a.nr;
-                            const float *xr = Gv.x + (int64_t)g * Gv.x_stride + (kt0 + kl) * 32 + 2 * c;
-#pragma unroll
-                            for (int p = 0; p < 4; ++p) {
-                                const float2 v = live ? __ldcg(reinterpret_cast<const float2 *>(xr + (p >> 1) * 16 + (p & 1) * 8))
-                                                      : make_float2(0.f, 0.f);
-                                bh[jj][p] = __float_as_uint(v.x);
-                                bl[jj][p] = __float_as_uint(v.y);
-                            }
+                            const float4 *xr = reinterpret_cast<const float4 *>(Gv.x + (int64_t)g * Gv.x_stride + (kt0 + kl) * 32 + 8 * c);
+                            const float4 lo = live ? __ldcg(xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            const float4 hi = live ? __ldcg(xr + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            bh[jj][0] = __float_as_uint(lo.x);
+                            bl[jj][0] = __float_as_uint(lo.y);
+                            bh[jj][1] = __float_as_uint(lo.z);
+                            bl[jj][1] = __float_as_uint(lo.w);
+                            bh[jj][2] = __float_as_uint(hi.x);
+                            bl[jj][2] = __float_as_uint(hi.y);
+                            bh[jj][3] = __float_as_uint(hi.z);
+                            bl[jj][3] = __float_as_uint(hi.w);
                         }
 #pragma unroll
                         for (int jj = 0; jj < KPW; ++jj) {
@@ -1385,7 +1388,7 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                                         wg[p] = u8x2_to_f32x2(wd[p], 0);
                                         wh[p] = u8x2_to_f32x2(wd[p], 2);
                                     }
-                                    const float *xk = xs + (j * kKsl + kl) * 32 + 2 * c;
+                                    const float *xk = xs + (j * kKsl + kl) * 32 + 8 * c;
 #pragma unroll
                                     for (int q = 0; q < NRC; ++q) {
                                         const float *xq = xk + q * (kPartKT * 32);
@@ -1393,7 +1396,7 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                                         float2 sg = __fmul2_rn(wg[0], x0), sh = __fmul2_rn(wh[0], x0);
 #pragma unroll
                                         for (int p = 1; p < 4; ++p) {
-                                            const float2 xp = *reinterpret_cast<const float2 *>(xq + (p >> 1) * 16 + (p & 1) * 8);
+                                            const float2 xp = *reinterpret_cast<const float2 *>(xq + 2 * p);
                                             sg = __ffma2_rn(wg[p], xp, sg);
                                             sh = __ffma2_rn(wh[p], xp, sh);
                                         }
