@@ -20,13 +20,13 @@
 //    them).
 //
 // Work of a phase is split evenly over the CTAs in a fixed order:
-//  * projections: units of (K-slice of 1024 inputs, row tile of 16 outputs), slice-major, so that a
-//    CTA's units mostly share one slice (its activations are loaded once).  Each warp multiplies
-//    4 k-tiles of the unit (tensor cores on f16 weights 1152 + q against hi + lo activation terms
-//    with f32 accumulation for 3..8 rows, f32 CUDA-core FMAs for 1..2 rows), the CTA sums its
-//    warps in warp order; a row tile cut into several slices is finished by the CTA that brings
-//    the last slice: it adds the slices' sums in slice order (deterministic: no atomics touch
-//    results);
+//  * projections: units of (K-part of 1024 inputs, row tile of 16 outputs); with no more parts
+//    than CTAs, each CTA takes a run of one part's row tiles (its activations are prepared once).
+//    Each warp multiplies 4 k-tiles of the unit (tensor cores on f16 weights 1152 + q against
+//    hi + lo activation terms with f32 accumulation for 3..8 rows, f32 CUDA-core FMAs for 1..2
+//    rows or when asked), the CTA sums its warps in warp order every four units; a unit over the
+//    whole K stores its row tile, a unit over a K-part adds it (red.add) into outputs zeroed at
+//    the start, so with three or more parts the last bits depend on the order the parts arrive;
 //  * attention: the plan's work items (session, KV head, piece); the item whose keys hold a
 //    row's position rotates and stores that row's k and v before the producer requests the stages
 //    that hold them; queries are rotated in shared memory; tensor cores for items of more than
