@@ -213,7 +213,8 @@ constexpr int kMmaConsumers = 4;             // consumer warps
 constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 constexpr int kMmaMaxStages = 8;
 constexpr int kHalfTile = kStKeys * 128;     // bytes of 32 keys x 64 dims (one swizzled box)
-constexpr int kAttnPreWaitStages = 2;        // stages requested before the wait on the previous kernel
+constexpr int kAttnPreWaitStages = 1;        // stages requested before the wait on the previous kernel
+                                             // (more delay the query fetch that follows the wait)
 
 // Ring depth per head dimension: two CTAs fit on an SM.
 __host__ __device__ constexpr int mma_stages(int D) { return D == 128 ? 4 : 8; }
@@ -492,7 +493,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
         // then the rest of the ring, so that those latency-critical lines go first
         const int stable = lmin - 1;
         const int nstable = k1 <= stable ? nst : max(0, (stable - k0) / kStKeys);
-        const int npre = min(min(nstable, kAttnPreWaitStages), nst);
+        const int npre = min(min(nstable, kAttnPreWaitStages), min(nst, S));
         auto issue_stage = [&](int i) {
             const int st = i % S;
             unsigned char *kd = ring + (size_t)st * kStageBytes;

@@ -1136,9 +1136,9 @@ int gemv_group(GemvArgs a, bool w16, int nr, int sm, int path, cudaStream_t st)
     a.ksl = cfg.ksl;
     a.rpr = cfg.rpr;
     a.stages = cfg.stages;
-    // two stages per CTA ahead of the activations: about what an SM receives while the previous
-    // kernel drains
-    a.pre = 2;
+    // one stage per CTA ahead of the activations (measured: more delay the activation fetch that
+    // follows the wait, none leaves the SM idle while the previous kernel drains)
+    a.pre = 1;
     const void *kern = pick_kernel(cfg.w16, cfg.mma, cfg.nrc, cfg.kwm);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid);
