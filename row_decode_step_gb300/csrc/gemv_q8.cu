@@ -928,7 +928,7 @@ void *pick_kernel(bool w16, bool mma, int nrc, int kwm)
 constexpr int kSmemLimit = 200 * 1024;
 // Two CTAs share an SM (registers are capped for it): ring bytes aimed at per CTA and the
 // largest footprint with which two fit.
-constexpr size_t kRingBudget = 80 * 1024;
+constexpr size_t kRingBudget = 64 * 1024;
 constexpr size_t kShareLimit = 110 * 1024;
 
 int prepare_kernel(const void *kern, int cs)
