@@ -72,7 +72,7 @@ constexpr uint32_t kSlot = kUnitW + kKsl * 32;       // ring slot: weights + sca
 constexpr int kPartSlots = 1;                        // slots of a projection unit at most
 constexpr int kPartKT = kPartSlots * kKsl;           // k-tiles of a unit's K part (4096 inputs)
 constexpr int kStages = 10;                          // ring slots
-constexpr int kRB = 4;                               // units per CTA-wide reduction
+constexpr int kRBMax = 8;                            // units per CTA-wide reduction, at most
 constexpr int kStKeys = 32;                          // keys per attention stage
 constexpr int kMaxQ = 32;                            // queries per work item
 constexpr int kCCMaxQ = 4;                           // CUDA-core attention up to this many queries
@@ -1237,11 +1237,14 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
             }
             int ub, ue;
             unit_share(Gv.RT, Gv.cs, cta, C, ub, ue);
-            float *red = reinterpret_cast<float *>(scr);                     // [kRB][kCW][128]: 16 KB
-            float *xs = reinterpret_cast<float *>(scr + 16 * 1024);          // CUDA-core path: [NRC][kPartKT * 32]
-            float *snc = reinterpret_cast<float *>(scr + 16 * 1024);         // tensor path: [kCW][KPW][bias, 1/scale][8]
-            static_assert(16 * 1024 + NRC * kPartKT * 32 * 4 <= (int)kScratch &&
-                          16 * 1024 + kCW * kPartSlots * kKWM * 2 * 8 * 4 <= (int)kScratch, "projection scratch fits");
+            // units per CTA-wide reduction: eight, or four when eight activation rows take the room
+            constexpr int RB = NRC > 4 ? kRBMax / 2 : kRBMax;
+            constexpr int kRed = RB * kCW * 128 * 4;
+            float *red = reinterpret_cast<float *>(scr);                     // [RB][kCW][128]
+            float *xs = reinterpret_cast<float *>(scr + kRed);               // CUDA-core path: [NRC][kPartKT * 32]
+            float *snc = reinterpret_cast<float *>(scr + kRed);              // tensor path: [kCW][KPW][bias, 1/scale][8]
+            static_assert(kRed + NRC * kPartKT * 32 * 4 <= (int)kScratch &&
+                          kRed + kCW * kPartSlots * kKWM * 2 * 8 * 4 <= (int)kScratch, "projection scratch fits");
             const int wk0 = warp * kKWM;
             constexpr int KPW = kPartSlots * kKWM;                             // k-tiles of a part per warp
             uint32_t bh[GMMA ? KPW : 1][4], bl[GMMA ? KPW : 1][4];
@@ -1255,7 +1258,7 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
             unsigned finished = 0;
             for (int u = ub; u < ue && !bad;) {
                 const int s = u / Gv.RT;
-                const int nb = min(kRB, min(ue, (s + 1) * Gv.RT) - u);
+                const int nb = min(RB, min(ue, (s + 1) * Gv.RT) - u);
                 const int kt0 = s * kPartKT, nkt = min(kPartKT, Gv.KT - kt0);
                 const int nsl = (nkt + kKsl - 1) / kKsl;                        // slots of a unit of this part
                 if (s != cur_s) {
