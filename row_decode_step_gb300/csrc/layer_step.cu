@@ -480,39 +480,46 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                 }
             }
             wait_pdl();
+        } else if (warp == kCW + 1) {
+            // outputs of projections whose K comes in parts start at zero (the parts are added into
+            // them): every CTA zeroes a share, after the previous kernel (it may read them), and
+            // counts itself in; a projection's first additions wait for every CTA's count
+            dl_pdl_wait();
+            bool any_parts = false;
+            for (int p = 0; p < a.n_gemv; ++p) {
+                const SGemv &G = a.g[p];
+                if (G.cs == 1) continue;
+                any_parts = true;
+                const int64_t n = (int64_t)a.nr * G.n_out;
+                int zb, ze;
+                share(n, cta, C, zb, ze);
+                for (int64_t e = zb + lane; e < ze; e += 32) {
+                    const int r = (int)(e / G.n_out), o = (int)(e - (int64_t)r * G.n_out);
+                    G.y[(int64_t)r * G.y_stride + o] = 0.f;
+                }
+            }
+            __syncwarp();
+            if (any_parts && lane == 0) {
+                __threadfence();
+                atomicAdd(a.sync + SY_ZEROED, 1u);
+            }
+        } else if (warp == kCW + 2) {
+            // this CTA's work items (the key counts and positions are caller inputs), one lane each
+            for (int j = lane; j < n_it; j += 32) item_meta(a, s_seq, s_posr, it_b + j, s_items[j], true);
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                *reinterpret_cast<volatile int *>(&s_items_ready) = 1;
+            }
         }
     } else {
         // ============================================================ consumers
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsRegs));
-        // this CTA's work items, one thread each (the key counts and positions are caller inputs)
-        if (tid < n_it) item_meta(a, s_seq, s_posr, it_b + tid, s_items[tid], true);
-        csync();
-        if (tid == 0) *reinterpret_cast<volatile int *>(&s_items_ready) = 1;
+        // the work items and the zeroing of the K-part outputs are done by the producer warpgroup's
+        // spare warps, off this path
         dl_pdl_wait();
-        // outputs of projections whose K comes in parts start at zero (the parts are added into
-        // them): every CTA zeroes a share and counts itself in; a projection's first additions wait
-        // for every CTA's count (long since reached but for the first one)
-        bool any_parts = false;
-        for (int p = 0; p < a.n_gemv; ++p) {
-            const SGemv &G = a.g[p];
-            if (G.cs == 1) continue;
-            any_parts = true;
-            const int64_t n = (int64_t)a.nr * G.n_out;
-            int zb, ze;
-            share(n, cta, C, zb, ze);
-            for (int64_t e = zb + tid; e < ze; e += kCT) {
-                const int r = (int)(e / G.n_out), o = (int)(e - (int64_t)r * G.n_out);
-                G.y[(int64_t)r * G.y_stride + o] = 0.f;
-            }
-        }
-        if (any_parts) {
-            csync();
-            if (tid == 0) {
-                __threadfence();
-                atomicAdd(a.sync + SY_ZEROED, 1u);
-            }
-        }
-        bool zeroed = !any_parts;
+        bool zeroed = true;
+        for (int p = 0; p < a.n_gemv; ++p) zeroed = zeroed && a.g[p].cs == 1;
         const int ctid = tid;
         uint32_t seq = 0;
         bool bad = false;
@@ -596,7 +603,21 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
         for (int ph = 0; ph < nph && !bad; ++ph) {
             if (ph == PH_ATTN) {
                 // ================================================= attention
-                if (!dep_wait(PH_QKV, (unsigned)(a.g[0].RT * a.g[0].cs))) {
+                // the work items described by the spare warp (long since, but bounded); the verdict
+                // reaches every consumer through the dependency wait's barrier
+                bool items_ok = true;
+                if (ctid == 0) {
+                    for (int it = 0; !*reinterpret_cast<volatile int *>(&s_items_ready); ++it) {
+                        if (it > kSpinLimit || aborted()) {
+                            items_ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    __threadfence_block();
+                    if (!items_ok) set_abort();
+                }
+                if (!dep_wait(PH_QKV, (unsigned)(a.g[0].RT * a.g[0].cs)) || !items_ok) {
                     bad = true;
                     break;
                 }
