@@ -140,6 +140,15 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
                  : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// the same product as plain (non-volatile) assembly: the compiler may interleave independent ones
+__device__ __forceinline__ void mma16816p(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
     mma16816(c, a[0], a[1], a[2], a[3], b0, b1);
@@ -1380,7 +1389,51 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                         const unsigned char *sw = ring + (size_t)sl * kSlot;
                         const unsigned char *sd = sw + kUnitW;
                         const int snkt = min(kKsl, nkt - j * kKsl);      // k-tiles of this slot
-                        if (wk0 < snkt) {
+                        if (wk0 < snkt && GMMA) {
+                            // every shared load of the warp's k-tiles first, then the hi and lo products in
+                            // independent accumulators, a k-step of all k-tiles at a time (eight chains of
+                            // two instead of four chains of four)
+                            uint4 w[kKWM];
+                            float2 dgh[kKWM];                                // (d[g], d[g+8])
+#pragma unroll
+                            for (int i = 0; i < kKWM; ++i) {
+                                const int kl = wk0 + i;                      // slot-local k-tile
+                                w[i] = *reinterpret_cast<const uint4 *>(sw + kl * 512 + lane * 16);
+                                dgh[i] = __half22float2(*reinterpret_cast<const __half2 *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4));
+                            }
+                            float th[kKWM][4], tl[kKWM][4];
+#pragma unroll
+                            for (int i = 0; i < kKWM; ++i)
+#pragma unroll
+                                for (int p = 0; p < 4; ++p) th[i][p] = tl[i][p] = 0.f;
+#pragma unroll
+                            for (int i = 0; i < kKWM; ++i) {
+                                const int jj = GMMA ? j * kKWM + i : 0;
+                                const uint32_t a0 = u8x2_to_h2(w[i].x, 0x4140u), a1 = u8x2_to_h2(w[i].x, 0x4342u);
+                                const uint32_t a2 = u8x2_to_h2(w[i].y, 0x4140u), a3 = u8x2_to_h2(w[i].y, 0x4342u);
+                                mma16816p(th[i], a0, a1, a2, a3, bh[jj][0], bh[jj][1]);
+                                mma16816p(tl[i], a0, a1, a2, a3, bl[jj][0], bl[jj][1]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < kKWM; ++i) {
+                                const int jj = GMMA ? j * kKWM + i : 0;
+                                const uint32_t a4 = u8x2_to_h2(w[i].z, 0x4140u), a5 = u8x2_to_h2(w[i].z, 0x4342u);
+                                const uint32_t a6 = u8x2_to_h2(w[i].w, 0x4140u), a7 = u8x2_to_h2(w[i].w, 0x4342u);
+                                mma16816p(th[i], a4, a5, a6, a7, bh[jj][2], bh[jj][3]);
+                                mma16816p(tl[i], a4, a5, a6, a7, bl[jj][2], bl[jj][3]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < kKWM; ++i) {
+                                // columns 2c, 2c + 1: the k-tile's bias terms and inverse scales
+                                const int jj = GMMA ? j * kKWM + i : 0;
+                                const float2 nc = *reinterpret_cast<const float2 *>(snc + ((warp * KPW + jj) * 2) * 8 + 2 * c);
+                                const float2 us = *reinterpret_cast<const float2 *>(snc + ((warp * KPW + jj) * 2 + 1) * 8 + 2 * c);
+                                const float2 t01 = __fadd2_rn(make_float2(th[i][0], th[i][1]), make_float2(tl[i][0], tl[i][1]));
+                                const float2 t23 = __fadd2_rn(make_float2(th[i][2], th[i][3]), make_float2(tl[i][2], tl[i][3]));
+                                acc01 = __ffma2_rn(make_float2(dgh[i].x * us.x, dgh[i].x * us.y), __fadd2_rn(t01, nc), acc01);
+                                acc23 = __ffma2_rn(make_float2(dgh[i].y * us.x, dgh[i].y * us.y), __fadd2_rn(t23, nc), acc23);
+                            }
+                        } else if (wk0 < snkt) {
 #pragma unroll
                             for (int i = 0; i < kKWM; ++i) {
                                 const int kl = wk0 + i;                  // slot-local k-tile
@@ -1388,23 +1441,7 @@ layer_step_kernel(const __grid_constant__ StepArgs ap, const __grid_constant__ C
                                 const __half2 sp = *reinterpret_cast<const __half2 *>(sd + (kl >> 2) * 128 + g * 16 + (kl & 3) * 4);
                                 const float2 dgh = __half22float2(sp);          // (d[g], d[g+8])
                                 const float dg = dgh.x, dh = dgh.y;
-                                if constexpr (GMMA) {
-                                    const int jj = j * kKWM + i;
-                                    float t[4] = {0.f, 0.f, 0.f, 0.f};
-                                    const uint32_t a0 = u8x2_to_h2(w.x, 0x4140u), a1 = u8x2_to_h2(w.x, 0x4342u);
-                                    const uint32_t a2 = u8x2_to_h2(w.y, 0x4140u), a3 = u8x2_to_h2(w.y, 0x4342u);
-                                    mma16816(t, a0, a1, a2, a3, bh[jj][0], bh[jj][1]);
-                                    mma16816(t, a0, a1, a2, a3, bl[jj][0], bl[jj][1]);
-                                    const uint32_t a4 = u8x2_to_h2(w.z, 0x4140u), a5 = u8x2_to_h2(w.z, 0x4342u);
-                                    const uint32_t a6 = u8x2_to_h2(w.w, 0x4140u), a7 = u8x2_to_h2(w.w, 0x4342u);
-                                    mma16816(t, a4, a5, a6, a7, bh[jj][2], bh[jj][3]);
-                                    mma16816(t, a4, a5, a6, a7, bl[jj][2], bl[jj][3]);
-                                    // columns 2c, 2c + 1: the k-tile's bias terms and inverse scales
-                                    const float2 nc = *reinterpret_cast<const float2 *>(snc + ((warp * KPW + jj) * 2) * 8 + 2 * c);
-                                    const float2 us = *reinterpret_cast<const float2 *>(snc + ((warp * KPW + jj) * 2 + 1) * 8 + 2 * c);
-                                    acc01 = __ffma2_rn(make_float2(dg * us.x, dg * us.y), __fadd2_rn(make_float2(t[0], t[1]), nc), acc01);
-                                    acc23 = __ffma2_rn(make_float2(dh * us.x, dh * us.y), __fadd2_rn(make_float2(t[2], t[3]), nc), acc23);
-                                } else {
+                                {
                                     const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
                                     float2 wg[4], wh[4];
 #pragma unroll
