@@ -1066,6 +1066,10 @@ int choose_cfg(bool w16, int nr, int RT, int KT, int sm, int path, GemvCfg *out)
     GemvCfg best{};
     long best_cost = -1;
     for (int kwm : {8, 6, 4, 2, 1}) {                           // fewer slices first
+        // Q8_0: a window of six or eight k-tiles per warp when one fits (timed against the byte
+        // count below, which prefers narrower windows: 3B step 64.1 -> 60.8 us at 8 rows, 54.0 ->
+        // 49.4 at 1 row, 1B 34.3 -> 29.9); narrower windows only when no wider one fits
+        if (!w16 && kwm < 6 && best_cost >= 0) break;
         const void *kern = pick_kernel(w16, mma, nrc, kwm);
         if (!kern) continue;
         const int ksl = kConsumers * kwm;
