@@ -108,13 +108,6 @@ __device__ __forceinline__ bool rope_pair(int j, int rot, int neox, int &i0, int
     return false;
 }
 
-__device__ __forceinline__ float warp_max(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -1256,7 +1249,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     }
                 }
             } else
-#pragma unroll 2
+#pragma unroll 4
             for (int ch = 0; ch < D / 8; ++ch) {
                 const uint4 kv = *reinterpret_cast<const uint4 *>(kst + (ch >> 3) * kHalfTile + lane * 128 +
                                                                   (((ch & 7) ^ (lane & 7)) << 4));
@@ -1278,19 +1271,26 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
                     }
                 }
             }
-            // online softmax per query over the stage's 32 keys
+            // online softmax per query over the stage's 32 keys: the queries' maxima reduced
+            // side by side, each lane keeping its own part of the sums (reduced after the loop)
             const int key = kb0 + lane;
-            float ps[QM];
+            float ps[QM], mx[QM];
 #pragma unroll
             for (int q = 0; q < QM; ++q) {
-                ps[q] = 0.f;
-                if (q >= nq) continue;
-                const float sv = key < lenq[q] ? ((sc[q].x + sd[q].x) + (sc[q].y + sd[q].y)) * a.qscale : -INFINITY;
-                const float mn = fmaxf(mq[q], warp_max(sv));
-                if (mn == -INFINITY) continue;             // no attended key yet (warp-uniform)
-                const float al = mq[q] == -INFINITY ? 0.f : fast_exp2(mq[q] - mn);
-                ps[q] = sv == -INFINITY ? 0.f : fast_exp2(sv - mn);
-                lq[q] = lq[q] * al + warp_sum(ps[q]);
+                ps[q] = q < nq && key < lenq[q] ? ((sc[q].x + sd[q].x) + (sc[q].y + sd[q].y)) * a.qscale : -INFINITY;
+                mx[q] = ps[q];
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int q = 0; q < QM; ++q) mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], off));
+#pragma unroll
+            for (int q = 0; q < QM; ++q) {
+                const float mn = fmaxf(mq[q], mx[q]);
+                // rescale of what is summed so far: 1 while no key is attended, 0 at the first one
+                const float al = mn == -INFINITY ? 1.f : mq[q] == -INFINITY ? 0.f : fast_exp2(mq[q] - mn);
+                ps[q] = ps[q] == -INFINITY ? 0.f : fast_exp2(ps[q] - mn);
+                lq[q] = lq[q] * al + ps[q];
                 mq[q] = mn;
 #pragma unroll
                 for (int e = 0; e < DPL; ++e) o[q][e] = __fmul2_rn(o[q][e], make_float2(al, al));
@@ -1302,7 +1302,7 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             __syncwarp();
             const unsigned char *vcol = KVQ8 ? vst + (d0 & 15) : vst + (dch >> 3) * kHalfTile + (d0 & (16 / EB - 1)) * EB;
             const uint16_t *vsr = reinterpret_cast<const uint16_t *>(kst + 2 * kCodeBytes + kScaleBytes) + d0 / 32;
-#pragma unroll 2
+#pragma unroll 4
             for (int j4 = 0; j4 < kStKeys; j4 += 4) {
                 float v[4][DPL];
 #pragma unroll
@@ -1361,6 +1361,8 @@ decode_attn_tma_kernel(const __grid_constant__ AttnArgs a, const __grid_constant
             else if (a.tail_merge) tail_merge();
             return;
         }
+#pragma unroll
+        for (int q = 0; q < QM; ++q) lq[q] = warp_sum(lq[q]);
         if (sg < NS) {
 #pragma unroll
             for (int q = 0; q < QM; ++q) {
