@@ -65,6 +65,20 @@ def test_attention_configs(dl, name, path):
     assert_attn_close(out, lse, ro, rl)
 
 
+@pytest.mark.parametrize("name,chunk", [("1b", 160), ("1b", 288), ("3b-1", 160), ("3b-2", 32), ("3b-1", 4096)])
+def test_attention_cuda_core_stage_counts(dl, name, chunk):
+    """CUDA-core form on forced piece lengths: 5 or 9 stages (a ring slot filled twice at head_dim
+    64 and 128, one stage group taking two stages), 1 stage per piece (8 queries per warp, 2 rows),
+    and 4096 keys (the ring cycling many times); every row ends in a ragged last piece."""
+    n_q, n_kv, D, n_reg, cap, seqlen, regions = CONFIGS[name]
+    k, v = kv_planes("attn/" + name, n_reg, n_kv, cap, D)
+    q = synth.normal_f32(0, "attn/%s/q" % name, (len(seqlen), n_q * D))
+    out, lse, plan = _run(dl, q, k, v, seqlen, regions, n_q, n_kv, D, force_chunk=chunk, path=1)
+    assert plan.chunk == chunk
+    ro, rl = _ref(q, k, v, seqlen, regions, n_q, n_kv, D, plan)
+    assert_attn_close(out, lse, ro, rl)
+
+
 def test_attention_twelve_streams(dl):
     """Twelve one-row streams with their own caches, lengths U{512..8192}, run as 6 + 6."""
     n_q, n_kv, D = 24, 8, 128
