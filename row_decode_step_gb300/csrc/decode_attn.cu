@@ -185,7 +185,9 @@ template <int D, int EB>
 const void *pick_attn_kernel(bool mma, int qm)
 {
     if (mma) return reinterpret_cast<const void *>(decode_attn_tma_kernel<D, true, 8, EB>);
-    return qm == 4 ? reinterpret_cast<const void *>(decode_attn_tma_kernel<D, false, 4, EB>)
+    if constexpr (EB == 2)
+        if (qm == 3) return reinterpret_cast<const void *>(decode_attn_tma_kernel<D, false, 3, EB>);
+    return qm <= 4 ? reinterpret_cast<const void *>(decode_attn_tma_kernel<D, false, 4, EB>)
          : qm == 6 ? reinterpret_cast<const void *>(decode_attn_tma_kernel<D, false, 6, EB>)
                    : reinterpret_cast<const void *>(decode_attn_tma_kernel<D, false, 8, EB>);
 }
@@ -487,13 +489,14 @@ static int decode_attn_impl(const float *q, int64_t q_stride, const dl_kv_cache 
     rc = make_kv_tmap(&tv, kv->v, kv);
     if (rc != DL_OK) return rc;
     const size_t smem = attn_mma_smem_bytes(plan->head_dim, eb);
-    // the CUDA-core form holds the queries of a warp in registers: 4 for one-row sessions; 6 when
-    // a work item serves 17..24 queries (four query groups keep all four consumer warps busy,
-    // where groups of 8 would leave one idle); else 8
-    const int qm = qmax <= 4 ? 4 : (qmax > 16 && qmax <= 24) ? 6 : 8;
+    // the CUDA-core form holds the queries of a warp in registers: 3 or 4 for one-row sessions
+    // (3 on the f16 mirror for GQA groups of up to 3 heads, so that no query slot idles; the other
+    // mirrors and the in-launch merges keep 4); 6 when a work item serves 17..24 queries (four
+    // query groups keep all four consumer warps busy, where groups of 8 would leave one idle); else 8
+    const int qm = qmax <= 3 ? 3 : qmax <= 4 ? 4 : (qmax > 16 && qmax <= 24) ? 6 : 8;
     // the in-launch merges (cluster, last piece) run in instances of their own
     const bool clustered = co && !tail;
-    const void *kern = (co || tail) ? dl::attn_kernel_merge_opts(plan->head_dim, eb, mma, qm)
+    const void *kern = (co || tail) ? dl::attn_kernel_merge_opts(plan->head_dim, eb, mma, qm == 3 ? 4 : qm)
                      : eb == 4 ? (plan->head_dim == 128 ? pick_attn_kernel<128, 4>(mma, qm) : pick_attn_kernel<64, 4>(mma, qm))
                      : eb == 1 ? (plan->head_dim == 128 ? pick_attn_kernel<128, 1>(mma, qm) : pick_attn_kernel<64, 1>(mma, qm))
                                : (plan->head_dim == 128 ? pick_attn_kernel<128, 2>(mma, qm) : pick_attn_kernel<64, 2>(mma, qm));
